@@ -1,0 +1,198 @@
+"""ctypes binding of libbqe.so (include/bqe.h), same names as the C ABI.
+
+Argument marshalling only: tensors become device pointers, host structs become
+ctypes structures, status codes become exceptions.  Every computation runs in
+the library's CUDA kernels; there is no fallback.  Importing this module when
+the library has not been built raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libbqe.so")
+
+BQE_OK, BQE_EINVAL, BQE_ENOSPC, BQE_ECUDA, BQE_EDEVICE, BQE_ETIMEOUT, BQE_EUNSUPPORTED = range(7)
+BQE_FMT_TQ1, BQE_FMT_Q2_0, BQE_FMT_Q3_K, BQE_FMT_MXFP4 = 1, 2, 3, 4
+
+
+class BqeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (what, status_name(status), status))
+
+
+class bqe_layer_desc(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("n_shared", ctypes.c_int32)]
+
+
+class bqe_pool(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("base_bytes", ctypes.c_uint64), ("slot_off", ctypes.c_void_p),
+                ("slot_fmt", ctypes.c_void_p), ("n_slots", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libbqe.so is not built (%s); run bit_quantised_expert_gb300.buildlib.build() "
+                          "or __graft_entry__.build() first" % LIB_PATH)
+    return ctypes.CDLL(LIB_PATH)
+
+
+lib = _load()
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_U64 = ctypes.c_uint64
+_DESC = ctypes.POINTER(bqe_layer_desc)
+_POOL = ctypes.POINTER(bqe_pool)
+
+# (name, restype, argtypes) for every symbol of include/bqe.h
+SIGNATURES = {
+    "bqe_block_weights": (_I32, [_I32]),
+    "bqe_block_bytes": (_I32, [_I32]),
+    "bqe_packed_bytes": (_U64, [_I32, _I32, _I32]),
+    "bqe_expert_bytes": (_U64, [_DESC, _I32]),
+    "bqe_scale_bytes": (_I32, [_I32]),
+    "bqe_pack": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P]),
+    "bqe_pool_pack_slot": (ctypes.c_int, [_DESC, _I32, _P, _P, _P]),
+    "bqe_dequant": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P]),
+    "bqe_workspace_bytes": (_U64, [_DESC, _I32]),
+    "bqe_workspace_init": (ctypes.c_int, [_P, _U64, _P]),
+    "bqe_moe_layer_forward": (ctypes.c_int, [_DESC, _I32, _P, _P, _P, _POOL, _P, _P, _P, _I32, _P, _P, _P, _U64, _P]),
+    "bqe_route": (ctypes.c_int, [_DESC, _I32, _P, _P, _P, _POOL, _P, _P, _P, _P, _P, _U64, _P]),
+    "bqe_experts": (ctypes.c_int, [_DESC, _I32, _POOL, _P, _I32, _P, _U64, _P]),
+    "bqe_moe_step": (ctypes.c_int, [_DESC, _I32, _I32, _P, _P, _P, _POOL, _P, _P, _P, _P, _U64, _P]),
+    "bqe_check": (ctypes.c_int, [_P, _P, ctypes.POINTER(_I32)]),
+    "bqe_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "bqe_set_wait_limit_ns": (None, [_U64]),
+    "bqe_set_pdl": (None, [ctypes.c_int]),
+}
+
+for _name, (_res, _args) in SIGNATURES.items():
+    if hasattr(lib, _name):
+        _f = getattr(lib, _name)
+        _f.restype = _res
+        _f.argtypes = _args
+
+
+def status_name(s: int) -> str:
+    return lib.bqe_status_str(int(s)).decode()
+
+
+def ptr(t) -> int | None:
+    """Device (or host) address of a tensor / array / raw int; None -> NULL."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    if hasattr(t, "ctypes"):
+        return t.ctypes.data
+    raise TypeError("cannot take the address of %r" % type(t))
+
+
+def stream_ptr(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ok(rc: int, what: str):
+    if rc != BQE_OK:
+        raise BqeError(rc, what)
+
+
+def desc(hidden, inter, n_experts, top_k, n_shared=1) -> bqe_layer_desc:
+    return bqe_layer_desc(hidden, inter, n_experts, top_k, n_shared)
+
+
+# --------------------------------------------------------------- formats
+def bqe_block_weights(fmt: int) -> int:
+    return lib.bqe_block_weights(fmt)
+
+
+def bqe_block_bytes(fmt: int) -> int:
+    return lib.bqe_block_bytes(fmt)
+
+
+def bqe_packed_bytes(fmt: int, rows: int, cols: int) -> int:
+    return lib.bqe_packed_bytes(fmt, rows, cols)
+
+
+def bqe_expert_bytes(d: bqe_layer_desc, fmt: int) -> int:
+    return lib.bqe_expert_bytes(ctypes.byref(d), fmt)
+
+
+def bqe_scale_bytes(fmt: int) -> int:
+    return lib.bqe_scale_bytes(fmt)
+
+
+def bqe_pack(fmt: int, rows: int, cols: int, codes, scales, out) -> None:
+    """Host packing: codes/scales/out are C-contiguous uint8 numpy arrays."""
+    _ok(lib.bqe_pack(fmt, rows, cols, ptr(codes), ptr(scales), ptr(out)), "bqe_pack")
+
+
+# ------------------------------------------------------------------ pool
+def bqe_pool_pack_slot(d, fmt, canon_src, slot_dst, stream=None) -> None:
+    _ok(lib.bqe_pool_pack_slot(ctypes.byref(d), fmt, ptr(canon_src), ptr(slot_dst), stream_ptr(stream)),
+        "bqe_pool_pack_slot")
+
+
+def bqe_dequant(fmt, rows, cols, src, out, stream=None) -> None:
+    _ok(lib.bqe_dequant(fmt, rows, cols, ptr(src), ptr(out), stream_ptr(stream)), "bqe_dequant")
+
+
+# ---------------------------------------------------------------- decode
+def bqe_workspace_bytes(d, M: int) -> int:
+    return lib.bqe_workspace_bytes(ctypes.byref(d), M)
+
+
+def bqe_workspace_init(ws, nbytes: int, stream=None) -> None:
+    _ok(lib.bqe_workspace_init(ptr(ws), nbytes, stream_ptr(stream)), "bqe_workspace_init")
+
+
+def bqe_moe_layer_forward(d, M, x, router_w, sel_bias, pool: bqe_pool, slot_table, forced_idx, out,
+                          accumulate, topk_idx, topk_w, ws, ws_bytes, stream=None) -> None:
+    _ok(lib.bqe_moe_layer_forward(ctypes.byref(d), M, ptr(x), ptr(router_w), ptr(sel_bias), ctypes.byref(pool),
+                                  ptr(slot_table), ptr(forced_idx), ptr(out), int(accumulate), ptr(topk_idx),
+                                  ptr(topk_w), ptr(ws), ws_bytes, stream_ptr(stream)), "bqe_moe_layer_forward")
+
+
+def bqe_route(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, topk_idx, topk_w, ws, ws_bytes,
+              stream=None) -> None:
+    _ok(lib.bqe_route(ctypes.byref(d), M, ptr(x), ptr(router_w), ptr(sel_bias), ctypes.byref(pool),
+                      ptr(slot_table), ptr(forced_idx), ptr(topk_idx), ptr(topk_w), ptr(ws), ws_bytes,
+                      stream_ptr(stream)), "bqe_route")
+
+
+def bqe_experts(d, M, pool, out, accumulate, ws, ws_bytes, stream=None) -> None:
+    _ok(lib.bqe_experts(ctypes.byref(d), M, ctypes.byref(pool), ptr(out), int(accumulate), ptr(ws), ws_bytes,
+                        stream_ptr(stream)), "bqe_experts")
+
+
+def bqe_moe_step(d, n_layers, M, resid, router_w, sel_bias, pool, slot_tables, forced_idx, t_out, ws, ws_bytes,
+                 stream=None) -> None:
+    _ok(lib.bqe_moe_step(ctypes.byref(d), n_layers, M, ptr(resid), ptr(router_w), ptr(sel_bias), ctypes.byref(pool),
+                         ptr(slot_tables), ptr(forced_idx), ptr(t_out), ptr(ws), ws_bytes, stream_ptr(stream)),
+        "bqe_moe_step")
+
+
+def bqe_check(ws, stream=None) -> tuple[int, int]:
+    """Returns (status, detail) without raising."""
+    det = _I32(0)
+    rc = lib.bqe_check(ptr(ws), stream_ptr(stream), ctypes.byref(det))
+    return rc, det.value
+
+
+def bqe_set_wait_limit_ns(ns: int) -> None:
+    lib.bqe_set_wait_limit_ns(int(ns))
+
+
+def bqe_set_pdl(on: bool) -> None:
+    lib.bqe_set_pdl(1 if on else 0)

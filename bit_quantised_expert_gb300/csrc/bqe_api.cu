@@ -1,0 +1,164 @@
+// bqe_api.cu — host entry points of the decode path: argument checks,
+// workspace geometry, kernel launches (stream-ordered, programmatic
+// dependent launch between the kernels of a layer and across layers).
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "bqe_internal.cuh"
+
+using namespace bqe;
+
+static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};  // 2 s per wait
+static std::atomic<int> g_use_pdl{1};
+
+// Diagnostic knobs (not part of the operation): the bound on every in-kernel
+// wait, and whether kernels are chained with programmatic dependent launch.
+extern "C" void bqe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
+extern "C" void bqe_set_pdl(int on) { g_use_pdl = on ? 1 : 0; }
+
+static int device_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static bool desc_ok(const bqe_layer_desc* d) {
+  return d && d->hidden > 0 && d->inter > 0 && d->hidden % 256 == 0 && d->inter % 256 == 0 && d->n_experts > 0 &&
+         d->n_experts <= 512 && d->top_k > 0 && d->top_k <= kMaxTopK && d->top_k <= d->n_experts &&
+         d->n_shared == 1 && d->top_k <= 32;
+}
+
+static Geo geo_of(const bqe_layer_desc* d, int M) { return make_geo(d->hidden, d->inter, d->n_experts, d->top_k, M); }
+
+extern "C" uint64_t bqe_workspace_bytes(const bqe_layer_desc* d, int32_t M) {
+  if (!desc_ok(d) || M < 1 || M > kMaxM) return 0;
+  return make_ws(geo_of(d, M)).total;
+}
+
+extern "C" int bqe_workspace_init(void* ws, uint64_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes == 0) return BQE_EINVAL;
+  return cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream) == cudaSuccess ? BQE_OK : BQE_ECUDA;
+}
+
+static int check_pool(const bqe_pool* p) {
+  if (!p || !p->base || !p->slot_off || !p->slot_fmt || p->n_slots <= 0 || ((uintptr_t)p->base & 15)) return BQE_EINVAL;
+  return BQE_OK;
+}
+
+static int route_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* resid, uint16_t* t_out,
+                        const float* router_w, const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
+                        const int32_t* forced_idx, int32_t* topk_idx, float* topk_w, void* ws, uint64_t ws_bytes,
+                        cudaStream_t st) {
+  if (!desc_ok(d) || M < 1 || M > kMaxM || (!x && !resid) || !router_w || !slot_table || !ws) return BQE_EINVAL;
+  if (((uintptr_t)ws & 255) || ((uintptr_t)router_w & 15)) return BQE_EINVAL;
+  int rc = check_pool(pool);
+  if (rc) return rc;
+  Geo g = geo_of(d, M);
+  WsLayout L = make_ws(g);
+  if (ws_bytes < L.total) return BQE_ENOSPC;
+  RouteParams P;
+  P.g = g;
+  P.L = L;
+  P.ws = (uint8_t*)ws;
+  P.x = x;
+  P.resid = resid;
+  P.t_out = t_out;
+  P.router_w = router_w;
+  P.bias = sel_bias;
+  P.forced = forced_idx;
+  P.slot_table = slot_table;
+  P.pool = *pool;
+  P.topk_idx = topk_idx;
+  P.topk_w = topk_w;
+  return launch_route(P, st, g_use_pdl.load() != 0);
+}
+
+static int experts_common(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out, int32_t accumulate,
+                          void* ws, uint64_t ws_bytes, cudaStream_t st) {
+  if (!desc_ok(d) || M < 1 || M > kMaxM || !out || !ws || ((uintptr_t)ws & 255)) return BQE_EINVAL;
+  int rc = check_pool(pool);
+  if (rc) return rc;
+  Geo g = geo_of(d, M);
+  WsLayout L = make_ws(g);
+  if (ws_bytes < L.total) return BQE_ENOSPC;
+  const int sms = device_sms();
+  if (sms <= 0) return BQE_ECUDA;
+  ExpParams P;
+  P.g = g;
+  P.L = L;
+  P.ws = (uint8_t*)ws;
+  P.out = out;
+  P.accumulate = accumulate ? 1 : 0;
+  P.limit_ns = g_wait_limit_ns.load();
+  const bool pdl = g_use_pdl.load() != 0;
+  for (int phase = 0; phase < 2; ++phase) {
+    int ns = 0;
+    experts_smem_bytes(g, phase, &ns);
+    if (ns < 2) return BQE_EUNSUPPORTED;
+    P.nstages = ns;
+    if ((rc = launch_experts(P, phase, sms, st, pdl))) return rc;
+  }
+  return BQE_OK;
+}
+
+extern "C" int bqe_route(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w,
+                         const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
+                         const int32_t* forced_idx, int32_t* topk_idx, float* topk_w, void* ws, uint64_t ws_bytes,
+                         void* stream) {
+  if (!x) return BQE_EINVAL;
+  return route_common(d, M, x, nullptr, nullptr, router_w, sel_bias, pool, slot_table, forced_idx, topk_idx, topk_w,
+                      ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int bqe_experts(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out,
+                           int32_t accumulate, void* ws, uint64_t ws_bytes, void* stream) {
+  return experts_common(d, M, pool, out, accumulate, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int bqe_moe_layer_forward(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w,
+                                     const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
+                                     const int32_t* forced_idx, float* out, int32_t accumulate, int32_t* topk_idx,
+                                     float* topk_w, void* ws, uint64_t ws_bytes, void* stream) {
+  int rc = bqe_route(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, topk_idx, topk_w, ws, ws_bytes,
+                     stream);
+  if (rc) return rc;
+  return experts_common(d, M, pool, out, accumulate, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M, float* resid,
+                            const float* router_w, const float* sel_bias, const bqe_pool* pool,
+                            const int32_t* slot_tables, const int32_t* forced_idx, uint16_t* t_out, void* ws,
+                            uint64_t ws_bytes, void* stream) {
+  if (!desc_ok(d) || n_layers < 1 || M < 1 || M > kMaxM || !resid || !router_w || !slot_tables) return BQE_EINVAL;
+  const int64_t E = d->n_experts, H = d->hidden, K = d->top_k;
+  cudaStream_t st = (cudaStream_t)stream;
+  for (int l = 0; l < n_layers; ++l) {
+    int rc = route_common(d, M, nullptr, resid, t_out ? t_out + (int64_t)l * M * H : nullptr, router_w + l * E * H,
+                          sel_bias ? sel_bias + l * E : nullptr, pool, slot_tables + l * (E + 1),
+                          forced_idx ? forced_idx + (int64_t)l * M * K : nullptr, nullptr, nullptr, ws, ws_bytes, st);
+    if (rc) return rc;
+    rc = experts_common(d, M, pool, resid, 1, ws, ws_bytes, st);
+    if (rc) return rc;
+  }
+  return BQE_OK;
+}
+
+extern "C" int bqe_check(void* ws, void* stream, int32_t* detail) {
+  if (!ws) return BQE_EINVAL;
+  int32_t h[2] = {0, 0};
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return BQE_ECUDA;
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return BQE_ECUDA;
+  if (detail) *detail = h[1];
+  if (h[0] == 0) return BQE_OK;
+  const int32_t z[2] = {0, 0};
+  if (cudaMemcpy(ws, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return BQE_ECUDA;
+  return h[0];
+}

@@ -1,0 +1,240 @@
+// bqe_internal.cuh — shared definitions of the CUDA library: block formats,
+// the device slot layout, workspace layout, and thin PTX wrappers for
+// mbarrier / bulk-copy / grid-dependency control on sm_103a.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/bqe.h"
+
+namespace bqe {
+
+// ----------------------------------------------------------------------------
+// Block formats.  Weights per block / bytes per block (bits per weight from
+// the Strata 4090 post, section 5.1, and the FP4 per-32 block of the field
+// report): TQ1 256/56, Q2_0 64/18, Q3_K 256/110, MXFP4 32/17.
+// ----------------------------------------------------------------------------
+__host__ __device__ constexpr int fmt_bw(int f) {
+  return f == BQE_FMT_TQ1 ? 256 : f == BQE_FMT_Q2_0 ? 64 : f == BQE_FMT_Q3_K ? 256 : f == BQE_FMT_MXFP4 ? 32 : 0;
+}
+__host__ __device__ constexpr int fmt_bb(int f) {
+  return f == BQE_FMT_TQ1 ? 56 : f == BQE_FMT_Q2_0 ? 18 : f == BQE_FMT_Q3_K ? 110 : f == BQE_FMT_MXFP4 ? 17 : 0;
+}
+__host__ __device__ constexpr bool fmt_ok(int f) { return f >= BQE_FMT_TQ1 && f <= BQE_FMT_MXFP4; }
+
+// ----------------------------------------------------------------------------
+// Device layout of one matrix (rows x K) of a slot.
+//
+//  * rows are grouped in panels of 32 (one row per lane of a warp);
+//  * K is cut in chunks of kc columns, kc = the largest of 1024/768/512/256
+//    dividing K, so every chunk holds whole blocks of every format;
+//  * tile (panel p, chunk c) is contiguous, tiles in order p*nchunks + c;
+//  * inside a tile (nb = kc / block_weights blocks per row), every
+//    per-(row, block) field is stored field-major, then block, then row, and
+//    fields of 16*n bytes are further split into n 16-byte pieces, so that 32
+//    lanes reading the same piece of the same block for their own row read
+//    512 contiguous bytes:
+//      MXFP4: codes16 @ b*512 + r*16           | E   @ nb*512 + b*32 + r
+//      Q2_0 : codes16 @ b*512 + r*16           | d   @ nb*512 + (b*32+r)*2
+//      TQ1  : bytes0..47 @ (b*3+q)*512 + r*16  | bytes48..55 @ nb*1536 + (b*32+r)*8
+//      Q3_K : lo64 @ (b*4+q)*512 + r*16        | hi32 @ nb*2048 + (b*2+q)*512 + r*16
+//             | scales12 @ nb*3072 + (b*32+r)*12 | d @ nb*3456 + (b*32+r)*2
+//  The bytes of every block are exactly its canonical bytes, rearranged.
+// ----------------------------------------------------------------------------
+__host__ __device__ constexpr int chunk_cols(int K) {
+  return (K % 1024 == 0) ? 1024 : (K % 768 == 0) ? 768 : (K % 512 == 0) ? 512 : 256;
+}
+__host__ __device__ constexpr uint32_t tile_bytes(int f, int kc) {
+  return 32u * (uint32_t)(kc / fmt_bw(f)) * (uint32_t)fmt_bb(f);
+}
+__host__ __device__ constexpr uint64_t matrix_bytes(int f, int rows, int K) {
+  return (uint64_t)rows * (uint64_t)(K / fmt_bw(f)) * (uint64_t)fmt_bb(f);
+}
+
+// Destination offset inside a tile of canonical byte `i` of block `b` of row
+// `r` (nb blocks per row in the tile).
+__host__ __device__ inline uint32_t tile_byte_offset(int f, int nb, int b, int r, int i) {
+  switch (f) {
+    case BQE_FMT_MXFP4:
+      return i < 16 ? (uint32_t)(b * 512 + r * 16 + i) : (uint32_t)(nb * 512 + b * 32 + r);
+    case BQE_FMT_Q2_0:
+      return i < 16 ? (uint32_t)(b * 512 + r * 16 + i) : (uint32_t)(nb * 512 + (b * 32 + r) * 2 + (i - 16));
+    case BQE_FMT_TQ1:
+      return i < 48 ? (uint32_t)((b * 3 + i / 16) * 512 + r * 16 + (i % 16))
+                    : (uint32_t)(nb * 1536 + (b * 32 + r) * 8 + (i - 48));
+    case BQE_FMT_Q3_K:
+      if (i < 64) return (uint32_t)((b * 4 + i / 16) * 512 + r * 16 + (i % 16));
+      if (i < 96) return (uint32_t)(nb * 2048 + (b * 2 + (i - 64) / 16) * 512 + r * 16 + ((i - 64) % 16));
+      if (i < 108) return (uint32_t)(nb * 3072 + (b * 32 + r) * 12 + (i - 96));
+      return (uint32_t)(nb * 3456 + (b * 32 + r) * 2 + (i - 108));
+  }
+  return 0;
+}
+
+// ----------------------------------------------------------------------------
+// Decode-call geometry shared by host and kernels.
+// ----------------------------------------------------------------------------
+constexpr int kMaxM = 8;          // rows per decode call
+constexpr int kMaxWarps = 8;      // consumer warps per CTA
+constexpr int kMaxTopK = 16;
+
+struct Geo {
+  int H, I, E, K, M;
+  int U;          // max distinct experts incl. the shared one = M*K + 1 (<= E+1)
+  int kcA, nchA, GA, npanA;  // W1/W3: K = H
+  int kcB, nchB, GB, npanB, PB;  // W2: K = I; PB panels per item
+};
+
+__host__ __device__ inline Geo make_geo(int H, int I, int E, int K, int M) {
+  Geo g;
+  g.H = H; g.I = I; g.E = E; g.K = K; g.M = M;
+  g.U = M * K + 1;
+  if (g.U > E + 1) g.U = E + 1;
+  g.kcA = chunk_cols(H); g.nchA = H / g.kcA; g.GA = g.kcA / 256; g.npanA = I / 32;
+  g.kcB = chunk_cols(I); g.nchB = I / g.kcB; g.GB = g.kcB / 256; g.npanB = H / 32;
+  int pb = kMaxWarps / g.GB;
+  if (pb < 1) pb = 1;
+  while (pb > 1 && (g.npanB % pb) != 0) --pb;
+  g.PB = pb;
+  return g;
+}
+
+// Workspace layout (offsets in bytes, each 256-aligned).
+struct WsLayout {
+  uint64_t err, ctr_route, nu, u_slot, u_fmt, u_addr, u_nrows, u_rows;
+  uint64_t comb_u, comb_r, comb_w, z, xf, pa, ctrA, h, pb, ctrB, total;
+};
+
+__host__ __device__ inline uint64_t al256(uint64_t x) { return (x + 255) & ~(uint64_t)255; }
+
+__host__ __device__ inline WsLayout make_ws(const Geo& g) {
+  WsLayout w;
+  uint64_t o = 0;
+  w.err = o; o = al256(o + 16);
+  w.ctr_route = o; o = al256(o + 16);
+  w.nu = o; o = al256(o + 16);
+  w.u_slot = o; o = al256(o + 4ull * g.U);
+  w.u_fmt = o; o = al256(o + 4ull * g.U);
+  w.u_addr = o; o = al256(o + 8ull * g.U);
+  w.u_nrows = o; o = al256(o + 4ull * g.U);
+  w.u_rows = o; o = al256(o + 4ull * g.U * kMaxM);
+  w.comb_u = o; o = al256(o + 4ull * g.M * g.K);
+  w.comb_r = o; o = al256(o + 4ull * g.M * g.K);
+  w.comb_w = o; o = al256(o + 4ull * g.M * g.K);
+  w.z = o; o = al256(o + 4ull * g.M * g.E);
+  w.xf = o; o = al256(o + 4ull * g.M * g.H);
+  w.pa = o; o = al256(o + 4ull * g.U * g.npanA * g.nchA * 2 * g.M * 32);
+  w.ctrA = o; o = al256(o + 4ull * g.U * g.npanA);
+  w.h = o; o = al256(o + 4ull * g.U * g.M * g.I);
+  w.pb = o; o = al256(o + 4ull * g.U * g.nchB * g.M * g.H);
+  w.ctrB = o; o = al256(o + 4ull * g.npanB);
+  w.total = o;
+  return w;
+}
+
+
+// Kernel parameter blocks (passed by value to the kernels).
+struct RouteParams {
+  Geo g;
+  WsLayout L;
+  uint8_t* ws;
+  const uint16_t* x;          // bf16 M x H, or null when resid is given
+  const float* resid;         // fp32 M x H (chained step: normalise first)
+  uint16_t* t_out;            // optional bf16 M x H copy of the layer input
+  const float* router_w;      // E x H
+  const float* bias;          // E or null
+  const int32_t* forced;      // M x K or null
+  const int32_t* slot_table;  // E + 1
+  bqe_pool pool;
+  int32_t* topk_idx;          // optional M x K
+  float* topk_w;              // optional M x K
+};
+
+struct ExpParams {
+  Geo g;
+  WsLayout L;
+  uint8_t* ws;
+  float* out;
+  int accumulate;
+  int nstages;        // ring depth (<= 16), chosen by the host from the smem budget
+  uint64_t limit_ns;  // bound on every mbarrier wait
+};
+
+// Launchers (one per translation unit that owns the kernel).
+int launch_route(const RouteParams& P, cudaStream_t st, bool pdl);
+int launch_experts(const ExpParams& P, int phase, int grid, cudaStream_t st, bool pdl);
+uint32_t experts_smem_bytes(const Geo& g, int phase, int* nstages_out);
+
+// Error detail codes written to ws.err[1].
+enum { kErrSlotRange = 1, kErrSlotFmt = 2, kErrSlotExtent = 3, kErrWaitFull = 4, kErrWaitEmpty = 5,
+       kErrForcedIdx = 6 };
+
+#ifdef __CUDACC__
+// ----------------------------------------------------------------------------
+// PTX wrappers (sm_90+ mbarrier / bulk copy; sm_90+ griddepcontrol).
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: spins until the phase with `parity` completes or `limit_ns`
+// elapses; returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes, dst, src
+// all multiples of 16).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void set_error(int32_t* err, int code, int detail) {
+  if (atomicCAS(err, 0, code) == 0) err[1] = detail;
+}
+#endif
+
+}  // namespace bqe

@@ -1,0 +1,299 @@
+// bqe_router.cu — router GEMV, sigmoid scores, selection-biased top-k, and the
+// per-call expert work list.
+//
+// Router (field report, section 1: 384 routed experts, 6 per token; Strata
+// 4090 post, section 5.3: a routing bias that changes which experts are
+// computed while the mixing weights stay exact):
+//   z[m,e] = sum_h x[m,h] Wr[e,h]   (fp32 accumulation)
+//   s = sigmoid(z), key = s + b, idx = top-k(key) (ties -> lower e),
+//   w_j = s[idx_j] / sum_j' s[idx_j'].
+// Work list: the distinct experts chosen by the M rows plus the shared
+// expert (u = 0), each with the rows that chose it, so every expert's bytes
+// are streamed once per call however many rows use it (field report, section
+// 4.2: one transfer of an expert's bytes serves every token of a batch).
+//
+// One kernel: every CTA computes z for two experts (four warps per expert,
+// one quarter of hidden each, all loads in flight at once); the last CTA to
+// finish (arrival counter, no waiting) selects, weighs and builds the list.
+#include <cuda_bf16.h>
+
+#include "bqe_internal.cuh"
+
+namespace bqe {
+
+
+constexpr int kRouteThreads = 256;
+constexpr int kMaxE = 512;  // routed experts per layer supported by the selection
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+__global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
+  const Geo& g = P.g;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = g.H, E = g.E, M = g.M, K = g.K;
+  int32_t* err = (int32_t*)(P.ws + P.L.err);
+  float* z = (float*)(P.ws + P.L.z);
+  float* xf = (float*)(P.ws + P.L.xf);
+
+  __shared__ float inv_rms[kMaxM];
+  __shared__ float red[8][kMaxM];
+  __shared__ int s_last;
+
+  griddep_wait();  // inputs may come from the previous layer's kernels
+
+  // ---- layer input: bf16 x, or bf16(rmsnorm(resid)) --------------------------
+  if (P.resid) {
+    for (int m = 0; m < M; ++m) {
+      float ss = 0.f;
+      for (int k = tid; k < H; k += kRouteThreads) {
+        float v = P.resid[(int64_t)m * H + k];
+        ss = fmaf(v, v, ss);
+      }
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) red[warp][m] = ss;
+    }
+    __syncthreads();
+    if (tid < M) {
+      float ss = 0.f;
+      for (int w = 0; w < kRouteThreads / 32; ++w) ss += red[w][tid];
+      inv_rms[tid] = 1.0f / sqrtf(ss / (float)H + 1e-6f);
+    }
+    __syncthreads();
+  }
+  auto xval = [&](int m, int k) -> float {
+    if (P.resid) {
+      __nv_bfloat16 t = __float2bfloat16_rn(P.resid[(int64_t)m * H + k] * inv_rms[m]);
+      return __bfloat162float(t);
+    }
+    return bf16_to_f32(P.x[(int64_t)m * H + k]);
+  };
+
+  // ---- side job: fp32 copy of the layer input for the expert kernels --------
+  {
+    const int64_t n = (int64_t)M * H;
+    const int64_t per = (n + gridDim.x - 1) / gridDim.x;
+    const int64_t lo = per * blockIdx.x, hi = min(n, lo + per);
+    for (int64_t i = lo + tid; i < hi; i += kRouteThreads) {
+      const int m = (int)(i / H), k = (int)(i % H);
+      float v = xval(m, k);
+      xf[i] = v;
+      if (P.t_out) P.t_out[i] = (uint16_t)(__float_as_uint(v) >> 16);
+    }
+  }
+
+  // ---- router GEMV: warp = (expert 2*blockIdx + warp/4, quarter warp%4) ------
+  const int e = blockIdx.x * 2 + (warp >> 2);
+  const int q = warp & 3;
+  const int Kq = H / 4;
+  float acc[kMaxM];
+#pragma unroll
+  for (int m = 0; m < kMaxM; ++m) acc[m] = 0.f;
+  if (e < E) {
+    const float4* wr = (const float4*)(P.router_w + (int64_t)e * H + (int64_t)q * Kq);
+    const int n4 = Kq / 4;
+#pragma unroll 10
+    for (int i = lane; i < n4; i += 32) {
+      const float4 w4 = __ldg(wr + i);
+      const int k = q * Kq + i * 4;
+#pragma unroll
+      for (int m = 0; m < kMaxM; ++m) {
+        if (m < M) {
+          acc[m] = fmaf(w4.x, xval(m, k + 0), acc[m]);
+          acc[m] = fmaf(w4.y, xval(m, k + 1), acc[m]);
+          acc[m] = fmaf(w4.z, xval(m, k + 2), acc[m]);
+          acc[m] = fmaf(w4.w, xval(m, k + 3), acc[m]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kMaxM; ++m) {
+    float v = acc[m];
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    acc[m] = v;
+  }
+  __syncthreads();  // red[] reuse
+  if (lane == 0)
+    for (int m = 0; m < M; ++m) red[warp][m] = acc[m];
+  __syncthreads();
+  if (tid < 2 * M) {
+    const int el = tid / M, m = tid % M, ee = blockIdx.x * 2 + el;
+    if (ee < E) {
+      float s = red[el * 4 + 0][m] + red[el * 4 + 1][m] + red[el * 4 + 2][m] + red[el * 4 + 3][m];
+      z[(int64_t)m * E + ee] = s;
+    }
+  }
+
+  // ---- last CTA: scores, top-k, weights, work list ---------------------------
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    unsigned int* ctr = (unsigned int*)(P.ws + P.L.ctr_route);
+    s_last = (atomicAdd(ctr, 1u) == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  __shared__ uint32_t s_mask[kMaxE];
+  __shared__ int s_uof[kMaxE];
+  __shared__ int s_idx[kMaxM][kMaxTopK];
+  __shared__ int s_bad;
+  __shared__ int s_nu;
+  if (tid == 0) s_bad = 0;
+  for (int i = tid; i < E; i += kRouteThreads) s_mask[i] = 0u;
+  __syncthreads();
+
+  if (warp < M) {
+    const int m = warp;
+    // lane holds the keys of experts lane, lane+32, ... (E <= kMaxE)
+    float key[kMaxE / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) {
+      const int ee = lane + 32 * i;
+      float kk = -INFINITY;
+      if (ee < E) {
+        const float s = 1.0f / (1.0f + expf(-__ldcg(z + (int64_t)m * E + ee)));
+        kk = P.bias ? s + P.bias[ee] : s;
+      }
+      key[i] = kk;
+    }
+    for (int j = 0; j < K; ++j) {
+      int best;
+      if (P.forced) {
+        best = P.forced[m * K + j];
+        if (best < 0 || best >= E) {
+          if (lane == 0) { set_error(err, BQE_EDEVICE, kErrForcedIdx); s_bad = 1; }
+          best = 0;
+        }
+      } else {
+        float bk = -INFINITY;
+        best = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i) {
+          const int ee = lane + 32 * i;
+          if (key[i] > bk || (key[i] == bk && ee < best)) { bk = key[i]; best = ee; }
+        }
+        for (int o = 16; o; o >>= 1) {
+          const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, best, o);
+          if (ok > bk || (ok == bk && oe < best)) { bk = ok; best = oe; }
+        }
+#pragma unroll
+        for (int i = 0; i < kMaxE / 32; ++i)
+          if (lane + 32 * i == best) key[i] = -INFINITY;
+      }
+      if (lane == 0) {
+        s_idx[m][j] = best;
+        atomicOr(&s_mask[best], 1u << m);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      // mixing weights from the unbiased scores of the selected experts
+      float sc[kMaxTopK];
+      float tot = 0.f;
+      for (int j = 0; j < K; ++j) {
+        sc[j] = 1.0f / (1.0f + expf(-__ldcg(z + (int64_t)m * E + s_idx[m][j])));
+        tot += sc[j];
+      }
+      for (int j = 0; j < K; ++j) {
+        const float w = sc[j] / tot;
+        ((float*)(P.ws + P.L.comb_w))[m * K + j] = w;
+        if (P.topk_idx) P.topk_idx[m * K + j] = s_idx[m][j];
+        if (P.topk_w) P.topk_w[m * K + j] = w;
+      }
+    }
+  }
+  __syncthreads();
+
+  int32_t* u_slot = (int32_t*)(P.ws + P.L.u_slot);
+  int32_t* u_fmt = (int32_t*)(P.ws + P.L.u_fmt);
+  uint64_t* u_addr = (uint64_t*)(P.ws + P.L.u_addr);
+  int32_t* u_nrows = (int32_t*)(P.ws + P.L.u_nrows);
+  int32_t* u_rows = (int32_t*)(P.ws + P.L.u_rows);
+
+  // compact the chosen experts in ascending id order (u = 1..), shared u = 0
+  if (warp == 0) {
+    int base_u = 1;
+    for (int b0 = 0; b0 < E; b0 += 32) {
+      const int ee = b0 + lane;
+      const bool on = ee < E && s_mask[ee] != 0u;
+      const uint32_t bal = __ballot_sync(0xffffffffu, on);
+      if (on) s_uof[ee] = base_u + __popc(bal & ((1u << lane) - 1u));
+      base_u += __popc(bal);
+    }
+    if (lane == 0) s_nu = base_u;
+  }
+  __syncthreads();
+  const int nU = s_nu;
+  // per-u descriptors
+  for (int u = tid; u < nU; u += kRouteThreads) {
+    int ee = -1;
+    uint32_t mask;
+    if (u == 0) {
+      mask = (M >= 32) ? 0xffffffffu : ((1u << M) - 1u);
+    } else {
+      // find the expert with s_uof == u (scan is fine: at most M*K+1 entries)
+      mask = 0u;
+      for (int c = 0; c < E; ++c)
+        if (s_mask[c] != 0u && s_uof[c] == u) { ee = c; mask = s_mask[c]; break; }
+    }
+    const int slot = (u == 0) ? P.slot_table[E] : P.slot_table[ee];
+    int fmt = 0;
+    uint64_t addr = 0;
+    if (slot < 0 || slot >= P.pool.n_slots) {
+      set_error(err, BQE_EDEVICE, kErrSlotRange);
+      s_bad = 1;
+    } else {
+      fmt = P.pool.slot_fmt[slot];
+      const uint64_t off = P.pool.slot_off[slot];
+      if (!fmt_ok(fmt)) {
+        set_error(err, BQE_EDEVICE, kErrSlotFmt);
+        s_bad = 1;
+      } else {
+        const uint64_t bytes = 2 * matrix_bytes(fmt, g.I, g.H) + matrix_bytes(fmt, g.H, g.I);
+        if ((off & 15) || off + bytes > P.pool.base_bytes) {
+          set_error(err, BQE_EDEVICE, kErrSlotExtent);
+          s_bad = 1;
+        }
+        addr = (uint64_t)P.pool.base + off;
+      }
+    }
+    u_slot[u] = slot;
+    u_fmt[u] = fmt;
+    u_addr[u] = addr;
+    int n = 0;
+    for (int m = 0; m < M; ++m)
+      if (mask & (1u << m)) u_rows[u * kMaxM + n++] = m;
+    u_nrows[u] = n;
+  }
+  if (warp < M && lane < K) {
+    const int m = warp, j = lane;
+    const int ee = s_idx[m][j];
+    ((int32_t*)(P.ws + P.L.comb_u))[m * K + j] = s_uof[ee];
+    ((int32_t*)(P.ws + P.L.comb_r))[m * K + j] = __popc(s_mask[ee] & ((1u << m) - 1u));
+  }
+  __syncthreads();
+  if (tid == 0) {
+    *(int32_t*)(P.ws + P.L.nu) = s_bad ? 0 : nU;
+    *(unsigned int*)(P.ws + P.L.ctr_route) = 0u;
+  }
+}
+
+int launch_route(const RouteParams& P, cudaStream_t st, bool pdl) {
+  const int grid = (P.g.E + 1) / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_route, P) == cudaSuccess ? BQE_OK : BQE_ECUDA;
+}
+
+}  // namespace bqe

@@ -1,0 +1,209 @@
+/*
+ * bqe.h — block-quantised MoE expert layer for GB300 (sm_103a): C ABI.
+ *
+ * The operation (DeepSeek-V4.1-Flash on 4xL20 field report, sections 1-2;
+ * Strata 4090 post, sections 1, 5.1 and 5.3): one MoE layer of a
+ * DeepSeek-V4.1-Flash-shaped model — hidden 5120, expert intermediate 2304,
+ * 384 routed experts + 1 shared, 6 experts per token:
+ *
+ *   z = x Wr^T (fp32 router), s = sigmoid(z), key = s + b (b steers the
+ *   choice only), idx = top-k(key) with ties to the lower expert id,
+ *   w = s[idx] / sum s[idx],
+ *   out = sum_j w_j W2_j (silu(W1_j x) * (W3_j x)) + (same for the shared expert).
+ *
+ * Expert weights are block-quantised (the pages give bits per weight; the
+ * block layouts are this library's specification):
+ *   BQE_FMT_TQ1   ternary PTQ1_0, 256 weights / 56 B (1.75 bpw)
+ *   BQE_FMT_Q2_0  64 weights / 18 B (2.25 bpw), w = d (2q - 3)
+ *   BQE_FMT_Q3_K  256 weights / 110 B (3.4375 bpw), w = d s_j (q - 4)
+ *   BQE_FMT_MXFP4 32 weights / 17 B (4.25 bpw), w = e2m1(c) 2^(E-127)
+ *
+ * Conventions for every entry point:
+ *   - Return value: BQE_OK or an error code; nothing throws across the ABI.
+ *     Argument errors are detected on the host before anything is enqueued.
+ *   - Pointers documented "device" are CUDA device addresses owned by the
+ *     caller; the library never allocates, frees or retains them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).  All
+ *     GPU work is asynchronous on it.  Errors found by the kernels themselves
+ *     (a slot id out of range, a wait that timed out) are recorded in the
+ *     workspace's error word and reported by bqe_check().
+ *   - Row-major, contiguous layouts throughout.
+ */
+#ifndef BQE_H
+#define BQE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  BQE_OK = 0,
+  BQE_EINVAL = 1,       /* bad argument (null pointer, size, alignment, format) */
+  BQE_ENOSPC = 2,       /* a caller buffer is too small */
+  BQE_ECUDA = 3,        /* a CUDA runtime call failed */
+  BQE_EDEVICE = 4,      /* a kernel detected an invalid slot / table entry */
+  BQE_ETIMEOUT = 5,     /* a kernel wait exceeded its limit and gave up */
+  BQE_EUNSUPPORTED = 6  /* shape or device not supported */
+};
+
+enum { BQE_FMT_TQ1 = 1, BQE_FMT_Q2_0 = 2, BQE_FMT_Q3_K = 3, BQE_FMT_MXFP4 = 4 };
+
+/* Shape of one MoE layer.  hidden and inter must be multiples of 256 (every
+ * format's block divides 256) and of 32 rows; n_shared must be 1.
+ * DeepSeek-V4.1-Flash: {5120, 2304, 384, 6, 1}. */
+typedef struct {
+  int32_t hidden;
+  int32_t inter;
+  int32_t n_experts;
+  int32_t top_k;
+  int32_t n_shared;
+} bqe_layer_desc;
+
+/* A slot pool: one caller-owned device buffer holding expert slots in the
+ * device layout (bqe_pool_pack_slot), plus two caller-owned device tables:
+ * slot_off[s] = byte offset of slot s in base (multiple of 16), slot_fmt[s]
+ * = its format.  The kernels check every slot id they use against n_slots
+ * and every slot's extent against base_bytes. */
+typedef struct {
+  const void* base;          /* device */
+  uint64_t base_bytes;
+  const uint64_t* slot_off;  /* device, n_slots entries */
+  const int32_t* slot_fmt;   /* device, n_slots entries */
+  int32_t n_slots;
+  int32_t reserved;
+} bqe_pool;
+
+/* ---- formats (host only) ------------------------------------------------ */
+
+/* Weights and bytes of one block of `fmt`; 0 for an unknown format. */
+int32_t bqe_block_weights(int32_t fmt);
+int32_t bqe_block_bytes(int32_t fmt);
+
+/* Bytes of a rows x cols matrix in `fmt` (canonical and device layouts have
+ * the same size); 0 if cols is not a multiple of the block. */
+uint64_t bqe_packed_bytes(int32_t fmt, int32_t rows, int32_t cols);
+
+/* Bytes of one expert slot: W1 (inter x hidden) | W3 (inter x hidden) |
+ * W2 (hidden x inter). 0 on a bad shape or format. */
+uint64_t bqe_expert_bytes(const bqe_layer_desc* d, int32_t fmt);
+
+/* Bytes of the scale field per block that bqe_pack() reads:
+ * TQ1 2 (fp16 d), Q2_0 2 (fp16 d), Q3_K 18 (16 six-bit sub-scales as bytes
+ * 0..63, then fp16 d), MXFP4 1 (the UE8M0 exponent byte). */
+int32_t bqe_scale_bytes(int32_t fmt);
+
+/* Host: pack a rows x cols matrix into canonical blocks (row-major; each row
+ * is cols/block consecutive blocks).  codes: one byte per weight, row-major,
+ * in the format's code domain (TQ1: t+1 in 0..2; Q2_0: q in 0..3; Q3_K: q in
+ * 0..7; MXFP4: 4-bit code 0..15).  scales: bqe_scale_bytes(fmt) bytes per
+ * block, blocks in row-major order.  out: bqe_packed_bytes() bytes.
+ * BQE_EINVAL on a code or scale out of its domain (nothing is written then
+ * for that block onward). */
+int bqe_pack(int32_t fmt, int32_t rows, int32_t cols, const uint8_t* codes,
+             const uint8_t* scales, uint8_t* out);
+
+/* ---- pool --------------------------------------------------------------- */
+
+/* Device: rewrite one expert from canonical bytes (device, bqe_expert_bytes
+ * bytes: W1 | W3 | W2 in canonical blocks) into the device layout at
+ * slot_dst (device, same size, 16-byte aligned).  The device layout groups
+ * 32 rows into a panel and 256..1024 columns into a chunk; each (panel,
+ * chunk) tile is contiguous so one bulk copy moves it.  The bytes are the
+ * canonical bytes, rearranged. */
+int bqe_pool_pack_slot(const bqe_layer_desc* d, int32_t fmt, const void* canon_src,
+                       void* slot_dst, void* stream);
+
+/* Device: dequantise one rows x cols matrix stored in the device layout
+ * (e.g. W1 of a slot: slot base; W3: + bqe_packed_bytes(fmt, inter, hidden);
+ * W2: + 2x that) into fp32 row-major `out` (device, rows*cols floats).
+ * Exact: every block value is representable in fp32. */
+int bqe_dequant(int32_t fmt, int32_t rows, int32_t cols, const void* src, float* out,
+                void* stream);
+
+/* ---- decode layer (M <= 8 token rows) ----------------------------------- */
+
+/* Workspace bytes one decode call with up to M rows needs. */
+uint64_t bqe_workspace_bytes(const bqe_layer_desc* d, int32_t M);
+
+/* Zero a workspace before its first use (its counters must start at 0; the
+ * kernels leave them at 0 after every successful call). */
+int bqe_workspace_init(void* ws, uint64_t ws_bytes, void* stream);
+
+/* One MoE layer for M in 1..8 token rows (the token plus speculative draft
+ * rows verified together; each row routes independently).
+ *   x          device, M x hidden bf16 (uint16 bit patterns)
+ *   router_w   device, n_experts x hidden fp32
+ *   sel_bias   device, n_experts fp32, or NULL for no bias
+ *   pool       host struct describing the device slot pool
+ *   slot_table device, n_experts + 1 int32: slot of each routed expert, then
+ *              of the shared expert
+ *   forced_idx device, M x top_k int32 or NULL: if given, the selection is
+ *              taken from it (the router still computes the scores, and the
+ *              mixing weights are the scores of the given experts)
+ *   out        device, M x hidden fp32; out = layer(x), or out += layer(x)
+ *              when accumulate != 0
+ *   topk_idx   device, M x top_k int32 or NULL: selected experts (key order)
+ *   topk_w     device, M x top_k fp32 or NULL: their mixing weights
+ *   ws         device workspace of ws_bytes >= bqe_workspace_bytes(d, M)
+ * Experts chosen by several rows are streamed once and applied to every row
+ * that chose them. */
+int bqe_moe_layer_forward(const bqe_layer_desc* d, int32_t M, const uint16_t* x,
+                          const float* router_w, const float* sel_bias, const bqe_pool* pool,
+                          const int32_t* slot_table, const int32_t* forced_idx, float* out,
+                          int32_t accumulate, int32_t* topk_idx, float* topk_w, void* ws,
+                          uint64_t ws_bytes, void* stream);
+
+/* The same call split in its two halves, for timing each: bqe_route runs the
+ * router GEMV, the scores, the biased top-k and builds the per-expert work
+ * list in ws; bqe_experts streams the selected experts (W1/W3 GEMV, SiLU-GLU,
+ * W2 GEMV) and combines into out.  bqe_experts must follow bqe_route on the
+ * same stream with the same ws. */
+int bqe_route(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w,
+              const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
+              const int32_t* forced_idx, int32_t* topk_idx, float* topk_w, void* ws,
+              uint64_t ws_bytes, void* stream);
+int bqe_experts(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out,
+                int32_t accumulate, void* ws, uint64_t ws_bytes, void* stream);
+
+/* Chained decode step over n_layers layers: r_0 = resid (in place),
+ * t_l = bf16(r_l / sqrt(mean(r_l^2) + 1e-6)), r_{l+1} = r_l + MoE_l(t_l).
+ *   resid       device, M x hidden fp32, updated in place
+ *   router_w    device, n_layers x n_experts x hidden fp32
+ *   sel_bias    device, n_layers x n_experts fp32, or NULL
+ *   slot_tables device, n_layers x (n_experts + 1) int32
+ *   forced_idx  device, n_layers x M x top_k int32, or NULL
+ *   t_out       device, n_layers x M x hidden bf16, or NULL: each layer's
+ *               normalised input (for per-layer checks)
+ * Enqueues 3 kernels per layer; capture it in a CUDA graph to replay. */
+int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M, float* resid,
+                 const float* router_w, const float* sel_bias, const bqe_pool* pool,
+                 const int32_t* slot_tables, const int32_t* forced_idx, uint16_t* t_out,
+                 void* ws, uint64_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, read the workspace error word and clear it.
+ * Returns BQE_OK, BQE_EDEVICE or BQE_ETIMEOUT (detail: optional host int,
+ * receives the kernel's detail code), or BQE_ECUDA. */
+int bqe_check(void* ws, void* stream, int32_t* detail);
+
+/* Human-readable name of a status code. */
+const char* bqe_status_str(int status);
+
+/* ---- diagnostics (process-wide settings, not part of the operation) ----- */
+
+/* Bound on every in-kernel wait (default 2 s).  A wait that runs out records
+ * BQE_ETIMEOUT in the workspace and the kernel returns; the workspace must be
+ * re-initialised (bqe_workspace_init) after such an error. */
+void bqe_set_wait_limit_ns(uint64_t ns);
+
+/* Chain the kernels of a call with programmatic dependent launch (default
+ * on).  Off: plain stream order. */
+void bqe_set_pdl(int on);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BQE_H */

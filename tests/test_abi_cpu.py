@@ -1,0 +1,129 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and
+exports every entry point of include/bqe.h, the format sizes agree with the
+pages' bits per weight, and the host packer writes blocks that the oracle
+decodes to the intended values."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import formats as F
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def A():
+    from bit_quantised_expert_gb300 import buildlib
+    buildlib.build()
+    from bit_quantised_expert_gb300 import _abi
+    return _abi
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(bqe_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(A):
+    names = declared_functions()
+    assert len(names) >= 15, names
+    missing = [n for n in names if not hasattr(A.lib, n)]
+    assert not missing, missing
+    # and the binding marshals every one of them
+    assert set(names) <= set(A.SIGNATURES), set(names) - set(A.SIGNATURES)
+
+
+def test_block_sizes(A):
+    for fmt, (bw, bb) in F.BLOCK.items():
+        assert A.bqe_block_weights(fmt) == bw
+        assert A.bqe_block_bytes(fmt) == bb
+    assert A.bqe_block_bytes(0) == 0 and A.bqe_block_bytes(5) == 0
+    assert A.bqe_packed_bytes(A.BQE_FMT_MXFP4, 2304, 5120) == 2304 * 160 * 17
+    assert A.bqe_packed_bytes(A.BQE_FMT_TQ1, 32, 100) == 0  # not a whole block
+    d = A.desc(5120, 2304, 384, 6)
+    assert A.bqe_expert_bytes(d, A.BQE_FMT_MXFP4) == 18_800_640
+    for fmt in (1, 2, 3, 4):
+        assert A.bqe_expert_bytes(d, fmt) == synth.expert_bytes(fmt, 5120, 2304)
+
+
+def test_workspace_bytes(A):
+    d = A.desc(5120, 2304, 384, 6)
+    w1 = A.bqe_workspace_bytes(d, 1)
+    w8 = A.bqe_workspace_bytes(d, 8)
+    assert 0 < w1 < w8
+    assert A.bqe_workspace_bytes(d, 0) == 0
+    assert A.bqe_workspace_bytes(d, 9) == 0
+    assert A.bqe_workspace_bytes(A.desc(5000, 2304, 384, 6), 1) == 0
+    assert A.bqe_workspace_bytes(A.desc(5120, 2304, 384, 6, 2), 1) == 0
+
+
+def _intended(fmt, codes, scales):
+    """Weights a packer input stands for, from the format definitions."""
+    bw = F.BLOCK[fmt][0]
+    c = codes.reshape(-1, bw).astype(np.float64)
+    if fmt == F.MXFP4:
+        mag = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6.0])
+        ci = codes.reshape(-1, bw).astype(np.int64)
+        v = np.where(ci & 8, -mag[ci & 7], mag[ci & 7])
+        return v * np.exp2(scales.reshape(-1, 1).astype(np.float64) - 127)
+    d = scales.reshape(-1, A_SB[fmt])[:, -2:].copy().view(np.float16).astype(np.float64)
+    if fmt == F.Q2_0:
+        return d * (2 * c - 3)
+    if fmt == F.TQ1:
+        return d * (c - 1)
+    s = scales.reshape(-1, 18)[:, :16].astype(np.float64)
+    return d * np.repeat(s, 16, axis=1) * (c - 4)
+
+
+A_SB = {F.TQ1: 2, F.Q2_0: 2, F.Q3_K: 18, F.MXFP4: 1}
+
+
+@pytest.mark.parametrize("fmt", [F.TQ1, F.Q2_0, F.Q3_K, F.MXFP4])
+def test_pack_matches_oracle_decode(A, fmt):
+    rng = np.random.default_rng(fmt)
+    rows, cols = 4, 512
+    bw, bb = F.BLOCK[fmt]
+    nblk = rows * cols // bw
+    hi = {F.TQ1: 3, F.Q2_0: 4, F.Q3_K: 8, F.MXFP4: 16}[fmt]
+    codes = rng.integers(0, hi, size=rows * cols, dtype=np.uint8)
+    if fmt == F.MXFP4:
+        scales = rng.integers(100, 140, size=nblk, dtype=np.uint8)
+    else:
+        d = np.abs(rng.normal(0, 0.05, size=nblk)).astype(np.float16).view(np.uint8).reshape(nblk, 2)
+        if fmt == F.Q3_K:
+            s = rng.integers(0, 64, size=(nblk, 16), dtype=np.uint8)
+            scales = np.concatenate([s, d], axis=1).reshape(-1)
+        else:
+            scales = d.reshape(-1)
+    out = np.zeros(A.bqe_packed_bytes(fmt, rows, cols), dtype=np.uint8)
+    A.bqe_pack(fmt, rows, cols, codes, np.ascontiguousarray(scales), out)
+    got = F.dequant_matrix(fmt, out, rows, cols).reshape(-1, bw)
+    want = _intended(fmt, codes, np.ascontiguousarray(scales))
+    assert np.array_equal(got, want)
+
+
+def test_pack_rejects_out_of_domain(A):
+    codes = np.full(64, 4, dtype=np.uint8)  # q = 4 is not a 2-bit code
+    scales = np.zeros(2, dtype=np.uint8)
+    out = np.zeros(18, dtype=np.uint8)
+    with pytest.raises(A.BqeError) as e:
+        A.bqe_pack(A.BQE_FMT_Q2_0, 1, 64, codes, scales, out)
+    assert e.value.status == A.BQE_EINVAL
+    with pytest.raises(A.BqeError):
+        A.bqe_pack(A.BQE_FMT_MXFP4, 1, 32, np.zeros(32, np.uint8), np.array([255], np.uint8),
+                   np.zeros(17, np.uint8))
+
+
+def test_status_strings(A):
+    for s in range(7):
+        assert A.status_name(s)
+    assert "unknown" in A.status_name(99)

@@ -1,0 +1,231 @@
+"""GPU parity of the decode path against the fp64 oracle, through the C ABI.
+
+Bars: dequantised weights and top-k indices bit-exact (rows whose k-th and
+(k+1)-th keys are within 1e-6 excepted); fp32 layer outputs within relative
+L2 1e-4 and max-abs 1e-3 x max|reference|."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import formats as F
+from oracle import moe as O
+
+from gpu_util import DeviceLayer, check_out, check_routing, oracle_layer_sampled, torch_dev
+
+pytestmark = pytest.mark.gpu
+
+ALL = [synth.TQ1, synth.Q2_0, synth.Q3_K, synth.MXFP4]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    from bit_quantised_expert_gb300 import buildlib
+    buildlib.build()
+    d = torch_dev()
+    torch.cuda.set_device(d)
+    return d
+
+
+# ------------------------------------------------------------------ dequant
+@pytest.mark.parametrize("fmt", ALL)
+@pytest.mark.parametrize("shape", [(512, 256), (2304, 5120)])
+def test_dequant_bit_exact(dev, fmt, shape):
+    import torch
+    from bit_quantised_expert_gb300 import _abi as A
+    from bit_quantised_expert_gb300.pool import SlotPool
+    H, I = shape
+    rng = np.random.default_rng(100 + fmt)
+    canon = synth.random_expert(rng, fmt, H, I)
+    # exercise every code and extreme scales in the first blocks
+    d = A.desc(H, I, 8, 2)
+    pool = SlotPool(d, [fmt], dev)
+    pool.upload(0, canon)
+    p1, p3, p2 = F.split_expert(fmt, canon, H, I)
+    base = pool.slot_ptr(0)
+    for k, (p, rows, cols) in enumerate([(p1, I, H), (p3, I, H), (p2, H, I)]):
+        out = torch.empty(rows * cols, dtype=torch.float32, device=dev)
+        A.bqe_dequant(fmt, rows, cols, base + k * p1.size, out)
+        got = out.cpu().numpy().reshape(rows, cols)
+        want = F.dequant_matrix(fmt, p, rows, cols).astype(np.float32)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (fmt, k)
+
+
+def test_dequant_special_values(dev):
+    """Signed zeros, subnormal fp16 d, extreme UE8M0 exponents survive exactly."""
+    import torch
+    from bit_quantised_expert_gb300 import _abi as A
+    from bit_quantised_expert_gb300.pool import SlotPool
+    H, I = 256, 256
+    rng = np.random.default_rng(5)
+    for fmt in ALL:
+        canon = synth.random_expert(rng, fmt, H, I)
+        bw, bb = F.BLOCK[fmt]
+        blk = canon.reshape(-1, bb)
+        if fmt == synth.MXFP4:
+            blk[0, 16] = 0        # 2^-127 (subnormal in fp32)
+            blk[1, 16] = 254      # 2^127
+            blk[2, :16] = 0x88    # -0.0 codes
+        else:
+            dpos = {synth.Q2_0: 16, synth.TQ1: 52, synth.Q3_K: 108}[fmt]
+            blk[0, dpos:dpos + 2] = (0x01, 0x00)   # smallest fp16 subnormal
+            blk[1, dpos:dpos + 2] = (0x00, 0x00)   # d = +0: products keep their signs
+            blk[2, dpos:dpos + 2] = (0x00, 0x80)   # d = -0
+            blk[3, dpos:dpos + 2] = (0xff, 0x7b)   # largest finite fp16
+        d = A.desc(H, I, 4, 1)
+        pool = SlotPool(d, [fmt], dev)
+        pool.upload(0, canon)
+        out = torch.empty(I * H, dtype=torch.float32, device=dev)
+        A.bqe_dequant(fmt, I, H, pool.slot_ptr(0), out)
+        got = out.cpu().numpy()
+        want = F.dequant_matrix(fmt, F.split_expert(fmt, canon, H, I)[0], I, H).astype(np.float32).reshape(-1)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), fmt
+
+
+# ------------------------------------------------------------ small layers
+@pytest.mark.parametrize("M", [1, 4])
+def test_tiny_q2_0_layer(dev, M):
+    """Tiny layer: hidden 512, inter 256, 16 routed + 1 shared, top-2, all Q2_0."""
+    L = synth.tiny_layer(seed=0, m=M)
+    DL = DeviceLayer(L, dev)
+    out, idx, w = DL.forward(L["x"])
+    ref = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 512, 256, 2, 16)
+    check_routing(ref, idx, w)
+    ref2 = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 512, 256, 2, 16, forced_idx=idx)
+    assert np.allclose(w, ref2["w"], rtol=2e-6, atol=0)
+    check_out(out, ref2["out"], what="tiny M=%d" % M)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 6, 8])
+def test_mixed_small_layer(dev, M):
+    """All four formats in one layer, selection bias N(0, 0.25), independent rows."""
+    fm = [ALL[(3 * e + 1) % 4] for e in range(24)] + [synth.Q2_0]
+    L = synth.small_layer(20 + M, fm, 1024, 768, 24, 3, M, bias_std=0.25)
+    DL = DeviceLayer(L, dev)
+    out, idx, w = DL.forward(L["x"])
+    ref = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 1024, 768, 3, 24)
+    check_routing(ref, idx, w)
+    ref2 = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 1024, 768, 3, 24, forced_idx=idx)
+    check_out(out, ref2["out"], what="mixed M=%d" % M)
+    # split entry points give the same bits
+    out2, idx2, _ = DL.forward(L["x"], split=True)
+    assert np.array_equal(out, out2) and np.array_equal(idx, idx2)
+
+
+@pytest.mark.parametrize("fmt", ALL)
+def test_single_format_layer(dev, fmt):
+    fm = [fmt] * 9
+    L = synth.small_layer(40 + fmt, fm, 512, 512, 8, 2, 3, bias_std=0.0)
+    DL = DeviceLayer(L, dev)
+    out, idx, w = DL.forward(L["x"])
+    ref2 = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 512, 512, 2, 8, forced_idx=idx)
+    check_out(out, ref2["out"], what="fmt %d" % fmt)
+
+
+def test_bias_changes_selection_not_weights(dev):
+    fm = [synth.Q2_0] * 17
+    L = synth.small_layer(7, fm, 512, 256, 16, 2, 4, bias_std=0.0)
+    DL = DeviceLayer(L, dev)
+    _, idx0, w0 = DL.forward(L["x"], use_bias=False)
+    # a large bias on the experts nobody chose moves the selection to them
+    import torch
+    b = np.zeros(16, np.float32)
+    unchosen = sorted(set(range(16)) - set(idx0.reshape(-1).tolist()))[:2]
+    b[unchosen] = 5.0
+    DL.bias = torch.from_numpy(b).to(dev)
+    out, idx1, w1 = DL.forward(L["x"])
+    assert all(sorted(r.tolist()) == sorted(unchosen) for r in idx1)
+    ref = O.moe_layer(L["x"], L["router"], b, L["experts"], L["fmts"], 512, 256, 2, 16)
+    assert np.allclose(w1, ref["w"], rtol=2e-6)
+    check_out(out, ref["out"], what="biased")
+
+
+def test_forced_idx_with_repeats_and_accumulate(dev):
+    import torch
+    fm = [synth.MXFP4, synth.TQ1, synth.Q3_K, synth.Q2_0] * 4 + [synth.Q3_K]
+    L = synth.small_layer(8, fm, 512, 256, 16, 3, 5, bias_std=0.0)
+    DL = DeviceLayer(L, dev)
+    forced = np.array([[0, 1, 2], [2, 2, 2], [15, 0, 7], [3, 3, 4], [9, 10, 11]], dtype=np.int32)
+    prior = torch.randn(5, 512, device=dev)
+    keep = prior.double().cpu().numpy()
+    out, idx, w = DL.forward(L["x"], forced=forced, accumulate_into=prior)
+    assert np.array_equal(idx, forced)
+    ref = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 512, 256, 3, 16, forced_idx=forced)
+    assert np.allclose(w, ref["w"], rtol=2e-6)
+    check_out(out - keep, ref["out"], rel=2e-4, what="accumulate")
+
+
+def test_deterministic(dev):
+    fm = [ALL[e % 4] for e in range(33)]
+    L = synth.small_layer(9, fm, 1024, 512, 32, 4, 6, bias_std=0.25)
+    DL = DeviceLayer(L, dev)
+    a = DL.forward(L["x"])
+    b = DL.forward(L["x"])
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ------------------------------------------------------- error reporting
+def test_bad_slot_is_reported(dev):
+    import torch
+    from bit_quantised_expert_gb300 import _abi as A
+    L = synth.tiny_layer(seed=1, m=1)
+    DL = DeviceLayer(L, dev)
+    DL.table = torch.full((17,), 999, dtype=torch.int32, device=dev)  # no such slot
+    ws, nb = DL.workspace(1)
+    x = torch.from_numpy(L["x"].view(np.int16)).to(dev)
+    out = torch.zeros(1, 512, device=dev)
+    A.bqe_moe_layer_forward(DL.d, 1, x, DL.wr, None, DL.pool.cstruct(), DL.table, None, out, 0, None, None, ws, nb)
+    rc, det = A.bqe_check(ws)
+    assert rc == A.BQE_EDEVICE and det == 1
+    A.bqe_workspace_init(ws, nb)
+    DL.table = torch.arange(17, dtype=torch.int32, device=dev)
+    o2, _, _ = DL.forward(L["x"])  # the context and the workspace are usable again
+    assert np.isfinite(o2).all()
+
+
+def test_host_argument_errors(dev):
+    import torch
+    from bit_quantised_expert_gb300 import _abi as A
+    L = synth.tiny_layer(seed=1, m=1)
+    DL = DeviceLayer(L, dev)
+    ws, nb = DL.workspace(1)
+    x = torch.from_numpy(L["x"].view(np.int16)).to(dev)
+    out = torch.zeros(1, 512, device=dev)
+    for M in (0, 9):
+        with pytest.raises(A.BqeError) as e:
+            A.bqe_moe_layer_forward(DL.d, M, x, DL.wr, None, DL.pool.cstruct(), DL.table, None, out, 0, None, None,
+                                    ws, nb)
+        assert e.value.status == A.BQE_EINVAL
+    with pytest.raises(A.BqeError) as e:
+        A.bqe_moe_layer_forward(DL.d, 1, x, DL.wr, None, DL.pool.cstruct(), DL.table, None, out, 0, None, None,
+                                ws, 64)
+    assert e.value.status == A.BQE_ENOSPC
+
+
+def test_wait_timeout_is_reported_and_recoverable(dev):
+    """A wait that runs out of its limit returns an error status; the context stays usable."""
+    from bit_quantised_expert_gb300 import _abi as A
+    fm = [synth.MXFP4] * 33
+    L = synth.small_layer(12, fm, 2048, 1024, 32, 4, 2)
+    DL = DeviceLayer(L, dev)
+    good, _, _ = DL.forward(L["x"])
+    A.bqe_set_wait_limit_ns(0)
+    try:
+        import torch
+        ws, nb = DL.workspace(2)
+        x = torch.from_numpy(L["x"].view(np.int16)).to(dev)
+        out = torch.zeros(2, 2048, device=dev)
+        seen = set()
+        for _ in range(20):
+            A.bqe_moe_layer_forward(DL.d, 2, x, DL.wr, None, DL.pool.cstruct(), DL.table, None, out, 0, None, None,
+                                    ws, nb)
+            rc, det = A.bqe_check(ws)
+            seen.add(rc)
+            A.bqe_workspace_init(ws, nb)
+            if rc == A.BQE_ETIMEOUT:
+                break
+        assert A.BQE_ETIMEOUT in seen
+    finally:
+        A.bqe_set_wait_limit_ns(2_000_000_000)
+    again, _, _ = DL.forward(L["x"])
+    assert np.array_equal(good, again)
