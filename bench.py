@@ -1,0 +1,560 @@
+#!/usr/bin/env python
+"""Benchmark of the block-quantised MoE expert layer (decode) on GB300.
+
+Metric: MoE layer decode expert-byte GB/s = bytes of the distinct experts a
+call streams (each read once) / layer time, router included; also us/layer,
+tokens/s and the fraction of measured HBM bandwidth.
+
+Default workload: one DeepSeek-V4.1-Flash-shaped MoE layer, every expert
+MXFP4 (hidden 5120, inter 2304, 384 routed + 1 shared, top-6), M = 1 token
+row; seeded synthetic weights and activations generated on the device.
+Consecutive timed steps rotate over 4 independent layer instances (own
+router, shared and routed experts), so every step streams weights that are
+not in L2 (inputs larger than L2).  Other workloads: --workload mixed-m1 | mixed-m6 | step40-m1 | step40-m6.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bqe|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the layer
+(replicas only: the decode layer has no exchange step); the time is the max
+over ranks and the value counts the bytes of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer decode: expert-byte GB/s (% of HBM peak) and us/layer at M=1 and M=6"
+HBM_FALLBACK_GBS = 6800.0
+WORKLOADS = {
+    "fp4-m1": "dsv4flash-moe-layer-mxfp4-decode-M1",
+    "mixed-m1": "dsv4flash-moe-layer-mixed-tq1-q2_0-q3_k-decode-M1",
+    "mixed-m6": "dsv4flash-moe-layer-mixed-tq1-q2_0-q3_k-decode-M6",
+    "step40-m1": "dsv4flash-40-layer-step-4288-slot-pool-M1",
+    "step40-m6": "dsv4flash-40-layer-step-4288-slot-pool-M6",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["bqe", "reference"], default="bqe")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="fp4-m1")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=2.0, help="untimed load before timing, for clock samples")
+    ap.add_argument("--variant", type=int, default=1, help="MXFP4 W1/W3 inner loop: 0 fp32 FMA, 1 f16-input FMA")
+    ap.add_argument("--instances", type=int, default=4, help="layer instances rotated so weights exceed L2")
+    ap.add_argument("--diag", action="store_true", help="print per-CTA cycle accounting of the expert kernels to stderr")
+    ap.add_argument("--experts", type=int, default=384,
+                    help="routed experts in the pool (profiling a smaller pool; per-call work is unchanged)")
+    ap.add_argument("--cpu-oracle-sample", default=None, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), "measured"
+    return HBM_FALLBACK_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled=True):
+        self.p = None
+        self.lines = []
+        if not enabled:
+            return
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.Q,
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            f = [t.strip() for t in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]), hw=f[5], hwt=f[6],
+                                 swt=f[7], swp=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        sm = sorted(r["sm"] for r in rows)
+        reasons = set()
+        for r in rows:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                            ("swp", "sw_power_cap")):
+                if r[k].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------- distributed
+def dist_setup(n):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_oracle_sample(workload: str, reps: int = 1):
+    """Time the oracle (as it stands) on a bounded sample of the workload on the
+    host cores.  Returns (expert bytes, seconds, sample description)."""
+    import numpy as np
+    import synth
+    from oracle import moe as O
+    rng = np.random.default_rng(12345)
+    H, I, E, K = 5120, 2304, 384, 6
+    if workload.startswith("fp4"):
+        fm = [synth.MXFP4] * 7
+        desc = "one MXFP4 layer call at M=1: router (384 x 5120 fp32) + 6 routed + 1 shared expert FFN, fp64"
+    else:
+        fm = [synth.TQ1, synth.TQ1, synth.TQ1, synth.Q2_0, synth.Q2_0, synth.Q3_K, synth.Q2_0]
+        desc = "one mixed-format layer call at M=1 (3 ternary, 2 Q2_0, 1 Q3_K routed + Q2_0 shared), fp64"
+    experts = [synth.random_expert(rng, int(f), H, I) for f in fm]
+    router = synth.router_weights(rng, E, H)
+    x = synth.x_bf16(rng, 1, H)
+    forced = np.arange(6, dtype=np.int32)[None, :]
+    nbytes = sum(synth.expert_bytes(int(f), H, I) for f in fm)
+    # the router scores all 384 experts; the 7 streamed experts are indices 0..6
+    fmts = np.array(fm, dtype=np.int32)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        O.moe_layer(x, router, None, experts, fmts, H, I, K, 6, forced_idx=forced)
+    dt = (time.perf_counter() - t0) / reps
+    return nbytes, dt, desc
+
+
+def run_cpu_baseline(workload: str):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-oracle-sample", workload],
+                       capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+    j = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": j["bytes"] / j["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": j["sample"] + "; %.1f s, single thread" % j["seconds"]}
+
+
+# ----------------------------------------------------------- GPU workloads
+def l2_bytes():
+    import torch
+    return torch.cuda.get_device_properties(0).L2_cache_size
+
+
+def run_layer(args, rank, world):
+    import numpy as np
+    import torch
+    from bit_quantised_expert_gb300 import buildlib
+    buildlib.build()
+    from bit_quantised_expert_gb300 import _abi as A
+    from synth import workloads as WL
+    import synth
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    A.bqe_set_variant(args.variant)
+    M = 6 if args.workload.endswith("m6") else 1
+    n_x = 64
+    NL = args.instances
+    kind = "fp4" if args.workload.startswith("fp4") else "mixed"
+    W = WL.LayerSet(dev, kind, NL, seed=1 if kind == "fp4" else 2, m=M, n_x=n_x, n_experts=args.experts)
+    d, K_ = W.d, 6
+    nb = A.bqe_workspace_bytes(d, M)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    A.bqe_workspace_init(ws, nb)
+    pool = W.pool.cstruct()
+    out = torch.zeros(M, 5120, device=dev)
+    steps, warm = args.steps, args.warmup
+    idx_log = torch.zeros(max(steps, 1), M, K_, dtype=torch.int32, device=dev)
+    idx_tmp = torch.zeros(M, K_, dtype=torch.int32, device=dev)
+    st = torch.cuda.current_stream()
+    xbuf = torch.empty_like(W.xs[0])
+    xs = [W.xs[i] for i in range(n_x)]
+
+    def layer(inst, ev=None):
+        # one decode layer: router + top-k, phase A, phase B (current stream)
+        if ev:
+            ev[0].record()
+        A.bqe_route(d, M, xbuf, W.wr[inst], None if W.bias is None else W.bias[inst], pool, W.tables[inst], None,
+                    idx_tmp, None, ws, nb)
+        if ev:
+            ev[1].record()
+        A.bqe_experts_phase(d, M, pool, out, 0, 0, ws, nb)
+        if ev:
+            ev[2].record()
+        A.bqe_experts_phase(d, M, pool, out, 0, 1, ws, nb)
+        if ev:
+            ev[3].record()
+
+    for i in range(warm):
+        xbuf.copy_(xs[i % n_x])
+        layer(i % NL)
+    torch.cuda.synchronize()
+    rc, det = A.bqe_check(ws)
+    assert rc == 0, (A.status_name(rc), det)
+
+    # The timed unit is one layer replayed from a CUDA graph (the way a decode
+    # loop runs it).  Consecutive steps rotate over NL layer instances whose
+    # weights together are several times L2, so every step streams cold
+    # weights.  Timing events are nodes inside the graph.
+    gev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    graphs = []
+    side = torch.cuda.Stream()
+    side.wait_stream(st)
+    with torch.cuda.stream(side):
+        layer(0)
+    st.wait_stream(side)
+    torch.cuda.synchronize()
+    for inst in range(NL):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layer(inst, gev)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device(), enabled=not args.no_clocks)
+    t_end = time.time() + args.soak_s
+    i = 0
+    while time.time() < t_end:  # untimed load so the clock samples see the GPU busy
+        xbuf.copy_(xs[i % n_x])
+        graphs[i % NL].replay()
+        i += 1
+        if i % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    t_route, t_a, t_b, t_layer = [], [], [], []
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for s_ in range(steps):
+        xbuf.copy_(xs[s_ % n_x])
+        graphs[s_ % NL].replay()
+        idx_log[s_].copy_(idx_tmp)
+        gev[3].synchronize()
+        t_route.append(gev[0].elapsed_time(gev[1]) * 1e-3)
+        t_a.append(gev[1].elapsed_time(gev[2]) * 1e-3)
+        t_b.append(gev[2].elapsed_time(gev[3]) * 1e-3)
+        t_layer.append(gev[0].elapsed_time(gev[3]) * 1e-3)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    clk = clocks.stop()
+    rc, det = A.bqe_check(ws)
+    assert rc == 0, (A.status_name(rc), det)
+
+    idx_np = idx_log.cpu().numpy()
+    bytes_e, bytes_a, bytes_b = [], [], []
+    for s_ in range(steps):
+        inst = s_ % NL
+        us = sorted(set(int(e) for e in idx_np[s_].reshape(-1)) | {W.E})
+        be = sum(W.expert_bytes(inst, e) for e in us)
+        ba = sum(2 * synth.matrix_bytes(int(W.fmts[W.slot(inst, e)]), 2304, 5120) for e in us)  # W1 + W3
+        bytes_e.append(be)
+        bytes_a.append(ba)
+        bytes_b.append(be - ba)
+    T = sum(t_layer)
+    T_max = reduce_max(T, world)
+    total_bytes = reduce_sum(float(sum(bytes_e)), world)
+    value = total_bytes / T_max / 1e9
+    hbm, hbm_kind = peaks()
+    mean = lambda v: sum(v) / len(v)  # noqa: E731
+    achieved_a = mean(bytes_a) / mean(t_a) / 1e9
+    l2mb = torch.cuda.get_device_properties(0).L2_cache_size / 2 ** 20
+    res = dict(
+        metric=METRIC, value=round(value, 2), unit="GB/s", n_gpus=world, steps=steps, warmup=warm,
+        ms_per_step=round(T_max / steps * 1e3, 5), higher_is_better=True, scaling="weak",
+        vs_baseline=None, dtype="fp32-accumulate over %s weights, bf16 activations" % (
+            "mxfp4" if kind == "fp4" else "ternary/q2_0/q3_k"),
+        data="synthetic (seeded, generated on the device)",
+        config=dict(workload=WORKLOADS[args.workload], hidden=5120, inter=2304, n_experts=W.E, top_k=6,
+                    n_shared=1, M=M,
+                    l2="inputs larger than L2: steps rotate over %d layer instances (%.0f MB of weights streamed "
+                       "between reuses vs %.0f MB L2)" % (NL, (NL - 1) * mean(bytes_e) / 1e6, l2mb),
+                    parallelism="replicas" if world > 1 else "single-gpu"),
+        us_per_layer=round(T_max / steps * 1e6, 3),
+        tokens_per_s=round(M * steps * world / T_max, 1),
+        frac_of_hbm=round(value / hbm, 4), hbm_peak_gbs=hbm, hbm_peak_kind=hbm_kind,
+        expert_bytes_per_step=round(mean(bytes_e)),
+        kernels_us=dict(route=round(mean(t_route) * 1e6, 3), phase_a=round(mean(t_a) * 1e6, 3),
+                        phase_b=round(mean(t_b) * 1e6, 3)),
+        roofline=dict(bound="hbm", achieved=round(achieved_a, 1), peak=hbm, unit="GB/s",
+                      frac=round(achieved_a / hbm, 4), traffic=None,
+                      kernel="k_experts<0> (W1/W3 dequant-GEMV + SiLU-GLU)",
+                      algorithmic_bytes_per_launch=round(mean(bytes_a)),
+                      peak_kind="%s hbm_gbs (burst copy)" % hbm_kind,
+                      phase_b=dict(achieved=round(mean(bytes_b) / mean(t_b) / 1e9, 1),
+                                   frac=round(mean(bytes_b) / mean(t_b) / 1e9 / hbm, 4))),
+        gpu_launches=3 * steps,
+        variant=args.variant,
+        timing="CUDA-graph replay per step, kernel split from event nodes inside the graph",
+        wall_s_timed_loop=round(wall, 4),
+    )
+    if clk:
+        res["clocks"] = clk
+
+    if args.diag:
+        # per-CTA cycle accounting (a separate, untimed pass)
+        A.bqe_set_diag(True)
+        A.bqe_workspace_init(ws, nb)
+        nd = 20
+        for s_ in range(nd):
+            xbuf.copy_(xs[s_ % n_x])
+            layer(s_ % NL)
+        torch.cuda.synchronize()
+        A.bqe_set_diag(False)
+        off = A.bqe_diag_offset(d, M)
+        dbg = ws[off:off + 8 * 2 * 1024 * 8].view(torch.int64).view(2, 1024, 8).cpu().numpy()
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        names = ["prod_wait_empty", "prod_issue", "cons_wait_stage", "cons_wait_redbuf", "cons_compute",
+                 "epi_wait", "epi_work", "cta_total"]
+        rep = {}
+        for ph in range(2):
+            v = dbg[ph, :sms].astype(np.float64) / nd / 2.07e3  # us per call at 2.07 GHz
+            rep["phase_%d" % ph] = {n: [round(float(v[:, k].mean()), 2), round(float(v[:, k].max()), 2)]
+                                    for k, n in enumerate(names)}
+        A.bqe_workspace_init(ws, nb)
+        sys.stderr.write("DIAG " + json.dumps(rep) + "\n")
+
+    # ---- end to end through the public call with host buffers --------------
+    xh = torch.empty(M, 5120, dtype=torch.int16).pin_memory()
+    oh = torch.empty(M, 5120, dtype=torch.float32).pin_memory()
+    xd = torch.empty(M, 5120, dtype=torch.int16, device=dev)
+    xs_host = [x.cpu() for x in xs]
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for s_ in range(steps):
+        inst = s_ % NL
+        xh.copy_(xs_host[s_ % n_x])
+        e2e_ev[s_][0].record(st)
+        xd.copy_(xh, non_blocking=True)
+        A.bqe_moe_layer_forward(d, M, xd, W.wr[inst], None if W.bias is None else W.bias[inst], pool,
+                                W.tables[inst], None, out, 0, idx_log[s_], None, ws, nb)
+        oh.copy_(out, non_blocking=True)
+        e2e_ev[s_][1].record(st)
+    torch.cuda.synchronize()
+    Te = sum(e2e_ev[s_][0].elapsed_time(e2e_ev[s_][1]) * 1e-3 for s_ in range(steps))
+    idx_np = idx_log.cpu().numpy()
+    be2 = sum(sum(W.expert_bytes(s_ % NL, e) for e in (set(int(v) for v in idx_np[s_].reshape(-1)) | {W.E}))
+              for s_ in range(steps))
+    Te_max = reduce_max(Te, world)
+    res["e2e"] = dict(value=round(reduce_sum(float(be2), world) / Te_max / 1e9, 2), unit="GB/s",
+                      h2d_bytes_per_step=M * 5120 * 2, d2h_bytes_per_step=M * 5120 * 4,
+                      us_per_layer=round(Te_max / steps * 1e6, 3),
+                      note="eager calls through bqe_moe_layer_forward, pinned host x in, host out back")
+    return res
+
+
+def run_step40(args, rank, world):
+    import torch
+    from bit_quantised_expert_gb300 import buildlib
+    buildlib.build()
+    from bit_quantised_expert_gb300 import _abi as A
+    from synth import workloads as WL
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    M = 6 if args.workload.endswith("m6") else 1
+    S = WL.Step40(dev, m=M)
+    d, L = S.d, S.n_layers
+    nb = A.bqe_workspace_bytes(d, M)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    A.bqe_workspace_init(ws, nb)
+    pool = S.pool.cstruct()
+    resid = torch.zeros(M, 5120, device=dev)
+    forced = torch.zeros(L, M, 6, dtype=torch.int32, device=dev)
+    nf = S.forced.shape[0]
+    st = torch.cuda.current_stream()
+
+    def load(i):
+        forced.copy_(S.forced[i % nf])
+        resid.copy_(S.x0[i % nf])
+
+    def run():
+        A.bqe_moe_step(d, L, M, resid, S.wr, None, pool, S.tables, forced, None, ws, nb, st.cuda_stream)
+
+    for i in range(max(args.warmup, 3)):
+        load(i)
+        run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    clocks = ClockSampler(torch.cuda.current_device(), enabled=not args.no_clocks)
+    t_end = time.time() + args.soak_s
+    i = 0
+    while time.time() < t_end:
+        load(i)
+        g.replay()
+        i += 1
+    torch.cuda.synchronize()
+    steps = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    barrier(world)
+    for s in range(steps):
+        load(s)
+        evs[s][0].record(st)
+        g.replay()
+        evs[s][1].record(st)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    rc, det = A.bqe_check(ws)
+    assert rc == 0, (A.status_name(rc), det)
+    ts = [evs[s][0].elapsed_time(evs[s][1]) * 1e-3 for s in range(steps)]
+    by = [sum(S.layer_bytes(l, s % nf) for l in range(L)) for s in range(steps)]
+    T = reduce_max(sum(ts), world)
+    tot = reduce_sum(float(sum(by)), world)
+    hbm, hbm_kind = peaks()
+    value = tot / T / 1e9
+    res = dict(metric=METRIC, value=round(value, 2), unit="GB/s", n_gpus=world, steps=steps, warmup=args.warmup,
+               ms_per_step=round(T / steps * 1e3, 4), higher_is_better=True, scaling="weak", vs_baseline=None,
+               dtype="fp32-accumulate over ternary/q2_0/q3_k weights, bf16 activations",
+               data="synthetic (seeded, generated on the device)",
+               config=dict(workload=WORKLOADS[args.workload], layers=L, slots=4288, M=M,
+                           l2="not flushed: each step streams ~3 GB, far above L2",
+                           routing="Zipf(1.0) forced selection, scores from the router",
+                           parallelism="replicas" if world > 1 else "single-gpu"),
+               us_per_layer=round(T / steps / L * 1e6, 3), tokens_per_s=round(M * steps * world / T, 1),
+               frac_of_hbm=round(value / hbm, 4), hbm_peak_gbs=hbm, expert_bytes_per_step=round(sum(by) / steps),
+               gpu_launches=3 * L * steps, cuda_graph=True)
+    if clk:
+        res["clocks"] = clk
+    return res
+
+
+def run_reference(args, rank, world):
+    """The oracle (fp64, as it stands) on the host cores, one bounded sample per step."""
+    if rank != 0:
+        return None
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ.setdefault(k, "1")  # before numpy loads its BLAS: report the threads really used
+    import numpy as np
+    import synth
+    from oracle import formats as F
+    from oracle import moe as O
+    rng = np.random.default_rng(777)
+    fmt = synth.MXFP4 if args.workload.startswith("fp4") else synth.Q2_0
+    H, I = 5120, 2304
+    ex = synth.random_expert(rng, fmt, H, I)
+    x = synth.x_bf16(rng, 1, H)
+    nbytes = synth.expert_bytes(fmt, H, I)
+
+    def step():
+        w1, w3, w2 = F.dequant_expert(fmt, ex, H, I)
+        O.expert_ffn(O.bf16_bits_to_f64(x), w1, w3, w2)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    T = time.perf_counter() - t0
+    value = nbytes * args.steps / T / 1e9
+    sample = "one expert FFN (%s, %d bytes) per step at M=1 in fp64 numpy" % (synth.FMT_NAMES[fmt], nbytes)
+    return dict(metric=METRIC, value=round(value, 4), unit="GB/s", n_gpus=world, steps=args.steps,
+                warmup=args.warmup, ms_per_step=round(T / args.steps * 1e3, 3), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic (seeded)", impl="reference",
+                config=dict(workload=WORKLOADS[args.workload], M=1),
+                cpu_baseline=dict(value=round(value, 4), unit="GB/s", cores=_threads_used(), kind="oracle",
+                                  sample=sample),
+                e2e=dict(value=round(value, 4), unit="GB/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+
+
+def _threads_used():
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count() or 1
+
+
+def main():
+    args = parse()
+    if args.cpu_oracle_sample:
+        nbytes, dt, desc = cpu_oracle_sample(args.cpu_oracle_sample)
+        print(json.dumps(dict(bytes=nbytes, seconds=dt, sample=desc)))
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res))
+        return
+    rank, world, local = dist_setup(args.gpus)
+    if args.workload.startswith("step40"):
+        res = run_step40(args, rank, world)
+    else:
+        res = run_layer(args, rank, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = run_cpu_baseline(args.workload)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -11,11 +11,17 @@ using namespace bqe;
 
 static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};  // 2 s per wait
 static std::atomic<int> g_use_pdl{1};
+static std::atomic<int> g_drop_item{-1};
+static std::atomic<int> g_variant{1};
+static std::atomic<int> g_diag{0};
 
 // Diagnostic knobs (not part of the operation): the bound on every in-kernel
 // wait, and whether kernels are chained with programmatic dependent launch.
 extern "C" void bqe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
 extern "C" void bqe_set_pdl(int on) { g_use_pdl = on ? 1 : 0; }
+extern "C" void bqe_set_test_drop_item(int32_t item) { g_drop_item = item; }
+extern "C" void bqe_set_variant(int32_t v) { g_variant = v; }
+extern "C" void bqe_set_diag(int32_t on) { g_diag = on ? 1 : 0; }
 
 static int device_sms() {
   static int cache[64] = {0};
@@ -36,6 +42,11 @@ static bool desc_ok(const bqe_layer_desc* d) {
 }
 
 static Geo geo_of(const bqe_layer_desc* d, int M) { return make_geo(d->hidden, d->inter, d->n_experts, d->top_k, M); }
+
+extern "C" uint64_t bqe_diag_offset(const bqe_layer_desc* d, int32_t M) {
+  if (!desc_ok(d) || M < 1 || M > kMaxM) return 0;
+  return make_ws(geo_of(d, M)).dbg;
+}
 
 extern "C" uint64_t bqe_workspace_bytes(const bqe_layer_desc* d, int32_t M) {
   if (!desc_ok(d) || M < 1 || M > kMaxM) return 0;
@@ -81,7 +92,7 @@ static int route_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, c
 }
 
 static int experts_common(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out, int32_t accumulate,
-                          void* ws, uint64_t ws_bytes, cudaStream_t st) {
+                          void* ws, uint64_t ws_bytes, cudaStream_t st, int only_phase = -1) {
   if (!desc_ok(d) || M < 1 || M > kMaxM || !out || !ws || ((uintptr_t)ws & 255)) return BQE_EINVAL;
   int rc = check_pool(pool);
   if (rc) return rc;
@@ -97,13 +108,18 @@ static int experts_common(const bqe_layer_desc* d, int32_t M, const bqe_pool* po
   P.out = out;
   P.accumulate = accumulate ? 1 : 0;
   P.limit_ns = g_wait_limit_ns.load();
+  P.drop_item = g_drop_item.load();
+  P.variant = g_variant.load();
+  P.diag = g_diag.load();
   const bool pdl = g_use_pdl.load() != 0;
   for (int phase = 0; phase < 2; ++phase) {
+    if (only_phase >= 0 && phase != only_phase) continue;
     int ns = 0;
     experts_smem_bytes(g, phase, &ns);
     if (ns < 2) return BQE_EUNSUPPORTED;
     P.nstages = ns;
     if ((rc = launch_experts(P, phase, sms, st, pdl))) return rc;
+    if ((rc = launch_finalize(P, phase, sms, st, pdl))) return rc;
   }
   return BQE_OK;
 }
@@ -120,6 +136,12 @@ extern "C" int bqe_route(const bqe_layer_desc* d, int32_t M, const uint16_t* x, 
 extern "C" int bqe_experts(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out,
                            int32_t accumulate, void* ws, uint64_t ws_bytes, void* stream) {
   return experts_common(d, M, pool, out, accumulate, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int bqe_experts_phase(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out,
+                                 int32_t accumulate, int32_t phase, void* ws, uint64_t ws_bytes, void* stream) {
+  if (phase != 0 && phase != 1) return BQE_EINVAL;
+  return experts_common(d, M, pool, out, accumulate, ws, ws_bytes, (cudaStream_t)stream, phase);
 }
 
 extern "C" int bqe_moe_layer_forward(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w,

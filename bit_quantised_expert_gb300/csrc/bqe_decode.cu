@@ -38,19 +38,16 @@ struct StageHdr {
   int u, p0, c, fmt, R, pad;
 };
 
-constexpr int kFmtMaxBytesPerCol = 17;  // MXFP4 tile: 17 bytes per column per 32 rows
-
 __host__ __device__ inline int phase_mats(int phase) { return phase == 0 ? 2 : 1; }
 
+__host__ __device__ inline int phase_panels(const Geo& g, int phase) { return phase == 0 ? g.PA : g.PB; }
+
 __host__ __device__ inline uint32_t stage_slot_bytes(const Geo& g, int phase) {
-  const int kc = phase == 0 ? g.kcA : g.kcB;
-  const int P = phase == 0 ? 1 : g.PB;
-  const uint32_t w = (uint32_t)phase_mats(phase) * P * kFmtMaxBytesPerCol * kc;
-  return ((w + (uint32_t)g.M * kc * 4u) + 127u) & ~127u;
+  return stage_bytes_for(phase_mats(phase), phase_panels(g, phase), phase == 0 ? g.kcA : g.kcB, g.M);
 }
 
 __host__ __device__ inline int phase_warps(const Geo& g, int phase) {
-  return phase == 0 ? 2 * g.GA : g.PB * g.GB;
+  return phase_mats(phase) * phase_panels(g, phase) * (phase == 0 ? g.GA : g.GB);
 }
 
 // ---------------------------------------------------------------------------
@@ -69,6 +66,26 @@ __device__ __forceinline__ float2 e2m1x2_f32(uint32_t byte) {
   return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
+// Four E2M1 pairs of one 32-bit word -> four f16x2 (exact; the low nibble of
+// each byte is the lower half), by the hardware E2M1x2 -> f16x2 conversion.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& h0, uint32_t& h1, uint32_t& h2,
+                                                uint32_t& h3) {
+  asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;\n"
+      "  cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      "  cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(w));
+}
+
+// a0 += lo(w) * lo(x), a1 += hi(w) * hi(x): f16 inputs, exact f32 products,
+// f32 accumulation (mixed-precision FMA of sm_100+).
+__device__ __forceinline__ void fma_f16x2_f32(uint32_t w, uint32_t x, float& a0, float& a1) {
+  asm("{ .reg .f16 wl, wh, xl, xh; mov.b32 {wl, wh}, %2; mov.b32 {xl, xh}, %3;\n"
+      "  fma.rn.f32.f16 %0, wl, xl, %0; fma.rn.f32.f16 %1, wh, xh, %1; }"
+      : "+f"(a0), "+f"(a1)
+      : "r"(w), "r"(x));
+}
+
 template <int R>
 __device__ __forceinline__ void group_mxfp4(const uint8_t* tile, int nb, int grp, const float* act, int kc, int lane,
                                             float2 (&acc)[R]) {
@@ -77,29 +94,67 @@ __device__ __forceinline__ void group_mxfp4(const uint8_t* tile, int nb, int grp
     const int b = grp * 8 + bi;
     const uint4 c4 = *reinterpret_cast<const uint4*>(tile + b * 512 + lane * 16);
     const float sc = ue8m0_f32(tile[nb * 512 + b * 32 + lane]);
-    float2 bs[R];
+    float2 bs[R][2];  // two independent chains per row
 #pragma unroll
-    for (int r = 0; r < R; ++r) bs[r] = f2(0.f, 0.f);
+    for (int r = 0; r < R; ++r) bs[r][0] = bs[r][1] = f2(0.f, 0.f);
     const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const float2 v0 = e2m1x2_f32(wd[w] & 0xFF);
-      const float2 v1 = e2m1x2_f32((wd[w] >> 8) & 0xFF);
-      const float2 v2 = e2m1x2_f32((wd[w] >> 16) & 0xFF);
-      const float2 v3 = e2m1x2_f32(wd[w] >> 24);
+      uint32_t h0, h1, h2, h3;
+      e2m1x8_to_f16x2(wd[w], h0, h1, h2, h3);
+      const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+      const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+      const float2 v2 = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      const float2 v3 = __half22float2(*reinterpret_cast<const __half2*>(&h3));
       const int k = grp * 256 + bi * 32 + w * 8;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const float4 xa = *reinterpret_cast<const float4*>(act + r * kc + k);
         const float4 xb = *reinterpret_cast<const float4*>(act + r * kc + k + 4);
-        bs[r] = __ffma2_rn(v0, f2(xa.x, xa.y), bs[r]);
-        bs[r] = __ffma2_rn(v1, f2(xa.z, xa.w), bs[r]);
-        bs[r] = __ffma2_rn(v2, f2(xb.x, xb.y), bs[r]);
-        bs[r] = __ffma2_rn(v3, f2(xb.z, xb.w), bs[r]);
+        bs[r][0] = __ffma2_rn(v0, f2(xa.x, xa.y), bs[r][0]);
+        bs[r][1] = __ffma2_rn(v1, f2(xa.z, xa.w), bs[r][1]);
+        bs[r][0] = __ffma2_rn(v2, f2(xb.x, xb.y), bs[r][0]);
+        bs[r][1] = __ffma2_rn(v3, f2(xb.z, xb.w), bs[r][1]);
       }
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = __ffma2_rn(bs[r], f2(sc, sc), acc[r]);
+    for (int r = 0; r < R; ++r)
+      acc[r] = __ffma2_rn(f2(bs[r][0].x + bs[r][1].x, bs[r][0].y + bs[r][1].y), f2(sc, sc), acc[r]);
+  }
+}
+
+// MXFP4 group with f16 activations (act_h: R rows x kc halves, scaled by a
+// power of two per row; the epilogue removes the scale).  Four accumulator
+// chains per row.
+template <int R>
+__device__ __forceinline__ void group_mxfp4_h(const uint8_t* tile, int nb, int grp, const uint16_t* act_h, int kc,
+                                              int lane, float2 (&acc)[R]) {
+#pragma unroll 1
+  for (int bi = 0; bi < 8; ++bi) {
+    const int b = grp * 8 + bi;
+    const uint4 c4 = *reinterpret_cast<const uint4*>(tile + b * 512 + lane * 16);
+    const float sc = ue8m0_f32(tile[nb * 512 + b * 32 + lane]);
+    float a[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r) a[r][0] = a[r][1] = a[r][2] = a[r][3] = 0.f;
+    const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t h0, h1, h2, h3;
+      e2m1x8_to_f16x2(wd[w], h0, h1, h2, h3);
+      const int k = grp * 256 + bi * 32 + w * 8;
+      const int ch = (w & 1) * 2;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(act_h + r * kc + k);
+        fma_f16x2_f32(h0, xv.x, a[r][ch], a[r][ch + 1]);
+        fma_f16x2_f32(h1, xv.y, a[r][ch], a[r][ch + 1]);
+        fma_f16x2_f32(h2, xv.z, a[r][ch], a[r][ch + 1]);
+        fma_f16x2_f32(h3, xv.w, a[r][ch], a[r][ch + 1]);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r].x = fmaf((a[r][0] + a[r][1]) + (a[r][2] + a[r][3]), sc, acc[r].x);
   }
 }
 
@@ -269,13 +324,18 @@ __device__ __forceinline__ void group_q3k(const uint8_t* tile, int nb, int grp, 
 
 template <int R>
 __device__ __forceinline__ void consume_group_R(int fmt, const uint8_t* tile, int kc, int grp, const float* act,
-                                                int lane, float* outv /* [r * 32 + lane] */) {
+                                                int lane, float* outv /* [r * 32 + lane] */, bool half_act) {
   float2 acc[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) acc[r] = f2(0.f, 0.f);
   const int nb = kc / fmt_bw(fmt);
   switch (fmt) {
-    case BQE_FMT_MXFP4: group_mxfp4<R>(tile, nb, grp, act, kc, lane, acc); break;
+    case BQE_FMT_MXFP4:
+      if (half_act)
+        group_mxfp4_h<R>(tile, nb, grp, reinterpret_cast<const uint16_t*>(act), kc, lane, acc);
+      else
+        group_mxfp4<R>(tile, nb, grp, act, kc, lane, acc);
+      break;
     case BQE_FMT_Q2_0: group_q2_0<R>(tile, nb, grp, act, kc, lane, acc); break;
     case BQE_FMT_TQ1: group_tq1<R>(tile, nb, grp, act, kc, lane, acc); break;
     case BQE_FMT_Q3_K: group_q3k<R>(tile, nb, grp, act, kc, lane, acc); break;
@@ -285,26 +345,57 @@ __device__ __forceinline__ void consume_group_R(int fmt, const uint8_t* tile, in
 }
 
 __device__ __forceinline__ void consume_group(int R, int fmt, const uint8_t* tile, int kc, int grp, const float* act,
-                                              int lane, float* outv) {
+                                              int lane, float* outv, bool half_act) {
   switch (R) {
-    case 1: consume_group_R<1>(fmt, tile, kc, grp, act, lane, outv); break;
-    case 2: consume_group_R<2>(fmt, tile, kc, grp, act, lane, outv); break;
-    case 3: consume_group_R<3>(fmt, tile, kc, grp, act, lane, outv); break;
-    case 4: consume_group_R<4>(fmt, tile, kc, grp, act, lane, outv); break;
-    case 5: consume_group_R<5>(fmt, tile, kc, grp, act, lane, outv); break;
-    case 6: consume_group_R<6>(fmt, tile, kc, grp, act, lane, outv); break;
-    case 7: consume_group_R<7>(fmt, tile, kc, grp, act, lane, outv); break;
-    case 8: consume_group_R<8>(fmt, tile, kc, grp, act, lane, outv); break;
+    case 1: consume_group_R<1>(fmt, tile, kc, grp, act, lane, outv, half_act); break;
+    case 2: consume_group_R<2>(fmt, tile, kc, grp, act, lane, outv, half_act); break;
+    case 3: consume_group_R<3>(fmt, tile, kc, grp, act, lane, outv, half_act); break;
+    case 4: consume_group_R<4>(fmt, tile, kc, grp, act, lane, outv, half_act); break;
+  }
+}
+
+// All R rows of one stage, kRowChunk rows at a time (the weights of the group
+// are decoded again for each further chunk; only rows 5..8 of a call pay it).
+__device__ __forceinline__ void consume_rows(int R, int fmt, const uint8_t* tile, int kc, int grp, const uint8_t* act,
+                                             int lane, float* outv, bool half_act) {
+  const size_t row_bytes = (size_t)kc * (half_act ? 2 : 4);
+  for (int r0 = 0; r0 < R; r0 += kRowChunk) {
+    const int n = R - r0 < kRowChunk ? R - r0 : kRowChunk;
+    consume_group(n, fmt, tile, kc, grp, reinterpret_cast<const float*>(act + r0 * row_bytes), lane, outv + r0 * 32,
+                  half_act);
   }
 }
 
 __device__ __forceinline__ float silu_f(float t) { return t / (1.0f + expf(-t)); }
 
+__device__ __forceinline__ long long clk() { return clock64(); }
+// diagnostic counters: 0 producer waiting for a free stage, 1 producer issuing,
+// 2 consumer (warp 1) waiting for a stage, 3 consumer waiting for a reduction
+// buffer, 4 consumer computing, 5 epilogue waiting, 6 epilogue working,
+// 7 whole CTA
+__device__ __forceinline__ void dbg_add(const ExpParams& P, int phase, int slot, long long v) {
+  if (P.diag && blockIdx.x < kDbgMaxCtas)
+    atomicAdd((unsigned long long*)(P.ws + P.L.dbg) + ((size_t)phase * kDbgMaxCtas + blockIdx.x) * kDbgSlots + slot,
+              (unsigned long long)v);
+}
+
 // ---------------------------------------------------------------------------
 // the engine
 // ---------------------------------------------------------------------------
+// Shared-memory map of the engine (offsets in bytes):
+//   0      StageHdr[16]               ring stage headers
+//   512    full[16], empty[16]        ring mbarriers
+//   768    rfull[kRed], rempty[kRed]  reduction-buffer mbarriers
+//   896    abort flag
+//   1024   RedMeta[kRed]
+//   2048   red[kRed][NW][M][32] floats (consumer partial sums for the epilogue)
+//   ...    ring of nstages slots
+struct RedMeta {
+  int u, p0, c, R;
+};
+
 template <int PHASE>
-__global__ void __launch_bounds__(32 * (kMaxWarps + 1), 1) k_experts(ExpParams P) {
+__global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P) {
   const Geo& g = P.g;
   extern __shared__ __align__(128) uint8_t smem[];
   const int NW = phase_warps(g, PHASE);
@@ -312,16 +403,20 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 1), 1) k_experts(ExpParams P
   const uint32_t slot_bytes = stage_slot_bytes(g, PHASE);
   const int nstages = P.nstages;
   StageHdr* hdr = reinterpret_cast<StageHdr*>(smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 1024);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + 512);
   uint64_t* empty = full + 16;
-  float* red = reinterpret_cast<float*>(smem + 2048);  // [2][kMaxWarps][kMaxM][32]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 1920);
-  uint8_t* ring = smem + 2048 + 2 * kMaxWarps * kMaxM * 32 * 4;
+  uint64_t* rfull = reinterpret_cast<uint64_t*>(smem + 768);
+  uint64_t* rempty = rfull + kRed;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 896);
+  RedMeta* rmeta = reinterpret_cast<RedMeta*>(smem + 1024);
+  float* red = reinterpret_cast<float*>(smem + kEngineBase);
+  const int red_stride = NW * g.M * 32;  // floats per reduction buffer; warp cw, row r at (cw * M + r) * 32
+  uint8_t* ring = smem + kEngineBase + red_bytes_for(NW, g.M);
   int32_t* err = (int32_t*)(P.ws + P.L.err);
 
   const int kc = PHASE == 0 ? g.kcA : g.kcB;
   const int nch = PHASE == 0 ? g.nchA : g.nchB;
-  const int P_ = PHASE == 0 ? 1 : g.PB;
+  const int P_ = phase_panels(g, PHASE);
   const int G = PHASE == 0 ? g.GA : g.GB;
   const int npan = PHASE == 0 ? g.npanA : g.npanB;
   const int per_u = (npan / P_) * nch;
@@ -330,6 +425,10 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 1), 1) k_experts(ExpParams P
     for (int s = 0; s < nstages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NW);
+    }
+    for (int b = 0; b < kRed; ++b) {
+      mbar_init(&rfull[b], NW);
+      mbar_init(&rempty[b], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -340,10 +439,19 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 1), 1) k_experts(ExpParams P
 
   const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
   const int nItems = nU * per_u;
-  const int32_t* u_fmt = (const int32_t*)(P.ws + P.L.u_fmt);
-  const uint64_t* u_addr = (const uint64_t*)(P.ws + P.L.u_addr);
-  const int32_t* u_nrows = (const int32_t*)(P.ws + P.L.u_nrows);
-  const int32_t* u_rows = (const int32_t*)(P.ws + P.L.u_rows);
+  // the work list (format, slot address, rows of every distinct expert) in
+  // shared memory, so no item waits on a global load
+  __shared__ int32_t s_ufmt[kMaxM * kMaxTopK + 1];
+  __shared__ int32_t s_unrows[kMaxM * kMaxTopK + 1];
+  __shared__ uint64_t s_uaddr[kMaxM * kMaxTopK + 1];
+  __shared__ int8_t s_urows[(kMaxM * kMaxTopK + 1) * kMaxM];
+  for (int u = tid; u < nU; u += blockDim.x) {
+    s_ufmt[u] = ((const int32_t*)(P.ws + P.L.u_fmt))[u];
+    s_unrows[u] = ((const int32_t*)(P.ws + P.L.u_nrows))[u];
+    s_uaddr[u] = ((const uint64_t*)(P.ws + P.L.u_addr))[u];
+    for (int r = 0; r < kMaxM; ++r) s_urows[u * kMaxM + r] = (int8_t)((const int32_t*)(P.ws + P.L.u_rows))[u * kMaxM + r];
+  }
+  __syncthreads();
   const float* xf = (const float*)(P.ws + P.L.xf);
   float* hbuf = (float*)(P.ws + P.L.h);
 
@@ -352,34 +460,43 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 1), 1) k_experts(ExpParams P
     if (lane == 0) {
       int last_issued[16];
       for (int s = 0; s < 16; ++s) last_issued[s] = -1;
+      long long pw = 0, pi_ = 0;
       int i = 0;
       for (int t = blockIdx.x; t < nItems; t += gridDim.x, ++i) {
         const int s = i % nstages;
         if (*abort_flag) break;
         if (i >= nstages) {
+          const long long t0 = clk();
           if (!mbar_wait_bounded(&empty[s], ((i / nstages) - 1) & 1, P.limit_ns)) {
             set_error(err, BQE_ETIMEOUT, kErrWaitEmpty);
             *abort_flag = 1;
             break;
           }
+          pw += clk() - t0;
         }
+        const long long t1 = clk();
+        if (i == P.drop_item && blockIdx.x == 0) continue;  // test hook: this stage never lands
         const int u = t / per_u, rem = t % per_u;
         const int pg = rem / nch, c = rem % nch;
-        const int fmt = u_fmt[u];
-        const int R = u_nrows[u];
-        const uint64_t addr = u_addr[u];
+        const int fmt = s_ufmt[u];
+        const int R = s_unrows[u];
+        const uint64_t addr = s_uaddr[u];
         StageHdr& H = hdr[s];
         H.addr = addr; H.u = u; H.p0 = pg * P_; H.c = c; H.fmt = fmt; H.R = R;
         const uint32_t tb = tile_bytes(fmt, kc);
         const uint32_t wbytes = (uint32_t)phase_mats(PHASE) * P_ * tb;
-        const uint32_t abytes = (uint32_t)R * kc * 4u;
+        const bool half_act = PHASE == 0 && fmt == BQE_FMT_MXFP4 && P.variant == 1;
+        const uint32_t arow = (uint32_t)kc * (half_act ? 2u : 4u);
+        const uint32_t abytes = (uint32_t)R * arow;
         uint8_t* dst = ring + (size_t)s * slot_bytes;
         mbar_arrive_expect_tx(&full[s], wbytes + abytes);
         const uint64_t m13 = matrix_bytes(fmt, g.I, g.H);
         if (PHASE == 0) {
-          const uint64_t toff = (uint64_t)(pg * nch + c) * tb;
-          bulk_g2s(dst, (const void*)(addr + toff), tb, &full[s]);
-          bulk_g2s(dst + tb, (const void*)(addr + m13 + toff), tb, &full[s]);
+          for (int j = 0; j < P_; ++j) {
+            const uint64_t toff = (uint64_t)((pg * P_ + j) * nch + c) * tb;
+            bulk_g2s(dst + j * tb, (const void*)(addr + toff), tb, &full[s]);                 // W1
+            bulk_g2s(dst + (P_ + j) * tb, (const void*)(addr + m13 + toff), tb, &full[s]);    // W3
+          }
         } else {
           for (int j = 0; j < P_; ++j) {
             const uint64_t toff = 2 * m13 + (uint64_t)((pg * P_ + j) * nch + c) * tb;
@@ -387,13 +504,21 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 1), 1) k_experts(ExpParams P
           }
         }
         uint8_t* adst = dst + wbytes;
+        const uint16_t* xh = (const uint16_t*)(P.ws + P.L.xh);
         for (int r = 0; r < R; ++r) {
-          const float* src = PHASE == 0 ? xf + (int64_t)u_rows[u * kMaxM + r] * g.H + (int64_t)c * kc
-                                        : hbuf + ((int64_t)u * g.M + r) * g.I + (int64_t)c * kc;
-          bulk_g2s(adst + (size_t)r * kc * 4, src, (uint32_t)kc * 4u, &full[s]);
+          const void* src;
+          if (PHASE == 0)
+            src = half_act ? (const void*)(xh + (int64_t)s_urows[u * kMaxM + r] * g.H + (int64_t)c * kc)
+                           : (const void*)(xf + (int64_t)s_urows[u * kMaxM + r] * g.H + (int64_t)c * kc);
+          else
+            src = hbuf + ((int64_t)u * g.M + r) * g.I + (int64_t)c * kc;
+          bulk_g2s(adst + (size_t)r * arow, src, arow, &full[s]);
         }
         last_issued[s] = i;
+        pi_ += clk() - t1;
       }
+      dbg_add(P, PHASE, 0, pw);
+      dbg_add(P, PHASE, 1, pi_);
       if (*abort_flag) {
         // drain this CTA's copies still in flight before leaving
         for (int s = 0; s < nstages; ++s)
@@ -403,126 +528,194 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 1), 1) k_experts(ExpParams P
     return;
   }
 
-  // --------------------------------- consumers --------------------------------
-  const int cw = warp - 1;
-  if (cw >= NW) return;
-  const int mat = PHASE == 0 ? cw / G : 0;
-  const int pan = PHASE == 0 ? 0 : cw / G;
-  const int grp = cw % G;
-  int i = 0;
-  for (int t = blockIdx.x; t < nItems; t += gridDim.x, ++i) {
-    const int s = i % nstages;
-    // every lane waits; the warp proceeds only if all lanes saw the stage land
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (i / nstages) & 1, P.limit_ns));
-    float* rb = red + (size_t)(i & 1) * kMaxWarps * kMaxM * 32;
-    const StageHdr H = hdr[s];
-    if (!ok) {
-      if (lane == 0) { set_error(err, BQE_ETIMEOUT, kErrWaitFull); *abort_flag = 1; }
-    } else {
+  if (warp <= NW) {
+    // --------------------------------- consumers ------------------------------
+    const int cw = warp - 1;
+    long long cwf = 0, cwr = 0, ccomp = 0;
+    const int mat = cw / (P_ * G);         // 0: W1 (or W2), 1: W3
+    const int pan = (cw / G) % P_;
+    const int grp = cw % G;
+    int i = 0;
+    for (int t = blockIdx.x; t < nItems; t += gridDim.x, ++i) {
+      const int s = i % nstages, b = i % kRed;
+      const long long t0 = clk();
+      // every lane waits; the warp proceeds only if all lanes saw the stage land
+      bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (i / nstages) & 1, P.limit_ns));
+      const long long t1 = clk();
+      if (ok && i >= kRed)
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&rempty[b], ((i / kRed) - 1) & 1, P.limit_ns));
+      const long long t2 = clk();
+      cwf += t1 - t0;
+      cwr += t2 - t1;
+      if (!ok) {
+        if (lane == 0) {
+          set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      const StageHdr H = hdr[s];
       const uint32_t tb = tile_bytes(H.fmt, kc);
       const uint8_t* slot = ring + (size_t)s * slot_bytes;
-      const uint8_t* tile = slot + (PHASE == 0 ? mat * tb : pan * tb);
-      const float* act = reinterpret_cast<const float*>(slot + (size_t)phase_mats(PHASE) * P_ * tb);
-      consume_group(H.R, H.fmt, tile, kc, grp, act, lane, rb + cw * kMaxM * 32);
+      const uint8_t* tile = slot + (size_t)(mat * P_ + pan) * tb;
+      const uint8_t* act = slot + (size_t)phase_mats(PHASE) * P_ * tb;
+      float* rb = red + (size_t)b * red_stride;
+      const bool half_act = PHASE == 0 && H.fmt == BQE_FMT_MXFP4 && P.variant == 1;
+      consume_rows(H.R, H.fmt, tile, kc, grp, act, lane, rb + cw * g.M * 32, half_act);
+      if (cw == 0 && lane == 0) rmeta[b] = RedMeta{H.u, H.p0, H.c, H.R};
+      ccomp += clk() - t2;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0) {
+        mbar_arrive(&empty[s]);  // the stage may be refilled
+        mbar_arrive(&rfull[b]);  // this warp's partial sums are in red[b]
+      }
     }
-    named_bar_sync(1, NW * 32);
-    if (*abort_flag) break;
+    if (cw == 0 && lane == 0) {
+      dbg_add(P, PHASE, 2, cwf);
+      dbg_add(P, PHASE, 3, cwr);
+      dbg_add(P, PHASE, 4, ccomp);
+    }
+    return;
+  }
 
-    // ------------------------------ epilogues ------------------------------
+  if (warp != NW + 1) return;
+  // ------------------------------- epilogue warp --------------------------------
+  int i = 0;
+  long long ew = 0, eb = 0, tprev = clk();
+  const long long tstart = tprev;
+  for (int t = blockIdx.x; t < nItems; t += gridDim.x, ++i) {
+    const int b = i % kRed;
+    const long long t0 = clk();
+    eb += t0 - tprev;
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&rfull[b], (i / kRed) & 1, P.limit_ns))) {
+      if (lane == 0) set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+      break;
+    }
+    tprev = clk();
+    ew += tprev - t0;
+    const RedMeta mt = rmeta[b];
+    const float* rb = red + (size_t)b * red_stride;
+    // partial sums of this item's chunk go to the workspace with plain stores;
+    // the finalize kernel adds the chunks in a fixed order
     if (PHASE == 0) {
-      if (cw == 0) {
-        const int p = H.p0;
-        const int row = p * 32 + lane;
-        if (nch == 1) {
-          for (int r = 0; r < H.R; ++r) {
-            float gs = 0.f, us = 0.f;
-            for (int gi = 0; gi < G; ++gi) {
-              gs += rb[(gi * kMaxM + r) * 32 + lane];
-              us += rb[((G + gi) * kMaxM + r) * 32 + lane];
-            }
-            hbuf[((int64_t)H.u * g.M + r) * g.I + row] = silu_f(gs) * us;
+      const bool half_act = s_ufmt[mt.u] == BQE_FMT_MXFP4 && P.variant == 1;
+      const float* xsc = (const float*)(P.ws + P.L.xsc);
+      float* pa = (float*)(P.ws + P.L.pa);
+      // W1 warps of panel pi are cw = pi*G + gi, W3 warps cw = (P + pi)*G + gi
+      for (int r = 0; r < mt.R; ++r) {
+        const float unscale = half_act ? xsc[s_urows[mt.u * kMaxM + r]] : 1.0f;  // 2^-s, exact
+        for (int pi = 0; pi < P_; ++pi) {
+          const int p = mt.p0 + pi;
+          const int64_t base = (((int64_t)mt.u * g.npanA + p) * nch + mt.c) * 2 * g.M;
+          float a0 = 0.f, a1 = 0.f;
+          for (int gi = 0; gi < G; ++gi) {
+            a0 += rb[((pi * G + gi) * g.M + r) * 32 + lane];
+            a1 += rb[(((P_ + pi) * G + gi) * g.M + r) * 32 + lane];
           }
-        } else {
-          float* pa = (float*)(P.ws + P.L.pa);
-          const int64_t base = (((int64_t)H.u * g.npanA + p) * nch + H.c) * 2 * g.M;
-          for (int r = 0; r < H.R; ++r) {
-            float gs = 0.f, us = 0.f;
-            for (int gi = 0; gi < G; ++gi) {
-              gs += rb[(gi * kMaxM + r) * 32 + lane];
-              us += rb[((G + gi) * kMaxM + r) * 32 + lane];
-            }
-            pa[(base + r) * 32 + lane] = gs;
-            pa[(base + g.M + r) * 32 + lane] = us;
-          }
-          __threadfence();
-          __syncwarp();
-          unsigned int old = 0;
-          unsigned int* ctr = (unsigned int*)(P.ws + P.L.ctrA) + H.u * g.npanA + p;
-          if (lane == 0) old = atomicAdd(ctr, 1u);
-          old = __shfl_sync(0xffffffffu, old, 0);
-          if (old == (unsigned int)(nch - 1)) {
-            __threadfence();
-            for (int r = 0; r < H.R; ++r) {
-              float gs = 0.f, us = 0.f;
-              for (int c = 0; c < nch; ++c) {
-                const int64_t b2 = (((int64_t)H.u * g.npanA + p) * nch + c) * 2 * g.M;
-                gs += __ldcg(pa + (b2 + r) * 32 + lane);
-                us += __ldcg(pa + (b2 + g.M + r) * 32 + lane);
-              }
-              hbuf[((int64_t)H.u * g.M + r) * g.I + row] = silu_f(gs) * us;
-            }
-            if (lane == 0) *ctr = 0u;
-          }
+          pa[(base + r) * 32 + lane] = a0 * unscale;
+          pa[(base + g.M + r) * 32 + lane] = a1 * unscale;
         }
       }
     } else {
-      if (cw < P_) {
-        const int p = H.p0 + cw;
-        const int n = p * 32 + lane;
-        float* pb = (float*)(P.ws + P.L.pb);
-        for (int r = 0; r < H.R; ++r) {
+      float* pb = (float*)(P.ws + P.L.pb);
+      for (int pi = 0; pi < P_; ++pi) {
+        const int n = (mt.p0 + pi) * 32 + lane;
+        for (int r = 0; r < mt.R; ++r) {
           float y = 0.f;
-          for (int gi = 0; gi < G; ++gi) y += rb[((cw * G + gi) * kMaxM + r) * 32 + lane];
-          pb[(((int64_t)H.u * nch + H.c) * g.M + r) * g.H + n] = y;
-        }
-        __threadfence();
-        __syncwarp();
-        unsigned int old = 0;
-        unsigned int* ctr = (unsigned int*)(P.ws + P.L.ctrB) + p;
-        if (lane == 0) old = atomicAdd(ctr, 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == (unsigned int)(nU * nch - 1)) {
-          __threadfence();
-          const int32_t* cu = (const int32_t*)(P.ws + P.L.comb_u);
-          const int32_t* cr = (const int32_t*)(P.ws + P.L.comb_r);
-          const float* cwt = (const float*)(P.ws + P.L.comb_w);
-          for (int m = 0; m < g.M; ++m) {
-            float ys = 0.f;
-            for (int c = 0; c < nch; ++c) ys += __ldcg(pb + (((int64_t)0 * nch + c) * g.M + m) * g.H + n);
-            float val = ys;
-            for (int j = 0; j < g.K; ++j) {
-              const int u = cu[m * g.K + j], r = cr[m * g.K + j];
-              float yj = 0.f;
-              for (int c = 0; c < nch; ++c) yj += __ldcg(pb + (((int64_t)u * nch + c) * g.M + r) * g.H + n);
-              val = fmaf(cwt[m * g.K + j], yj, val);
-            }
-            float* o = P.out + (int64_t)m * g.H + n;
-            *o = P.accumulate ? *o + val : val;
-          }
-          if (lane == 0) *ctr = 0u;
+          for (int gi = 0; gi < G; ++gi) y += rb[((pi * G + gi) * g.M + r) * 32 + lane];
+          pb[(((int64_t)mt.u * nch + mt.c) * g.M + r) * g.H + n] = y;
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rempty[b]);  // red[b] has been read
+  }
+  if (lane == 0) {
+    const long long tend = clk();
+    dbg_add(P, PHASE, 5, ew);
+    dbg_add(P, PHASE, 6, eb + (tend - tprev));
+    dbg_add(P, PHASE, 7, tend - tstart);
   }
 }
 
+// ---------------------------------------------------------------------------
+// finalize: add the chunk partials in chunk order
+//   phase A: h[u, r, i] = silu(sum_c g_c) * (sum_c u_c)
+//   phase B: out[m, n] (+)= y_shared[m, n] + sum_j w[m, j] y[u(m,j), r(m,j), n]
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_finalize_a(ExpParams P) {
+  const Geo& g = P.g;
+  griddep_wait();
+  const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
+  const int32_t* u_nrows = (const int32_t*)(P.ws + P.L.u_nrows);
+  const float* pa = (const float*)(P.ws + P.L.pa);
+  float* hbuf = (float*)(P.ws + P.L.h);
+  const int nch = g.nchA;
+  const int64_t n = (int64_t)nU * g.M * g.I;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
+    const int u = (int)(t / ((int64_t)g.M * g.I));
+    const int r = (int)((t / g.I) % g.M);
+    const int i = (int)(t % g.I);
+    if (r >= u_nrows[u]) continue;
+    const int p = i >> 5, lane = i & 31;
+    float a0 = 0.f, a1 = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      const int64_t base = (((int64_t)u * g.npanA + p) * nch + c) * 2 * g.M;
+      a0 += pa[(base + r) * 32 + lane];
+      a1 += pa[(base + g.M + r) * 32 + lane];
+    }
+    hbuf[((int64_t)u * g.M + r) * g.I + i] = silu_f(a0) * a1;
+  }
+}
+
+__global__ void __launch_bounds__(256) k_finalize_b(ExpParams P) {
+  const Geo& g = P.g;
+  griddep_wait();
+  const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
+  const float* pb = (const float*)(P.ws + P.L.pb);
+  const int32_t* cu = (const int32_t*)(P.ws + P.L.comb_u);
+  const int32_t* cr = (const int32_t*)(P.ws + P.L.comb_r);
+  const float* cwt = (const float*)(P.ws + P.L.comb_w);
+  const int nch = g.nchB;
+  if (nU == 0) return;  // the router reported an error; out is left untouched
+  const int64_t n = (int64_t)g.M * g.H;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
+    const int m = (int)(t / g.H), col = (int)(t % g.H);
+    float val = 0.f;
+    for (int c = 0; c < nch; ++c) val += pb[((int64_t)c * g.M + m) * g.H + col];  // shared expert, u = 0
+    for (int j = 0; j < g.K; ++j) {
+      const int u = cu[m * g.K + j], r = cr[m * g.K + j];
+      float yj = 0.f;
+      for (int c = 0; c < nch; ++c) yj += pb[(((int64_t)u * nch + c) * g.M + r) * g.H + col];
+      val = fmaf(cwt[m * g.K + j], yj, val);
+    }
+    float* o = P.out + t;
+    *o = P.accumulate ? *o + val : val;
+  }
+}
+
+int launch_finalize(const ExpParams& P, int phase, int sms, cudaStream_t st, bool pdl) {
+  const int64_t n = phase == 0 ? (int64_t)P.g.U * P.g.M * P.g.I : (int64_t)P.g.M * P.g.H;
+  int grid = (int)((n + 255) / 256);
+  if (grid > 2 * sms) grid = 2 * sms;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = phase == 0 ? cudaLaunchKernelEx(&cfg, k_finalize_a, P) : cudaLaunchKernelEx(&cfg, k_finalize_b, P);
+  return e == cudaSuccess ? BQE_OK : BQE_ECUDA;
+}
+
 uint32_t experts_smem_bytes(const Geo& g, int phase, int* nstages_out) {
-  const uint32_t base = 2048 + 2 * kMaxWarps * kMaxM * 32 * 4;
+  const uint32_t base = kEngineBase + red_bytes_for(phase_warps(g, phase), g.M);
   const uint32_t slot = stage_slot_bytes(g, phase);
-  const uint32_t budget = 220 * 1024;
-  int ns = (int)((budget - base) / slot);
+  int ns = (int)((kSmemBudget - base) / slot);
   if (ns > 8) ns = 8;
   if (nstages_out) *nstages_out = ns;
   return base + (uint32_t)ns * slot;
@@ -532,12 +725,26 @@ int launch_experts(const ExpParams& P, int phase, int grid, cudaStream_t st, boo
   int ns = 0;
   const uint32_t smem = experts_smem_bytes(P.g, phase, &ns);
   if (ns < 2) return BQE_EUNSUPPORTED;
-  const void* fn = phase == 0 ? (const void*)k_experts<0> : (const void*)k_experts<1>;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return BQE_ECUDA;
+  // raise the kernel's dynamic shared memory limit once per device (the call is slow)
+  static int limit_set[2][64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BQE_ECUDA;
+  if (limit_set[phase][dev] < (int)smem) {
+    const void* fn = phase == 0 ? (const void*)k_experts<0> : (const void*)k_experts<1>;
+    int optin = 0;
+    cudaFuncAttributes fa;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, fn) != cudaSuccess)
+      return BQE_ECUDA;
+    const int dyn_max = optin - (int)fa.sharedSizeBytes;  // dynamic + static must fit the opt-in limit
+    if (dyn_max < (int)smem) return BQE_EUNSUPPORTED;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max) != cudaSuccess)
+      return BQE_ECUDA;
+    limit_set[phase][dev] = dyn_max;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(32 * (1 + phase_warps(P.g, phase)));
+  cfg.blockDim = dim3(32 * (2 + phase_warps(P.g, phase)));  // producer + consumers + epilogue
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute at[1];

@@ -76,15 +76,41 @@ __host__ __device__ inline uint32_t tile_byte_offset(int f, int nb, int b, int r
 // Decode-call geometry shared by host and kernels.
 // ----------------------------------------------------------------------------
 constexpr int kMaxM = 8;          // rows per decode call
-constexpr int kMaxWarps = 8;      // consumer warps per CTA
+constexpr int kMaxWarps = 16;     // consumer warps per CTA
 constexpr int kMaxTopK = 16;
+constexpr int kRowChunk = 4;      // rows accumulated together (larger row sets are done in chunks)
+constexpr int kRed = 2;           // reduction buffers between consumers and the epilogue warp
+constexpr uint32_t kSmemBudget = 220 * 1024;
+constexpr uint32_t kEngineBase = 2048;  // headers and mbarriers in front of the reduction buffers
+constexpr int kFmtMaxBytesPerCol = 17;  // MXFP4 tile: 17 bytes per column per 32 rows (largest format)
 
 struct Geo {
   int H, I, E, K, M;
-  int U;          // max distinct experts incl. the shared one = M*K + 1 (<= E+1)
-  int kcA, nchA, GA, npanA;  // W1/W3: K = H
-  int kcB, nchB, GB, npanB, PB;  // W2: K = I; PB panels per item
+  int U;                          // max distinct experts incl. the shared one = M*K + 1 (<= E+1)
+  int kcA, nchA, GA, npanA, PA;   // W1/W3: K = H; PA panels of 32 rows per work item
+  int kcB, nchB, GB, npanB, PB;   // W2: K = I; PB panels per work item
 };
+
+// Bytes of one ring stage: P panels of `mats` matrices (largest format) plus
+// the activation chunk of M rows (fp32, the larger of the two encodings).
+__host__ __device__ inline uint32_t stage_bytes_for(int mats, int P, int kc, int M) {
+  const uint32_t w = (uint32_t)mats * P * kFmtMaxBytesPerCol * kc;
+  return ((w + (uint32_t)M * kc * 4u) + 127u) & ~127u;
+}
+__host__ __device__ inline uint32_t red_bytes_for(int nw, int M) {
+  return ((uint32_t)kRed * nw * M * 32 * 4 + 127u) & ~127u;
+}
+// Largest P (panels per item) with mats*P*G consumer warps <= kMaxWarps,
+// P dividing the panel count and at least two stages fitting the budget.
+__host__ __device__ inline int pick_panels(int mats, int G, int npan, int kc, int M) {
+  int best = 1;
+  for (int P = 1; P * mats * G <= kMaxWarps; ++P) {
+    if (npan % P) continue;
+    const uint32_t need = kEngineBase + red_bytes_for(mats * P * G, M) + 2 * stage_bytes_for(mats, P, kc, M);
+    if (need <= kSmemBudget) best = P;
+  }
+  return best;
+}
 
 __host__ __device__ inline Geo make_geo(int H, int I, int E, int K, int M) {
   Geo g;
@@ -93,18 +119,18 @@ __host__ __device__ inline Geo make_geo(int H, int I, int E, int K, int M) {
   if (g.U > E + 1) g.U = E + 1;
   g.kcA = chunk_cols(H); g.nchA = H / g.kcA; g.GA = g.kcA / 256; g.npanA = I / 32;
   g.kcB = chunk_cols(I); g.nchB = I / g.kcB; g.GB = g.kcB / 256; g.npanB = H / 32;
-  int pb = kMaxWarps / g.GB;
-  if (pb < 1) pb = 1;
-  while (pb > 1 && (g.npanB % pb) != 0) --pb;
-  g.PB = pb;
+  g.PA = pick_panels(2, g.GA, g.npanA, g.kcA, M);
+  g.PB = pick_panels(1, g.GB, g.npanB, g.kcB, M);
   return g;
 }
 
 // Workspace layout (offsets in bytes, each 256-aligned).
 struct WsLayout {
   uint64_t err, ctr_route, nu, u_slot, u_fmt, u_addr, u_nrows, u_rows;
-  uint64_t comb_u, comb_r, comb_w, z, xf, pa, ctrA, h, pb, ctrB, total;
+  uint64_t comb_u, comb_r, comb_w, z, xf, xh, xsc, pa, h, pb, dbg, total;
 };
+constexpr int kDbgSlots = 8;      // per-CTA cycle counters of the diagnostic mode
+constexpr int kDbgMaxCtas = 1024;
 
 __host__ __device__ inline uint64_t al256(uint64_t x) { return (x + 255) & ~(uint64_t)255; }
 
@@ -124,11 +150,12 @@ __host__ __device__ inline WsLayout make_ws(const Geo& g) {
   w.comb_w = o; o = al256(o + 4ull * g.M * g.K);
   w.z = o; o = al256(o + 4ull * g.M * g.E);
   w.xf = o; o = al256(o + 4ull * g.M * g.H);
+  w.xh = o; o = al256(o + 2ull * g.M * g.H);   // f16(x * 2^s_m): exact, per-row power-of-two scale
+  w.xsc = o; o = al256(o + 4ull * kMaxM);      // 2^-s_m
   w.pa = o; o = al256(o + 4ull * g.U * g.npanA * g.nchA * 2 * g.M * 32);
-  w.ctrA = o; o = al256(o + 4ull * g.U * g.npanA);
   w.h = o; o = al256(o + 4ull * g.U * g.M * g.I);
   w.pb = o; o = al256(o + 4ull * g.U * g.nchB * g.M * g.H);
-  w.ctrB = o; o = al256(o + 4ull * g.npanB);
+  w.dbg = o; o = al256(o + 8ull * 2 * kDbgMaxCtas * kDbgSlots);  // [phase][cta][slot] cycles
   w.total = o;
   return w;
 }
@@ -158,12 +185,16 @@ struct ExpParams {
   float* out;
   int accumulate;
   int nstages;        // ring depth (<= 16), chosen by the host from the smem budget
+  int drop_item;      // test hook: CTA 0's producer never issues its item number drop_item (-1: off)
+  int variant;        // inner-loop variant for MXFP4 in phase A (0: f32 FMA, 1: f16-input FMA)
+  int diag;           // 1: accumulate per-CTA cycle counters into ws.dbg
   uint64_t limit_ns;  // bound on every mbarrier wait
 };
 
 // Launchers (one per translation unit that owns the kernel).
 int launch_route(const RouteParams& P, cudaStream_t st, bool pdl);
 int launch_experts(const ExpParams& P, int phase, int grid, cudaStream_t st, bool pdl);
+int launch_finalize(const ExpParams& P, int phase, int sms, cudaStream_t st, bool pdl);
 uint32_t experts_smem_bytes(const Geo& g, int phase, int* nstages_out);
 
 // Error detail codes written to ws.err[1].
@@ -230,6 +261,17 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Named barrier that also ORs a predicate over the participating threads:
+// every participant gets the same answer.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %3, 0; bar.red.or.pred q, %1, %2, p; selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"(id), "r"(nthreads), "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
 }
 
 __device__ __forceinline__ void set_error(int32_t* err, int code, int detail) {

@@ -16,6 +16,7 @@
 // one quarter of hidden each, all loads in flight at once); the last CTA to
 // finish (arrival counter, no waiting) selects, weighs and builds the list.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "bqe_internal.cuh"
 
@@ -27,21 +28,42 @@ constexpr int kMaxE = 512;  // routed experts per layer supported by the selecti
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
+constexpr int kRouteMaxNI = 16;  // float4 router loads per lane: hidden / 512 (hidden <= 8192)
+
+// One instance per row count MR (= M) keeps each instance's code short: a
+// decode call runs this kernel once, so every instruction is fetched cold.
+template <int MR>
 __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
   const Geo& g = P.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = g.H, E = g.E, M = g.M, K = g.K;
+  const int H = g.H, E = g.E, K = g.K;
+  constexpr int M = MR;
   int32_t* err = (int32_t*)(P.ws + P.L.err);
   float* z = (float*)(P.ws + P.L.z);
   float* xf = (float*)(P.ws + P.L.xf);
+  extern __shared__ __align__(16) uint16_t xs[];  // M x H bf16 layer input
 
   __shared__ float inv_rms[kMaxM];
   __shared__ float red[8][kMaxM];
   __shared__ int s_last;
 
-  griddep_wait();  // inputs may come from the previous layer's kernels
+  // warp = (expert 2*blockIdx + warp/4, quarter warp%4); every router load of
+  // the lane is issued before anything waits
+  const int e = blockIdx.x * 2 + (warp >> 2);
+  const int q = warp & 3;
+  const int Kq = H / 4;
+  const int ni = Kq / 128;
+  float4 w4[kRouteMaxNI];
+  if (e < E) {
+    const float4* wr = (const float4*)(P.router_w + (int64_t)e * H + (int64_t)q * Kq);
+#pragma unroll
+    for (int i = 0; i < kRouteMaxNI; ++i)
+      if (i < ni) w4[i] = __ldg(wr + i * 32 + lane);
+  }
 
-  // ---- layer input: bf16 x, or bf16(rmsnorm(resid)) --------------------------
+  griddep_wait();  // the layer input may come from the previous kernels
+
+  // ---- layer input into shared memory: bf16 x, or bf16(rmsnorm(resid)) -------
   if (P.resid) {
     for (int m = 0; m < M; ++m) {
       float ss = 0.f;
@@ -59,55 +81,72 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
       inv_rms[tid] = 1.0f / sqrtf(ss / (float)H + 1e-6f);
     }
     __syncthreads();
-  }
-  auto xval = [&](int m, int k) -> float {
-    if (P.resid) {
-      __nv_bfloat16 t = __float2bfloat16_rn(P.resid[(int64_t)m * H + k] * inv_rms[m]);
-      return __bfloat162float(t);
+    for (int i = tid; i < M * H; i += kRouteThreads) {
+      const int m = i / H;
+      const __nv_bfloat16 t = __float2bfloat16_rn(P.resid[i] * inv_rms[m]);
+      xs[i] = __bfloat16_as_ushort(t);
     }
-    return bf16_to_f32(P.x[(int64_t)m * H + k]);
-  };
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(P.x);
+    uint4* dst = reinterpret_cast<uint4*>(xs);
+    for (int i = tid; i < M * H / 8; i += kRouteThreads) dst[i] = src[i];
+  }
+  __syncthreads();
 
-  // ---- side job: fp32 copy of the layer input for the expert kernels --------
+  // ---- side job: fp32 and scaled-f16 copies of the layer input --------------
+  // f16(x * 2^s) is exact for a bf16 x as long as x * 2^s is a normal f16;
+  // s puts the row's largest |x| in [2^14, 2^15).  Every CTA derives the same s.
+  __shared__ int s_emax[kMaxM];
+  if (tid < M) s_emax[tid] = -1000;
+  __syncthreads();
+  for (int m = 0; m < M; ++m) {
+    uint32_t mx = 0;
+    for (int k = tid; k < H; k += kRouteThreads) mx = max(mx, (uint32_t)(xs[m * H + k] & 0x7FFFu));
+    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0 && mx) atomicMax(&s_emax[m], (int)(mx >> 7) - 127);  // floor(log2 max|x|)
+  }
+  __syncthreads();
   {
-    const int64_t n = (int64_t)M * H;
-    const int64_t per = (n + gridDim.x - 1) / gridDim.x;
-    const int64_t lo = per * blockIdx.x, hi = min(n, lo + per);
-    for (int64_t i = lo + tid; i < hi; i += kRouteThreads) {
-      const int m = (int)(i / H), k = (int)(i % H);
-      float v = xval(m, k);
+    uint16_t* xh = (uint16_t*)(P.ws + P.L.xh);
+    const int n = M * H;
+    const int per = (n + gridDim.x - 1) / gridDim.x;
+    const int lo = per * blockIdx.x, hi = min(n, lo + per);
+    for (int i = lo + tid; i < hi; i += kRouteThreads) {
+      const float v = bf16_to_f32(xs[i]);
+      const int m = i / H;
+      const int sh = s_emax[m] == -1000 ? 0 : 14 - s_emax[m];
       xf[i] = v;
-      if (P.t_out) P.t_out[i] = (uint16_t)(__float_as_uint(v) >> 16);
+      xh[i] = __half_as_ushort(__float2half_rn(ldexpf(v, sh)));
+      if (P.t_out) P.t_out[i] = xs[i];
+    }
+    if (blockIdx.x == 0 && tid < M) {
+      const int sh = s_emax[tid] == -1000 ? 0 : 14 - s_emax[tid];
+      ((float*)(P.ws + P.L.xsc))[tid] = ldexpf(1.0f, -sh);
     }
   }
 
-  // ---- router GEMV: warp = (expert 2*blockIdx + warp/4, quarter warp%4) ------
-  const int e = blockIdx.x * 2 + (warp >> 2);
-  const int q = warp & 3;
-  const int Kq = H / 4;
-  float acc[kMaxM];
+  // ---- router GEMV ----------------------------------------------------------
+  float acc[M];
 #pragma unroll
-  for (int m = 0; m < kMaxM; ++m) acc[m] = 0.f;
+  for (int m = 0; m < M; ++m) acc[m] = 0.f;
   if (e < E) {
-    const float4* wr = (const float4*)(P.router_w + (int64_t)e * H + (int64_t)q * Kq);
-    const int n4 = Kq / 4;
-#pragma unroll 10
-    for (int i = lane; i < n4; i += 32) {
-      const float4 w4 = __ldg(wr + i);
-      const int k = q * Kq + i * 4;
 #pragma unroll
-      for (int m = 0; m < kMaxM; ++m) {
-        if (m < M) {
-          acc[m] = fmaf(w4.x, xval(m, k + 0), acc[m]);
-          acc[m] = fmaf(w4.y, xval(m, k + 1), acc[m]);
-          acc[m] = fmaf(w4.z, xval(m, k + 2), acc[m]);
-          acc[m] = fmaf(w4.w, xval(m, k + 3), acc[m]);
+    for (int i = 0; i < kRouteMaxNI; ++i) {
+      if (i < ni) {
+        const int k = q * Kq + (i * 32 + lane) * 4;
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          const uint2 xv = *reinterpret_cast<const uint2*>(xs + m * H + k);
+          acc[m] = fmaf(w4[i].x, __uint_as_float(xv.x << 16), acc[m]);
+          acc[m] = fmaf(w4[i].y, __uint_as_float(xv.x & 0xFFFF0000u), acc[m]);
+          acc[m] = fmaf(w4[i].z, __uint_as_float(xv.y << 16), acc[m]);
+          acc[m] = fmaf(w4[i].w, __uint_as_float(xv.y & 0xFFFF0000u), acc[m]);
         }
       }
     }
   }
 #pragma unroll
-  for (int m = 0; m < kMaxM; ++m) {
+  for (int m = 0; m < M; ++m) {
     float v = acc[m];
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     acc[m] = v;
@@ -119,8 +158,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
   if (tid < 2 * M) {
     const int el = tid / M, m = tid % M, ee = blockIdx.x * 2 + el;
     if (ee < E) {
-      float s = red[el * 4 + 0][m] + red[el * 4 + 1][m] + red[el * 4 + 2][m] + red[el * 4 + 3][m];
-      z[(int64_t)m * E + ee] = s;
+      float sum = red[el * 4 + 0][m] + red[el * 4 + 1][m] + red[el * 4 + 2][m] + red[el * 4 + 3][m];
+      z[(int64_t)m * E + ee] = sum;
     }
   }
 
@@ -190,15 +229,23 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
     }
     __syncwarp();
     if (lane == 0) {
-      // mixing weights from the unbiased scores of the selected experts
-      float sc[kMaxTopK];
+      // mixing weights w_j = s_j / sum s from the unbiased scores, evaluated as
+      // exp(log s_j - max log s) / sum exp(...): the same ratio, but it stays
+      // finite when every selected sigmoid underflows in fp32
+      float ls[kMaxTopK];
+      float mx = -INFINITY;
+      for (int j = 0; j < K; ++j) {
+        const float zz = __ldcg(z + (int64_t)m * E + s_idx[m][j]);
+        ls[j] = zz < 0.f ? zz - log1pf(expf(zz)) : -log1pf(expf(-zz));  // log sigmoid(z)
+        mx = fmaxf(mx, ls[j]);
+      }
       float tot = 0.f;
       for (int j = 0; j < K; ++j) {
-        sc[j] = 1.0f / (1.0f + expf(-__ldcg(z + (int64_t)m * E + s_idx[m][j])));
-        tot += sc[j];
+        ls[j] = expf(ls[j] - mx);
+        tot += ls[j];
       }
       for (int j = 0; j < K; ++j) {
-        const float w = sc[j] / tot;
+        const float w = ls[j] / tot;
         ((float*)(P.ws + P.L.comb_w))[m * K + j] = w;
         if (P.topk_idx) P.topk_idx[m * K + j] = s_idx[m][j];
         if (P.topk_w) P.topk_w[m * K + j] = w;
@@ -283,17 +330,31 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
 
 int launch_route(const RouteParams& P, cudaStream_t st, bool pdl) {
   const int grid = (P.g.E + 1) / 2;
+  const size_t smem = (size_t)P.g.M * P.g.H * 2;
+  if (P.g.H / 4 / 128 > kRouteMaxNI || P.g.H % 512) return BQE_EUNSUPPORTED;
+  static int limit_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BQE_ECUDA;
+  void (*fns[kMaxM])(RouteParams) = {k_route<1>, k_route<2>, k_route<3>, k_route<4>,
+                                     k_route<5>, k_route<6>, k_route<7>, k_route<8>};
+  auto fn = fns[P.g.M - 1];
+  if (smem > 48 * 1024 && limit_set[dev] < (int)smem) {
+    for (int m = 0; m < kMaxM; ++m)
+      if (cudaFuncSetAttribute(fns[m], cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
+        return BQE_ECUDA;
+    limit_set[dev] = 200 * 1024;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kRouteThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_route, P) == cudaSuccess ? BQE_OK : BQE_ECUDA;
+  return cudaLaunchKernelEx(&cfg, fn, P) == cudaSuccess ? BQE_OK : BQE_ECUDA;
 }
 
 }  // namespace bqe

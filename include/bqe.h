@@ -168,6 +168,12 @@ int bqe_route(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float
 int bqe_experts(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out,
                 int32_t accumulate, void* ws, uint64_t ws_bytes, void* stream);
 
+/* One phase of bqe_experts alone (phase 0: W1/W3 GEMV + SiLU-GLU into the
+ * workspace; phase 1: W2 GEMV + combine into out), so each kernel can be
+ * timed on its own.  bqe_experts == phase 0 then phase 1. */
+int bqe_experts_phase(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out,
+                      int32_t accumulate, int32_t phase, void* ws, uint64_t ws_bytes, void* stream);
+
 /* Chained decode step over n_layers layers: r_0 = resid (in place),
  * t_l = bf16(r_l / sqrt(mean(r_l^2) + 1e-6)), r_{l+1} = r_l + MoE_l(t_l).
  *   resid       device, M x hidden fp32, updated in place
@@ -201,6 +207,27 @@ void bqe_set_wait_limit_ns(uint64_t ns);
 /* Chain the kernels of a call with programmatic dependent launch (default
  * on).  Off: plain stream order. */
 void bqe_set_pdl(int on);
+
+/* Test hook for the timeout path, injected from the host: while item >= 0,
+ * the first CTA of each expert kernel never issues the copies of its work
+ * item number `item`, so the consumers' wait for that stage runs out of its
+ * limit and the call reports BQE_ETIMEOUT.  -1 (default) turns it off. */
+void bqe_set_test_drop_item(int32_t item);
+
+/* Inner-loop variant of the MXFP4 W1/W3 kernel (default 1): 0 converts
+ * weights to fp32 and uses packed fp32 FMAs; 1 keeps weights and the
+ * activations (scaled by a power of two per row, exact) in f16 and
+ * accumulates with fp32-accumulating mixed-precision FMAs.  Both give the
+ * same products; only the summation order differs. */
+void bqe_set_variant(int32_t v);
+
+/* Diagnostic mode (default off): the expert kernels add per-CTA clock64()
+ * cycle counts (producer waiting / issuing, consumer waiting for a stage /
+ * for a reduction buffer / computing, epilogue waiting / working, whole CTA)
+ * into the workspace at byte offset bqe_diag_offset(d, M): uint64
+ * [2 phases][1024 CTAs][8 counters], zeroed by bqe_workspace_init. */
+void bqe_set_diag(int32_t on);
+uint64_t bqe_diag_offset(const bqe_layer_desc* d, int32_t M);
 
 #ifdef __cplusplus
 }

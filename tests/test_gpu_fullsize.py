@@ -1,0 +1,118 @@
+"""GPU parity at the full DeepSeek-V4.1-Flash layer sizes (hidden 5120,
+inter 2304, 384 routed + 1 shared, top-6), in the launch configuration the
+benchmark times, on sampled outputs the oracle computes one by one."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import moe as O
+
+from gpu_util import check_out, check_routing, oracle_layer_sampled
+
+pytestmark = pytest.mark.gpu
+
+H, I, E, K = 5120, 2304, 384, 6
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+    from bit_quantised_expert_gb300 import buildlib
+    buildlib.build()
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")
+
+
+def _run_layer(W, dev, xi, M):
+    import torch
+    from bit_quantised_expert_gb300 import _abi as A
+    nb = A.bqe_workspace_bytes(W.d, M)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    A.bqe_workspace_init(ws, nb)
+    out = torch.zeros(M, H, device=dev)
+    idx = torch.zeros(M, K, dtype=torch.int32, device=dev)
+    wts = torch.zeros(M, K, dtype=torch.float32, device=dev)
+    x = W.xs[xi]
+    A.bqe_moe_layer_forward(W.d, M, x, W.wr, W.bias, W.pool.cstruct(), W.table, None, out, 0, idx, wts, ws, nb)
+    rc, det = A.bqe_check(ws)
+    assert rc == A.BQE_OK, (A.status_name(rc), det)
+    x_bits = x.cpu().numpy().view(np.uint16)
+    return out.double().cpu().numpy(), idx.cpu().numpy(), wts.cpu().numpy(), x_bits
+
+
+def _check_layer(W, dev, M, xi, ncols=48):
+    out, idx, wts, x_bits = _run_layer(W, dev, xi, M)
+    router = W.wr.cpu().numpy()
+    bias = None if W.bias is None else W.bias.cpu().numpy()
+    ref = O.route(O.bf16_bits_to_f64(x_bits), router, bias, K)
+    check_routing(ref, idx, wts)
+    cols = np.random.default_rng(xi).choice(H, ncols, replace=False)
+    cache = {}
+
+    def canon(e):
+        if e not in cache:
+            cache[e] = W.canon(e).cpu().numpy()
+        return cache[e]
+    oref, r2 = oracle_layer_sampled(W.fmts, canon, x_bits, router, bias, idx, H, I, E, K, cols)
+    assert np.allclose(wts, r2["w"], rtol=2e-6, atol=0)
+    return check_out(out[:, cols], oref, what="full M=%d" % M)
+
+
+def test_fp4_layer_m1(dev):
+    from synth import workloads as WL
+    W = WL.fp4_layer(dev, m=1, n_x=3)
+    for xi in range(2):
+        _check_layer(W, dev, 1, xi)
+
+
+@pytest.mark.parametrize("M", [1, 6, 8])
+def test_mixed_layer(dev, M):
+    from synth import workloads as WL
+    W = WL.mixed_layer(dev, m=M, n_x=2)
+    _check_layer(W, dev, M, 0, ncols=24 if M > 1 else 48)
+
+
+def test_step40_teacher_forced(dev):
+    """40 chained layers over the 4288-slot pool (Zipf-forced routing): the
+    whole step equals the layer-by-layer run bit for bit, each layer's input
+    is the bf16 RMS-normalised residual, and sampled layers match the oracle
+    when fed the GPU's own layer inputs (teacher forcing)."""
+    import torch
+    from bit_quantised_expert_gb300 import _abi as A
+    from synth import workloads as WL
+    M = 1
+    S = WL.Step40(dev, m=M, n_steps_forced=1)
+    L = S.n_layers
+    nb = A.bqe_workspace_bytes(S.d, M)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    A.bqe_workspace_init(ws, nb)
+    pool = S.pool.cstruct()
+    forced = S.forced[0].contiguous()                       # (L, M, K)
+    t_all = torch.zeros(L, M, H, dtype=torch.int16, device=dev)
+    resid = S.x0[0].clone()
+    snaps = [resid.double().cpu().numpy()]
+    EH = E * H
+    for l in range(L):
+        A.bqe_moe_step(S.d, 1, M, resid, S.wr[l], None, pool, S.tables[l], forced[l], t_all[l], ws, nb)
+        snaps.append(resid.double().cpu().numpy())
+    rc, det = A.bqe_check(ws)
+    assert rc == A.BQE_OK, (A.status_name(rc), det)
+    whole = S.x0[0].clone()
+    A.bqe_moe_step(S.d, L, M, whole, S.wr, None, pool, S.tables, forced, None, ws, nb)
+    assert A.bqe_check(ws)[0] == A.BQE_OK
+    assert np.array_equal(whole.double().cpu().numpy(), snaps[-1])
+    t_np = t_all.cpu().numpy().view(np.uint16)
+    # layer inputs: bf16(rmsnorm(r_l)), within one bf16 step of the fp64 statement
+    for l in range(L):
+        want = O.rmsnorm_to_bf16(snaps[l])
+        diff = np.abs(t_np[l].astype(np.int64) - want.astype(np.int64))
+        assert diff.max() <= 1 and (diff > 0).mean() < 0.01, l
+    router_all = S.wr.cpu().numpy()
+    for l in (0, 17, 39):
+        table = S.tables_np[l]
+        fm = np.array([S.fmts[table[e]] for e in range(E + 1)], dtype=np.int32)
+        cols = np.random.default_rng(l).choice(H, 32, replace=False)
+        oref, _ = oracle_layer_sampled(fm, lambda e: S.canon(int(table[e])).cpu().numpy(), t_np[l], router_all[l],
+                                       None, S.forced_np[0, l], H, I, E, K, cols)
+        got = (snaps[l + 1] - snaps[l])[:, cols]
+        check_out(got, oref, rel=1e-4, what="layer %d" % l)
