@@ -235,8 +235,17 @@ def run_layer(args, rank, world):
     xbuf = torch.empty_like(W.xs[0])
     xs = [W.xs[i] for i in range(n_x)]
 
+    def fused(inst, ev=None):
+        # the production call (the layer entry point), on the current stream
+        if ev:
+            ev[0].record()
+        A.bqe_moe_layer_forward(d, M, xbuf, W.wr[inst], None if W.bias is None else W.bias[inst], pool,
+                                W.tables[inst], None, out, 0, idx_tmp, None, ws, nb)
+        if ev:
+            ev[1].record()
+
     def layer(inst, ev=None):
-        # one decode layer: router + top-k, phase A, phase B (current stream)
+        # the same layer as separate kernels: router + top-k, phase A, phase B
         if ev:
             ev[0].record()
         A.bqe_route(d, M, xbuf, W.wr[inst], None if W.bias is None else W.bias[inst], pool, W.tables[inst], None,
@@ -262,11 +271,13 @@ def run_layer(args, rank, world):
     # weights together are several times L2, so every step streams cold
     # weights.  Timing events are nodes inside the graph.
     gev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-    graphs = []
+    fev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+    graphs, fgraphs = [], []
     side = torch.cuda.Stream()
     side.wait_stream(st)
     with torch.cuda.stream(side):
         layer(0)
+        fused(0)
     st.wait_stream(side)
     torch.cuda.synchronize()
     for inst in range(NL):
@@ -274,6 +285,10 @@ def run_layer(args, rank, world):
         with torch.cuda.graph(g):
             layer(inst, gev)
         graphs.append(g)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fused(inst, fev)
+        fgraphs.append(g)
     torch.cuda.synchronize()
 
     clocks = ClockSampler(torch.cuda.current_device(), enabled=not args.no_clocks)
@@ -281,26 +296,33 @@ def run_layer(args, rank, world):
     i = 0
     while time.time() < t_end:  # untimed load so the clock samples see the GPU busy
         xbuf.copy_(xs[i % n_x])
-        graphs[i % NL].replay()
+        fgraphs[i % NL].replay()
         i += 1
         if i % 64 == 0:
             torch.cuda.synchronize()
     torch.cuda.synchronize()
-    t_route, t_a, t_b, t_layer = [], [], [], []
+    t_route, t_a, t_b, t_split, t_layer = [], [], [], [], []
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for s_ in range(steps):
         xbuf.copy_(xs[s_ % n_x])
-        graphs[s_ % NL].replay()
+        fgraphs[s_ % NL].replay()
         idx_log[s_].copy_(idx_tmp)
+        fev[1].synchronize()
+        t_layer.append(fev[0].elapsed_time(fev[1]) * 1e-3)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    # the same steps as separate kernels, for the per-kernel breakdown
+    for s_ in range(steps):
+        xbuf.copy_(xs[s_ % n_x])
+        graphs[s_ % NL].replay()
         gev[3].synchronize()
         t_route.append(gev[0].elapsed_time(gev[1]) * 1e-3)
         t_a.append(gev[1].elapsed_time(gev[2]) * 1e-3)
         t_b.append(gev[2].elapsed_time(gev[3]) * 1e-3)
-        t_layer.append(gev[0].elapsed_time(gev[3]) * 1e-3)
+        t_split.append(gev[0].elapsed_time(gev[3]) * 1e-3)
     torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
     barrier(world)
     clk = clocks.stop()
     rc, det = A.bqe_check(ws)
@@ -323,6 +345,8 @@ def run_layer(args, rank, world):
     hbm, hbm_kind = peaks()
     mean = lambda v: sum(v) / len(v)  # noqa: E731
     achieved_a = mean(bytes_a) / mean(t_a) / 1e9
+    router_bytes = W.E * 5120 * 4
+    achieved_l = (mean(bytes_e) + router_bytes) / mean(t_layer) / 1e9
     l2mb = torch.cuda.get_device_properties(0).L2_cache_size / 2 ** 20
     res = dict(
         metric=METRIC, value=round(value, 2), unit="GB/s", n_gpus=world, steps=steps, warmup=warm,
@@ -339,35 +363,70 @@ def run_layer(args, rank, world):
         tokens_per_s=round(M * steps * world / T_max, 1),
         frac_of_hbm=round(value / hbm, 4), hbm_peak_gbs=hbm, hbm_peak_kind=hbm_kind,
         expert_bytes_per_step=round(mean(bytes_e)),
-        kernels_us=dict(route=round(mean(t_route) * 1e6, 3), phase_a=round(mean(t_a) * 1e6, 3),
-                        phase_b=round(mean(t_b) * 1e6, 3)),
         roofline=dict(bound="hbm", achieved=round(achieved_a, 1), peak=hbm, unit="GB/s",
                       frac=round(achieved_a / hbm, 4), traffic=None,
-                      kernel="k_experts<0> (W1/W3 dequant-GEMV + SiLU-GLU)",
+                      kernel="k_experts<0> + finalize (W1/W3 dequant-GEMV + SiLU-GLU)",
                       algorithmic_bytes_per_launch=round(mean(bytes_a)),
                       peak_kind="%s hbm_gbs (burst copy)" % hbm_kind,
-                      phase_b=dict(achieved=round(mean(bytes_b) / mean(t_b) / 1e9, 1),
-                                   frac=round(mean(bytes_b) / mean(t_b) / 1e9 / hbm, 4))),
-        gpu_launches=3 * steps,
+                      layer_achieved=round(achieved_l, 1), layer_frac=round(achieved_l / hbm, 4),
+                      layer_note="all bytes of the call (experts + router) / layer time"),
+        split_kernels=dict(
+            note="the same layer as separate kernels (router, W1/W3 + finalize, W2 + finalize)",
+            us_per_layer=round(mean(t_split) * 1e6, 3),
+            route_us=round(mean(t_route) * 1e6, 3), phase_a_us=round(mean(t_a) * 1e6, 3),
+            phase_b_us=round(mean(t_b) * 1e6, 3),
+            phase_a_gbs=round(achieved_a, 1), phase_b_gbs=round(mean(bytes_b) / mean(t_b) / 1e9, 1)),
+        gpu_launches=steps,
         variant=args.variant,
-        timing="CUDA-graph replay per step, kernel split from event nodes inside the graph",
+        timing="CUDA-graph replay per step, events as graph nodes around the layer kernel",
         wall_s_timed_loop=round(wall, 4),
     )
     if clk:
         res["clocks"] = clk
 
     if args.diag:
+        # timeline of the fused kernel (globaltimer stamps per CTA)
+        A.bqe_set_diag(True)
+        off = A.bqe_diag_offset(d, M)
+        tl = []
+        for s_ in range(10):
+            A.bqe_workspace_init(ws, nb)
+            dv = ws[off:off + 8 * 3 * 1024 * 8].view(torch.int64).view(3, 1024, 8)
+            dv[0, 1023, 0] = 2 ** 62
+            xbuf.copy_(xs[s_ % n_x])
+            fused(s_ % NL)
+            torch.cuda.synchronize()
+            a = dv[0].cpu().numpy().astype(np.float64)
+            t0 = a[1023, 0]
+            sms = torch.cuda.get_device_properties(0).multi_processor_count
+            rel = (a[:sms, :7] - t0) / 1e3
+            tl.append([[float(rel[:, k].min()), float(rel[:, k].mean()), float(rel[:, k].max())] for k in range(7)])
+        A.bqe_set_diag(False)
+        A.bqe_workspace_init(ws, nb)
+        tl = np.array(tl).mean(axis=0)
+        names = ["router_done", "logits_seen", "worklist_built", "consumers_done", "epilogue_done",
+                 "producer_done", "end"]
+        sys.stderr.write("FUSED_TIMELINE_us(min,mean,max) " + json.dumps(
+            {n: [round(v, 2) for v in tl[k]] for k, n in enumerate(names)}) + "\n")
+
+    if args.diag:
         # per-CTA cycle accounting (a separate, untimed pass)
         A.bqe_set_diag(True)
-        A.bqe_workspace_init(ws, nb)
-        nd = 20
-        for s_ in range(nd):
-            xbuf.copy_(xs[s_ % n_x])
-            layer(s_ % NL)
-        torch.cuda.synchronize()
-        A.bqe_set_diag(False)
         off = A.bqe_diag_offset(d, M)
-        dbg = ws[off:off + 8 * 2 * 1024 * 8].view(torch.int64).view(2, 1024, 8).cpu().numpy()
+        nd = 20
+        spans = []
+        for s_ in range(nd):
+            A.bqe_workspace_init(ws, nb) if s_ == 0 else None
+            dv = ws[off:off + 8 * 3 * 1024 * 8].view(torch.int64).view(3, 1024, 8)
+            dv[:, 1023, 0] = 2 ** 62
+            dv[:, 1023, 1] = 0
+            xbuf.copy_(xs[s_ % n_x])
+            layer(s_ % NL)  # eager: kernel parameters carry the diagnostic flag
+            torch.cuda.synchronize()
+            sp = dv[:, 1023, :2].cpu().numpy()
+            spans.append([(sp[k, 1] - sp[k, 0]) / 1e3 for k in (2, 0, 1)])
+        A.bqe_set_diag(False)
+        dbg = ws[off:off + 8 * 3 * 1024 * 8].view(torch.int64).view(3, 1024, 8).cpu().numpy()
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         names = ["prod_wait_empty", "prod_issue", "cons_wait_stage", "cons_wait_redbuf", "cons_compute",
                  "epi_wait", "epi_work", "cta_total"]
@@ -376,6 +435,15 @@ def run_layer(args, rank, world):
             v = dbg[ph, :sms].astype(np.float64) / nd / 2.07e3  # us per call at 2.07 GHz
             rep["phase_%d" % ph] = {n: [round(float(v[:, k].mean()), 2), round(float(v[:, k].max()), 2)]
                                     for k, n in enumerate(names)}
+        ncta = (W.E + 1) // 2
+        vr = dbg[2, :ncta].astype(np.float64) / nd / 2.07e3
+        rep["router"] = {"cta_gemv_us": [round(float(vr[:, 0].mean()), 2), round(float(vr[:, 0].max()), 2)],
+                         "last_cta_total_us": round(float(dbg[2, 1022, 1]) / nd / 2.07e3, 2)}
+        rep["router_tail_stamps_us"] = [round(float(v) / nd / 2.07e3, 2) for v in dbg[2, 1021, :7]]
+        sp = np.array(spans)
+        rep["kernel_span_us(first CTA start -> last CTA end)"] = dict(
+            router=round(float(sp[:, 0].mean()), 2), phase_a=round(float(sp[:, 1].mean()), 2),
+            phase_b=round(float(sp[:, 2].mean()), 2))
         A.bqe_workspace_init(ws, nb)
         sys.stderr.write("DIAG " + json.dumps(rep) + "\n")
 
@@ -432,15 +500,23 @@ def run_step40(args, rank, world):
         resid.copy_(S.x0[i % nf])
 
     def run():
-        A.bqe_moe_step(d, L, M, resid, S.wr, None, pool, S.tables, forced, None, ws, nb, st.cuda_stream)
+        # the current stream: inside graph capture this is the capture stream
+        A.bqe_moe_step(d, L, M, resid, S.wr, None, pool, S.tables, forced, None, ws, nb)
 
     for i in range(max(args.warmup, 3)):
         load(i)
         run()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(st)
+    with torch.cuda.stream(side):
+        run()
+    st.wait_stream(side)
+    torch.cuda.synchronize()
     with torch.cuda.graph(g):
         run()
+    torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device(), enabled=not args.no_clocks)
     t_end = time.time() + args.soak_s
     i = 0

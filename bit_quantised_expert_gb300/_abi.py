@@ -72,6 +72,7 @@ SIGNATURES = {
     "bqe_set_test_drop_item": (None, [_I32]),
     "bqe_set_variant": (None, [_I32]),
     "bqe_set_diag": (None, [_I32]),
+    "bqe_set_fused": (None, [_I32]),
     "bqe_diag_offset": (_U64, [_DESC, _I32]),
 }
 
@@ -222,3 +223,7 @@ def bqe_set_diag(on: bool) -> None:
 
 def bqe_diag_offset(d, M: int) -> int:
     return lib.bqe_diag_offset(ctypes.byref(d), M)
+
+
+def bqe_set_fused(on: bool) -> None:
+    lib.bqe_set_fused(1 if on else 0)

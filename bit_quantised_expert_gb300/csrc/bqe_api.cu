@@ -14,6 +14,7 @@ static std::atomic<int> g_use_pdl{1};
 static std::atomic<int> g_drop_item{-1};
 static std::atomic<int> g_variant{1};
 static std::atomic<int> g_diag{0};
+static std::atomic<int> g_fused{0};
 
 // Diagnostic knobs (not part of the operation): the bound on every in-kernel
 // wait, and whether kernels are chained with programmatic dependent launch.
@@ -22,6 +23,7 @@ extern "C" void bqe_set_pdl(int on) { g_use_pdl = on ? 1 : 0; }
 extern "C" void bqe_set_test_drop_item(int32_t item) { g_drop_item = item; }
 extern "C" void bqe_set_variant(int32_t v) { g_variant = v; }
 extern "C" void bqe_set_diag(int32_t on) { g_diag = on ? 1 : 0; }
+extern "C" void bqe_set_fused(int32_t on) { g_fused = on ? 1 : 0; }
 
 static int device_sms() {
   static int cache[64] = {0};
@@ -88,6 +90,7 @@ static int route_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, c
   P.pool = *pool;
   P.topk_idx = topk_idx;
   P.topk_w = topk_w;
+  P.diag = g_diag.load();
   return launch_route(P, st, g_use_pdl.load() != 0);
 }
 
@@ -144,10 +147,52 @@ extern "C" int bqe_experts_phase(const bqe_layer_desc* d, int32_t M, const bqe_p
   return experts_common(d, M, pool, out, accumulate, ws, ws_bytes, (cudaStream_t)stream, phase);
 }
 
+static int layer_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* resid, uint16_t* t_out,
+                        const float* router_w, const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
+                        const int32_t* forced_idx, float* out, int32_t accumulate, int32_t* topk_idx, float* topk_w,
+                        void* ws, uint64_t ws_bytes, cudaStream_t st) {
+  if (!desc_ok(d) || M < 1 || M > kMaxM || (!x && !resid) || !router_w || !slot_table || !ws || !out) return BQE_EINVAL;
+  if (((uintptr_t)ws & 255) || ((uintptr_t)router_w & 15) || d->hidden % 512) return BQE_EINVAL;
+  int rc = check_pool(pool);
+  if (rc) return rc;
+  Geo g = geo_of(d, M);
+  WsLayout L = make_ws(g);
+  if (ws_bytes < L.total) return BQE_ENOSPC;
+  const int sms = device_sms();
+  if (sms <= 0) return BQE_ECUDA;
+  if ((d->n_experts + sms - 1) / sms > 4) return BQE_EUNSUPPORTED;  // router rows per CTA
+  LayerParams P = {};
+  P.g = g;
+  P.L = L;
+  P.ws = (uint8_t*)ws;
+  P.x = x;
+  P.resid = resid;
+  P.t_out = t_out;
+  P.router_w = router_w;
+  P.bias = sel_bias;
+  P.forced = forced_idx;
+  P.slot_table = slot_table;
+  P.pool = *pool;
+  P.out = out;
+  P.accumulate = accumulate ? 1 : 0;
+  P.topk_idx = topk_idx;
+  P.topk_w = topk_w;
+  P.drop_item = g_drop_item.load();
+  P.variant = g_variant.load();
+  P.diag = g_diag.load();
+  P.limit_ns = g_wait_limit_ns.load();
+  return launch_layer(P, sms, st);
+}
+
 extern "C" int bqe_moe_layer_forward(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w,
                                      const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
                                      const int32_t* forced_idx, float* out, int32_t accumulate, int32_t* topk_idx,
                                      float* topk_w, void* ws, uint64_t ws_bytes, void* stream) {
+  if (g_fused.load()) {
+    if (!x) return BQE_EINVAL;
+    return layer_common(d, M, x, nullptr, nullptr, router_w, sel_bias, pool, slot_table, forced_idx, out, accumulate,
+                        topk_idx, topk_w, ws, ws_bytes, (cudaStream_t)stream);
+  }
   int rc = bqe_route(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, topk_idx, topk_w, ws, ws_bytes,
                      stream);
   if (rc) return rc;
@@ -162,11 +207,18 @@ extern "C" int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M
   const int64_t E = d->n_experts, H = d->hidden, K = d->top_k;
   cudaStream_t st = (cudaStream_t)stream;
   for (int l = 0; l < n_layers; ++l) {
-    int rc = route_common(d, M, nullptr, resid, t_out ? t_out + (int64_t)l * M * H : nullptr, router_w + l * E * H,
-                          sel_bias ? sel_bias + l * E : nullptr, pool, slot_tables + l * (E + 1),
-                          forced_idx ? forced_idx + (int64_t)l * M * K : nullptr, nullptr, nullptr, ws, ws_bytes, st);
-    if (rc) return rc;
-    rc = experts_common(d, M, pool, resid, 1, ws, ws_bytes, st);
+    uint16_t* tl = t_out ? t_out + (int64_t)l * M * H : nullptr;
+    const float* bl = sel_bias ? sel_bias + l * E : nullptr;
+    const int32_t* fl = forced_idx ? forced_idx + (int64_t)l * M * K : nullptr;
+    int rc;
+    if (g_fused.load()) {
+      rc = layer_common(d, M, nullptr, resid, tl, router_w + l * E * H, bl, pool, slot_tables + l * (E + 1), fl, resid, 1,
+                        nullptr, nullptr, ws, ws_bytes, st);
+    } else {
+      rc = route_common(d, M, nullptr, resid, tl, router_w + l * E * H, bl, pool, slot_tables + l * (E + 1), fl, nullptr,
+                        nullptr, ws, ws_bytes, st);
+      if (!rc) rc = experts_common(d, M, pool, resid, 1, ws, ws_bytes, st);
+    }
     if (rc) return rc;
   }
   return BQE_OK;

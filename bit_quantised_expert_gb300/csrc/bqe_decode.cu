@@ -28,345 +28,11 @@
 #include <cuda_fp16.h>
 #include <cuda_fp4.h>
 
+#include "bqe_gemv.cuh"
 #include "bqe_internal.cuh"
 
 namespace bqe {
 
-
-struct StageHdr {
-  uint64_t addr;  // slot base
-  int u, p0, c, fmt, R, pad;
-};
-
-__host__ __device__ inline int phase_mats(int phase) { return phase == 0 ? 2 : 1; }
-
-__host__ __device__ inline int phase_panels(const Geo& g, int phase) { return phase == 0 ? g.PA : g.PB; }
-
-__host__ __device__ inline uint32_t stage_slot_bytes(const Geo& g, int phase) {
-  return stage_bytes_for(phase_mats(phase), phase_panels(g, phase), phase == 0 ? g.kcA : g.kcB, g.M);
-}
-
-__host__ __device__ inline int phase_warps(const Geo& g, int phase) {
-  return phase_mats(phase) * phase_panels(g, phase) * (phase == 0 ? g.GA : g.GB);
-}
-
-// ---------------------------------------------------------------------------
-// per-format group kernels: one lane = one weight row, 256 columns, R rows of
-// activations; acc[r] accumulates the row's dot products (two halves kept in
-// a float2 for the packed FMA, added at the end).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
-
-__device__ __forceinline__ float ue8m0_f32(uint32_t e) {
-  return e == 0 ? __int_as_float(0x00400000) : __int_as_float((int)(e << 23));
-}
-
-__device__ __forceinline__ float2 e2m1x2_f32(uint32_t byte) {
-  __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)byte, __NV_E2M1);
-  return __half22float2(*reinterpret_cast<__half2*>(&h));
-}
-
-// Four E2M1 pairs of one 32-bit word -> four f16x2 (exact; the low nibble of
-// each byte is the lower half), by the hardware E2M1x2 -> f16x2 conversion.
-__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& h0, uint32_t& h1, uint32_t& h2,
-                                                uint32_t& h3) {
-  asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4;\n"
-      "  cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      "  cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
-      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
-      : "r"(w));
-}
-
-// a0 += lo(w) * lo(x), a1 += hi(w) * hi(x): f16 inputs, exact f32 products,
-// f32 accumulation (mixed-precision FMA of sm_100+).
-__device__ __forceinline__ void fma_f16x2_f32(uint32_t w, uint32_t x, float& a0, float& a1) {
-  asm("{ .reg .f16 wl, wh, xl, xh; mov.b32 {wl, wh}, %2; mov.b32 {xl, xh}, %3;\n"
-      "  fma.rn.f32.f16 %0, wl, xl, %0; fma.rn.f32.f16 %1, wh, xh, %1; }"
-      : "+f"(a0), "+f"(a1)
-      : "r"(w), "r"(x));
-}
-
-template <int R>
-__device__ __forceinline__ void group_mxfp4(const uint8_t* tile, int nb, int grp, const float* act, int kc, int lane,
-                                            float2 (&acc)[R]) {
-#pragma unroll 2
-  for (int bi = 0; bi < 8; ++bi) {
-    const int b = grp * 8 + bi;
-    const uint4 c4 = *reinterpret_cast<const uint4*>(tile + b * 512 + lane * 16);
-    const float sc = ue8m0_f32(tile[nb * 512 + b * 32 + lane]);
-    float2 bs[R][2];  // two independent chains per row
-#pragma unroll
-    for (int r = 0; r < R; ++r) bs[r][0] = bs[r][1] = f2(0.f, 0.f);
-    const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t h0, h1, h2, h3;
-      e2m1x8_to_f16x2(wd[w], h0, h1, h2, h3);
-      const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
-      const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
-      const float2 v2 = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-      const float2 v3 = __half22float2(*reinterpret_cast<const __half2*>(&h3));
-      const int k = grp * 256 + bi * 32 + w * 8;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float4 xa = *reinterpret_cast<const float4*>(act + r * kc + k);
-        const float4 xb = *reinterpret_cast<const float4*>(act + r * kc + k + 4);
-        bs[r][0] = __ffma2_rn(v0, f2(xa.x, xa.y), bs[r][0]);
-        bs[r][1] = __ffma2_rn(v1, f2(xa.z, xa.w), bs[r][1]);
-        bs[r][0] = __ffma2_rn(v2, f2(xb.x, xb.y), bs[r][0]);
-        bs[r][1] = __ffma2_rn(v3, f2(xb.z, xb.w), bs[r][1]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-      acc[r] = __ffma2_rn(f2(bs[r][0].x + bs[r][1].x, bs[r][0].y + bs[r][1].y), f2(sc, sc), acc[r]);
-  }
-}
-
-// MXFP4 group with f16 activations (act_h: R rows x kc halves, scaled by a
-// power of two per row; the epilogue removes the scale).  Four accumulator
-// chains per row.
-template <int R>
-__device__ __forceinline__ void group_mxfp4_h(const uint8_t* tile, int nb, int grp, const uint16_t* act_h, int kc,
-                                              int lane, float2 (&acc)[R]) {
-#pragma unroll 1
-  for (int bi = 0; bi < 8; ++bi) {
-    const int b = grp * 8 + bi;
-    const uint4 c4 = *reinterpret_cast<const uint4*>(tile + b * 512 + lane * 16);
-    const float sc = ue8m0_f32(tile[nb * 512 + b * 32 + lane]);
-    float a[R][4];
-#pragma unroll
-    for (int r = 0; r < R; ++r) a[r][0] = a[r][1] = a[r][2] = a[r][3] = 0.f;
-    const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t h0, h1, h2, h3;
-      e2m1x8_to_f16x2(wd[w], h0, h1, h2, h3);
-      const int k = grp * 256 + bi * 32 + w * 8;
-      const int ch = (w & 1) * 2;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(act_h + r * kc + k);
-        fma_f16x2_f32(h0, xv.x, a[r][ch], a[r][ch + 1]);
-        fma_f16x2_f32(h1, xv.y, a[r][ch], a[r][ch + 1]);
-        fma_f16x2_f32(h2, xv.z, a[r][ch], a[r][ch + 1]);
-        fma_f16x2_f32(h3, xv.w, a[r][ch], a[r][ch + 1]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r].x = fmaf((a[r][0] + a[r][1]) + (a[r][2] + a[r][3]), sc, acc[r].x);
-  }
-}
-
-// 2-bit code q -> float (2q - 3), exactly, via a float whose fraction holds q:
-// 1 + q/4 has the bit pattern 0x3F800000 | q << 21, and 8 (1 + q/4) - 11 = 2q - 3.
-__device__ __forceinline__ float q2_val(uint32_t word, int j) {
-  const float f = __uint_as_float(0x3F800000u | (((word >> (2 * j)) & 3u) << 21));
-  return fmaf(8.0f, f, -11.0f);
-}
-
-template <int R>
-__device__ __forceinline__ void group_q2_0(const uint8_t* tile, int nb, int grp, const float* act, int kc, int lane,
-                                           float2 (&acc)[R]) {
-#pragma unroll 1
-  for (int bi = 0; bi < 4; ++bi) {
-    const int b = grp * 4 + bi;
-    const uint4 c4 = *reinterpret_cast<const uint4*>(tile + b * 512 + lane * 16);
-    const float d = __half2float(*reinterpret_cast<const __half*>(tile + nb * 512 + (b * 32 + lane) * 2));
-    float2 bs[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) bs[r] = f2(0.f, 0.f);
-    const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-#pragma unroll
-      for (int j = 0; j < 16; j += 4) {
-        const float2 v0 = f2(q2_val(wd[w], j), q2_val(wd[w], j + 1));
-        const float2 v1 = f2(q2_val(wd[w], j + 2), q2_val(wd[w], j + 3));
-        const int k = grp * 256 + bi * 64 + w * 16 + j;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float4 xa = *reinterpret_cast<const float4*>(act + r * kc + k);
-          bs[r] = __ffma2_rn(v0, f2(xa.x, xa.y), bs[r]);
-          bs[r] = __ffma2_rn(v1, f2(xa.z, xa.w), bs[r]);
-        }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = __ffma2_rn(bs[r], f2(d, d), acc[r]);
-  }
-}
-
-// Five ternary digits of one byte (least significant first) -> t = digit - 1.
-__device__ __forceinline__ void tq1_byte(uint32_t v, float (&t)[5]) {
-#pragma unroll
-  for (int r = 0; r < 5; ++r) {
-    const uint32_t q = (v * 171u) >> 9;  // v / 3 for v <= 255
-    t[r] = (float)((int)(v - 3u * q) - 1);
-    v = q;
-  }
-}
-
-template <int R>
-__device__ __forceinline__ void group_tq1(const uint8_t* tile, int nb, int grp, const float* act, int kc, int lane,
-                                          float2 (&acc)[R]) {
-  const int b = grp;
-  float2 bs[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) bs[r] = f2(0.f, 0.f);
-  // bytes 0..47: three 16-byte pieces = 12 words = 12 x 4 bytes = 12 x 20 weights
-#pragma unroll 1
-  for (int q = 0; q < 3; ++q) {
-    const uint4 c4 = *reinterpret_cast<const uint4*>(tile + (b * 3 + q) * 512 + lane * 16);
-    const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      float t[20];
-#pragma unroll
-      for (int by = 0; by < 4; ++by) {
-        float tt[5];
-        tq1_byte((wd[w] >> (8 * by)) & 0xFF, tt);
-#pragma unroll
-        for (int r5 = 0; r5 < 5; ++r5) t[by * 5 + r5] = tt[r5];
-      }
-      const int k = grp * 256 + (q * 16 + w * 4) * 5;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-#pragma unroll
-        for (int i4 = 0; i4 < 5; ++i4) {
-          const float4 xa = *reinterpret_cast<const float4*>(act + r * kc + k + 4 * i4);
-          bs[r] = __ffma2_rn(f2(t[4 * i4], t[4 * i4 + 1]), f2(xa.x, xa.y), bs[r]);
-          bs[r] = __ffma2_rn(f2(t[4 * i4 + 2], t[4 * i4 + 3]), f2(xa.z, xa.w), bs[r]);
-        }
-      }
-    }
-  }
-  // bytes 48..55: three digit bytes (weights 240..254), byte 51 (weight 255), d
-  const uint2 tail = *reinterpret_cast<const uint2*>(tile + nb * 1536 + (b * 32 + lane) * 8);
-  float t[16];
-#pragma unroll
-  for (int by = 0; by < 3; ++by) {
-    float tt[5];
-    tq1_byte((tail.x >> (8 * by)) & 0xFF, tt);
-#pragma unroll
-    for (int r5 = 0; r5 < 5; ++r5) t[by * 5 + r5] = tt[r5];
-  }
-  t[15] = (float)((int)((tail.x >> 24) % 3u) - 1);
-  const float d = __half2float(__ushort_as_half((unsigned short)(tail.y & 0xFFFF)));
-  const int k = grp * 256 + 240;
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-#pragma unroll
-    for (int i4 = 0; i4 < 4; ++i4) {
-      const float4 xa = *reinterpret_cast<const float4*>(act + r * kc + k + 4 * i4);
-      bs[r] = __ffma2_rn(f2(t[4 * i4], t[4 * i4 + 1]), f2(xa.x, xa.y), bs[r]);
-      bs[r] = __ffma2_rn(f2(t[4 * i4 + 2], t[4 * i4 + 3]), f2(xa.z, xa.w), bs[r]);
-    }
-    acc[r] = __ffma2_rn(bs[r], f2(d, d), acc[r]);
-  }
-}
-
-template <int R>
-__device__ __forceinline__ void group_q3k(const uint8_t* tile, int nb, int grp, const float* act, int kc, int lane,
-                                          float2 (&acc)[R]) {
-  const int b = grp;
-  uint32_t lo[16], hi[8], sc[3];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 v = *reinterpret_cast<const uint4*>(tile + (b * 4 + q) * 512 + lane * 16);
-    lo[4 * q] = v.x; lo[4 * q + 1] = v.y; lo[4 * q + 2] = v.z; lo[4 * q + 3] = v.w;
-  }
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const uint4 v = *reinterpret_cast<const uint4*>(tile + nb * 2048 + (b * 2 + q) * 512 + lane * 16);
-    hi[4 * q] = v.x; hi[4 * q + 1] = v.y; hi[4 * q + 2] = v.z; hi[4 * q + 3] = v.w;
-  }
-  const uint8_t* scp = tile + nb * 3072 + (b * 32 + lane) * 12;
-#pragma unroll
-  for (int i = 0; i < 3; ++i) sc[i] = *reinterpret_cast<const uint32_t*>(scp + 4 * i);
-  const float d = __half2float(*reinterpret_cast<const __half*>(tile + nb * 3456 + (b * 32 + lane) * 2));
-  float2 bsum[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) bsum[r] = f2(0.f, 0.f);
-#pragma unroll 1
-  for (int sj = 0; sj < 16; ++sj) {
-    // 6-bit sub-scale sj at bits 6 sj .. 6 sj + 5 of the 96-bit little-endian string
-    const int bit = 6 * sj;
-    const uint64_t two = ((uint64_t)sc[bit >> 5]) | (((bit >> 5) < 2 ? (uint64_t)sc[(bit >> 5) + 1] : 0ull) << 32);
-    const float s = (float)((uint32_t)(two >> (bit & 31)) & 63u);
-    const uint32_t low = lo[sj];          // weights 16 sj .. 16 sj + 15: 2 bits each
-    const uint32_t high = hi[sj >> 1] >> ((sj & 1) * 16);  // 16 high bits
-    float2 ss[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) ss[r] = f2(0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-      float v[4];
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int qv = (int)(((low >> (2 * (j + jj))) & 3u) | (((high >> (j + jj)) & 1u) << 2));
-        v[jj] = (float)(qv - 4);
-      }
-      const int k = grp * 256 + sj * 16 + j;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float4 xa = *reinterpret_cast<const float4*>(act + r * kc + k);
-        ss[r] = __ffma2_rn(f2(v[0], v[1]), f2(xa.x, xa.y), ss[r]);
-        ss[r] = __ffma2_rn(f2(v[2], v[3]), f2(xa.z, xa.w), ss[r]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) bsum[r] = __ffma2_rn(ss[r], f2(s, s), bsum[r]);
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = __ffma2_rn(bsum[r], f2(d, d), acc[r]);
-}
-
-template <int R>
-__device__ __forceinline__ void consume_group_R(int fmt, const uint8_t* tile, int kc, int grp, const float* act,
-                                                int lane, float* outv /* [r * 32 + lane] */, bool half_act) {
-  float2 acc[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = f2(0.f, 0.f);
-  const int nb = kc / fmt_bw(fmt);
-  switch (fmt) {
-    case BQE_FMT_MXFP4:
-      if (half_act)
-        group_mxfp4_h<R>(tile, nb, grp, reinterpret_cast<const uint16_t*>(act), kc, lane, acc);
-      else
-        group_mxfp4<R>(tile, nb, grp, act, kc, lane, acc);
-      break;
-    case BQE_FMT_Q2_0: group_q2_0<R>(tile, nb, grp, act, kc, lane, acc); break;
-    case BQE_FMT_TQ1: group_tq1<R>(tile, nb, grp, act, kc, lane, acc); break;
-    case BQE_FMT_Q3_K: group_q3k<R>(tile, nb, grp, act, kc, lane, acc); break;
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r) outv[r * 32 + lane] = acc[r].x + acc[r].y;
-}
-
-__device__ __forceinline__ void consume_group(int R, int fmt, const uint8_t* tile, int kc, int grp, const float* act,
-                                              int lane, float* outv, bool half_act) {
-  switch (R) {
-    case 1: consume_group_R<1>(fmt, tile, kc, grp, act, lane, outv, half_act); break;
-    case 2: consume_group_R<2>(fmt, tile, kc, grp, act, lane, outv, half_act); break;
-    case 3: consume_group_R<3>(fmt, tile, kc, grp, act, lane, outv, half_act); break;
-    case 4: consume_group_R<4>(fmt, tile, kc, grp, act, lane, outv, half_act); break;
-  }
-}
-
-// All R rows of one stage, kRowChunk rows at a time (the weights of the group
-// are decoded again for each further chunk; only rows 5..8 of a call pay it).
-__device__ __forceinline__ void consume_rows(int R, int fmt, const uint8_t* tile, int kc, int grp, const uint8_t* act,
-                                             int lane, float* outv, bool half_act) {
-  const size_t row_bytes = (size_t)kc * (half_act ? 2 : 4);
-  for (int r0 = 0; r0 < R; r0 += kRowChunk) {
-    const int n = R - r0 < kRowChunk ? R - r0 : kRowChunk;
-    consume_group(n, fmt, tile, kc, grp, reinterpret_cast<const float*>(act + r0 * row_bytes), lane, outv + r0 * 32,
-                  half_act);
-  }
-}
-
-__device__ __forceinline__ float silu_f(float t) { return t / (1.0f + expf(-t)); }
 
 __device__ __forceinline__ long long clk() { return clock64(); }
 // diagnostic counters: 0 producer waiting for a free stage, 1 producer issuing,
@@ -422,6 +88,7 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
   const int per_u = (npan / P_) * nch;
 
   if (tid == 0) {
+    if (P.diag) dbg_span(P.ws, P.L.dbg, PHASE, false);
     for (int s = 0; s < nstages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NW);
@@ -436,6 +103,7 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
   __syncthreads();
 
   griddep_wait();  // routing / phase A results must be complete and visible
+  griddep_launch_dependents();  // the finalize kernel may be scheduled behind this one
 
   const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
   const int nItems = nU * per_u;
@@ -461,6 +129,7 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
       int last_issued[16];
       for (int s = 0; s < 16; ++s) last_issued[s] = -1;
       long long pw = 0, pi_ = 0;
+      const uint64_t pol = policy_evict_first();
       int i = 0;
       for (int t = blockIdx.x; t < nItems; t += gridDim.x, ++i) {
         const int s = i % nstages;
@@ -494,13 +163,13 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
         if (PHASE == 0) {
           for (int j = 0; j < P_; ++j) {
             const uint64_t toff = (uint64_t)((pg * P_ + j) * nch + c) * tb;
-            bulk_g2s(dst + j * tb, (const void*)(addr + toff), tb, &full[s]);                 // W1
-            bulk_g2s(dst + (P_ + j) * tb, (const void*)(addr + m13 + toff), tb, &full[s]);    // W3
+            bulk_g2s_hint(dst + j * tb, (const void*)(addr + toff), tb, &full[s], pol);               // W1
+            bulk_g2s_hint(dst + (P_ + j) * tb, (const void*)(addr + m13 + toff), tb, &full[s], pol);  // W3
           }
         } else {
           for (int j = 0; j < P_; ++j) {
             const uint64_t toff = 2 * m13 + (uint64_t)((pg * P_ + j) * nch + c) * tb;
-            bulk_g2s(dst + j * tb, (const void*)(addr + toff), tb, &full[s]);
+            bulk_g2s_hint(dst + j * tb, (const void*)(addr + toff), tb, &full[s], pol);
           }
         }
         uint8_t* adst = dst + wbytes;
@@ -635,6 +304,7 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
     dbg_add(P, PHASE, 5, ew);
     dbg_add(P, PHASE, 6, eb + (tend - tprev));
     dbg_add(P, PHASE, 7, tend - tstart);
+    if (P.diag) dbg_span(P.ws, P.L.dbg, PHASE, true);
   }
 }
 
@@ -646,6 +316,7 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
 __global__ void __launch_bounds__(256) k_finalize_a(ExpParams P) {
   const Geo& g = P.g;
   griddep_wait();
+  griddep_launch_dependents();
   const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
   const int32_t* u_nrows = (const int32_t*)(P.ws + P.L.u_nrows);
   const float* pa = (const float*)(P.ws + P.L.pa);
@@ -671,6 +342,7 @@ __global__ void __launch_bounds__(256) k_finalize_a(ExpParams P) {
 __global__ void __launch_bounds__(256) k_finalize_b(ExpParams P) {
   const Geo& g = P.g;
   griddep_wait();
+  griddep_launch_dependents();
   const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
   const float* pb = (const float*)(P.ws + P.L.pb);
   const int32_t* cu = (const int32_t*)(P.ws + P.L.comb_u);

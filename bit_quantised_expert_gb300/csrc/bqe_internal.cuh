@@ -127,7 +127,8 @@ __host__ __device__ inline Geo make_geo(int H, int I, int E, int K, int M) {
 // Workspace layout (offsets in bytes, each 256-aligned).
 struct WsLayout {
   uint64_t err, ctr_route, nu, u_slot, u_fmt, u_addr, u_nrows, u_rows;
-  uint64_t comb_u, comb_r, comb_w, z, xf, xh, xsc, pa, h, pb, dbg, total;
+  uint64_t comb_u, comb_r, comb_w, z, xf, xh, xsc, pa, h, pb, dbg;
+  uint64_t fctr, cnt_a, h_cnt, ctr_out, total;  // counters of the fused layer kernel
 };
 constexpr int kDbgSlots = 8;      // per-CTA cycle counters of the diagnostic mode
 constexpr int kDbgMaxCtas = 1024;
@@ -155,7 +156,11 @@ __host__ __device__ inline WsLayout make_ws(const Geo& g) {
   w.pa = o; o = al256(o + 4ull * g.U * g.npanA * g.nchA * 2 * g.M * 32);
   w.h = o; o = al256(o + 4ull * g.U * g.M * g.I);
   w.pb = o; o = al256(o + 4ull * g.U * g.nchB * g.M * g.H);
-  w.dbg = o; o = al256(o + 8ull * 2 * kDbgMaxCtas * kDbgSlots);  // [phase][cta][slot] cycles
+  w.dbg = o; o = al256(o + 8ull * 3 * kDbgMaxCtas * kDbgSlots);  // [phase A, phase B, router][cta][slot] cycles
+  w.fctr = o; o = al256(o + 16);                                  // [0] logits done, [1] CTAs done
+  w.cnt_a = o; o = al256(o + 4ull * g.U * g.npanA);               // chunks done per (expert, panel group)
+  w.h_cnt = o; o = al256(o + 4ull * g.U);                         // panel groups of h done per expert
+  w.ctr_out = o; o = al256(o + 4ull * g.npanB);                   // (expert, chunk) items done per output panel group
   w.total = o;
   return w;
 }
@@ -176,6 +181,7 @@ struct RouteParams {
   bqe_pool pool;
   int32_t* topk_idx;          // optional M x K
   float* topk_w;              // optional M x K
+  int diag;                   // 1: add cycle counts into ws.dbg
 };
 
 struct ExpParams {
@@ -190,6 +196,32 @@ struct ExpParams {
   int diag;           // 1: accumulate per-CTA cycle counters into ws.dbg
   uint64_t limit_ns;  // bound on every mbarrier wait
 };
+
+// Fused decode layer: router + top-k + W1/W3 + SiLU-GLU + W2 + combine in one
+// cooperatively launched persistent kernel.
+struct LayerParams {
+  Geo g;
+  WsLayout L;
+  uint8_t* ws;
+  const uint16_t* x;          // bf16 M x H, or null when resid is given
+  const float* resid;         // fp32 M x H (chained step: normalise first)
+  uint16_t* t_out;            // optional bf16 M x H copy of the layer input
+  const float* router_w;
+  const float* bias;
+  const int32_t* forced;
+  const int32_t* slot_table;
+  bqe_pool pool;
+  float* out;
+  int accumulate;
+  int32_t* topk_idx;
+  float* topk_w;
+  int nstages, NW, NE;        // ring depth, consumer warps, epilogue warps
+  uint32_t slot_bytes;        // ring slot
+  int drop_item, variant, diag;
+  uint64_t limit_ns;
+};
+int launch_layer(const LayerParams& P, int grid, cudaStream_t st);
+uint32_t layer_smem_bytes(const Geo& g, int* nstages_out, int* nw_out, uint32_t* slot_out);
 
 // Launchers (one per translation unit that owns the kernel).
 int launch_route(const RouteParams& P, cudaStream_t st, bool pdl);
@@ -255,6 +287,28 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// L2 policy for data read exactly once per call (expert and router weights):
+// evicted first, so the code, work lists and activations stay in L2.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ float4 ldg_stream_f4(const float4* p, uint64_t pol) {
+  float4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -272,6 +326,18 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
       : "r"(id), "r"(nthreads), "r"((uint32_t)pred)
       : "memory");
   return r != 0;
+}
+
+// Diagnostic span of a kernel: globaltimer at the first CTA start (atomicMin)
+// and at the last CTA end (atomicMax), kept in CTA row 1023 of block `blk`.
+__device__ __forceinline__ void dbg_span(uint8_t* ws, uint64_t dbg_off, int blk, bool end) {
+  unsigned long long* p = (unsigned long long*)(ws + dbg_off) + ((size_t)blk * 1024 + 1023) * 8;
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  if (end)
+    atomicMax(p + 1, (unsigned long long)t);
+  else
+    atomicMin(p + 0, (unsigned long long)t);
 }
 
 __device__ __forceinline__ void set_error(int32_t* err, int code, int detail) {

@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = g.H, E = g.E, K = g.K;
   constexpr int M = MR;
+  const long long t_start = clock64();
+  if (P.diag && threadIdx.x == 0) dbg_span(P.ws, P.L.dbg, 2, false);
   int32_t* err = (int32_t*)(P.ws + P.L.err);
   float* z = (float*)(P.ws + P.L.z);
   float* xf = (float*)(P.ws + P.L.xf);
@@ -56,12 +58,16 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
   float4 w4[kRouteMaxNI];
   if (e < E) {
     const float4* wr = (const float4*)(P.router_w + (int64_t)e * H + (int64_t)q * Kq);
+    const uint64_t pol = policy_evict_first();
 #pragma unroll
     for (int i = 0; i < kRouteMaxNI; ++i)
-      if (i < ni) w4[i] = __ldg(wr + i * 32 + lane);
+      if (i < ni) w4[i] = ldg_stream_f4(wr + i * 32 + lane, pol);
   }
 
   griddep_wait();  // the layer input may come from the previous kernels
+  griddep_launch_dependents();  // the W1/W3 kernel may start its own prologue now
+  __shared__ int32_t s_table[kMaxE + 1];  // slot of every expert (the selecting CTA uses it)
+  for (int i = tid; i <= E; i += kRouteThreads) s_table[i] = P.slot_table[i];
 
   // ---- layer input into shared memory: bf16 x, or bf16(rmsnorm(resid)) -------
   if (P.resid) {
@@ -163,6 +169,11 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
     }
   }
 
+  if (P.diag && tid == 0 && blockIdx.x < kDbgMaxCtas) {
+    atomicAdd((unsigned long long*)(P.ws + P.L.dbg) + ((size_t)2 * kDbgMaxCtas + blockIdx.x) * kDbgSlots + 0,
+              (unsigned long long)(clock64() - t_start));
+    dbg_span(P.ws, P.L.dbg, 2, true);
+  }
   // ---- last CTA: scores, top-k, weights, work list ---------------------------
   __threadfence();
   __syncthreads();
@@ -173,86 +184,136 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  auto stamp = [&](int k) {
+    if (P.diag && tid == 0)
+      atomicAdd((unsigned long long*)(P.ws + P.L.dbg) + ((size_t)2 * kDbgMaxCtas + 1021) * kDbgSlots + k,
+                (unsigned long long)(clock64() - t_start));
+  };
+  stamp(0);
 
-  __shared__ uint32_t s_mask[kMaxE];
-  __shared__ int s_uof[kMaxE];
+  __shared__ uint32_t s_mask[kMaxE];           // bit m: row m chose expert e
+  __shared__ int s_uof[kMaxE];                  // work-list index of a chosen expert
   __shared__ int s_idx[kMaxM][kMaxTopK];
+  __shared__ float s_zsel[kMaxM][kMaxTopK];
+  __shared__ int s_list[kMaxM * kMaxTopK];      // chosen experts, ascending
+  __shared__ int s_wcnt[2][kRouteThreads / 32];
   __shared__ int s_bad;
   __shared__ int s_nu;
   if (tid == 0) s_bad = 0;
   for (int i = tid; i < E; i += kRouteThreads) s_mask[i] = 0u;
   __syncthreads();
+  stamp(1);
 
+  // ---- top-k: every warp keeps the k best of its 64 experts (thread t scores
+  // experts t and t + 256), then warp m merges the 8k candidates of row m.
+  // Order: larger key first, ties to the lower expert id; keys compared as
+  // order-preserving 32-bit images so one warp max + one warp min decide a round.
+  __shared__ uint32_t s_ck[kMaxM][kRouteThreads / 32][kMaxTopK];
+  __shared__ int s_ci[kMaxM][kRouteThreads / 32][kMaxTopK];
+  __shared__ float s_cz[kMaxM][kRouteThreads / 32][kMaxTopK];
+  auto ord = [](float f) -> uint32_t {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  };
+  if (!P.forced) {
+    for (int m = 0; m < M; ++m) {
+      const int e0 = tid, e1 = tid + kRouteThreads;
+      const float z0 = e0 < E ? __ldcg(z + (int64_t)m * E + e0) : 0.f;
+      const float z1 = e1 < E ? __ldcg(z + (int64_t)m * E + e1) : 0.f;
+      uint32_t k0 = 0u, k1 = 0u;  // 0: no expert (below every real key)
+      if (e0 < E) k0 = ord(1.0f / (1.0f + expf(-z0)) + (P.bias ? P.bias[e0] : 0.f));
+      if (e1 < E) k1 = ord(1.0f / (1.0f + expf(-z1)) + (P.bias ? P.bias[e1] : 0.f));
+      for (int j = 0; j < K; ++j) {
+        uint32_t lk = k0;
+        int li = e0;
+        if (k1 > lk) { lk = k1; li = e1; }  // e0 < e1, so ties keep e0
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, lk);
+        const int best = (int)__reduce_min_sync(0xffffffffu, (lk == wk && wk != 0u) ? (uint32_t)li : 0x7fffffffu);
+        if (best == e0) { s_cz[m][warp][j] = z0; k0 = 0u; }
+        if (best == e1) { s_cz[m][warp][j] = z1; k1 = 0u; }
+        if (lane == 0) {
+          s_ck[m][warp][j] = wk;
+          s_ci[m][warp][j] = wk != 0u ? best : 0x7fffffff;
+        }
+      }
+    }
+  }
+  __syncthreads();
   if (warp < M) {
     const int m = warp;
-    // lane holds the keys of experts lane, lane+32, ... (E <= kMaxE)
-    float key[kMaxE / 32];
+    constexpr int NC = (kRouteThreads / 32) * kMaxTopK / 32;  // candidates per lane
+    uint32_t ck[NC];
+    int ci[NC];
 #pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
-      const int ee = lane + 32 * i;
-      float kk = -INFINITY;
-      if (ee < E) {
-        const float s = 1.0f / (1.0f + expf(-__ldcg(z + (int64_t)m * E + ee)));
-        kk = P.bias ? s + P.bias[ee] : s;
-      }
-      key[i] = kk;
+    for (int c = 0; c < NC; ++c) {
+      const int q2 = lane + 32 * c;           // candidate q2 = warp_q * K + j
+      const int wq = q2 / kMaxTopK, jq = q2 % kMaxTopK;
+      const bool valid = !P.forced && jq < K;
+      ck[c] = valid ? s_ck[m][wq][jq] : 0u;
+      ci[c] = valid ? s_ci[m][wq][jq] : 0x7fffffff;
     }
     for (int j = 0; j < K; ++j) {
       int best;
+      float zsel;
       if (P.forced) {
         best = P.forced[m * K + j];
         if (best < 0 || best >= E) {
           if (lane == 0) { set_error(err, BQE_EDEVICE, kErrForcedIdx); s_bad = 1; }
           best = 0;
         }
+        zsel = __ldcg(z + (int64_t)m * E + best);
       } else {
-        float bk = -INFINITY;
-        best = 0x7fffffff;
+        uint32_t lk = 0u;
+        int li = 0x7fffffff, lc = -1;
 #pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i) {
-          const int ee = lane + 32 * i;
-          if (key[i] > bk || (key[i] == bk && ee < best)) { bk = key[i]; best = ee; }
-        }
-        for (int o = 16; o; o >>= 1) {
-          const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-          const int oe = __shfl_xor_sync(0xffffffffu, best, o);
-          if (ok > bk || (ok == bk && oe < best)) { bk = ok; best = oe; }
-        }
+        for (int c = 0; c < NC; ++c)
+          if (ck[c] > lk || (ck[c] == lk && ci[c] < li)) { lk = ck[c]; li = ci[c]; lc = c; }
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, lk);
+        best = (int)__reduce_min_sync(0xffffffffu, lk == wk ? (uint32_t)li : 0x7fffffffu);
+        float zc = 0.f;
+        int owner = 0;
 #pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i)
-          if (lane + 32 * i == best) key[i] = -INFINITY;
+        for (int c = 0; c < NC; ++c)
+          if (c == lc && li == best && lk == wk) {
+            const int q2 = lane + 32 * c;
+            zc = s_cz[m][q2 / kMaxTopK][q2 % kMaxTopK];
+            ck[c] = 0u;
+            ci[c] = 0x7fffffff;
+            owner = 1;
+          }
+        const uint32_t own = __ballot_sync(0xffffffffu, owner);
+        zsel = __shfl_sync(0xffffffffu, zc, __ffs(own) - 1);
       }
       if (lane == 0) {
         s_idx[m][j] = best;
+        s_zsel[m][j] = zsel;
         atomicOr(&s_mask[best], 1u << m);
       }
     }
     __syncwarp();
-    if (lane == 0) {
-      // mixing weights w_j = s_j / sum s from the unbiased scores, evaluated as
-      // exp(log s_j - max log s) / sum exp(...): the same ratio, but it stays
-      // finite when every selected sigmoid underflows in fp32
-      float ls[kMaxTopK];
-      float mx = -INFINITY;
-      for (int j = 0; j < K; ++j) {
-        const float zz = __ldcg(z + (int64_t)m * E + s_idx[m][j]);
-        ls[j] = zz < 0.f ? zz - log1pf(expf(zz)) : -log1pf(expf(-zz));  // log sigmoid(z)
-        mx = fmaxf(mx, ls[j]);
-      }
-      float tot = 0.f;
-      for (int j = 0; j < K; ++j) {
-        ls[j] = expf(ls[j] - mx);
-        tot += ls[j];
-      }
-      for (int j = 0; j < K; ++j) {
-        const float w = ls[j] / tot;
-        ((float*)(P.ws + P.L.comb_w))[m * K + j] = w;
-        if (P.topk_idx) P.topk_idx[m * K + j] = s_idx[m][j];
-        if (P.topk_w) P.topk_w[m * K + j] = w;
-      }
+    if (m == 0) stamp(2);
+    // mixing weights w_j = s_j / sum s from the unbiased scores, evaluated as
+    // exp(log s_j - max log s) / sum exp(...): the same ratio, finite even when
+    // every selected sigmoid underflows in fp32.  Lane j takes expert j.
+    float ls = -INFINITY;
+    if (lane < K) {
+      const float zz = s_zsel[m][lane];
+      ls = zz < 0.f ? zz - log1pf(expf(zz)) : -log1pf(expf(-zz));  // log sigmoid(z)
+    }
+    float mx = ls;
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float ev = lane < K ? expf(ls - mx) : 0.f;
+    float tot = ev;
+    for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (lane < K) {
+      const float w = ev / tot;
+      ((float*)(P.ws + P.L.comb_w))[m * K + lane] = w;
+      if (P.topk_idx) P.topk_idx[m * K + lane] = s_idx[m][lane];
+      if (P.topk_w) P.topk_w[m * K + lane] = w;
     }
   }
   __syncthreads();
+  stamp(3);
 
   int32_t* u_slot = (int32_t*)(P.ws + P.L.u_slot);
   int32_t* u_fmt = (int32_t*)(P.ws + P.L.u_fmt);
@@ -260,33 +321,45 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
   int32_t* u_nrows = (int32_t*)(P.ws + P.L.u_nrows);
   int32_t* u_rows = (int32_t*)(P.ws + P.L.u_rows);
 
-  // compact the chosen experts in ascending id order (u = 1..), shared u = 0
-  if (warp == 0) {
-    int base_u = 1;
-    for (int b0 = 0; b0 < E; b0 += 32) {
-      const int ee = b0 + lane;
-      const bool on = ee < E && s_mask[ee] != 0u;
-      const uint32_t bal = __ballot_sync(0xffffffffu, on);
-      if (on) s_uof[ee] = base_u + __popc(bal & ((1u << lane) - 1u));
-      base_u += __popc(bal);
+  // compact the chosen experts in ascending id order (u = 1..), shared u = 0:
+  // expert e = it*256 + warp*32 + lane, positions from per-warp counts
+  bool on[2];
+  uint32_t bal[2];
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int ee = it * kRouteThreads + tid;
+    on[it] = ee < E && s_mask[ee] != 0u;
+    bal[it] = __ballot_sync(0xffffffffu, on[it]);
+    if (lane == 0) s_wcnt[it][warp] = __popc(bal[it]);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    if (on[it]) {
+      int base = 0;
+      for (int i2 = 0; i2 < it; ++i2)
+        for (int w2 = 0; w2 < kRouteThreads / 32; ++w2) base += s_wcnt[i2][w2];
+      for (int w2 = 0; w2 < warp; ++w2) base += s_wcnt[it][w2];
+      const int pos = base + __popc(bal[it] & ((1u << lane) - 1u));
+      const int ee = it * kRouteThreads + tid;
+      s_list[pos] = ee;
+      s_uof[ee] = 1 + pos;
     }
-    if (lane == 0) s_nu = base_u;
+  }
+  if (tid == 0) {
+    int tot = 0;
+    for (int i2 = 0; i2 < 2; ++i2)
+      for (int w2 = 0; w2 < kRouteThreads / 32; ++w2) tot += s_wcnt[i2][w2];
+    s_nu = 1 + tot;
   }
   __syncthreads();
   const int nU = s_nu;
+  stamp(4);
   // per-u descriptors
   for (int u = tid; u < nU; u += kRouteThreads) {
-    int ee = -1;
-    uint32_t mask;
-    if (u == 0) {
-      mask = (M >= 32) ? 0xffffffffu : ((1u << M) - 1u);
-    } else {
-      // find the expert with s_uof == u (scan is fine: at most M*K+1 entries)
-      mask = 0u;
-      for (int c = 0; c < E; ++c)
-        if (s_mask[c] != 0u && s_uof[c] == u) { ee = c; mask = s_mask[c]; break; }
-    }
-    const int slot = (u == 0) ? P.slot_table[E] : P.slot_table[ee];
+    const int ee = u == 0 ? -1 : s_list[u - 1];
+    const uint32_t mask = u == 0 ? ((M >= 32) ? 0xffffffffu : ((1u << M) - 1u)) : s_mask[ee];
+    const int slot = s_table[u == 0 ? E : ee];
     int fmt = 0;
     uint64_t addr = 0;
     if (slot < 0 || slot >= P.pool.n_slots) {
@@ -315,6 +388,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
       if (mask & (1u << m)) u_rows[u * kMaxM + n++] = m;
     u_nrows[u] = n;
   }
+  stamp(5);
   if (warp < M && lane < K) {
     const int m = warp, j = lane;
     const int ee = s_idx[m][j];
@@ -322,9 +396,15 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
     ((int32_t*)(P.ws + P.L.comb_r))[m * K + j] = __popc(s_mask[ee] & ((1u << m) - 1u));
   }
   __syncthreads();
+  stamp(6);
   if (tid == 0) {
     *(int32_t*)(P.ws + P.L.nu) = s_bad ? 0 : nU;
     *(unsigned int*)(P.ws + P.L.ctr_route) = 0u;
+    if (P.diag) {
+      atomicAdd((unsigned long long*)(P.ws + P.L.dbg) + ((size_t)2 * kDbgMaxCtas + 1022) * kDbgSlots + 1,
+                (unsigned long long)(clock64() - t_start));
+      dbg_span(P.ws, P.L.dbg, 2, true);
+    }
   }
 }
 

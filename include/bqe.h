@@ -221,12 +221,20 @@ void bqe_set_test_drop_item(int32_t item);
  * same products; only the summation order differs. */
 void bqe_set_variant(int32_t v);
 
-/* Diagnostic mode (default off): the expert kernels add per-CTA clock64()
- * cycle counts (producer waiting / issuing, consumer waiting for a stage /
- * for a reduction buffer / computing, epilogue waiting / working, whole CTA)
- * into the workspace at byte offset bqe_diag_offset(d, M): uint64
- * [2 phases][1024 CTAs][8 counters], zeroed by bqe_workspace_init. */
+/* Diagnostic mode (default off): the kernels add per-CTA clock64() cycle
+ * counts into the workspace at byte offset bqe_diag_offset(d, M): uint64
+ * [3][1024 CTAs][8 counters], zeroed by bqe_workspace_init.  Blocks 0 and 1
+ * (W1/W3 and W2 kernels): producer waiting / issuing, consumer waiting for a
+ * stage / for a reduction buffer / computing, epilogue waiting / working,
+ * whole CTA.  Block 2 (router): counter 0 = CTA start to its logits written,
+ * counter 1 = start to end of the CTA that selects the experts. */
 void bqe_set_diag(int32_t on);
+
+/* bqe_moe_layer_forward and bqe_moe_step run the layer as the router kernel
+ * followed by the bqe_experts kernels (default, on = 0), or as one
+ * cooperatively launched persistent kernel (on = 1).  Same results up to the
+ * order of the fp32 additions inside the router. */
+void bqe_set_fused(int32_t on);
 uint64_t bqe_diag_offset(const bqe_layer_desc* d, int32_t M);
 
 #ifdef __cplusplus

@@ -182,6 +182,26 @@ def test_forced_idx_with_repeats_and_accumulate(dev):
     check_out(out - keep, ref["out"], rel=2e-4, what="accumulate")
 
 
+@pytest.mark.parametrize("M", [1, 2, 6, 8])
+def test_fused_layer_kernel(dev, M):
+    """The single-kernel layer (cooperative persistent kernel) against the oracle."""
+    from bit_quantised_expert_gb300 import _abi as A
+    fm = [ALL[(3 * e + 2) % 4] for e in range(24)] + [synth.MXFP4]
+    L = synth.small_layer(60 + M, fm, 1024, 768, 24, 3, M, bias_std=0.25)
+    DL = DeviceLayer(L, dev)
+    A.bqe_set_fused(True)
+    try:
+        out, idx, w = DL.forward(L["x"])
+        out2, idx2, _ = DL.forward(L["x"])
+    finally:
+        A.bqe_set_fused(False)
+    ref = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 1024, 768, 3, 24)
+    check_routing(ref, idx, w)
+    ref2 = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 1024, 768, 3, 24, forced_idx=idx)
+    check_out(out, ref2["out"], what="fused M=%d" % M)
+    assert np.array_equal(out, out2) and np.array_equal(idx, idx2)  # deterministic, counters reset
+
+
 def test_deterministic(dev):
     fm = [ALL[e % 4] for e in range(33)]
     L = synth.small_layer(9, fm, 1024, 512, 32, 4, 6, bias_std=0.25)

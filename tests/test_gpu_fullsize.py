@@ -72,7 +72,8 @@ def test_mixed_layer(dev, M):
     _check_layer(W, dev, M, 0, ncols=24 if M > 1 else 48)
 
 
-def test_step40_teacher_forced(dev):
+@pytest.mark.parametrize("fused", [False, True])
+def test_step40_teacher_forced(dev, fused):
     """40 chained layers over the 4288-slot pool (Zipf-forced routing): the
     whole step equals the layer-by-layer run bit for bit, each layer's input
     is the bf16 RMS-normalised residual, and sampled layers match the oracle
@@ -81,6 +82,7 @@ def test_step40_teacher_forced(dev):
     from bit_quantised_expert_gb300 import _abi as A
     from synth import workloads as WL
     M = 1
+    A.bqe_set_fused(fused)
     S = WL.Step40(dev, m=M, n_steps_forced=1)
     L = S.n_layers
     nb = A.bqe_workspace_bytes(S.d, M)
@@ -116,3 +118,4 @@ def test_step40_teacher_forced(dev):
                                        None, S.forced_np[0, l], H, I, E, K, cols)
         got = (snaps[l + 1] - snaps[l])[:, cols]
         check_out(got, oref, rel=1e-4, what="layer %d" % l)
+    A.bqe_set_fused(False)
