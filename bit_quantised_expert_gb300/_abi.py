@@ -64,6 +64,8 @@ SIGNATURES = {
     "bqe_route": (ctypes.c_int, [_DESC, _I32, _P, _P, _P, _POOL, _P, _P, _P, _P, _P, _U64, _P]),
     "bqe_experts": (ctypes.c_int, [_DESC, _I32, _POOL, _P, _I32, _P, _U64, _P]),
     "bqe_experts_phase": (ctypes.c_int, [_DESC, _I32, _POOL, _P, _I32, _I32, _P, _U64, _P]),
+    "bqe_moe_layer_forward_noalloc": (ctypes.c_int, [_DESC, _I32, _P, _P, _P, _POOL, _P, _P, _P, _I32, _P, _P, _P,
+                                                     _P]),
     "bqe_moe_step": (ctypes.c_int, [_DESC, _I32, _I32, _P, _P, _P, _POOL, _P, _P, _P, _P, _U64, _P]),
     "bqe_check": (ctypes.c_int, [_P, _P, ctypes.POINTER(_I32)]),
     "bqe_status_str": (ctypes.c_char_p, [ctypes.c_int]),
@@ -168,6 +170,15 @@ def bqe_moe_layer_forward(d, M, x, router_w, sel_bias, pool: bqe_pool, slot_tabl
     _ok(lib.bqe_moe_layer_forward(ctypes.byref(d), M, ptr(x), ptr(router_w), ptr(sel_bias), ctypes.byref(pool),
                                   ptr(slot_table), ptr(forced_idx), ptr(out), int(accumulate), ptr(topk_idx),
                                   ptr(topk_w), ptr(ws), ws_bytes, stream_ptr(stream)), "bqe_moe_layer_forward")
+
+
+def bqe_moe_layer_forward_noalloc(d, M, x, router_w, sel_bias, pool: bqe_pool, slot_table, forced_idx, out,
+                                  accumulate, topk_idx, topk_w, status_out, stream=None) -> None:
+    """The layer with the library's fixed scratch array as workspace (no allocation)."""
+    _ok(lib.bqe_moe_layer_forward_noalloc(ctypes.byref(d), M, ptr(x), ptr(router_w), ptr(sel_bias),
+                                          ctypes.byref(pool), ptr(slot_table), ptr(forced_idx), ptr(out),
+                                          int(accumulate), ptr(topk_idx), ptr(topk_w), ptr(status_out),
+                                          stream_ptr(stream)), "bqe_moe_layer_forward_noalloc")
 
 
 def bqe_route(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, topk_idx, topk_w, ws, ws_bytes,

@@ -189,6 +189,31 @@ int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M, float* re
                  const int32_t* slot_tables, const int32_t* forced_idx, uint16_t* t_out,
                  void* ws, uint64_t ws_bytes, void* stream);
 
+/* The decode layer without a caller-provided workspace.  The pages describe
+ * no such call (there is no counterpart in them): it exists for callers that
+ * cannot allocate device memory where they run a layer — for instance a
+ * plugin inside a host framework whose allocator owns all device memory, or
+ * a service that allows no device allocation after start-up.
+ * Same arguments and results as bqe_moe_layer_forward, without ws/ws_bytes.
+ * The workspace is a fixed 8 MiB array in the library (one per device that
+ * loads it, kept until the process exits); a layer whose
+ * bqe_workspace_bytes(d, M) exceeds 8 MiB is rejected with BQE_ENOSPC (for
+ * the DeepSeek-V4.1-Flash shape that allows M <= 2).  Nothing is allocated:
+ * no cudaMalloc, no cudaFree.
+ *   - The first call on a device finds the array's address and zeroes it
+ *     (enqueued on `stream`); make that first call before any stream capture.
+ *   - Every call reuses the same array and clears its counters and error
+ *     word first, so calls whose GPU work overlaps (other streams, other
+ *     threads) race on it: order them.
+ *   - status_out: device, 2 int32 or NULL; receives the call's device error
+ *     word and detail (0 = ok, else a BQE_* code as bqe_check reports). */
+int bqe_moe_layer_forward_noalloc(const bqe_layer_desc* d, int32_t M, const uint16_t* x,
+                                  const float* router_w, const float* sel_bias,
+                                  const bqe_pool* pool, const int32_t* slot_table,
+                                  const int32_t* forced_idx, float* out, int32_t accumulate,
+                                  int32_t* topk_idx, float* topk_w, int32_t* status_out,
+                                  void* stream);
+
 /* Synchronise `stream`, read the workspace error word and clear it.
  * Returns BQE_OK, BQE_EDEVICE or BQE_ETIMEOUT (detail: optional host int,
  * receives the kernel's detail code), or BQE_ECUDA. */
