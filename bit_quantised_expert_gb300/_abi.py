@@ -66,6 +66,8 @@ SIGNATURES = {
     "bqe_experts_phase": (ctypes.c_int, [_DESC, _I32, _POOL, _P, _I32, _I32, _P, _U64, _P]),
     "bqe_moe_layer_forward_noalloc": (ctypes.c_int, [_DESC, _I32, _P, _P, _P, _POOL, _P, _P, _P, _I32, _P, _P, _P,
                                                      _P]),
+    "bqe_prefill_workspace_bytes": (_U64, [_DESC, _I32]),
+    "bqe_moe_prefill": (ctypes.c_int, [_DESC, _I32, _P, _P, _P, _POOL, _P, _P, _P, _I32, _P, _P, _P, _U64, _P]),
     "bqe_moe_step": (ctypes.c_int, [_DESC, _I32, _I32, _P, _P, _P, _POOL, _P, _P, _P, _P, _U64, _P]),
     "bqe_check": (ctypes.c_int, [_P, _P, ctypes.POINTER(_I32)]),
     "bqe_status_str": (ctypes.c_char_p, [ctypes.c_int]),
@@ -73,6 +75,7 @@ SIGNATURES = {
     "bqe_set_pdl": (None, [ctypes.c_int]),
     "bqe_set_test_drop_item": (None, [_I32]),
     "bqe_set_variant": (None, [_I32]),
+    "bqe_set_prefill_f16": (None, [_I32]),
     "bqe_set_diag": (None, [_I32]),
     "bqe_set_fused": (None, [_I32]),
     "bqe_diag_offset": (_U64, [_DESC, _I32]),
@@ -181,6 +184,18 @@ def bqe_moe_layer_forward_noalloc(d, M, x, router_w, sel_bias, pool: bqe_pool, s
                                           stream_ptr(stream)), "bqe_moe_layer_forward_noalloc")
 
 
+# ---------------------------------------------------------------- prefill
+def bqe_prefill_workspace_bytes(d, T: int) -> int:
+    return lib.bqe_prefill_workspace_bytes(ctypes.byref(d), T)
+
+
+def bqe_moe_prefill(d, T, x, router_w, sel_bias, pool: bqe_pool, slot_table, forced_idx, out, accumulate,
+                    topk_idx, topk_w, ws, ws_bytes, stream=None) -> None:
+    _ok(lib.bqe_moe_prefill(ctypes.byref(d), T, ptr(x), ptr(router_w), ptr(sel_bias), ctypes.byref(pool),
+                            ptr(slot_table), ptr(forced_idx), ptr(out), int(accumulate), ptr(topk_idx),
+                            ptr(topk_w), ptr(ws), ws_bytes, stream_ptr(stream)), "bqe_moe_prefill")
+
+
 def bqe_route(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, topk_idx, topk_w, ws, ws_bytes,
               stream=None) -> None:
     _ok(lib.bqe_route(ctypes.byref(d), M, ptr(x), ptr(router_w), ptr(sel_bias), ctypes.byref(pool),
@@ -238,3 +253,7 @@ def bqe_diag_offset(d, M: int) -> int:
 
 def bqe_set_fused(on: bool) -> None:
     lib.bqe_set_fused(1 if on else 0)
+
+
+def bqe_set_prefill_f16(on: bool) -> None:
+    lib.bqe_set_prefill_f16(1 if on else 0)

@@ -6,6 +6,7 @@
 #include <atomic>
 
 #include "bqe_internal.cuh"
+#include "bqe_prefill.cuh"
 
 using namespace bqe;
 
@@ -15,6 +16,7 @@ static std::atomic<int> g_drop_item{-1};
 static std::atomic<int> g_variant{1};
 static std::atomic<int> g_diag{0};
 static std::atomic<int> g_fused{0};
+static std::atomic<int> g_pf_f16{1};
 
 // Diagnostic knobs (not part of the operation): the bound on every in-kernel
 // wait, and whether kernels are chained with programmatic dependent launch.
@@ -24,6 +26,7 @@ extern "C" void bqe_set_test_drop_item(int32_t item) { g_drop_item = item; }
 extern "C" void bqe_set_variant(int32_t v) { g_variant = v; }
 extern "C" void bqe_set_diag(int32_t on) { g_diag = on ? 1 : 0; }
 extern "C" void bqe_set_fused(int32_t on) { g_fused = on ? 1 : 0; }
+extern "C" void bqe_set_prefill_f16(int32_t on) { g_pf_f16 = on ? 1 : 0; }
 
 static int device_sms() {
   static int cache[64] = {0};
@@ -222,6 +225,48 @@ extern "C" int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M
     if (rc) return rc;
   }
   return BQE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Prefill
+// ---------------------------------------------------------------------------
+static constexpr int32_t kPfMaxT = 1 << 20;
+
+extern "C" uint64_t bqe_prefill_workspace_bytes(const bqe_layer_desc* d, int32_t T) {
+  if (!desc_ok(d) || T < 1 || T > kPfMaxT) return 0;
+  return make_pf_ws(make_pf_geo(d->hidden, d->inter, d->n_experts, d->top_k, T)).total;
+}
+
+extern "C" int bqe_moe_prefill(const bqe_layer_desc* d, int32_t T, const uint16_t* x, const float* router_w,
+                               const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
+                               const int32_t* forced_idx, float* out, int32_t accumulate, int32_t* topk_idx,
+                               float* topk_w, void* ws, uint64_t ws_bytes, void* stream) {
+  if (!desc_ok(d) || T < 1 || T > kPfMaxT || !x || !router_w || !slot_table || !out || !ws) return BQE_EINVAL;
+  if (((uintptr_t)ws & 255) || ((uintptr_t)router_w & 15) || ((uintptr_t)x & 15) || ((uintptr_t)out & 15))
+    return BQE_EINVAL;
+  int rc = check_pool(pool);
+  if (rc) return rc;
+  PfParams P;
+  P.g = make_pf_geo(d->hidden, d->inter, d->n_experts, d->top_k, T);
+  P.L = make_pf_ws(P.g);
+  if (ws_bytes < P.L.total) return BQE_ENOSPC;
+  P.ws = (uint8_t*)ws;
+  P.x = x;
+  P.router_w = router_w;
+  P.bias = sel_bias;
+  P.forced = forced_idx;
+  P.slot_table = slot_table;
+  P.pool = *pool;
+  P.out = out;
+  P.accumulate = accumulate ? 1 : 0;
+  P.topk_idx = topk_idx;
+  P.topk_w = topk_w;
+  P.f16 = g_pf_f16.load();
+  P.limit_ns = g_wait_limit_ns.load();
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(P.ws + P.L.err, 0, 16, st) != cudaSuccess) return BQE_ECUDA;
+  if (cudaMemsetAsync(P.ws + P.L.cnt, 0, 4ull * (P.g.E + 1), st) != cudaSuccess) return BQE_ECUDA;
+  return launch_prefill(P, st);
 }
 
 extern "C" int bqe_check(void* ws, void* stream, int32_t* detail) {

@@ -1,0 +1,951 @@
+// bqe_prefill.cu — the prefill path: one MoE layer over T token rows.
+//
+//   1. k_pf_logits   z = x Wr^T in fp32 (tiled SIMT GEMM; the top-k needs
+//                    fp32 logits, as in decode)
+//   2. k_pf_select   per token: sigmoid scores, biased top-k (ties to the lower
+//                    expert id) or the forced choice, mixing weights, counts
+//   3. k_pf_plan     per expert: validated slot, row range padded to 16, tiles
+//   4. k_pf_fill     per expert: its (token, choice) pairs in token order
+//   5. k_pf_gather   x rows, scaled per token by 2^s, copied into expert-grouped
+//                    swizzled 16-bit tiles
+//   6. k_pf_gemm<0>  per (expert tile, 64 features): gate and up rows of W1/W3
+//                    dequantised in shared memory, tcgen05 MMA into tensor
+//                    memory, h 2^s = silu(gate) * up 2^s written as 16-bit tiles
+//   7. k_pf_gemm<1>  per (expert tile, 128 outputs): W2 the same way,
+//                    y = w 2^-s (W2 h 2^s)
+//   8. k_pf_combine  out[t] = y_shared + sum_j y_j in a fixed order
+//
+// Prefill only regroups the tokens of a layer by expert: the result per token
+// is the decode layer's (the Strata 4090 post, section 5.3, requires prefill
+// accelerations to leave results unchanged); the 16-bit operands of the tensor
+// cores are the only difference (section 4 of the same post: tensor-core
+// experts for prefill).  Operand type: fp16 by default.  x is exact in it once
+// scaled by a power of two per token (max |x 2^s| in [1, 2)); TQ1 weights d t
+// are exact, Q2_0 and Q3_K weights rounded to 11 bits; h carries the same
+// per-token scale so it stays in range.  MXFP4 experts use bf16 (E2M1 times
+// 2^(E-127) is exact there for every E).  bf16 for every expert is selectable.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "bqe_gemv.cuh"
+#include "bqe_prefill.cuh"
+#include "bqe_umma.cuh"
+
+namespace bqe {
+
+enum { kErrPfProducer = 7, kErrPfDequant = 8, kErrPfMma = 9, kErrPfEpilogue = 10, kErrPfRange = 11 };
+
+// ----------------------------------------------------------------------------
+// 1. Router logits: z (T x E) = x (T x H, bf16) . Wr (E x H, fp32)^T, fp32.
+// Tile 128 tokens x 64 experts x 32 columns, 256 threads, 8 x 4 per thread.
+// ----------------------------------------------------------------------------
+constexpr int kLgBM = 128, kLgBN = 64, kLgBK = 32;
+
+__global__ void __launch_bounds__(256) k_pf_logits(const uint16_t* __restrict__ x, const float* __restrict__ wr,
+                                                   float* __restrict__ z, int T, int E, int H) {
+  __shared__ __align__(16) float As[kLgBK][kLgBM];
+  __shared__ __align__(16) float Bs[kLgBK][kLgBN];
+  const int tid = threadIdx.x;
+  const int t0 = blockIdx.y * kLgBM, e0 = blockIdx.x * kLgBN;
+  const int ty = tid / 16, tx = tid % 16;
+  // loader mapping: A: token tid % 128, columns (tid / 128) * 16 .. +15;
+  //                 B: expert tid % 64, columns (tid / 64) * 8 .. +7
+  const int la_t = tid % kLgBM, la_k = (tid / kLgBM) * 16;
+  const int lb_e = tid % kLgBN, lb_k = (tid / kLgBN) * 8;
+  const bool a_ok = t0 + la_t < T, b_ok = e0 + lb_e < E;
+  const uint16_t* ap = x + (int64_t)(a_ok ? t0 + la_t : 0) * H + la_k;
+  const float* bp = wr + (int64_t)(b_ok ? e0 + lb_e : 0) * H + lb_k;
+  float acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  uint4 ra0 = make_uint4(0, 0, 0, 0), ra1 = ra0;
+  float4 rb0 = make_float4(0.f, 0.f, 0.f, 0.f), rb1 = rb0;
+  auto load = [&](int k0) {
+    if (a_ok) {
+      ra0 = *reinterpret_cast<const uint4*>(ap + k0);
+      ra1 = *reinterpret_cast<const uint4*>(ap + k0 + 8);
+    }
+    if (b_ok) {
+      rb0 = *reinterpret_cast<const float4*>(bp + k0);
+      rb1 = *reinterpret_cast<const float4*>(bp + k0 + 4);
+    }
+  };
+  auto bf = [](uint32_t w, int hi) { return __uint_as_float(hi ? (w & 0xFFFF0000u) : (w << 16)); };
+  load(0);
+  for (int k0 = 0; k0 < H; k0 += kLgBK) {
+    const uint32_t aw[8] = {ra0.x, ra0.y, ra0.z, ra0.w, ra1.x, ra1.y, ra1.z, ra1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      As[la_k + 2 * i][la_t] = bf(aw[i], 0);
+      As[la_k + 2 * i + 1][la_t] = bf(aw[i], 1);
+    }
+    Bs[lb_k + 0][lb_e] = rb0.x; Bs[lb_k + 1][lb_e] = rb0.y; Bs[lb_k + 2][lb_e] = rb0.z; Bs[lb_k + 3][lb_e] = rb0.w;
+    Bs[lb_k + 4][lb_e] = rb1.x; Bs[lb_k + 5][lb_e] = rb1.y; Bs[lb_k + 6][lb_e] = rb1.z; Bs[lb_k + 7][lb_e] = rb1.w;
+    __syncthreads();
+    if (k0 + kLgBK < H) load(k0 + kLgBK);
+#pragma unroll 8
+    for (int k = 0; k < kLgBK; ++k) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[k][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[k][ty * 8 + 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[k][tx * 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + ty * 8 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) z[(int64_t)t * E + e] = acc[i][j];
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// 2. Selection, one warp per token.  Order: larger key s + b first, ties to
+// the lower expert id (keys compared through an order-preserving uint image);
+// weights w_j = s_j / sum s from the unbiased scores in the log domain (finite
+// when every selected sigmoid underflows).
+// ----------------------------------------------------------------------------
+constexpr int kSelPerLane = 16;  // E <= 512
+
+__global__ void __launch_bounds__(256) k_pf_select(PfParams P) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int E = P.g.E, K = P.g.K, T = P.g.T;
+  if (t >= T) return;
+  const float* z = (const float*)(P.ws + P.L.z) + (int64_t)t * E;
+  int32_t* idx = (int32_t*)(P.ws + P.L.idx) + (int64_t)t * K;
+  float* wout = (float*)(P.ws + P.L.w) + (int64_t)t * K;
+  int32_t* cnt = (int32_t*)(P.ws + P.L.cnt);
+  int32_t* err = (int32_t*)(P.ws + P.L.err);
+  auto ord = [](float f) -> uint32_t {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  };
+  {
+    // per-token power of two: max |x_t| 2^s in [1, 2) (the magnitude bits of a
+    // bf16 order like its value, so an integer max finds the largest |x|)
+    const uint4* xr = reinterpret_cast<const uint4*>(P.x + (int64_t)t * P.g.H);
+    uint32_t mx = 0;
+    for (int i = lane; i < P.g.H / 8; i += 32) {
+      const uint4 v = xr[i];
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mx = max(mx, max(wv[k] & 0x7FFFu, (wv[k] >> 16) & 0x7FFFu));
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    const int ex = (int)(mx >> 7);
+    const int sh = ex == 0 ? 0 : min(max(127 - ex, -126), 126);
+    if (lane == 0) ((float*)(P.ws + P.L.tok_sc))[t] = __int_as_float((127 - sh) << 23);
+  }
+  int sel = -1;      // lane j < K: the j-th choice
+  float zsel = 0.f;
+  if (P.forced) {
+    if (lane < K) {
+      sel = P.forced[(int64_t)t * K + lane];
+      if (sel < 0 || sel >= E) {
+        set_error(err, BQE_EDEVICE, kErrForcedIdx);
+        sel = 0;
+      }
+      zsel = z[sel];
+    }
+  } else {
+    uint32_t key[kSelPerLane];
+#pragma unroll
+    for (int i = 0; i < kSelPerLane; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = 0u;  // 0: no expert (below every real key)
+      if (e < E) key[i] = ord(1.0f / (1.0f + expf(-z[e])) + (P.bias ? P.bias[e] : 0.f));
+    }
+    for (int j = 0; j < K; ++j) {
+      uint32_t lk = 0u;
+      int li = 0x7fffffff, lc = -1;
+#pragma unroll
+      for (int i = 0; i < kSelPerLane; ++i)
+        if (key[i] > lk) { lk = key[i]; li = lane + 32 * i; lc = i; }  // ascending e: ties keep the lower
+      const uint32_t wk = __reduce_max_sync(0xffffffffu, lk);
+      const int best = (int)__reduce_min_sync(0xffffffffu, (lk == wk && wk != 0u) ? (uint32_t)li : 0x7fffffffu);
+#pragma unroll
+      for (int i = 0; i < kSelPerLane; ++i)
+        if (i == lc && li == best) key[i] = 0u;
+      if (lane == j) { sel = best; zsel = z[best]; }
+    }
+  }
+  float ls = -INFINITY;
+  if (lane < K) ls = zsel < 0.f ? zsel - log1pf(expf(zsel)) : -log1pf(expf(-zsel));  // log sigmoid(z)
+  float mx = ls;
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float ev = lane < K ? expf(ls - mx) : 0.f;
+  float tot = ev;
+  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  if (lane < K) {
+    const float w = ev / tot;
+    idx[lane] = sel;
+    wout[lane] = w;
+    if (P.topk_idx) P.topk_idx[(int64_t)t * K + lane] = sel;
+    if (P.topk_w) P.topk_w[(int64_t)t * K + lane] = w;
+    atomicAdd(&cnt[sel], 1);
+  }
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x multiple of 32,
+// <= 1024); returns the exclusive prefix, *total the block sum.
+__device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  __syncthreads();
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int wv = lane < nw ? s_warp[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wv, o);
+      if (lane >= o) wv += n;
+    }
+    if (lane < nw) s_warp[lane] = wv;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int before = warp ? s_warp[warp - 1] : 0;
+  *total = s_warp[nw - 1];
+  return before + inc - v;
+}
+
+// ----------------------------------------------------------------------------
+// 3. Plan (one CTA of 1024 threads, one group per thread; group E is the
+// shared expert with all T rows).  Invalid slots raise BQE_EDEVICE and their
+// group is skipped.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) k_pf_plan(PfParams P) {
+  __shared__ int s_warp[32];
+  const int G = P.g.E + 1, T = P.g.T;
+  const int gi = threadIdx.x;
+  int32_t* cnt = (int32_t*)(P.ws + P.L.cnt);
+  int32_t* goff = (int32_t*)(P.ws + P.L.goff);
+  uint64_t* gaddr = (uint64_t*)(P.ws + P.L.gaddr);
+  int32_t* gfmt = (int32_t*)(P.ws + P.L.gfmt);
+  int32_t* gf16 = (int32_t*)(P.ws + P.L.gf16);
+  int32_t* ctr = (int32_t*)(P.ws + P.L.ctr);
+  int32_t* err = (int32_t*)(P.ws + P.L.err);
+  int3* tiles = (int3*)(P.ws + P.L.tile);
+  int n = 0, fmt = 0;
+  uint64_t addr = 0;
+  if (gi < G) {
+    n = gi < P.g.E ? cnt[gi] : T;
+    const int slot = P.slot_table[gi];
+    if (n > 0) {
+      int code = 0;
+      if (slot < 0 || slot >= P.pool.n_slots) {
+        code = kErrSlotRange;
+      } else {
+        fmt = P.pool.slot_fmt[slot];
+        const uint64_t off = P.pool.slot_off[slot];
+        if (!fmt_ok(fmt)) {
+          code = kErrSlotFmt;
+        } else {
+          const uint64_t bytes = 2 * matrix_bytes(fmt, P.g.I, P.g.H) + matrix_bytes(fmt, P.g.H, P.g.I);
+          if ((off & 15) || off + bytes > P.pool.base_bytes) code = kErrSlotExtent;
+          addr = (uint64_t)P.pool.base + off;
+        }
+      }
+      if (code) {
+        set_error(err, BQE_EDEVICE, code);
+        n = 0;
+        fmt = 0;
+      }
+    }
+    gaddr[gi] = addr;
+    gfmt[gi] = fmt;
+    gf16[gi] = P.f16 && fmt != BQE_FMT_MXFP4;
+    cnt[gi] = n;
+  }
+  const int padded = (n + kPfRowAlign - 1) / kPfRowAlign * kPfRowAlign;
+  const int ntile = (n + kPfTileN - 1) / kPfTileN;
+  int rows_total, tiles_total;
+  const int row0 = block_excl_scan(padded, s_warp, &rows_total);
+  const int tile0 = block_excl_scan(ntile, s_warp, &tiles_total);
+  if (gi < G) {
+    goff[gi] = row0;
+    for (int tt = 0; tt < ntile; ++tt)
+      tiles[tile0 + tt] = make_int3(gi, row0 + tt * kPfTileN, min(kPfTileN, n - tt * kPfTileN));
+  }
+  if (gi == 0) {
+    goff[G] = rows_total;
+    ctr[0] = tiles_total;
+    ctr[1] = rows_total;
+  }
+}
+
+// ----------------------------------------------------------------------------
+// 4. Fill: CTA g lists the (token, choice) pairs of expert g in token order
+// (the same order for every run), records each pair's grouped row and the
+// padding rows of its range.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_pf_fill(PfParams P) {
+  __shared__ int s_warp[32];
+  const int g = blockIdx.x, E = P.g.E, K = P.g.K, T = P.g.T;
+  const int32_t* cnt = (const int32_t*)(P.ws + P.L.cnt);
+  const int32_t* goff = (const int32_t*)(P.ws + P.L.goff);
+  const int32_t* gfmt = (const int32_t*)(P.ws + P.L.gfmt);
+  const int32_t* idx = (const int32_t*)(P.ws + P.L.idx);
+  const float* wsel = (const float*)(P.ws + P.L.w);
+  int32_t* prow_tok = (int32_t*)(P.ws + P.L.prow_tok);
+  float* prow_w = (float*)(P.ws + P.L.prow_w);
+  float* prow_sc = (float*)(P.ws + P.L.prow_sc);
+  const float* tok_sc = (const float*)(P.ws + P.L.tok_sc);
+  int32_t* pos = (int32_t*)(P.ws + P.L.pos);
+  const bool valid = gfmt[g] != 0;
+  const int base = goff[g];
+  const int n = cnt[g];
+  if (g == E) {
+    for (int t = threadIdx.x; t < T; t += blockDim.x) {
+      pos[(int64_t)t * (K + 1) + K] = valid ? base + t : -1;
+      if (valid) {
+        prow_tok[base + t] = t;
+        prow_w[base + t] = 1.0f;
+        prow_sc[base + t] = tok_sc[t];
+      }
+    }
+  } else {
+    int running = 0;
+    for (int t0 = 0; t0 < T; t0 += blockDim.x) {
+      const int t = t0 + threadIdx.x;
+      int c = 0;
+      if (t < T)
+        for (int j = 0; j < K; ++j) c += idx[(int64_t)t * K + j] == g;
+      int total;
+      const int ex = block_excl_scan(c, s_warp, &total);
+      if (c) {
+        int r = base + running + ex;
+        for (int j = 0; j < K; ++j)
+          if (idx[(int64_t)t * K + j] == g) {
+            pos[(int64_t)t * (K + 1) + j] = valid ? r : -1;
+            if (valid) {
+              prow_tok[r] = t;
+              prow_w[r] = wsel[(int64_t)t * K + j];
+              prow_sc[r] = tok_sc[t];
+            }
+            ++r;
+          }
+      }
+      running += total;
+    }
+  }
+  if (valid) {
+    const int padded = (n + kPfRowAlign - 1) / kPfRowAlign * kPfRowAlign;
+    for (int r = n + threadIdx.x; r < padded; r += blockDim.x) {
+      prow_tok[base + r] = -1;
+      prow_w[base + r] = 0.f;
+      prow_sc[base + r] = 1.f;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// 5. Gather, one CTA per tile: grouped row p gets x[prow_tok[p]] 2^s (zeros
+// for padding) in the tile's operand type, stored as K-step-major tiles: 64
+// columns x 8 rows = one 1024-byte swizzled atom at ((ks R/8) + p/8) 1024, so
+// one contiguous copy brings the 64 columns of any run of rows into shared
+// memory in the layout the tensor core reads.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_pf_gather(PfParams P) {
+  const int tile = blockIdx.x;
+  if (tile >= ((const int32_t*)(P.ws + P.L.ctr))[0]) return;
+  const int3 tl = ((const int3*)(P.ws + P.L.tile))[tile];
+  const bool f16 = ((const int32_t*)(P.ws + P.L.gf16))[tl.x] != 0;
+  const int npad = (tl.z + 15) & ~15;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int H = P.g.H;
+  const int64_t R8 = P.g.R / 8;
+  uint8_t* xp = P.ws + P.L.xp;
+  for (int r = warp; r < npad; r += 8) {
+    const int p = tl.y + r;
+    const int tok = ((const int32_t*)(P.ws + P.L.prow_tok))[p];
+    const float scale = 1.0f / ((const float*)(P.ws + P.L.prow_sc))[p];  // 2^s, exact
+    const uint4* src = reinterpret_cast<const uint4*>(P.x + (int64_t)(tok < 0 ? 0 : tok) * H);
+    for (int i = lane; i < H / 8; i += 32) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (tok >= 0) {
+        const uint4 b = src[i];
+        uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float lo = __uint_as_float(w[k] << 16) * scale, hi = __uint_as_float(w[k] & 0xFFFF0000u) * scale;
+          if (f16) {
+            const __half2 h2 = __floats2half2_rn(lo, hi);
+            w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+          } else {
+            w[k] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);  // exact: scaled bf16
+          }
+        }
+        v = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      const int ks = i >> 3, c = i & 7;
+      *reinterpret_cast<uint4*>(xp + ((int64_t)ks * R8 + (p >> 3)) * 1024 + sw128_offset(p & 7, c)) = v;
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// 6/7. Grouped GEMM on the tensor cores.
+//
+// Work item = (tile, block): tile = up to 256 grouped rows of one expert,
+// block = 128 weight rows (phase 0: 64 rows of W1 and the same 64 rows of W3;
+// phase 1: 128 rows of W2).  D (128 weight rows x N tokens, fp32) lives in
+// tensor memory, two accumulators so the epilogue of one item overlaps the
+// main loop of the next.  Per 64-column K-step the A operand (weights) is
+// dequantised by warps 0-3 (one 32-row panel each, one row per lane) from a
+// ring of raw quantised 256-column groups, and the B operand (tokens) arrives
+// by one bulk copy of the pre-swizzled grouped rows.
+// ----------------------------------------------------------------------------
+// Two fp32 values -> one 32-bit pair of the operand type (round to nearest
+// even; the first value in the low half).
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if (F16) {
+    const __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  } else {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+}
+constexpr float kF16Max = 65504.f;
+
+// Raw 256-column group of one 32-row panel: the pieces of the device tile
+// layout that hold these columns, packed as [codes | small fields].
+__device__ __forceinline__ void issue_raw_group(int fmt, const uint8_t* tile, int nb, int gi, uint8_t* dst,
+                                                uint64_t* bar) {
+  switch (fmt) {
+    case BQE_FMT_Q2_0:
+      bulk_g2s(dst, tile + gi * 2048, 2048, bar);
+      bulk_g2s(dst + 2048, tile + nb * 512 + gi * 256, 256, bar);
+      break;
+    case BQE_FMT_MXFP4:
+      bulk_g2s(dst, tile + gi * 4096, 4096, bar);
+      bulk_g2s(dst + 4096, tile + nb * 512 + gi * 256, 256, bar);
+      break;
+    case BQE_FMT_TQ1:
+      bulk_g2s(dst, tile + gi * 1536, 1536, bar);
+      bulk_g2s(dst + 1536, tile + nb * 1536 + gi * 256, 256, bar);
+      break;
+    default:  // Q3_K
+      bulk_g2s(dst, tile + gi * 2048, 2048, bar);
+      bulk_g2s(dst + 2048, tile + nb * 2048 + gi * 1024, 1024, bar);
+      bulk_g2s(dst + 3072, tile + nb * 3072 + gi * 384, 384, bar);
+      bulk_g2s(dst + 3456, tile + nb * 3456 + gi * 64, 64, bar);
+      break;
+  }
+}
+__host__ __device__ constexpr uint32_t raw_group_bytes(int fmt) { return 32u * 256u / fmt_bw(fmt) * fmt_bb(fmt); }
+
+__device__ __forceinline__ void store_chunk(uint8_t* a_stage, int row, int c, uint32_t w0, uint32_t w1, uint32_t w2,
+                                            uint32_t w3) {
+  *reinterpret_cast<uint4*>(a_stage + sw128_offset(row, c)) = make_uint4(w0, w1, w2, w3);
+}
+
+// Q2_0, K-step kq = block kq of the group: w = d (2q - 3) = 8d (1 + q/4) - 11d,
+// one exact fp32 fma per weight (1 + q/4 built from the code bits).
+template <bool F16>
+__device__ __forceinline__ void dq_q2_0(const uint8_t* P, int kq, int lane, uint8_t* A, int row, bool& bad) {
+  const uint4 c4 = *reinterpret_cast<const uint4*>(P + kq * 512 + lane * 16);
+  const float d = __half2float(*reinterpret_cast<const __half*>(P + 2048 + (kq * 32 + lane) * 2));
+  const float a8 = 8.f * d, b11 = -11.f * d;
+  if (F16 && !(3.f * fabsf(d) <= kF16Max)) bad = true;
+  const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t word = wd[c >> 1];
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = 8 * (c & 1) + 2 * i;
+      const float f0 = __uint_as_float(0x3F800000u | (((word >> (2 * j)) & 3u) << 21));
+      const float f1 = __uint_as_float(0x3F800000u | (((word >> (2 * j + 2)) & 3u) << 21));
+      o[i] = pack2<F16>(fmaf(f0, a8, b11), fmaf(f1, a8, b11));
+    }
+    store_chunk(A, row, c, o[0], o[1], o[2], o[3]);
+  }
+}
+
+// MXFP4, K-step kq = blocks 2kq, 2kq+1: w = e2m1(code) * 2^(E-127), exact.
+__device__ __forceinline__ void dq_mxfp4(const uint8_t* P, int kq, int lane, uint8_t* A, int row) {  // bf16 only
+#pragma unroll
+  for (int bi = 0; bi < 2; ++bi) {
+    const int b = 2 * kq + bi;
+    const uint4 c4 = *reinterpret_cast<const uint4*>(P + b * 512 + lane * 16);
+    const float sc = ue8m0_f32(P[4096 + b * 32 + lane]);
+    const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {  // one word = 8 weights = one 16-byte chunk
+      uint32_t o[4];
+#pragma unroll
+      for (int by = 0; by < 4; ++by) {
+        const float2 v = e2m1x2_f32((wd[w] >> (8 * by)) & 0xFFu);
+        o[by] = pack2<false>(v.x * sc, v.y * sc);
+      }
+      store_chunk(A, row, bi * 4 + w, o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// TQ1, K-step KQ = weights 64 KQ .. 64 KQ + 63 of the 256-weight block.  Byte
+// i < 51 holds weights 5i .. 5i+4 as base-3 digits (least significant first,
+// digit = t + 1), byte 51 holds weight 255; w = d t.
+template <int KQ, bool F16>
+__device__ __forceinline__ void dq_tq1_k(const uint32_t (&W)[14], float d, uint8_t* A, int row) {
+  constexpr int J0 = 64 * KQ;
+  constexpr int B0 = J0 / 5;
+  constexpr int B1 = (J0 + 63) / 5 < 51 ? (J0 + 63) / 5 : 51;
+  float t[(B1 - B0 + 1) * 5];
+#pragma unroll
+  for (int i = B0; i <= B1; ++i) {
+    uint32_t v = (W[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+    if (i == 51) {
+      t[(i - B0) * 5] = (float)((int)(v % 3u) - 1);
+    } else {
+#pragma unroll
+      for (int r = 0; r < 5; ++r) {
+        const uint32_t q = (v * 171u) >> 9;  // v / 3 for v <= 255
+        t[(i - B0) * 5 + r] = (float)((int)(v - 3u * q) - 1);
+        v = q;
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = J0 + 8 * c + 2 * i - 5 * B0;
+      o[i] = pack2<F16>(d * t[j], d * t[j + 1]);
+    }
+    store_chunk(A, row, c, o[0], o[1], o[2], o[3]);
+  }
+}
+template <bool F16>
+__device__ __forceinline__ void dq_tq1(const uint8_t* P, int kq, int lane, uint8_t* A, int row) {
+  uint32_t W[14];
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    const uint4 v = *reinterpret_cast<const uint4*>(P + q * 512 + lane * 16);
+    W[4 * q] = v.x; W[4 * q + 1] = v.y; W[4 * q + 2] = v.z; W[4 * q + 3] = v.w;
+  }
+  const uint2 tail = *reinterpret_cast<const uint2*>(P + 1536 + lane * 8);
+  W[12] = tail.x;
+  W[13] = tail.y;
+  const float d = __half2float(__ushort_as_half((unsigned short)(tail.y & 0xFFFFu)));
+  switch (kq) {
+    case 0: dq_tq1_k<0, F16>(W, d, A, row); break;
+    case 1: dq_tq1_k<1, F16>(W, d, A, row); break;
+    case 2: dq_tq1_k<2, F16>(W, d, A, row); break;
+    default: dq_tq1_k<3, F16>(W, d, A, row); break;
+  }
+}
+
+// Q3_K, K-step kq = weights 64 kq .. 64 kq + 63: q = lo2 + 4 hi1, w = d s_j (q - 4)
+// with j = weight / 16; as d s (8 (1 + q/8) - 12), one exact fp32 fma.
+template <bool F16>
+__device__ __forceinline__ void dq_q3k(const uint8_t* P, int kq, int lane, uint8_t* A, int row, bool& bad) {
+  const uint4 lo4 = *reinterpret_cast<const uint4*>(P + kq * 512 + lane * 16);
+  const uint2 hi2 = *reinterpret_cast<const uint2*>(P + 2048 + (kq >> 1) * 512 + lane * 16 + (kq & 1) * 8);
+  const uint32_t* scw = reinterpret_cast<const uint32_t*>(P + 3072 + lane * 12);
+  const uint32_t sc[4] = {scw[0], scw[1], scw[2], 0u};
+  const float d = __half2float(*reinterpret_cast<const __half*>(P + 3456 + lane * 2));
+  const uint32_t lo[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
+  const uint32_t hi[2] = {hi2.x, hi2.y};
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {  // sub-block 4 kq + m: weights 16 m .. 16 m + 15 of this K-step
+    const int bit = 6 * (4 * kq + m);
+    const uint64_t two = (uint64_t)sc[bit >> 5] | ((uint64_t)sc[(bit >> 5) + 1] << 32);
+    const float ds = d * (float)((uint32_t)(two >> (bit & 31)) & 63u);
+    const float a8 = 8.f * ds, b12 = -12.f * ds;
+    if (F16 && !(4.f * fabsf(ds) <= kF16Max)) bad = true;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {  // 8 weights = one chunk
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float v[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = 16 * m + 8 * half + 2 * i + e;  // weight within the K-step
+          const uint32_t q = ((lo[j >> 4] >> (2 * (j & 15))) & 3u) | (((hi[j >> 5] >> (j & 31)) & 1u) << 2);
+          v[e] = fmaf(__uint_as_float(0x3F800000u | (q << 20)), a8, b12);
+        }
+        o[i] = pack2<F16>(v[0], v[1]);
+      }
+      store_chunk(A, row, 2 * m + half, o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// One 64-column K-step of the lane's row, as fp16 (f16) or bf16.  `bad` is set
+// when an fp16 weight would leave the fp16 range.
+__device__ __forceinline__ void dequant_kstep(int fmt, bool f16, const uint8_t* P, int kq, int lane, uint8_t* A,
+                                              int row, bool& bad) {
+  switch (fmt) {
+    case BQE_FMT_Q2_0:
+      if (f16) dq_q2_0<true>(P, kq, lane, A, row, bad); else dq_q2_0<false>(P, kq, lane, A, row, bad);
+      break;
+    case BQE_FMT_MXFP4: dq_mxfp4(P, kq, lane, A, row); break;
+    case BQE_FMT_TQ1:
+      if (f16) dq_tq1<true>(P, kq, lane, A, row); else dq_tq1<false>(P, kq, lane, A, row);
+      break;
+    default:
+      if (f16) dq_q3k<true>(P, kq, lane, A, row, bad); else dq_q3k<false>(P, kq, lane, A, row, bad);
+      break;
+  }
+}
+
+struct PfItem {
+  int g, row0, n, npad, blk, fmt;
+  bool f16;             // operand type of this expert: fp16 (else bf16)
+  const uint8_t* base;  // slot
+};
+
+__device__ __forceinline__ PfItem pf_item(const PfParams& P, int item, int nblk) {
+  PfItem it;
+  const int3 tl = ((const int3*)(P.ws + P.L.tile))[item / nblk];
+  it.g = tl.x;
+  it.row0 = tl.y;
+  it.n = tl.z;
+  it.npad = (tl.z + 15) & ~15;
+  it.blk = item % nblk;
+  it.fmt = ((const int32_t*)(P.ws + P.L.gfmt))[tl.x];
+  it.f16 = ((const int32_t*)(P.ws + P.L.gf16))[tl.x] != 0;
+  it.base = (const uint8_t*)((const uint64_t*)(P.ws + P.L.gaddr))[tl.x];
+  return it;
+}
+
+template <int PH>
+__global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
+  extern __shared__ uint8_t pf_smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)pf_smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = sm + kPfOffA;
+  uint8_t* sB = sm + kPfOffB;
+  uint8_t* sRaw = sm + kPfOffRaw;
+  float* sEpi = (float*)(sm + kPfOffEpi);
+  uint64_t* bars = (uint64_t*)(sm + kPfOffBar);
+  uint64_t* raw_full = bars;                        // [kPfRawStages]
+  uint64_t* raw_empty = bars + kPfRawStages;        // [kPfRawStages]
+  uint64_t* a_full = bars + 2 * kPfRawStages;       // [kPfStages]
+  uint64_t* b_full = a_full + kPfStages;            // [kPfStages]
+  uint64_t* st_empty = b_full + kPfStages;          // [kPfStages]
+  uint64_t* acc_full = st_empty + kPfStages;        // [2]
+  uint64_t* acc_empty = acc_full + 2;               // [2]
+  uint64_t* fin = acc_empty + 2;
+  uint32_t* s_tmem = (uint32_t*)(fin + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const PfGeo& g = P.g;
+  const int Kc = PH == 0 ? g.H : g.I;  // contraction length
+  const int ngrp = Kc / 256;
+  const int kc = chunk_cols(Kc), nch = Kc / kc, gpc = kc / 256;
+  const int nblk = PH == 0 ? g.nblkA : g.nblkB;
+  const int64_t R8 = g.R / 8;
+  const int nitems = ((const int32_t*)(P.ws + P.L.ctr))[0] * nblk;
+  int32_t* err = (int32_t*)(P.ws + P.L.err);
+  const uint64_t lim = P.limit_ns;
+
+  if (tid == 0) {
+    for (int i = 0; i < kPfRawStages; ++i) { mbar_init(&raw_full[i], 1); mbar_init(&raw_empty[i], 4); }
+    for (int i = 0; i < kPfStages; ++i) {
+      mbar_init(&a_full[i], 4);
+      mbar_init(&b_full[i], 1);
+      mbar_init(&st_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
+    mbar_init(fin, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(s_tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == 4) {
+    // ---------------- loads: raw weight groups and B tiles ----------------
+    if (lane == 0) {
+      const uint8_t* bsrc = P.ws + (PH == 0 ? P.L.xp : P.L.hp);
+      int rs = 0, s = 0;
+      uint32_t rph = 0, sph = 0;
+      uint32_t raw_par[kPfRawStages], b_par[kPfStages];
+      bool raw_armed[kPfRawStages] = {}, b_armed[kPfStages] = {};
+      bool ok = true;
+      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
+        const PfItem it = pf_item(P, item, nblk);
+        const int fmt = it.fmt;
+        const uint64_t m13 = matrix_bytes(fmt, g.I, g.H);
+        const uint32_t tb = tile_bytes(fmt, kc);
+        const int nb = kc / fmt_bw(fmt);
+        const uint8_t* mat[4];
+        int panel[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          if (PH == 0) {
+            mat[w] = it.base + (w < 2 ? 0 : m13);
+            panel[w] = 2 * it.blk + (w & 1);
+          } else {
+            mat[w] = it.base + 2 * m13;
+            panel[w] = 4 * it.blk + w;
+          }
+        }
+        const uint32_t bbytes = (uint32_t)it.npad * 128u;
+        for (int grp = 0; grp < ngrp && ok; ++grp) {
+          const int c = grp / gpc, gi = grp % gpc;
+          if (!mbar_wait_bounded(&raw_empty[rs], rph ^ 1, lim)) { ok = false; break; }
+          mbar_arrive_expect_tx(&raw_full[rs], 4 * raw_group_bytes(fmt));
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            issue_raw_group(fmt, mat[w] + ((uint64_t)panel[w] * nch + c) * tb, nb, gi,
+                            sRaw + rs * kPfRawStage + w * kPfRawPanel, &raw_full[rs]);
+          raw_par[rs] = rph;
+          raw_armed[rs] = true;
+          if (++rs == kPfRawStages) { rs = 0; rph ^= 1; }
+          for (int kq = 0; kq < 4; ++kq) {
+            const int ks = grp * 4 + kq;
+            if (!mbar_wait_bounded(&st_empty[s], sph ^ 1, lim)) { ok = false; break; }
+            mbar_arrive_expect_tx(&b_full[s], bbytes);
+            bulk_g2s(sB + s * kPfBStage, bsrc + ((uint64_t)ks * R8 + (it.row0 >> 3)) * 1024, bbytes, &b_full[s]);
+            b_par[s] = sph;
+            b_armed[s] = true;
+            if (++s == kPfStages) { s = 0; sph ^= 1; }
+          }
+        }
+      }
+      if (!ok) set_error(err, BQE_ETIMEOUT, kErrPfProducer);
+      // every copy this thread started has landed before the CTA may exit
+      for (int i = 0; i < kPfRawStages; ++i)
+        if (raw_armed[i]) mbar_wait_bounded(&raw_full[i], raw_par[i], lim);
+      for (int i = 0; i < kPfStages; ++i)
+        if (b_armed[i]) mbar_wait_bounded(&b_full[i], b_par[i], lim);
+    }
+  } else if (warp < 4) {
+    // ---------------- dequant: A rows 32 warp .. 32 warp + 31 ----------------
+    int rs = 0, s = 0;
+    uint32_t rph = 0, sph = 0;
+    bool ok = true, bad = false;
+    const int row = warp * 32 + lane;
+    for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
+      const PfItem it = pf_item(P, item, nblk);
+      for (int grp = 0; grp < ngrp && ok; ++grp) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&raw_full[rs], rph, lim))) { ok = false; break; }
+        const uint8_t* praw = sRaw + rs * kPfRawStage + warp * kPfRawPanel;
+        for (int kq = 0; kq < 4; ++kq) {
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&st_empty[s], sph ^ 1, lim))) { ok = false; break; }
+          dequant_kstep(it.fmt, it.f16, praw, kq, lane, sA + s * kPfAStage, row, bad);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[s]);
+          if (++s == kPfStages) { s = 0; sph ^= 1; }
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&raw_empty[rs]);
+        if (++rs == kPfRawStages) { rs = 0; rph ^= 1; }
+      }
+    }
+    if (!ok && lane == 0) set_error(err, BQE_ETIMEOUT, kErrPfDequant);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, BQE_EUNSUPPORTED, kErrPfRange);
+  } else if (warp == 5) {
+    // ---------------- MMA issue (one thread) ----------------
+    if (lane == 0) {
+      int s = 0;
+      uint32_t sph = 0;
+      bool ok = true;
+      int lc = 0;
+      for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++lc) {
+        const PfItem it = pf_item(P, item, nblk);
+        const int ab = lc & 1;
+        const uint32_t aph = (lc >> 1) & 1;
+        if (!mbar_wait_bounded(&acc_empty[ab], aph ^ 1, lim)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + ab * 256;
+        const uint32_t idesc = umma_idesc_f16(128, it.npad, !it.f16);
+        for (int ks = 0; ks < ngrp * 4; ++ks) {
+          if (!mbar_wait_bounded(&a_full[s], sph, lim) || !mbar_wait_bounded(&b_full[s], sph, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t da = umma_desc_sw128(sA + s * kPfAStage);
+          const uint64_t db = umma_desc_sw128(sB + s * kPfBStage);
+#pragma unroll
+          for (int k16 = 0; k16 < 4; ++k16) umma_bf16(d, da + 2 * k16, db + 2 * k16, idesc, (ks | k16) != 0);
+          umma_commit(&st_empty[s]);
+          if (++s == kPfStages) { s = 0; sph ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[ab]);
+      }
+      if (!ok) set_error(err, BQE_ETIMEOUT, kErrPfMma);
+      // all MMAs issued by this thread are complete before tensor memory is freed
+      umma_commit(fin);
+      mbar_wait_bounded(fin, 0, lim);
+    }
+  } else {
+    // ---------------- epilogue: warps 6-9, lane quarter warp % 4 ----------------
+    const int q = warp & 3;
+    const int et = tid - 6 * 32;  // 0..127
+    bool ok = true;
+    int lc = 0;
+    for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++lc) {
+      const PfItem it = pf_item(P, item, nblk);
+      const int ab = lc & 1;
+      const uint32_t aph = (lc >> 1) & 1;
+      const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[ab], aph, lim));
+      if (named_bar_or(1, 128, !got)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + ab * 256;
+      if (PH == 0) {
+        float* ubuf = sEpi;                                       // [64][17] up values
+        uint16_t* htile = (uint16_t*)(sEpi + 64 * 17);            // [16 tokens][64 features] 16-bit
+        uint8_t* hp = P.ws + P.L.hp;
+        const float* prow_sc = (const float*)(P.ws + P.L.prow_sc);
+        for (int c0 = 0; c0 < it.npad; c0 += 16) {
+          float v[16];
+          tmem_ld16(tq + c0, v);
+          const float scl = lane < 16 ? prow_sc[it.row0 + c0 + lane] : 1.f;  // 2^-s of the 16 tokens
+          if (q >= 2) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ubuf[((q - 2) * 32 + lane) * 17 + i] = v[i];
+          }
+          named_bar_sync(1, 128);
+          if (q < 2) {
+            // gate and up come scaled by 2^s (x was): h 2^s = silu(gate 2^s 2^-s) (up 2^s)
+            bool big = false;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float u = ubuf[(q * 32 + lane) * 17 + i];
+              const float hv = silu_f(v[i] * __shfl_sync(0xffffffffu, scl, i)) * u;
+              if (it.f16) {
+                big |= !(fabsf(hv) <= kF16Max);
+                htile[i * 64 + q * 32 + lane] = __half_as_ushort(__float2half_rn(hv));
+              } else {
+                htile[i * 64 + q * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+              }
+            }
+            if (__any_sync(0xffffffffu, big) && lane == 0) set_error(err, BQE_EUNSUPPORTED, kErrPfRange);
+          }
+          named_bar_sync(1, 128);
+          {
+            const int j = et >> 3, c = et & 7;
+            const int p = it.row0 + c0 + j;
+            const uint4 val = *reinterpret_cast<const uint4*>(htile + j * 64 + c * 8);
+            *reinterpret_cast<uint4*>(hp + ((int64_t)it.blk * R8 + (p >> 3)) * 1024 + sw128_offset(p & 7, c)) = val;
+          }
+          named_bar_sync(1, 128);
+        }
+      } else {
+        float* yb = sEpi + q * (16 * 33);
+        const float* prow_w = (const float*)(P.ws + P.L.prow_w);
+        const float* prow_sc = (const float*)(P.ws + P.L.prow_sc);
+        float* Y = (float*)(P.ws + P.L.y);
+        for (int c0 = 0; c0 < it.npad; c0 += 16) {
+          float v[16];
+          tmem_ld16(tq + c0, v);
+          // mixing weight times 2^-s: the accumulator holds 2^s y
+          const float wl = lane < 16 ? prow_w[it.row0 + c0 + lane] * prow_sc[it.row0 + c0 + lane] : 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) yb[i * 33 + lane] = v[i] * __shfl_sync(0xffffffffu, wl, i);
+          __syncwarp();
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int i = (lane >> 3) + 4 * r, c4 = (lane & 7) * 4;
+            if (c0 + i < it.n) {
+              const float4 val = make_float4(yb[i * 33 + c4], yb[i * 33 + c4 + 1], yb[i * 33 + c4 + 2],
+                                             yb[i * 33 + c4 + 3]);
+              *reinterpret_cast<float4*>(Y + (int64_t)(it.row0 + c0 + i) * g.H + it.blk * 128 + q * 32 + c4) = val;
+            }
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
+    }
+    if (!ok && et == 0) set_error(err, BQE_ETIMEOUT, kErrPfEpilogue);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// ----------------------------------------------------------------------------
+// 8. Combine, one CTA per token: out = y_shared + y_0 + ... + y_{K-1} (each y
+// already carries its mixing weight), added in this order.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_pf_combine(PfParams P) {
+  const int t = blockIdx.x, K = P.g.K, H = P.g.H;
+  const int32_t* pos = (const int32_t*)(P.ws + P.L.pos) + (int64_t)t * (K + 1);
+  const float* Y = (const float*)(P.ws + P.L.y);
+  __shared__ int s_pos[kMaxTopK + 1];
+  if (threadIdx.x <= K) s_pos[threadIdx.x] = pos[threadIdx.x == 0 ? K : threadIdx.x - 1];
+  __syncthreads();
+  float* o = P.out + (int64_t)t * H;
+  for (int c = threadIdx.x * 4; c < H; c += blockDim.x * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j <= K; ++j) {
+      const int p = s_pos[j];
+      if (p < 0) continue;
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(Y + (int64_t)p * H + c));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    if (P.accumulate) {
+      const float4 prev = *reinterpret_cast<const float4*>(o + c);
+      acc.x += prev.x; acc.y += prev.y; acc.z += prev.z; acc.w += prev.w;
+    }
+    *reinterpret_cast<float4*>(o + c) = acc;
+  }
+}
+
+// ----------------------------------------------------------------------------
+int launch_prefill(const PfParams& P, cudaStream_t st) {
+  static int s_attr_done[64] = {};
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BQE_ECUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BQE_ECUDA;
+  if (!s_attr_done[dev]) {
+    if (cudaFuncSetAttribute(k_pf_gemm<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPfSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_pf_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPfSmemBytes) !=
+            cudaSuccess)
+      return BQE_ECUDA;
+    s_attr_done[dev] = 1;
+  }
+  const PfGeo& g = P.g;
+  dim3 lg((g.E + kLgBN - 1) / kLgBN, (g.T + kLgBM - 1) / kLgBM);
+  k_pf_logits<<<lg, 256, 0, st>>>(P.x, P.router_w, (float*)(P.ws + P.L.z), g.T, g.E, g.H);
+  k_pf_select<<<(g.T + 7) / 8, 256, 0, st>>>(P);
+  k_pf_plan<<<1, 1024, 0, st>>>(P);
+  k_pf_fill<<<g.E + 1, 256, 0, st>>>(P);
+  k_pf_gather<<<g.maxTiles, 256, 0, st>>>(P);
+  k_pf_gemm<0><<<sms, kPfThreads, kPfSmemBytes, st>>>(P);
+  k_pf_gemm<1><<<sms, kPfThreads, kPfSmemBytes, st>>>(P);
+  k_pf_combine<<<g.T, 256, 0, st>>>(P);
+  return cudaGetLastError() == cudaSuccess ? BQE_OK : BQE_ECUDA;
+}
+
+}  // namespace bqe

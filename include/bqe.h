@@ -189,6 +189,48 @@ int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M, float* re
                  const int32_t* slot_tables, const int32_t* forced_idx, uint16_t* t_out,
                  void* ws, uint64_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Prefill: one MoE layer over T token rows at once (large T; Strata 4090
+ * post, section 4: tensor-core experts for prefill; section 5.3: prefill
+ * accelerations must leave the per-token result unchanged).  The result per
+ * token is that of bqe_moe_layer_forward: router logits in fp32, the same
+ * selection rule and mixing weights, the shared expert on every row.  The
+ * tokens are regrouped by expert and each expert's W1/W3 and W2 run as grouped
+ * GEMMs on the tensor cores, with the weights dequantised in shared memory to
+ * a 16-bit float type and h = silu(W1 x) * (W3 x) rounded to it before W2;
+ * products are accumulated in fp32.  The type is fp16 by default (see
+ * bqe_set_prefill_f16): x scaled per token by a power of two is exact in it,
+ * TQ1 weights are exact, Q2_0 / Q3_K weights keep 11 significant bits, h keeps
+ * the token's scale; MXFP4 experts use bf16 (exact for every scale).  A call
+ * whose fp16 weights or h would leave the fp16 range reports BQE_EUNSUPPORTED
+ * through bqe_check (detail 11).
+ *
+ * bqe_prefill_workspace_bytes(d, T): bytes of device workspace for T rows
+ * (about 4 (K + 1) T hidden x 1.6 bytes: the expert-grouped copies of x, h and
+ * the per-expert outputs), 0 if the shape is unsupported (same layer rules as
+ * decode; 1 <= T <= 1048576).
+ *
+ * bqe_moe_prefill: same arguments as bqe_moe_layer_forward with M = T.
+ *   x           device, T x hidden bf16 (16-byte aligned)
+ *   router_w    device, n_experts x hidden fp32 (16-byte aligned)
+ *   sel_bias    device, n_experts fp32 or NULL (selection only)
+ *   pool        slot pool; slot_table device, n_experts + 1 int32 (last: shared)
+ *   forced_idx  device, T x top_k int32 or NULL (selection given; weights still
+ *               from the scores)
+ *   out         device, T x hidden fp32 (16-byte aligned); accumulate = 1 adds
+ *   topk_idx / topk_w  device, T x top_k, or NULL
+ *   ws          device, 256-byte aligned, >= bqe_prefill_workspace_bytes; its
+ *               contents need no initialisation (the call clears what it needs)
+ * Enqueues 8 kernels on `stream` and returns without waiting.  Device-side
+ * problems (bad slot, forced index out of range, a wait past its limit) are
+ * reported through bqe_check(ws, ...) like the decode calls; the output of
+ * such a call is undefined. */
+uint64_t bqe_prefill_workspace_bytes(const bqe_layer_desc* d, int32_t T);
+int bqe_moe_prefill(const bqe_layer_desc* d, int32_t T, const uint16_t* x, const float* router_w,
+                    const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
+                    const int32_t* forced_idx, float* out, int32_t accumulate, int32_t* topk_idx,
+                    float* topk_w, void* ws, uint64_t ws_bytes, void* stream);
+
 /* The decode layer without a caller-provided workspace.  The pages describe
  * no such call (there is no counterpart in them): it exists for callers that
  * cannot allocate device memory where they run a layer — for instance a
@@ -260,6 +302,13 @@ void bqe_set_diag(int32_t on);
  * cooperatively launched persistent kernel (on = 1).  Same results up to the
  * order of the fp32 additions inside the router. */
 void bqe_set_fused(int32_t on);
+
+/* Operand type of the prefill tensor-core GEMMs: 1 (default) fp16 with the
+ * per-token power-of-two scaling described at bqe_moe_prefill, MXFP4 experts
+ * in bf16; 0: bf16 for every expert (weights and h rounded to 8 significant
+ * bits: relative L2 error about 3e-3 against exact arithmetic, against about
+ * 4e-4 for fp16).  Both run at the same tensor-core rate. */
+void bqe_set_prefill_f16(int32_t on);
 uint64_t bqe_diag_offset(const bqe_layer_desc* d, int32_t M);
 
 #ifdef __cplusplus

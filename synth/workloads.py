@@ -171,3 +171,36 @@ class LayerSet:
 
     def expert_bytes(self, inst, e):
         return expert_bytes(int(self.fmts[self.slot(inst, e)]), H, I)
+
+
+class Prefill:
+    """One mixed-format layer (as mixed_layer) over T token rows: x bf16
+    N(0, 1) and a forced Zipf(s) routing, expert perm[r] having rank r (with
+    T = 8192, s = 0.8: about 128 rows per expert on average, a few thousand on
+    the most popular one).  The selection bias N(0, 0.25) is passed but has no
+    effect under forced routing."""
+
+    def __init__(self, device, seed=5, T=8192, zipf_s=0.8, n_experts=E):
+        import torch
+        lay = mixed_layer(device, seed=seed, m=1, n_x=1, n_experts=n_experts)
+        self.layer, self.T, self.E = lay, T, n_experts
+        self.d, self.pool, self.wr, self.bias, self.table, self.fmts = (lay.d, lay.pool, lay.wr, lay.bias,
+                                                                         lay.table, lay.fmts)
+        rng = np.random.default_rng(seed * 13 + 1)
+        self.perm = rng.permutation(n_experts)
+        self.forced_np = zipf_forced_idx(rng, T, n_experts, K, zipf_s, self.perm)
+        self.forced = torch.from_numpy(self.forced_np).to(device)
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 7 + 3)
+        self.x = torch.randn(T, H, generator=g, device=device).to(torch.bfloat16).view(torch.int16).contiguous()
+
+    def canon(self, slot):
+        return self.layer.canon(slot)
+
+    def counts(self):
+        return np.bincount(self.forced_np.reshape(-1), minlength=self.E)
+
+    def flops(self):
+        """Tensor-core FLOPs of the expert GEMMs: every (token, expert) row of
+        the routed experts and the shared expert, 3 matrices of H x I."""
+        return 2.0 * 3 * H * I * self.T * (K + 1)

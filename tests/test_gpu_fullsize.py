@@ -119,3 +119,83 @@ def test_step40_teacher_forced(dev, fused):
         got = (snaps[l + 1] - snaps[l])[:, cols]
         check_out(got, oref, rel=1e-4, what="layer %d" % l)
     A.bqe_set_fused(False)
+
+
+PF_TOL = 5e-3
+
+
+def _prefill_sample(forced, cnt, budget):
+    """Tokens whose outputs the oracle checks at the full prefill size: the
+    rows at the tile boundaries of the most loaded expert, one token of each
+    of the next three most and the four least loaded experts (the one adding
+    the fewest new experts), then tokens adding at most one new expert while
+    the set of experts to dequantise stays within `budget`."""
+    T = forced.shape[0]
+    sets = [set(r.tolist()) for r in forced]
+    order = np.argsort(-cnt, kind="stable")
+    most = [int(e) for e in order[:4]]
+    least = [int(e) for e in order[::-1] if cnt[e] > 0][:4]
+    S, sel = {E}, []
+
+    def group(e):
+        return [t for t in range(T) if e in sets[t]]
+    g = group(most[0])
+    for p in (0, 255, 256, 511, 512, len(g) - 1):
+        if 0 <= p < len(g) and g[p] not in sel:
+            sel.append(g[p])
+            S |= sets[g[p]]
+    for e in most[1:] + least:
+        t = min(group(e), key=lambda t: len(sets[t] - S))
+        if t not in sel:
+            sel.append(t)
+            S |= sets[t]
+    rng = np.random.default_rng(9)
+    for t in rng.permutation(T):
+        t = int(t)
+        if len(sel) >= 96:
+            break
+        new = sets[t] - S
+        if t not in sel and (not new or (len(new) == 1 and len(S) < budget)):
+            sel.append(t)
+            S |= new
+    return np.array(sel), most, least
+
+
+def test_prefill_dsv4_zipf(dev):
+    """8192 tokens, Zipf(0.8) forced routing over the mixed-format layer: the
+    selection and mixing weights of every token, and sampled outputs (tile
+    boundaries of the most loaded expert, the least loaded experts) against
+    the oracle."""
+    import torch
+    from bit_quantised_expert_gb300 import _abi as A
+    from synth import workloads as WL
+    W = WL.Prefill(dev)
+    T = W.T
+    nb = A.bqe_prefill_workspace_bytes(W.d, T)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    out = torch.full((T, H), float("nan"), device=dev)
+    idx = torch.zeros(T, K, dtype=torch.int32, device=dev)
+    wts = torch.zeros(T, K, dtype=torch.float32, device=dev)
+    A.bqe_moe_prefill(W.d, T, W.x, W.wr, W.bias, W.pool.cstruct(), W.table, W.forced, out, 0, idx, wts, ws, nb)
+    rc, det = A.bqe_check(ws)
+    assert rc == A.BQE_OK, (A.status_name(rc), det)
+    out = out.double().cpu().numpy()
+    assert np.isfinite(out).all()
+    assert np.array_equal(idx.cpu().numpy(), W.forced_np)
+    x_bits = W.x.cpu().numpy().view(np.uint16)
+    router = W.wr.cpu().numpy()
+    ref = O.route(O.bf16_bits_to_f64(x_bits), router, None, K, W.forced_np)
+    np.testing.assert_allclose(wts.cpu().numpy(), ref["w"], rtol=1e-5, atol=1e-7)
+    cnt = W.counts()
+    assert cnt.sum() == T * K and cnt.max() > 512
+    sample, most, least = _prefill_sample(W.forced_np, cnt, budget=48)
+    cols = np.random.default_rng(3).choice(H, 256, replace=False)
+    cache = {}
+
+    def canon(e):
+        if e not in cache:
+            cache[e] = W.canon(e).cpu().numpy()
+        return cache[e]
+    oref, _ = oracle_layer_sampled(W.fmts, canon, x_bits[sample], router, None, W.forced_np[sample], H, I, E, K,
+                                   cols)
+    check_out(out[sample][:, cols], oref, PF_TOL, PF_TOL, "prefill T=8192")
