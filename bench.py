@@ -10,7 +10,9 @@ MXFP4 (hidden 5120, inter 2304, 384 routed + 1 shared, top-6), M = 1 token
 row; seeded synthetic weights and activations generated on the device.
 Consecutive timed steps rotate over 4 independent layer instances (own
 router, shared and routed experts), so every step streams weights that are
-not in L2 (inputs larger than L2).  Other workloads: --workload mixed-m1 | mixed-m6 | step40-m1 | step40-m6.
+not in L2 (inputs larger than L2).  Other workloads: --workload mixed-m1 | mixed-m6 | step40-m1 | step40-m6,
+and --workload prefill (one mixed-format layer over 8192 tokens, tcgen05 grouped GEMMs; tokens/s and
+tensor TFLOP/s).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bqe|reference]
 
@@ -39,7 +41,9 @@ WORKLOADS = {
     "mixed-m6": "dsv4flash-moe-layer-mixed-tq1-q2_0-q3_k-decode-M6",
     "step40-m1": "dsv4flash-40-layer-step-4288-slot-pool-M1",
     "step40-m6": "dsv4flash-40-layer-step-4288-slot-pool-M6",
+    "prefill": "dsv4flash-moe-layer-mixed-prefill-T8192-zipf0.8",
 }
+PREFILL_METRIC = "MoE layer prefill: tokens/s and expert-GEMM TFLOP/s at T=8192 (Zipf 0.8 routing)"
 
 
 def parse():
@@ -57,6 +61,7 @@ def parse():
     ap.add_argument("--diag", action="store_true", help="print per-CTA cycle accounting of the expert kernels to stderr")
     ap.add_argument("--experts", type=int, default=384,
                     help="routed experts in the pool (profiling a smaller pool; per-call work is unchanged)")
+    ap.add_argument("--tokens", type=int, default=8192, help="prefill: token rows per call")
     ap.add_argument("--cpu-oracle-sample", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -67,6 +72,18 @@ def peaks():
         j = json.load(open(p))
         return float(j["hbm_gbs"]), "measured"
     return HBM_FALLBACK_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the sustained measurement (the GEMM
+    kernels run for milliseconds inside a longer step), else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        for k in ("bf16_tflops_sustained", "bf16_tflops"):
+            if j.get(k):
+                return float(j[k]), "measured %s" % k
+    return 1700.0, "fallback sustained"
 
 
 # ---------------------------------------------------------------- clocks
@@ -140,12 +157,17 @@ def barrier(world):
         dist.barrier()
 
 
+def _reduce_device():
+    import torch.distributed as dist
+    return "cpu" if dist.get_backend() == "gloo" else "cuda"
+
+
 def reduce_max(v, world):
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=_reduce_device())
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -155,9 +177,15 @@ def reduce_sum(v, world):
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=_reduce_device())
     dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
+
+
+def replica_throughput(units_local, seconds_local, world):
+    """Whole-job throughput of independent replicas: the units every rank
+    processed over the slowest rank's time."""
+    return reduce_sum(float(units_local), world) / reduce_max(float(seconds_local), world)
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -169,6 +197,19 @@ def cpu_oracle_sample(workload: str, reps: int = 1):
     from oracle import moe as O
     rng = np.random.default_rng(12345)
     H, I, E, K = 5120, 2304, 384, 6
+    if workload == "prefill":
+        # two tokens of the prefill layer: router over both, 2 x (6 routed + shared) expert FFNs
+        fm = [synth.TQ1, synth.Q2_0, synth.Q3_K, synth.TQ1, synth.Q2_0, synth.TQ1, synth.Q2_0]
+        experts = [synth.random_expert(rng, int(f), H, I) for f in fm]
+        router = synth.router_weights(rng, E, H)
+        x = synth.x_bf16(rng, 2, H)
+        forced = np.array([[0, 1, 2, 3, 4, 5], [5, 4, 3, 2, 1, 0]], dtype=np.int32)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            O.prefill_rows(x, router, None, experts, np.array(fm, np.int32), H, I, K, 6, forced, [0, 1])
+        dt = (time.perf_counter() - t0) / reps
+        return 2, dt, ("two prefill tokens of the mixed layer (router over 384 experts, 6 routed + shared expert "
+                       "FFN each, experts dequantised once), fp64")
     if workload.startswith("fp4"):
         fm = [synth.MXFP4] * 7
         desc = "one MXFP4 layer call at M=1: router (384 x 5120 fp32) + 6 routed + 1 shared expert FFN, fp64"
@@ -196,6 +237,9 @@ def run_cpu_baseline(workload: str):
     if r.returncode != 0:
         return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
     j = json.loads(r.stdout.strip().splitlines()[-1])
+    if workload == "prefill":
+        return {"value": j["bytes"] / j["seconds"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                "sample": j["sample"] + "; %.1f s, single thread" % j["seconds"]}
     return {"value": j["bytes"] / j["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": j["sample"] + "; %.1f s, single thread" % j["seconds"]}
 
@@ -376,7 +420,7 @@ def run_layer(args, rank, world):
             route_us=round(mean(t_route) * 1e6, 3), phase_a_us=round(mean(t_a) * 1e6, 3),
             phase_b_us=round(mean(t_b) * 1e6, 3),
             phase_a_gbs=round(achieved_a, 1), phase_b_gbs=round(mean(bytes_b) / mean(t_b) / 1e9, 1)),
-        gpu_launches=steps,
+        gpu_launches=5 * steps,  # router, W1/W3 + its finalize, W2 + its finalize
         variant=args.variant,
         timing="CUDA-graph replay per step, events as graph nodes around the layer kernel",
         wall_s_timed_loop=round(wall, 4),
@@ -560,6 +604,108 @@ def run_step40(args, rank, world):
     return res
 
 
+def run_prefill(args, rank, world):
+    """One mixed-format layer over T = 8192 token rows (Zipf 0.8 forced routing)
+    through bqe_moe_prefill, eager calls (8 kernels each, a few ms per call)."""
+    import numpy as np
+    import torch
+    from bit_quantised_expert_gb300 import buildlib
+    buildlib.build()
+    from bit_quantised_expert_gb300 import _abi as A
+    from synth import workloads as WL
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    W = WL.Prefill(dev, T=args.tokens, n_experts=args.experts)
+    T, H = W.T, 5120
+    nb = A.bqe_prefill_workspace_bytes(W.d, T)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    out = torch.empty(T, H, device=dev)
+    pool = W.pool.cstruct()
+    st = torch.cuda.current_stream()
+
+    def call(x):
+        A.bqe_moe_prefill(W.d, T, x, W.wr, W.bias, pool, W.table, W.forced, out, 0, None, None, ws, nb)
+
+    for _ in range(max(args.warmup, 3)):
+        call(W.x)
+    torch.cuda.synchronize()
+    rc, det = A.bqe_check(ws)
+    assert rc == 0, (A.status_name(rc), det)
+    clocks = ClockSampler(torch.cuda.current_device(), enabled=not args.no_clocks)
+    t_end = time.time() + args.soak_s
+    while time.time() < t_end:
+        call(W.x)
+        torch.cuda.synchronize()
+    steps = args.steps
+    A.bqe_set_diag(True)  # events between the library's kernels, on this stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    per_kernel = []
+    barrier(world)
+    torch.cuda.synchronize()
+    for s_ in range(steps):
+        evs[s_][0].record(st)
+        call(W.x)
+        evs[s_][1].record(st)
+        per_kernel.append(A.bqe_prefill_kernel_ms())
+    torch.cuda.synchronize()
+    barrier(world)
+    A.bqe_set_diag(False)
+    clk = clocks.stop()
+    rc, det = A.bqe_check(ws)
+    assert rc == 0, (A.status_name(rc), det)
+    ts = [evs[s_][0].elapsed_time(evs[s_][1]) * 1e-3 for s_ in range(steps)]
+    Tt = reduce_max(sum(ts), world)
+    value = T * steps * world / Tt
+    flops = W.flops()
+    cnt = W.counts()
+    rows = T * 7
+    f_w13, f_w2 = 2.0 * 2 * 5120 * 2304 * rows, 2.0 * 5120 * 2304 * rows
+    km = {k: sum(p[k] for p in per_kernel) / steps for k in per_kernel[0]}
+    bf16_peak, pk_kind = tensor_peak()
+    ach = f_w13 / (km["gemm_w13"] * 1e-3) / 1e12
+    res = dict(metric=PREFILL_METRIC, value=round(value, 1), unit="tokens/s", n_gpus=world, steps=steps,
+               warmup=args.warmup, ms_per_step=round(Tt / steps * 1e3, 4), higher_is_better=True, scaling="weak",
+               vs_baseline=None,
+               dtype="fp16 tensor-core operands (bf16 for MXFP4 experts), fp32 accumulate; ternary/q2_0/q3_k weights",
+               data="synthetic (seeded, generated on the device)",
+               config=dict(workload=WORKLOADS["prefill"], hidden=5120, inter=2304, n_experts=W.E, top_k=6,
+                           n_shared=1, T=T, routing="Zipf(0.8) forced selection, weights from the router",
+                           rows_per_expert=dict(max=int(cnt.max()), median=float(np.median(cnt)),
+                                                min=int(cnt.min()), mean=float(cnt.mean())),
+                           l2="inputs larger than L2 (x 84 MB, weights ~3.8 GB, grouped operands ~1 GB per call)",
+                           parallelism="replicas" if world > 1 else "single-gpu"),
+               tflops=round(flops * steps * world / Tt / 1e12, 2),
+               expert_gemm_flops_per_step=flops,
+               kernel_ms=km,
+               roofline=dict(bound="tensor", achieved=round(ach, 1), peak=bf16_peak, unit="TFLOP/s",
+                             frac=round(ach / bf16_peak, 4), traffic=None,
+                             kernel="k_pf_gemm<0> (W1/W3 grouped GEMM: in-smem dequant + tcgen05 MMA + SiLU-GLU)",
+                             algorithmic_flops_per_launch=f_w13,
+                             peak_kind="%s bf16 dense (fp16 runs at the same rate)" % pk_kind,
+                             w2_achieved=round(f_w2 / (km["gemm_w2"] * 1e-3) / 1e12, 1)),
+               gpu_launches=8 * steps,
+               timing="eager calls; CUDA events on the calling stream around each call and between its kernels")
+    if clk:
+        res["clocks"] = clk
+    # end to end: pinned host x in, host out back, every step
+    xh = W.x.cpu().pin_memory()
+    oh = torch.empty(T, H, dtype=torch.float32).pin_memory()
+    xd = torch.empty_like(W.x)
+    e2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(min(steps, 10))]
+    for s_ in range(len(e2)):
+        e2[s_][0].record(st)
+        xd.copy_(xh, non_blocking=True)
+        call(xd)
+        oh.copy_(out, non_blocking=True)
+        e2[s_][1].record(st)
+    torch.cuda.synchronize()
+    Te = reduce_max(sum(a.elapsed_time(b) * 1e-3 for a, b in e2), world)
+    res["e2e"] = dict(value=round(T * len(e2) * world / Te, 1), unit="tokens/s", h2d_bytes_per_step=T * H * 2,
+                      d2h_bytes_per_step=T * H * 4, ms_per_step=round(Te / len(e2) * 1e3, 3),
+                      note="eager bqe_moe_prefill with pinned host x in and host out back")
+    return res
+
+
 def run_reference(args, rank, world):
     """The oracle (fp64, as it stands) on the host cores, one bounded sample per step."""
     if rank != 0:
@@ -621,6 +767,8 @@ def main():
     rank, world, local = dist_setup(args.gpus)
     if args.workload.startswith("step40"):
         res = run_step40(args, rank, world)
+    elif args.workload == "prefill":
+        res = run_prefill(args, rank, world)
     else:
         res = run_layer(args, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -76,6 +76,7 @@ SIGNATURES = {
     "bqe_set_test_drop_item": (None, [_I32]),
     "bqe_set_variant": (None, [_I32]),
     "bqe_set_prefill_f16": (None, [_I32]),
+    "bqe_prefill_kernel_ms": (ctypes.c_int, [_P]),
     "bqe_set_diag": (None, [_I32]),
     "bqe_set_fused": (None, [_I32]),
     "bqe_diag_offset": (_U64, [_DESC, _I32]),
@@ -257,3 +258,13 @@ def bqe_set_fused(on: bool) -> None:
 
 def bqe_set_prefill_f16(on: bool) -> None:
     lib.bqe_set_prefill_f16(1 if on else 0)
+
+
+PREFILL_KERNELS = ("logits", "select", "plan", "fill", "gather", "gemm_w13", "gemm_w2", "combine")
+
+
+def bqe_prefill_kernel_ms() -> dict:
+    """Per-kernel milliseconds of the last bqe_moe_prefill call made in diagnostic mode."""
+    buf = (ctypes.c_float * len(PREFILL_KERNELS))()
+    _ok(lib.bqe_prefill_kernel_ms(ctypes.addressof(buf)), "bqe_prefill_kernel_ms")
+    return dict(zip(PREFILL_KERNELS, list(buf)))

@@ -232,6 +232,20 @@ extern "C" int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M
 // ---------------------------------------------------------------------------
 static constexpr int32_t kPfMaxT = 1 << 20;
 
+// Events of the diagnostic mode, one set per device, created on first use.
+static cudaEvent_t* pf_events() {
+  static cudaEvent_t ev[64][kPfKernels + 1];
+  static bool made[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!made[dev]) {
+    for (int i = 0; i <= kPfKernels; ++i)
+      if (cudaEventCreate(&ev[dev][i]) != cudaSuccess) return nullptr;
+    made[dev] = true;
+  }
+  return ev[dev];
+}
+
 extern "C" uint64_t bqe_prefill_workspace_bytes(const bqe_layer_desc* d, int32_t T) {
   if (!desc_ok(d) || T < 1 || T > kPfMaxT) return 0;
   return make_pf_ws(make_pf_geo(d->hidden, d->inter, d->n_experts, d->top_k, T)).total;
@@ -266,7 +280,17 @@ extern "C" int bqe_moe_prefill(const bqe_layer_desc* d, int32_t T, const uint16_
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(P.ws + P.L.err, 0, 16, st) != cudaSuccess) return BQE_ECUDA;
   if (cudaMemsetAsync(P.ws + P.L.cnt, 0, 4ull * (P.g.E + 1), st) != cudaSuccess) return BQE_ECUDA;
-  return launch_prefill(P, st);
+  return launch_prefill(P, st, g_diag.load() ? pf_events() : nullptr);
+}
+
+extern "C" int bqe_prefill_kernel_ms(float* ms) {
+  if (!ms) return BQE_EINVAL;
+  cudaEvent_t* ev = pf_events();
+  if (!ev) return BQE_ECUDA;
+  if (cudaEventSynchronize(ev[kPfKernels]) != cudaSuccess) return BQE_ECUDA;
+  for (int i = 0; i < kPfKernels; ++i)
+    if (cudaEventElapsedTime(&ms[i], ev[i], ev[i + 1]) != cudaSuccess) return BQE_ECUDA;
+  return BQE_OK;
 }
 
 extern "C" int bqe_check(void* ws, void* stream, int32_t* detail) {

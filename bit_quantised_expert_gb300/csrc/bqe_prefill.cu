@@ -663,7 +663,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
   const uint64_t lim = P.limit_ns;
 
   if (tid == 0) {
-    for (int i = 0; i < kPfRawStages; ++i) { mbar_init(&raw_full[i], 1); mbar_init(&raw_empty[i], 4); }
+    for (int i = 0; i < kPfRawStages; ++i) { mbar_init(&raw_full[i], 1); mbar_init(&raw_empty[i], kPfDqWarps); }
     for (int i = 0; i < kPfStages; ++i) {
       mbar_init(&a_full[i], 4);
       mbar_init(&b_full[i], 1);
@@ -673,7 +673,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
     mbar_init(fin, 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  constexpr int kWLoad = kPfDqWarps, kWMma = kPfDqWarps + 1, kWEpi = kPfDqWarps + 2;
+  if (warp == kWMma) {
     tmem_alloc(s_tmem, 512);
     tmem_relinquish();
   }
@@ -682,14 +683,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == 4) {
+  if (warp == kWLoad) {
     // ---------------- loads: raw weight groups and B tiles ----------------
     if (lane == 0) {
       const uint8_t* bsrc = P.ws + (PH == 0 ? P.L.xp : P.L.hp);
-      int rs = 0, s = 0;
-      uint32_t rph = 0, sph = 0;
-      uint32_t raw_par[kPfRawStages], b_par[kPfStages];
-      bool raw_armed[kPfRawStages] = {}, b_armed[kPfStages] = {};
+      uint32_t nr = 0, nbs = 0;  // raw groups and B stages issued so far
       bool ok = true;
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
         const PfItem it = pf_item(P, item, nblk);
@@ -712,61 +710,67 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
         const uint32_t bbytes = (uint32_t)it.npad * 128u;
         for (int grp = 0; grp < ngrp && ok; ++grp) {
           const int c = grp / gpc, gi = grp % gpc;
+          const uint32_t rs = nr % kPfRawStages, rph = (nr / kPfRawStages) & 1;
           if (!mbar_wait_bounded(&raw_empty[rs], rph ^ 1, lim)) { ok = false; break; }
           mbar_arrive_expect_tx(&raw_full[rs], 4 * raw_group_bytes(fmt));
 #pragma unroll
           for (int w = 0; w < 4; ++w)
             issue_raw_group(fmt, mat[w] + ((uint64_t)panel[w] * nch + c) * tb, nb, gi,
                             sRaw + rs * kPfRawStage + w * kPfRawPanel, &raw_full[rs]);
-          raw_par[rs] = rph;
-          raw_armed[rs] = true;
-          if (++rs == kPfRawStages) { rs = 0; rph ^= 1; }
+          ++nr;
           for (int kq = 0; kq < 4; ++kq) {
             const int ks = grp * 4 + kq;
+            const uint32_t s = nbs % kPfStages, sph = (nbs / kPfStages) & 1;
             if (!mbar_wait_bounded(&st_empty[s], sph ^ 1, lim)) { ok = false; break; }
             mbar_arrive_expect_tx(&b_full[s], bbytes);
             bulk_g2s(sB + s * kPfBStage, bsrc + ((uint64_t)ks * R8 + (it.row0 >> 3)) * 1024, bbytes, &b_full[s]);
-            b_par[s] = sph;
-            b_armed[s] = true;
-            if (++s == kPfStages) { s = 0; sph ^= 1; }
+            ++nbs;
           }
         }
       }
       if (!ok) set_error(err, BQE_ETIMEOUT, kErrPfProducer);
-      // every copy this thread started has landed before the CTA may exit
-      for (int i = 0; i < kPfRawStages; ++i)
-        if (raw_armed[i]) mbar_wait_bounded(&raw_full[i], raw_par[i], lim);
-      for (int i = 0; i < kPfStages; ++i)
-        if (b_armed[i]) mbar_wait_bounded(&b_full[i], b_par[i], lim);
+      // every copy this thread started has landed before the CTA may exit:
+      // the last (up to ring size) issues of each ring are the only ones
+      // that can still be in flight
+      for (uint32_t i = 0; i < kPfRawStages && i < nr; ++i) {
+        const uint32_t n = nr - 1 - i;
+        mbar_wait_bounded(&raw_full[n % kPfRawStages], (n / kPfRawStages) & 1, lim);
+      }
+      for (uint32_t i = 0; i < kPfStages && i < nbs; ++i) {
+        const uint32_t n = nbs - 1 - i;
+        mbar_wait_bounded(&b_full[n % kPfStages], (n / kPfStages) & 1, lim);
+      }
     }
-  } else if (warp < 4) {
-    // ---------------- dequant: A rows 32 warp .. 32 warp + 31 ----------------
-    int rs = 0, s = 0;
-    uint32_t rph = 0, sph = 0;
+  } else if (warp < kPfDqWarps) {
+    // ---------------- dequant: panel warp % 4 (A rows 32 (warp % 4) ..), K-steps n % sets == warp / 4
+    const int set = warp / 4, pw = warp % 4;
+    uint32_t nr = 0, n = 0;  // raw groups and K-steps passed so far (the whole CTA's sequence)
     bool ok = true, bad = false;
-    const int row = warp * 32 + lane;
+    const int row = pw * 32 + lane;
     for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
       const PfItem it = pf_item(P, item, nblk);
       for (int grp = 0; grp < ngrp && ok; ++grp) {
+        const uint32_t rs = nr % kPfRawStages, rph = (nr / kPfRawStages) & 1;
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(&raw_full[rs], rph, lim))) { ok = false; break; }
-        const uint8_t* praw = sRaw + rs * kPfRawStage + warp * kPfRawPanel;
-        for (int kq = 0; kq < 4; ++kq) {
+        const uint8_t* praw = sRaw + rs * kPfRawStage + pw * kPfRawPanel;
+        for (int kq = 0; kq < 4; ++kq, ++n) {
+          if ((int)(n % kPfDqSets) != set) continue;
+          const uint32_t s = n % kPfStages, sph = (n / kPfStages) & 1;
           if (!__all_sync(0xffffffffu, mbar_wait_bounded(&st_empty[s], sph ^ 1, lim))) { ok = false; break; }
           dequant_kstep(it.fmt, it.f16, praw, kq, lane, sA + s * kPfAStage, row, bad);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&a_full[s]);
-          if (++s == kPfStages) { s = 0; sph ^= 1; }
         }
         if (!ok) break;
         __syncwarp();
         if (lane == 0) mbar_arrive(&raw_empty[rs]);
-        if (++rs == kPfRawStages) { rs = 0; rph ^= 1; }
+        ++nr;
       }
     }
     if (!ok && lane == 0) set_error(err, BQE_ETIMEOUT, kErrPfDequant);
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, BQE_EUNSUPPORTED, kErrPfRange);
-  } else if (warp == 5) {
+  } else if (warp == kWMma) {
     // ---------------- MMA issue (one thread) ----------------
     if (lane == 0) {
       int s = 0;
@@ -790,7 +794,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
           const uint64_t da = umma_desc_sw128(sA + s * kPfAStage);
           const uint64_t db = umma_desc_sw128(sB + s * kPfBStage);
 #pragma unroll
-          for (int k16 = 0; k16 < 4; ++k16) umma_bf16(d, da + 2 * k16, db + 2 * k16, idesc, (ks | k16) != 0);
+          for (int k16 = 0; k16 < 4; ++k16) umma_f16(d, da + 2 * k16, db + 2 * k16, idesc, (ks | k16) != 0);
           umma_commit(&st_empty[s]);
           if (++s == kPfStages) { s = 0; sph ^= 1; }
         }
@@ -805,7 +809,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
   } else {
     // ---------------- epilogue: warps 6-9, lane quarter warp % 4 ----------------
     const int q = warp & 3;
-    const int et = tid - 6 * 32;  // 0..127
+    const int et = tid - kWEpi * 32;  // 0..127
     bool ok = true;
     int lc = 0;
     for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++lc) {
@@ -890,7 +894,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == kWMma) tmem_dealloc(tmem, 512);
 }
 
 // ----------------------------------------------------------------------------
@@ -922,7 +926,7 @@ __global__ void __launch_bounds__(256) k_pf_combine(PfParams P) {
 }
 
 // ----------------------------------------------------------------------------
-int launch_prefill(const PfParams& P, cudaStream_t st) {
+int launch_prefill(const PfParams& P, cudaStream_t st, cudaEvent_t* ev) {
   static int s_attr_done[64] = {};
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BQE_ECUDA;
@@ -936,15 +940,27 @@ int launch_prefill(const PfParams& P, cudaStream_t st) {
     s_attr_done[dev] = 1;
   }
   const PfGeo& g = P.g;
+  auto mark = [&](int i) {
+    if (ev) cudaEventRecord(ev[i], st);
+  };
   dim3 lg((g.E + kLgBN - 1) / kLgBN, (g.T + kLgBM - 1) / kLgBM);
+  mark(0);
   k_pf_logits<<<lg, 256, 0, st>>>(P.x, P.router_w, (float*)(P.ws + P.L.z), g.T, g.E, g.H);
+  mark(1);
   k_pf_select<<<(g.T + 7) / 8, 256, 0, st>>>(P);
+  mark(2);
   k_pf_plan<<<1, 1024, 0, st>>>(P);
+  mark(3);
   k_pf_fill<<<g.E + 1, 256, 0, st>>>(P);
+  mark(4);
   k_pf_gather<<<g.maxTiles, 256, 0, st>>>(P);
+  mark(5);
   k_pf_gemm<0><<<sms, kPfThreads, kPfSmemBytes, st>>>(P);
+  mark(6);
   k_pf_gemm<1><<<sms, kPfThreads, kPfSmemBytes, st>>>(P);
+  mark(7);
   k_pf_combine<<<g.T, 256, 0, st>>>(P);
+  mark(8);
   return cudaGetLastError() == cudaSuccess ? BQE_OK : BQE_ECUDA;
 }
 

@@ -24,7 +24,9 @@ constexpr uint32_t kPfOffRaw = kPfOffB + kPfStages * kPfBStage;
 constexpr uint32_t kPfOffEpi = kPfOffRaw + kPfRawStages * kPfRawStage;
 constexpr uint32_t kPfOffBar = kPfOffEpi + kPfEpiBytes;
 constexpr uint32_t kPfSmemBytes = kPfOffBar + 256 + 1024;  // + barriers + alignment slack
-constexpr int kPfThreads = 320;     // warps 0-3 dequant, 4 loads, 5 MMA, 6-9 epilogue
+constexpr int kPfDqSets = 2;       // sets of 4 dequant warps; set j takes the K-steps n with n % sets == j
+constexpr int kPfDqWarps = 4 * kPfDqSets;
+constexpr int kPfThreads = 32 * (kPfDqWarps + 6);  // dequant warps, then loads, MMA, 4 epilogue warps
 constexpr int kPfMaxE = 1024;
 
 struct PfGeo {
@@ -95,6 +97,8 @@ struct PfParams {
   uint64_t limit_ns;
 };
 
-int launch_prefill(const PfParams& P, cudaStream_t st);
+constexpr int kPfKernels = 8;
+// ev: null, or kPfKernels + 1 events recorded on `st` around the kernels
+int launch_prefill(const PfParams& P, cudaStream_t st, cudaEvent_t* ev);
 
 }  // namespace bqe

@@ -309,6 +309,12 @@ void bqe_set_fused(int32_t on);
  * bits: relative L2 error about 3e-3 against exact arithmetic, against about
  * 4e-4 for fp16).  Both run at the same tensor-core rate. */
 void bqe_set_prefill_f16(int32_t on);
+
+/* Diagnostic (with bqe_set_diag(1)): bqe_moe_prefill records CUDA events on
+ * its stream around each of its 8 kernels (router logits, selection, plan,
+ * fill, gather, W1/W3 GEMM, W2 GEMM, combine); this waits for the last call's
+ * events and writes the 8 durations in milliseconds to ms (host, 8 floats). */
+int bqe_prefill_kernel_ms(float* ms);
 uint64_t bqe_diag_offset(const bqe_layer_desc* d, int32_t M);
 
 #ifdef __cplusplus
