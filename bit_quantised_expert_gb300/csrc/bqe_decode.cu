@@ -154,8 +154,8 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
         H.addr = addr; H.u = u; H.p0 = pg * P_; H.c = c; H.fmt = fmt; H.R = R;
         const uint32_t tb = tile_bytes(fmt, kc);
         const uint32_t wbytes = (uint32_t)phase_mats(PHASE) * P_ * tb;
-        const bool half_act = PHASE == 0 && fmt == BQE_FMT_MXFP4 && P.variant == 1;
-        const uint32_t arow = (uint32_t)kc * (half_act ? 2u : 4u);
+        const int amode = act_mode(PHASE, fmt, P.variant);
+        const uint32_t arow = (uint32_t)act_row_bytes(amode, fmt, kc);
         const uint32_t abytes = (uint32_t)R * arow;
         uint8_t* dst = ring + (size_t)s * slot_bytes;
         mbar_arrive_expect_tx(&full[s], wbytes + abytes);
@@ -175,10 +175,37 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
         uint8_t* adst = dst + wbytes;
         const uint16_t* xh = (const uint16_t*)(P.ws + P.L.xh);
         for (int r = 0; r < R; ++r) {
+          const int64_t row = PHASE == 0 ? s_urows[u * kMaxM + r] : 0;
+          if (amode == kActInt) {
+            // X_hi and X_lo of this chunk in the format's order, then their 16-column sums:
+            // the layer input (W1/W3) or the expert's h (W2)
+            const uint32_t xb = (uint32_t)act_x_bytes(fmt, kc), xbl = (uint32_t)act_xl_bytes(fmt, kc);
+            const int Kr = PHASE == 0 ? g.H : g.I;
+            const int64_t rowi = PHASE == 0 ? row : (int64_t)u * g.M + r;
+            const uint8_t* hi0 = P.ws + (PHASE == 0 ? (fmt == BQE_FMT_TQ1 ? P.L.xt : P.L.xq) : P.L.hq);
+            const uint8_t* lo0 = P.ws + (PHASE == 0 ? (fmt == BQE_FMT_TQ1 ? P.L.xtl : P.L.xql) : P.L.hql);
+            const int64_t cofs_h = (int64_t)c * (fmt == BQE_FMT_TQ1 ? (kc / 256) * kTOrderBlock : kc * 2);
+            const int64_t cofs_l = (int64_t)c * (fmt == BQE_FMT_TQ1 ? (kc / 256) * kTOrderBlockL : kc);
+            const int64_t so = (rowi * (Kr / 16) + (int64_t)c * (kc / 16)) * 4;
+            uint8_t* d0 = adst + (size_t)r * arow;
+            const bool tq = fmt == BQE_FMT_TQ1;
+            const int64_t roh = PHASE == 0 ? (tq ? rowi * (Kr / 256) * kTOrderBlock : rowi * Kr * 2)
+                                           : h_row_off_hi(rowi, Kr);
+            const int64_t rol = PHASE == 0 ? (tq ? rowi * (Kr / 256) * kTOrderBlockL : rowi * Kr)
+                                           : h_row_off_lo(rowi, Kr);
+            bulk_g2s(d0, hi0 + roh + cofs_h, xb, &full[s]);
+            bulk_g2s(d0 + xb, lo0 + rol + cofs_l, xbl, &full[s]);
+            bulk_g2s(d0 + xb + xbl, P.ws + (PHASE == 0 ? P.L.s16 : P.L.hs16) + so, (uint32_t)kc / 4, &full[s]);
+            bulk_g2s(d0 + xb + xbl + kc / 4, P.ws + (PHASE == 0 ? P.L.s16l : P.L.hs16l) + so, (uint32_t)kc / 4,
+                     &full[s]);
+            bulk_g2s(d0 + xb + xbl + kc / 2, P.ws + (PHASE == 0 ? P.L.xsb : P.L.hsb) + (rowi * nch + c) * 16, 16u,
+                     &full[s]);
+            continue;
+          }
           const void* src;
           if (PHASE == 0)
-            src = half_act ? (const void*)(xh + (int64_t)s_urows[u * kMaxM + r] * g.H + (int64_t)c * kc)
-                           : (const void*)(xf + (int64_t)s_urows[u * kMaxM + r] * g.H + (int64_t)c * kc);
+            src = amode == kActF16 ? (const void*)(xh + row * g.H + (int64_t)c * kc)
+                                   : (const void*)(xf + row * g.H + (int64_t)c * kc);
           else
             src = hbuf + ((int64_t)u * g.M + r) * g.I + (int64_t)c * kc;
           bulk_g2s(adst + (size_t)r * arow, src, arow, &full[s]);
@@ -229,8 +256,7 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
       const uint8_t* tile = slot + (size_t)(mat * P_ + pan) * tb;
       const uint8_t* act = slot + (size_t)phase_mats(PHASE) * P_ * tb;
       float* rb = red + (size_t)b * red_stride;
-      const bool half_act = PHASE == 0 && H.fmt == BQE_FMT_MXFP4 && P.variant == 1;
-      consume_rows(H.R, H.fmt, tile, kc, grp, act, lane, rb + cw * g.M * 32, half_act);
+      consume_rows(H.R, H.fmt, tile, kc, grp, act, lane, rb + cw * g.M * 32, act_mode(PHASE, H.fmt, P.variant));
       if (cw == 0 && lane == 0) rmeta[b] = RedMeta{H.u, H.p0, H.c, H.R};
       ccomp += clk() - t2;
       __syncwarp();
@@ -267,12 +293,13 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
     // partial sums of this item's chunk go to the workspace with plain stores;
     // the finalize kernel adds the chunks in a fixed order
     if (PHASE == 0) {
-      const bool half_act = s_ufmt[mt.u] == BQE_FMT_MXFP4 && P.variant == 1;
+      const int amode = act_mode(PHASE, s_ufmt[mt.u], P.variant);
       const float* xsc = (const float*)(P.ws + P.L.xsc);
       float* pa = (float*)(P.ws + P.L.pa);
       // W1 warps of panel pi are cw = pi*G + gi, W3 warps cw = (P + pi)*G + gi
       for (int r = 0; r < mt.R; ++r) {
-        const float unscale = half_act ? xsc[s_urows[mt.u * kMaxM + r]] : 1.0f;  // 2^-s, exact
+        // f16 rows carry 2^s (removed here, exact); integer rows were unscaled per block
+        const float unscale = amode == kActF16 ? xsc[s_urows[mt.u * kMaxM + r]] : 1.0f;
         for (int pi = 0; pi < P_; ++pi) {
           const int p = mt.p0 + pi;
           const int64_t base = (((int64_t)mt.u * g.npanA + p) * nch + mt.c) * 2 * g.M;
@@ -313,29 +340,76 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
 //   phase A: h[u, r, i] = silu(sum_c g_c) * (sum_c u_c)
 //   phase B: out[m, n] (+)= y_shared[m, n] + sum_j w[m, j] y[u(m,j), r(m,j), n]
 // ---------------------------------------------------------------------------
+// h = silu(g) * u, one CTA per (expert, row, 256 columns), one column per
+// thread: the chunk partials of g and u added in a fixed order; h kept in fp32
+// and, for the integer W2 paths, as X_hi + X_lo / 128 of h 2^si (max |h| 2^si
+// of the 256 columns in [2^13, 2^14)) in the order of the expert's format,
+// with the sums of X_hi and X_lo over every 16 columns and 2^-si.
 __global__ void __launch_bounds__(256) k_finalize_a(ExpParams P) {
   const Geo& g = P.g;
   griddep_wait();
   griddep_launch_dependents();
   const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
-  const int32_t* u_nrows = (const int32_t*)(P.ws + P.L.u_nrows);
+  const int nbl = g.I / 256;
+  const int u = blockIdx.x / (g.M * nbl), r = (blockIdx.x / nbl) % g.M, blk = blockIdx.x % nbl;
+  if (u >= nU) return;
+  if (r >= ((const int32_t*)(P.ws + P.L.u_nrows))[u]) return;
+  const int fmt = ((const int32_t*)(P.ws + P.L.u_fmt))[u];
   const float* pa = (const float*)(P.ws + P.L.pa);
-  float* hbuf = (float*)(P.ws + P.L.h);
-  const int nch = g.nchA;
-  const int64_t n = (int64_t)nU * g.M * g.I;
-  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
-    const int u = (int)(t / ((int64_t)g.M * g.I));
-    const int r = (int)((t / g.I) % g.M);
-    const int i = (int)(t % g.I);
-    if (r >= u_nrows[u]) continue;
-    const int p = i >> 5, lane = i & 31;
-    float a0 = 0.f, a1 = 0.f;
-    for (int c = 0; c < nch; ++c) {
-      const int64_t base = (((int64_t)u * g.npanA + p) * nch + c) * 2 * g.M;
-      a0 += pa[(base + r) * 32 + lane];
-      a1 += pa[(base + g.M + r) * 32 + lane];
+  const int nch = g.nchA, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blk * 256 + tid;
+  const int p = i >> 5;
+  float a0 = 0.f, a1 = 0.f;
+  for (int c = 0; c < nch; ++c) {
+    const int64_t base = (((int64_t)u * g.npanA + p) * nch + c) * 2 * g.M;
+    a0 += pa[(base + r) * 32 + lane];
+    a1 += pa[(base + g.M + r) * 32 + lane];
+  }
+  const float hv = silu_f(a0) * a1;
+  const int64_t rowi = (int64_t)u * g.M + r;
+  ((float*)(P.ws + P.L.h))[rowi * g.I + i] = hv;
+  if (act_mode(1, fmt, P.variant) != kActInt) return;
+  __shared__ uint32_t s_mx[8];
+  const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(hv) & 0x7FFFFFFFu);
+  if (lane == 0) s_mx[warp] = mx;
+  __syncthreads();
+  uint32_t bm = 0;
+  for (int w = 0; w < 8; ++w) bm = max(bm, s_mx[w]);
+  const int ex = (int)(bm >> 23);  // biased exponent of max |h| (0: all zero or subnormal)
+  const int si = ex == 0 ? 0 : min(max(13 - (ex - 127), -100), 100);
+  if (tid == 0) {
+    const int bpc = g.kcB / 256;
+    ((float*)(P.ws + P.L.hsb))[(rowi * g.nchB + blk / bpc) * 4 + blk % bpc] = ldexpf(1.0f, -si);
+  }
+  int16_t* hq = (int16_t*)(P.ws + P.L.hq + h_row_off_hi(rowi, g.I));
+  int8_t* hql = (int8_t*)(P.ws + P.L.hql + h_row_off_lo(rowi, g.I));
+  const float v = ldexpf(hv, si);
+  const int Xh = __float2int_rn(v);
+  const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
+  const int j = tid;
+  if (fmt == BQE_FMT_TQ1) {
+    const int run = j / 20, jr = j % 20, q4 = jr / 5, rd = jr % 5;
+    hq[blk * 264 + run * 20 + 4 * rd + 2 * (q4 >> 1) + (q4 & 1)] = (int16_t)Xh;
+    hql[blk * 272 + run * 20 + 4 * rd + q4] = (int8_t)Xl;
+    if (tid < 16) {  // T-order slots past column 255 and the padding
+      const int slot = tid < 4 ? 240 + 4 * (tid + 1) + 3 : 260 + (tid - 4);
+      if (tid < 8) hq[blk * 264 + slot] = 0;
+      hql[blk * 272 + slot] = 0;
     }
-    hbuf[((int64_t)u * g.M + r) * g.I + i] = silu_f(a0) * a1;
+  } else {
+    const int jj = j & 15, kq = jj & 3, iq = jj >> 2;
+    hq[blk * 256 + (j & ~15) + 4 * kq + 2 * (iq >> 1) + (iq & 1)] = (int16_t)Xh;
+    hql[blk * 256 + (j & ~15) + 4 * kq + iq] = (int8_t)Xl;
+  }
+  int ph = Xh, pl = Xl;
+#pragma unroll
+  for (int o = 8; o; o >>= 1) {
+    ph += __shfl_xor_sync(0xffffffffu, ph, o);
+    pl += __shfl_xor_sync(0xffffffffu, pl, o);
+  }
+  if ((lane & 15) == 0) {
+    ((int32_t*)(P.ws + P.L.hs16))[rowi * (g.I / 16) + blk * 16 + (tid >> 4)] = ph;
+    ((int32_t*)(P.ws + P.L.hs16l))[rowi * (g.I / 16) + blk * 16 + (tid >> 4)] = pl;
   }
 }
 
@@ -345,21 +419,28 @@ __global__ void __launch_bounds__(256) k_finalize_b(ExpParams P) {
   griddep_launch_dependents();
   const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
   const float* pb = (const float*)(P.ws + P.L.pb);
-  const int32_t* cu = (const int32_t*)(P.ws + P.L.comb_u);
-  const int32_t* cr = (const int32_t*)(P.ws + P.L.comb_r);
-  const float* cwt = (const float*)(P.ws + P.L.comb_w);
   const int nch = g.nchB;
   if (nU == 0) return;  // the router reported an error; out is left untouched
+  // every row's (expert slot, row in expert, weight) once in shared memory, so
+  // all partial loads of an output element are independent
+  __shared__ int s_cu[kMaxM * kMaxTopK], s_cr[kMaxM * kMaxTopK];
+  __shared__ float s_cw[kMaxM * kMaxTopK];
+  for (int i = threadIdx.x; i < g.M * g.K; i += blockDim.x) {
+    s_cu[i] = ((const int32_t*)(P.ws + P.L.comb_u))[i];
+    s_cr[i] = ((const int32_t*)(P.ws + P.L.comb_r))[i];
+    s_cw[i] = ((const float*)(P.ws + P.L.comb_w))[i];
+  }
+  __syncthreads();
   const int64_t n = (int64_t)g.M * g.H;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
     const int m = (int)(t / g.H), col = (int)(t % g.H);
     float val = 0.f;
     for (int c = 0; c < nch; ++c) val += pb[((int64_t)c * g.M + m) * g.H + col];  // shared expert, u = 0
     for (int j = 0; j < g.K; ++j) {
-      const int u = cu[m * g.K + j], r = cr[m * g.K + j];
+      const int u = s_cu[m * g.K + j], r = s_cr[m * g.K + j];
       float yj = 0.f;
       for (int c = 0; c < nch; ++c) yj += pb[(((int64_t)u * nch + c) * g.M + r) * g.H + col];
-      val = fmaf(cwt[m * g.K + j], yj, val);
+      val = fmaf(s_cw[m * g.K + j], yj, val);
     }
     float* o = P.out + t;
     *o = P.accumulate ? *o + val : val;
@@ -367,10 +448,16 @@ __global__ void __launch_bounds__(256) k_finalize_b(ExpParams P) {
 }
 
 int launch_finalize(const ExpParams& P, int phase, int sms, cudaStream_t st, bool pdl) {
-  const int64_t n = phase == 0 ? (int64_t)P.g.U * P.g.M * P.g.I : (int64_t)P.g.M * P.g.H;
-  int grid = (int)((n + 255) / 256);
-  if (grid > 2 * sms) grid = 2 * sms;
-  if (grid < 1) grid = 1;
+  int grid;
+  if (phase == 0) {
+    if (P.g.I % 256) return BQE_EUNSUPPORTED;
+    grid = P.g.U * P.g.M * (P.g.I / 256);  // one CTA per (expert, row, 256 columns)
+  } else {
+    const int64_t n = (int64_t)P.g.M * P.g.H;
+    grid = (int)((n + 255) / 256);
+    if (grid > 2 * sms) grid = 2 * sms;
+    if (grid < 1) grid = 1;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(256);

@@ -127,7 +127,8 @@ __host__ __device__ inline Geo make_geo(int H, int I, int E, int K, int M) {
 // Workspace layout (offsets in bytes, each 256-aligned).
 struct WsLayout {
   uint64_t err, ctr_route, nu, u_slot, u_fmt, u_addr, u_nrows, u_rows;
-  uint64_t comb_u, comb_r, comb_w, z, xf, xh, xsc, pa, h, pb, dbg;
+  uint64_t comb_u, comb_r, comb_w, z, xf, xh, xsc, xq, xql, xt, xtl, s16, s16l, xsb, pa, h, hq, hql, hs16, hs16l,
+      hsb, pb, dbg;
   uint64_t fctr, cnt_a, h_cnt, ctr_out, total;  // counters of the fused layer kernel
 };
 constexpr int kDbgSlots = 8;      // per-CTA cycle counters of the diagnostic mode
@@ -153,8 +154,25 @@ __host__ __device__ inline WsLayout make_ws(const Geo& g) {
   w.xf = o; o = al256(o + 4ull * g.M * g.H);
   w.xh = o; o = al256(o + 2ull * g.M * g.H);   // f16(x * 2^s_m): exact, per-row power-of-two scale
   w.xsc = o; o = al256(o + 4ull * kMaxM);      // 2^-s_m
+  // x as X_hi + X_lo / 128 with X_hi = rint(x 2^si) (int16) and X_lo the
+  // int8 residual, each in the two orders of the integer GEMV paths
+  w.xq = o; o = al256(o + 2ull * g.M * g.H);                   // X_hi, "Q order" per 16 columns
+  w.xql = o; o = al256(o + 1ull * g.M * g.H);                  // X_lo, Q order
+  w.xt = o; o = al256(o + 528ull * g.M * (g.H / 256));        // X_hi, "T order" (528 bytes per 256 columns)
+  w.xtl = o; o = al256(o + 272ull * g.M * (g.H / 256));       // X_lo, T order (272 bytes per 256 columns)
+  w.s16 = o; o = al256(o + 4ull * g.M * (g.H / 16));          // int32 sum of X_hi over every 16 columns
+  w.s16l = o; o = al256(o + 4ull * g.M * (g.H / 16));         // ... of X_lo
+  w.xsb = o; o = al256(o + 16ull * g.M * g.nchA);             // 2^-si per 256 columns, 4 slots per K chunk
   w.pa = o; o = al256(o + 4ull * g.U * g.npanA * g.nchA * 2 * g.M * 32);
   w.h = o; o = al256(o + 4ull * g.U * g.M * g.I);
+  // h of every (expert, row) for the integer W2 paths: X_hi / X_lo in the
+  // order of that expert's format (every row has room for T order: 528 + 272
+  // bytes per 256 columns), the 16-column sums, and 2^-si of each 256 columns
+  w.hq = o; o = al256(o + 528ull * g.U * g.M * (g.I / 256));  // every row sized for T order
+  w.hql = o; o = al256(o + 272ull * g.U * g.M * (g.I / 256));
+  w.hs16 = o; o = al256(o + 4ull * g.U * g.M * (g.I / 16));
+  w.hs16l = o; o = al256(o + 4ull * g.U * g.M * (g.I / 16));
+  w.hsb = o; o = al256(o + 16ull * g.U * g.M * g.nchB);       // 2^-si per 256 columns of h, 4 slots per chunk
   w.pb = o; o = al256(o + 4ull * g.U * g.nchB * g.M * g.H);
   w.dbg = o; o = al256(o + 8ull * 3 * kDbgMaxCtas * kDbgSlots);  // [phase A, phase B, router][cta][slot] cycles
   w.fctr = o; o = al256(o + 16);                                  // [0] logits done, [1] CTAs done
@@ -301,6 +319,31 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
+}
+// L2 policy for data fetched ahead of its use in a later kernel of the same
+// call: kept while the streams of evict-first data pass through L2.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// Bulk prefetch of [src, src + bytes) into L2 (bytes and src multiples of 16;
+// no completion to wait for).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// This CTA's share [lo, hi) of n bytes split over `parts` CTAs, on 16-byte
+// boundaries.
+__device__ __forceinline__ void cta_share16(uint64_t n, int part, int parts, uint64_t& lo, uint64_t& hi) {
+  const uint64_t per = ((n + parts - 1) / parts + 15) & ~(uint64_t)15;
+  lo = per * part;
+  hi = lo + per;
+  if (lo > n) lo = n;
+  if (hi > n) hi = n;
 }
 __device__ __forceinline__ float4 ldg_stream_f4(const float4* p, uint64_t pol) {
   float4 v;

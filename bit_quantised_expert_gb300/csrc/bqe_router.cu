@@ -130,6 +130,54 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
       ((float*)(P.ws + P.L.xsc))[tid] = ldexpf(1.0f, -sh);
     }
   }
+  {
+    // x as X_hi + X_lo / 128: X_hi = rint(x 2^si) (int16, max |x| 2^si in
+    // [2^13, 2^14)), X_lo = rint((x 2^si - X_hi) 128) (int8, |X_lo| <= 64), in
+    // the two orders the integer GEMV paths read, and the sums of X_hi and X_lo
+    // over every 16 columns.  One CTA per 256-column block, one column per
+    // thread, so the extra work is spread thinly over the grid.
+    int16_t* xq = (int16_t*)(P.ws + P.L.xq);
+    int8_t* xql = (int8_t*)(P.ws + P.L.xql);
+    int16_t* xt = (int16_t*)(P.ws + P.L.xt);
+    int8_t* xtl = (int8_t*)(P.ws + P.L.xtl);
+    int32_t* s16 = (int32_t*)(P.ws + P.L.s16);
+    int32_t* s16l = (int32_t*)(P.ws + P.L.s16l);
+    const int nbr = H / 256, nblk = M * nbr;
+    for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+      const int m = blk / nbr, bj = blk % nbr;
+      const int si = s_emax[m] == -1000 ? 0 : 13 - s_emax[m];
+      const int64_t q0 = (int64_t)m * H + bj * 256, t0 = (int64_t)m * nbr + bj;
+      const int j = tid;  // column within the block
+      const float v = ldexpf(bf16_to_f32(xs[m * H + bj * 256 + j]), si);
+      const int Xh = __float2int_rn(v);
+      const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
+      const int jj = j & 15, kq = jj & 3, iq = jj >> 2;
+      xq[q0 + (j & ~15) + 4 * kq + 2 * (iq >> 1) + (iq & 1)] = (int16_t)Xh;
+      xql[q0 + (j & ~15) + 4 * kq + iq] = (int8_t)Xl;
+      const int run = j / 20, jr = j % 20, q4 = jr / 5, rd = jr % 5;
+      xt[t0 * 264 + run * 20 + 4 * rd + 2 * (q4 >> 1) + (q4 & 1)] = (int16_t)Xh;
+      xtl[t0 * 272 + run * 20 + 4 * rd + q4] = (int8_t)Xl;
+      int ph = Xh, pl = Xl;
+#pragma unroll
+      for (int o = 8; o; o >>= 1) {
+        ph += __shfl_xor_sync(0xffffffffu, ph, o);
+        pl += __shfl_xor_sync(0xffffffffu, pl, o);
+      }
+      if ((lane & 15) == 0) {
+        s16[(int64_t)m * (H / 16) + bj * 16 + (tid >> 4)] = ph;
+        s16l[(int64_t)m * (H / 16) + bj * 16 + (tid >> 4)] = pl;
+      }
+      if (tid == 0) {  // 2^-si of this block, in the slot of its K chunk
+        const int bpc = g.kcA / 256;
+        ((float*)(P.ws + P.L.xsb))[((int64_t)m * g.nchA + bj / bpc) * 4 + bj % bpc] = ldexpf(1.0f, -si);
+      }
+      if (tid < 16) {  // T-order slots past column 255 (run 12, weights 255 + 1..4) and the padding
+        const int slot = tid < 4 ? 240 + 4 * (tid + 1) + 3 : 260 + (tid - 4);
+        if (tid < 8) xt[t0 * 264 + slot] = 0;
+        xtl[t0 * 272 + slot] = 0;
+      }
+    }
+  }
 
   // ---- router GEMV ----------------------------------------------------------
   float acc[M];
@@ -190,6 +238,17 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
                 (unsigned long long)(clock64() - t_start));
   };
   stamp(0);
+
+  // slot format and offset of every expert, loaded now so the loads overlap
+  // the selection below (out-of-range slots are reported when used)
+  __shared__ int32_t s_sfmt[kMaxE + 1];
+  __shared__ uint64_t s_soff[kMaxE + 1];
+  for (int i = tid; i <= E; i += kRouteThreads) {
+    const int sl = s_table[i];
+    const bool okr = sl >= 0 && sl < P.pool.n_slots;
+    s_sfmt[i] = okr ? P.pool.slot_fmt[sl] : 0;
+    s_soff[i] = okr ? P.pool.slot_off[sl] : 0;
+  }
 
   __shared__ uint32_t s_mask[kMaxE];           // bit m: row m chose expert e
   __shared__ int s_uof[kMaxE];                  // work-list index of a chosen expert
@@ -366,8 +425,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
       set_error(err, BQE_EDEVICE, kErrSlotRange);
       s_bad = 1;
     } else {
-      fmt = P.pool.slot_fmt[slot];
-      const uint64_t off = P.pool.slot_off[slot];
+      fmt = s_sfmt[u == 0 ? E : ee];
+      const uint64_t off = s_soff[u == 0 ? E : ee];
       if (!fmt_ok(fmt)) {
         set_error(err, BQE_EDEVICE, kErrSlotFmt);
         s_bad = 1;
