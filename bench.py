@@ -687,6 +687,24 @@ def run_prefill(args, rank, world):
                timing="eager calls; CUDA events on the calling stream around each call and between its kernels")
     if clk:
         res["clocks"] = clk
+    if args.diag:
+        # per-role cycle accounting of the two GEMM kernels of one more call
+        A.bqe_set_diag(True)
+        call(W.x)
+        torch.cuda.synchronize()
+        A.bqe_set_diag(False)
+        off = A.bqe_prefill_diag_offset(W.d, T)
+        dv = ws[off:off + 8 * 2 * 256 * 12].view(torch.int64).view(2, 256, 12).cpu().numpy().astype(np.float64)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        names = ["load_wait", "dq_wait_raw", "dq_wait_stage", "dq_work", "mma_wait_a", "mma_issue",
+                 "mma_wait_acc", "epi_wait", "epi_work", "cta_total", "items", "mma_wait_b"]
+        rep = {}
+        for gi, gname in enumerate(("gemm_w13", "gemm_w2")):
+            v = dv[gi, :sms]
+            rep[gname] = {n: [round(float(v[:, k].mean()) / 2.07e3, 1), round(float(v[:, k].max()) / 2.07e3, 1)]
+                          for k, n in enumerate(names) if n != "items"}
+            rep[gname]["items_per_cta"] = [float(v[:, 10].mean()), float(v[:, 10].max())]
+        sys.stderr.write("PREFILL_DIAG_us(mean,max over CTAs) " + json.dumps(rep) + "\n")
     # end to end: pinned host x in, host out back, every step
     xh = W.x.cpu().pin_memory()
     oh = torch.empty(T, H, dtype=torch.float32).pin_memory()

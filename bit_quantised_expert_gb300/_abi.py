@@ -77,6 +77,7 @@ SIGNATURES = {
     "bqe_set_variant": (None, [_I32]),
     "bqe_set_prefill_f16": (None, [_I32]),
     "bqe_prefill_kernel_ms": (ctypes.c_int, [_P]),
+    "bqe_prefill_diag_offset": (_U64, [_DESC, _I32]),
     "bqe_set_diag": (None, [_I32]),
     "bqe_set_fused": (None, [_I32]),
     "bqe_diag_offset": (_U64, [_DESC, _I32]),
@@ -258,6 +259,10 @@ def bqe_set_fused(on: bool) -> None:
 
 def bqe_set_prefill_f16(on: bool) -> None:
     lib.bqe_set_prefill_f16(1 if on else 0)
+
+
+def bqe_prefill_diag_offset(d, T: int) -> int:
+    return lib.bqe_prefill_diag_offset(ctypes.byref(d), T)
 
 
 PREFILL_KERNELS = ("logits", "select", "plan", "fill", "gather", "gemm_w13", "gemm_w2", "combine")

@@ -276,11 +276,18 @@ extern "C" int bqe_moe_prefill(const bqe_layer_desc* d, int32_t T, const uint16_
   P.topk_idx = topk_idx;
   P.topk_w = topk_w;
   P.f16 = g_pf_f16.load();
+  P.diag = g_diag.load();
   P.limit_ns = g_wait_limit_ns.load();
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(P.ws + P.L.err, 0, 16, st) != cudaSuccess) return BQE_ECUDA;
   if (cudaMemsetAsync(P.ws + P.L.cnt, 0, 4ull * (P.g.E + 1), st) != cudaSuccess) return BQE_ECUDA;
+  if (P.diag && cudaMemsetAsync(P.ws + P.L.dbg, 0, P.L.total - P.L.dbg, st) != cudaSuccess) return BQE_ECUDA;
   return launch_prefill(P, st, g_diag.load() ? pf_events() : nullptr);
+}
+
+extern "C" uint64_t bqe_prefill_diag_offset(const bqe_layer_desc* d, int32_t T) {
+  if (!desc_ok(d) || T < 1 || T > kPfMaxT) return 0;
+  return make_pf_ws(make_pf_geo(d->hidden, d->inter, d->n_experts, d->top_k, T)).dbg;
 }
 
 extern "C" int bqe_prefill_kernel_ms(float* ms) {

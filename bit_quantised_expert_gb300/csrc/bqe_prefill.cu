@@ -35,6 +35,20 @@ namespace bqe {
 
 enum { kErrPfProducer = 7, kErrPfDequant = 8, kErrPfMma = 9, kErrPfEpilogue = 10, kErrPfRange = 11 };
 
+// Order of the 64 columns of a K-step in the grouped operands of an expert:
+// natural, or "paired" for fp16 Q2_0 (columns j and j + 8 of every 16 next to
+// each other) and Q3_K (j and j + 16 of every 32); see the dequant routines.
+__host__ __device__ inline int paired_col(int fmt, int p) {  // column of K-step position p
+  return fmt == BQE_FMT_Q2_0   ? 16 * (p / 16) + (p % 16) / 2 + 8 * (p % 2)
+         : fmt == BQE_FMT_Q3_K ? 32 * (p / 32) + (p % 32) / 2 + 16 * (p % 2)
+                               : p;
+}
+__host__ __device__ inline int paired_pos(int fmt, int f) {  // position of column f
+  return fmt == BQE_FMT_Q2_0   ? 16 * (f / 16) + 2 * (f % 8) + (f % 16) / 8
+         : fmt == BQE_FMT_Q3_K ? 32 * (f / 32) + 2 * (f % 16) + (f % 32) / 16
+                               : f;
+}
+
 // ----------------------------------------------------------------------------
 // 1. Router logits: z (T x E) = x (T x H, bf16) . Wr (E x H, fp32)^T, fp32.
 // Tile 128 tokens x 64 experts x 32 columns, 256 threads, 8 x 4 per thread.
@@ -367,34 +381,45 @@ __global__ void __launch_bounds__(256) k_pf_gather(PfParams P) {
   if (tile >= ((const int32_t*)(P.ws + P.L.ctr))[0]) return;
   const int3 tl = ((const int3*)(P.ws + P.L.tile))[tile];
   const bool f16 = ((const int32_t*)(P.ws + P.L.gf16))[tl.x] != 0;
+  const int gfmt = ((const int32_t*)(P.ws + P.L.gfmt))[tl.x];
+  const int order = f16 && (gfmt == BQE_FMT_Q2_0 || gfmt == BQE_FMT_Q3_K) ? gfmt : 0;
   const int npad = (tl.z + 15) & ~15;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int H = P.g.H;
   const int64_t R8 = P.g.R / 8;
   uint8_t* xp = P.ws + P.L.xp;
+  auto cvt2 = [&](uint32_t lo_bits, uint32_t hi_bits, float scale) -> uint32_t {  // two bf16 -> operand type
+    const float lo = __uint_as_float(lo_bits << 16) * scale, hi = __uint_as_float(hi_bits << 16) * scale;
+    if (f16) {
+      const __half2 h2 = __floats2half2_rn(lo, hi);
+      return *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);  // exact: scaled bf16
+  };
   for (int r = warp; r < npad; r += 8) {
     const int p = tl.y + r;
     const int tok = ((const int32_t*)(P.ws + P.L.prow_tok))[p];
     const float scale = 1.0f / ((const float*)(P.ws + P.L.prow_sc))[p];  // 2^s, exact
-    const uint4* src = reinterpret_cast<const uint4*>(P.x + (int64_t)(tok < 0 ? 0 : tok) * H);
-    for (int i = lane; i < H / 8; i += 32) {
+    const uint16_t* xrow = P.x + (int64_t)(tok < 0 ? 0 : tok) * H;
+    for (int i = lane; i < H / 8; i += 32) {  // 16-byte chunk i = K-step i / 8, chunk i % 8
+      const int ks = i >> 3, c = i & 7;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (tok >= 0) {
-        const uint4 b = src[i];
-        uint32_t w[4] = {b.x, b.y, b.z, b.w};
+        uint32_t w[4];
+        if (order == 0) {
+          const uint4 b = reinterpret_cast<const uint4*>(xrow)[i];
+          w[0] = b.x; w[1] = b.y; w[2] = b.z; w[3] = b.w;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float lo = __uint_as_float(w[k] << 16) * scale, hi = __uint_as_float(w[k] & 0xFFFF0000u) * scale;
-          if (f16) {
-            const __half2 h2 = __floats2half2_rn(lo, hi);
-            w[k] = *reinterpret_cast<const uint32_t*>(&h2);
-          } else {
-            w[k] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);  // exact: scaled bf16
+          for (int k = 0; k < 4; ++k) w[k] = cvt2(w[k] & 0xFFFFu, w[k] >> 16, scale);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int p0 = 8 * c + 2 * k;
+            w[k] = cvt2(xrow[ks * 64 + paired_col(order, p0)], xrow[ks * 64 + paired_col(order, p0 + 1)], scale);
           }
         }
         v = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      const int ks = i >> 3, c = i & 7;
       *reinterpret_cast<uint4*>(xp + ((int64_t)ks * R8 + (p >> 3)) * 1024 + sw128_offset(p & 7, c)) = v;
     }
   }
@@ -505,23 +530,26 @@ __device__ __forceinline__ void dq_mxfp4(const uint8_t* P, int kq, int lane, uin
 
 // TQ1, K-step KQ = weights 64 KQ .. 64 KQ + 63 of the 256-weight block.  Byte
 // i < 51 holds weights 5i .. 5i+4 as base-3 digits (least significant first,
-// digit = t + 1), byte 51 holds weight 255; w = d t.
-template <int KQ, bool F16>
-__device__ __forceinline__ void dq_tq1_k(const uint32_t (&W)[14], float d, uint8_t* A, int row) {
+// digit t = w/d + 1), byte 51 holds weight 255.  A weight is one of -d, 0, +d:
+// a byte permute picks its 16-bit pattern from a 3-entry table, two weights
+// per permute (selector nibbles 2t, 2t + 1 of each).
+template <int KQ>
+__device__ __forceinline__ void dq_tq1_k(const uint32_t (&W)[14], uint32_t tab_lo, uint32_t tab_hi, uint8_t* A,
+                                         int row) {
   constexpr int J0 = 64 * KQ;
   constexpr int B0 = J0 / 5;
   constexpr int B1 = (J0 + 63) / 5 < 51 ? (J0 + 63) / 5 : 51;
-  float t[(B1 - B0 + 1) * 5];
+  uint32_t t[(B1 - B0 + 1) * 5];
 #pragma unroll
   for (int i = B0; i <= B1; ++i) {
     uint32_t v = (W[i >> 2] >> (8 * (i & 3))) & 0xFFu;
     if (i == 51) {
-      t[(i - B0) * 5] = (float)((int)(v % 3u) - 1);
+      t[(i - B0) * 5] = v;  // 0..2
     } else {
 #pragma unroll
       for (int r = 0; r < 5; ++r) {
         const uint32_t q = (v * 171u) >> 9;  // v / 3 for v <= 255
-        t[(i - B0) * 5 + r] = (float)((int)(v - 3u * q) - 1);
+        t[(i - B0) * 5 + r] = v - 3u * q;
         v = q;
       }
     }
@@ -532,7 +560,7 @@ __device__ __forceinline__ void dq_tq1_k(const uint32_t (&W)[14], float d, uint8
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int j = J0 + 8 * c + 2 * i - 5 * B0;
-      o[i] = pack2<F16>(d * t[j], d * t[j + 1]);
+      o[i] = __byte_perm(tab_lo, tab_hi, 0x1010u + t[j] * 0x22u + t[j + 1] * 0x2200u);
     }
     store_chunk(A, row, c, o[0], o[1], o[2], o[3]);
   }
@@ -548,12 +576,95 @@ __device__ __forceinline__ void dq_tq1(const uint8_t* P, int kq, int lane, uint8
   const uint2 tail = *reinterpret_cast<const uint2*>(P + 1536 + lane * 8);
   W[12] = tail.x;
   W[13] = tail.y;
-  const float d = __half2float(__ushort_as_half((unsigned short)(tail.y & 0xFFFFu)));
+  // d in the operand type (fp16: exact; bf16: rounded), then the table
+  // {-d, 0 | +d, .}: selector values 0, 2, 4 pick bytes of -d, 0, +d
+  const uint32_t dbits =
+      F16 ? (tail.y & 0xFFFFu)
+          : (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__half2float(__ushort_as_half((unsigned short)(tail.y & 0xFFFFu)))));
+  const uint32_t tab_lo = dbits ^ 0x8000u, tab_hi = dbits;
   switch (kq) {
-    case 0: dq_tq1_k<0, F16>(W, d, A, row); break;
-    case 1: dq_tq1_k<1, F16>(W, d, A, row); break;
-    case 2: dq_tq1_k<2, F16>(W, d, A, row); break;
-    default: dq_tq1_k<3, F16>(W, d, A, row); break;
+    case 0: dq_tq1_k<0>(W, tab_lo, tab_hi, A, row); break;
+    case 1: dq_tq1_k<1>(W, tab_lo, tab_hi, A, row); break;
+    case 2: dq_tq1_k<2>(W, tab_lo, tab_hi, A, row); break;
+    default: dq_tq1_k<3>(W, tab_lo, tab_hi, A, row); break;
+  }
+}
+
+// fp16 operand paths of Q2_0 and Q3_K in the "paired" K order of a 64-column
+// K-step (the grouped x and h are stored in the same order, so the products
+// are unchanged): Q2_0 pairs weights j and j + 8 of every 16, Q3_K weights
+// j and j + 16 of every 32, which one shift and mask of the packed codes give
+// at once.  The codes become exact small integers in both fp16 lanes (bits
+// ORed under the exponent of 1024), one fp16x2 subtract removes the offset
+// and one fp16x2 multiply applies the scale, rounding once.
+__device__ __forceinline__ uint32_t h2sub(uint32_t a, uint32_t b) {
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t h2mul(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ void dq_q2_0_paired(const uint8_t* P, int kq, int lane, uint8_t* A, int row, bool& bad) {
+  const uint4 c4 = *reinterpret_cast<const uint4*>(P + kq * 512 + lane * 16);
+  const uint32_t db = *reinterpret_cast<const uint16_t*>(P + 2048 + (kq * 32 + lane) * 2);
+  if (!(3.f * fabsf(__half2float(__ushort_as_half((unsigned short)db))) <= kF16Max)) bad = true;
+  const uint32_t d2 = db | (db << 16);
+  const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = 4 * half + i;
+        const uint32_t sh = j == 0 ? (wd[w] << 1) : (wd[w] >> (2 * j - 1));  // 2 q_j, 2 q_{j+8} at bits 1, 17
+        const uint32_t x = (sh & 0x00060006u) | 0x64006400u;                  // 1024 + 2q in each lane
+        o[i] = h2mul(h2sub(x, 0x64036403u), d2);                              // d (2q - 3)
+      }
+      store_chunk(A, row, 2 * w + half, o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+__device__ __forceinline__ void dq_q3k_paired(const uint8_t* P, int kq, int lane, uint8_t* A, int row, bool& bad) {
+  const uint4 lo4 = *reinterpret_cast<const uint4*>(P + kq * 512 + lane * 16);
+  const uint2 hi2 = *reinterpret_cast<const uint2*>(P + 2048 + (kq >> 1) * 512 + lane * 16 + (kq & 1) * 8);
+  const uint32_t* scw = reinterpret_cast<const uint32_t*>(P + 3072 + lane * 12);
+  const uint32_t sc[4] = {scw[0], scw[1], scw[2], 0u};
+  const float d = __half2float(*reinterpret_cast<const __half*>(P + 3456 + lane * 2));
+  const uint32_t lo[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
+#pragma unroll
+  for (int mp = 0; mp < 2; ++mp) {  // sub-blocks a = 4 kq + 2 mp and b = a + 1
+    float dsv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int bit = 6 * (4 * kq + 2 * mp + e);
+      const uint64_t two = (uint64_t)sc[bit >> 5] | ((uint64_t)sc[(bit >> 5) + 1] << 32);
+      dsv[e] = d * (float)((uint32_t)(two >> (bit & 31)) & 63u);
+      if (!(4.f * fabsf(dsv[e]) <= kF16Max)) bad = true;
+    }
+    const __half2 ds2h = __floats2half2_rn(dsv[0], dsv[1]);
+    const uint32_t ds2 = *reinterpret_cast<const uint32_t*>(&ds2h);
+    const uint32_t X = __byte_perm(lo[2 * mp], lo[2 * mp + 1], 0x5410);  // codes 0..7 of a | of b
+    const uint32_t Y = __byte_perm(lo[2 * mp], lo[2 * mp + 1], 0x7632);  // codes 8..15 of a | of b
+    const uint32_t H = mp == 0 ? hi2.x : hi2.y;                            // high bits of a | of b
+#pragma unroll
+    for (int cq = 0; cq < 4; ++cq) {
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = 4 * cq + i;
+        const uint32_t src = j < 8 ? X : Y;
+        const uint32_t lo2 = (src >> (2 * (j & 7))) & 0x00030003u;
+        const uint32_t hb = j < 2 ? (H << (2 - j)) : (H >> (j - 2));  // bits j, 16 + j at 2, 18
+        const uint32_t x = (lo2 | (hb & 0x00040004u)) | 0x64006400u;   // 1024 + q in each lane
+        o[i] = h2mul(h2sub(x, 0x64046404u), ds2);                      // d s (q - 4)
+      }
+      store_chunk(A, row, 4 * mp + cq, o[0], o[1], o[2], o[3]);
+    }
   }
 }
 
@@ -595,21 +706,39 @@ __device__ __forceinline__ void dq_q3k(const uint8_t* P, int kq, int lane, uint8
 }
 
 // One 64-column K-step of the lane's row, as fp16 (f16) or bf16.  `bad` is set
-// when an fp16 weight would leave the fp16 range.
+// when an fp16 weight would leave the fp16 range.  fp16 Q2_0 / Q3_K use the
+// paired K order.
 __device__ __forceinline__ void dequant_kstep(int fmt, bool f16, const uint8_t* P, int kq, int lane, uint8_t* A,
                                               int row, bool& bad) {
   switch (fmt) {
     case BQE_FMT_Q2_0:
-      if (f16) dq_q2_0<true>(P, kq, lane, A, row, bad); else dq_q2_0<false>(P, kq, lane, A, row, bad);
+      if (f16) dq_q2_0_paired(P, kq, lane, A, row, bad); else dq_q2_0<false>(P, kq, lane, A, row, bad);
       break;
     case BQE_FMT_MXFP4: dq_mxfp4(P, kq, lane, A, row); break;
     case BQE_FMT_TQ1:
       if (f16) dq_tq1<true>(P, kq, lane, A, row); else dq_tq1<false>(P, kq, lane, A, row);
       break;
     default:
-      if (f16) dq_q3k<true>(P, kq, lane, A, row, bad); else dq_q3k<false>(P, kq, lane, A, row, bad);
+      if (f16) dq_q3k_paired(P, kq, lane, A, row, bad); else dq_q3k<false>(P, kq, lane, A, row, bad);
       break;
   }
+}
+// K-step order of a group's grouped operands: paired for fp16 Q2_0 / Q3_K.
+__device__ __forceinline__ int kstep_order(int fmt, bool f16) {
+  return f16 && (fmt == BQE_FMT_Q2_0 || fmt == BQE_FMT_Q3_K) ? fmt : 0;
+}
+
+__device__ __forceinline__ long long pf_clk() { return clock64(); }
+__device__ __forceinline__ void pf_dbg(const PfParams& P, int ph, int slot, long long v) {
+  if (P.diag && blockIdx.x < kPfDbgCtas)
+    atomicAdd((unsigned long long*)(P.ws + P.L.dbg) + ((size_t)ph * kPfDbgCtas + blockIdx.x) * kPfDbgSlots + slot,
+              (unsigned long long)v);
+}
+
+// Stages of the B area for a tile of npad rows: as many as fit, at most kPfBMaxStages.
+__device__ __forceinline__ int b_stages(int npad) {
+  const int n = (int)(kPfBStages * kPfBStage / ((uint32_t)npad * 128u));
+  return n < kPfBMaxStages ? n : kPfBMaxStages;
 }
 
 struct PfItem {
@@ -636,6 +765,7 @@ template <int PH>
 __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
   extern __shared__ uint8_t pf_smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)pf_smem_raw + 1023) & ~(uintptr_t)1023);
+  const long long t_cta = clock64();
   uint8_t* sA = sm + kPfOffA;
   uint8_t* sB = sm + kPfOffB;
   uint8_t* sRaw = sm + kPfOffRaw;
@@ -643,10 +773,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
   uint64_t* bars = (uint64_t*)(sm + kPfOffBar);
   uint64_t* raw_full = bars;                        // [kPfRawStages]
   uint64_t* raw_empty = bars + kPfRawStages;        // [kPfRawStages]
-  uint64_t* a_full = bars + 2 * kPfRawStages;       // [kPfStages]
-  uint64_t* b_full = a_full + kPfStages;            // [kPfStages]
-  uint64_t* st_empty = b_full + kPfStages;          // [kPfStages]
-  uint64_t* acc_full = st_empty + kPfStages;        // [2]
+  uint64_t* a_full = bars + 2 * kPfRawStages;       // [kPfAStages]
+  uint64_t* a_empty = a_full + kPfAStages;          // [kPfAStages]
+  uint64_t* b_full = a_empty + kPfAStages;          // [kPfBMaxStages]
+  uint64_t* b_empty = b_full + kPfBMaxStages;       // [kPfBMaxStages]
+  uint64_t* acc_full = b_empty + kPfBMaxStages;     // [2]
   uint64_t* acc_empty = acc_full + 2;               // [2]
   uint64_t* fin = acc_empty + 2;
   uint32_t* s_tmem = (uint32_t*)(fin + 1);
@@ -664,16 +795,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
 
   if (tid == 0) {
     for (int i = 0; i < kPfRawStages; ++i) { mbar_init(&raw_full[i], 1); mbar_init(&raw_empty[i], kPfDqWarps); }
-    for (int i = 0; i < kPfStages; ++i) {
+    for (int i = 0; i < kPfAStages; ++i) {
       mbar_init(&a_full[i], 4);
+      mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < kPfBMaxStages; ++i) {
       mbar_init(&b_full[i], 1);
-      mbar_init(&st_empty[i], 1);
+      mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], 4); }
     mbar_init(fin, 1);
     fence_mbar_init();
   }
-  constexpr int kWLoad = kPfDqWarps, kWMma = kPfDqWarps + 1, kWEpi = kPfDqWarps + 2;
+  // roles: dequant warps, raw-weight load warp, B load warp, MMA warp, epilogue warps
+  constexpr int kWRaw = kPfDqWarps, kWB = kPfDqWarps + 1, kWMma = kPfDqWarps + 2, kWEpi = kPfDqWarps + 3;
   if (warp == kWMma) {
     tmem_alloc(s_tmem, 512);
     tmem_relinquish();
@@ -683,84 +818,118 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == kWLoad) {
-    // ---------------- loads: raw weight groups and B tiles ----------------
+  if (warp == kWRaw || warp == kWB) {
+    // ---------------- loads: one warp (lane 0) the raw weight groups, the
+    // other the B tiles, each as far ahead as its own ring allows (separate
+    // warps: a sleeping wait of one never holds the other) ----------------
     if (lane == 0) {
       const uint8_t* bsrc = P.ws + (PH == 0 ? P.L.xp : P.L.hp);
-      uint32_t nr = 0, nbs = 0;  // raw groups and B stages issued so far
+      const bool raw_lane = warp == kWRaw;
+      uint32_t nis = 0;  // issues of this lane's ring so far
+      uint32_t b_par = 0, b_used = 0;  // B lane: per barrier, uses mod 2 and whether used
+      int last_b = -1;
       bool ok = true;
+      long long c_wait = 0;
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
         const PfItem it = pf_item(P, item, nblk);
         const int fmt = it.fmt;
-        const uint64_t m13 = matrix_bytes(fmt, g.I, g.H);
-        const uint32_t tb = tile_bytes(fmt, kc);
-        const int nb = kc / fmt_bw(fmt);
-        const uint8_t* mat[4];
-        int panel[4];
+        if (raw_lane) {
+          const uint64_t m13 = matrix_bytes(fmt, g.I, g.H);
+          const uint32_t tb = tile_bytes(fmt, kc);
+          const int nb = kc / fmt_bw(fmt);
+          const uint8_t* mat[4];
+          int panel[4];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          if (PH == 0) {
-            mat[w] = it.base + (w < 2 ? 0 : m13);
-            panel[w] = 2 * it.blk + (w & 1);
-          } else {
-            mat[w] = it.base + 2 * m13;
-            panel[w] = 4 * it.blk + w;
+          for (int w = 0; w < 4; ++w) {
+            if (PH == 0) {
+              mat[w] = it.base + (w < 2 ? 0 : m13);
+              panel[w] = 2 * it.blk + (w & 1);
+            } else {
+              mat[w] = it.base + 2 * m13;
+              panel[w] = 4 * it.blk + w;
+            }
           }
-        }
-        const uint32_t bbytes = (uint32_t)it.npad * 128u;
-        for (int grp = 0; grp < ngrp && ok; ++grp) {
-          const int c = grp / gpc, gi = grp % gpc;
-          const uint32_t rs = nr % kPfRawStages, rph = (nr / kPfRawStages) & 1;
-          if (!mbar_wait_bounded(&raw_empty[rs], rph ^ 1, lim)) { ok = false; break; }
-          mbar_arrive_expect_tx(&raw_full[rs], 4 * raw_group_bytes(fmt));
+          for (int grp = 0; grp < ngrp; ++grp) {
+            const int c = grp / gpc, gi = grp % gpc;
+            const uint32_t rs = nis % kPfRawStages, rph = (nis / kPfRawStages) & 1;
+            const long long tw = pf_clk();
+            if (!mbar_wait_sleep_bounded(&raw_empty[rs], rph ^ 1, lim)) { ok = false; break; }
+            c_wait += pf_clk() - tw;
+            mbar_arrive_expect_tx(&raw_full[rs], 4 * raw_group_bytes(fmt));
 #pragma unroll
-          for (int w = 0; w < 4; ++w)
-            issue_raw_group(fmt, mat[w] + ((uint64_t)panel[w] * nch + c) * tb, nb, gi,
-                            sRaw + rs * kPfRawStage + w * kPfRawPanel, &raw_full[rs]);
-          ++nr;
-          for (int kq = 0; kq < 4; ++kq) {
-            const int ks = grp * 4 + kq;
-            const uint32_t s = nbs % kPfStages, sph = (nbs / kPfStages) & 1;
-            if (!mbar_wait_bounded(&st_empty[s], sph ^ 1, lim)) { ok = false; break; }
-            mbar_arrive_expect_tx(&b_full[s], bbytes);
-            bulk_g2s(sB + s * kPfBStage, bsrc + ((uint64_t)ks * R8 + (it.row0 >> 3)) * 1024, bbytes, &b_full[s]);
-            ++nbs;
+            for (int w = 0; w < 4; ++w)
+              issue_raw_group(fmt, mat[w] + ((uint64_t)panel[w] * nch + c) * tb, nb, gi,
+                              sRaw + rs * kPfRawStage + w * kPfRawPanel, &raw_full[rs]);
+            ++nis;
+          }
+        } else {
+          // the B area is re-split for this item's row count; every stage of
+          // the previous split is released first (per-barrier use parities)
+          const uint32_t bbytes = (uint32_t)it.npad * 128u;
+          const int nsb = b_stages(it.npad);
+          const long long tw = pf_clk();
+          for (int i = 0; i < kPfBMaxStages && ok; ++i)
+            if ((b_used >> i) & 1u)
+              ok = mbar_wait_sleep_bounded(&b_empty[i], ((b_par >> i) & 1u) ^ 1u, lim);
+          c_wait += pf_clk() - tw;
+          for (int ks = 0; ks < ngrp * 4 && ok; ++ks) {
+            const int sb = ks % nsb;
+            if (ks >= nsb) {  // stage sb was used earlier in this item: wait for its release
+              const long long t2 = pf_clk();
+              if (!mbar_wait_sleep_bounded(&b_empty[sb], ((b_par >> sb) & 1u) ^ 1u, lim)) { ok = false; break; }
+              c_wait += pf_clk() - t2;
+            }
+            mbar_arrive_expect_tx(&b_full[sb], bbytes);
+            bulk_g2s(sB + (uint32_t)sb * bbytes, bsrc + ((uint64_t)ks * R8 + (it.row0 >> 3)) * 1024, bbytes,
+                     &b_full[sb]);
+            b_par ^= 1u << sb;  // uses of barrier sb, mod 2
+            b_used |= 1u << sb;
+            last_b = sb;
+            ++nis;
           }
         }
       }
       if (!ok) set_error(err, BQE_ETIMEOUT, kErrPfProducer);
-      // every copy this thread started has landed before the CTA may exit:
-      // the last (up to ring size) issues of each ring are the only ones
-      // that can still be in flight
-      for (uint32_t i = 0; i < kPfRawStages && i < nr; ++i) {
-        const uint32_t n = nr - 1 - i;
-        mbar_wait_bounded(&raw_full[n % kPfRawStages], (n / kPfRawStages) & 1, lim);
+      if (raw_lane) pf_dbg(P, PH, 0, c_wait);
+      // every copy this lane started has landed before the CTA may exit
+      if (raw_lane) {  // the last (up to ring size) issues are the only ones still in flight
+        for (uint32_t i = 0; i < kPfRawStages && i < nis; ++i) {
+          const uint32_t n = nis - 1 - i;
+          mbar_wait_sleep_bounded(&raw_full[n % kPfRawStages], (n / kPfRawStages) & 1, lim);
+        }
+      } else {  // the last use of every B barrier
+        for (int i = 0; i < kPfBMaxStages; ++i)
+          if ((b_used >> i) & 1u) mbar_wait_sleep_bounded(&b_full[i], ((b_par >> i) & 1u) ^ 1u, lim);
       }
-      for (uint32_t i = 0; i < kPfStages && i < nbs; ++i) {
-        const uint32_t n = nbs - 1 - i;
-        mbar_wait_bounded(&b_full[n % kPfStages], (n / kPfStages) & 1, lim);
-      }
+      (void)last_b;
     }
   } else if (warp < kPfDqWarps) {
     // ---------------- dequant: panel warp % 4 (A rows 32 (warp % 4) ..), K-steps n % sets == warp / 4
     const int set = warp / 4, pw = warp % 4;
     uint32_t nr = 0, n = 0;  // raw groups and K-steps passed so far (the whole CTA's sequence)
     bool ok = true, bad = false;
+    long long c_raw = 0, c_st = 0, c_work = 0;
     const int row = pw * 32 + lane;
     for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x) {
       const PfItem it = pf_item(P, item, nblk);
       for (int grp = 0; grp < ngrp && ok; ++grp) {
         const uint32_t rs = nr % kPfRawStages, rph = (nr / kPfRawStages) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&raw_full[rs], rph, lim))) { ok = false; break; }
+        long long t0 = pf_clk();
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep_bounded(&raw_full[rs], rph, lim))) { ok = false; break; }
+        c_raw += pf_clk() - t0;
         const uint8_t* praw = sRaw + rs * kPfRawStage + pw * kPfRawPanel;
         for (int kq = 0; kq < 4; ++kq, ++n) {
           if ((int)(n % kPfDqSets) != set) continue;
-          const uint32_t s = n % kPfStages, sph = (n / kPfStages) & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&st_empty[s], sph ^ 1, lim))) { ok = false; break; }
+          const uint32_t s = n % kPfAStages, sph = (n / kPfAStages) & 1;
+          t0 = pf_clk();
+          if (!__all_sync(0xffffffffu, mbar_wait_sleep_bounded(&a_empty[s], sph ^ 1, lim))) { ok = false; break; }
+          const long long t1 = pf_clk();
+          c_st += t1 - t0;
           dequant_kstep(it.fmt, it.f16, praw, kq, lane, sA + s * kPfAStage, row, bad);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&a_full[s]);
+          c_work += pf_clk() - t1;
         }
         if (!ok) break;
         __syncwarp();
@@ -770,41 +939,63 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
     }
     if (!ok && lane == 0) set_error(err, BQE_ETIMEOUT, kErrPfDequant);
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, BQE_EUNSUPPORTED, kErrPfRange);
+    if (lane == 0 && warp == 0) {
+      pf_dbg(P, PH, 1, c_raw);
+      pf_dbg(P, PH, 2, c_st);
+      pf_dbg(P, PH, 3, c_work);
+    }
   } else if (warp == kWMma) {
     // ---------------- MMA issue (one thread) ----------------
     if (lane == 0) {
-      int s = 0;
-      uint32_t sph = 0;
+      uint32_t n = 0;  // K-steps consumed so far
+      uint32_t bf_par = 0;  // per B barrier: completions consumed, mod 2
       bool ok = true;
       int lc = 0;
+      long long c_op = 0, c_iss = 0, c_acc = 0, c_opb = 0;
       for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++lc) {
         const PfItem it = pf_item(P, item, nblk);
         const int ab = lc & 1;
         const uint32_t aph = (lc >> 1) & 1;
-        if (!mbar_wait_bounded(&acc_empty[ab], aph ^ 1, lim)) { ok = false; break; }
+        long long t0 = pf_clk();
+        if (!mbar_wait_sleep_bounded(&acc_empty[ab], aph ^ 1, lim)) { ok = false; break; }
+        c_acc += pf_clk() - t0;
         tc_fence_after();
         const uint32_t d = tmem + ab * 256;
         const uint32_t idesc = umma_idesc_f16(128, it.npad, !it.f16);
-        for (int ks = 0; ks < ngrp * 4; ++ks) {
-          if (!mbar_wait_bounded(&a_full[s], sph, lim) || !mbar_wait_bounded(&b_full[s], sph, lim)) {
-            ok = false;
-            break;
-          }
+        const int nsb = b_stages(it.npad);
+        const uint32_t bbytes = (uint32_t)it.npad * 128u;
+        for (int ks = 0; ks < ngrp * 4; ++ks, ++n) {
+          const uint32_t sa = n % kPfAStages, pa_ = (n / kPfAStages) & 1;
+          const uint32_t sb = (uint32_t)(ks % nsb), pb_ = (bf_par >> sb) & 1u;
+          t0 = pf_clk();
+          if (!mbar_wait_sleep_bounded(&a_full[sa], pa_, lim)) { ok = false; break; }
+          const long long tm = pf_clk();
+          if (!mbar_wait_sleep_bounded(&b_full[sb], pb_, lim)) { ok = false; break; }
+          const long long t1 = pf_clk();
+          c_op += tm - t0;
+          c_opb += t1 - tm;
           tc_fence_after();
-          const uint64_t da = umma_desc_sw128(sA + s * kPfAStage);
-          const uint64_t db = umma_desc_sw128(sB + s * kPfBStage);
+          const uint64_t da = umma_desc_sw128(sA + sa * kPfAStage);
+          const uint64_t db = umma_desc_sw128(sB + sb * bbytes);
+          bf_par ^= 1u << sb;
 #pragma unroll
           for (int k16 = 0; k16 < 4; ++k16) umma_f16(d, da + 2 * k16, db + 2 * k16, idesc, (ks | k16) != 0);
-          umma_commit(&st_empty[s]);
-          if (++s == kPfStages) { s = 0; sph ^= 1; }
+          umma_commit(&a_empty[sa]);
+          umma_commit(&b_empty[sb]);
+          c_iss += pf_clk() - t1;
         }
         if (!ok) break;
         umma_commit(&acc_full[ab]);
       }
       if (!ok) set_error(err, BQE_ETIMEOUT, kErrPfMma);
+      pf_dbg(P, PH, 4, c_op);
+      pf_dbg(P, PH, 5, c_iss);
+      pf_dbg(P, PH, 6, c_acc);
+      pf_dbg(P, PH, 10, lc);
+      pf_dbg(P, PH, 11, c_opb);
       // all MMAs issued by this thread are complete before tensor memory is freed
       umma_commit(fin);
-      mbar_wait_bounded(fin, 0, lim);
+      mbar_wait_sleep_bounded(fin, 0, lim);
     }
   } else {
     // ---------------- epilogue: warps 6-9, lane quarter warp % 4 ----------------
@@ -812,12 +1003,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
     const int et = tid - kWEpi * 32;  // 0..127
     bool ok = true;
     int lc = 0;
+    long long c_ew = 0, c_ek = 0;
     for (int item = blockIdx.x; item < nitems && ok; item += gridDim.x, ++lc) {
       const PfItem it = pf_item(P, item, nblk);
       const int ab = lc & 1;
       const uint32_t aph = (lc >> 1) & 1;
-      const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[ab], aph, lim));
+      const long long t0 = pf_clk();
+      const bool got = __all_sync(0xffffffffu, mbar_wait_sleep_bounded(&acc_full[ab], aph, lim));
       if (named_bar_or(1, 128, !got)) { ok = false; break; }
+      const long long t1 = pf_clk();
+      c_ew += t1 - t0;
       tc_fence_after();
       const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + ab * 256;
       if (PH == 0) {
@@ -825,6 +1020,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
         uint16_t* htile = (uint16_t*)(sEpi + 64 * 17);            // [16 tokens][64 features] 16-bit
         uint8_t* hp = P.ws + P.L.hp;
         const float* prow_sc = (const float*)(P.ws + P.L.prow_sc);
+        const int hord = kstep_order(it.fmt, it.f16);
         for (int c0 = 0; c0 < it.npad; c0 += 16) {
           float v[16];
           tmem_ld16(tq + c0, v);
@@ -841,11 +1037,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
             for (int i = 0; i < 16; ++i) {
               const float u = ubuf[(q * 32 + lane) * 17 + i];
               const float hv = silu_f(v[i] * __shfl_sync(0xffffffffu, scl, i)) * u;
+              const int hpos = paired_pos(hord, q * 32 + lane);  // the W2 K-step order of this expert
               if (it.f16) {
                 big |= !(fabsf(hv) <= kF16Max);
-                htile[i * 64 + q * 32 + lane] = __half_as_ushort(__float2half_rn(hv));
+                htile[i * 64 + hpos] = __half_as_ushort(__float2half_rn(hv));
               } else {
-                htile[i * 64 + q * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+                htile[i * 64 + hpos] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
               }
             }
             if (__any_sync(0xffffffffu, big) && lane == 0) set_error(err, BQE_EUNSUPPORTED, kErrPfRange);
@@ -887,13 +1084,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) k_pf_gemm(PfParams P) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      c_ek += pf_clk() - t1;
     }
     if (!ok && et == 0) set_error(err, BQE_ETIMEOUT, kErrPfEpilogue);
+    if (et == 0) {
+      pf_dbg(P, PH, 7, c_ew);
+      pf_dbg(P, PH, 8, c_ek);
+    }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0) pf_dbg(P, PH, 9, clock64() - t_cta);
   if (warp == kWMma) tmem_dealloc(tmem, 512);
 }
 

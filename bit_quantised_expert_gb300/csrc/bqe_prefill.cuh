@@ -11,22 +11,24 @@ namespace bqe {
 
 constexpr int kPfTileN = 256;       // token rows per GEMM tile (MMA N, multiple of 16)
 constexpr int kPfRowAlign = 16;     // every expert's row range starts on a multiple of 16
-constexpr int kPfStages = 3;        // A/B operand ring (one 64-column K-step per stage)
-constexpr int kPfRawStages = 3;     // quantised-weight ring (one 256-column group per stage)
+constexpr int kPfAStages = 5;       // dequantised A ring (one 64-column K-step per stage)
+constexpr int kPfBStages = 3;       // B (token rows) area: 3 stages of 256 rows, re-split per item
+constexpr int kPfBMaxStages = 16;   // stages of the B area for short tiles (area / (rows * 128 bytes), at most)
+constexpr int kPfRawStages = 2;     // quantised-weight ring (one 256-column group per stage)
 constexpr uint32_t kPfRawPanel = 4352;                 // 32 rows x 256 columns, largest format (MXFP4)
 constexpr uint32_t kPfRawStage = 4 * kPfRawPanel;      // four 32-row panels = one 128-row A tile
 constexpr uint32_t kPfAStage = 128 * 128;              // 128 rows x 64 16-bit values
 constexpr uint32_t kPfBStage = kPfTileN * 128;         // 256 rows x 64 16-bit values
 constexpr uint32_t kPfEpiBytes = 4 * 16 * 33 * 4;      // epilogue staging (largest of the two phases)
 constexpr uint32_t kPfOffA = 0;
-constexpr uint32_t kPfOffB = kPfOffA + kPfStages * kPfAStage;
-constexpr uint32_t kPfOffRaw = kPfOffB + kPfStages * kPfBStage;
+constexpr uint32_t kPfOffB = kPfOffA + kPfAStages * kPfAStage;
+constexpr uint32_t kPfOffRaw = kPfOffB + kPfBStages * kPfBStage;
 constexpr uint32_t kPfOffEpi = kPfOffRaw + kPfRawStages * kPfRawStage;
 constexpr uint32_t kPfOffBar = kPfOffEpi + kPfEpiBytes;
 constexpr uint32_t kPfSmemBytes = kPfOffBar + 256 + 1024;  // + barriers + alignment slack
 constexpr int kPfDqSets = 2;       // sets of 4 dequant warps; set j takes the K-steps n with n % sets == j
 constexpr int kPfDqWarps = 4 * kPfDqSets;
-constexpr int kPfThreads = 32 * (kPfDqWarps + 6);  // dequant warps, then loads, MMA, 4 epilogue warps
+constexpr int kPfThreads = 32 * (kPfDqWarps + 7);  // dequant warps, then 2 load warps, MMA, 4 epilogue warps
 constexpr int kPfMaxE = 1024;
 
 struct PfGeo {
@@ -48,9 +50,15 @@ __host__ __device__ inline PfGeo make_pf_geo(int H, int I, int E, int K, int T) 
   return g;
 }
 
+constexpr int kPfDbgCtas = 256, kPfDbgSlots = 12;
+// diagnostic counters (cycles, summed over the CTA's work): 0 load warp waiting
+// for a free raw / B stage, 1 dequant waiting raw data, 2 dequant waiting a free
+// A stage, 3 dequant working, 4 MMA waiting operands, 5 MMA issuing, 6 MMA
+// waiting a free accumulator, 7 epilogue waiting, 8 epilogue working, 9 CTA
+// total, 10 items
 struct PfLayout {
   uint64_t err, ctr, z, idx, w, tok_sc, cnt, goff, gaddr, gfmt, gf16, tile, prow_tok, prow_w, prow_sc, pos, xp, hp, y,
-      total;
+      dbg, total;
 };
 
 __host__ __device__ inline PfLayout make_pf_ws(const PfGeo& g) {
@@ -75,6 +83,7 @@ __host__ __device__ inline PfLayout make_pf_ws(const PfGeo& g) {
   L.xp = o; o = al256(o + 2ull * g.R * g.H);                     // grouped x 2^s, 16-bit, K-step-major swizzled tiles
   L.hp = o; o = al256(o + 2ull * g.R * g.I);                     // grouped h 2^s, same layout
   L.y = o; o = al256(o + 4ull * g.R * g.H);                      // weighted expert outputs, fp32, row-major
+  L.dbg = o; o = al256(o + 8ull * 2 * kPfDbgCtas * kPfDbgSlots);  // diagnostic cycle counters [gemm][cta][slot]
   L.total = o;
   return L;
 }
@@ -94,6 +103,7 @@ struct PfParams {
   int32_t* topk_idx;          // optional T x K
   float* topk_w;              // optional T x K
   int f16;                    // 1: fp16 tensor-core operands (MXFP4 experts stay bf16), 0: bf16 everywhere
+  int diag;                   // 1: add per-role cycle counts into ws.dbg
   uint64_t limit_ns;
 };
 

@@ -315,6 +315,13 @@ void bqe_set_prefill_f16(int32_t on);
  * fill, gather, W1/W3 GEMM, W2 GEMM, combine); this waits for the last call's
  * events and writes the 8 durations in milliseconds to ms (host, 8 floats). */
 int bqe_prefill_kernel_ms(float* ms);
+
+/* Diagnostic (with bqe_set_diag(1)): byte offset in the prefill workspace of
+ * uint64 [2 GEMMs][256 CTAs][12] cycle counters of the last call (load warp
+ * waiting; dequant waiting raw data / a free stage / working; MMA waiting
+ * operands / issuing / waiting an accumulator; epilogue waiting / working;
+ * CTA total; items).  0 for an unsupported shape. */
+uint64_t bqe_prefill_diag_offset(const bqe_layer_desc* d, int32_t T);
 uint64_t bqe_diag_offset(const bqe_layer_desc* d, int32_t M);
 
 #ifdef __cplusplus
