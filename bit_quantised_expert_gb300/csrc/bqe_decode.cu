@@ -359,11 +359,32 @@ __global__ void __launch_bounds__(256) k_finalize_a(ExpParams P) {
   const int nch = g.nchA, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blk * 256 + tid;
   const int p = i >> 5;
+  // every chunk partial is loaded before any is added (independent loads in
+  // flight together), then added in chunk order
+  constexpr int kMaxCh = 8;  // K chunks of W1/W3 taken this way: hidden / chunk <= 8 (else a plain loop)
   float a0 = 0.f, a1 = 0.f;
-  for (int c = 0; c < nch; ++c) {
-    const int64_t base = (((int64_t)u * g.npanA + p) * nch + c) * 2 * g.M;
-    a0 += pa[(base + r) * 32 + lane];
-    a1 += pa[(base + g.M + r) * 32 + lane];
+  if (nch <= kMaxCh) {
+    float pg[kMaxCh], pu[kMaxCh];
+#pragma unroll
+    for (int c = 0; c < kMaxCh; ++c) {
+      if (c < nch) {
+        const int64_t base = (((int64_t)u * g.npanA + p) * nch + c) * 2 * g.M;
+        pg[c] = pa[(base + r) * 32 + lane];
+        pu[c] = pa[(base + g.M + r) * 32 + lane];
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kMaxCh; ++c)
+      if (c < nch) {
+        a0 += pg[c];
+        a1 += pu[c];
+      }
+  } else {
+    for (int c = 0; c < nch; ++c) {
+      const int64_t base = (((int64_t)u * g.npanA + p) * nch + c) * 2 * g.M;
+      a0 += pa[(base + r) * 32 + lane];
+      a1 += pa[(base + g.M + r) * 32 + lane];
+    }
   }
   const float hv = silu_f(a0) * a1;
   const int64_t rowi = (int64_t)u * g.M + r;
@@ -432,15 +453,50 @@ __global__ void __launch_bounds__(256) k_finalize_b(ExpParams P) {
   }
   __syncthreads();
   const int64_t n = (int64_t)g.M * g.H;
+  constexpr int kMaxCh = 4;  // K chunks of W2 taken the fast way: inter / chunk <= 4 (else plain loops)
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < n; t += (int64_t)gridDim.x * blockDim.x) {
     const int m = (int)(t / g.H), col = (int)(t % g.H);
+    if (nch > kMaxCh) {  // many W2 chunks: plain loops, same order
+      float val = 0.f;
+      for (int c = 0; c < nch; ++c) val += pb[((int64_t)c * g.M + m) * g.H + col];
+      for (int j = 0; j < g.K; ++j) {
+        const int u = s_cu[m * g.K + j], r = s_cr[m * g.K + j];
+        float yj = 0.f;
+        for (int c = 0; c < nch; ++c) yj += pb[(((int64_t)u * nch + c) * g.M + r) * g.H + col];
+        val = fmaf(s_cw[m * g.K + j], yj, val);
+      }
+      float* o = P.out + t;
+      *o = P.accumulate ? *o + val : val;
+      continue;
+    }
+    // all partials of this element loaded first (independent loads in flight
+    // together), then added in a fixed order: shared expert, then j = 0..K-1
+    float ps[kMaxCh], py[kMaxTopK][kMaxCh];
+#pragma unroll
+    for (int c = 0; c < kMaxCh; ++c)
+      if (c < nch) ps[c] = pb[((int64_t)c * g.M + m) * g.H + col];  // shared expert, u = 0
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < g.K) {
+        const int u = s_cu[m * g.K + j], r = s_cr[m * g.K + j];
+#pragma unroll
+        for (int c = 0; c < kMaxCh; ++c)
+          if (c < nch) py[j][c] = pb[(((int64_t)u * nch + c) * g.M + r) * g.H + col];
+      }
+    }
     float val = 0.f;
-    for (int c = 0; c < nch; ++c) val += pb[((int64_t)c * g.M + m) * g.H + col];  // shared expert, u = 0
-    for (int j = 0; j < g.K; ++j) {
-      const int u = s_cu[m * g.K + j], r = s_cr[m * g.K + j];
-      float yj = 0.f;
-      for (int c = 0; c < nch; ++c) yj += pb[(((int64_t)u * nch + c) * g.M + r) * g.H + col];
-      val = fmaf(s_cw[m * g.K + j], yj, val);
+#pragma unroll
+    for (int c = 0; c < kMaxCh; ++c)
+      if (c < nch) val += ps[c];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < g.K) {
+        float yj = 0.f;
+#pragma unroll
+        for (int c = 0; c < kMaxCh; ++c)
+          if (c < nch) yj += py[j][c];
+        val = fmaf(s_cw[m * g.K + j], yj, val);
+      }
     }
     float* o = P.out + t;
     *o = P.accumulate ? *o + val : val;
