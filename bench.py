@@ -62,6 +62,7 @@ def parse():
     ap.add_argument("--experts", type=int, default=384,
                     help="routed experts in the pool (profiling a smaller pool; per-call work is unchanged)")
     ap.add_argument("--tokens", type=int, default=8192, help="prefill: token rows per call")
+    ap.add_argument("--panels", default=None, help="decode: max panels per work item, 'A,B' (diagnostic)")
     ap.add_argument("--cpu-oracle-sample", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -261,6 +262,9 @@ def run_layer(args, rank, world):
 
     dev = torch.device("cuda", torch.cuda.current_device())
     A.bqe_set_variant(args.variant)
+    if args.panels:
+        pa, pb = (int(v) for v in args.panels.split(","))
+        A.bqe_set_panels(pa, pb)
     M = 6 if args.workload.endswith("m6") else 1
     n_x = 64
     NL = args.instances

@@ -76,6 +76,7 @@ SIGNATURES = {
     "bqe_set_test_drop_item": (None, [_I32]),
     "bqe_set_variant": (None, [_I32]),
     "bqe_set_prefill_f16": (None, [_I32]),
+    "bqe_set_panels": (None, [_I32, _I32]),
     "bqe_prefill_kernel_ms": (ctypes.c_int, [_P]),
     "bqe_prefill_diag_offset": (_U64, [_DESC, _I32]),
     "bqe_set_diag": (None, [_I32]),
@@ -255,6 +256,10 @@ def bqe_diag_offset(d, M: int) -> int:
 
 def bqe_set_fused(on: bool) -> None:
     lib.bqe_set_fused(1 if on else 0)
+
+
+def bqe_set_panels(max_a: int, max_b: int) -> None:
+    lib.bqe_set_panels(int(max_a), int(max_b))
 
 
 def bqe_set_prefill_f16(on: bool) -> None:

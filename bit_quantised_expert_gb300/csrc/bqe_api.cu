@@ -17,6 +17,7 @@ static std::atomic<int> g_variant{1};
 static std::atomic<int> g_diag{0};
 static std::atomic<int> g_fused{0};
 static std::atomic<int> g_pf_f16{1};
+static std::atomic<int> g_pmax_a{0}, g_pmax_b{0};
 
 // Diagnostic knobs (not part of the operation): the bound on every in-kernel
 // wait, and whether kernels are chained with programmatic dependent launch.
@@ -27,6 +28,18 @@ extern "C" void bqe_set_variant(int32_t v) { g_variant = v; }
 extern "C" void bqe_set_diag(int32_t on) { g_diag = on ? 1 : 0; }
 extern "C" void bqe_set_fused(int32_t on) { g_fused = on ? 1 : 0; }
 extern "C" void bqe_set_prefill_f16(int32_t on) { g_pf_f16 = on ? 1 : 0; }
+extern "C" void bqe_set_panels(int32_t max_a, int32_t max_b) {
+  g_pmax_a = max_a > 0 ? max_a : 0;
+  g_pmax_b = max_b > 0 ? max_b : 0;
+}
+
+// Largest panel count <= cap that divides npan (cap 0: keep P).
+static int cap_panels(int P, int npan, int cap) {
+  if (cap <= 0) return P;
+  if (P > cap) P = cap;
+  while (P > 1 && npan % P) --P;
+  return P;
+}
 
 static int device_sms() {
   static int cache[64] = {0};
@@ -107,6 +120,8 @@ static int experts_common(const bqe_layer_desc* d, int32_t M, const bqe_pool* po
   if (ws_bytes < L.total) return BQE_ENOSPC;
   const int sms = device_sms();
   if (sms <= 0) return BQE_ECUDA;
+  g.PA = cap_panels(g.PA, g.npanA, g_pmax_a.load());  // diagnostic override; the layout does not depend on it
+  g.PB = cap_panels(g.PB, g.npanB, g_pmax_b.load());
   ExpParams P;
   P.g = g;
   P.L = L;

@@ -310,6 +310,12 @@ void bqe_set_fused(int32_t on);
  * 4e-4 for fp16).  Both run at the same tensor-core rate. */
 void bqe_set_prefill_f16(int32_t on);
 
+/* Diagnostic: at most max_a (W1/W3) and max_b (W2) 32-row panels per work
+ * item of the decode expert kernels (0: the default choice, the largest that
+ * fits).  Fewer panels per item leave room for more ring stages.  Results do
+ * not change. */
+void bqe_set_panels(int32_t max_a, int32_t max_b);
+
 /* Diagnostic (with bqe_set_diag(1)): bqe_moe_prefill records CUDA events on
  * its stream around each of its 8 kernels (router logits, selection, plan,
  * fill, gather, W1/W3 GEMM, W2 GEMM, combine); this waits for the last call's
