@@ -33,6 +33,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+# DRAM bytes read + written per layer call by k_experts<0> and k_finalize_a on the MXFP4 M=1 layer
+# (ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/k_experts_decode_fp4_m1_E64.md).
+# Set to None whenever either kernel changes after that capture.
+DECODE_FP4_M1_TRAFFIC = 87.87e6 + 2.44e6 + 0.66e6
+
 METRIC = "MoE layer decode: expert-byte GB/s (% of HBM peak) and us/layer at M=1 and M=6"
 HBM_FALLBACK_GBS = 6800.0
 WORKLOADS = {
@@ -63,6 +68,7 @@ def parse():
                     help="routed experts in the pool (profiling a smaller pool; per-call work is unchanged)")
     ap.add_argument("--tokens", type=int, default=8192, help="prefill: token rows per call")
     ap.add_argument("--panels", default=None, help="decode: max panels per work item, 'A,B' (diagnostic)")
+    ap.add_argument("--fused", action="store_true", help="decode: the single-kernel layer (bqe_set_fused)")
     ap.add_argument("--cpu-oracle-sample", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -265,6 +271,8 @@ def run_layer(args, rank, world):
     if args.panels:
         pa, pb = (int(v) for v in args.panels.split(","))
         A.bqe_set_panels(pa, pb)
+    if args.fused:
+        A.bqe_set_fused(True)
     M = 6 if args.workload.endswith("m6") else 1
     n_x = 64
     NL = args.instances
@@ -412,7 +420,8 @@ def run_layer(args, rank, world):
         frac_of_hbm=round(value / hbm, 4), hbm_peak_gbs=hbm, hbm_peak_kind=hbm_kind,
         expert_bytes_per_step=round(mean(bytes_e)),
         roofline=dict(bound="hbm", achieved=round(achieved_a, 1), peak=hbm, unit="GB/s",
-                      frac=round(achieved_a / hbm, 4), traffic=None,
+                      frac=round(achieved_a / hbm, 4),
+                      traffic=DECODE_FP4_M1_TRAFFIC if (args.workload == "fp4-m1" and not args.fused) else None,
                       kernel="k_experts<0> + finalize (W1/W3 dequant-GEMV + SiLU-GLU)",
                       algorithmic_bytes_per_launch=round(mean(bytes_a)),
                       peak_kind="%s hbm_gbs (burst copy)" % hbm_kind,
