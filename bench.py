@@ -68,6 +68,8 @@ def parse():
                     help="routed experts in the pool (profiling a smaller pool; per-call work is unchanged)")
     ap.add_argument("--tokens", type=int, default=8192, help="prefill: token rows per call")
     ap.add_argument("--panels", default=None, help="decode: max panels per work item, 'A,B' (diagnostic)")
+    ap.add_argument("--preload", type=int, default=None,
+                    help="decode: max shared-expert stages streamed before the wait (diagnostic)")
     ap.add_argument("--fused", action="store_true", help="decode: the single-kernel layer (bqe_set_fused)")
     ap.add_argument("--cpu-oracle-sample", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -271,6 +273,8 @@ def run_layer(args, rank, world):
     if args.panels:
         pa, pb = (int(v) for v in args.panels.split(","))
         A.bqe_set_panels(pa, pb)
+    if args.preload is not None:
+        A.bqe_set_preload(args.preload)
     if args.fused:
         A.bqe_set_fused(True)
     M = 6 if args.workload.endswith("m6") else 1
@@ -478,7 +482,7 @@ def run_layer(args, rank, world):
             dv[:, 1023, 0] = 2 ** 62
             dv[:, 1023, 1] = 0
             xbuf.copy_(xs[s_ % n_x])
-            layer(s_ % NL)  # eager: kernel parameters carry the diagnostic flag
+            fused(s_ % NL)  # the layer entry point, eager: kernel parameters carry the diagnostic flag
             torch.cuda.synchronize()
             sp = dv[:, 1023, :2].cpu().numpy()
             spans.append([(sp[k, 1] - sp[k, 0]) / 1e3 for k in (2, 0, 1)])

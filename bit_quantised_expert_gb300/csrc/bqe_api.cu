@@ -18,6 +18,7 @@ static std::atomic<int> g_diag{0};
 static std::atomic<int> g_fused{0};
 static std::atomic<int> g_pf_f16{1};
 static std::atomic<int> g_pmax_a{0}, g_pmax_b{0};
+static std::atomic<int> g_preload{16};
 
 // Diagnostic knobs (not part of the operation): the bound on every in-kernel
 // wait, and whether kernels are chained with programmatic dependent launch.
@@ -28,6 +29,7 @@ extern "C" void bqe_set_variant(int32_t v) { g_variant = v; }
 extern "C" void bqe_set_diag(int32_t on) { g_diag = on ? 1 : 0; }
 extern "C" void bqe_set_fused(int32_t on) { g_fused = on ? 1 : 0; }
 extern "C" void bqe_set_prefill_f16(int32_t on) { g_pf_f16 = on ? 1 : 0; }
+extern "C" void bqe_set_preload(int32_t n) { g_preload = n < 0 ? 0 : n; }
 extern "C" void bqe_set_panels(int32_t max_a, int32_t max_b) {
   g_pmax_a = max_a > 0 ? max_a : 0;
   g_pmax_b = max_b > 0 ? max_b : 0;
@@ -110,8 +112,11 @@ static int route_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, c
   return launch_route(P, st, g_use_pdl.load() != 0);
 }
 
+// slot_table (optional): the layer's slot table, from which the expert kernels
+// read the shared expert's slot so they can stream its weights in early.
 static int experts_common(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out, int32_t accumulate,
-                          void* ws, uint64_t ws_bytes, cudaStream_t st, int only_phase = -1) {
+                          void* ws, uint64_t ws_bytes, cudaStream_t st, int only_phase = -1,
+                          const int32_t* slot_table = nullptr) {
   if (!desc_ok(d) || M < 1 || M > kMaxM || !out || !ws || ((uintptr_t)ws & 255)) return BQE_EINVAL;
   int rc = check_pool(pool);
   if (rc) return rc;
@@ -132,6 +137,9 @@ static int experts_common(const bqe_layer_desc* d, int32_t M, const bqe_pool* po
   P.drop_item = g_drop_item.load();
   P.variant = g_variant.load();
   P.diag = g_diag.load();
+  P.slot_table = slot_table;
+  P.pool = *pool;
+  P.max_pre = g_preload.load();
   const bool pdl = g_use_pdl.load() != 0;
   for (int phase = 0; phase < 2; ++phase) {
     if (only_phase >= 0 && phase != only_phase) continue;
@@ -214,7 +222,7 @@ extern "C" int bqe_moe_layer_forward(const bqe_layer_desc* d, int32_t M, const u
   int rc = bqe_route(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, topk_idx, topk_w, ws, ws_bytes,
                      stream);
   if (rc) return rc;
-  return experts_common(d, M, pool, out, accumulate, ws, ws_bytes, (cudaStream_t)stream);
+  return experts_common(d, M, pool, out, accumulate, ws, ws_bytes, (cudaStream_t)stream, -1, slot_table);
 }
 
 extern "C" int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M, float* resid,
@@ -235,7 +243,7 @@ extern "C" int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M
     } else {
       rc = route_common(d, M, nullptr, resid, tl, router_w + l * E * H, bl, pool, slot_tables + l * (E + 1), fl, nullptr,
                         nullptr, ws, ws_bytes, st);
-      if (!rc) rc = experts_common(d, M, pool, resid, 1, ws, ws_bytes, st);
+      if (!rc) rc = experts_common(d, M, pool, resid, 1, ws, ws_bytes, st, -1, slot_tables + l * (E + 1));
     }
     if (rc) return rc;
   }

@@ -35,6 +35,7 @@ namespace bqe {
 
 
 __device__ __forceinline__ long long clk() { return clock64(); }
+constexpr int kFinBThreads = 128;  // k_finalize_b CTA size: small enough to sit beside a W2 CTA
 // diagnostic counters: 0 producer waiting for a free stage, 1 producer issuing,
 // 2 consumer (warp 1) waiting for a stage, 3 consumer waiting for a reduction
 // buffer, 4 consumer computing, 5 epilogue waiting, 6 epilogue working,
@@ -60,7 +61,8 @@ struct RedMeta {
   int u, p0, c, R;
 };
 
-template <int PHASE>
+// RC: rows decoded together (1 for one-row calls, else kRowChunk)
+template <int PHASE, int RC>
 __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P) {
   const Geo& g = P.g;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -102,41 +104,172 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
   }
   __syncthreads();
 
+  // Item t = u * per_u + pg * nch + c (expert u, panel group pg, K chunk c):
+  // the quotients by per_u and nch come from a multiply by the rounded-up
+  // 2^32 / divisor (up to 2^32 itself for divisor 1), exact for t * divisor < 2^32.
+  const uint64_t mag_pu = (0x100000000ull + per_u - 1) / per_u;
+  const uint64_t mag_ch = (0x100000000ull + nch - 1) / nch;
+  auto split_item = [&](int t, int& u, int& pg, int& c) {
+    u = (int)(((uint64_t)t * mag_pu) >> 32);
+    const int rem = t - u * per_u;
+    pg = (int)(((uint64_t)rem * mag_ch) >> 32);
+    c = rem - pg * nch;
+  };
+  // Stage `s` of item `i`: header and weight tiles.  `pre`: issued before the
+  // routing results are visible, so the barrier only learns the byte count now
+  // and gets its arrival with the activation rows later.
+  auto issue_weights = [&](int s, int u, int pg, int c, int fmt, uint64_t addr, int R, uint32_t tb, bool pre,
+                           uint64_t pol) -> uint32_t {
+    StageHdr& H = hdr[s];
+    H.addr = addr; H.u = u; H.p0 = pg * P_; H.c = c; H.fmt = fmt; H.R = R;
+    const uint32_t wbytes = (uint32_t)phase_mats(PHASE) * P_ * tb;
+    uint8_t* dst = ring + (size_t)s * slot_bytes;
+    if (pre) mbar_expect_tx(&full[s], wbytes);
+    const uint64_t src0 = addr + (PHASE == 0 ? 0ull : 2 * matrix_bytes(fmt, g.I, g.H)) +
+                          (uint64_t)(pg * P_ * nch + c) * tb;
+    const uint64_t m13 = PHASE == 0 ? matrix_bytes(fmt, g.I, g.H) : 0ull;
+    for (int j = 0; j < P_; ++j) {
+      const uint64_t src = src0 + (uint64_t)j * nch * tb;
+      bulk_g2s_hint(dst + j * tb, (const void*)src, tb, &full[s], pol);  // W1 (or W2)
+      if (PHASE == 0) bulk_g2s_hint(dst + (P_ + j) * tb, (const void*)(src + m13), tb, &full[s], pol);  // W3
+    }
+    return wbytes;
+  };
+
+  // ---- the shared expert before the routing results --------------------------
+  // Its slot comes from the inputs (slot_table[E]), not from the router, so
+  // the producer streams the weight tiles of this CTA's first shared-expert
+  // items (u = 0 comes first in the item order) into the ring while the
+  // previous kernel is still finishing.
+  int npre = 0;
+  uint64_t pre_addr = 0;
+  int pre_fmt = 0;
+  if (warp == 0 && lane == 0 && P.slot_table) {
+    const int sl = P.slot_table[g.E];
+    if (sl >= 0 && sl < P.pool.n_slots) {
+      const int fmt = P.pool.slot_fmt[sl];
+      const uint64_t off = P.pool.slot_off[sl];
+      if (fmt_ok(fmt) && !(off & 15) &&
+          off + 2 * matrix_bytes(fmt, g.I, g.H) + matrix_bytes(fmt, g.H, g.I) <= P.pool.base_bytes) {
+        pre_addr = (uint64_t)P.pool.base + off;
+        pre_fmt = fmt;
+        const uint64_t pol = policy_evict_first();
+        const uint32_t tb = tile_bytes(fmt, kc);
+        for (; npre < nstages && npre < P.max_pre; ++npre) {
+          const int t = blockIdx.x + npre * gridDim.x;
+          if (t >= per_u) break;
+          if (npre == P.drop_item && blockIdx.x == 0) break;  // the test hook's item goes through the main loop
+          int u, pg, c;
+          split_item(t, u, pg, c);
+          issue_weights(npre, u, pg, c, fmt, pre_addr, g.M, tb, true, pol);
+        }
+      }
+    }
+  }
+
   griddep_wait();  // routing / phase A results must be complete and visible
   griddep_launch_dependents();  // the finalize kernel may be scheduled behind this one
 
-  const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
-  const int nItems = nU * per_u;
-  // the work list (format, slot address, rows of every distinct expert) in
-  // shared memory, so no item waits on a global load
+  // the work list (format, slot address, rows of every distinct expert) and
+  // what the producer derives from it, in shared memory, so no item waits on
+  // a global load or recomputes a per-expert size
   __shared__ int32_t s_ufmt[kMaxM * kMaxTopK + 1];
   __shared__ int32_t s_unrows[kMaxM * kMaxTopK + 1];
   __shared__ uint64_t s_uaddr[kMaxM * kMaxTopK + 1];
   __shared__ int8_t s_urows[(kMaxM * kMaxTopK + 1) * kMaxM];
+  __shared__ uint32_t s_utb[kMaxM * kMaxTopK + 1];   // tile bytes
+  __shared__ uint32_t s_uarow[kMaxM * kMaxTopK + 1]; // staged bytes of one activation row
+  __shared__ uint64_t s_uact[kMaxM * kMaxTopK + 1];  // workspace offset of the activation rows' chunk 0
+  __shared__ uint32_t s_ustr[kMaxM * kMaxTopK + 1];  // ... bytes from one chunk to the next (row stride: chunks * this)
+  __shared__ float s_xsc[kMaxM];                     // 2^-s of the f16 rows of x
+  // activation rows of expert u: staged bytes of one row, bytes from one chunk
+  // to the next, and the workspace offset of its chunk 0
+  auto act_table = [&](int u, int fmt, uint32_t& arow, uint32_t& str, uint64_t& act) {
+    const int amode = act_mode(PHASE, fmt, P.variant);
+    arow = (uint32_t)act_row_bytes(amode, fmt, kc);
+    if (amode == kActInt) {
+      // one record per (row, chunk): x rows in the format's order, or h rows of this expert
+      act = PHASE == 0 ? (fmt == BQE_FMT_TQ1 ? P.L.xrt : P.L.xrq) : P.L.hr + (uint64_t)u * g.M * nch * int_rec_bytes(1, kc);
+      str = PHASE == 0 ? arow : int_rec_bytes(1, kc);
+    } else {
+      act = PHASE == 0 ? (amode == kActF16 ? P.L.xh : P.L.xf) : P.L.h + (uint64_t)u * g.M * g.I * 4;
+      str = arow;
+    }
+  };
+  const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
+  const int nItems = nU * per_u;
+  if (tid < g.M) s_xsc[tid] = ((const float*)(P.ws + P.L.xsc))[tid];
   for (int u = tid; u < nU; u += blockDim.x) {
-    s_ufmt[u] = ((const int32_t*)(P.ws + P.L.u_fmt))[u];
-    s_unrows[u] = ((const int32_t*)(P.ws + P.L.u_nrows))[u];
-    s_uaddr[u] = ((const uint64_t*)(P.ws + P.L.u_addr))[u];
     for (int r = 0; r < kMaxM; ++r) s_urows[u * kMaxM + r] = (int8_t)((const int32_t*)(P.ws + P.L.u_rows))[u * kMaxM + r];
+    const int fmt = ((const int32_t*)(P.ws + P.L.u_fmt))[u];
+    s_ufmt[u] = fmt;
+    s_uaddr[u] = ((const uint64_t*)(P.ws + P.L.u_addr))[u];
+    s_unrows[u] = ((const int32_t*)(P.ws + P.L.u_nrows))[u];
+    if (fmt_ok(fmt)) {
+      uint32_t arow, str;
+      uint64_t act;
+      act_table(u, fmt, arow, str, act);
+      s_utb[u] = tile_bytes(fmt, kc);
+      s_uarow[u] = arow;
+      s_ustr[u] = str;
+      s_uact[u] = act;
+    }
   }
+  __shared__ int s_npre;  // items of this CTA preloaded (shared expert)
+  if (tid == 0) s_npre = npre;  // the producer lane is thread 0
   __syncthreads();
-  const float* xf = (const float*)(P.ws + P.L.xf);
-  float* hbuf = (float*)(P.ws + P.L.h);
+  // Preloaded items are processed even when the router reported an error
+  // (no items): their stages are armed and must drain.
+  const int npre_s = s_npre;
 
   if (warp == 0) {
     // ------------------------------- producer -------------------------------
     if (lane == 0) {
       int last_issued[16];
       for (int s = 0; s < 16; ++s) last_issued[s] = -1;
+      for (int i = 0; i < npre; ++i) last_issued[i] = i;
       long long pw = 0, pi_ = 0;
       const uint64_t pol = policy_evict_first();
+      // activation rows of an item into stage s: one bulk copy per row (x rows
+      // for W1/W3: the rows that chose the expert; h rows for W2: its own rows)
+      auto issue_acts = [&](int s, uint32_t expect_w, uint32_t wbytes, int R, uint32_t arow, uint32_t str,
+                            uint64_t act, const int8_t* rows, int c) {
+        uint8_t* adst = ring + (size_t)s * slot_bytes + wbytes;
+        mbar_arrive_expect_tx(&full[s], expect_w + (uint32_t)R * arow);
+        const uint8_t* src0 = P.ws + act + (uint64_t)c * str;
+        for (int r = 0; r < R; ++r) {
+          const int row = (PHASE == 0 && rows) ? rows[r] : r;
+          bulk_g2s(adst + (size_t)r * arow, src0 + (uint64_t)row * nch * str, arow, &full[s]);
+        }
+      };
       int i = 0;
-      for (int t = blockIdx.x; t < nItems; t += gridDim.x, ++i) {
+      if (npre > 0) {
+        // the preloaded shared-expert items: their activation rows (all M rows)
+        uint32_t arow, str;
+        uint64_t act;
+        act_table(0, pre_fmt, arow, str, act);
+        const uint32_t wb = (uint32_t)phase_mats(PHASE) * P_ * tile_bytes(pre_fmt, kc);
+        for (; i < npre; ++i) {
+          int u, pg, c;
+          split_item(blockIdx.x + i * gridDim.x, u, pg, c);
+          const long long t1 = clk();
+          issue_acts(i % nstages, 0u, wb, g.M, arow, str, act, nullptr, c);
+          pi_ += clk() - t1;
+        }
+      }
+      if (npre > 0 && nItems > 0 && (s_uaddr[0] != pre_addr || s_ufmt[0] != pre_fmt || s_unrows[0] != g.M)) {
+        // the work list's shared-expert entry must be the one preloaded
+        set_error(err, BQE_EDEVICE, kErrPreload);
+        *abort_flag = 1;
+      }
+      for (int t = blockIdx.x + i * gridDim.x; t < nItems; t += gridDim.x, ++i) {
         const int s = i % nstages;
         if (*abort_flag) break;
+        int u, pg, c;
+        split_item(t, u, pg, c);
         if (i >= nstages) {
           const long long t0 = clk();
-          if (!mbar_wait_bounded(&empty[s], ((i / nstages) - 1) & 1, P.limit_ns)) {
+          if (!mbar_wait_sleep_bounded(&empty[s], ((i / nstages) - 1) & 1, P.limit_ns)) {
             set_error(err, BQE_ETIMEOUT, kErrWaitEmpty);
             *abort_flag = 1;
             break;
@@ -145,71 +278,9 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
         }
         const long long t1 = clk();
         if (i == P.drop_item && blockIdx.x == 0) continue;  // test hook: this stage never lands
-        const int u = t / per_u, rem = t % per_u;
-        const int pg = rem / nch, c = rem % nch;
-        const int fmt = s_ufmt[u];
         const int R = s_unrows[u];
-        const uint64_t addr = s_uaddr[u];
-        StageHdr& H = hdr[s];
-        H.addr = addr; H.u = u; H.p0 = pg * P_; H.c = c; H.fmt = fmt; H.R = R;
-        const uint32_t tb = tile_bytes(fmt, kc);
-        const uint32_t wbytes = (uint32_t)phase_mats(PHASE) * P_ * tb;
-        const int amode = act_mode(PHASE, fmt, P.variant);
-        const uint32_t arow = (uint32_t)act_row_bytes(amode, fmt, kc);
-        const uint32_t abytes = (uint32_t)R * arow;
-        uint8_t* dst = ring + (size_t)s * slot_bytes;
-        mbar_arrive_expect_tx(&full[s], wbytes + abytes);
-        const uint64_t m13 = matrix_bytes(fmt, g.I, g.H);
-        if (PHASE == 0) {
-          for (int j = 0; j < P_; ++j) {
-            const uint64_t toff = (uint64_t)((pg * P_ + j) * nch + c) * tb;
-            bulk_g2s_hint(dst + j * tb, (const void*)(addr + toff), tb, &full[s], pol);               // W1
-            bulk_g2s_hint(dst + (P_ + j) * tb, (const void*)(addr + m13 + toff), tb, &full[s], pol);  // W3
-          }
-        } else {
-          for (int j = 0; j < P_; ++j) {
-            const uint64_t toff = 2 * m13 + (uint64_t)((pg * P_ + j) * nch + c) * tb;
-            bulk_g2s_hint(dst + j * tb, (const void*)(addr + toff), tb, &full[s], pol);
-          }
-        }
-        uint8_t* adst = dst + wbytes;
-        const uint16_t* xh = (const uint16_t*)(P.ws + P.L.xh);
-        for (int r = 0; r < R; ++r) {
-          const int64_t row = PHASE == 0 ? s_urows[u * kMaxM + r] : 0;
-          if (amode == kActInt) {
-            // X_hi and X_lo of this chunk in the format's order, then their 16-column sums:
-            // the layer input (W1/W3) or the expert's h (W2)
-            const uint32_t xb = (uint32_t)act_x_bytes(fmt, kc), xbl = (uint32_t)act_xl_bytes(fmt, kc);
-            const int Kr = PHASE == 0 ? g.H : g.I;
-            const int64_t rowi = PHASE == 0 ? row : (int64_t)u * g.M + r;
-            const uint8_t* hi0 = P.ws + (PHASE == 0 ? (fmt == BQE_FMT_TQ1 ? P.L.xt : P.L.xq) : P.L.hq);
-            const uint8_t* lo0 = P.ws + (PHASE == 0 ? (fmt == BQE_FMT_TQ1 ? P.L.xtl : P.L.xql) : P.L.hql);
-            const int64_t cofs_h = (int64_t)c * (fmt == BQE_FMT_TQ1 ? (kc / 256) * kTOrderBlock : kc * 2);
-            const int64_t cofs_l = (int64_t)c * (fmt == BQE_FMT_TQ1 ? (kc / 256) * kTOrderBlockL : kc);
-            const int64_t so = (rowi * (Kr / 16) + (int64_t)c * (kc / 16)) * 4;
-            uint8_t* d0 = adst + (size_t)r * arow;
-            const bool tq = fmt == BQE_FMT_TQ1;
-            const int64_t roh = PHASE == 0 ? (tq ? rowi * (Kr / 256) * kTOrderBlock : rowi * Kr * 2)
-                                           : h_row_off_hi(rowi, Kr);
-            const int64_t rol = PHASE == 0 ? (tq ? rowi * (Kr / 256) * kTOrderBlockL : rowi * Kr)
-                                           : h_row_off_lo(rowi, Kr);
-            bulk_g2s(d0, hi0 + roh + cofs_h, xb, &full[s]);
-            bulk_g2s(d0 + xb, lo0 + rol + cofs_l, xbl, &full[s]);
-            bulk_g2s(d0 + xb + xbl, P.ws + (PHASE == 0 ? P.L.s16 : P.L.hs16) + so, (uint32_t)kc / 4, &full[s]);
-            bulk_g2s(d0 + xb + xbl + kc / 4, P.ws + (PHASE == 0 ? P.L.s16l : P.L.hs16l) + so, (uint32_t)kc / 4,
-                     &full[s]);
-            bulk_g2s(d0 + xb + xbl + kc / 2, P.ws + (PHASE == 0 ? P.L.xsb : P.L.hsb) + (rowi * nch + c) * 16, 16u,
-                     &full[s]);
-            continue;
-          }
-          const void* src;
-          if (PHASE == 0)
-            src = amode == kActF16 ? (const void*)(xh + row * g.H + (int64_t)c * kc)
-                                   : (const void*)(xf + row * g.H + (int64_t)c * kc);
-          else
-            src = hbuf + ((int64_t)u * g.M + r) * g.I + (int64_t)c * kc;
-          bulk_g2s(adst + (size_t)r * arow, src, arow, &full[s]);
-        }
+        const uint32_t wbytes = issue_weights(s, u, pg, c, s_ufmt[u], s_uaddr[u], R, s_utb[u], false, pol);
+        issue_acts(s, wbytes, wbytes, R, s_uarow[u], s_ustr[u], s_uact[u], &s_urows[u * kMaxM], c);
         last_issued[s] = i;
         pi_ += clk() - t1;
       }
@@ -231,15 +302,16 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
     const int mat = cw / (P_ * G);         // 0: W1 (or W2), 1: W3
     const int pan = (cw / G) % P_;
     const int grp = cw % G;
-    int i = 0;
-    for (int t = blockIdx.x; t < nItems; t += gridDim.x, ++i) {
+    for (int i = 0;; ++i) {
+      const int t = blockIdx.x + i * gridDim.x;
+      if (i >= npre_s && t >= nItems) break;
       const int s = i % nstages, b = i % kRed;
       const long long t0 = clk();
       // every lane waits; the warp proceeds only if all lanes saw the stage land
-      bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (i / nstages) & 1, P.limit_ns));
+      bool ok = __all_sync(0xffffffffu, mbar_wait_sleep_bounded(&full[s], (i / nstages) & 1, P.limit_ns));
       const long long t1 = clk();
       if (ok && i >= kRed)
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&rempty[b], ((i / kRed) - 1) & 1, P.limit_ns));
+        ok = __all_sync(0xffffffffu, mbar_wait_sleep_bounded(&rempty[b], ((i / kRed) - 1) & 1, P.limit_ns));
       const long long t2 = clk();
       cwf += t1 - t0;
       cwr += t2 - t1;
@@ -256,7 +328,7 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
       const uint8_t* tile = slot + (size_t)(mat * P_ + pan) * tb;
       const uint8_t* act = slot + (size_t)phase_mats(PHASE) * P_ * tb;
       float* rb = red + (size_t)b * red_stride;
-      consume_rows(H.R, H.fmt, tile, kc, grp, act, lane, rb + cw * g.M * 32, act_mode(PHASE, H.fmt, P.variant));
+      consume_rows<RC>(H.R, H.fmt, tile, kc, grp, act, lane, rb + cw * g.M * 32, act_mode(PHASE, H.fmt, P.variant));
       if (cw == 0 && lane == 0) rmeta[b] = RedMeta{H.u, H.p0, H.c, H.R};
       ccomp += clk() - t2;
       __syncwarp();
@@ -275,14 +347,15 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
 
   if (warp != NW + 1) return;
   // ------------------------------- epilogue warp --------------------------------
-  int i = 0;
   long long ew = 0, eb = 0, tprev = clk();
   const long long tstart = tprev;
-  for (int t = blockIdx.x; t < nItems; t += gridDim.x, ++i) {
+  for (int i = 0;; ++i) {
+    const int t = blockIdx.x + i * gridDim.x;
+    if (i >= npre_s && t >= nItems) break;
     const int b = i % kRed;
     const long long t0 = clk();
     eb += t0 - tprev;
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&rfull[b], (i / kRed) & 1, P.limit_ns))) {
+    if (!__all_sync(0xffffffffu, mbar_wait_sleep_bounded(&rfull[b], (i / kRed) & 1, P.limit_ns))) {
       if (lane == 0) set_error(err, BQE_ETIMEOUT, kErrWaitFull);
       break;
     }
@@ -294,12 +367,11 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
     // the finalize kernel adds the chunks in a fixed order
     if (PHASE == 0) {
       const int amode = act_mode(PHASE, s_ufmt[mt.u], P.variant);
-      const float* xsc = (const float*)(P.ws + P.L.xsc);
       float* pa = (float*)(P.ws + P.L.pa);
       // W1 warps of panel pi are cw = pi*G + gi, W3 warps cw = (P + pi)*G + gi
       for (int r = 0; r < mt.R; ++r) {
         // f16 rows carry 2^s (removed here, exact); integer rows were unscaled per block
-        const float unscale = amode == kActF16 ? xsc[s_urows[mt.u * kMaxM + r]] : 1.0f;
+        const float unscale = amode == kActF16 ? s_xsc[s_urows[mt.u * kMaxM + r]] : 1.0f;
         for (int pi = 0; pi < P_; ++pi) {
           const int p = mt.p0 + pi;
           const int64_t base = (((int64_t)mt.u * g.npanA + p) * nch + mt.c) * 2 * g.M;
@@ -345,15 +417,9 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
 // and, for the integer W2 paths, as X_hi + X_lo / 128 of h 2^si (max |h| 2^si
 // of the 256 columns in [2^13, 2^14)) in the order of the expert's format,
 // with the sums of X_hi and X_lo over every 16 columns and 2^-si.
-__global__ void __launch_bounds__(256) k_finalize_a(ExpParams P) {
+// h of 256 columns of row r of expert u (one column per thread)
+__device__ __forceinline__ void finalize_a_block(const ExpParams& P, int u, int r, int blk) {
   const Geo& g = P.g;
-  griddep_wait();
-  griddep_launch_dependents();
-  const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
-  const int nbl = g.I / 256;
-  const int u = blockIdx.x / (g.M * nbl), r = (blockIdx.x / nbl) % g.M, blk = blockIdx.x % nbl;
-  if (u >= nU) return;
-  if (r >= ((const int32_t*)(P.ws + P.L.u_nrows))[u]) return;
   const int fmt = ((const int32_t*)(P.ws + P.L.u_fmt))[u];
   const float* pa = (const float*)(P.ws + P.L.pa);
   const int nch = g.nchA, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -398,46 +464,58 @@ __global__ void __launch_bounds__(256) k_finalize_a(ExpParams P) {
   for (int w = 0; w < 8; ++w) bm = max(bm, s_mx[w]);
   const int ex = (int)(bm >> 23);  // biased exponent of max |h| (0: all zero or subnormal)
   const int si = ex == 0 ? 0 : min(max(13 - (ex - 127), -100), 100);
-  if (tid == 0) {
-    const int bpc = g.kcB / 256;
-    ((float*)(P.ws + P.L.hsb))[(rowi * g.nchB + blk / bpc) * 4 + blk % bpc] = ldexpf(1.0f, -si);
-  }
-  int16_t* hq = (int16_t*)(P.ws + P.L.hq + h_row_off_hi(rowi, g.I));
-  int8_t* hql = (int8_t*)(P.ws + P.L.hql + h_row_off_lo(rowi, g.I));
+  const int tq = fmt == BQE_FMT_TQ1;
+  const int bpc = g.kcB / 256, ck = blk / bpc, k = blk % bpc;  // K chunk of W2 holding the block, place in it
+  uint8_t* rec = P.ws + P.L.hr + ((size_t)rowi * g.nchB + ck) * int_rec_bytes(1, g.kcB);
+  if (tid == 0) rec_put_scale(rec, tq, g.kcB, k, ldexpf(1.0f, -si));
   const float v = ldexpf(hv, si);
   const int Xh = __float2int_rn(v);
   const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
-  const int j = tid;
-  if (fmt == BQE_FMT_TQ1) {
-    const int run = j / 20, jr = j % 20, q4 = jr / 5, rd = jr % 5;
-    hq[blk * 264 + run * 20 + 4 * rd + 2 * (q4 >> 1) + (q4 & 1)] = (int16_t)Xh;
-    hql[blk * 272 + run * 20 + 4 * rd + q4] = (int8_t)Xl;
-    if (tid < 16) {  // T-order slots past column 255 and the padding
-      const int slot = tid < 4 ? 240 + 4 * (tid + 1) + 3 : 260 + (tid - 4);
-      if (tid < 8) hq[blk * 264 + slot] = 0;
-      hql[blk * 272 + slot] = 0;
-    }
-  } else {
-    const int jj = j & 15, kq = jj & 3, iq = jj >> 2;
-    hq[blk * 256 + (j & ~15) + 4 * kq + 2 * (iq >> 1) + (iq & 1)] = (int16_t)Xh;
-    hql[blk * 256 + (j & ~15) + 4 * kq + iq] = (int8_t)Xl;
-  }
+  rec_put(rec, tq, g.kcB, k, tid, Xh, Xl);
+  if (tq && tid < 16) rec_put_pad(rec, g.kcB, k, tid);
   int ph = Xh, pl = Xl;
 #pragma unroll
   for (int o = 8; o; o >>= 1) {
     ph += __shfl_xor_sync(0xffffffffu, ph, o);
     pl += __shfl_xor_sync(0xffffffffu, pl, o);
   }
-  if ((lane & 15) == 0) {
-    ((int32_t*)(P.ws + P.L.hs16))[rowi * (g.I / 16) + blk * 16 + (tid >> 4)] = ph;
-    ((int32_t*)(P.ws + P.L.hs16l))[rowi * (g.I / 16) + blk * 16 + (tid >> 4)] = pl;
+  if ((lane & 15) == 0) rec_put_sums(rec, tq, g.kcB, k, tid >> 4, ph, pl);
+}
+
+__global__ void __maxnreg__(32) k_finalize_a(ExpParams P) {  // 32 registers: fits beside a W1/W3 CTA
+  const Geo& g = P.g;
+  // The W2 kernel may launch now: its CTAs take SMs as the W1/W3 kernel's
+  // leave and stream the shared expert's W2 tiles until they may read h.
+  griddep_launch_dependents();
+  griddep_wait();
+  const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
+  const int nbl = g.I / 256;
+  // work = (expert, row of the expert, 256 columns); prefix sums of the rows
+  __shared__ int s_pre[kMaxM * kMaxTopK + 2];
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int u = 0; u < nU; ++u) {
+      s_pre[u] = acc;
+      acc += ((const int32_t*)(P.ws + P.L.u_nrows))[u];
+    }
+    s_pre[nU] = acc;
+  }
+  __syncthreads();
+  const int nwork = s_pre[nU] * nbl;
+  for (int wk = blockIdx.x; wk < nwork; wk += gridDim.x) {
+    const int rowg = wk / nbl, blk = wk % nbl;
+    int u = 0;
+    while (u + 1 < nU && s_pre[u + 1] <= rowg) ++u;
+    const int r = rowg - s_pre[u];
+    finalize_a_block(P, u, r, blk);
+    __syncthreads();  // shared scratch of the block is reused
   }
 }
 
-__global__ void __launch_bounds__(256) k_finalize_b(ExpParams P) {
+__global__ void __launch_bounds__(kFinBThreads) k_finalize_b(ExpParams P) {
   const Geo& g = P.g;
+  griddep_launch_dependents();  // the next layer's router may start loading its weights
   griddep_wait();
-  griddep_launch_dependents();
   const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
   const float* pb = (const float*)(P.ws + P.L.pb);
   const int nch = g.nchB;
@@ -503,20 +581,24 @@ __global__ void __launch_bounds__(256) k_finalize_b(ExpParams P) {
   }
 }
 
+// The finalize kernels run at most one CTA per SM, each looping over its
+// share of the work, so that the whole grid fits beside the expert kernel's
+// CTAs (launched early, it waits on the SMs and starts the moment the expert
+// kernel completes).
 int launch_finalize(const ExpParams& P, int phase, int sms, cudaStream_t st, bool pdl) {
   int grid;
   if (phase == 0) {
     if (P.g.I % 256) return BQE_EUNSUPPORTED;
-    grid = P.g.U * P.g.M * (P.g.I / 256);  // one CTA per (expert, row, 256 columns)
+    grid = P.g.U * P.g.M * (P.g.I / 256);  // (expert, row, 256 columns) work items at most
   } else {
     const int64_t n = (int64_t)P.g.M * P.g.H;
-    grid = (int)((n + 255) / 256);
-    if (grid > 2 * sms) grid = 2 * sms;
-    if (grid < 1) grid = 1;
+    grid = (int)((n + kFinBThreads - 1) / kFinBThreads);
   }
+  if (grid > sms) grid = sms;
+  if (grid < 1) grid = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(phase == 0 ? 256 : kFinBThreads);
   cfg.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -537,15 +619,18 @@ uint32_t experts_smem_bytes(const Geo& g, int phase, int* nstages_out) {
 }
 
 int launch_experts(const ExpParams& P, int phase, int grid, cudaStream_t st, bool pdl) {
+  void (*kfns[2][2])(ExpParams) = {{k_experts<0, 1>, k_experts<0, kRowChunk>}, {k_experts<1, 1>, k_experts<1, kRowChunk>}};
+  const int rc = P.g.M == 1 ? 0 : 1;
+  void (*kfn)(ExpParams) = kfns[phase][rc];
   int ns = 0;
   const uint32_t smem = experts_smem_bytes(P.g, phase, &ns);
   if (ns < 2) return BQE_EUNSUPPORTED;
   // raise the kernel's dynamic shared memory limit once per device (the call is slow)
-  static int limit_set[2][64] = {};
+  static int limit_set[2][2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BQE_ECUDA;
-  if (limit_set[phase][dev] < (int)smem) {
-    const void* fn = phase == 0 ? (const void*)k_experts<0> : (const void*)k_experts<1>;
+  if (limit_set[phase][rc][dev] < (int)smem) {
+    const void* fn = (const void*)kfn;
     int optin = 0;
     cudaFuncAttributes fa;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
@@ -555,7 +640,7 @@ int launch_experts(const ExpParams& P, int phase, int grid, cudaStream_t st, boo
     if (dyn_max < (int)smem) return BQE_EUNSUPPORTED;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max) != cudaSuccess)
       return BQE_ECUDA;
-    limit_set[phase][dev] = dyn_max;
+    limit_set[phase][rc][dev] = dyn_max;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -567,7 +652,7 @@ int launch_experts(const ExpParams& P, int phase, int grid, cudaStream_t st, boo
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e = phase == 0 ? cudaLaunchKernelEx(&cfg, k_experts<0>, P) : cudaLaunchKernelEx(&cfg, k_experts<1>, P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kfn, P);
   return e == cudaSuccess ? BQE_OK : BQE_ECUDA;
 }
 

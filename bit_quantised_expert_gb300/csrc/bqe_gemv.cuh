@@ -323,12 +323,8 @@ __device__ __forceinline__ void group_q3k(const uint8_t* tile, int nb, int grp, 
 constexpr int kTOrderBlock = 528;   // bytes of one 256-column block of X_hi in T order
 constexpr int kTOrderBlockL = 272;  // ... of X_lo
 
-__host__ __device__ inline int act_x_bytes(int fmt, int kc) {
-  return fmt == BQE_FMT_TQ1 ? (kc / 256) * kTOrderBlock : kc * 2;
-}
-__host__ __device__ inline int act_xl_bytes(int fmt, int kc) {
-  return fmt == BQE_FMT_TQ1 ? (kc / 256) * kTOrderBlockL : kc;
-}
+__host__ __device__ inline int act_x_bytes(int fmt, int kc) { return (int)int_rec_hi_bytes(fmt == BQE_FMT_TQ1, kc); }
+__host__ __device__ inline int act_xl_bytes(int fmt, int kc) { return (int)int_rec_lo_bytes(fmt == BQE_FMT_TQ1, kc); }
 
 // Pointers into one staged row of the integer mode: [X_hi | X_lo | sums of
 // X_hi | sums of X_lo | 2^-si of each 256 columns (4 slots)].
@@ -424,7 +420,7 @@ __device__ __forceinline__ void group_q3k_i(const uint8_t* tile, int nb, int grp
   int bh[R], bl[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) bh[r] = bl[r] = 0;
-#pragma unroll 4
+#pragma unroll
   for (int sj = 0; sj < 16; ++sj) {
     const int bit = 6 * sj;
     const uint64_t two = ((uint64_t)sc[bit >> 5]) | (((bit >> 5) < 2 ? (uint64_t)sc[(bit >> 5) + 1] : 0ull) << 32);
@@ -533,15 +529,9 @@ __host__ __device__ inline int act_mode(int phase, int fmt, int variant) {
   if (fmt != BQE_FMT_MXFP4) return 2;
   return phase == 0 && variant == 1 ? 1 : 0;
 }
-// Byte offsets of row `rowi` of the integer staging of h (X_hi, X_lo): every
-// row has room for T order, whatever its expert's format (K a multiple of 256).
-__host__ __device__ inline int64_t h_row_off_hi(int64_t rowi, int K) { return rowi * (K / 256) * kTOrderBlock; }
-__host__ __device__ inline int64_t h_row_off_lo(int64_t rowi, int K) { return rowi * (K / 256) * kTOrderBlockL; }
 
 __host__ __device__ inline int act_row_bytes(int amode, int fmt, int kc) {
-  return amode == kActF32 ? kc * 4
-         : amode == kActF16 ? kc * 2
-                            : act_x_bytes(fmt, kc) + act_xl_bytes(fmt, kc) + kc / 2 + 16;
+  return amode == kActF32 ? kc * 4 : amode == kActF16 ? kc * 2 : (int)int_rec_bytes(fmt == BQE_FMT_TQ1, kc);
 }
 
 template <int R>
@@ -576,24 +566,32 @@ __device__ __forceinline__ void consume_group_R(int fmt, const uint8_t* tile, in
   for (int r = 0; r < R; ++r) outv[r * 32 + lane] = acc[r].x + acc[r].y;
 }
 
+template <int RC>
 __device__ __forceinline__ void consume_group(int R, int fmt, const uint8_t* tile, int kc, int grp,
                                               const uint8_t* act, int lane, float* outv, int amode) {
+  if (RC == 1 || R == 1) {
+    consume_group_R<1>(fmt, tile, kc, grp, act, lane, outv, amode);
+    return;
+  }
   switch (R) {
-    case 1: consume_group_R<1>(fmt, tile, kc, grp, act, lane, outv, amode); break;
     case 2: consume_group_R<2>(fmt, tile, kc, grp, act, lane, outv, amode); break;
     case 3: consume_group_R<3>(fmt, tile, kc, grp, act, lane, outv, amode); break;
     case 4: consume_group_R<4>(fmt, tile, kc, grp, act, lane, outv, amode); break;
   }
 }
 
-// All R rows of one stage, kRowChunk rows at a time (the weights of the group
-// are decoded again for each further chunk; only rows 5..8 of a call pay it).
+// All R rows of one stage, RC (1 or kRowChunk) rows at a time (the weights of
+// the group are decoded again for each further chunk).  A kernel instance for
+// one-row calls (RC = 1) carries only the one-row inner loops, which keeps its
+// code small and its register count low.
+template <int RC>
 __device__ __forceinline__ void consume_rows(int R, int fmt, const uint8_t* tile, int kc, int grp, const uint8_t* act,
                                              int lane, float* outv, int amode) {
+  static_assert(RC == 1 || RC == kRowChunk, "row chunk");
   const size_t row_bytes = (size_t)act_row_bytes(amode, fmt, kc);
-  for (int r0 = 0; r0 < R; r0 += kRowChunk) {
-    const int n = R - r0 < kRowChunk ? R - r0 : kRowChunk;
-    consume_group(n, fmt, tile, kc, grp, act + r0 * row_bytes, lane, outv + r0 * 32, amode);
+  for (int r0 = 0; r0 < R; r0 += RC) {
+    const int n = R - r0 < RC ? R - r0 : RC;
+    consume_group<RC>(n, fmt, tile, kc, grp, act + r0 * row_bytes, lane, outv + r0 * 32, amode);
   }
 }
 

@@ -124,11 +124,23 @@ __host__ __device__ inline Geo make_geo(int H, int I, int E, int K, int M) {
   return g;
 }
 
+// Integer staging record of one activation row and one K chunk of kc
+// columns (kc a multiple of 256):
+//   [X_hi | X_lo | int32 sums of X_hi per 16 columns | the same of X_lo |
+//    2^-si of each 256 columns (4 float slots)]
+// with X_hi / X_lo in "Q order" (tq = 0: 2 kc + kc bytes) or "T order"
+// (tq = 1: 528 + 272 bytes per 256 columns).  One record is exactly one
+// staged activation row of a ring stage, so it moves with one bulk copy.
+__host__ __device__ constexpr uint32_t int_rec_hi_bytes(int tq, int kc) { return tq ? (kc / 256) * 528 : kc * 2; }
+__host__ __device__ constexpr uint32_t int_rec_lo_bytes(int tq, int kc) { return tq ? (kc / 256) * 272 : kc; }
+__host__ __device__ constexpr uint32_t int_rec_bytes(int tq, int kc) {
+  return int_rec_hi_bytes(tq, kc) + int_rec_lo_bytes(tq, kc) + kc / 2 + 16;
+}
+
 // Workspace layout (offsets in bytes, each 256-aligned).
 struct WsLayout {
   uint64_t err, ctr_route, nu, u_slot, u_fmt, u_addr, u_nrows, u_rows;
-  uint64_t comb_u, comb_r, comb_w, z, xf, xh, xsc, xq, xql, xt, xtl, s16, s16l, xsb, pa, h, hq, hql, hs16, hs16l,
-      hsb, pb, dbg;
+  uint64_t comb_u, comb_r, comb_w, z, xf, xh, xsc, xrq, xrt, pa, h, hr, pb, dbg;
   uint64_t fctr, cnt_a, h_cnt, ctr_out, total;  // counters of the fused layer kernel
 };
 constexpr int kDbgSlots = 8;      // per-CTA cycle counters of the diagnostic mode
@@ -155,24 +167,15 @@ __host__ __device__ inline WsLayout make_ws(const Geo& g) {
   w.xh = o; o = al256(o + 2ull * g.M * g.H);   // f16(x * 2^s_m): exact, per-row power-of-two scale
   w.xsc = o; o = al256(o + 4ull * kMaxM);      // 2^-s_m
   // x as X_hi + X_lo / 128 with X_hi = rint(x 2^si) (int16) and X_lo the
-  // int8 residual, each in the two orders of the integer GEMV paths
-  w.xq = o; o = al256(o + 2ull * g.M * g.H);                   // X_hi, "Q order" per 16 columns
-  w.xql = o; o = al256(o + 1ull * g.M * g.H);                  // X_lo, Q order
-  w.xt = o; o = al256(o + 528ull * g.M * (g.H / 256));        // X_hi, "T order" (528 bytes per 256 columns)
-  w.xtl = o; o = al256(o + 272ull * g.M * (g.H / 256));       // X_lo, T order (272 bytes per 256 columns)
-  w.s16 = o; o = al256(o + 4ull * g.M * (g.H / 16));          // int32 sum of X_hi over every 16 columns
-  w.s16l = o; o = al256(o + 4ull * g.M * (g.H / 16));         // ... of X_lo
-  w.xsb = o; o = al256(o + 16ull * g.M * g.nchA);             // 2^-si per 256 columns, 4 slots per K chunk
+  // int8 residual: one record per (row, K chunk) in each of the two orders
+  // of the integer GEMV paths (int_rec_bytes)
+  w.xrq = o; o = al256(o + (uint64_t)int_rec_bytes(0, g.kcA) * g.M * g.nchA);
+  w.xrt = o; o = al256(o + (uint64_t)int_rec_bytes(1, g.kcA) * g.M * g.nchA);
   w.pa = o; o = al256(o + 4ull * g.U * g.npanA * g.nchA * 2 * g.M * 32);
   w.h = o; o = al256(o + 4ull * g.U * g.M * g.I);
-  // h of every (expert, row) for the integer W2 paths: X_hi / X_lo in the
-  // order of that expert's format (every row has room for T order: 528 + 272
-  // bytes per 256 columns), the 16-column sums, and 2^-si of each 256 columns
-  w.hq = o; o = al256(o + 528ull * g.U * g.M * (g.I / 256));  // every row sized for T order
-  w.hql = o; o = al256(o + 272ull * g.U * g.M * (g.I / 256));
-  w.hs16 = o; o = al256(o + 4ull * g.U * g.M * (g.I / 16));
-  w.hs16l = o; o = al256(o + 4ull * g.U * g.M * (g.I / 16));
-  w.hsb = o; o = al256(o + 16ull * g.U * g.M * g.nchB);       // 2^-si per 256 columns of h, 4 slots per chunk
+  // h of every (expert, row) for the integer W2 paths: one record per K
+  // chunk in the order of that expert's format, each sized for T order
+  w.hr = o; o = al256(o + (uint64_t)int_rec_bytes(1, g.kcB) * g.U * g.M * g.nchB);
   w.pb = o; o = al256(o + 4ull * g.U * g.nchB * g.M * g.H);
   w.dbg = o; o = al256(o + 8ull * 3 * kDbgMaxCtas * kDbgSlots);  // [phase A, phase B, router][cta][slot] cycles
   w.fctr = o; o = al256(o + 16);                                  // [0] logits done, [1] CTAs done
@@ -211,6 +214,10 @@ struct ExpParams {
   int nstages;        // ring depth (<= 16), chosen by the host from the smem budget
   int drop_item;      // test hook: CTA 0's producer never issues its item number drop_item (-1: off)
   int variant;        // inner-loop variant for MXFP4 in phase A (0: f32 FMA, 1: f16-input FMA)
+  const int32_t* slot_table;  // E + 1 slots, or null: with it, the shared expert's weights (slot_table[E])
+                              // are streamed in before the routing results are awaited
+  bqe_pool pool;
+  int max_pre;                // at most this many shared-expert stages streamed before the wait
   int diag;           // 1: accumulate per-CTA cycle counters into ws.dbg
   uint64_t limit_ns;  // bound on every mbarrier wait
 };
@@ -249,7 +256,7 @@ uint32_t experts_smem_bytes(const Geo& g, int phase, int* nstages_out);
 
 // Error detail codes written to ws.err[1].
 enum { kErrSlotRange = 1, kErrSlotFmt = 2, kErrSlotExtent = 3, kErrWaitFull = 4, kErrWaitEmpty = 5,
-       kErrForcedIdx = 6 };
+       kErrForcedIdx = 6, kErrPreload = 12 };  // 7..11: the prefill kernels
 
 #ifdef __CUDACC__
 // ----------------------------------------------------------------------------
@@ -268,6 +275,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
+}
+// Raise the transaction count of the current phase without arriving (bulk
+// copies issued before the arrival that completes the phase).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -372,6 +384,54 @@ __device__ __forceinline__ float4 ldg_stream_f4(const float4* p, uint64_t pol) {
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "l"(p), "l"(pol));
   return v;
+}
+// Writers of the integer staging records (int_rec_bytes): X_hi / X_lo of
+// column j (0..255) of the k-th 256-column block of the chunk, in the
+// record's order.  Q order: within 16 columns, X_hi word 2q = (x_q, x_{q+4}),
+// word 2q + 1 = (x_{q+8}, x_{q+12}), X_lo word q = (x_q, x_{q+4}, x_{q+8},
+// x_{q+12}).  T order: in run m of 20 columns, X_hi word 2r = (x_{20m+r},
+// x_{20m+5+r}), word 2r + 1 = (x_{20m+10+r}, x_{20m+15+r}), X_lo word r =
+// (x_{20m+r}, x_{20m+5+r}, x_{20m+10+r}, x_{20m+15+r}); slots past column
+// 255 are zero (rec_put_pad).
+__device__ __forceinline__ void rec_put(uint8_t* rec, int tq, int kc, int k, int j, int Xh, int Xl) {
+  int16_t* hi = reinterpret_cast<int16_t*>(rec);
+  int8_t* lo = reinterpret_cast<int8_t*>(rec + int_rec_hi_bytes(tq, kc));
+  if (tq) {
+    const int run = j / 20, jr = j % 20, q4 = jr / 5, rd = jr % 5;
+    hi[k * 264 + run * 20 + 4 * rd + 2 * (q4 >> 1) + (q4 & 1)] = (int16_t)Xh;
+    lo[k * 272 + run * 20 + 4 * rd + q4] = (int8_t)Xl;
+  } else {
+    const int jj = j & 15, kq = jj & 3, iq = jj >> 2;
+    hi[k * 256 + (j & ~15) + 4 * kq + 2 * (iq >> 1) + (iq & 1)] = (int16_t)Xh;
+    lo[k * 256 + (j & ~15) + 4 * kq + iq] = (int8_t)Xl;
+  }
+}
+// T order: slot i (0..15) of the padding of block k (run 12's weights 256..259
+// and the tail slots), written as zero
+__device__ __forceinline__ void rec_put_pad(uint8_t* rec, int kc, int k, int i) {
+  int16_t* hi = reinterpret_cast<int16_t*>(rec);
+  int8_t* lo = reinterpret_cast<int8_t*>(rec + int_rec_hi_bytes(1, kc));
+  const int slot = i < 4 ? 240 + 4 * (i + 1) + 3 : 260 + (i - 4);
+  if (i < 8) hi[k * 264 + slot] = 0;
+  lo[k * 272 + slot] = 0;
+}
+// sums of X_hi and X_lo over the 16-column group g16 (0..15) of block k
+__device__ __forceinline__ void rec_put_sums(uint8_t* rec, int tq, int kc, int k, int g16, int sh, int sl) {
+  int32_t* sp = reinterpret_cast<int32_t*>(rec + int_rec_hi_bytes(tq, kc) + int_rec_lo_bytes(tq, kc));
+  sp[k * 16 + g16] = sh;
+  sp[kc / 16 + k * 16 + g16] = sl;
+}
+// 2^-si of block k
+__device__ __forceinline__ void rec_put_scale(uint8_t* rec, int tq, int kc, int k, float v) {
+  reinterpret_cast<float*>(rec + int_rec_hi_bytes(tq, kc) + int_rec_lo_bytes(tq, kc) + kc / 2)[k] = v;
+}
+
+// Selection key of an expert: sigmoid(z) + b as an order-preserving 32-bit
+// image (larger key = larger value; 0 is below every real key).
+__device__ __forceinline__ uint32_t sel_key(float zv, float b) {
+  const float f = 1.0f / (1.0f + expf(-zv)) + b;
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {

@@ -15,6 +15,8 @@
 // One kernel: every CTA computes z for two experts (four warps per expert,
 // one quarter of hidden each, all loads in flight at once); the last CTA to
 // finish (arrival counter, no waiting) selects, weighs and builds the list.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -64,10 +66,24 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
       if (i < ni) w4[i] = ldg_stream_f4(wr + i * 32 + lane, pol);
   }
 
+  // inputs of the selection, read while the previous kernel finishes (no
+  // kernel of the layer writes them): the slot of every expert, the slot's
+  // format and offset (out-of-range slots are reported when used), the bias
+  __shared__ int32_t s_table[kMaxE + 1];
+  __shared__ int32_t s_sfmt[kMaxE + 1];
+  __shared__ uint64_t s_soff[kMaxE + 1];
+  __shared__ float s_bias[kMaxE];
+  for (int i = tid; i <= E; i += kRouteThreads) {
+    const int sl = P.slot_table[i];
+    const bool okr = sl >= 0 && sl < P.pool.n_slots;
+    s_table[i] = sl;
+    s_sfmt[i] = okr ? P.pool.slot_fmt[sl] : 0;
+    s_soff[i] = okr ? P.pool.slot_off[sl] : 0;
+    if (i < E) s_bias[i] = P.bias ? P.bias[i] : 0.f;
+  }
+
   griddep_wait();  // the layer input may come from the previous kernels
   griddep_launch_dependents();  // the W1/W3 kernel may start its own prologue now
-  __shared__ int32_t s_table[kMaxE + 1];  // slot of every expert (the selecting CTA uses it)
-  for (int i = tid; i <= E; i += kRouteThreads) s_table[i] = P.slot_table[i];
 
   // ---- layer input into shared memory: bf16 x, or bf16(rmsnorm(resid)) -------
   if (P.resid) {
@@ -98,86 +114,6 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
     for (int i = tid; i < M * H / 8; i += kRouteThreads) dst[i] = src[i];
   }
   __syncthreads();
-
-  // ---- side job: fp32 and scaled-f16 copies of the layer input --------------
-  // f16(x * 2^s) is exact for a bf16 x as long as x * 2^s is a normal f16;
-  // s puts the row's largest |x| in [2^14, 2^15).  Every CTA derives the same s.
-  __shared__ int s_emax[kMaxM];
-  if (tid < M) s_emax[tid] = -1000;
-  __syncthreads();
-  for (int m = 0; m < M; ++m) {
-    uint32_t mx = 0;
-    for (int k = tid; k < H; k += kRouteThreads) mx = max(mx, (uint32_t)(xs[m * H + k] & 0x7FFFu));
-    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0 && mx) atomicMax(&s_emax[m], (int)(mx >> 7) - 127);  // floor(log2 max|x|)
-  }
-  __syncthreads();
-  {
-    uint16_t* xh = (uint16_t*)(P.ws + P.L.xh);
-    const int n = M * H;
-    const int per = (n + gridDim.x - 1) / gridDim.x;
-    const int lo = per * blockIdx.x, hi = min(n, lo + per);
-    for (int i = lo + tid; i < hi; i += kRouteThreads) {
-      const float v = bf16_to_f32(xs[i]);
-      const int m = i / H;
-      const int sh = s_emax[m] == -1000 ? 0 : 14 - s_emax[m];
-      xf[i] = v;
-      xh[i] = __half_as_ushort(__float2half_rn(ldexpf(v, sh)));
-      if (P.t_out) P.t_out[i] = xs[i];
-    }
-    if (blockIdx.x == 0 && tid < M) {
-      const int sh = s_emax[tid] == -1000 ? 0 : 14 - s_emax[tid];
-      ((float*)(P.ws + P.L.xsc))[tid] = ldexpf(1.0f, -sh);
-    }
-  }
-  {
-    // x as X_hi + X_lo / 128: X_hi = rint(x 2^si) (int16, max |x| 2^si in
-    // [2^13, 2^14)), X_lo = rint((x 2^si - X_hi) 128) (int8, |X_lo| <= 64), in
-    // the two orders the integer GEMV paths read, and the sums of X_hi and X_lo
-    // over every 16 columns.  One CTA per 256-column block, one column per
-    // thread, so the extra work is spread thinly over the grid.
-    int16_t* xq = (int16_t*)(P.ws + P.L.xq);
-    int8_t* xql = (int8_t*)(P.ws + P.L.xql);
-    int16_t* xt = (int16_t*)(P.ws + P.L.xt);
-    int8_t* xtl = (int8_t*)(P.ws + P.L.xtl);
-    int32_t* s16 = (int32_t*)(P.ws + P.L.s16);
-    int32_t* s16l = (int32_t*)(P.ws + P.L.s16l);
-    const int nbr = H / 256, nblk = M * nbr;
-    for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
-      const int m = blk / nbr, bj = blk % nbr;
-      const int si = s_emax[m] == -1000 ? 0 : 13 - s_emax[m];
-      const int64_t q0 = (int64_t)m * H + bj * 256, t0 = (int64_t)m * nbr + bj;
-      const int j = tid;  // column within the block
-      const float v = ldexpf(bf16_to_f32(xs[m * H + bj * 256 + j]), si);
-      const int Xh = __float2int_rn(v);
-      const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
-      const int jj = j & 15, kq = jj & 3, iq = jj >> 2;
-      xq[q0 + (j & ~15) + 4 * kq + 2 * (iq >> 1) + (iq & 1)] = (int16_t)Xh;
-      xql[q0 + (j & ~15) + 4 * kq + iq] = (int8_t)Xl;
-      const int run = j / 20, jr = j % 20, q4 = jr / 5, rd = jr % 5;
-      xt[t0 * 264 + run * 20 + 4 * rd + 2 * (q4 >> 1) + (q4 & 1)] = (int16_t)Xh;
-      xtl[t0 * 272 + run * 20 + 4 * rd + q4] = (int8_t)Xl;
-      int ph = Xh, pl = Xl;
-#pragma unroll
-      for (int o = 8; o; o >>= 1) {
-        ph += __shfl_xor_sync(0xffffffffu, ph, o);
-        pl += __shfl_xor_sync(0xffffffffu, pl, o);
-      }
-      if ((lane & 15) == 0) {
-        s16[(int64_t)m * (H / 16) + bj * 16 + (tid >> 4)] = ph;
-        s16l[(int64_t)m * (H / 16) + bj * 16 + (tid >> 4)] = pl;
-      }
-      if (tid == 0) {  // 2^-si of this block, in the slot of its K chunk
-        const int bpc = g.kcA / 256;
-        ((float*)(P.ws + P.L.xsb))[((int64_t)m * g.nchA + bj / bpc) * 4 + bj % bpc] = ldexpf(1.0f, -si);
-      }
-      if (tid < 16) {  // T-order slots past column 255 (run 12, weights 255 + 1..4) and the padding
-        const int slot = tid < 4 ? 240 + 4 * (tid + 1) + 3 : 260 + (tid - 4);
-        if (tid < 8) xt[t0 * 264 + slot] = 0;
-        xtl[t0 * 272 + slot] = 0;
-      }
-    }
-  }
 
   // ---- router GEMV ----------------------------------------------------------
   float acc[M];
@@ -222,15 +158,90 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
               (unsigned long long)(clock64() - t_start));
     dbg_span(P.ws, P.L.dbg, 2, true);
   }
-  // ---- last CTA: scores, top-k, weights, work list ---------------------------
+  // ---- arrival: the last CTA selects, every other one takes a share of the
+  // side job (the copies of x the expert kernels read), by arrival rank ------
   __threadfence();
   __syncthreads();
   if (tid == 0) {
     unsigned int* ctr = (unsigned int*)(P.ws + P.L.ctr_route);
-    s_last = (atomicAdd(ctr, 1u) == gridDim.x - 1);
+    s_last = (int)atomicAdd(ctr, 1u);
   }
   __syncthreads();
-  if (!s_last) return;
+  const int rank = s_last;
+  const bool last = rank == (int)gridDim.x - 1;
+  __shared__ int s_emax[kMaxM];
+  if (!last || gridDim.x == 1) {
+    const int nside = gridDim.x == 1 ? 1 : (int)gridDim.x - 1;
+    const int srank = gridDim.x == 1 ? 0 : rank;
+  // ---- side job: fp32 and scaled-f16 copies of the layer input --------------
+  // f16(x * 2^s) is exact for a bf16 x as long as x * 2^s is a normal f16;
+  // s puts the row's largest |x| in [2^14, 2^15).  Every CTA derives the same s.
+  if (tid < M) s_emax[tid] = -1000;
+  __syncthreads();
+  for (int m = 0; m < M; ++m) {
+    uint32_t mx = 0;
+    for (int k = tid; k < H; k += kRouteThreads) mx = max(mx, (uint32_t)(xs[m * H + k] & 0x7FFFu));
+    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0 && mx) atomicMax(&s_emax[m], (int)(mx >> 7) - 127);  // floor(log2 max|x|)
+  }
+  __syncthreads();
+  {
+    uint16_t* xh = (uint16_t*)(P.ws + P.L.xh);
+    const int n = M * H;
+    const int per = (n + nside - 1) / nside;
+    const int lo = per * srank, hi = min(n, lo + per);
+    for (int i = lo + tid; i < hi; i += kRouteThreads) {
+      const float v = bf16_to_f32(xs[i]);
+      const int m = i / H;
+      const int sh = s_emax[m] == -1000 ? 0 : 14 - s_emax[m];
+      xf[i] = v;
+      xh[i] = __half_as_ushort(__float2half_rn(ldexpf(v, sh)));
+      if (P.t_out) P.t_out[i] = xs[i];
+    }
+    if (srank == 0 && tid < M) {
+      const int sh = s_emax[tid] == -1000 ? 0 : 14 - s_emax[tid];
+      ((float*)(P.ws + P.L.xsc))[tid] = ldexpf(1.0f, -sh);
+    }
+  }
+  {
+    // x as X_hi + X_lo / 128: X_hi = rint(x 2^si) (int16, max |x| 2^si in
+    // [2^13, 2^14)), X_lo = rint((x 2^si - X_hi) 128) (int8, |X_lo| <= 64), in
+    // the two orders the integer GEMV paths read, and the sums of X_hi and X_lo
+    // over every 16 columns.  One CTA per 256-column block, one column per
+    // thread, so the extra work is spread thinly over the side-job CTAs.
+    const int nbr = H / 256, nblk = M * nbr, bpc = g.kcA / 256;
+    for (int blk = srank; blk < nblk; blk += nside) {
+      const int m = blk / nbr, bj = blk % nbr;
+      const int c = bj / bpc, k = bj % bpc;  // K chunk of the block and its place in the chunk
+      uint8_t* rq = P.ws + P.L.xrq + ((size_t)m * g.nchA + c) * int_rec_bytes(0, g.kcA);
+      uint8_t* rt = P.ws + P.L.xrt + ((size_t)m * g.nchA + c) * int_rec_bytes(1, g.kcA);
+      const int si = s_emax[m] == -1000 ? 0 : 13 - s_emax[m];
+      const int j = tid;  // column within the block
+      const float v = ldexpf(bf16_to_f32(xs[m * H + bj * 256 + j]), si);
+      const int Xh = __float2int_rn(v);
+      const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
+      rec_put(rq, 0, g.kcA, k, j, Xh, Xl);
+      rec_put(rt, 1, g.kcA, k, j, Xh, Xl);
+      if (tid < 16) rec_put_pad(rt, g.kcA, k, tid);
+      int ph = Xh, pl = Xl;
+#pragma unroll
+      for (int o = 8; o; o >>= 1) {
+        ph += __shfl_xor_sync(0xffffffffu, ph, o);
+        pl += __shfl_xor_sync(0xffffffffu, pl, o);
+      }
+      if ((lane & 15) == 0) {
+        rec_put_sums(rq, 0, g.kcA, k, tid >> 4, ph, pl);
+        rec_put_sums(rt, 1, g.kcA, k, tid >> 4, ph, pl);
+      }
+      if (tid == 0) {  // 2^-si of this block
+        rec_put_scale(rq, 0, g.kcA, k, ldexpf(1.0f, -si));
+        rec_put_scale(rt, 1, g.kcA, k, ldexpf(1.0f, -si));
+      }
+    }
+  }
+
+  }
+  if (!last) return;
   __threadfence();
   auto stamp = [&](int k) {
     if (P.diag && tid == 0)
@@ -239,16 +250,6 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
   };
   stamp(0);
 
-  // slot format and offset of every expert, loaded now so the loads overlap
-  // the selection below (out-of-range slots are reported when used)
-  __shared__ int32_t s_sfmt[kMaxE + 1];
-  __shared__ uint64_t s_soff[kMaxE + 1];
-  for (int i = tid; i <= E; i += kRouteThreads) {
-    const int sl = s_table[i];
-    const bool okr = sl >= 0 && sl < P.pool.n_slots;
-    s_sfmt[i] = okr ? P.pool.slot_fmt[sl] : 0;
-    s_soff[i] = okr ? P.pool.slot_off[sl] : 0;
-  }
 
   __shared__ uint32_t s_mask[kMaxE];           // bit m: row m chose expert e
   __shared__ int s_uof[kMaxE];                  // work-list index of a chosen expert
@@ -270,18 +271,14 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
   __shared__ uint32_t s_ck[kMaxM][kRouteThreads / 32][kMaxTopK];
   __shared__ int s_ci[kMaxM][kRouteThreads / 32][kMaxTopK];
   __shared__ float s_cz[kMaxM][kRouteThreads / 32][kMaxTopK];
-  auto ord = [](float f) -> uint32_t {
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  };
   if (!P.forced) {
     for (int m = 0; m < M; ++m) {
       const int e0 = tid, e1 = tid + kRouteThreads;
       const float z0 = e0 < E ? __ldcg(z + (int64_t)m * E + e0) : 0.f;
       const float z1 = e1 < E ? __ldcg(z + (int64_t)m * E + e1) : 0.f;
       uint32_t k0 = 0u, k1 = 0u;  // 0: no expert (below every real key)
-      if (e0 < E) k0 = ord(1.0f / (1.0f + expf(-z0)) + (P.bias ? P.bias[e0] : 0.f));
-      if (e1 < E) k1 = ord(1.0f / (1.0f + expf(-z1)) + (P.bias ? P.bias[e1] : 0.f));
+      if (e0 < E) k0 = sel_key(z0, s_bias[e0]);
+      if (e1 < E) k1 = sel_key(z1, s_bias[e1]);
       for (int j = 0; j < K; ++j) {
         uint32_t lk = k0;
         int li = e0;
@@ -478,10 +475,21 @@ int launch_route(const RouteParams& P, cudaStream_t st, bool pdl) {
                                      k_route<5>, k_route<6>, k_route<7>, k_route<8>};
   auto fn = fns[P.g.M - 1];
   if (smem > 48 * 1024 && limit_set[dev] < (int)smem) {
+    // dynamic + static shared memory must fit the opt-in limit of a block
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return BQE_ECUDA;
+    int lim = 1 << 30;
+    for (int m = 0; m < kMaxM; ++m) {
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, fns[m]) != cudaSuccess) return BQE_ECUDA;
+      lim = std::min(lim, optin - (int)fa.sharedSizeBytes);
+    }
+    if (lim < (int)smem) return BQE_EUNSUPPORTED;
     for (int m = 0; m < kMaxM; ++m)
-      if (cudaFuncSetAttribute(fns[m], cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
+      if (cudaFuncSetAttribute(fns[m], cudaFuncAttributeMaxDynamicSharedMemorySize, lim) != cudaSuccess)
         return BQE_ECUDA;
-    limit_set[dev] = 200 * 1024;
+    limit_set[dev] = lim;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -310,6 +310,11 @@ void bqe_set_fused(int32_t on);
  * 4e-4 for fp16).  Both run at the same tensor-core rate. */
 void bqe_set_prefill_f16(int32_t on);
 
+/* Diagnostic: at most n ring stages of shared-expert weights streamed by each
+ * expert-kernel CTA before it waits for the previous kernel (default 16: as
+ * many as the ring holds; 0: none).  Results do not change. */
+void bqe_set_preload(int32_t n);
+
 /* Diagnostic: at most max_a (W1/W3) and max_b (W2) 32-row panels per work
  * item of the decode expert kernels (0: the default choice, the largest that
  * fits).  Fewer panels per item leave room for more ring stages.  Results do
