@@ -68,8 +68,8 @@ def parse():
                     help="routed experts in the pool (profiling a smaller pool; per-call work is unchanged)")
     ap.add_argument("--tokens", type=int, default=8192, help="prefill: token rows per call")
     ap.add_argument("--panels", default=None, help="decode: max panels per work item, 'A,B' (diagnostic)")
-    ap.add_argument("--preload", type=int, default=None,
-                    help="decode: max shared-expert stages streamed before the wait (diagnostic)")
+    ap.add_argument("--preload", default=None,
+                    help="decode: max shared-expert stages streamed before the wait, 'A,B' (diagnostic)")
     ap.add_argument("--fused", action="store_true", help="decode: the single-kernel layer (bqe_set_fused)")
     ap.add_argument("--cpu-oracle-sample", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -274,7 +274,8 @@ def run_layer(args, rank, world):
         pa, pb = (int(v) for v in args.panels.split(","))
         A.bqe_set_panels(pa, pb)
     if args.preload is not None:
-        A.bqe_set_preload(args.preload)
+        pa_, pb_ = (int(v) for v in args.preload.split(","))
+        A.bqe_set_preload(pa_, pb_)
     if args.fused:
         A.bqe_set_fused(True)
     M = 6 if args.workload.endswith("m6") else 1
@@ -481,11 +482,21 @@ def run_layer(args, rank, world):
             dv = ws[off:off + 8 * 3 * 1024 * 8].view(torch.int64).view(3, 1024, 8)
             dv[:, 1023, 0] = 2 ** 62
             dv[:, 1023, 1] = 0
+            dv[:2, 1023, 2] = 2 ** 62  # phases A, B: first and last CTA past the wait
+            dv[:2, 1023, 3] = 0
+            dv[2, 1023, 4] = 2 ** 62   # finalize kernels: first CTA past the wait, last CTA end
+            dv[2, 1023, 5] = 0
+            dv[2, 1023, 6] = 2 ** 62
+            dv[2, 1023, 7] = 0
             xbuf.copy_(xs[s_ % n_x])
             fused(s_ % NL)  # the layer entry point, eager: kernel parameters carry the diagnostic flag
             torch.cuda.synchronize()
-            sp = dv[:, 1023, :2].cpu().numpy()
-            spans.append([(sp[k, 1] - sp[k, 0]) / 1e3 for k in (2, 0, 1)])
+            sp = dv[:, 1023, :].cpu().numpy().astype(np.float64)
+            t0 = sp[2, 0]
+            spans.append([(sp[k, 1] - sp[k, 0]) / 1e3 for k in (2, 0, 1)] +
+                         [(v - t0) / 1e3 for v in (sp[2, 1], sp[0, 0], sp[0, 2], sp[0, 3], sp[0, 1], sp[2, 4],
+                                                   sp[2, 5], sp[1, 0], sp[1, 2], sp[1, 3], sp[1, 1], sp[2, 6],
+                                                   sp[2, 7])])
         A.bqe_set_diag(False)
         dbg = ws[off:off + 8 * 3 * 1024 * 8].view(torch.int64).view(3, 1024, 8).cpu().numpy()
         sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -500,11 +511,16 @@ def run_layer(args, rank, world):
         vr = dbg[2, :ncta].astype(np.float64) / nd / 2.07e3
         rep["router"] = {"cta_gemv_us": [round(float(vr[:, 0].mean()), 2), round(float(vr[:, 0].max()), 2)],
                          "last_cta_total_us": round(float(dbg[2, 1022, 1]) / nd / 2.07e3, 2)}
-        rep["router_tail_stamps_us"] = [round(float(v) / nd / 2.07e3, 2) for v in dbg[2, 1021, :7]]
+        rep["router_tail_stamps_us"] = [round(float(v) / nd / 2.07e3, 2) for v in dbg[2, 1021, :8]]
         sp = np.array(spans)
         rep["kernel_span_us(first CTA start -> last CTA end)"] = dict(
             router=round(float(sp[:, 0].mean()), 2), phase_a=round(float(sp[:, 1].mean()), 2),
             phase_b=round(float(sp[:, 2].mean()), 2))
+        tl_names = ["router_end", "A_start", "A_first_past_wait", "A_last_past_wait", "A_end", "finA_past_wait",
+                    "finA_end", "B_start", "B_first_past_wait", "B_last_past_wait", "B_end", "finB_past_wait",
+                    "finB_end"]
+        rep["timeline_us(from router start)"] = {n: round(float(sp[:, 3 + k].mean()), 2)
+                                                 for k, n in enumerate(tl_names)}
         A.bqe_workspace_init(ws, nb)
         sys.stderr.write("DIAG " + json.dumps(rep) + "\n")
 

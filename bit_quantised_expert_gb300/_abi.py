@@ -77,7 +77,7 @@ SIGNATURES = {
     "bqe_set_variant": (None, [_I32]),
     "bqe_set_prefill_f16": (None, [_I32]),
     "bqe_set_panels": (None, [_I32, _I32]),
-    "bqe_set_preload": (None, [_I32]),
+    "bqe_set_preload": (None, [_I32, _I32]),
     "bqe_prefill_kernel_ms": (ctypes.c_int, [_P]),
     "bqe_prefill_diag_offset": (_U64, [_DESC, _I32]),
     "bqe_set_diag": (None, [_I32]),
@@ -263,8 +263,8 @@ def bqe_set_panels(max_a: int, max_b: int) -> None:
     lib.bqe_set_panels(int(max_a), int(max_b))
 
 
-def bqe_set_preload(n: int) -> None:
-    lib.bqe_set_preload(int(n))
+def bqe_set_preload(n_a: int, n_b: int) -> None:
+    lib.bqe_set_preload(int(n_a), int(n_b))
 
 
 def bqe_set_prefill_f16(on: bool) -> None:

@@ -18,7 +18,7 @@ static std::atomic<int> g_diag{0};
 static std::atomic<int> g_fused{0};
 static std::atomic<int> g_pf_f16{1};
 static std::atomic<int> g_pmax_a{0}, g_pmax_b{0};
-static std::atomic<int> g_preload{16};
+static std::atomic<int> g_preload_a{16}, g_preload_b{16};
 
 // Diagnostic knobs (not part of the operation): the bound on every in-kernel
 // wait, and whether kernels are chained with programmatic dependent launch.
@@ -29,7 +29,10 @@ extern "C" void bqe_set_variant(int32_t v) { g_variant = v; }
 extern "C" void bqe_set_diag(int32_t on) { g_diag = on ? 1 : 0; }
 extern "C" void bqe_set_fused(int32_t on) { g_fused = on ? 1 : 0; }
 extern "C" void bqe_set_prefill_f16(int32_t on) { g_pf_f16 = on ? 1 : 0; }
-extern "C" void bqe_set_preload(int32_t n) { g_preload = n < 0 ? 0 : n; }
+extern "C" void bqe_set_preload(int32_t n_a, int32_t n_b) {
+  g_preload_a = n_a < 0 ? 0 : n_a;
+  g_preload_b = n_b < 0 ? 0 : n_b;
+}
 extern "C" void bqe_set_panels(int32_t max_a, int32_t max_b) {
   g_pmax_a = max_a > 0 ? max_a : 0;
   g_pmax_b = max_b > 0 ? max_b : 0;
@@ -139,7 +142,7 @@ static int experts_common(const bqe_layer_desc* d, int32_t M, const bqe_pool* po
   P.diag = g_diag.load();
   P.slot_table = slot_table;
   P.pool = *pool;
-  P.max_pre = g_preload.load();
+  P.max_pre = 0;
   const bool pdl = g_use_pdl.load() != 0;
   for (int phase = 0; phase < 2; ++phase) {
     if (only_phase >= 0 && phase != only_phase) continue;
@@ -147,6 +150,7 @@ static int experts_common(const bqe_layer_desc* d, int32_t M, const bqe_pool* po
     experts_smem_bytes(g, phase, &ns);
     if (ns < 2) return BQE_EUNSUPPORTED;
     P.nstages = ns;
+    P.max_pre = phase == 0 ? g_preload_a.load() : g_preload_b.load();
     if ((rc = launch_experts(P, phase, sms, st, pdl))) return rc;
     if ((rc = launch_finalize(P, phase, sms, st, pdl))) return rc;
   }

@@ -169,6 +169,10 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
 
   griddep_wait();  // routing / phase A results must be complete and visible
   griddep_launch_dependents();  // the finalize kernel may be scheduled behind this one
+  if (P.diag && tid == 0) {
+    dbg_time(P.ws, P.L.dbg, PHASE, 2, false);  // first CTA past the wait
+    dbg_time(P.ws, P.L.dbg, PHASE, 3, true);   // last CTA past the wait
+  }
 
   // the work list (format, slot address, rows of every distinct expert) and
   // what the producer derives from it, in shared memory, so no item waits on
@@ -488,17 +492,17 @@ __global__ void __maxnreg__(32) k_finalize_a(ExpParams P) {  // 32 registers: fi
   // leave and stream the shared expert's W2 tiles until they may read h.
   griddep_launch_dependents();
   griddep_wait();
+  if (P.diag && threadIdx.x == 0) dbg_time(P.ws, P.L.dbg, 2, 4, false);
   const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
   const int nbl = g.I / 256;
   // work = (expert, row of the expert, 256 columns); prefix sums of the rows
+  // (the row counts loaded in parallel, then added up in shared memory)
   __shared__ int s_pre[kMaxM * kMaxTopK + 2];
+  for (int u = threadIdx.x; u < nU; u += blockDim.x) s_pre[u + 1] = ((const int32_t*)(P.ws + P.L.u_nrows))[u];
+  __syncthreads();
   if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int u = 0; u < nU; ++u) {
-      s_pre[u] = acc;
-      acc += ((const int32_t*)(P.ws + P.L.u_nrows))[u];
-    }
-    s_pre[nU] = acc;
+    s_pre[0] = 0;
+    for (int u = 0; u < nU; ++u) s_pre[u + 1] += s_pre[u];
   }
   __syncthreads();
   const int nwork = s_pre[nU] * nbl;
@@ -510,12 +514,14 @@ __global__ void __maxnreg__(32) k_finalize_a(ExpParams P) {  // 32 registers: fi
     finalize_a_block(P, u, r, blk);
     __syncthreads();  // shared scratch of the block is reused
   }
+  if (P.diag && threadIdx.x == 0) dbg_time(P.ws, P.L.dbg, 2, 5, true);
 }
 
 __global__ void __launch_bounds__(kFinBThreads) k_finalize_b(ExpParams P) {
   const Geo& g = P.g;
   griddep_launch_dependents();  // the next layer's router may start loading its weights
   griddep_wait();
+  if (P.diag && threadIdx.x == 0) dbg_time(P.ws, P.L.dbg, 2, 6, false);
   const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
   const float* pb = (const float*)(P.ws + P.L.pb);
   const int nch = g.nchB;
@@ -579,6 +585,7 @@ __global__ void __launch_bounds__(kFinBThreads) k_finalize_b(ExpParams P) {
     float* o = P.out + t;
     *o = P.accumulate ? *o + val : val;
   }
+  if (P.diag && threadIdx.x == 0) dbg_time(P.ws, P.L.dbg, 2, 7, true);
 }
 
 // The finalize kernels run at most one CTA per SM, each looping over its

@@ -464,6 +464,18 @@ __device__ __forceinline__ void dbg_span(uint8_t* ws, uint64_t dbg_off, int blk,
     atomicMin(p + 0, (unsigned long long)t);
 }
 
+// Diagnostic timeline: globaltimer into slot `slot` (2..7) of row 1023 of
+// block blk, as a running minimum or maximum over CTAs.
+__device__ __forceinline__ void dbg_time(uint8_t* ws, uint64_t dbg_off, int blk, int slot, bool is_max) {
+  unsigned long long* p = (unsigned long long*)(ws + dbg_off) + ((size_t)blk * 1024 + 1023) * 8 + slot;
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  if (is_max)
+    atomicMax(p, (unsigned long long)t);
+  else
+    atomicMin(p, (unsigned long long)t);
+}
+
 __device__ __forceinline__ void set_error(int32_t* err, int code, int detail) {
   if (atomicCAS(err, 0, code) == 0) err[1] = detail;
 }

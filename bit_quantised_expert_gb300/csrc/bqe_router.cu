@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
 
 
   __shared__ uint32_t s_mask[kMaxE];           // bit m: row m chose expert e
-  __shared__ int s_uof[kMaxE];                  // work-list index of a chosen expert
+  __shared__ int16_t s_uof[kMaxE];              // work-list index of a chosen expert
   __shared__ int s_idx[kMaxM][kMaxTopK];
   __shared__ float s_zsel[kMaxM][kMaxTopK];
   __shared__ int s_list[kMaxM * kMaxTopK];      // chosen experts, ascending
@@ -264,49 +264,31 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
   __syncthreads();
   stamp(1);
 
-  // ---- top-k: every warp keeps the k best of its 64 experts (thread t scores
-  // experts t and t + 256), then warp m merges the 8k candidates of row m.
-  // Order: larger key first, ties to the lower expert id; keys compared as
-  // order-preserving 32-bit images so one warp max + one warp min decide a round.
-  __shared__ uint32_t s_ck[kMaxM][kRouteThreads / 32][kMaxTopK];
-  __shared__ int s_ci[kMaxM][kRouteThreads / 32][kMaxTopK];
-  __shared__ float s_cz[kMaxM][kRouteThreads / 32][kMaxTopK];
+  // ---- top-k: the keys of every row in shared memory (all threads), then
+  // warp m selects row m: each lane holds the keys of experts lane, lane + 32,
+  // ...; a round takes the lane's largest key (strict compare in ascending
+  // expert order keeps the lower id on a tie), then one warp max and one warp
+  // min decide the round.  Order: larger key first, ties to the lower id.
+  __shared__ uint32_t s_key[kMaxM][kMaxE];
+  float* s_zr = reinterpret_cast<float*>(xs);  // logits, row-major M x E (x is no longer needed; E <= H / 2)
   if (!P.forced) {
-    for (int m = 0; m < M; ++m) {
-      const int e0 = tid, e1 = tid + kRouteThreads;
-      const float z0 = e0 < E ? __ldcg(z + (int64_t)m * E + e0) : 0.f;
-      const float z1 = e1 < E ? __ldcg(z + (int64_t)m * E + e1) : 0.f;
-      uint32_t k0 = 0u, k1 = 0u;  // 0: no expert (below every real key)
-      if (e0 < E) k0 = sel_key(z0, s_bias[e0]);
-      if (e1 < E) k1 = sel_key(z1, s_bias[e1]);
-      for (int j = 0; j < K; ++j) {
-        uint32_t lk = k0;
-        int li = e0;
-        if (k1 > lk) { lk = k1; li = e1; }  // e0 < e1, so ties keep e0
-        const uint32_t wk = __reduce_max_sync(0xffffffffu, lk);
-        const int best = (int)__reduce_min_sync(0xffffffffu, (lk == wk && wk != 0u) ? (uint32_t)li : 0x7fffffffu);
-        if (best == e0) { s_cz[m][warp][j] = z0; k0 = 0u; }
-        if (best == e1) { s_cz[m][warp][j] = z1; k1 = 0u; }
-        if (lane == 0) {
-          s_ck[m][warp][j] = wk;
-          s_ci[m][warp][j] = wk != 0u ? best : 0x7fffffff;
-        }
-      }
+    for (int i = tid; i < M * E; i += kRouteThreads) {
+      const int m = i / E, e = i - m * E;
+      const float zv = __ldcg(z + i);
+      s_zr[i] = zv;
+      s_key[m][e] = sel_key(zv, s_bias[e]);
     }
   }
   __syncthreads();
+  stamp(7);
   if (warp < M) {
     const int m = warp;
-    constexpr int NC = (kRouteThreads / 32) * kMaxTopK / 32;  // candidates per lane
-    uint32_t ck[NC];
-    int ci[NC];
+    constexpr int QN = kMaxE / 32;
+    uint32_t kk[QN];
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const int q2 = lane + 32 * c;           // candidate q2 = warp_q * K + j
-      const int wq = q2 / kMaxTopK, jq = q2 % kMaxTopK;
-      const bool valid = !P.forced && jq < K;
-      ck[c] = valid ? s_ck[m][wq][jq] : 0u;
-      ci[c] = valid ? s_ci[m][wq][jq] : 0x7fffffff;
+    for (int q = 0; q < QN; ++q) {
+      const int e = lane + 32 * q;
+      kk[q] = (!P.forced && e < E) ? s_key[m][e] : 0u;
     }
     for (int j = 0; j < K; ++j) {
       int best;
@@ -319,26 +301,22 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
         }
         zsel = __ldcg(z + (int64_t)m * E + best);
       } else {
-        uint32_t lk = 0u;
-        int li = 0x7fffffff, lc = -1;
+        uint32_t bk = 0u;
+        int bq = 0;
 #pragma unroll
-        for (int c = 0; c < NC; ++c)
-          if (ck[c] > lk || (ck[c] == lk && ci[c] < li)) { lk = ck[c]; li = ci[c]; lc = c; }
-        const uint32_t wk = __reduce_max_sync(0xffffffffu, lk);
-        best = (int)__reduce_min_sync(0xffffffffu, lk == wk ? (uint32_t)li : 0x7fffffffu);
-        float zc = 0.f;
-        int owner = 0;
-#pragma unroll
-        for (int c = 0; c < NC; ++c)
-          if (c == lc && li == best && lk == wk) {
-            const int q2 = lane + 32 * c;
-            zc = s_cz[m][q2 / kMaxTopK][q2 % kMaxTopK];
-            ck[c] = 0u;
-            ci[c] = 0x7fffffff;
-            owner = 1;
+        for (int q = 0; q < QN; ++q)
+          if (kk[q] > bk) {
+            bk = kk[q];
+            bq = q;
           }
-        const uint32_t own = __ballot_sync(0xffffffffu, owner);
-        zsel = __shfl_sync(0xffffffffu, zc, __ffs(own) - 1);
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t eb =
+            __reduce_min_sync(0xffffffffu, (bk == wk && wk != 0u) ? (uint32_t)(lane + 32 * bq) : 0xffffffffu);
+#pragma unroll
+        for (int q = 0; q < QN; ++q)
+          if (eb == (uint32_t)(lane + 32 * q)) kk[q] = 0u;
+        best = eb == 0xffffffffu ? 0 : (int)eb;
+        zsel = s_zr[m * E + best];
       }
       if (lane == 0) {
         s_idx[m][j] = best;
@@ -467,7 +445,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
 int launch_route(const RouteParams& P, cudaStream_t st, bool pdl) {
   const int grid = (P.g.E + 1) / 2;
   const size_t smem = (size_t)P.g.M * P.g.H * 2;
-  if (P.g.H / 4 / 128 > kRouteMaxNI || P.g.H % 512) return BQE_EUNSUPPORTED;
+  if (P.g.H / 4 / 128 > kRouteMaxNI || P.g.H % 512 || 2 * P.g.E > P.g.H) return BQE_EUNSUPPORTED;
   static int limit_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BQE_ECUDA;

@@ -52,7 +52,10 @@ enum {
 enum { BQE_FMT_TQ1 = 1, BQE_FMT_Q2_0 = 2, BQE_FMT_Q3_K = 3, BQE_FMT_MXFP4 = 4 };
 
 /* Shape of one MoE layer.  hidden and inter must be multiples of 256 (every
- * format's block divides 256) and of 32 rows; n_shared must be 1.
+ * format's block divides 256) and of 32 rows; n_shared must be 1; at most
+ * 512 routed experts and top_k <= 16.  The decode router (bqe_route and the
+ * layer entry points) also needs hidden a multiple of 512, at most 8192, and
+ * n_experts <= hidden / 2 (BQE_EUNSUPPORTED otherwise).
  * DeepSeek-V4.1-Flash: {5120, 2304, 384, 6, 1}. */
 typedef struct {
   int32_t hidden;
@@ -128,8 +131,9 @@ int bqe_dequant(int32_t fmt, int32_t rows, int32_t cols, const void* src, float*
 /* Workspace bytes one decode call with up to M rows needs. */
 uint64_t bqe_workspace_bytes(const bqe_layer_desc* d, int32_t M);
 
-/* Zero a workspace before its first use (its counters must start at 0; the
- * kernels leave them at 0 after every successful call). */
+/* Zero a workspace before its first use and after any call that reported an
+ * error (its counters must start at 0; the kernels leave them at 0 after
+ * every successful call). */
 int bqe_workspace_init(void* ws, uint64_t ws_bytes, void* stream);
 
 /* One MoE layer for M in 1..8 token rows (the token plus speculative draft
@@ -310,10 +314,11 @@ void bqe_set_fused(int32_t on);
  * 4e-4 for fp16).  Both run at the same tensor-core rate. */
 void bqe_set_prefill_f16(int32_t on);
 
-/* Diagnostic: at most n ring stages of shared-expert weights streamed by each
- * expert-kernel CTA before it waits for the previous kernel (default 16: as
- * many as the ring holds; 0: none).  Results do not change. */
-void bqe_set_preload(int32_t n);
+/* Diagnostic: at most n_a (W1/W3 kernel) and n_b (W2 kernel) ring stages of
+ * shared-expert weights streamed by each expert-kernel CTA before it waits
+ * for the previous kernel (default 16: as many as the ring holds; 0: none).
+ * Results do not change. */
+void bqe_set_preload(int32_t n_a, int32_t n_b);
 
 /* Diagnostic: at most max_a (W1/W3) and max_b (W2) 32-row panels per work
  * item of the decode expert kernels (0: the default choice, the largest that
