@@ -422,9 +422,8 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
 // of the 256 columns in [2^13, 2^14)) in the order of the expert's format,
 // with the sums of X_hi and X_lo over every 16 columns and 2^-si.
 // h of 256 columns of row r of expert u (one column per thread)
-__device__ __forceinline__ void finalize_a_block(const ExpParams& P, int u, int r, int blk) {
+__device__ __forceinline__ void finalize_a_block(const ExpParams& P, int u, int r, int blk, int fmt) {
   const Geo& g = P.g;
-  const int fmt = ((const int32_t*)(P.ws + P.L.u_fmt))[u];
   const float* pa = (const float*)(P.ws + P.L.pa);
   const int nch = g.nchA, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blk * 256 + tid;
@@ -493,13 +492,20 @@ __global__ void __maxnreg__(32) k_finalize_a(ExpParams P) {  // 32 registers: fi
   griddep_launch_dependents();
   griddep_wait();
   if (P.diag && threadIdx.x == 0) dbg_time(P.ws, P.L.dbg, 2, 4, false);
-  const int nU = *(volatile const int32_t*)(P.ws + P.L.nu);
   const int nbl = g.I / 256;
-  // work = (expert, row of the expert, 256 columns); prefix sums of the rows
-  // (the row counts loaded in parallel, then added up in shared memory)
+  // work = (expert, row of the expert, 256 columns).  The expert count, every
+  // entry's row count and format come in one round of loads (entries past the
+  // count are not used), then the row counts are added up in shared memory.
   __shared__ int s_pre[kMaxM * kMaxTopK + 2];
-  for (int u = threadIdx.x; u < nU; u += blockDim.x) s_pre[u + 1] = ((const int32_t*)(P.ws + P.L.u_nrows))[u];
+  __shared__ int s_fmt[kMaxM * kMaxTopK + 1];
+  __shared__ int s_nu;
+  if (threadIdx.x == 0) s_nu = *(volatile const int32_t*)(P.ws + P.L.nu);
+  for (int u = threadIdx.x; u < g.U; u += blockDim.x) {
+    s_pre[u + 1] = ((const int32_t*)(P.ws + P.L.u_nrows))[u];
+    s_fmt[u] = ((const int32_t*)(P.ws + P.L.u_fmt))[u];
+  }
   __syncthreads();
+  const int nU = s_nu;
   if (threadIdx.x == 0) {
     s_pre[0] = 0;
     for (int u = 0; u < nU; ++u) s_pre[u + 1] += s_pre[u];
@@ -511,7 +517,7 @@ __global__ void __maxnreg__(32) k_finalize_a(ExpParams P) {  // 32 registers: fi
     int u = 0;
     while (u + 1 < nU && s_pre[u + 1] <= rowg) ++u;
     const int r = rowg - s_pre[u];
-    finalize_a_block(P, u, r, blk);
+    finalize_a_block(P, u, r, blk, s_fmt[u]);
     __syncthreads();  // shared scratch of the block is reused
   }
   if (P.diag && threadIdx.x == 0) dbg_time(P.ws, P.L.dbg, 2, 5, true);

@@ -211,6 +211,22 @@ def test_deterministic(dev):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+def test_preload_does_not_change_results(dev):
+    """Streaming the shared expert's tiles before the routing wait is a
+    scheduling choice only: with and without it the outputs are identical."""
+    from bit_quantised_expert_gb300 import _abi as A
+    fm = [ALL[e % 4] for e in range(33)]
+    L = synth.small_layer(10, fm, 1024, 512, 32, 4, 3, bias_std=0.25)
+    DL = DeviceLayer(L, dev)
+    a = DL.forward(L["x"])
+    A.bqe_set_preload(0, 0)
+    try:
+        b = DL.forward(L["x"])
+    finally:
+        A.bqe_set_preload(16, 16)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
 # ------------------------------------------------------- error reporting
 def test_bad_slot_is_reported(dev):
     import torch
