@@ -36,7 +36,7 @@ if ROOT not in sys.path:
 # DRAM bytes read + written per layer call by k_experts<0> and k_finalize_a on the MXFP4 M=1 layer
 # (ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/k_experts_decode_fp4_m1_E64.md), or None
 # while either kernel has changed since that capture.
-DECODE_FP4_M1_TRAFFIC = (87.87 + 1.81 + 0.67) * 1e6
+DECODE_FP4_M1_TRAFFIC = (87.86 + 1.69 + 0.67) * 1e6
 
 METRIC = "MoE layer decode: expert-byte GB/s (% of HBM peak) and us/layer at M=1 and M=6"
 HBM_FALLBACK_GBS = 6800.0

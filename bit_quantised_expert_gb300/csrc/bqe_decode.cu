@@ -121,7 +121,8 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
   auto issue_weights = [&](int s, int u, int pg, int c, int fmt, uint64_t addr, int R, uint32_t tb, bool pre,
                            uint64_t pol) -> uint32_t {
     StageHdr& H = hdr[s];
-    H.addr = addr; H.u = u; H.p0 = pg * P_; H.c = c; H.fmt = fmt; H.R = R;
+    H.addr = addr; H.u = u; H.p0 = pg * P_; H.c = (int16_t)c; H.fmt = fmt; H.R = (int16_t)R;
+    H.tb = tb; H.nb = (uint16_t)(kc / fmt_bw(fmt)); H.amode = (uint8_t)act_mode(PHASE, fmt, P.variant);
     const uint32_t wbytes = (uint32_t)phase_mats(PHASE) * P_ * tb;
     uint8_t* dst = ring + (size_t)s * slot_bytes;
     if (pre) mbar_expect_tx(&full[s], wbytes);
@@ -326,13 +327,13 @@ __global__ void __launch_bounds__(32 * (kMaxWarps + 2), 1) k_experts(ExpParams P
         }
         break;
       }
+      // the item's sizes come with the header (computed once, by the producer)
       const StageHdr H = hdr[s];
-      const uint32_t tb = tile_bytes(H.fmt, kc);
       const uint8_t* slot = ring + (size_t)s * slot_bytes;
-      const uint8_t* tile = slot + (size_t)(mat * P_ + pan) * tb;
-      const uint8_t* act = slot + (size_t)phase_mats(PHASE) * P_ * tb;
+      const uint8_t* tile = slot + (size_t)(mat * P_ + pan) * H.tb;
+      const uint8_t* act = slot + (size_t)phase_mats(PHASE) * P_ * H.tb;
       float* rb = red + (size_t)b * red_stride;
-      consume_rows<RC>(H.R, H.fmt, tile, kc, grp, act, lane, rb + cw * g.M * 32, act_mode(PHASE, H.fmt, P.variant));
+      consume_rows<RC>(H.R, H.fmt, tile, kc, H.nb, grp, act, lane, rb + cw * g.M * 32, H.amode);
       if (cw == 0 && lane == 0) rmeta[b] = RedMeta{H.u, H.p0, H.c, H.R};
       ccomp += clk() - t2;
       __syncwarp();

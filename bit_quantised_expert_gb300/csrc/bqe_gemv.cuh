@@ -12,8 +12,14 @@
 namespace bqe {
 
 struct StageHdr {
-  uint64_t addr;  // slot base
-  int u, p0, c, fmt, R, pad;
+  uint64_t addr;   // slot base
+  int u, p0;       // expert (work-list index), first panel
+  int fmt;
+  uint32_t tb;     // bytes of one weight tile of the stage
+  int16_t c, R;    // K chunk, activation rows
+  uint16_t nb;     // format blocks per tile row (chunk columns / block width)
+  uint8_t amode;   // staging mode of the activation rows
+  uint8_t pad;     // free here (the single-kernel layer marks W2 items with it)
 };
 
 __host__ __device__ inline int phase_mats(int phase) { return phase == 0 ? 2 : 1; }
@@ -534,13 +540,14 @@ __host__ __device__ inline int act_row_bytes(int amode, int fmt, int kc) {
   return amode == kActF32 ? kc * 4 : amode == kActF16 ? kc * 2 : (int)int_rec_bytes(fmt == BQE_FMT_TQ1, kc);
 }
 
+// nb: format blocks per tile row (kc / block width), from the stage header
 template <int R>
-__device__ __forceinline__ void consume_group_R(int fmt, const uint8_t* tile, int kc, int grp, const uint8_t* act,
-                                                int lane, float* outv /* [r * 32 + lane] */, int amode) {
+__device__ __forceinline__ void consume_group_R(int fmt, const uint8_t* tile, int kc, int nb, int grp,
+                                                const uint8_t* act, int lane, float* outv /* [r * 32 + lane] */,
+                                                int amode) {
   float2 acc[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) acc[r] = f2(0.f, 0.f);
-  const int nb = kc / fmt_bw(fmt);
   if (amode == kActInt) {
     const int rowb = act_row_bytes(kActInt, fmt, kc);
     switch (fmt) {
@@ -567,16 +574,16 @@ __device__ __forceinline__ void consume_group_R(int fmt, const uint8_t* tile, in
 }
 
 template <int RC>
-__device__ __forceinline__ void consume_group(int R, int fmt, const uint8_t* tile, int kc, int grp,
+__device__ __forceinline__ void consume_group(int R, int fmt, const uint8_t* tile, int kc, int nb, int grp,
                                               const uint8_t* act, int lane, float* outv, int amode) {
   if (RC == 1 || R == 1) {
-    consume_group_R<1>(fmt, tile, kc, grp, act, lane, outv, amode);
+    consume_group_R<1>(fmt, tile, kc, nb, grp, act, lane, outv, amode);
     return;
   }
   switch (R) {
-    case 2: consume_group_R<2>(fmt, tile, kc, grp, act, lane, outv, amode); break;
-    case 3: consume_group_R<3>(fmt, tile, kc, grp, act, lane, outv, amode); break;
-    case 4: consume_group_R<4>(fmt, tile, kc, grp, act, lane, outv, amode); break;
+    case 2: consume_group_R<2>(fmt, tile, kc, nb, grp, act, lane, outv, amode); break;
+    case 3: consume_group_R<3>(fmt, tile, kc, nb, grp, act, lane, outv, amode); break;
+    case 4: consume_group_R<4>(fmt, tile, kc, nb, grp, act, lane, outv, amode); break;
   }
 }
 
@@ -585,13 +592,13 @@ __device__ __forceinline__ void consume_group(int R, int fmt, const uint8_t* til
 // one-row calls (RC = 1) carries only the one-row inner loops, which keeps its
 // code small and its register count low.
 template <int RC>
-__device__ __forceinline__ void consume_rows(int R, int fmt, const uint8_t* tile, int kc, int grp, const uint8_t* act,
-                                             int lane, float* outv, int amode) {
+__device__ __forceinline__ void consume_rows(int R, int fmt, const uint8_t* tile, int kc, int nb, int grp,
+                                             const uint8_t* act, int lane, float* outv, int amode) {
   static_assert(RC == 1 || RC == kRowChunk, "row chunk");
   const size_t row_bytes = (size_t)act_row_bytes(amode, fmt, kc);
   for (int r0 = 0; r0 < R; r0 += RC) {
     const int n = R - r0 < RC ? R - r0 : RC;
-    consume_group<RC>(n, fmt, tile, kc, grp, act + r0 * row_bytes, lane, outv + r0 * 32, amode);
+    consume_group<RC>(n, fmt, tile, kc, nb, grp, act + r0 * row_bytes, lane, outv + r0 * 32, amode);
   }
 }
 

@@ -610,7 +610,8 @@ __global__ void __launch_bounds__(32 * (1 + kMaxWarps + kMaxEpi), 1) k_layer(Lay
           const uint8_t* tile = slot + (size_t)(mat * Pp + pan) * tb;
           const uint8_t* act = slot + (size_t)(isA ? 2 : 1) * Pp * tb;
           const bool half_act = isA && Hd.fmt == BQE_FMT_MXFP4 && P.variant == 1;
-          consume_rows<kRowChunk>(Hd.R, Hd.fmt, tile, kc, grp, act, lane, rb + cw * M * 32, half_act ? kActF16 : kActF32);
+          consume_rows<kRowChunk>(Hd.R, Hd.fmt, tile, kc, kc / fmt_bw(Hd.fmt), grp, act, lane, rb + cw * M * 32,
+                                  half_act ? kActF16 : kActF32);
         }
         if (cw == 0 && lane == 0) rmeta[b] = FRedMeta{t, Hd.u, Hd.p0, Hd.c, Hd.R, isA ? 0 : 1};
         __syncwarp();
