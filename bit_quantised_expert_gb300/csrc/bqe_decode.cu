@@ -35,7 +35,7 @@ namespace bqe {
 
 
 __device__ __forceinline__ long long clk() { return clock64(); }
-constexpr int kFinBThreads = 128;  // k_finalize_b CTA size: small enough to sit beside a W2 CTA
+constexpr int kFinBThreads = 128;  // k_finalize_b CTA size (at most one CTA per SM)
 // diagnostic counters: 0 producer waiting for a free stage, 1 producer issuing,
 // 2 consumer (warp 1) waiting for a stage, 3 consumer waiting for a reduction
 // buffer, 4 consumer computing, 5 epilogue waiting, 6 epilogue working,
