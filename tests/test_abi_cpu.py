@@ -127,3 +127,38 @@ def test_status_strings(A):
     for s in range(7):
         assert A.status_name(s)
     assert "unknown" in A.status_name(99)
+
+
+def test_argument_checks_before_any_device_work(A):
+    """The entry points reject bad arguments synchronously, before touching a
+    pointer or the device (fake, aligned addresses; nothing is dereferenced)."""
+    import ctypes
+    lib = A.lib
+    d = A.desc(5120, 2304, 384, 6)
+    fake = ctypes.c_void_p(1 << 20)  # 256-byte aligned, never dereferenced
+    pool = A.bqe_pool(base=1 << 20, base_bytes=1 << 30, slot_off=1 << 21, slot_fmt=1 << 22, n_slots=385)
+    bad_pool = A.bqe_pool(base=None, base_bytes=0, slot_off=None, slot_fmt=None, n_slots=0)
+    need = A.bqe_workspace_bytes(d, 1)
+    args = lambda M, x, ws, nb, p=pool: (ctypes.byref(d), M, x, fake, None, ctypes.byref(p), fake, None, fake, 0,  # noqa: E731
+                                         None, None, ws, nb, None)
+    assert lib.bqe_moe_layer_forward(*args(0, fake, fake, need)) == A.BQE_EINVAL      # no rows
+    assert lib.bqe_moe_layer_forward(*args(9, fake, fake, need)) == A.BQE_EINVAL      # more than 8 rows
+    assert lib.bqe_moe_layer_forward(*args(1, None, fake, need)) == A.BQE_EINVAL      # no input
+    assert lib.bqe_moe_layer_forward(*args(1, fake, None, need)) == A.BQE_EINVAL      # no workspace
+    assert lib.bqe_moe_layer_forward(*args(1, fake, ctypes.c_void_p((1 << 20) + 16), need)) == A.BQE_EINVAL  # misaligned
+    assert lib.bqe_moe_layer_forward(*args(1, fake, fake, need, bad_pool)) == A.BQE_EINVAL  # empty pool
+    assert lib.bqe_moe_layer_forward(*args(1, fake, fake, need - 256)) == A.BQE_ENOSPC     # workspace too small
+    for bad in (A.desc(5120, 2304, 384, 6, n_shared=2), A.desc(5120, 2304, 384, 0), A.desc(5000, 2304, 384, 6),
+                A.desc(5120, 2304, 513, 6), A.desc(5120, 2304, 384, 17)):
+        assert A.bqe_workspace_bytes(bad, 1) == 0
+        assert lib.bqe_moe_layer_forward(ctypes.byref(bad), 1, fake, fake, None, ctypes.byref(pool), fake, None,
+                                         fake, 0, None, None, fake, need, None) == A.BQE_EINVAL
+    # prefill: token count bounds and the workspace size
+    assert A.bqe_prefill_workspace_bytes(d, 0) == 0
+    pneed = A.bqe_prefill_workspace_bytes(d, 64)
+    assert pneed > 0 and A.bqe_prefill_workspace_bytes(d, 128) > pneed
+    assert lib.bqe_moe_prefill(ctypes.byref(d), 0, fake, fake, None, ctypes.byref(pool), fake, None, fake, 0, None,
+                               None, fake, pneed, None) == A.BQE_EINVAL
+    assert lib.bqe_moe_prefill(ctypes.byref(d), 64, fake, fake, None, ctypes.byref(pool), fake, None, fake, 0, None,
+                               None, fake, pneed - 256, None) == A.BQE_ENOSPC
+    assert lib.bqe_workspace_init(None, 16, None) == A.BQE_EINVAL
