@@ -446,8 +446,8 @@ def run_layer(args, rank, world):
     if clk:
         res["clocks"] = clk
 
-    if args.diag:
-        # timeline of the fused kernel (globaltimer stamps per CTA)
+    if args.diag and args.fused:
+        # timeline of the single-kernel layer (globaltimer stamps per CTA)
         A.bqe_set_diag(True)
         off = A.bqe_diag_offset(d, M)
         tl = []
