@@ -297,8 +297,13 @@ void bqe_set_variant(int32_t v);
  * [3][1024 CTAs][8 counters], zeroed by bqe_workspace_init.  Blocks 0 and 1
  * (W1/W3 and W2 kernels): producer waiting / issuing, consumer waiting for a
  * stage / for a reduction buffer / computing, epilogue waiting / working,
- * whole CTA.  Block 2 (router): counter 0 = CTA start to its logits written,
- * counter 1 = start to end of the CTA that selects the experts. */
+ * whole CTA.  Block 2 (router): counter 0 = CTA start to its logits written;
+ * row 1022 counter 1 = start to end of the CTA that selects the experts, row
+ * 1021 = its stage stamps.  Row 1023 of every block holds globaltimer
+ * stamps (the caller presets minima to a large value and maxima to 0):
+ * [0] first CTA start (minimum), [1] last CTA end (maximum); blocks 0 and 1:
+ * [2] / [3] first / last CTA past its wait; block 2: [4] / [5] k_finalize_a
+ * past its wait / last CTA end, [6] / [7] the same for k_finalize_b. */
 void bqe_set_diag(int32_t on);
 
 /* bqe_moe_layer_forward and bqe_moe_step run the layer as the router kernel
