@@ -447,3 +447,188 @@ def test_planted_bias_in_weights_is_caught():
     r = O.route(x, wr, b, 2)
     key = r["key"][0, r["idx"][0]]
     assert not np.allclose(r["w"][0], key / key.sum())
+
+
+# ------------------------------------------- layer combine and chain, brute force
+#
+# These pins restate the layer with plain Python loops over scalars (no call
+# into oracle.moe): the weighted combine with k >= 2 and a non-zero bias, the
+# RMS normalisation on a vector whose mean |r| differs from its RMS, and a
+# two-layer residual chain.  bf16 rounding here goes through torch's own
+# conversion (binary64 -> binary32 -> bfloat16, round to nearest even), not
+# the oracle's integer rounding.  The planted-mistake tests below run
+# mutated oracle functions (monkeypatched into oracle.moe) through these same
+# pins and require each one to fail.
+
+import struct
+
+import torch
+
+
+def _bf16_to_float(b):
+    return struct.unpack("<f", struct.pack("<I", int(b) << 16))[0]
+
+
+def _float_to_bf16_bits(v):
+    t = torch.tensor([float(np.float32(v))], dtype=torch.float32).to(torch.bfloat16)
+    return int(t.view(torch.int16).item()) & 0xFFFF
+
+
+def _brute_layer(x_bits, router, bias, experts, fmts, H, I, k, shared):
+    """out[m] = y_shared(x_m) + sum_j s_j / (sum s) y_j(x_m), scalar loops."""
+    E = router.shape[0]
+    dense = {}
+
+    def weights(e):
+        if e not in dense:
+            dense[e] = [m.tolist() for m in F.dequant_expert(int(fmts[e]), experts[e], H, I)]
+        return dense[e]
+
+    def ffn(e, xv):
+        w1, w3, w2 = weights(e)
+        h = []
+        for i in range(I):
+            g = 0.0
+            u = 0.0
+            for j in range(H):
+                g += w1[i][j] * xv[j]
+                u += w3[i][j] * xv[j]
+            h.append(g / (1.0 + math.exp(-g)) * u)
+        return [sum(w2[n][i] * h[i] for i in range(I)) for n in range(H)]
+
+    outs = []
+    for row in x_bits:
+        xv = [_bf16_to_float(b) for b in row]
+        s = []
+        for e in range(E):
+            z = 0.0
+            for j in range(H):
+                z += float(router[e][j]) * xv[j]
+            s.append(1.0 / (1.0 + math.exp(-z)))
+        key = [s[e] + float(bias[e]) for e in range(E)]
+        chosen = sorted(range(E), key=lambda e: (-key[e], e))[:k]
+        tot = sum(s[e] for e in chosen)
+        out = ffn(shared, xv)
+        for e in chosen:
+            y = ffn(e, xv)
+            for n in range(H):
+                out[n] += s[e] / tot * y[n]
+        outs.append(out)
+    return np.array(outs)
+
+
+def _combine_case(k):
+    # 5 routed experts + shared, H = I = 64 (Q2_0 and MXFP4 blocks divide 64)
+    fmts = [synth.Q2_0, synth.MXFP4, synth.Q2_0, synth.MXFP4, synth.Q2_0, synth.MXFP4]
+    return synth.small_layer(20 + k, fmts, 64, 64, 5, k, 2, bias_std=0.25)
+
+
+def pin_combine(k):
+    L = _combine_case(k)
+    got = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 64, 64, k, 5)["out"]
+    want = _brute_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 64, 64, k, 5)
+    assert np.allclose(got, want, rtol=1e-11, atol=1e-12), np.abs(got - want).max()
+
+
+def pin_rmsnorm_nonconstant():
+    # r = (3, 4, 0, 0): mean r^2 = 6.25, rms = sqrt(6.25 + 1e-6); mean |r| = 1.75
+    r = np.array([[3.0, 4.0, 0.0, 0.0], [-6.0, 0.0, 8.0, 0.0]])
+    t = O.rmsnorm_to_bf16(r)
+    rms = [math.sqrt(6.25 + 1e-6), math.sqrt(25.0 + 1e-6)]
+    for m in range(2):
+        for j in range(4):
+            assert t[m, j] == _float_to_bf16_bits(r[m, j] / rms[m]), (m, j, t[m, j])
+    # closed form of the first row: 3 / 2.5 -> bf16 1.203125, 4 / 2.5 -> bf16 1.6015625
+    assert _bf16_to_float(t[0, 0]) == 1.203125 and _bf16_to_float(t[0, 1]) == 1.6015625
+
+
+def pin_chain():
+    H = I = 64
+    fmts = [synth.MXFP4, synth.Q2_0, synth.MXFP4, synth.Q2_0, synth.Q2_0]
+    layers = []
+    for l in range(2):
+        L = synth.small_layer(40 + l, fmts, H, I, 4, 2, 2, bias_std=0.25)
+        layers.append(dict(router=L["router"], bias=L["bias"], experts=L["experts"], fmts=L["fmts"],
+                           shared=4))
+    x_bits = synth.small_layer(50, fmts, H, I, 4, 2, 2)["x"]
+    got = O.moe_chain(x_bits, layers, H, I, 2)
+    r = [[_bf16_to_float(b) for b in row] for row in x_bits]
+    for l, L in enumerate(layers):
+        t = []
+        for row in r:
+            rms = math.sqrt(sum(v * v for v in row) / H + 1e-6)
+            t.append([_float_to_bf16_bits(v / rms) for v in row])
+        t = np.array(t, dtype=np.uint16)
+        assert np.array_equal(t, got["ts"][l]), l
+        out = _brute_layer(t, L["router"], L["bias"], L["experts"], L["fmts"], H, I, 2, 4)
+        assert np.allclose(out, got["outs"][l], rtol=1e-11, atol=1e-12), l
+        r = [[r[m][n] + out[m][n] for n in range(H)] for m in range(len(r))]
+    assert np.allclose(np.array(r), got["resid"], rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("k", [2, 3])
+def test_weighted_combine_brute_force(k):
+    pin_combine(k)
+
+
+def test_rmsnorm_nonconstant_closed_form():
+    pin_rmsnorm_nonconstant()
+
+
+def test_two_layer_chain_brute_force():
+    pin_chain()
+
+
+# planted mistakes, each run through the oracle and caught by a named pin
+
+def _route_with(w_of):
+    real = O.route
+
+    def mutated(x, router_w, sel_bias, top_k, forced_idx=None):
+        r = real(x, router_w, sel_bias, top_k, forced_idx)
+        r["w"] = w_of(r)
+        return r
+    return mutated
+
+
+def test_planted_dropped_mixing_weight_fails_combine_pin(monkeypatch):
+    monkeypatch.setattr(O, "route", _route_with(lambda r: np.ones_like(r["w"])))
+    with pytest.raises(AssertionError):
+        pin_combine(2)
+
+
+def test_planted_biased_key_weights_fail_combine_pin(monkeypatch):
+    def biased(r):
+        kk = np.take_along_axis(r["key"], r["idx"], axis=1)
+        return kk / kk.sum(axis=1, keepdims=True)
+    monkeypatch.setattr(O, "route", _route_with(biased))
+    with pytest.raises(AssertionError):
+        pin_combine(3)
+
+
+def test_planted_mean_abs_norm_fails_norm_and_chain_pins(monkeypatch):
+    def mean_abs(resid):
+        rr = np.asarray(resid, dtype=np.float64)
+        return O.round_to_bf16(rr / (np.mean(np.abs(rr), axis=-1, keepdims=True) + O.RMS_EPS))
+    monkeypatch.setattr(O, "rmsnorm_to_bf16", mean_abs)
+    with pytest.raises(AssertionError):
+        pin_rmsnorm_nonconstant()
+    with pytest.raises(AssertionError):
+        pin_chain()
+
+
+def test_planted_transposed_w2_fails_combine_pin(monkeypatch):
+    def transposed(x, w1, w3, w2):
+        g = x @ w1.T
+        u = x @ w3.T
+        h = O.silu(g) * u
+        return h @ w2, h  # W2 applied transposed (square at H = I)
+    monkeypatch.setattr(O, "expert_ffn", transposed)
+    with pytest.raises(AssertionError):
+        pin_combine(2)
+
+
+def test_planted_silu_sign_fails_combine_pin(monkeypatch):
+    monkeypatch.setattr(O, "silu", lambda t: t / (1.0 + np.exp(t)))
+    with pytest.raises(AssertionError):
+        pin_combine(2)
