@@ -33,6 +33,11 @@ class bqe_pool(ctypes.Structure):
                 ("slot_fmt", ctypes.c_void_p), ("n_slots", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
+class bqe_stats(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int32), ("experts_streamed", ctypes.c_int32), ("per_format", ctypes.c_int32 * 5),
+                ("row_uses", ctypes.c_int32), ("expert_bytes", ctypes.c_uint64), ("router_bytes", ctypes.c_uint64)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError("libbqe.so is not built (%s); run bit_quantised_expert_gb300.buildlib.build() "
@@ -57,6 +62,11 @@ SIGNATURES = {
     "bqe_scale_bytes": (_I32, [_I32]),
     "bqe_pack": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P]),
     "bqe_pool_pack_slot": (ctypes.c_int, [_DESC, _I32, _P, _P, _P]),
+    "bqe_pool_bytes": (_U64, [_DESC, _I32, _P]),
+    "bqe_pool_init": (ctypes.c_int, [_POOL, _DESC, _I32, _P, _P, _U64, _P]),
+    "bqe_pool_upload": (ctypes.c_int, [_POOL, _DESC, _I32, _P, _P]),
+    "bqe_unpack_host": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P]),
+    "bqe_layer_stats": (ctypes.c_int, [_DESC, _I32, _P, _P, ctypes.POINTER(bqe_stats)]),
     "bqe_dequant": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _P]),
     "bqe_workspace_bytes": (_U64, [_DESC, _I32]),
     "bqe_workspace_init": (ctypes.c_int, [_P, _U64, _P]),
@@ -157,6 +167,38 @@ def bqe_pack(fmt: int, rows: int, cols: int, codes, scales, out) -> None:
 def bqe_pool_pack_slot(d, fmt, canon_src, slot_dst, stream=None) -> None:
     _ok(lib.bqe_pool_pack_slot(ctypes.byref(d), fmt, ptr(canon_src), ptr(slot_dst), stream_ptr(stream)),
         "bqe_pool_pack_slot")
+
+
+def bqe_pool_bytes(d, slot_fmts) -> int:
+    import numpy as np
+    f = np.ascontiguousarray(slot_fmts, dtype=np.int32)
+    return lib.bqe_pool_bytes(ctypes.byref(d), int(f.size), f.ctypes.data)
+
+
+def bqe_pool_init(d, slot_fmts, dev_mem, dev_bytes, stream=None) -> bqe_pool:
+    import numpy as np
+    f = np.ascontiguousarray(slot_fmts, dtype=np.int32)
+    p = bqe_pool()
+    _ok(lib.bqe_pool_init(ctypes.byref(p), ctypes.byref(d), int(f.size), f.ctypes.data, ptr(dev_mem), int(dev_bytes),
+                          stream_ptr(stream)), "bqe_pool_init")
+    return p
+
+
+def bqe_pool_upload(pool: bqe_pool, d, slot: int, canon_dev, stream=None) -> None:
+    _ok(lib.bqe_pool_upload(ctypes.byref(pool), ctypes.byref(d), int(slot), ptr(canon_dev), stream_ptr(stream)),
+        "bqe_pool_upload")
+
+
+def bqe_unpack_host(fmt: int, rows: int, cols: int, packed, codes, scales) -> None:
+    """Host unpacking (inverse of bqe_pack): C-contiguous uint8 numpy arrays."""
+    _ok(lib.bqe_unpack_host(fmt, rows, cols, ptr(packed), ptr(codes), ptr(scales)), "bqe_unpack_host")
+
+
+def bqe_layer_stats(d, M: int, ws, stream=None) -> dict:
+    st = bqe_stats()
+    _ok(lib.bqe_layer_stats(ctypes.byref(d), M, ptr(ws), stream_ptr(stream), ctypes.byref(st)), "bqe_layer_stats")
+    return dict(rows=st.rows, experts_streamed=st.experts_streamed, per_format=list(st.per_format),
+                row_uses=st.row_uses, expert_bytes=st.expert_bytes, router_bytes=st.router_bytes)
 
 
 def bqe_dequant(fmt, rows, cols, src, out, stream=None) -> None:

@@ -15,7 +15,7 @@ static std::atomic<int> g_use_pdl{1};
 static std::atomic<int> g_drop_item{-1};
 static std::atomic<int> g_variant{1};
 static std::atomic<int> g_diag{0};
-static std::atomic<int> g_fused{0};
+static std::atomic<int> g_fused{1};
 static std::atomic<int> g_pf_f16{1};
 static std::atomic<int> g_pmax_a{0}, g_pmax_b{0};
 static std::atomic<int> g_preload_a{16}, g_preload_b{16};
@@ -214,19 +214,85 @@ static int layer_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, c
   return launch_layer(P, sms, st);
 }
 
+// The decode layer as one persistent kernel (bqe_moe.cu).
+static int moe_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* resid, uint16_t* t_out,
+                      const float* router_w, const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
+                      const int32_t* forced_idx, float* out, int32_t accumulate, int32_t* topk_idx, float* topk_w,
+                      void* ws, uint64_t ws_bytes, cudaStream_t st) {
+  if (!desc_ok(d) || M < 1 || M > kMaxM || (!x && !resid) || !router_w || !slot_table || !ws || !out) return BQE_EINVAL;
+  if (((uintptr_t)ws & 255) || ((uintptr_t)router_w & 15) || d->hidden % 512) return BQE_EINVAL;
+  if (x && ((uintptr_t)x & 15)) return BQE_EINVAL;
+  int rc = check_pool(pool);
+  if (rc) return rc;
+  Geo g = geo_of(d, M);
+  WsLayout L = make_ws(g);
+  if (ws_bytes < L.total) return BQE_ENOSPC;
+  const int sms = device_sms();
+  if (sms <= 0) return BQE_ECUDA;
+  MoeParams P = {};
+  P.g = g;
+  P.L = L;
+  P.ws = (uint8_t*)ws;
+  P.x = x;
+  P.resid = resid;
+  P.t_out = t_out;
+  P.router_w = router_w;
+  P.bias = sel_bias;
+  P.forced = forced_idx;
+  P.slot_table = slot_table;
+  P.pool = *pool;
+  P.out = out;
+  P.accumulate = accumulate ? 1 : 0;
+  P.topk_idx = topk_idx;
+  P.topk_w = topk_w;
+  P.drop_item = g_drop_item.load();
+  P.variant = g_variant.load();
+  P.diag = g_diag.load();
+  P.limit_ns = g_wait_limit_ns.load();
+  return launch_moe(P, sms, st);
+}
+
 extern "C" int bqe_moe_layer_forward(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w,
                                      const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
                                      const int32_t* forced_idx, float* out, int32_t accumulate, int32_t* topk_idx,
                                      float* topk_w, void* ws, uint64_t ws_bytes, void* stream) {
   if (g_fused.load()) {
     if (!x) return BQE_EINVAL;
-    return layer_common(d, M, x, nullptr, nullptr, router_w, sel_bias, pool, slot_table, forced_idx, out, accumulate,
-                        topk_idx, topk_w, ws, ws_bytes, (cudaStream_t)stream);
+    return moe_common(d, M, x, nullptr, nullptr, router_w, sel_bias, pool, slot_table, forced_idx, out, accumulate,
+                      topk_idx, topk_w, ws, ws_bytes, (cudaStream_t)stream);
   }
   int rc = bqe_route(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, topk_idx, topk_w, ws, ws_bytes,
                      stream);
   if (rc) return rc;
   return experts_common(d, M, pool, out, accumulate, ws, ws_bytes, (cudaStream_t)stream, -1, slot_table);
+}
+
+extern "C" int bqe_layer_stats(const bqe_layer_desc* d, int32_t M, const void* ws, void* stream, bqe_stats* out) {
+  if (!desc_ok(d) || M < 1 || M > kMaxM || !ws || !out) return BQE_EINVAL;
+  const Geo g = geo_of(d, M);
+  const WsLayout L = make_ws(g);
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t nu = 0;
+  const uint8_t* w = (const uint8_t*)ws;
+  if (cudaStreamSynchronize(st) != cudaSuccess || cudaMemcpy(&nu, w + L.nu, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BQE_ECUDA;
+  if (nu < 0 || nu > g.U) return BQE_EDEVICE;
+  int32_t fmt[kMaxM * kMaxTopK + 1] = {}, rows[kMaxM * kMaxTopK + 1] = {};
+  if (nu > 0 && (cudaMemcpy(fmt, w + L.u_fmt, 4ull * nu, cudaMemcpyDeviceToHost) != cudaSuccess ||
+                 cudaMemcpy(rows, w + L.u_nrows, 4ull * nu, cudaMemcpyDeviceToHost) != cudaSuccess))
+    return BQE_ECUDA;
+  bqe_stats s = {};
+  s.rows = M;
+  s.experts_streamed = nu;
+  for (int u = 0; u < nu; ++u) {
+    if (!fmt_ok(fmt[u])) return BQE_EDEVICE;
+    s.per_format[fmt[u]] += 1;
+    s.expert_bytes += 2 * matrix_bytes(fmt[u], d->inter, d->hidden) + matrix_bytes(fmt[u], d->hidden, d->inter);
+    s.row_uses += rows[u];
+  }
+  s.router_bytes = 4ull * d->n_experts * d->hidden;
+  *out = s;
+  return BQE_OK;
 }
 
 extern "C" int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M, float* resid,
@@ -242,8 +308,8 @@ extern "C" int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M
     const int32_t* fl = forced_idx ? forced_idx + (int64_t)l * M * K : nullptr;
     int rc;
     if (g_fused.load()) {
-      rc = layer_common(d, M, nullptr, resid, tl, router_w + l * E * H, bl, pool, slot_tables + l * (E + 1), fl, resid, 1,
-                        nullptr, nullptr, ws, ws_bytes, st);
+      rc = moe_common(d, M, nullptr, resid, tl, router_w + l * E * H, bl, pool, slot_tables + l * (E + 1), fl, resid, 1,
+                      nullptr, nullptr, ws, ws_bytes, st);
     } else {
       rc = route_common(d, M, nullptr, resid, tl, router_w + l * E * H, bl, pool, slot_tables + l * (E + 1), fl, nullptr,
                         nullptr, ws, ws_bytes, st);

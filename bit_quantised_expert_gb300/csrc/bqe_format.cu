@@ -17,6 +17,7 @@
 #include <cuda_fp16.h>
 
 #include <cstring>
+#include <vector>
 
 #include "bqe_internal.cuh"
 
@@ -154,6 +155,132 @@ extern "C" int bqe_pool_pack_slot(const bqe_layer_desc* d, int32_t fmt, const vo
   if ((rc = launch_pack(fmt, d->inter, d->hidden, s, o, st))) return rc;
   if ((rc = launch_pack(fmt, d->inter, d->hidden, s + m13, o + m13, st))) return rc;
   return launch_pack(fmt, d->hidden, d->inter, s + 2 * m13, o + 2 * m13, st);
+}
+
+// ----------------------------------------------------------------------------
+// slot pool: [slot offsets (uint64) | slot formats (int32) | slots], every
+// part 256-byte aligned, in one caller-owned device buffer
+// ----------------------------------------------------------------------------
+static uint64_t pool_tables_bytes(int32_t n) {
+  return al256(8ull * (uint64_t)n) + al256(4ull * (uint64_t)n);
+}
+
+// Slot offsets (relative to the first slot) for the formats; false on a bad format.
+static bool pool_offsets(const bqe_layer_desc* d, int32_t n, const int32_t* fmt, std::vector<uint64_t>& off,
+                         uint64_t& slots_bytes) {
+  off.resize(n);
+  uint64_t o = 0;
+  for (int32_t s = 0; s < n; ++s) {
+    if (!fmt_ok(fmt[s])) return false;
+    off[s] = o;
+    o = al256(o + 2 * matrix_bytes(fmt[s], d->inter, d->hidden) + matrix_bytes(fmt[s], d->hidden, d->inter));
+  }
+  slots_bytes = o;
+  return true;
+}
+
+extern "C" uint64_t bqe_pool_bytes(const bqe_layer_desc* d, int32_t n_slots, const int32_t* slot_fmt) {
+  if (!shape_ok(d) || n_slots <= 0 || !slot_fmt) return 0;
+  std::vector<uint64_t> off;
+  uint64_t sb = 0;
+  if (!pool_offsets(d, n_slots, slot_fmt, off, sb)) return 0;
+  return pool_tables_bytes(n_slots) + sb;
+}
+
+extern "C" int bqe_pool_init(bqe_pool* p, const bqe_layer_desc* d, int32_t n_slots, const int32_t* slot_fmt,
+                             void* dev_mem, uint64_t dev_bytes, void* stream) {
+  if (!p || !shape_ok(d) || n_slots <= 0 || !slot_fmt || !dev_mem || ((uintptr_t)dev_mem & 255)) return BQE_EINVAL;
+  std::vector<uint64_t> off;
+  uint64_t sb = 0;
+  if (!pool_offsets(d, n_slots, slot_fmt, off, sb)) return BQE_EINVAL;
+  const uint64_t tb = pool_tables_bytes(n_slots);
+  if (dev_bytes < tb + sb) return BQE_ENOSPC;
+  uint8_t* mem = (uint8_t*)dev_mem;
+  cudaStream_t st = (cudaStream_t)stream;
+  // from pageable host memory: the call returns once the host arrays are staged
+  if (cudaMemcpyAsync(mem, off.data(), 8ull * n_slots, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(mem + al256(8ull * n_slots), slot_fmt, 4ull * n_slots, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess)
+    return BQE_ECUDA;
+  p->base = mem + tb;
+  p->base_bytes = sb;
+  p->slot_off = (const uint64_t*)mem;
+  p->slot_fmt = (const int32_t*)(mem + al256(8ull * n_slots));
+  p->n_slots = n_slots;
+  p->reserved = 0;
+  return BQE_OK;
+}
+
+extern "C" int bqe_pool_upload(const bqe_pool* p, const bqe_layer_desc* d, int32_t slot, const void* canon_dev,
+                               void* stream) {
+  if (!p || !p->base || !p->slot_off || !p->slot_fmt || !shape_ok(d) || slot < 0 || slot >= p->n_slots ||
+      !canon_dev)
+    return BQE_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint64_t off = 0;
+  int32_t fmt = 0;
+  // the slot's place and format, from the pool's own tables (ordered after bqe_pool_init on the stream)
+  if (cudaMemcpyAsync(&off, p->slot_off + slot, 8, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(&fmt, p->slot_fmt + slot, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return BQE_ECUDA;
+  if (!fmt_ok(fmt) || (off & 15) ||
+      off + 2 * matrix_bytes(fmt, d->inter, d->hidden) + matrix_bytes(fmt, d->hidden, d->inter) > p->base_bytes)
+    return BQE_EINVAL;
+  return bqe_pool_pack_slot(d, fmt, canon_dev, (uint8_t*)p->base + off, stream);
+}
+
+extern "C" int bqe_unpack_host(int32_t fmt, int32_t rows, int32_t cols, const uint8_t* packed, uint8_t* codes,
+                               uint8_t* scales) {
+  if (!fmt_ok(fmt) || rows <= 0 || cols <= 0 || cols % fmt_bw(fmt) != 0 || !packed || !codes || !scales)
+    return BQE_EINVAL;
+  const int bw = fmt_bw(fmt), bb = fmt_bb(fmt), sb = bqe_scale_bytes(fmt);
+  const int64_t nblocks = (int64_t)rows * (cols / bw);
+  for (int64_t blk = 0; blk < nblocks; ++blk) {
+    const uint8_t* b = packed + blk * bb;
+    uint8_t* c = codes + blk * bw;
+    uint8_t* s = scales + blk * sb;
+    switch (fmt) {
+      case BQE_FMT_MXFP4:
+        for (int j = 0; j < 32; ++j) c[j] = (uint8_t)((b[j >> 1] >> ((j & 1) * 4)) & 15);
+        s[0] = b[16];
+        break;
+      case BQE_FMT_Q2_0:
+        for (int j = 0; j < 64; ++j) c[j] = (uint8_t)((b[j >> 2] >> (2 * (j & 3))) & 3);
+        s[0] = b[16];
+        s[1] = b[17];
+        break;
+      case BQE_FMT_TQ1:
+        for (int i = 0; i < 51; ++i) {
+          if (b[i] > 242) return BQE_EINVAL;
+          int v = b[i];
+          for (int r = 0; r < 5; ++r) {
+            c[5 * i + r] = (uint8_t)(v % 3);
+            v /= 3;
+          }
+        }
+        if (b[51] > 2) return BQE_EINVAL;
+        c[255] = b[51];
+        s[0] = b[52];
+        s[1] = b[53];
+        break;
+      case BQE_FMT_Q3_K:
+        for (int j = 0; j < 256; ++j)
+          c[j] = (uint8_t)(((b[j >> 2] >> (2 * (j & 3))) & 3) | (((b[64 + (j >> 3)] >> (j & 7)) & 1) << 2));
+        for (int j = 0; j < 16; ++j) {
+          int v = 0;
+          for (int bit = 0; bit < 6; ++bit) {
+            const int pos = 6 * j + bit;
+            v |= ((b[96 + (pos >> 3)] >> (pos & 7)) & 1) << bit;
+          }
+          s[j] = (uint8_t)v;
+        }
+        s[16] = b[108];
+        s[17] = b[109];
+        break;
+    }
+  }
+  return BQE_OK;
 }
 
 // ----------------------------------------------------------------------------

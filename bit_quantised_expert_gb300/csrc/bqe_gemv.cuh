@@ -580,10 +580,14 @@ __device__ __forceinline__ void consume_group(int R, int fmt, const uint8_t* til
     consume_group_R<1>(fmt, tile, kc, nb, grp, act, lane, outv, amode);
     return;
   }
+  if (RC == 2) {
+    consume_group_R<(RC >= 2 ? 2 : 1)>(fmt, tile, kc, nb, grp, act, lane, outv, amode);
+    return;
+  }
   switch (R) {
     case 2: consume_group_R<2>(fmt, tile, kc, nb, grp, act, lane, outv, amode); break;
-    case 3: consume_group_R<3>(fmt, tile, kc, nb, grp, act, lane, outv, amode); break;
-    case 4: consume_group_R<4>(fmt, tile, kc, nb, grp, act, lane, outv, amode); break;
+    case 3: consume_group_R<(RC >= 3 ? 3 : 1)>(fmt, tile, kc, nb, grp, act, lane, outv, amode); break;
+    case 4: consume_group_R<(RC >= 4 ? 4 : 1)>(fmt, tile, kc, nb, grp, act, lane, outv, amode); break;
   }
 }
 
@@ -594,7 +598,7 @@ __device__ __forceinline__ void consume_group(int R, int fmt, const uint8_t* til
 template <int RC>
 __device__ __forceinline__ void consume_rows(int R, int fmt, const uint8_t* tile, int kc, int nb, int grp,
                                              const uint8_t* act, int lane, float* outv, int amode) {
-  static_assert(RC == 1 || RC == kRowChunk, "row chunk");
+  static_assert(RC == 1 || RC == 2 || RC == kRowChunk, "row chunk");
   const size_t row_bytes = (size_t)act_row_bytes(amode, fmt, kc);
   for (int r0 = 0; r0 < R; r0 += RC) {
     const int n = R - r0 < RC ? R - r0 : RC;

@@ -141,7 +141,13 @@ __host__ __device__ constexpr uint32_t int_rec_bytes(int tq, int kc) {
 struct WsLayout {
   uint64_t err, ctr_route, nu, u_slot, u_fmt, u_addr, u_nrows, u_rows;
   uint64_t comb_u, comb_r, comb_w, z, xf, xh, xsc, xrq, xrt, pa, h, hr, pb, dbg;
-  uint64_t fctr, cnt_a, h_cnt, ctr_out, total;  // counters of the fused layer kernel
+  uint64_t fctr, cnt_a, h_cnt, ctr_out;  // counters of the fused layer kernel
+  // single-kernel decode layer (k_moe), per "row slot" (an expert's r-th row;
+  // M (K + 1) slots at most): call epoch, epoch-tagged logits, K-chunk
+  // partials of g/u and of y, h in fp32, the integer records of h, the grid
+  // barrier counter (64-bit, three arrivals per CTA per call)
+  uint64_t epoch, zt, m_pa, m_pb, m_h, m_hr, m_done;
+  uint64_t total;
 };
 constexpr int kDbgSlots = 8;      // per-CTA cycle counters of the diagnostic mode
 constexpr int kDbgMaxCtas = 1024;
@@ -182,6 +188,14 @@ __host__ __device__ inline WsLayout make_ws(const Geo& g) {
   w.cnt_a = o; o = al256(o + 4ull * g.U * g.npanA);               // chunks done per (expert, panel group)
   w.h_cnt = o; o = al256(o + 4ull * g.U);                         // panel groups of h done per expert
   w.ctr_out = o; o = al256(o + 4ull * g.npanB);                   // (expert, chunk) items done per output panel group
+  w.epoch = o; o = al256(o + 16);
+  w.zt = o; o = al256(o + 8ull * g.M * g.E);                       // (logit bits | tag << 32) per (row, expert)
+  const uint64_t nrs = (uint64_t)g.M * (g.K + 1);
+  w.m_pa = o; o = al256(o + 4ull * nrs * g.npanA * g.nchA * 2 * 32);
+  w.m_pb = o; o = al256(o + 4ull * nrs * g.nchB * g.H);
+  w.m_h = o; o = al256(o + 4ull * nrs * g.I);
+  w.m_hr = o; o = al256(o + (uint64_t)int_rec_bytes(1, g.kcB) * nrs * g.nchB);
+  w.m_done = o; o = al256(o + 16);
   w.total = o;
   return w;
 }
@@ -246,6 +260,34 @@ struct LayerParams {
   uint64_t limit_ns;
 };
 int launch_layer(const LayerParams& P, int grid, cudaStream_t st);
+
+// Single-kernel decode layer (bqe_moe.cu).
+struct MoeParams {
+  Geo g;
+  WsLayout L;
+  uint8_t* ws;
+  const uint16_t* x;          // bf16 M x H, or null when resid is given
+  const float* resid;         // fp32 M x H (chained step: normalise first, out += into it)
+  uint16_t* t_out;            // optional bf16 M x H copy of the layer input
+  const float* router_w;      // E x H
+  const float* bias;          // E or null
+  const int32_t* forced;      // M x K or null
+  const int32_t* slot_table;  // E + 1
+  bqe_pool pool;
+  float* out;
+  int accumulate;
+  int32_t* topk_idx;
+  float* topk_w;
+  uint32_t ring_bytes;        // byte ring for work items
+  uint32_t xstage_off;        // ring offset of the bf16 layer input (used until the routing is known)
+  uint32_t rt_off;            // ring offset of this CTA's router rows (used until the routing is known)
+  uint64_t magA, magA2, magB, magB2;  // ceil(2^32 / d) for the item-index divisors (exact here)
+  int PB;                     // W2 output panels per item
+  int drop_item, variant, diag;
+  uint64_t limit_ns;
+};
+int launch_moe(const MoeParams& P, int grid, cudaStream_t st);
+
 uint32_t layer_smem_bytes(const Geo& g, int* nstages_out, int* nw_out, uint32_t* slot_out);
 
 // Launchers (one per translation unit that owns the kernel).

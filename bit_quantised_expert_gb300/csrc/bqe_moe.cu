@@ -1,0 +1,1298 @@
+// bqe_moe.cu — the decode layer (M <= 8 token rows) as one persistent kernel.
+//
+// The layer's cost is the expert bytes each token streams (field report,
+// section 2: single-stream speed is set by the bytes each token moves), so
+// the kernel is built to keep HBM busy from its first cycle to its last:
+//
+//   * one CTA per SM, launched cooperatively (every CTA resident, so CTAs may
+//     wait on one another; every such wait is bounded by %globaltimer);
+//   * warp 0 (one lane) streams work items into a byte ring in shared memory
+//     with cp.async.bulk and mbarrier completion; warps 1..16 compute; warp
+//     17 finishes each item (partial sums out, dependency counters);
+//   * before the routing is known, the producer streams this CTA's share of
+//     the shared expert's W1/W3 (always used), while the compute warps read
+//     this CTA's rows of the router (z = x Wr^T, fp32), write this CTA's slice
+//     of the staged activations, publish the logits tagged with the call's
+//     epoch, wait until every CTA's logits carry it, and then select the
+//     top-k and build the expert work list themselves (the same result in
+//     every CTA: no serial tail, no second kernel);
+//   * work items are (expert, 32-row panel, K chunk) of W1 and W3, then
+//     (expert, group of W2 output panels, K chunk) of W2, shared expert first,
+//     dealt round-robin over the CTAs, so every expert's W1/W3 is finished by
+//     all CTAs together, long before its W2 items come up;
+//   * the CTA that adds the last K chunk of a (expert, panel) forms
+//     h = silu(g) * u for it (a fixed order over the chunks); the last panel of
+//     a 256-column block of h writes its integer staging record; W2 items wait
+//     (bounded) only for the h chunk they read, and stream their weights
+//     before that wait;
+//   * the CTA that adds the last item of a W2 output panel group combines
+//     out = y_shared + sum_j w_j y_j for it, in a fixed order, so results are
+//     the same run to run.
+//
+// Router, selection and mixing follow the field report (384 routed experts,
+// 6 per token, one shared) and the Strata 4090 post, section 5.3 (the bias
+// steers the choice; the mixing weights are the unbiased scores).  The
+// per-format dequant-GEMV inner loops are those of bqe_gemv.cuh.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "bqe_gemv.cuh"
+#include "bqe_internal.cuh"
+
+namespace bqe {
+
+constexpr int kNQ = 16;                    // items in flight per CTA (barrier ring)
+constexpr int kCW = 16;                    // compute warps
+constexpr int kNP = 2;                     // producer warps
+// producers, compute warps, reducer: 19 warps, at most 5 per SM
+// sub-partition, so each thread may hold 96 registers
+constexpr int kMoeThreads = 32 * (kNP + kCW + 1);
+constexpr int kMaxU = 64;                  // distinct experts of one call (M top_k + 1 <= 64)
+constexpr int kMaxEM = 512;                // routed experts supported
+constexpr int kRouteTasks = 16;            // (expert of this CTA, quarter of hidden) router tasks
+
+
+// Per-item header (slot i % kNQ): where the item's bytes sit in the ring and
+// what they are.
+struct ItemHdr {
+  uint32_t off;       // ring offset of the item
+  uint32_t tb;        // bytes of one weight tile
+  uint32_t act;       // offset of the activation rows (from off)
+  uint32_t red;       // offset of the partial sums (from off)
+  uint32_t arow;      // staged bytes of one activation row
+  int16_t u, p, c, R; // expert (work-list index), panel (W1/W3) or panel group (W2), K chunk, rows
+  uint8_t phase, fmt, amode, nb;
+};
+
+// Everything about the items of one (phase, expert) but their place: the
+// header to copy (off, p, c filled per item), the ring bytes, the weight
+// source and the activation rows' addressing in the workspace.
+struct ItemTpl {
+  ItemHdr h;
+  uint32_t size, wbytes;   // ring bytes of an item; bytes of its weight tiles
+  uint64_t wsrc;           // W1 (phase 0) or W2 (phase 1) of the expert's slot
+  uint32_t m13;            // phase 0: W3 - W1
+  uint32_t act_base;       // workspace offset of activation row 0, chunk 0
+  uint32_t act_rs, act_cs; // bytes from one row (row slot) to the next, one chunk to the next
+};
+
+__device__ __forceinline__ uint32_t al128(uint32_t v) { return (v + 127u) & ~127u; }
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const void* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(void* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ float silu_m(float t) { return t / (1.0f + expf(-t)); }
+
+// Diagnostic timeline of one call: globaltimer stamps kept as minima or
+// maxima over CTAs in row 1023 of dbg blocks 0..2 (8 slots each).
+__device__ __forceinline__ void mstamp(const MoeParams& P, int k, bool is_max) {
+  if (P.diag) dbg_time(P.ws, P.L.dbg, k >> 3, k & 7, is_max);
+}
+enum {
+  kStStart = 0,       // min: first CTA start
+  kStZPub = 1,        // max: last CTA published its logits
+  kStRouted = 2,      // min / max (+8): CTA knows the routing
+  kStRoutedMax = 10,
+  kStFirstItem = 3,   // min: first item landed
+  kStAEnd = 4,        // max: last W1/W3 item finished
+  kStBFirst = 5,      // min: first W2 item landed
+  kStEnd = 6,         // max: last CTA end
+  kStProdEnd = 7,     // max: last producer done issuing
+  kStConsEnd = 9,     // max: last compute warp done
+  kStHWaitMax = 11,   // max: a producer's longest h wait (ns, as a value)
+};
+
+// Diagnostic per-CTA time accounts (ns) in dbg block 2, row = CTA: 0 producer
+// waiting for ring space, 1 producer waiting for h, 2 compute warp 0 waiting
+// for items, 3 compute warp 0 computing, 4 reducer waiting, 5 reducer waiting
+// for queue space, 6 finishers polling partials, 7 CTA start to end.
+// Block 1, row = CTA: 0 producer issuing (outside its waits), 1 items issued,
+// 2 CTA start to its logits published, 3 ... to the routing known, 4 ... to
+// its router rows landed, 5 reducer working, 6 finishers working.
+__device__ __forceinline__ void dacc(const MoeParams& P, int slot, uint64_t ns, int blk = 2) {
+  if (P.diag && blockIdx.x < 1023)
+    atomicAdd((unsigned long long*)(P.ws + P.L.dbg) + ((size_t)blk * 1024 + blockIdx.x) * 8 + slot,
+              (unsigned long long)ns);
+}
+
+// Diagnostic: per-CTA time from the CTA's start to routing step k (dbg block
+// 0, row 300 + CTA, slot k).
+__device__ __forceinline__ void rstamp(const MoeParams& P, int k, uint64_t t0) {
+  if (P.diag && blockIdx.x < 700)
+    atomicAdd((unsigned long long*)(P.ws + P.L.dbg) + ((size_t)300 + blockIdx.x) * 8 + k,
+              (unsigned long long)(globaltimer_ns() - t0));
+}
+
+// Bounded wait on an mbarrier phase, sleeping between checks; also gives up
+// when another CTA has already recorded an error.
+__device__ __forceinline__ bool mwait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, const int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*(volatile const int32_t*)err) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Bounded wait until *p >= target (other CTAs' progress); false on timeout
+// or when an error has been recorded.
+__device__ __forceinline__ bool wait_ge(const unsigned int* p, uint32_t target, uint64_t limit_ns,
+                                        const int32_t* err) {
+  if (ld_acquire_u32(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 16; ++i) {
+      __nanosleep(40);
+      if (ld_acquire_u32(p) >= target) return true;
+    }
+    if (*(volatile const int32_t*)err) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Template of the items of (phase ph, expert u) in format fmt at slot address
+// addr with R activation rows, the first of them in row slot rb.
+__device__ inline void make_tpl(const MoeParams& P, ItemTpl& T, int ph, int u, int fmt, uint64_t addr, int R, int rb) {
+  const Geo& g = P.g;
+  const int kc = ph ? g.kcB : g.kcA;
+  const int amode = act_mode(ph, fmt, P.variant);
+  ItemHdr& h = T.h;
+  h.tb = tile_bytes(fmt, kc);
+  h.arow = (uint32_t)act_row_bytes(amode, fmt, kc);
+  T.wbytes = (uint32_t)(ph ? P.PB : 2) * h.tb;
+  h.act = al128(T.wbytes);
+  h.red = h.act + al128((uint32_t)R * h.arow);
+  h.off = 0;
+  h.u = (int16_t)u; h.p = 0; h.c = 0; h.R = (int16_t)R;
+  h.phase = (uint8_t)ph; h.fmt = (uint8_t)fmt; h.amode = (uint8_t)amode; h.nb = (uint8_t)(kc / fmt_bw(fmt));
+  T.size = h.red + (uint32_t)(ph ? P.PB * g.GB : 2 * g.GA) * R * 32 * 4;
+  const uint64_t m13 = matrix_bytes(fmt, g.I, g.H);
+  T.m13 = (uint32_t)m13;
+  T.wsrc = addr + (ph ? 2 * m13 : 0);
+  if (ph == 0) {
+    if (amode == kActInt) {
+      T.act_base = (uint32_t)(fmt == BQE_FMT_TQ1 ? P.L.xrt : P.L.xrq);
+      T.act_cs = h.arow;
+      T.act_rs = h.arow * g.nchA;
+    } else {
+      const uint32_t es = amode == kActF16 ? 2 : 4;
+      T.act_base = (uint32_t)(amode == kActF16 ? P.L.xh : P.L.xf);
+      T.act_cs = (uint32_t)kc * es;
+      T.act_rs = (uint32_t)g.H * es;
+    }
+  } else {
+    if (amode == kActInt) {
+      const uint32_t rec = int_rec_bytes(1, g.kcB);
+      T.act_base = (uint32_t)(P.L.m_hr + (uint64_t)rb * g.nchB * rec);
+      T.act_cs = rec;
+      T.act_rs = rec * g.nchB;
+    } else {
+      T.act_base = (uint32_t)(P.L.m_h + (uint64_t)rb * g.I * 4);
+      T.act_cs = (uint32_t)g.kcB * 4;
+      T.act_rs = (uint32_t)g.I * 4;
+    }
+  }
+}
+
+template <int RC>
+__global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
+  const Geo& g = P.g;
+  const int H = g.H, I = g.I, E = g.E, K = g.K, M = g.M;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t* err = (int32_t*)(P.ws + P.L.err);
+
+  extern __shared__ __align__(128) uint8_t dsm[];
+  float* s_z = reinterpret_cast<float*>(dsm);                       // M x E logits
+  uint8_t* ring = dsm + ((4u * M * E + 127u) & ~127u);
+  const uint16_t* s_x = reinterpret_cast<const uint16_t*>(ring + P.xstage_off);  // M x H bf16 (startup only)
+  const float* s_rw = reinterpret_cast<const float*>(ring + P.rt_off);  // this CTA's router rows (startup only)
+
+  __shared__ ItemHdr hdr[kNQ];
+  __shared__ __align__(8) uint64_t full[kNQ], cons[kNQ], freed[kNQ], route_bar, rbar;
+  __shared__ __align__(8) uint64_t a_done, b_done, fb_bar;  // this CTA's W1/W3 / W2 partials written; h ready
+  __shared__ int s_rbase[kMaxU + 1];   // first row slot of each work-list expert
+  __shared__ int s_rs[kMaxM][kMaxTopK];  // row slot of (row m, choice j)
+  __shared__ int s_done[kNQ];
+  __shared__ int32_t s_ufmt[kMaxU], s_unrows[kMaxU];
+  __shared__ uint64_t s_uaddr[kMaxU];
+  __shared__ int8_t s_urows[kMaxU * kMaxM];
+  __shared__ float s_cw[kMaxM][kMaxTopK];
+  __shared__ int s_idx[kMaxM][kMaxTopK];
+  __shared__ float s_zsel[kMaxM][kMaxTopK];
+  __shared__ uint32_t s_mask[kMaxEM];
+  __shared__ int16_t s_uof[kMaxEM];
+  __shared__ int s_wcnt[kMaxEM / 32];
+  __shared__ float s_part[kRouteTasks][kMaxM];
+  __shared__ float s_inv_rms[kMaxM], s_xsc[kMaxM];
+  __shared__ int s_emax[kMaxM];
+  __shared__ float s_red[kCW][kMaxM];
+  __shared__ float s_bias[kMaxEM];
+  __shared__ uint64_t s_eaddr[kMaxEM + 1];  // slot address of each expert (E: the shared one)
+  __shared__ int16_t s_eslot[kMaxEM + 1];   // its slot
+  __shared__ uint8_t s_efmt[kMaxEM + 1];    // its slot's format (0: invalid)
+  __shared__ uint8_t s_ebad[kMaxEM + 1];    // error detail of an invalid slot
+  __shared__ int s_nu, s_bad;
+  __shared__ volatile int s_abort, s_issued[kNP], s_turn;  // s_turn: next item to get ring space
+  __shared__ uint32_t s_startq[kNQ];   // ring offset of each item in flight
+  __shared__ volatile uint32_t s_head; // end of the newest allocation
+  __shared__ volatile int s_oldest;    // oldest item not yet known to be freed
+  __shared__ volatile int s_npre;      // items pre-issued before the routing (-1: not yet known)
+  __shared__ ItemTpl s_tpl[2][kMaxU];
+
+  const uint32_t tag = *(volatile const uint32_t*)(P.ws + P.L.epoch) + 1u;
+  if (tid == 0) {
+    for (int s = 0; s < kNQ; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&cons[s], 1);
+      mbar_init(&freed[s], 1);
+      s_done[s] = 0;
+    }
+    mbar_init(&a_done, 1);
+    mbar_init(&b_done, 1);
+    mbar_init(&fb_bar, 1);
+    mbar_init(&route_bar, 1);
+    mbar_init(&rbar, 1);
+    s_abort = 0;
+    for (int q = 0; q < kNP; ++q) s_issued[q] = 0;
+    s_turn = 0;
+    s_npre = -1;
+    s_head = 0;
+    s_oldest = 0;
+    s_bad = 0;
+    s_nu = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) mstamp(P, kStStart, false);
+  const uint64_t t_cta0 = P.diag ? globaltimer_ns() : 0;
+
+  // geometry of the two item kinds
+  const int TA = 2 * g.GA, TB = P.PB * g.GB;             // compute tasks per item
+  const int nAper = g.npanA * g.nchA;                    // W1/W3 items per expert
+  const int nBper = (g.npanB / P.PB) * g.nchB;           // W2 items per expert
+  const int bpcB = g.kcB / 256;                          // 256-column blocks of h per W2 chunk
+
+  if (warp < kNP) {
+    // ============================== producers =================================
+    // Producer pp (warp pp, one lane) issues items i = pp, pp + kNP, ..., so
+    // the bookkeeping of one overlaps the other's bulk-copy issue (a thread
+    // waits in cp.async.bulk until the copy engine takes the bytes).  Both
+    // share one ring, allocated in item order; items i and i + kNQ share
+    // barriers and a producer.
+    const int pp = warp;
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int issued = -1;  // last own item whose copies went out
+      bool ok = true;
+      // Ring space [at, at + sz) of [0, end) for item i.  Items get their space
+      // in item order (the two producers take turns; the state is shared);
+      // waits (bounded) for the turn and for frees when may_wait.  -1: no room
+      // (or not this item's turn) without waiting, -2: timeout.
+      auto alloc = [&](int i, uint32_t sz, uint32_t end, bool may_wait) -> int64_t {
+        if (s_turn != i) {
+          if (!may_wait) return -1;
+          const uint64_t t0 = globaltimer_ns();
+          while (s_turn != i) {
+            __nanosleep(32);
+            if (s_abort || *(volatile const int32_t*)err || globaltimer_ns() - t0 > P.limit_ns) return -2;
+          }
+        }
+        int oldest = s_oldest;
+        uint32_t head = s_head;
+        if (i >= kNQ) {
+          const int j = i - kNQ;
+          if (oldest <= j) {
+            if (!may_wait) return -1;
+            if (!mwait(&freed[j % kNQ], (j / kNQ) & 1, P.limit_ns, err)) return -2;
+            oldest = j + 1;
+          }
+        }
+        int64_t at = -1;
+        while (true) {
+          if (oldest == i) {
+            head = 0;
+            at = sz <= end ? 0 : -3;
+            break;
+          }
+          const uint32_t tail = s_startq[oldest % kNQ];
+          if (head > tail) {
+            if (head + sz <= end) { at = head; break; }
+            if (sz <= tail) { at = 0; break; }
+          } else if (head < tail) {
+            if (head + sz <= tail) { at = head; break; }
+          }
+          if (!may_wait) break;
+          if (!mwait(&freed[oldest % kNQ], (oldest / kNQ) & 1, P.limit_ns, err)) return -2;
+          ++oldest;
+        }
+        s_oldest = oldest;
+        if (at >= 0) {
+          s_startq[i % kNQ] = (uint32_t)at;
+          s_head = (uint32_t)at + sz;
+        }
+        return at;
+      };
+      // the copies of item i from template T: weight tiles, then (acts) activation rows
+      auto issue = [&](int i, const ItemTpl& T, int p, int c, bool weights, bool acts, bool pre) {
+        const uint32_t off = hdr[i % kNQ].off;
+        uint8_t* dst = ring + off;
+        uint64_t* bar = &full[i % kNQ];
+        if (weights) {
+          if (pre) mbar_expect_tx(bar, T.wbytes);
+          if (T.h.phase == 0) {
+            const uint64_t src = T.wsrc + (uint64_t)(p * g.nchA + c) * T.h.tb;
+            bulk_g2s_hint(dst, (const void*)src, T.h.tb, bar, pol);                       // W1 tile
+            bulk_g2s_hint(dst + T.h.tb, (const void*)(src + T.m13), T.h.tb, bar, pol);   // W3 tile
+          } else {
+            for (int j = 0; j < P.PB; ++j) {
+              const uint64_t src = T.wsrc + (uint64_t)((p * P.PB + j) * g.nchB + c) * T.h.tb;
+              bulk_g2s_hint(dst + j * T.h.tb, (const void*)src, T.h.tb, bar, pol);          // W2 tiles
+            }
+          }
+        }
+        if (acts) {
+          if (pre) mbar_arrive_expect_tx(bar, (uint32_t)T.h.R * T.h.arow);
+          const uint8_t* src0 = P.ws + T.act_base + (uint64_t)c * T.act_cs;
+          for (int r = 0; r < T.h.R; ++r) {
+            const int row = (T.h.phase == 0 && T.h.u != 0) ? s_urows[T.h.u * kMaxM + r] : r;
+            bulk_g2s(dst + T.h.act + (size_t)r * T.h.arow, src0 + (uint64_t)row * T.act_rs, T.h.arow, bar);
+          }
+        }
+      };
+      // ---- producer 0: this CTA's router rows (experts cta, cta + G, ...)
+      if (pp == 0) {
+        const int nexp = E > cta ? (E - cta + G - 1) / G : 0;
+        const uint32_t rowb = (uint32_t)H * 4;
+        mbar_arrive_expect_tx(&rbar, (uint32_t)nexp * rowb);
+        for (int j = 0; j < nexp; ++j)
+          bulk_g2s_hint(ring + P.rt_off + j * rowb, P.router_w + (int64_t)(cta + j * G) * H, rowb, &rbar, pol);
+      }
+      // ---- before the routing: own shared-expert W1/W3 items, weights only.
+      // The shared expert's slot comes from the inputs, not from the router.
+      ItemTpl sh;
+      bool sh_ok = false;
+      {
+        const int sl = P.slot_table[E];
+        if (sl >= 0 && sl < P.pool.n_slots) {
+          const int f = P.pool.slot_fmt[sl];
+          const uint64_t off = P.pool.slot_off[sl];
+          if (fmt_ok(f) && !(off & 15) && off + 2 * matrix_bytes(f, I, H) + matrix_bytes(f, H, I) <= P.pool.base_bytes) {
+            make_tpl(P, sh, 0, 0, f, (uint64_t)P.pool.base + off, M, 0);
+            sh_ok = true;
+          }
+        }
+      }
+      // producer 0 pre-issues items 0, 1, ... (weights only) while they fit below
+      // the startup data; each item's owner (i % kNP) issues its activation rows
+      // once the routing is known
+      if (!mwait(&rbar, 0, P.limit_ns, err)) sh_ok = false;
+      if (pp == 0) {
+        int n = 0;
+        if (sh_ok) {
+          for (int i = 0;; ++i) {
+            const int t = cta + i * G;
+            if (t >= nAper || i >= kNQ) break;
+            if (i == P.drop_item && cta == 0) break;  // the test hook's item goes through the main loop
+            const int64_t at = alloc(i, sh.size, P.rt_off, false);
+            if (at < 0) break;
+            ItemHdr h = sh.h;
+            h.off = (uint32_t)at;
+            h.p = (int16_t)(t / g.nchA);
+            h.c = (int16_t)(t - h.p * g.nchA);
+            hdr[i % kNQ] = h;
+            s_done[i % kNQ] = 0;
+            issue(i, sh, h.p, h.c, true, false, true);
+            s_issued[i % kNP] = i + 1;
+            s_turn = i + 1;
+            ++n;
+          }
+        }
+        s_npre = n;
+      } else {
+        const uint64_t t0 = globaltimer_ns();  // producer 0's count of pre-issued items
+        while (s_npre < 0 && globaltimer_ns() - t0 < P.limit_ns) __nanosleep(32);
+      }
+      const int npre = max(0, (int)s_npre);
+      // ---- the routing (work list and item templates built by the compute warps)
+      if (!mwait(&route_bar, 0, P.limit_ns, err)) {
+        set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+        s_abort = 1;
+        ok = false;
+      }
+      const int nU = s_nu;
+      fence_proxy_async_global();  // the staged inputs of every CTA are read by bulk copies below
+      for (int i = pp; i < npre; i += kNP) {
+        issue(i, sh, hdr[i % kNQ].p, hdr[i % kNQ].c, false, true, true);
+        issued = i;
+      }
+      const int nTot = nU * (nAper + nBper), nA = nU * nAper;
+      long long hwait_max = 0;
+      int dropped = -1;
+      bool h_ready = false;
+      long long cyc_loop = P.diag ? clock64() : 0, cyc_bulk = 0, cyc_alloc = 0, cyc_h = 0;
+      int first = pp;
+      while (first < npre) first += kNP;
+      for (int i = first; ok; i += kNP) {
+        const int t = cta + i * G;
+        if (t >= nTot || s_abort) break;
+        // item t: W1/W3 items of experts 0..nU-1 (panel-major, chunk fastest), then W2 items
+        int ph, u, p, c;
+        if (t < nA) {
+          ph = 0;
+          u = (int)(((uint64_t)t * P.magA) >> 32);
+          const int r = t - u * nAper;
+          p = (int)(((uint64_t)r * P.magA2) >> 32);
+          c = r - p * g.nchA;
+        } else {
+          const int tb = t - nA;
+          ph = 1;
+          u = (int)(((uint64_t)tb * P.magB) >> 32);
+          const int r = tb - u * nBper;
+          p = (int)(((uint64_t)r * P.magB2) >> 32);
+          c = r - p * g.nchB;
+        }
+        const ItemTpl& T = s_tpl[ph][u];
+        const long long ta = P.diag ? clock64() : 0;
+        const int64_t at = alloc(i, T.size, P.ring_bytes, true);
+        if (P.diag) cyc_alloc += clock64() - ta;
+        if (at < 0) {
+          set_error(err, at == -2 ? BQE_ETIMEOUT : BQE_EUNSUPPORTED, kErrWaitEmpty);
+          s_abort = 1;
+          break;
+        }
+        ItemHdr h = T.h;
+        h.off = (uint32_t)at;
+        h.p = (int16_t)p;
+        h.c = (int16_t)c;
+        hdr[i % kNQ] = h;
+        s_done[i % kNQ] = 0;
+        s_issued[pp] = i + 1;
+        s_turn = i + 1;  // the next item may get its ring space
+        if (i == P.drop_item && cta == 0) {  // test hook: this item's copies are never issued
+          dropped = i;
+          continue;
+        }
+        mbar_arrive_expect_tx(&full[i % kNQ], T.wbytes + (uint32_t)h.R * h.arow);
+        const long long tb0 = P.diag ? clock64() : 0;
+        issue(i, T, p, c, true, false, false);
+        if (P.diag) cyc_bulk += clock64() - tb0;
+        issued = i;
+        if (ph == 1 && !h_ready) {
+          // h of every expert is written (all CTAs passed the h phase) before the
+          // first W2 activation rows are copied; the weights above are already on their way
+          const long long w0 = P.diag ? (long long)globaltimer_ns() : 0;
+          const long long tc0 = P.diag ? clock64() : 0;
+          if (!mwait(&fb_bar, 0, P.limit_ns, err)) {
+            set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+            s_abort = 1;
+            ok = false;  // the activation copies still go out (valid addresses) so the stage drains
+          }
+          if (P.diag) {
+            hwait_max = max(hwait_max, (long long)globaltimer_ns() - w0);
+            dacc(P, 1, globaltimer_ns() - w0);
+            cyc_h += clock64() - tc0;
+          }
+          fence_proxy_async_global();
+          h_ready = true;
+        }
+        const long long tb1 = P.diag ? clock64() : 0;
+        issue(i, T, p, c, false, true, false);
+        if (P.diag) cyc_bulk += clock64() - tb1;
+      }
+      if (P.diag) {
+        dacc(P, 0, clock64() - cyc_loop, 1);
+        dacc(P, 1, (issued + kNP) / kNP, 1);
+        dacc(P, 5, cyc_bulk, 1);
+        dacc(P, 6, cyc_alloc, 1);
+        dacc(P, 7, cyc_h, 1);
+        dbg_time(P.ws, P.L.dbg, 0, kStProdEnd, true);
+        atomicMax((unsigned long long*)(P.ws + P.L.dbg) + ((size_t)1 * 1024 + 1023) * 8 + (kStHWaitMax & 7),
+                  (unsigned long long)hwait_max);
+      }
+      // leave no copy in flight: every issued own item has landed before the CTA
+      // ends (own items older than the last kNQ / kNP were freed, so they landed)
+      for (int i = issued; i >= 0 && i > issued - kNQ; i -= kNP)
+        if (i != dropped) mbar_wait_bounded(&full[i % kNQ], (i / kNQ) & 1, 2000000000ull);
+    }
+  } else if (warp < kNP + kCW) {
+    // ============================ compute warps ===============================
+    const int ct = tid - 32 * kNP, cw = warp - kNP;
+    constexpr int NCT = kCW * 32;
+    // ---- this CTA's router rows: experts cta + j G, task (j, quarter of hidden)
+    const int nexp = E > cta ? (E - cta + G - 1) / G : 0;
+    const int Kq = H / 4, ni = Kq / 128;
+    const int rj = cw >> 2, rq = cw & 3;
+    const bool rtask = cw < nexp * 4;
+    // ---- the layer input as bf16 in shared memory: x, or bf16(rmsnorm(resid))
+    uint16_t* xs = const_cast<uint16_t*>(s_x);
+    if (ct < M) s_emax[ct] = -1000;
+    if (P.resid) {
+      for (int m = 0; m < M; ++m) {
+        float ss = 0.f;
+        for (int k = ct; k < H; k += NCT) {
+          const float v = P.resid[(int64_t)m * H + k];
+          ss = fmaf(v, v, ss);
+        }
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) s_red[cw][m] = ss;
+      }
+      named_bar_sync(1, NCT);
+      if (ct < M) {
+        float ss = 0.f;
+        for (int w = 0; w < kCW; ++w) ss += s_red[w][ct];
+        s_inv_rms[ct] = 1.0f / sqrtf(ss / (float)H + 1e-6f);
+      }
+      named_bar_sync(1, NCT);
+      for (int i = ct; i < M * H; i += NCT)
+        xs[i] = __bfloat16_as_ushort(__float2bfloat16_rn(P.resid[i] * s_inv_rms[i / H]));
+    } else {
+      const uint4* src = reinterpret_cast<const uint4*>(P.x);
+      uint4* dst = reinterpret_cast<uint4*>(xs);
+      for (int i = ct; i < M * H / 8; i += NCT) dst[i] = src[i];
+    }
+    named_bar_sync(1, NCT);
+    if (P.diag && ct == 0) dacc(P, 0, globaltimer_ns() - t_cta0, 0);
+    // per-row scale: s puts the row's largest |x| in [2^14, 2^15) for the f16
+    // copy and in [2^13, 2^14) for the integer records (every CTA derives the same)
+    for (int m = 0; m < M; ++m) {
+      uint32_t mx = 0;
+      for (int k = ct; k < H; k += NCT) mx = max(mx, (uint32_t)(xs[m * H + k] & 0x7FFFu));
+      for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0 && mx) atomicMax(&s_emax[m], (int)(mx >> 7) - 127);
+    }
+    named_bar_sync(1, NCT);
+    if (ct < M) s_xsc[ct] = ldexpf(1.0f, -(s_emax[ct] == -1000 ? 0 : 14 - s_emax[ct]));
+    // ---- this CTA's slice of the staged copies of the input (read by every CTA's bulk copies)
+    {
+      float* xf = (float*)(P.ws + P.L.xf);
+      uint16_t* xh = (uint16_t*)(P.ws + P.L.xh);
+      const int n = M * H, per = (n + G - 1) / G, lo = min(n, per * cta), hi = min(n, lo + per);
+      for (int i = lo + ct; i < hi; i += NCT) {
+        const int m = i / H;
+        const float v = __uint_as_float((uint32_t)xs[i] << 16);
+        const int sh = s_emax[m] == -1000 ? 0 : 14 - s_emax[m];
+        xf[i] = v;
+        xh[i] = __half_as_ushort(__float2half_rn(ldexpf(v, sh)));
+        if (P.t_out) P.t_out[i] = xs[i];
+      }
+      // integer records X_hi + X_lo / 128 of x 2^si in the two orders, one
+      // 256-column block per 256 threads
+      const int nbr = H / 256, nblk = M * nbr, bpc = g.kcA / 256;
+      const int half = ct >> 8, j = ct & 255;
+      for (int blk = cta + half * G; blk < nblk; blk += 2 * G) {
+        const int m = blk / nbr, bj = blk % nbr;
+        const int c = bj / bpc, k = bj % bpc;
+        uint8_t* rq = P.ws + P.L.xrq + ((size_t)m * g.nchA + c) * int_rec_bytes(0, g.kcA);
+        uint8_t* rt = P.ws + P.L.xrt + ((size_t)m * g.nchA + c) * int_rec_bytes(1, g.kcA);
+        const int si = s_emax[m] == -1000 ? 0 : 13 - s_emax[m];
+        const float v = ldexpf(__uint_as_float((uint32_t)xs[m * H + bj * 256 + j] << 16), si);
+        const int Xh = __float2int_rn(v);
+        const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
+        rec_put(rq, 0, g.kcA, k, j, Xh, Xl);
+        rec_put(rt, 1, g.kcA, k, j, Xh, Xl);
+        if (j < 16) rec_put_pad(rt, g.kcA, k, j);
+        int ph = Xh, pl = Xl;
+#pragma unroll
+        for (int o = 8; o; o >>= 1) {
+          ph += __shfl_xor_sync(0xffffffffu, ph, o);
+          pl += __shfl_xor_sync(0xffffffffu, pl, o);
+        }
+        if ((lane & 15) == 0) {
+          rec_put_sums(rq, 0, g.kcA, k, j >> 4, ph, pl);
+          rec_put_sums(rt, 1, g.kcA, k, j >> 4, ph, pl);
+        }
+        if (j == 0) {
+          rec_put_scale(rq, 0, g.kcA, k, ldexpf(1.0f, -si));
+          rec_put_scale(rt, 1, g.kcA, k, ldexpf(1.0f, -si));
+        }
+      }
+    }
+    // ---- selection inputs, read before the logits sync (no kernel writes them):
+    // the bias, and the slot descriptor of expert e = ct (e = E: the shared one)
+    for (int i = ct; i < E; i += NCT) s_bias[i] = P.bias ? P.bias[i] : 0.f;
+    auto slot_desc = [&](int e, int& slot, int& fmt, uint64_t& addr, int& bad) {
+      slot = P.slot_table[e];
+      fmt = 0;
+      addr = 0;
+      bad = 0;
+      if (slot < 0 || slot >= P.pool.n_slots) {
+        bad = kErrSlotRange;
+        return;
+      }
+      const int f = P.pool.slot_fmt[slot];
+      const uint64_t off = P.pool.slot_off[slot];
+      if (!fmt_ok(f)) {
+        bad = kErrSlotFmt;
+        return;
+      }
+      if ((off & 15) || off + 2 * matrix_bytes(f, I, H) + matrix_bytes(f, H, I) > P.pool.base_bytes) {
+        bad = kErrSlotExtent;
+        return;
+      }
+      fmt = f;
+      addr = (uint64_t)P.pool.base + off;
+    };
+    // into shared memory now, so none of these loads waits until after the routing
+    for (int e = ct; e <= E; e += NCT) {
+      int sl, f, bad;
+      uint64_t ad;
+      slot_desc(e, sl, f, ad, bad);
+      s_eslot[e] = (int16_t)sl;
+      s_efmt[e] = (uint8_t)f;
+      s_eaddr[e] = ad;
+      s_ebad[e] = (uint8_t)bad;
+    }
+    // the staged slices are read by other CTAs' bulk copies once the routing
+    // is known: fence them now, while the router rows are still landing
+    // (the gpu-scope release is the CTA's arrival on the logits counter below)
+    fence_proxy_async_global();
+    if (P.diag && ct == 0) dacc(P, 1, globaltimer_ns() - t_cta0, 0);
+    float* zg = (float*)(P.ws + P.L.z);
+    // The routing: keys, top-k, mixing weights, work list, row slots and item
+    // templates (dry: a pass without effect outside this CTA's shared memory,
+    // kept for timing experiments; the call makes one real pass)
+    auto routing = [&](bool dry) {
+    // logits and selection keys of every (row, expert), all threads; the keys
+    // go where this CTA's router rows were (no longer needed)
+    uint32_t* s_key = dry ? reinterpret_cast<uint32_t*>(s_z) : reinterpret_cast<uint32_t*>(ring + P.rt_off);
+    const bool forced = P.forced && !dry;
+    for (int i = ct; i < M * E; i += NCT) {
+      const float zv = dry ? s_z[i] : __ldcg(zg + i);
+      if (!dry) s_z[i] = zv;
+      if (!forced) s_key[i] = sel_key(zv, s_bias[i % E]);
+    }
+    for (int i = ct; i < E; i += NCT) s_mask[i] = 0u;
+    named_bar_sync(1, NCT);
+    if (ct == 0 && !dry) {
+      mstamp(P, kStRouted, false);
+      rstamp(P, 0, t_cta0);
+    }
+    // ---- top-k of each row (warp m selects row m), mixing weights
+    if (cw < M && (dry || !s_abort)) {
+      const int m = cw;
+      constexpr int QN = kMaxEM / 32;
+      const int qn = (E + 31) / 32;
+      uint32_t kk[QN];
+#pragma unroll
+      for (int q = 0; q < QN; ++q) {
+        const int e = lane + 32 * q;
+        kk[q] = (!forced && q < qn && e < E) ? s_key[m * E + e] : 0u;
+      }
+      for (int j = 0; j < K; ++j) {
+        int best;
+        if (forced) {
+          best = P.forced[m * K + j];
+          if (best < 0 || best >= E) {
+            if (lane == 0) { set_error(err, BQE_EDEVICE, kErrForcedIdx); s_bad = 1; }
+            best = 0;
+          }
+        } else {
+          uint32_t bk = 0u;
+          int bq = 0;
+#pragma unroll
+          for (int q = 0; q < QN; ++q)
+            if (q < qn && kk[q] > bk) {
+              bk = kk[q];
+              bq = q;
+            }
+          const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+          const uint32_t eb =
+              __reduce_min_sync(0xffffffffu, (bk == wk && wk != 0u) ? (uint32_t)(lane + 32 * bq) : 0xffffffffu);
+          if (eb != 0xffffffffu && (int)(eb & 31u) == lane) {
+#pragma unroll
+            for (int q = 0; q < QN; ++q)
+              if ((uint32_t)q == (eb >> 5)) kk[q] = 0u;
+          }
+          best = eb == 0xffffffffu ? 0 : (int)eb;
+        }
+        if (lane == 0) {
+          s_idx[m][j] = best;
+          s_zsel[m][j] = s_z[m * E + best];
+          atomicOr(&s_mask[best], 1u << m);
+        }
+      }
+      __syncwarp();
+      // w_j = s_j / sum s as exp(log s_j - max log s) / sum exp(...): finite
+      // even when every selected sigmoid underflows in fp32
+      float ls = -INFINITY;
+      if (lane < K) {
+        const float zz = s_zsel[m][lane];
+        ls = zz < 0.f ? zz - log1pf(expf(zz)) : -log1pf(expf(-zz));
+      }
+      float mx = ls;
+      for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float ev = lane < K ? expf(ls - mx) : 0.f;
+      float tot = ev;
+      for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      if (lane < K) {
+        const float w = ev / tot;
+        s_cw[m][lane] = w;
+        if (cta == 0 && !dry) {
+          if (P.topk_idx) P.topk_idx[m * K + lane] = s_idx[m][lane];
+          if (P.topk_w) P.topk_w[m * K + lane] = w;
+        }
+      }
+    }
+    named_bar_sync(1, NCT);
+    if (ct == 0 && !dry) rstamp(P, 1, t_cta0);
+    // ---- work list: the chosen experts in ascending id order (u = 1..), shared u = 0
+    {
+      const int e = ct;  // E <= 512 = NCT
+      const bool on = e < E && s_mask[e] != 0u;
+      const uint32_t bal = __ballot_sync(0xffffffffu, on);
+      if (lane == 0) s_wcnt[cw] = __popc(bal);
+      named_bar_sync(1, NCT);
+      if (on) {
+        int base = 0;
+        for (int w2 = 0; w2 < cw; ++w2) base += s_wcnt[w2];
+        s_uof[e] = (int16_t)(1 + base + __popc(bal & ((1u << lane) - 1u)));
+      }
+      named_bar_sync(1, NCT);
+      if (on) {
+        const int u = s_uof[e];
+        const int my_bad = s_ebad[e], my_fmt = s_efmt[e], my_slot = s_eslot[e];
+        if (my_bad && !dry) {
+          set_error(err, BQE_EDEVICE, my_bad);
+          s_bad = 1;
+        }
+        s_ufmt[u] = my_fmt;
+        s_uaddr[u] = s_eaddr[e];
+        const uint32_t mask = s_mask[e];
+        int n = 0;
+        for (int m = 0; m < M; ++m)
+          if (mask & (1u << m)) s_urows[u * kMaxM + n++] = (int8_t)m;
+        s_unrows[u] = n;
+        if (cta == 0 && !dry) {  // the call's work list, for bqe_layer_stats
+          ((int32_t*)(P.ws + P.L.u_slot))[u] = my_slot;
+          ((int32_t*)(P.ws + P.L.u_fmt))[u] = my_fmt;
+          ((int32_t*)(P.ws + P.L.u_nrows))[u] = n;
+        }
+      }
+      if (ct == NCT - 1) {
+        // the shared expert, u = 0 (validated like the others)
+        const int sh_bad = s_ebad[E], sh_fmt = s_efmt[E], sh_slot = s_eslot[E];
+        if (sh_bad && !dry) {
+          set_error(err, BQE_EDEVICE, sh_bad);
+          s_bad = 2;
+        }
+        s_ufmt[0] = sh_fmt;
+        s_uaddr[0] = s_eaddr[E];
+        s_unrows[0] = M;
+        if (cta == 0 && !dry) {
+          ((int32_t*)(P.ws + P.L.u_slot))[0] = sh_slot;
+          ((int32_t*)(P.ws + P.L.u_fmt))[0] = sh_fmt;
+          ((int32_t*)(P.ws + P.L.u_nrows))[0] = M;
+        }
+        for (int m = 0; m < M; ++m) s_urows[m] = (int8_t)m;
+      }
+      named_bar_sync(1, NCT);
+      if (ct == 0 && !dry) rstamp(P, 2, t_cta0);
+      if (ct == 0) {
+        int tot = 0;
+        for (int w2 = 0; w2 < kCW; ++w2) tot += s_wcnt[w2];
+        // row slots: the shared expert's M rows first, then each chosen
+        // expert's rows in work-list order
+        int acc = 0;
+        for (int u = 0; u <= tot; ++u) {
+          s_rbase[u] = acc;
+          acc += s_unrows[u];
+        }
+        s_rbase[tot + 1] = acc;
+        // on an invalid routed slot only the shared expert runs (the call
+        // reports the error; its output is undefined); an invalid shared slot
+        // or an aborted routing streams nothing
+        s_nu = (s_abort || s_bad == 2) ? 0 : s_bad ? 1 : 1 + tot;
+        if (cta == 0 && !dry) *(int32_t*)(P.ws + P.L.nu) = s_nu;
+      }
+      named_bar_sync(1, NCT);
+      if (ct == 0 && !dry) rstamp(P, 3, t_cta0);
+      if (ct < M * K && (dry || !s_abort)) {
+        const int m = ct / K, j = ct % K;
+        const int ee = s_idx[m][j];
+        s_rs[m][j] = s_rbase[s_uof[ee]] + __popc(s_mask[ee] & ((1u << m) - 1u));
+      }
+      // item templates of every (phase, work-list expert)
+      if (ct >= 64 && ct < 64 + 2 * s_nu) {
+        const int ph = (ct - 64) & 1, u = (ct - 64) >> 1;
+        if (fmt_ok(s_ufmt[u])) make_tpl(P, s_tpl[ph][u], ph, u, s_ufmt[u], s_uaddr[u], s_unrows[u], s_rbase[u]);
+      }
+      named_bar_sync(1, NCT);
+      if (ct == 0 && !dry) {
+        mstamp(P, kStRoutedMax, true);
+        if (P.diag) dacc(P, 3, globaltimer_ns() - t_cta0, 1);
+        mbar_arrive(&route_bar);
+      }
+    }
+    };
+    // ---- router dot products of this CTA's experts (rows landed in shared memory)
+    {
+      const bool okr = __all_sync(0xffffffffu, mwait(&rbar, 0, P.limit_ns, err));
+      if (!okr && lane == 0) {
+        set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+        s_abort = 1;
+      }
+      if (P.diag && ct == 0) dacc(P, 4, globaltimer_ns() - t_cta0, 1);
+      float acc[kMaxM];
+#pragma unroll
+      for (int m = 0; m < kMaxM; ++m) acc[m] = 0.f;
+      if (rtask && okr) {
+        const float4* wr = reinterpret_cast<const float4*>(s_rw + rj * H + rq * Kq);
+#pragma unroll 4
+        for (int i = 0; i < ni; ++i) {
+          {
+            const float4 wv = wr[i * 32 + lane];
+            const int k = rq * Kq + (i * 32 + lane) * 4;
+#pragma unroll
+            for (int m = 0; m < kMaxM; ++m) {
+              if (m < M) {
+                const uint2 xv = *reinterpret_cast<const uint2*>(xs + m * H + k);
+                acc[m] = fmaf(wv.x, __uint_as_float(xv.x << 16), acc[m]);
+                acc[m] = fmaf(wv.y, __uint_as_float(xv.x & 0xFFFF0000u), acc[m]);
+                acc[m] = fmaf(wv.z, __uint_as_float(xv.y << 16), acc[m]);
+                acc[m] = fmaf(wv.w, __uint_as_float(xv.y & 0xFFFF0000u), acc[m]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < kMaxM; ++m) {
+        float v = acc[m];
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0 && rtask && m < M) s_part[cw][m] = v;
+      }
+    }
+    named_bar_sync(1, NCT);  // logits partials of this CTA are in shared memory
+    if (ct < nexp * M) {
+      const int j = ct / M, m = ct % M, e = cta + j * G;
+      zg[(size_t)m * E + e] = (s_part[4 * j][m] + s_part[4 * j + 1][m]) + (s_part[4 * j + 2][m] + s_part[4 * j + 3][m]);
+    }
+    named_bar_sync(1, NCT);
+    // publish: one arrival per CTA on the call's logits counter (monotonic:
+    // G per call), released after this CTA's logits and staged slices; then
+    // wait (bounded) until every CTA has arrived, and read all logits
+    unsigned long long* zcnt = (unsigned long long*)(P.ws + P.L.zt);
+    if (ct == 0) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      atomicAdd(zcnt, 1ull);
+      mstamp(P, kStZPub, true);
+      if (P.diag) dacc(P, 2, globaltimer_ns() - t_cta0, 1);
+      const unsigned long long target = (unsigned long long)G * tag;
+      const uint64_t t0 = globaltimer_ns();
+      bool okz = true;
+      while (ld_acquire_u64(zcnt) < target) {
+        __nanosleep(32);
+        if (globaltimer_ns() - t0 > P.limit_ns || *(volatile const int32_t*)err) {
+          okz = false;
+          break;
+        }
+      }
+      if (!okz) {
+        set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+        s_abort = 1;
+      }
+      if (P.diag) dacc(P, 2, globaltimer_ns() - t_cta0, 0);
+    }
+    named_bar_sync(1, NCT);
+    routing(false);
+    // ---- work items: this warp takes tasks cw, cw + 16, ... of the CTA's task sequence
+    const int nU = s_nu;
+    const int nTot = nU * (nAper + nBper), nA = nU * nAper;
+    const int nmine = cta < nTot ? (nTot - cta + G - 1) / G : 0;
+    const int nAmine = cta < nA ? (nA - cta + G - 1) / G : 0;
+    int k = cw, Ki = 0;
+    bool first = true, okc = !s_abort;
+    auto run_items = [&](int i0, int i1) {
+      for (int i = i0; i < i1 && okc; ++i) {
+        const bool isA = cta + i * G < nA;
+        const int T = isA ? TA : TB;
+        if (k >= Ki + T) {  // no task of this warp in item i
+          Ki += T;
+          continue;
+        }
+        // Wait until item i is issued: the producer issues it only after item
+        // i - kNQ (same barriers) is freed, so the phase parity then names
+        // item i's landing and no other; then wait for the landing itself.
+        bool ok = true;
+        const uint64_t tw = (P.diag && cw == 0) ? globaltimer_ns() : 0;
+        if (s_issued[i % kNP] <= i) {
+          const uint64_t t0 = globaltimer_ns();
+          for (int spin = 0; s_issued[i % kNP] <= i; ++spin) {
+            __nanosleep(32);
+            if (s_abort || ((spin & 63) == 63 && (*(volatile const int32_t*)err || globaltimer_ns() - t0 > P.limit_ns))) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        ok = __all_sync(0xffffffffu, ok && mwait(&full[i % kNQ], (i / kNQ) & 1, P.limit_ns, err));
+        if (!ok || s_abort) {
+          if (lane == 0) {
+            if (!ok) set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+            s_abort = 1;
+          }
+          okc = false;
+          break;
+        }
+        if (first && ct == 0) {
+          mstamp(P, kStFirstItem, false);
+          first = false;
+        }
+        const uint64_t tc = (P.diag && cw == 0) ? globaltimer_ns() : 0;
+        if (P.diag && cw == 0 && lane == 0) dacc(P, 2, tc - tw);
+        const ItemHdr h = hdr[i % kNQ];
+        const int tau = k - Ki;
+        const uint8_t* base = ring + h.off;
+        int tile_i, grp;
+        if (isA) {
+          tile_i = tau / g.GA;
+          grp = tau - tile_i * g.GA;
+        } else {
+          tile_i = tau / g.GB;
+          grp = tau - tile_i * g.GB;
+        }
+        float* red = reinterpret_cast<float*>(const_cast<uint8_t*>(base) + h.red) + tau * h.R * 32;
+        consume_rows<RC>(h.R, h.fmt, base + tile_i * h.tb, isA ? g.kcA : g.kcB, h.nb, grp, base + h.act, lane, red,
+                         h.amode);
+        __syncwarp();
+        if (P.diag && cw == 0 && lane == 0) dacc(P, 3, globaltimer_ns() - tc);
+        if (lane == 0) {
+          __threadfence_block();
+          const int old = atomicAdd(&s_done[i % kNQ], 1);
+          if (old == T - 1) {
+            __threadfence_block();
+            mbar_arrive(&cons[i % kNQ]);
+          }
+        }
+        k += kCW;
+        Ki += T;
+      }
+    };
+    // grid barrier b of this call (thread ct == 0 arrives and waits; the other
+    // compute threads wait at the CTA barrier behind it)
+    auto grid_barrier = [&](int b, uint64_t* local_done) {
+      fence_proxy_async_global();  // this thread's writes are read by other CTAs' bulk copies
+      named_bar_sync(1, NCT);
+      if (ct == 0) {
+        const uint64_t tb0 = P.diag ? globaltimer_ns() : 0;
+        bool okb = true;
+        if (local_done) okb = mwait(local_done, 0, P.limit_ns, err);  // this CTA's partial sums are written
+        fence_proxy_async_global();
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        unsigned long long* ctr = (unsigned long long*)(P.ws + P.L.m_done);
+        atomicAdd(ctr, 1ull);
+        const unsigned long long target = (unsigned long long)G * (3ull * (tag - 1u) + (unsigned)b + 1ull);
+        const uint64_t t0 = globaltimer_ns();
+        while (okb && ld_acquire_u64(ctr) < target) {
+          __nanosleep(64);
+          if (*(volatile const int32_t*)err || globaltimer_ns() - t0 > P.limit_ns) okb = false;
+        }
+        if (!okb) {
+          set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+          s_abort = 1;
+        }
+        if (P.diag) dacc(P, 3 + 2 * b, globaltimer_ns() - tb0, 0);  // slots 3, 5, 7: barriers 0, 1, 2
+      }
+      named_bar_sync(1, NCT);
+    };
+    // ---- phase A: W1/W3 items
+    run_items(0, nAmine);
+    if (lane == 0) mstamp(P, kStAEnd, true);
+    grid_barrier(0, &a_done);
+    const uint64_t tF = P.diag ? globaltimer_ns() : 0;
+    // ---- h = silu(g) * u of every (row slot, 256 columns of the intermediate
+    // dimension), the K-chunk partials added in chunk order, kept in fp32 for
+    // the MXFP4 W2 loops and as integer records (X_hi + X_lo / 128 of h 2^si,
+    // max |h| 2^si in [2^13, 2^14), in the order of the expert's format, with
+    // the 16-column sums and 2^-si) for the others; 256 threads per unit
+    {
+      const float* pa = (const float*)(P.ws + P.L.m_pa);
+      float* hbuf = (float*)(P.ws + P.L.m_h);
+      const int nrs = nU > 0 ? s_rbase[nU] : 0;
+      const int nblk = I / 256, nunits = nrs * nblk;
+      const int half = ct >> 8, j = ct & 255;
+      __shared__ uint32_t s_hmx[2][8];
+      // (no abort test inside: the 256 threads of a half meet at named barriers)
+      for (int unit = cta + half * G; unit < nunits; unit += 2 * G) {
+        const int rs = unit / nblk, blk = unit - (unit / nblk) * nblk;
+        int u = 0;
+        while (u + 1 < nU && s_rbase[u + 1] <= rs) ++u;
+        const int i = blk * 256 + j, p = i >> 5, l = i & 31;
+        const float* src = pa + (((int64_t)rs * g.npanA + p) * g.nchA) * 2 * 32 + l;
+        float pg[8], pu[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          if (c < g.nchA) {
+            pg[c] = __ldcg(src + c * 64);
+            pu[c] = __ldcg(src + c * 64 + 32);
+          }
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          if (c < g.nchA) {
+            a0 += pg[c];
+            a1 += pu[c];
+          }
+        const float hv = silu_m(a0) * a1;
+        const int fmt = s_ufmt[u];
+        if (act_mode(1, fmt, P.variant) != kActInt) {
+          hbuf[(int64_t)rs * I + i] = hv;
+          continue;
+        }
+        const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(hv) & 0x7FFFFFFFu);
+        if (lane == 0) s_hmx[half][(ct >> 5) & 7] = mx;
+        named_bar_sync(3 + half, 256);
+        uint32_t bm = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) bm = max(bm, s_hmx[half][w]);
+        named_bar_sync(3 + half, 256);  // s_hmx is reused by the next unit
+        const int ex = (int)(bm >> 23);  // biased exponent of max |h| (0: all zero or subnormal)
+        const int si = ex == 0 ? 0 : min(max(13 - (ex - 127), -100), 100);
+        const int tq = fmt == BQE_FMT_TQ1;
+        const int ck = blk / bpcB, kb = blk - ck * bpcB;
+        uint8_t* rec = P.ws + P.L.m_hr + ((size_t)rs * g.nchB + ck) * int_rec_bytes(1, g.kcB);
+        if (j == 0) rec_put_scale(rec, tq, g.kcB, kb, ldexpf(1.0f, -si));
+        const float v = ldexpf(hv, si);
+        const int Xh = __float2int_rn(v);
+        const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
+        rec_put(rec, tq, g.kcB, kb, j, Xh, Xl);
+        if (tq && j < 16) rec_put_pad(rec, g.kcB, kb, j);
+        int ph = Xh, pl = Xl;
+#pragma unroll
+        for (int o = 8; o; o >>= 1) {
+          ph += __shfl_xor_sync(0xffffffffu, ph, o);
+          pl += __shfl_xor_sync(0xffffffffu, pl, o);
+        }
+        if ((lane & 15) == 0) rec_put_sums(rec, tq, g.kcB, kb, j >> 4, ph, pl);
+      }
+    }
+    if (P.diag && ct == 0) dacc(P, 4, globaltimer_ns() - tF, 0);  // slot 4: the h phase
+    grid_barrier(1, nullptr);
+    if (ct == 0) mbar_arrive(&fb_bar);  // the producers may copy h now
+    // ---- phase B: W2 items
+    run_items(nAmine, nmine);
+    if (lane == 0) mstamp(P, kStConsEnd, true);
+    grid_barrier(2, &b_done);
+    const uint64_t tC = P.diag ? globaltimer_ns() : 0;
+    // ---- out = y_shared + sum_j w_j y_j (W2 chunk partials added in chunk
+    // order, experts in a fixed order), one output element per thread
+    {
+      const float* pb = (const float*)(P.ws + P.L.m_pb);
+      const int n_out = M * H, per = (n_out + G - 1) / G;
+      const int lo = min(n_out, per * cta), hi = min(n_out, lo + per);
+      const int nj = nU > 1 ? K : 0;
+      // every partial of one output element loaded together when the shared
+      // expert plus the row's experts number <= 8 and W2 has <= 3 K chunks
+      const bool batched = nj + 1 <= 8 && g.nchB <= 3;
+      for (int e = lo + ct; e < hi && !s_abort; e += NCT) {
+        const int m = e / H, n = e - m * H;
+        float val = 0.f;
+        if (batched) {
+          float ys[8][3];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int rs = jj == 0 ? m : s_rs[m][jj > 0 ? jj - 1 : 0];
+#pragma unroll
+            for (int c = 0; c < 3; ++c)
+              if (jj <= nj && c < g.nchB) ys[jj][c] = __ldcg(pb + ((int64_t)rs * g.nchB + c) * H + n);
+          }
+#pragma unroll
+          for (int c = 0; c < 3; ++c)
+            if (c < g.nchB) val += ys[0][c];
+#pragma unroll
+          for (int jj = 1; jj < 8; ++jj) {
+            if (jj <= nj) {
+              float yj = 0.f;
+#pragma unroll
+              for (int c = 0; c < 3; ++c)
+                if (c < g.nchB) yj += ys[jj][c];
+              val = fmaf(s_cw[m][jj - 1], yj, val);
+            }
+          }
+        } else {
+          // expert by expert, in the same order
+          float ys[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (c < g.nchB) ys[c] = __ldcg(pb + ((int64_t)m * g.nchB + c) * H + n);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            if (c < g.nchB) val += ys[c];
+          for (int jj = 0; jj < nj; ++jj) {
+            const int rs = s_rs[m][jj];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              if (c < g.nchB) ys[c] = __ldcg(pb + ((int64_t)rs * g.nchB + c) * H + n);
+            float yj = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              if (c < g.nchB) yj += ys[c];
+            val = fmaf(s_cw[m][jj], yj, val);
+          }
+        }
+        P.out[e] = P.accumulate ? P.out[e] + val : val;
+      }
+      if (P.diag && ct == 0) dacc(P, 6, globaltimer_ns() - tC, 0);  // slot 6: the combine
+    }
+  } else {
+    // =============================== reducer ==================================
+    // Adds each item's task partials in a fixed order and writes them to the
+    // workspace, then frees the item's ring bytes; tells the compute warps
+    // when this CTA's W1/W3 and W2 partials are all written.
+    const bool ok0 = __all_sync(0xffffffffu, mwait(&route_bar, 0, P.limit_ns, err));
+    const int nU = ok0 ? s_nu : 0;
+    const int nTot = nU * (nAper + nBper), nA = nU * nAper;
+    const int nmine = cta < nTot ? (nTot - cta + G - 1) / G : 0;
+    const int nAmine = cta < nA ? (nA - cta + G - 1) / G : 0;
+    float* pa = (float*)(P.ws + P.L.m_pa);
+    float* pb = (float*)(P.ws + P.L.m_pb);
+    if (nAmine == 0 && lane == 0) mbar_arrive(&a_done);
+    for (int i = 0; i < nmine; ++i) {
+      const uint64_t tr = P.diag ? globaltimer_ns() : 0;
+      const bool okc = __all_sync(0xffffffffu, mwait(&cons[i % kNQ], (i / kNQ) & 1, P.limit_ns, err));
+      if (P.diag && lane == 0) dacc(P, 4, globaltimer_ns() - tr);
+      if (!okc || s_abort) {
+        if (lane == 0) {
+          set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+          s_abort = 1;
+        }
+        break;
+      }
+      const ItemHdr h = hdr[i % kNQ];
+      const float* red = reinterpret_cast<const float*>(ring + h.off + h.red);
+      const int u = h.u, R = h.R, rb = s_rbase[u];
+      if (h.phase == 0) {
+        // chunk partials of g and u for this panel (the f16 input's scale removed: exact power of two)
+        for (int r = 0; r < R; ++r) {
+          const int row = u == 0 ? r : s_urows[u * kMaxM + r];
+          const float unscale = h.amode == kActF16 ? s_xsc[row] : 1.0f;
+          float a0 = 0.f, a1 = 0.f;
+          for (int gi = 0; gi < g.GA; ++gi) {
+            a0 += red[(gi * R + r) * 32 + lane];
+            a1 += red[((g.GA + gi) * R + r) * 32 + lane];
+          }
+          const int64_t base = ((((int64_t)(rb + r) * g.npanA + h.p) * g.nchA + h.c) * 2) * 32;
+          pa[base + lane] = a0 * unscale;
+          pa[base + 32 + lane] = a1 * unscale;
+        }
+      } else {
+        for (int pi = 0; pi < P.PB; ++pi) {
+          const int n = (h.p * P.PB + pi) * 32 + lane;
+          for (int r = 0; r < R; ++r) {
+            float y = 0.f;
+            for (int gi = 0; gi < g.GB; ++gi) y += red[((pi * g.GB + gi) * R + r) * 32 + lane];
+            pb[((int64_t)(rb + r) * g.nchB + h.c) * H + n] = y;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&freed[i % kNQ]);  // the item's ring bytes may be reused
+        if (i + 1 == nAmine) mbar_arrive(&a_done);
+      }
+    }
+    if (lane == 0) mbar_arrive(&b_done);
+  }
+
+  // ---- end: after the last grid barrier every CTA has read this call's tag,
+  // so CTA 0 advances the epoch for the next call
+  __syncthreads();
+  if (tid == 0) {
+    mstamp(P, kStEnd, true);
+    dacc(P, 7, globaltimer_ns() - t_cta0);
+    if (cta == 0) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      *(volatile uint32_t*)(P.ws + P.L.epoch) = tag;
+    }
+  }
+}
+
+// W2 output panels per item: the largest count that divides the panels and
+// keeps the item at <= 8 compute tasks.
+static int moe_pb(const Geo& g) {
+  int best = 1;
+  for (int pb = 1; pb * g.GB <= 8; ++pb)
+    if (g.npanB % pb == 0) best = pb;
+  return best;
+}
+
+// Largest byte size of one item (MXFP4 tiles are the largest of the formats).
+static uint32_t moe_max_item(const Geo& g, int PB) {
+  auto a128 = [](uint32_t v) { return (v + 127u) & ~127u; };
+  const uint32_t actA = (uint32_t)int_rec_bytes(0, g.kcA) > (uint32_t)g.kcA * 4 ? int_rec_bytes(0, g.kcA) : g.kcA * 4;
+  const uint32_t actA2 = int_rec_bytes(1, g.kcA) > actA ? int_rec_bytes(1, g.kcA) : actA;
+  const uint32_t A = a128(2 * tile_bytes(BQE_FMT_MXFP4, g.kcA)) + a128(g.M * actA2) + 2 * g.GA * g.M * 128;
+  const uint32_t actB = int_rec_bytes(1, g.kcB) > (uint32_t)g.kcB * 4 ? int_rec_bytes(1, g.kcB) : g.kcB * 4;
+  const uint32_t B = a128(PB * tile_bytes(BQE_FMT_MXFP4, g.kcB)) + a128(g.M * actB) + PB * g.GB * g.M * 128;
+  return A > B ? A : B;
+}
+
+int launch_moe(const MoeParams& P0, int grid, cudaStream_t st) {
+  MoeParams P = P0;
+  const Geo& g = P.g;
+  if (g.E > kMaxEM || g.E > 4 * grid || g.H / 4 / 128 > 16 || g.H % 512 || g.I % 256 || g.K > kMaxTopK ||
+      g.U > kMaxU || 2 * g.nchA > 24 || (uint64_t)g.M * (g.K + 1) * g.nchB * int_rec_bytes(1, g.kcB) >= (1ull << 32))
+    return BQE_EUNSUPPORTED;
+  P.PB = moe_pb(g);
+  static int limit_set[2][64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BQE_ECUDA;
+  const int rc = g.M == 1 ? 0 : 1;
+  // one-row calls carry only the one-row inner loops; others take rows two at
+  // a time (four at a time would spill under this kernel's register budget)
+  void (*kfn)(MoeParams) = rc ? k_moe<2> : k_moe<1>;
+  int optin = 0;
+  cudaFuncAttributes fa;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaFuncGetAttributes(&fa, (const void*)kfn) != cudaSuccess)
+    return BQE_ECUDA;
+  const int dyn_max = optin - (int)fa.sharedSizeBytes;
+  const uint32_t zb = (4u * g.M * g.E + 127u) & ~127u;
+  if (dyn_max <= (int)zb) return BQE_EUNSUPPORTED;
+  P.ring_bytes = ((uint32_t)dyn_max - zb) & ~127u;
+  const uint32_t xst = ((uint32_t)g.M * g.H * 2 + 127u) & ~127u;
+  const uint32_t rtb = (uint32_t)((g.E + grid - 1) / grid) * g.H * 4;  // router rows of one CTA
+  if (P.ring_bytes < moe_max_item(g, P.PB) || P.ring_bytes < xst + rtb + 1024) return BQE_EUNSUPPORTED;
+  P.xstage_off = P.ring_bytes - xst;
+  P.rt_off = P.xstage_off - rtb;
+  if ((uint64_t)g.M * g.E * 4 > rtb) return BQE_EUNSUPPORTED;  // the selection keys reuse the router rows' room
+  // item index t -> (expert, panel, chunk) by multiply-high: exact while t * d < 2^32
+  auto mag = [](uint64_t d) { return (0x100000000ull + d - 1) / d; };
+  const uint32_t nAper = (uint32_t)g.npanA * g.nchA, nBper = (uint32_t)(g.npanB / P.PB) * g.nchB;
+  if ((uint64_t)g.U * (nAper + nBper) * (nAper > nBper ? nAper : nBper) >= (1ull << 32)) return BQE_EUNSUPPORTED;
+  P.magA = mag(nAper);
+  P.magA2 = mag(g.nchA);
+  P.magB = mag(nBper);
+  P.magB2 = mag(g.nchB);
+  if (limit_set[rc][dev] < dyn_max) {
+    if (cudaFuncSetAttribute((const void*)kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max) != cudaSuccess)
+      return BQE_ECUDA;
+    limit_set[rc][dev] = dyn_max;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMoeThreads);
+  cfg.dynamicSmemBytes = zb + P.ring_bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: CTAs wait on one another
+  at[0].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kfn, P) == cudaSuccess ? BQE_OK : BQE_ECUDA;
+}
+
+}  // namespace bqe

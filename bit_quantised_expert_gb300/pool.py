@@ -1,9 +1,10 @@
 """Slot pool: expert slots in one caller-owned device buffer.
 
-The pool is a torch uint8 tensor on the device (PyTorch provides the memory);
-each slot holds one expert (W1 | W3 | W2) in the device layout written by
-bqe_pool_pack_slot, at a 256-byte-aligned offset.  Two small device tables
-(slot byte offsets, slot formats) describe it to the kernels.
+PyTorch provides the memory (a uint8 tensor on the device); the library lays
+the pool out (bqe_pool_bytes / bqe_pool_init: the slot-offset and slot-format
+tables at the front, then every slot 256-byte aligned) and writes each expert
+into its slot in the device layout (bqe_pool_upload).  Nothing here computes
+offsets or sizes.
 """
 from __future__ import annotations
 
@@ -18,26 +19,22 @@ class SlotPool:
         self.d = d
         self.fmts = np.asarray(slot_fmts, dtype=np.int32)
         self.device = torch.device(device)
-        sizes = [_abi.bqe_expert_bytes(d, int(f)) for f in self.fmts]
-        if any(s == 0 for s in sizes):
+        nbytes = _abi.bqe_pool_bytes(d, self.fmts)
+        if nbytes == 0:
             raise ValueError("bad layer shape or slot format")
-        offs, o = [], 0
-        for s in sizes:
-            offs.append(o)
-            o += (s + 255) // 256 * 256
-        self.sizes = np.asarray(sizes, dtype=np.int64)
-        self.offsets = np.asarray(offs, dtype=np.int64)
-        self.nbytes = o
-        self.buf = torch.empty(max(o, 256), dtype=torch.uint8, device=self.device)
-        self.slot_off = torch.from_numpy(self.offsets.copy()).to(self.device)
-        self.slot_fmt = torch.from_numpy(self.fmts.copy()).to(self.device)
+        self.mem = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        self.pool = _abi.bqe_pool_init(d, self.fmts, self.mem, nbytes)
+        self.sizes = np.array([_abi.bqe_expert_bytes(d, int(f)) for f in self.fmts], dtype=np.int64)
         self._staging = None
 
     def __len__(self):
         return len(self.fmts)
 
     def slot_ptr(self, s: int) -> int:
-        return self.buf.data_ptr() + int(self.offsets[s])
+        """Device address of slot s, from the pool's own offset table."""
+        at = int(self.pool.slot_off) - self.mem.data_ptr()
+        off = self.mem[at:at + 8 * len(self.fmts)].view(torch.int64)[int(s)].item()
+        return int(self.pool.base) + int(off)
 
     def upload(self, s: int, canon, stream=None):
         """canon: canonical expert bytes (numpy uint8 on the host or a uint8 device tensor)."""
@@ -53,8 +50,7 @@ class SlotPool:
             src = canon
             if src.numel() != n:
                 raise ValueError("slot %d expects %d bytes, got %d" % (s, n, src.numel()))
-        _abi.bqe_pool_pack_slot(self.d, int(self.fmts[s]), src, self.slot_ptr(s), stream)
+        _abi.bqe_pool_upload(self.pool, self.d, int(s), src, stream)
 
     def cstruct(self) -> _abi.bqe_pool:
-        return _abi.bqe_pool(self.buf.data_ptr(), self.nbytes, self.slot_off.data_ptr(), self.slot_fmt.data_ptr(),
-                             len(self.fmts), 0)
+        return self.pool

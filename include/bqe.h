@@ -79,6 +79,18 @@ typedef struct {
   int32_t reserved;
 } bqe_pool;
 
+/* Accounting of one decode call (bqe_layer_stats): what it streamed.  The
+ * pages report the same kind of per-step account of where each token's
+ * experts came from (field report, section 3B: "experts: N hit, ..."). */
+typedef struct {
+  int32_t rows;              /* token rows of the call (M) */
+  int32_t experts_streamed;  /* distinct experts read, the shared one included */
+  int32_t per_format[5];     /* of those, how many in each format (index = BQE_FMT_*) */
+  int32_t row_uses;          /* (expert, row) pairs computed: sum over experts of the rows that chose it */
+  uint64_t expert_bytes;     /* packed bytes of those experts, each read once */
+  uint64_t router_bytes;     /* fp32 router weights read (n_experts x hidden x 4) */
+} bqe_stats;
+
 /* ---- formats (host only) ------------------------------------------------ */
 
 /* Weights and bytes of one block of `fmt`; 0 for an unknown format. */
@@ -108,6 +120,13 @@ int32_t bqe_scale_bytes(int32_t fmt);
 int bqe_pack(int32_t fmt, int32_t rows, int32_t cols, const uint8_t* codes,
              const uint8_t* scales, uint8_t* out);
 
+/* Host: the inverse of bqe_pack (a self-check of the format module, not a
+ * compute path): canonical blocks back to one code byte per weight and
+ * bqe_scale_bytes(fmt) scale bytes per block, in bqe_pack's conventions.
+ * BQE_EINVAL on a ternary byte above 242 (never written by bqe_pack). */
+int bqe_unpack_host(int32_t fmt, int32_t rows, int32_t cols, const uint8_t* packed, uint8_t* codes,
+                    uint8_t* scales);
+
 /* ---- pool --------------------------------------------------------------- */
 
 /* Device: rewrite one expert from canonical bytes (device, bqe_expert_bytes
@@ -118,6 +137,31 @@ int bqe_pack(int32_t fmt, int32_t rows, int32_t cols, const uint8_t* codes,
  * canonical bytes, rearranged. */
 int bqe_pool_pack_slot(const bqe_layer_desc* d, int32_t fmt, const void* canon_src,
                        void* slot_dst, void* stream);
+
+/* Bytes of device memory for a slot pool of n_slots experts with formats
+ * slot_fmt (host, n_slots entries): the slot-offset table (uint64), the
+ * slot-format table (int32), then every slot at a 256-byte-aligned offset,
+ * each part 256-byte aligned.  0 on a bad shape, count or format. */
+uint64_t bqe_pool_bytes(const bqe_layer_desc* d, int32_t n_slots, const int32_t* slot_fmt);
+
+/* Lay out a slot pool in caller-owned device memory dev_mem (256-byte
+ * aligned, dev_bytes >= bqe_pool_bytes): writes the two tables at its front
+ * (copies enqueued on `stream`; slot_fmt is host memory and may be released
+ * when the call returns) and fills *p (host struct) so that it describes the
+ * pool: base = the first slot, slot_off / slot_fmt = the device tables.  The
+ * library keeps no reference to dev_mem.  BQE_ENOSPC if dev_bytes is short,
+ * BQE_EINVAL on a bad argument. */
+int bqe_pool_init(bqe_pool* p, const bqe_layer_desc* d, int32_t n_slots, const int32_t* slot_fmt,
+                  void* dev_mem, uint64_t dev_bytes, void* stream);
+
+/* Write one expert into slot `slot` of a pool made by bqe_pool_init: its
+ * canonical bytes (device, bqe_expert_bytes(d, fmt of the slot): W1 | W3 |
+ * W2) are rewritten into the device layout (as bqe_pool_pack_slot).  The
+ * slot's offset and format are read back from the pool's tables, so the call
+ * synchronises `stream` once before enqueueing the rewrite.  BQE_EINVAL on a
+ * slot out of range or a table entry that does not fit the pool. */
+int bqe_pool_upload(const bqe_pool* p, const bqe_layer_desc* d, int32_t slot, const void* canon_dev,
+                    void* stream);
 
 /* Device: dequantise one rows x cols matrix stored in the device layout
  * (e.g. W1 of a slot: slot base; W3: + bqe_packed_bytes(fmt, inter, hidden);
@@ -259,6 +303,12 @@ int bqe_moe_layer_forward_noalloc(const bqe_layer_desc* d, int32_t M, const uint
                                   const int32_t* forced_idx, float* out, int32_t accumulate,
                                   int32_t* topk_idx, float* topk_w, int32_t* status_out,
                                   void* stream);
+
+/* After a decode call (bqe_moe_layer_forward, or the last layer of
+ * bqe_moe_step) on `ws`: synchronise `stream` and describe what the call
+ * streamed (bqe_stats, host).  BQE_EDEVICE if the workspace holds no valid
+ * work list (e.g. the call failed). */
+int bqe_layer_stats(const bqe_layer_desc* d, int32_t M, const void* ws, void* stream, bqe_stats* out);
 
 /* Synchronise `stream`, read the workspace error word and clear it.
  * Returns BQE_OK, BQE_EDEVICE or BQE_ETIMEOUT (detail: optional host int,
