@@ -5,24 +5,36 @@ Metric: MoE layer decode expert-byte GB/s = bytes of the distinct experts a
 call streams (each read once) / layer time, router included; also us/layer,
 tokens/s and the fraction of measured HBM bandwidth.
 
-Default workload: one DeepSeek-V4.1-Flash-shaped MoE layer, every expert
-MXFP4 (hidden 5120, inter 2304, 384 routed + 1 shared, top-6), M = 1 token
-row; seeded synthetic weights and activations generated on the device.
-Consecutive timed steps rotate over 4 independent layer instances (own
-router, shared and routed experts), so every step streams weights that are
-not in L2 (inputs larger than L2).  Other workloads: --workload mixed-m1 | mixed-m6 | step40-m1 | step40-m6,
-and --workload prefill (one mixed-format layer over 8192 tokens, tcgen05 grouped GEMMs; tokens/s and
-tensor TFLOP/s).
+Headline (`value`): one DeepSeek-V4.1-Flash-shaped MoE layer with every
+expert MXFP4 (hidden 5120, inter 2304, 384 routed + 1 shared, top-6) at M = 1
+token row, seeded synthetic weights and activations generated on the device.
+Consecutive timed steps rotate over 4 independent layer instances (own router,
+shared and routed experts) and a bank of 64 inputs, so every step streams
+weights that are not in L2 (inputs larger than L2).
+
+The default run adds sub-records, timed in interleaved rounds under the same
+clock record, each with us/layer as median and p10/p90 over its steps:
+  mixed_m1   mixed-format layers (ternary / Q2_0 / Q3_K experts in the weight
+             shares 42.8 / 39.2 / 18.0 %, Q2_0 shared, bias N(0, 0.25)), M = 1
+  mixed_m6   the same layers at M = 6 independent rows (a batched verify of
+             one token and five drafted ones)
+  step40_m1  40 chained layers over a 4288-slot pool with Zipf(1.0) routing,
+             one CUDA graph per step
+--workload picks one of them as the only (headline) record instead;
+--workload prefill times one mixed layer over 8192 tokens (tcgen05 grouped
+GEMMs: tokens/s and tensor TFLOP/s).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl bqe|reference]
 
 Under torchrun (N > 1) every rank runs an independent replica of the layer
 (replicas only: the decode layer has no exchange step); the time is the max
-over ranks and the value counts the bytes of all ranks.
+over ranks and the value counts the bytes of all ranks.  --impl reference
+times the fp64 oracle on the host cores instead (rank 0 only).
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import subprocess
@@ -33,11 +45,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-# DRAM bytes read + written per layer call by k_experts<0> and k_finalize_a on the MXFP4 M=1 layer
-# (ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/k_experts_decode_fp4_m1_E64.md), or None
-# while either kernel has changed since that capture.
-DECODE_FP4_M1_TRAFFIC = (87.86 + 1.69 + 0.67) * 1e6
-
+H, I, E, K = 5120, 2304, 384, 6
 METRIC = "MoE layer decode: expert-byte GB/s (% of HBM peak) and us/layer at M=1 and M=6"
 HBM_FALLBACK_GBS = 6800.0
 WORKLOADS = {
@@ -48,7 +56,27 @@ WORKLOADS = {
     "step40-m6": "dsv4flash-40-layer-step-4288-slot-pool-M6",
     "prefill": "dsv4flash-moe-layer-mixed-prefill-T8192-zipf0.8",
 }
+SUB_RECORDS = ("mixed-m1", "mixed-m6", "step40-m1")
 PREFILL_METRIC = "MoE layer prefill: tokens/s and expert-GEMM TFLOP/s at T=8192 (Zipf 0.8 routing)"
+
+# DRAM traffic of one decode-layer launch (k_moe) on the MXFP4 M=1 layer:
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of the kernel on a
+# 64-expert pool, plus the router rows of the 320 experts that pool lacks
+# (5120 x 4 bytes each; what a launch streams besides the router does not
+# depend on the pool size).  The figure holds only for the kernel sources
+# whose digest is recorded with it; after any change to them the bench
+# reports null until a new capture is taken.
+KERNEL_SOURCES = ("bit_quantised_expert_gb300/csrc/bqe_moe.cu", "bit_quantised_expert_gb300/csrc/bqe_gemv.cuh",
+                  "bit_quantised_expert_gb300/csrc/bqe_internal.cuh")
+TRAFFIC_FP4_M1 = dict(sha256=None, bytes=None)
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def parse():
@@ -57,21 +85,18 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["bqe", "reference"], default="bqe")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="fp4-m1")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=None,
+                    help="time only this workload as the headline (default: fp4-m1 plus the sub-records)")
+    ap.add_argument("--sub-steps", type=int, default=60, help="steps per sub-record, split over --rounds")
+    ap.add_argument("--rounds", type=int, default=3, help="interleaved rounds of the sub-records")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--soak-s", type=float, default=2.0, help="untimed load before timing, for clock samples")
-    ap.add_argument("--variant", type=int, default=1, help="MXFP4 W1/W3 inner loop: 0 fp32 FMA, 1 f16-input FMA")
     ap.add_argument("--instances", type=int, default=4, help="layer instances rotated so weights exceed L2")
-    ap.add_argument("--diag", action="store_true", help="print per-CTA cycle accounting of the expert kernels to stderr")
+    ap.add_argument("--diag", action="store_true", help="print a per-CTA timeline of one decode call to stderr")
     ap.add_argument("--experts", type=int, default=384,
                     help="routed experts in the pool (profiling a smaller pool; per-call work is unchanged)")
     ap.add_argument("--tokens", type=int, default=8192, help="prefill: token rows per call")
-    ap.add_argument("--panels", default=None, help="decode: max panels per work item, 'A,B' (diagnostic)")
-    ap.add_argument("--preload", default=None,
-                    help="decode: max shared-expert stages streamed before the wait, 'A,B' (diagnostic)")
-    ap.add_argument("--fused", action="store_true", help="decode: the single-kernel layer (bqe_set_fused)")
-    ap.add_argument("--cpu-oracle-sample", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -93,6 +118,17 @@ def tensor_peak():
             if j.get(k):
                 return float(j[k]), "measured %s" % k
     return 1700.0, "fallback sustained"
+
+
+def pct(v, q):
+    """q-th percentile (0..100) of v, linear between order statistics."""
+    v = sorted(v)
+    if not v:
+        return None
+    r = (len(v) - 1) * q / 100.0
+    lo = int(r)
+    hi = min(lo + 1, len(v) - 1)
+    return v[lo] + (v[hi] - v[lo]) * (r - lo)
 
 
 # ---------------------------------------------------------------- clocks
@@ -198,443 +234,512 @@ def replica_throughput(units_local, seconds_local, world):
 
 
 # ------------------------------------------------------------ CPU oracle
-def cpu_oracle_sample(workload: str, reps: int = 1):
-    """Time the oracle (as it stands) on a bounded sample of the workload on the
-    host cores.  Returns (expert bytes, seconds, sample description)."""
+# The oracle (fp64 numpy, as it stands) timed on the host cores: P worker
+# processes (spawned, never forked) each run one full call of the layer on
+# their own seeded inputs; the value counts the expert bytes of all P calls
+# over the wall time of the slowest.
+def _oracle_worker_init(workload: str, seed: int):
     import numpy as np
     import synth
-    from oracle import moe as O
-    rng = np.random.default_rng(12345)
-    H, I, E, K = 5120, 2304, 384, 6
+    global _ORACLE_CASE
+    rng = np.random.default_rng(12345 + seed)
     if workload == "prefill":
-        # two tokens of the prefill layer: router over both, 2 x (6 routed + shared) expert FFNs
+        # two tokens of the prefill layer: router over both, 6 routed + shared expert FFNs each
         fm = [synth.TQ1, synth.Q2_0, synth.Q3_K, synth.TQ1, synth.Q2_0, synth.TQ1, synth.Q2_0]
         experts = [synth.random_expert(rng, int(f), H, I) for f in fm]
         router = synth.router_weights(rng, E, H)
         x = synth.x_bf16(rng, 2, H)
         forced = np.array([[0, 1, 2, 3, 4, 5], [5, 4, 3, 2, 1, 0]], dtype=np.int32)
-        t0 = time.perf_counter()
-        for _ in range(reps):
-            O.prefill_rows(x, router, None, experts, np.array(fm, np.int32), H, I, K, 6, forced, [0, 1])
-        dt = (time.perf_counter() - t0) / reps
-        return 2, dt, ("two prefill tokens of the mixed layer (router over 384 experts, 6 routed + shared expert "
-                       "FFN each, experts dequantised once), fp64")
+        _ORACLE_CASE = ("prefill", x, router, experts, np.array(fm, np.int32), forced, 6)
+        return
     if workload.startswith("fp4"):
         fm = [synth.MXFP4] * 7
-        desc = "one MXFP4 layer call at M=1: router (384 x 5120 fp32) + 6 routed + 1 shared expert FFN, fp64"
     else:
         fm = [synth.TQ1, synth.TQ1, synth.TQ1, synth.Q2_0, synth.Q2_0, synth.Q3_K, synth.Q2_0]
-        desc = "one mixed-format layer call at M=1 (3 ternary, 2 Q2_0, 1 Q3_K routed + Q2_0 shared), fp64"
+    M = 6 if workload.endswith("m6") else 1
+    if M > 1:
+        # six independent rows touch up to 36 distinct routed experts; the
+        # sample keeps 12 of them (two per rank), each row choosing 6
+        fm = [fm[e % 6] for e in range(12)] + [synth.Q2_0]
+    nexp = len(fm) - 1
     experts = [synth.random_expert(rng, int(f), H, I) for f in fm]
     router = synth.router_weights(rng, E, H)
-    x = synth.x_bf16(rng, 1, H)
-    forced = np.arange(6, dtype=np.int32)[None, :]
-    nbytes = sum(synth.expert_bytes(int(f), H, I) for f in fm)
-    # the router scores all 384 experts; the 7 streamed experts are indices 0..6
-    fmts = np.array(fm, dtype=np.int32)
+    x = synth.x_bf16(rng, M, H)
+    forced = np.stack([(np.arange(K) + 2 * m) % nexp for m in range(M)]).astype(np.int32)
+    _ORACLE_CASE = ("decode", x, router, experts, np.array(fm, np.int32), forced, nexp)
+
+
+def _oracle_worker_run(_):
+    from oracle import moe as O
+    kind, x, router, experts, fmts, forced, nexp = _ORACLE_CASE
     t0 = time.perf_counter()
-    for _ in range(reps):
-        O.moe_layer(x, router, None, experts, fmts, H, I, K, 6, forced_idx=forced)
-    dt = (time.perf_counter() - t0) / reps
-    return nbytes, dt, desc
+    if kind == "prefill":
+        O.prefill_rows(x, router, None, experts, fmts, H, I, K, nexp, forced, [0, 1])
+    else:
+        O.moe_layer(x, router, None, experts, fmts, H, I, K, nexp, forced_idx=forced)
+    return time.perf_counter() - t0
+
+
+def _oracle_bytes(workload: str) -> int:
+    import synth
+    if workload.startswith("fp4"):
+        fm = [synth.MXFP4] * 7
+    else:
+        fm = [synth.TQ1, synth.TQ1, synth.TQ1, synth.Q2_0, synth.Q2_0, synth.Q3_K, synth.Q2_0]
+    if workload.endswith("m6"):
+        fm = [fm[e % 6] for e in range(12)] + [synth.Q2_0]
+    return sum(synth.expert_bytes(int(f), H, I) for f in fm)
+
+
+def _oracle_sample_desc(workload: str) -> str:
+    if workload == "prefill":
+        return ("two prefill tokens of the mixed layer (router over 384 experts, 6 routed + shared expert FFN "
+                "each), fp64")
+    if workload.startswith("fp4"):
+        return "one MXFP4 layer call at M=1 (router 384 x 5120 fp32, 6 routed + 1 shared expert FFN), fp64"
+    if workload.endswith("m6"):
+        return ("one mixed-format layer call at M=6 (router 384 x 5120 fp32, 6 routed experts per row among 12 "
+                "distinct ternary/Q2_0/Q3_K ones + Q2_0 shared), fp64")
+    return "one mixed-format layer call at M=1 (3 ternary, 2 Q2_0, 1 Q3_K routed + Q2_0 shared), fp64"
+
+
+def oracle_workers() -> int:
+    """Host cores to use, bounded so that every worker's fp64 expert copies
+    (about 3 GB for a layer call) fit in the available memory."""
+    n = os.cpu_count() or 1
+    try:
+        with open("/proc/meminfo") as fh:
+            for line in fh:
+                if line.startswith("MemAvailable:"):
+                    avail = int(line.split()[1]) * 1024
+                    n = min(n, max(1, int(avail // 3.5e9)))
+                    break
+    except OSError:
+        pass
+    return n
+
+
+class OraclePool:
+    """P spawned workers, each holding one seeded layer-call sample."""
+
+    def __init__(self, workload: str, n: int):
+        import multiprocessing as mp
+        self.n = n
+        self.ctx = mp.get_context("spawn")
+        self.pools = [self.ctx.Pool(1, initializer=_oracle_worker_init, initargs=(workload, i)) for i in range(n)]
+
+    def step(self):
+        """Every worker runs its call once; returns (wall seconds, per-call seconds)."""
+        t0 = time.perf_counter()
+        rs = [p.apply_async(_oracle_worker_run, (0,)) for p in self.pools]
+        per = [r.get() for r in rs]
+        return time.perf_counter() - t0, per
+
+    def close(self):
+        for p in self.pools:
+            p.close()
+        for p in self.pools:
+            p.join()
 
 
 def run_cpu_baseline(workload: str):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-oracle-sample", workload],
-                       capture_output=True, text=True, env=env, timeout=600)
-    if r.returncode != 0:
-        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
-    j = json.loads(r.stdout.strip().splitlines()[-1])
+    """The oracle on all usable host cores: two rounds of one layer call per
+    worker, after one untimed round (imports, first-touch of the weights)."""
+    # single-threaded BLAS inside each worker: the cores are used by the workers
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    n = oracle_workers()
+    pool = OraclePool(workload, n)
+    try:
+        pool.step()
+        walls = [pool.step()[0] for _ in range(2)]
+    finally:
+        pool.close()
+    T = sum(walls)
+    sample = "%s; %d worker processes (one per core, 1 BLAS thread each) x %d rounds, %.1f s" % (
+        _oracle_sample_desc(workload), n, len(walls), T)
     if workload == "prefill":
-        return {"value": j["bytes"] / j["seconds"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                "sample": j["sample"] + "; %.1f s, single thread" % j["seconds"]}
-    return {"value": j["bytes"] / j["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": j["sample"] + "; %.1f s, single thread" % j["seconds"]}
+        return {"value": round(n * len(walls) * 2 / T, 4), "unit": "tokens/s", "cores": n, "kind": "oracle",
+                "sample": sample}
+    return {"value": round(n * len(walls) * _oracle_bytes(workload) / T / 1e9, 5), "unit": "GB/s", "cores": n,
+            "kind": "oracle", "sample": sample}
 
 
 # ----------------------------------------------------------- GPU workloads
-def l2_bytes():
+class LayerCase:
+    """One decode workload resident on the device: layer instances, a bank of
+    inputs, a workspace and one CUDA graph per instance (events as graph
+    nodes around the layer call)."""
+
+    def __init__(self, A, dev, W, M, xs, name):
+        import torch
+        self.A, self.dev, self.W, self.M, self.name = A, dev, W, M, name
+        self.xs = xs                      # (n_x, M, H) int16 (bf16 bits)
+        self.n_x, self.NL = xs.shape[0], W.n_inst
+        self.nb = A.bqe_workspace_bytes(W.d, M)
+        self.ws = torch.empty(self.nb, dtype=torch.uint8, device=dev)
+        A.bqe_workspace_init(self.ws, self.nb)
+        self.pool = W.pool.cstruct()
+        self.out = torch.zeros(M, H, device=dev)
+        self.idx = torch.zeros(M, K, dtype=torch.int32, device=dev)
+        self.xbuf = torch.empty_like(xs[0])
+        self.ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+        self.times, self.bytes = [], []
+        self.launches = 0
+
+    def call(self, inst, ev=None, x=None, idx=None):
+        if ev:
+            ev[0].record()
+        W = self.W
+        self.A.bqe_moe_layer_forward(W.d, self.M, self.xbuf if x is None else x, W.wr[inst],
+                                     None if W.bias is None else W.bias[inst], self.pool, W.tables[inst], None,
+                                     self.out, 0, self.idx if idx is None else idx, None, self.ws, self.nb)
+        if ev:
+            ev[1].record()
+
+    def prepare(self, warm):
+        import torch
+        for i in range(warm):
+            self.xbuf.copy_(self.xs[i % self.n_x])
+            self.call(i % self.NL)
+        torch.cuda.synchronize()
+        self.check()
+        st = torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        side.wait_stream(st)
+        with torch.cuda.stream(side):
+            self.call(0)
+        st.wait_stream(side)
+        torch.cuda.synchronize()
+        self.graphs = []
+        for inst in range(self.NL):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.call(inst, self.ev)
+            self.graphs.append(g)
+        torch.cuda.synchronize()
+        self.step_no = 0
+
+    def check(self):
+        rc, det = self.A.bqe_check(self.ws)
+        assert rc == 0, (self.name, self.A.status_name(rc), det)
+
+    def soak(self, i):
+        self.xbuf.copy_(self.xs[i % self.n_x])
+        self.graphs[i % self.NL].replay()
+
+    def run(self, n):
+        """n timed steps; per step the layer time (graph events) and the expert
+        bytes of the distinct experts its routing chose."""
+        for _ in range(n):
+            s = self.step_no
+            inst = s % self.NL
+            self.xbuf.copy_(self.xs[s % self.n_x])
+            self.graphs[inst].replay()
+            self.ev[1].synchronize()
+            self.times.append(self.ev[0].elapsed_time(self.ev[1]) * 1e-3)
+            idx = self.idx.cpu().numpy()
+            us = set(int(e) for e in idx.reshape(-1)) | {self.W.E}
+            self.bytes.append(sum(self.W.expert_bytes(inst, e) for e in us))
+            self.launches += 1
+            self.step_no += 1
+
+
+class Step40Case:
+    """40 chained decode layers (bqe_moe_step) captured in one CUDA graph."""
+
+    def __init__(self, A, dev, M, name):
+        import torch
+        from synth import workloads as WL
+        self.A, self.dev, self.M, self.name = A, dev, M, name
+        self.S = S = WL.Step40(dev, m=M)
+        self.nb = A.bqe_workspace_bytes(S.d, M)
+        self.ws = torch.empty(self.nb, dtype=torch.uint8, device=dev)
+        A.bqe_workspace_init(self.ws, self.nb)
+        self.pool = S.pool.cstruct()
+        self.resid = torch.zeros(M, H, device=dev)
+        self.forced = torch.zeros(S.n_layers, M, K, dtype=torch.int32, device=dev)
+        self.nf = S.forced.shape[0]
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        self.times, self.bytes = [], []
+        self.launches = 0
+
+    def load(self, i):
+        self.forced.copy_(self.S.forced[i % self.nf])
+        self.resid.copy_(self.S.x0[i % self.nf])
+
+    def call(self):
+        S = self.S
+        self.A.bqe_moe_step(S.d, S.n_layers, self.M, self.resid, S.wr, None, self.pool, S.tables, self.forced, None,
+                            self.ws, self.nb)
+
+    def prepare(self, warm):
+        import torch
+        for i in range(max(warm, 1)):
+            self.load(i)
+            self.call()
+        torch.cuda.synchronize()
+        self.check()
+        st = torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        side.wait_stream(st)
+        with torch.cuda.stream(side):
+            self.call()
+        st.wait_stream(side)
+        torch.cuda.synchronize()
+        self.g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g):
+            self.call()
+        torch.cuda.synchronize()
+        self.step_no = 0
+
+    def check(self):
+        rc, det = self.A.bqe_check(self.ws)
+        assert rc == 0, (self.name, self.A.status_name(rc), det)
+
+    def soak(self, i):
+        self.load(i)
+        self.g.replay()
+
+    def run(self, n):
+        import torch
+        st = torch.cuda.current_stream()
+        L = self.S.n_layers
+        for _ in range(n):
+            s = self.step_no
+            self.load(s)
+            self.ev[0].record(st)
+            self.g.replay()
+            self.ev[1].record(st)
+            self.ev[1].synchronize()
+            self.times.append(self.ev[0].elapsed_time(self.ev[1]) * 1e-3 / L)  # per layer
+            self.bytes.append(sum(self.S.layer_bytes(l, s % self.nf) for l in range(L)) / L)
+            self.launches += L
+            self.step_no += 1
+
+
+def make_case(A, dev, workload, args, banks):
+    """The device workload of `workload`; `banks` shares layer sets between
+    the M = 1 and M = 6 mixed records (M = 1 takes each bank entry's first row)."""
+    from synth import workloads as WL
+    M = 6 if workload.endswith("m6") else 1
+    if workload.startswith("step40"):
+        return Step40Case(A, dev, M, workload)
+    kind = "fp4" if workload.startswith("fp4") else "mixed"
+    if kind not in banks:
+        m = 6 if kind == "mixed" else 1
+        banks[kind] = WL.LayerSet(dev, kind, args.instances, seed=1 if kind == "fp4" else 2, m=m, n_x=64,
+                                  n_experts=args.experts)
+    W = banks[kind]
+    xs = W.xs if W.m == M else W.xs[:, :M].contiguous()
+    return LayerCase(A, dev, W, M, xs, workload)
+
+
+def summary(case, hbm):
+    """us/layer as median and p10/p90 over the steps, expert-byte GB/s over
+    their sum, and the fraction of HBM."""
+    T, B = sum(case.times), sum(case.bytes)
+    gbs = B / T / 1e9
+    us = [t * 1e6 for t in case.times]
+    return dict(workload=WORKLOADS[case.name], M=case.M, steps=len(us),
+                us_per_layer_median=round(pct(us, 50), 3), us_per_layer_p10=round(pct(us, 10), 3),
+                us_per_layer_p90=round(pct(us, 90), 3), us_per_layer_mean=round(sum(us) / len(us), 3),
+                expert_gbs=round(gbs, 2), frac_of_hbm=round(gbs / hbm, 4),
+                expert_bytes_per_layer=round(B / len(us)), tokens_per_s=round(case.M * len(us) / T, 1))
+
+
+def soak(cases, seconds):
+    """Untimed load before timing, so the clock samples see the GPU busy."""
     import torch
-    return torch.cuda.get_device_properties(0).L2_cache_size
+    t_end = time.time() + seconds
+    i = 0
+    while time.time() < t_end:
+        for c in cases:
+            c.soak(i)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
 
 
-def run_layer(args, rank, world):
+def diag_timeline(A, case):
+    """Per-CTA timeline of one eager decode call (globaltimer stamps), to stderr."""
     import numpy as np
+    import torch
+    W, M = case.W, case.M
+    off = A.bqe_diag_offset(W.d, M)
+    dbg = case.ws[off:off + 8 * 3 * 1024 * 8].view(torch.int64).view(3, 1024, 8)
+    rows = []
+    for s_ in range(10):
+        dbg.zero_()
+        for k in (0, 2, 3, 5):
+            dbg[k >> 3, 1023, k & 7] = 2 ** 62
+        case.xbuf.copy_(case.xs[s_ % case.n_x])
+        A.bqe_set_diag(True)
+        try:
+            case.call(s_ % case.NL)
+        finally:
+            A.bqe_set_diag(False)
+        torch.cuda.synchronize()
+        d = dbg.cpu().numpy().astype(np.float64)
+        t0 = d[0, 1023, 0]
+        rows.append([(d[k >> 3, 1023, k & 7] - t0) / 1e3 for k in (1, 2, 10, 3, 4, 9, 6)])
+    case.check()
+    names = ["logits_published_max", "routing_known_min", "routing_known_max", "first_item_landed",
+             "last_w13_item_done", "last_compute_done", "end"]
+    tl = np.array(rows).mean(axis=0)
+    sys.stderr.write("DECODE_TIMELINE_us(from first CTA start) %s %s\n" % (case.name, json.dumps(
+        {n: round(float(v), 2) for n, v in zip(names, tl)})))
+
+
+def run_decode(args, rank, world):
     import torch
     from bit_quantised_expert_gb300 import buildlib
     buildlib.build()
     from bit_quantised_expert_gb300 import _abi as A
-    from synth import workloads as WL
-    import synth
 
     dev = torch.device("cuda", torch.cuda.current_device())
-    A.bqe_set_variant(args.variant)
-    if args.panels:
-        pa, pb = (int(v) for v in args.panels.split(","))
-        A.bqe_set_panels(pa, pb)
-    if args.preload is not None:
-        pa_, pb_ = (int(v) for v in args.preload.split(","))
-        A.bqe_set_preload(pa_, pb_)
-    if args.fused:
-        A.bqe_set_fused(True)
-    M = 6 if args.workload.endswith("m6") else 1
-    n_x = 64
-    NL = args.instances
-    kind = "fp4" if args.workload.startswith("fp4") else "mixed"
-    W = WL.LayerSet(dev, kind, NL, seed=1 if kind == "fp4" else 2, m=M, n_x=n_x, n_experts=args.experts)
-    d, K_ = W.d, 6
-    nb = A.bqe_workspace_bytes(d, M)
-    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
-    A.bqe_workspace_init(ws, nb)
-    pool = W.pool.cstruct()
-    out = torch.zeros(M, 5120, device=dev)
-    steps, warm = args.steps, args.warmup
-    idx_log = torch.zeros(max(steps, 1), M, K_, dtype=torch.int32, device=dev)
-    idx_tmp = torch.zeros(M, K_, dtype=torch.int32, device=dev)
-    st = torch.cuda.current_stream()
-    xbuf = torch.empty_like(W.xs[0])
-    xs = [W.xs[i] for i in range(n_x)]
-
-    def fused(inst, ev=None):
-        # the production call (the layer entry point), on the current stream
-        if ev:
-            ev[0].record()
-        A.bqe_moe_layer_forward(d, M, xbuf, W.wr[inst], None if W.bias is None else W.bias[inst], pool,
-                                W.tables[inst], None, out, 0, idx_tmp, None, ws, nb)
-        if ev:
-            ev[1].record()
-
-    def layer(inst, ev=None):
-        # the same layer as separate kernels: router + top-k, phase A, phase B
-        if ev:
-            ev[0].record()
-        A.bqe_route(d, M, xbuf, W.wr[inst], None if W.bias is None else W.bias[inst], pool, W.tables[inst], None,
-                    idx_tmp, None, ws, nb)
-        if ev:
-            ev[1].record()
-        A.bqe_experts_phase(d, M, pool, out, 0, 0, ws, nb)
-        if ev:
-            ev[2].record()
-        A.bqe_experts_phase(d, M, pool, out, 0, 1, ws, nb)
-        if ev:
-            ev[3].record()
-
-    for i in range(warm):
-        xbuf.copy_(xs[i % n_x])
-        layer(i % NL)
-    torch.cuda.synchronize()
-    rc, det = A.bqe_check(ws)
-    assert rc == 0, (A.status_name(rc), det)
-
-    # The timed unit is one layer replayed from a CUDA graph (the way a decode
-    # loop runs it).  Consecutive steps rotate over NL layer instances whose
-    # weights together are several times L2, so every step streams cold
-    # weights.  Timing events are nodes inside the graph.
-    gev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-    fev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-    graphs, fgraphs = [], []
-    side = torch.cuda.Stream()
-    side.wait_stream(st)
-    with torch.cuda.stream(side):
-        layer(0)
-        fused(0)
-    st.wait_stream(side)
-    torch.cuda.synchronize()
-    for inst in range(NL):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            layer(inst, gev)
-        graphs.append(g)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fused(inst, fev)
-        fgraphs.append(g)
-    torch.cuda.synchronize()
+    head_name = args.workload or "fp4-m1"
+    subs = [] if args.workload else list(SUB_RECORDS)
+    banks = {}
+    head = make_case(A, dev, head_name, args, banks)
+    subcases = [make_case(A, dev, w, args, banks) for w in subs]
+    warm = max(args.warmup, 3)
+    for c in [head] + subcases:
+        c.prepare(warm)
+    hbm, hbm_kind = peaks()
 
     clocks = ClockSampler(torch.cuda.current_device(), enabled=not args.no_clocks)
-    t_end = time.time() + args.soak_s
-    i = 0
-    while time.time() < t_end:  # untimed load so the clock samples see the GPU busy
-        xbuf.copy_(xs[i % n_x])
-        fgraphs[i % NL].replay()
-        i += 1
-        if i % 64 == 0:
-            torch.cuda.synchronize()
-    torch.cuda.synchronize()
-    t_route, t_a, t_b, t_split, t_layer = [], [], [], [], []
+    soak([head] + subcases, args.soak_s)
+    # headline: exactly K timed steps, bracketed by barrier + synchronize
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    for s_ in range(steps):
-        xbuf.copy_(xs[s_ % n_x])
-        fgraphs[s_ % NL].replay()
-        idx_log[s_].copy_(idx_tmp)
-        fev[1].synchronize()
-        t_layer.append(fev[0].elapsed_time(fev[1]) * 1e-3)
+    head.run(args.steps)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    # the same steps as separate kernels, for the per-kernel breakdown
-    for s_ in range(steps):
-        xbuf.copy_(xs[s_ % n_x])
-        graphs[s_ % NL].replay()
-        gev[3].synchronize()
-        t_route.append(gev[0].elapsed_time(gev[1]) * 1e-3)
-        t_a.append(gev[1].elapsed_time(gev[2]) * 1e-3)
-        t_b.append(gev[2].elapsed_time(gev[3]) * 1e-3)
-        t_split.append(gev[0].elapsed_time(gev[3]) * 1e-3)
+    barrier(world)
+    # sub-records: interleaved rounds, each workload a block of steps per round
+    R = max(1, args.rounds)
+    per = [args.sub_steps // R + (1 if r < args.sub_steps % R else 0) for r in range(R)]
+    for r in range(R):
+        for c in subcases:
+            torch.cuda.synchronize()
+            c.run(per[r])
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    rc, det = A.bqe_check(ws)
-    assert rc == 0, (A.status_name(rc), det)
+    for c in [head] + subcases:
+        c.check()
 
-    idx_np = idx_log.cpu().numpy()
-    bytes_e, bytes_a, bytes_b = [], [], []
-    for s_ in range(steps):
-        inst = s_ % NL
-        us = sorted(set(int(e) for e in idx_np[s_].reshape(-1)) | {W.E})
-        be = sum(W.expert_bytes(inst, e) for e in us)
-        ba = sum(2 * synth.matrix_bytes(int(W.fmts[W.slot(inst, e)]), 2304, 5120) for e in us)  # W1 + W3
-        bytes_e.append(be)
-        bytes_a.append(ba)
-        bytes_b.append(be - ba)
-    T = sum(t_layer)
-    T_max = reduce_max(T, world)
-    total_bytes = reduce_sum(float(sum(bytes_e)), world)
+    T_max = reduce_max(sum(head.times), world)
+    total_bytes = reduce_sum(float(sum(head.bytes)), world)
     value = total_bytes / T_max / 1e9
-    hbm, hbm_kind = peaks()
+    steps = args.steps
+    M = head.M
     mean = lambda v: sum(v) / len(v)  # noqa: E731
-    achieved_a = mean(bytes_a) / mean(t_a) / 1e9
-    router_bytes = W.E * 5120 * 4
-    achieved_l = (mean(bytes_e) + router_bytes) / mean(t_layer) / 1e9
     l2mb = torch.cuda.get_device_properties(0).L2_cache_size / 2 ** 20
+    if isinstance(head, LayerCase):
+        router_bytes = head.W.E * H * 4
+        cfg = dict(workload=WORKLOADS[head_name], hidden=H, inter=I, n_experts=head.W.E, top_k=K, n_shared=1, M=M,
+                   l2="inputs larger than L2: steps rotate over %d layer instances and 64 inputs (%.0f MB of "
+                      "weights streamed between reuses vs %.0f MB L2)" % (
+                          head.NL, (head.NL - 1) * mean(head.bytes) / 1e6, l2mb),
+                   parallelism="replicas" if world > 1 else "single-gpu")
+        kind = "mxfp4" if head_name.startswith("fp4") else "ternary/q2_0/q3_k"
+    else:
+        router_bytes = E * H * 4
+        cfg = dict(workload=WORKLOADS[head_name], layers=head.S.n_layers, slots=4288, M=M,
+                   l2="inputs larger than L2: each step streams ~3 GB",
+                   routing="Zipf(1.0) forced selection, weights from the router",
+                   parallelism="replicas" if world > 1 else "single-gpu")
+        kind = "ternary/q2_0/q3_k"
+    # roofline of the one kernel of the layer: all bytes it must read (the
+    # distinct experts and the fp32 router) over its CUDA-event duration
+    alg = mean(head.bytes) + router_bytes
+    achieved = alg / mean(head.times) / 1e9
+    traffic = None
+    if (head_name == "fp4-m1" and args.experts == E and TRAFFIC_FP4_M1["bytes"]
+            and TRAFFIC_FP4_M1["sha256"] == kernel_digest()):
+        traffic = TRAFFIC_FP4_M1["bytes"]
+    us = [t * 1e6 for t in head.times]
     res = dict(
-        metric=METRIC, value=round(value, 2), unit="GB/s", n_gpus=world, steps=steps, warmup=warm,
+        metric=METRIC, value=round(value, 2), unit="GB/s", n_gpus=world, steps=steps, warmup=args.warmup,
         ms_per_step=round(T_max / steps * 1e3, 5), higher_is_better=True, scaling="weak",
-        vs_baseline=None, dtype="fp32-accumulate over %s weights, bf16 activations" % (
-            "mxfp4" if kind == "fp4" else "ternary/q2_0/q3_k"),
-        data="synthetic (seeded, generated on the device)",
-        config=dict(workload=WORKLOADS[args.workload], hidden=5120, inter=2304, n_experts=W.E, top_k=6,
-                    n_shared=1, M=M,
-                    l2="inputs larger than L2: steps rotate over %d layer instances (%.0f MB of weights streamed "
-                       "between reuses vs %.0f MB L2)" % (NL, (NL - 1) * mean(bytes_e) / 1e6, l2mb),
-                    parallelism="replicas" if world > 1 else "single-gpu"),
-        us_per_layer=round(T_max / steps * 1e6, 3),
+        vs_baseline=None, dtype="fp32-accumulate over %s weights, bf16 activations" % kind,
+        data="synthetic (seeded, generated on the device)", config=cfg,
+        us_per_layer=round(T_max / steps * 1e6 / (head.S.n_layers if not isinstance(head, LayerCase) else 1), 3),
+        us_per_layer_median=round(pct(us, 50), 3), us_per_layer_p10=round(pct(us, 10), 3),
+        us_per_layer_p90=round(pct(us, 90), 3),
         tokens_per_s=round(M * steps * world / T_max, 1),
         frac_of_hbm=round(value / hbm, 4), hbm_peak_gbs=hbm, hbm_peak_kind=hbm_kind,
-        expert_bytes_per_step=round(mean(bytes_e)),
-        roofline=dict(bound="hbm", achieved=round(achieved_a, 1), peak=hbm, unit="GB/s",
-                      frac=round(achieved_a / hbm, 4),
-                      traffic=DECODE_FP4_M1_TRAFFIC if (args.workload == "fp4-m1" and not args.fused) else None,
-                      kernel="k_experts<0> + finalize (W1/W3 dequant-GEMV + SiLU-GLU)",
-                      algorithmic_bytes_per_launch=round(mean(bytes_a)),
-                      peak_kind="%s hbm_gbs (burst copy)" % hbm_kind,
-                      layer_achieved=round(achieved_l, 1), layer_frac=round(achieved_l / hbm, 4),
-                      layer_note="all bytes of the call (experts + router) / layer time"),
-        split_kernels=dict(
-            note="the same layer as separate kernels (router, W1/W3 + finalize, W2 + finalize)",
-            us_per_layer=round(mean(t_split) * 1e6, 3),
-            route_us=round(mean(t_route) * 1e6, 3), phase_a_us=round(mean(t_a) * 1e6, 3),
-            phase_b_us=round(mean(t_b) * 1e6, 3),
-            phase_a_gbs=round(achieved_a, 1), phase_b_gbs=round(mean(bytes_b) / mean(t_b) / 1e9, 1)),
-        gpu_launches=5 * steps,  # router, W1/W3 + its finalize, W2 + its finalize
-        variant=args.variant,
-        timing="CUDA-graph replay per step, events as graph nodes around the layer kernel",
+        expert_bytes_per_step=round(mean(head.bytes)),
+        roofline=dict(bound="hbm", achieved=round(achieved, 1), peak=hbm, unit="GB/s",
+                      frac=round(achieved / hbm, 4), traffic=traffic,
+                      kernel="k_moe (the whole decode layer: router, top-k, W1/W3, SiLU-GLU, W2, combine)",
+                      algorithmic_bytes_per_launch=round(alg),
+                      peak_kind="%s hbm_gbs (burst copy; the kernel is timed alone)" % hbm_kind),
+        gpu_launches=head.launches,
+        timing="CUDA-graph replay per step, CUDA events around the layer kernel on its stream",
         wall_s_timed_loop=round(wall, 4),
     )
+    if not isinstance(head, LayerCase):
+        res["ms_per_step"] = round(T_max / steps * head.S.n_layers * 1e3, 4)
+        res["cuda_graph"] = True
+    if subcases:
+        res["sub_records"] = {c.name.replace("-", "_"): summary(c, hbm) for c in subcases}
+        res["sub_records_timing"] = ("%d interleaved rounds after the headline steps, CUDA-graph replay, "
+                                     "events around each layer (step40: around the 40-layer graph, per layer)" % R)
+        res["sub_records_gpu_launches"] = sum(c.launches for c in subcases)
     if clk:
         res["clocks"] = clk
-
-    if args.diag and args.fused:
-        # timeline of the single-kernel layer (globaltimer stamps per CTA)
-        A.bqe_set_diag(True)
-        off = A.bqe_diag_offset(d, M)
-        tl = []
-        for s_ in range(10):
-            A.bqe_workspace_init(ws, nb)
-            dv = ws[off:off + 8 * 3 * 1024 * 8].view(torch.int64).view(3, 1024, 8)
-            dv[0, 1023, 0] = 2 ** 62
-            xbuf.copy_(xs[s_ % n_x])
-            fused(s_ % NL)
-            torch.cuda.synchronize()
-            a = dv[0].cpu().numpy().astype(np.float64)
-            t0 = a[1023, 0]
-            sms = torch.cuda.get_device_properties(0).multi_processor_count
-            rel = (a[:sms, :7] - t0) / 1e3
-            tl.append([[float(rel[:, k].min()), float(rel[:, k].mean()), float(rel[:, k].max())] for k in range(7)])
-        A.bqe_set_diag(False)
-        A.bqe_workspace_init(ws, nb)
-        tl = np.array(tl).mean(axis=0)
-        names = ["router_done", "logits_seen", "worklist_built", "consumers_done", "epilogue_done",
-                 "producer_done", "end"]
-        sys.stderr.write("FUSED_TIMELINE_us(min,mean,max) " + json.dumps(
-            {n: [round(v, 2) for v in tl[k]] for k, n in enumerate(names)}) + "\n")
-
-    if args.diag:
-        # per-CTA cycle accounting (a separate, untimed pass)
-        A.bqe_set_diag(True)
-        off = A.bqe_diag_offset(d, M)
-        nd = 20
-        spans = []
-        for s_ in range(nd):
-            A.bqe_workspace_init(ws, nb) if s_ == 0 else None
-            dv = ws[off:off + 8 * 3 * 1024 * 8].view(torch.int64).view(3, 1024, 8)
-            dv[:, 1023, 0] = 2 ** 62
-            dv[:, 1023, 1] = 0
-            dv[:2, 1023, 2] = 2 ** 62  # phases A, B: first and last CTA past the wait
-            dv[:2, 1023, 3] = 0
-            dv[2, 1023, 4] = 2 ** 62   # finalize kernels: first CTA past the wait, last CTA end
-            dv[2, 1023, 5] = 0
-            dv[2, 1023, 6] = 2 ** 62
-            dv[2, 1023, 7] = 0
-            xbuf.copy_(xs[s_ % n_x])
-            fused(s_ % NL)  # the layer entry point, eager: kernel parameters carry the diagnostic flag
-            torch.cuda.synchronize()
-            sp = dv[:, 1023, :].cpu().numpy().astype(np.float64)
-            t0 = sp[2, 0]
-            spans.append([(sp[k, 1] - sp[k, 0]) / 1e3 for k in (2, 0, 1)] +
-                         [(v - t0) / 1e3 for v in (sp[2, 1], sp[0, 0], sp[0, 2], sp[0, 3], sp[0, 1], sp[2, 4],
-                                                   sp[2, 5], sp[1, 0], sp[1, 2], sp[1, 3], sp[1, 1], sp[2, 6],
-                                                   sp[2, 7])])
-        A.bqe_set_diag(False)
-        dbg = ws[off:off + 8 * 3 * 1024 * 8].view(torch.int64).view(3, 1024, 8).cpu().numpy()
-        sms = torch.cuda.get_device_properties(0).multi_processor_count
-        names = ["prod_wait_empty", "prod_issue", "cons_wait_stage", "cons_wait_redbuf", "cons_compute",
-                 "epi_wait", "epi_work", "cta_total"]
-        rep = {}
-        for ph in range(2):
-            v = dbg[ph, :sms].astype(np.float64) / nd / 2.07e3  # us per call at 2.07 GHz
-            rep["phase_%d" % ph] = {n: [round(float(v[:, k].mean()), 2), round(float(v[:, k].max()), 2)]
-                                    for k, n in enumerate(names)}
-        ncta = (W.E + 1) // 2
-        vr = dbg[2, :ncta].astype(np.float64) / nd / 2.07e3
-        rep["router"] = {"cta_gemv_us": [round(float(vr[:, 0].mean()), 2), round(float(vr[:, 0].max()), 2)],
-                         "last_cta_total_us": round(float(dbg[2, 1022, 1]) / nd / 2.07e3, 2)}
-        rep["router_tail_stamps_us"] = [round(float(v) / nd / 2.07e3, 2) for v in dbg[2, 1021, :8]]
-        sp = np.array(spans)
-        rep["kernel_span_us(first CTA start -> last CTA end)"] = dict(
-            router=round(float(sp[:, 0].mean()), 2), phase_a=round(float(sp[:, 1].mean()), 2),
-            phase_b=round(float(sp[:, 2].mean()), 2))
-        tl_names = ["router_end", "A_start", "A_first_past_wait", "A_last_past_wait", "A_end", "finA_past_wait",
-                    "finA_end", "B_start", "B_first_past_wait", "B_last_past_wait", "B_end", "finB_past_wait",
-                    "finB_end"]
-        rep["timeline_us(from router start)"] = {n: round(float(sp[:, 3 + k].mean()), 2)
-                                                 for k, n in enumerate(tl_names)}
-        A.bqe_workspace_init(ws, nb)
-        sys.stderr.write("DIAG " + json.dumps(rep) + "\n")
+    if args.diag and isinstance(head, LayerCase):
+        diag_timeline(A, head)
+        for c in subcases:
+            if isinstance(c, LayerCase):
+                diag_timeline(A, c)
 
     # ---- end to end through the public call with host buffers --------------
-    xh = torch.empty(M, 5120, dtype=torch.int16).pin_memory()
-    oh = torch.empty(M, 5120, dtype=torch.float32).pin_memory()
-    xd = torch.empty(M, 5120, dtype=torch.int16, device=dev)
-    xs_host = [x.cpu() for x in xs]
-    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
-    for s_ in range(steps):
-        inst = s_ % NL
-        xh.copy_(xs_host[s_ % n_x])
-        e2e_ev[s_][0].record(st)
-        xd.copy_(xh, non_blocking=True)
-        A.bqe_moe_layer_forward(d, M, xd, W.wr[inst], None if W.bias is None else W.bias[inst], pool,
-                                W.tables[inst], None, out, 0, idx_log[s_], None, ws, nb)
-        oh.copy_(out, non_blocking=True)
-        e2e_ev[s_][1].record(st)
-    torch.cuda.synchronize()
-    Te = sum(e2e_ev[s_][0].elapsed_time(e2e_ev[s_][1]) * 1e-3 for s_ in range(steps))
-    idx_np = idx_log.cpu().numpy()
-    be2 = sum(sum(W.expert_bytes(s_ % NL, e) for e in (set(int(v) for v in idx_np[s_].reshape(-1)) | {W.E}))
-              for s_ in range(steps))
-    Te_max = reduce_max(Te, world)
-    res["e2e"] = dict(value=round(reduce_sum(float(be2), world) / Te_max / 1e9, 2), unit="GB/s",
-                      h2d_bytes_per_step=M * 5120 * 2, d2h_bytes_per_step=M * 5120 * 4,
-                      us_per_layer=round(Te_max / steps * 1e6, 3),
-                      note="eager calls through bqe_moe_layer_forward, pinned host x in, host out back")
+    if isinstance(head, LayerCase):
+        res["e2e"] = e2e_layer(A, dev, head, steps, world)
     return res
 
 
-def run_step40(args, rank, world):
+def e2e_layer(A, dev, case, steps, world):
+    """Eager calls of bqe_moe_layer_forward: every step copies its input from
+    pinned host memory and reads the output back into pinned host memory,
+    inside the timed region."""
     import torch
-    from bit_quantised_expert_gb300 import buildlib
-    buildlib.build()
-    from bit_quantised_expert_gb300 import _abi as A
-    from synth import workloads as WL
-
-    dev = torch.device("cuda", torch.cuda.current_device())
-    M = 6 if args.workload.endswith("m6") else 1
-    S = WL.Step40(dev, m=M)
-    d, L = S.d, S.n_layers
-    nb = A.bqe_workspace_bytes(d, M)
-    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
-    A.bqe_workspace_init(ws, nb)
-    pool = S.pool.cstruct()
-    resid = torch.zeros(M, 5120, device=dev)
-    forced = torch.zeros(L, M, 6, dtype=torch.int32, device=dev)
-    nf = S.forced.shape[0]
+    M = case.M
     st = torch.cuda.current_stream()
-
-    def load(i):
-        forced.copy_(S.forced[i % nf])
-        resid.copy_(S.x0[i % nf])
-
-    def run():
-        # the current stream: inside graph capture this is the capture stream
-        A.bqe_moe_step(d, L, M, resid, S.wr, None, pool, S.tables, forced, None, ws, nb)
-
-    for i in range(max(args.warmup, 3)):
-        load(i)
-        run()
+    xh = torch.empty(M, H, dtype=torch.int16).pin_memory()
+    oh = torch.empty(M, H, dtype=torch.float32).pin_memory()
+    xd = torch.empty(M, H, dtype=torch.int16, device=dev)
+    xs_host = [x.cpu() for x in case.xs]
+    idx_log = torch.zeros(steps, M, K, dtype=torch.int32, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for s_ in range(3):
+        xd.copy_(xs_host[s_ % case.n_x].to(dev))
+        case.call(s_ % case.NL, x=xd)
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream()
-    side.wait_stream(st)
-    with torch.cuda.stream(side):
-        run()
-    st.wait_stream(side)
+    for s_ in range(steps):
+        xh.copy_(xs_host[s_ % case.n_x])
+        ev[s_][0].record(st)
+        xd.copy_(xh, non_blocking=True)
+        case.call(s_ % case.NL, x=xd, idx=idx_log[s_])
+        oh.copy_(case.out, non_blocking=True)
+        ev[s_][1].record(st)
     torch.cuda.synchronize()
-    with torch.cuda.graph(g):
-        run()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(torch.cuda.current_device(), enabled=not args.no_clocks)
-    t_end = time.time() + args.soak_s
-    i = 0
-    while time.time() < t_end:
-        load(i)
-        g.replay()
-        i += 1
-    torch.cuda.synchronize()
-    steps = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
-    barrier(world)
-    for s in range(steps):
-        load(s)
-        evs[s][0].record(st)
-        g.replay()
-        evs[s][1].record(st)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    rc, det = A.bqe_check(ws)
-    assert rc == 0, (A.status_name(rc), det)
-    ts = [evs[s][0].elapsed_time(evs[s][1]) * 1e-3 for s in range(steps)]
-    by = [sum(S.layer_bytes(l, s % nf) for l in range(L)) for s in range(steps)]
-    T = reduce_max(sum(ts), world)
-    tot = reduce_sum(float(sum(by)), world)
-    hbm, hbm_kind = peaks()
-    value = tot / T / 1e9
-    res = dict(metric=METRIC, value=round(value, 2), unit="GB/s", n_gpus=world, steps=steps, warmup=args.warmup,
-               ms_per_step=round(T / steps * 1e3, 4), higher_is_better=True, scaling="weak", vs_baseline=None,
-               dtype="fp32-accumulate over ternary/q2_0/q3_k weights, bf16 activations",
-               data="synthetic (seeded, generated on the device)",
-               config=dict(workload=WORKLOADS[args.workload], layers=L, slots=4288, M=M,
-                           l2="not flushed: each step streams ~3 GB, far above L2",
-                           routing="Zipf(1.0) forced selection, scores from the router",
-                           parallelism="replicas" if world > 1 else "single-gpu"),
-               us_per_layer=round(T / steps / L * 1e6, 3), tokens_per_s=round(M * steps * world / T, 1),
-               frac_of_hbm=round(value / hbm, 4), hbm_peak_gbs=hbm, expert_bytes_per_step=round(sum(by) / steps),
-               gpu_launches=3 * L * steps, cuda_graph=True)
-    if clk:
-        res["clocks"] = clk
-    return res
+    case.check()
+    Te = sum(ev[s_][0].elapsed_time(ev[s_][1]) * 1e-3 for s_ in range(steps))
+    idx_np = idx_log.cpu().numpy()
+    be = sum(sum(case.W.expert_bytes(s_ % case.NL, e) for e in (set(int(v) for v in idx_np[s_].reshape(-1)) |
+                                                                 {case.W.E})) for s_ in range(steps))
+    Te_max = reduce_max(Te, world)
+    return dict(value=round(reduce_sum(float(be), world) / Te_max / 1e9, 2), unit="GB/s",
+                h2d_bytes_per_step=M * H * 2, d2h_bytes_per_step=M * H * 4,
+                us_per_layer=round(Te_max / steps * 1e6, 3),
+                note="eager calls through bqe_moe_layer_forward, pinned host x in, host out back")
 
 
 def run_prefill(args, rank, world):
@@ -758,56 +863,48 @@ def run_prefill(args, rank, world):
 
 
 def run_reference(args, rank, world):
-    """The oracle (fp64, as it stands) on the host cores, one bounded sample per step."""
+    """The oracle (fp64, as it stands) on the host cores: each step, every
+    worker process runs one full call of the headline layer on its own seeded
+    inputs (rank 0 only)."""
     if rank != 0:
         return None
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ.setdefault(k, "1")  # before numpy loads its BLAS: report the threads really used
-    import numpy as np
-    import synth
-    from oracle import formats as F
-    from oracle import moe as O
-    rng = np.random.default_rng(777)
-    fmt = synth.MXFP4 if args.workload.startswith("fp4") else synth.Q2_0
-    H, I = 5120, 2304
-    ex = synth.random_expert(rng, fmt, H, I)
-    x = synth.x_bf16(rng, 1, H)
-    nbytes = synth.expert_bytes(fmt, H, I)
-
-    def step():
-        w1, w3, w2 = F.dequant_expert(fmt, ex, H, I)
-        O.expert_ffn(O.bf16_bits_to_f64(x), w1, w3, w2)
-
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    T = time.perf_counter() - t0
-    value = nbytes * args.steps / T / 1e9
-    sample = "one expert FFN (%s, %d bytes) per step at M=1 in fp64 numpy" % (synth.FMT_NAMES[fmt], nbytes)
-    return dict(metric=METRIC, value=round(value, 4), unit="GB/s", n_gpus=world, steps=args.steps,
+        os.environ[k] = "1"
+    workload = args.workload or "fp4-m1"
+    if workload.startswith("step40"):
+        workload = "mixed-m1"  # one layer of the step: the sample unit of the per-layer metric
+    n = oracle_workers()
+    pool = OraclePool(workload, n)
+    try:
+        for _ in range(args.warmup):
+            pool.step()
+        walls = [pool.step()[0] for _ in range(args.steps)]
+    finally:
+        pool.close()
+    T = sum(walls)
+    sample = "%s; %d worker processes (one per core, 1 BLAS thread each) per step" % (
+        _oracle_sample_desc(workload), n)
+    if workload == "prefill":
+        value = n * 2 * args.steps / T
+        return dict(metric=PREFILL_METRIC, value=round(value, 4), unit="tokens/s", n_gpus=world,
+                    steps=args.steps, warmup=args.warmup, ms_per_step=round(T / args.steps * 1e3, 3),
+                    higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic (seeded)",
+                    impl="reference", config=dict(workload=WORKLOADS[workload], hidden=H, inter=I, n_experts=E,
+                                                  top_k=K, n_shared=1, T=2),
+                    cpu_baseline=dict(value=round(value, 4), unit="tokens/s", cores=n, kind="oracle", sample=sample),
+                    e2e=dict(value=round(value, 4), unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    value = n * _oracle_bytes(workload) * args.steps / T / 1e9
+    return dict(metric=METRIC, value=round(value, 5), unit="GB/s", n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=round(T / args.steps * 1e3, 3), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic (seeded)", impl="reference",
-                config=dict(workload=WORKLOADS[args.workload], M=1),
-                cpu_baseline=dict(value=round(value, 4), unit="GB/s", cores=_threads_used(), kind="oracle",
-                                  sample=sample),
-                e2e=dict(value=round(value, 4), unit="GB/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
-
-
-def _threads_used():
-    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
-        if os.environ.get(k):
-            return int(os.environ[k])
-    return os.cpu_count() or 1
+                config=dict(workload=WORKLOADS[workload], hidden=H, inter=I, n_experts=E, top_k=K, n_shared=1,
+                            M=6 if workload.endswith("m6") else 1),
+                cpu_baseline=dict(value=round(value, 5), unit="GB/s", cores=n, kind="oracle", sample=sample),
+                e2e=dict(value=round(value, 5), unit="GB/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
 
 
 def main():
     args = parse()
-    if args.cpu_oracle_sample:
-        nbytes, dt, desc = cpu_oracle_sample(args.cpu_oracle_sample)
-        print(json.dumps(dict(bytes=nbytes, seconds=dt, sample=desc)))
-        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
@@ -816,14 +913,12 @@ def main():
             print(json.dumps(res))
         return
     rank, world, local = dist_setup(args.gpus)
-    if args.workload.startswith("step40"):
-        res = run_step40(args, rank, world)
-    elif args.workload == "prefill":
+    if args.workload == "prefill":
         res = run_prefill(args, rank, world)
     else:
-        res = run_layer(args, rank, world)
+        res = run_decode(args, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = run_cpu_baseline(args.workload)
+        res["cpu_baseline"] = run_cpu_baseline("prefill" if args.workload == "prefill" else (args.workload or "fp4-m1"))
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

@@ -72,26 +72,20 @@ SIGNATURES = {
     "bqe_workspace_init": (ctypes.c_int, [_P, _U64, _P]),
     "bqe_moe_layer_forward": (ctypes.c_int, [_DESC, _I32, _P, _P, _P, _POOL, _P, _P, _P, _I32, _P, _P, _P, _U64, _P]),
     "bqe_route": (ctypes.c_int, [_DESC, _I32, _P, _P, _P, _POOL, _P, _P, _P, _P, _P, _U64, _P]),
-    "bqe_experts": (ctypes.c_int, [_DESC, _I32, _POOL, _P, _I32, _P, _U64, _P]),
-    "bqe_experts_phase": (ctypes.c_int, [_DESC, _I32, _POOL, _P, _I32, _I32, _P, _U64, _P]),
     "bqe_moe_layer_forward_noalloc": (ctypes.c_int, [_DESC, _I32, _P, _P, _P, _POOL, _P, _P, _P, _I32, _P, _P, _P,
                                                      _P]),
     "bqe_prefill_workspace_bytes": (_U64, [_DESC, _I32]),
     "bqe_moe_prefill": (ctypes.c_int, [_DESC, _I32, _P, _P, _P, _POOL, _P, _P, _P, _I32, _P, _P, _P, _U64, _P]),
     "bqe_moe_step": (ctypes.c_int, [_DESC, _I32, _I32, _P, _P, _P, _POOL, _P, _P, _P, _P, _U64, _P]),
     "bqe_check": (ctypes.c_int, [_P, _P, ctypes.POINTER(_I32)]),
+    "bqe_check_noalloc": (ctypes.c_int, [_P, ctypes.POINTER(_I32)]),
     "bqe_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "bqe_set_wait_limit_ns": (None, [_U64]),
-    "bqe_set_pdl": (None, [ctypes.c_int]),
     "bqe_set_test_drop_item": (None, [_I32]),
-    "bqe_set_variant": (None, [_I32]),
     "bqe_set_prefill_f16": (None, [_I32]),
-    "bqe_set_panels": (None, [_I32, _I32]),
-    "bqe_set_preload": (None, [_I32, _I32]),
     "bqe_prefill_kernel_ms": (ctypes.c_int, [_P]),
     "bqe_prefill_diag_offset": (_U64, [_DESC, _I32]),
     "bqe_set_diag": (None, [_I32]),
-    "bqe_set_fused": (None, [_I32]),
     "bqe_diag_offset": (_U64, [_DESC, _I32]),
 }
 
@@ -249,16 +243,6 @@ def bqe_route(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, topk_id
                       stream_ptr(stream)), "bqe_route")
 
 
-def bqe_experts(d, M, pool, out, accumulate, ws, ws_bytes, stream=None) -> None:
-    _ok(lib.bqe_experts(ctypes.byref(d), M, ctypes.byref(pool), ptr(out), int(accumulate), ptr(ws), ws_bytes,
-                        stream_ptr(stream)), "bqe_experts")
-
-
-def bqe_experts_phase(d, M, pool, out, accumulate, phase, ws, ws_bytes, stream=None) -> None:
-    _ok(lib.bqe_experts_phase(ctypes.byref(d), M, ctypes.byref(pool), ptr(out), int(accumulate), int(phase), ptr(ws),
-                              ws_bytes, stream_ptr(stream)), "bqe_experts_phase")
-
-
 def bqe_moe_step(d, n_layers, M, resid, router_w, sel_bias, pool, slot_tables, forced_idx, t_out, ws, ws_bytes,
                  stream=None) -> None:
     _ok(lib.bqe_moe_step(ctypes.byref(d), n_layers, M, ptr(resid), ptr(router_w), ptr(sel_bias), ctypes.byref(pool),
@@ -273,20 +257,19 @@ def bqe_check(ws, stream=None) -> tuple[int, int]:
     return rc, det.value
 
 
+def bqe_check_noalloc(stream=None) -> tuple[int, int]:
+    """The no-allocation entry point's error word: (status, detail) without raising."""
+    det = _I32(0)
+    rc = lib.bqe_check_noalloc(stream_ptr(stream), ctypes.byref(det))
+    return rc, det.value
+
+
 def bqe_set_wait_limit_ns(ns: int) -> None:
     lib.bqe_set_wait_limit_ns(int(ns))
 
 
-def bqe_set_pdl(on: bool) -> None:
-    lib.bqe_set_pdl(1 if on else 0)
-
-
 def bqe_set_test_drop_item(item: int) -> None:
     lib.bqe_set_test_drop_item(int(item))
-
-
-def bqe_set_variant(v: int) -> None:
-    lib.bqe_set_variant(int(v))
 
 
 def bqe_set_diag(on: bool) -> None:
@@ -295,18 +278,6 @@ def bqe_set_diag(on: bool) -> None:
 
 def bqe_diag_offset(d, M: int) -> int:
     return lib.bqe_diag_offset(ctypes.byref(d), M)
-
-
-def bqe_set_fused(on: bool) -> None:
-    lib.bqe_set_fused(1 if on else 0)
-
-
-def bqe_set_panels(max_a: int, max_b: int) -> None:
-    lib.bqe_set_panels(int(max_a), int(max_b))
-
-
-def bqe_set_preload(n_a: int, n_b: int) -> None:
-    lib.bqe_set_preload(int(n_a), int(n_b))
 
 
 def bqe_set_prefill_f16(on: bool) -> None:

@@ -1,6 +1,6 @@
 // bqe_api.cu — host entry points of the decode path: argument checks,
-// workspace geometry, kernel launches (stream-ordered, programmatic
-// dependent launch between the kernels of a layer and across layers).
+// workspace geometry, and the launches (stream-ordered: one persistent kernel
+// per layer; the chained step launches one per layer).
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -10,41 +10,17 @@
 
 using namespace bqe;
 
+// Process-wide settings for diagnostics and tests (not part of the operation;
+// read at each launch, not synchronised with launches in other threads).
 static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};  // 2 s per wait
-static std::atomic<int> g_use_pdl{1};
 static std::atomic<int> g_drop_item{-1};
-static std::atomic<int> g_variant{1};
 static std::atomic<int> g_diag{0};
-static std::atomic<int> g_fused{1};
 static std::atomic<int> g_pf_f16{1};
-static std::atomic<int> g_pmax_a{0}, g_pmax_b{0};
-static std::atomic<int> g_preload_a{16}, g_preload_b{16};
 
-// Diagnostic knobs (not part of the operation): the bound on every in-kernel
-// wait, and whether kernels are chained with programmatic dependent launch.
 extern "C" void bqe_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
-extern "C" void bqe_set_pdl(int on) { g_use_pdl = on ? 1 : 0; }
 extern "C" void bqe_set_test_drop_item(int32_t item) { g_drop_item = item; }
-extern "C" void bqe_set_variant(int32_t v) { g_variant = v; }
 extern "C" void bqe_set_diag(int32_t on) { g_diag = on ? 1 : 0; }
-extern "C" void bqe_set_fused(int32_t on) { g_fused = on ? 1 : 0; }
 extern "C" void bqe_set_prefill_f16(int32_t on) { g_pf_f16 = on ? 1 : 0; }
-extern "C" void bqe_set_preload(int32_t n_a, int32_t n_b) {
-  g_preload_a = n_a < 0 ? 0 : n_a;
-  g_preload_b = n_b < 0 ? 0 : n_b;
-}
-extern "C" void bqe_set_panels(int32_t max_a, int32_t max_b) {
-  g_pmax_a = max_a > 0 ? max_a : 0;
-  g_pmax_b = max_b > 0 ? max_b : 0;
-}
-
-// Largest panel count <= cap that divides npan (cap 0: keep P).
-static int cap_panels(int P, int npan, int cap) {
-  if (cap <= 0) return P;
-  if (P > cap) P = cap;
-  while (P > 1 && npan % P) --P;
-  return P;
-}
 
 static int device_sms() {
   static int cache[64] = {0};
@@ -61,7 +37,7 @@ static int device_sms() {
 static bool desc_ok(const bqe_layer_desc* d) {
   return d && d->hidden > 0 && d->inter > 0 && d->hidden % 256 == 0 && d->inter % 256 == 0 && d->n_experts > 0 &&
          d->n_experts <= 512 && d->top_k > 0 && d->top_k <= kMaxTopK && d->top_k <= d->n_experts &&
-         d->n_shared == 1 && d->top_k <= 32;
+         d->n_shared == 1;
 }
 
 static Geo geo_of(const bqe_layer_desc* d, int M) { return make_geo(d->hidden, d->inter, d->n_experts, d->top_k, M); }
@@ -86,11 +62,23 @@ static int check_pool(const bqe_pool* p) {
   return BQE_OK;
 }
 
-static int route_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* resid, uint16_t* t_out,
-                        const float* router_w, const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
+namespace bqe {
+// Host-side checks of a decode-layer call (everything but the workspace): the
+// same for the workspace and the no-allocation entry points, made before
+// anything is enqueued.
+int check_layer_args(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* resid, const float* router_w,
+                     const bqe_pool* pool, const int32_t* slot_table, const float* out) {
+  if (!desc_ok(d) || M < 1 || M > kMaxM || (!x && !resid) || !router_w || !slot_table || !out) return BQE_EINVAL;
+  if (((uintptr_t)router_w & 15) || (x && ((uintptr_t)x & 15)) || d->hidden % 512) return BQE_EINVAL;
+  return check_pool(pool);
+}
+}  // namespace bqe
+
+static int route_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w,
+                        const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
                         const int32_t* forced_idx, int32_t* topk_idx, float* topk_w, void* ws, uint64_t ws_bytes,
                         cudaStream_t st) {
-  if (!desc_ok(d) || M < 1 || M > kMaxM || (!x && !resid) || !router_w || !slot_table || !ws) return BQE_EINVAL;
+  if (!desc_ok(d) || M < 1 || M > kMaxM || !x || !router_w || !slot_table || !ws) return BQE_EINVAL;
   if (((uintptr_t)ws & 255) || ((uintptr_t)router_w & 15)) return BQE_EINVAL;
   int rc = check_pool(pool);
   if (rc) return rc;
@@ -102,8 +90,8 @@ static int route_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, c
   P.L = L;
   P.ws = (uint8_t*)ws;
   P.x = x;
-  P.resid = resid;
-  P.t_out = t_out;
+  P.resid = nullptr;
+  P.t_out = nullptr;
   P.router_w = router_w;
   P.bias = sel_bias;
   P.forced = forced_idx;
@@ -111,119 +99,26 @@ static int route_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, c
   P.pool = *pool;
   P.topk_idx = topk_idx;
   P.topk_w = topk_w;
-  P.diag = g_diag.load();
-  return launch_route(P, st, g_use_pdl.load() != 0);
-}
-
-// slot_table (optional): the layer's slot table, from which the expert kernels
-// read the shared expert's slot so they can stream its weights in early.
-static int experts_common(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out, int32_t accumulate,
-                          void* ws, uint64_t ws_bytes, cudaStream_t st, int only_phase = -1,
-                          const int32_t* slot_table = nullptr) {
-  if (!desc_ok(d) || M < 1 || M > kMaxM || !out || !ws || ((uintptr_t)ws & 255)) return BQE_EINVAL;
-  int rc = check_pool(pool);
-  if (rc) return rc;
-  Geo g = geo_of(d, M);
-  WsLayout L = make_ws(g);
-  if (ws_bytes < L.total) return BQE_ENOSPC;
-  const int sms = device_sms();
-  if (sms <= 0) return BQE_ECUDA;
-  g.PA = cap_panels(g.PA, g.npanA, g_pmax_a.load());  // diagnostic override; the layout does not depend on it
-  g.PB = cap_panels(g.PB, g.npanB, g_pmax_b.load());
-  ExpParams P;
-  P.g = g;
-  P.L = L;
-  P.ws = (uint8_t*)ws;
-  P.out = out;
-  P.accumulate = accumulate ? 1 : 0;
-  P.limit_ns = g_wait_limit_ns.load();
-  P.drop_item = g_drop_item.load();
-  P.variant = g_variant.load();
-  P.diag = g_diag.load();
-  P.slot_table = slot_table;
-  P.pool = *pool;
-  P.max_pre = 0;
-  const bool pdl = g_use_pdl.load() != 0;
-  for (int phase = 0; phase < 2; ++phase) {
-    if (only_phase >= 0 && phase != only_phase) continue;
-    int ns = 0;
-    experts_smem_bytes(g, phase, &ns);
-    if (ns < 2) return BQE_EUNSUPPORTED;
-    P.nstages = ns;
-    P.max_pre = phase == 0 ? g_preload_a.load() : g_preload_b.load();
-    if ((rc = launch_experts(P, phase, sms, st, pdl))) return rc;
-    if ((rc = launch_finalize(P, phase, sms, st, pdl))) return rc;
-  }
-  return BQE_OK;
+  P.diag = 0;
+  return launch_route(P, st, false);
 }
 
 extern "C" int bqe_route(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w,
                          const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
                          const int32_t* forced_idx, int32_t* topk_idx, float* topk_w, void* ws, uint64_t ws_bytes,
                          void* stream) {
-  if (!x) return BQE_EINVAL;
-  return route_common(d, M, x, nullptr, nullptr, router_w, sel_bias, pool, slot_table, forced_idx, topk_idx, topk_w,
-                      ws, ws_bytes, (cudaStream_t)stream);
-}
-
-extern "C" int bqe_experts(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out,
-                           int32_t accumulate, void* ws, uint64_t ws_bytes, void* stream) {
-  return experts_common(d, M, pool, out, accumulate, ws, ws_bytes, (cudaStream_t)stream);
-}
-
-extern "C" int bqe_experts_phase(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out,
-                                 int32_t accumulate, int32_t phase, void* ws, uint64_t ws_bytes, void* stream) {
-  if (phase != 0 && phase != 1) return BQE_EINVAL;
-  return experts_common(d, M, pool, out, accumulate, ws, ws_bytes, (cudaStream_t)stream, phase);
-}
-
-static int layer_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* resid, uint16_t* t_out,
-                        const float* router_w, const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
-                        const int32_t* forced_idx, float* out, int32_t accumulate, int32_t* topk_idx, float* topk_w,
-                        void* ws, uint64_t ws_bytes, cudaStream_t st) {
-  if (!desc_ok(d) || M < 1 || M > kMaxM || (!x && !resid) || !router_w || !slot_table || !ws || !out) return BQE_EINVAL;
-  if (((uintptr_t)ws & 255) || ((uintptr_t)router_w & 15) || d->hidden % 512) return BQE_EINVAL;
-  int rc = check_pool(pool);
-  if (rc) return rc;
-  Geo g = geo_of(d, M);
-  WsLayout L = make_ws(g);
-  if (ws_bytes < L.total) return BQE_ENOSPC;
-  const int sms = device_sms();
-  if (sms <= 0) return BQE_ECUDA;
-  if ((d->n_experts + sms - 1) / sms > 4) return BQE_EUNSUPPORTED;  // router rows per CTA
-  LayerParams P = {};
-  P.g = g;
-  P.L = L;
-  P.ws = (uint8_t*)ws;
-  P.x = x;
-  P.resid = resid;
-  P.t_out = t_out;
-  P.router_w = router_w;
-  P.bias = sel_bias;
-  P.forced = forced_idx;
-  P.slot_table = slot_table;
-  P.pool = *pool;
-  P.out = out;
-  P.accumulate = accumulate ? 1 : 0;
-  P.topk_idx = topk_idx;
-  P.topk_w = topk_w;
-  P.drop_item = g_drop_item.load();
-  P.variant = g_variant.load();
-  P.diag = g_diag.load();
-  P.limit_ns = g_wait_limit_ns.load();
-  return launch_layer(P, sms, st);
+  return route_common(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, topk_idx, topk_w, ws, ws_bytes,
+                      (cudaStream_t)stream);
 }
 
 // The decode layer as one persistent kernel (bqe_moe.cu).
 static int moe_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* resid, uint16_t* t_out,
                       const float* router_w, const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
                       const int32_t* forced_idx, float* out, int32_t accumulate, int32_t* topk_idx, float* topk_w,
-                      void* ws, uint64_t ws_bytes, cudaStream_t st) {
-  if (!desc_ok(d) || M < 1 || M > kMaxM || (!x && !resid) || !router_w || !slot_table || !ws || !out) return BQE_EINVAL;
-  if (((uintptr_t)ws & 255) || ((uintptr_t)router_w & 15) || d->hidden % 512) return BQE_EINVAL;
-  if (x && ((uintptr_t)x & 15)) return BQE_EINVAL;
-  int rc = check_pool(pool);
+                      void* ws, uint64_t ws_bytes, cudaStream_t st, bool allow_diag = true) {
+  int rc = check_layer_args(d, M, x, resid, router_w, pool, slot_table, out);
   if (rc) return rc;
+  if (!ws || ((uintptr_t)ws & 255)) return BQE_EINVAL;
   Geo g = geo_of(d, M);
   WsLayout L = make_ws(g);
   if (ws_bytes < L.total) return BQE_ENOSPC;
@@ -246,25 +141,29 @@ static int moe_common(const bqe_layer_desc* d, int32_t M, const uint16_t* x, con
   P.topk_idx = topk_idx;
   P.topk_w = topk_w;
   P.drop_item = g_drop_item.load();
-  P.variant = g_variant.load();
-  P.diag = g_diag.load();
+  P.diag = allow_diag ? g_diag.load() : 0;
   P.limit_ns = g_wait_limit_ns.load();
   return launch_moe(P, sms, st);
 }
+
+namespace bqe {
+int moe_forward(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w, const float* sel_bias,
+                const bqe_pool* pool, const int32_t* slot_table, const int32_t* forced_idx, float* out,
+                int32_t accumulate, int32_t* topk_idx, float* topk_w, void* ws, uint64_t ws_bytes, cudaStream_t st,
+                bool allow_diag) {
+  if (!x) return BQE_EINVAL;
+  return moe_common(d, M, x, nullptr, nullptr, router_w, sel_bias, pool, slot_table, forced_idx, out, accumulate,
+                    topk_idx, topk_w, ws, ws_bytes, st, allow_diag);
+}
+}  // namespace bqe
 
 extern "C" int bqe_moe_layer_forward(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w,
                                      const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
                                      const int32_t* forced_idx, float* out, int32_t accumulate, int32_t* topk_idx,
                                      float* topk_w, void* ws, uint64_t ws_bytes, void* stream) {
-  if (g_fused.load()) {
-    if (!x) return BQE_EINVAL;
-    return moe_common(d, M, x, nullptr, nullptr, router_w, sel_bias, pool, slot_table, forced_idx, out, accumulate,
-                      topk_idx, topk_w, ws, ws_bytes, (cudaStream_t)stream);
-  }
-  int rc = bqe_route(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, topk_idx, topk_w, ws, ws_bytes,
-                     stream);
-  if (rc) return rc;
-  return experts_common(d, M, pool, out, accumulate, ws, ws_bytes, (cudaStream_t)stream, -1, slot_table);
+  if (!x) return BQE_EINVAL;
+  return moe_common(d, M, x, nullptr, nullptr, router_w, sel_bias, pool, slot_table, forced_idx, out, accumulate,
+                    topk_idx, topk_w, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 extern "C" int bqe_layer_stats(const bqe_layer_desc* d, int32_t M, const void* ws, void* stream, bqe_stats* out) {
@@ -306,15 +205,8 @@ extern "C" int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M
     uint16_t* tl = t_out ? t_out + (int64_t)l * M * H : nullptr;
     const float* bl = sel_bias ? sel_bias + l * E : nullptr;
     const int32_t* fl = forced_idx ? forced_idx + (int64_t)l * M * K : nullptr;
-    int rc;
-    if (g_fused.load()) {
-      rc = moe_common(d, M, nullptr, resid, tl, router_w + l * E * H, bl, pool, slot_tables + l * (E + 1), fl, resid, 1,
-                      nullptr, nullptr, ws, ws_bytes, st);
-    } else {
-      rc = route_common(d, M, nullptr, resid, tl, router_w + l * E * H, bl, pool, slot_tables + l * (E + 1), fl, nullptr,
-                        nullptr, ws, ws_bytes, st);
-      if (!rc) rc = experts_common(d, M, pool, resid, 1, ws, ws_bytes, st, -1, slot_tables + l * (E + 1));
-    }
+    const int rc = moe_common(d, M, nullptr, resid, tl, router_w + l * E * H, bl, pool, slot_tables + l * (E + 1), fl,
+                              resid, 1, nullptr, nullptr, ws, ws_bytes, st);
     if (rc) return rc;
   }
   return BQE_OK;

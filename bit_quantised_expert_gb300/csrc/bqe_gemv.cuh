@@ -1,6 +1,6 @@
-// bqe_gemv.cuh — the per-format dequant-GEMV group kernels shared by the
-// decode kernels: one lane = one weight row, one 256-column group of a tile in
-// shared memory, R <= 4 activation rows at a time, fp32 accumulation.
+// bqe_gemv.cuh — the per-format dequant-GEMV group kernels of the decode
+// layer: one lane = one weight row, one 256-column group of a tile in shared
+// memory, R <= 4 activation rows at a time, fp32 accumulation.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -10,29 +10,6 @@
 #include "bqe_internal.cuh"
 
 namespace bqe {
-
-struct StageHdr {
-  uint64_t addr;   // slot base
-  int u, p0;       // expert (work-list index), first panel
-  int fmt;
-  uint32_t tb;     // bytes of one weight tile of the stage
-  int16_t c, R;    // K chunk, activation rows
-  uint16_t nb;     // format blocks per tile row (chunk columns / block width)
-  uint8_t amode;   // staging mode of the activation rows
-  uint8_t pad;     // free here (the single-kernel layer marks W2 items with it)
-};
-
-__host__ __device__ inline int phase_mats(int phase) { return phase == 0 ? 2 : 1; }
-
-__host__ __device__ inline int phase_panels(const Geo& g, int phase) { return phase == 0 ? g.PA : g.PB; }
-
-__host__ __device__ inline uint32_t stage_slot_bytes(const Geo& g, int phase) {
-  return stage_bytes_for(phase_mats(phase), phase_panels(g, phase), phase == 0 ? g.kcA : g.kcB, g.M);
-}
-
-__host__ __device__ inline int phase_warps(const Geo& g, int phase) {
-  return phase_mats(phase) * phase_panels(g, phase) * (phase == 0 ? g.GA : g.GB);
-}
 
 // ---------------------------------------------------------------------------
 // per-format group kernels: one lane = one weight row, 256 columns, R rows of
@@ -140,170 +117,6 @@ __device__ __forceinline__ void group_mxfp4_h(const uint8_t* tile, int nb, int g
 #pragma unroll
     for (int r = 0; r < R; ++r) acc[r].x = fmaf((a[r][0] + a[r][1]) + (a[r][2] + a[r][3]), sc, acc[r].x);
   }
-}
-
-// 2-bit code q -> float (2q - 3), exactly, via a float whose fraction holds q:
-// 1 + q/4 has the bit pattern 0x3F800000 | q << 21, and 8 (1 + q/4) - 11 = 2q - 3.
-__device__ __forceinline__ float q2_val(uint32_t word, int j) {
-  const float f = __uint_as_float(0x3F800000u | (((word >> (2 * j)) & 3u) << 21));
-  return fmaf(8.0f, f, -11.0f);
-}
-
-template <int R>
-__device__ __forceinline__ void group_q2_0(const uint8_t* tile, int nb, int grp, const float* act, int kc, int lane,
-                                           float2 (&acc)[R]) {
-#pragma unroll 1
-  for (int bi = 0; bi < 4; ++bi) {
-    const int b = grp * 4 + bi;
-    const uint4 c4 = *reinterpret_cast<const uint4*>(tile + b * 512 + lane * 16);
-    const float d = __half2float(*reinterpret_cast<const __half*>(tile + nb * 512 + (b * 32 + lane) * 2));
-    float2 bs[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) bs[r] = f2(0.f, 0.f);
-    const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-#pragma unroll
-      for (int j = 0; j < 16; j += 4) {
-        const float2 v0 = f2(q2_val(wd[w], j), q2_val(wd[w], j + 1));
-        const float2 v1 = f2(q2_val(wd[w], j + 2), q2_val(wd[w], j + 3));
-        const int k = grp * 256 + bi * 64 + w * 16 + j;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float4 xa = *reinterpret_cast<const float4*>(act + r * kc + k);
-          bs[r] = __ffma2_rn(v0, f2(xa.x, xa.y), bs[r]);
-          bs[r] = __ffma2_rn(v1, f2(xa.z, xa.w), bs[r]);
-        }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = __ffma2_rn(bs[r], f2(d, d), acc[r]);
-  }
-}
-
-// Five ternary digits of one byte (least significant first) -> t = digit - 1.
-__device__ __forceinline__ void tq1_byte(uint32_t v, float (&t)[5]) {
-#pragma unroll
-  for (int r = 0; r < 5; ++r) {
-    const uint32_t q = (v * 171u) >> 9;  // v / 3 for v <= 255
-    t[r] = (float)((int)(v - 3u * q) - 1);
-    v = q;
-  }
-}
-
-template <int R>
-__device__ __forceinline__ void group_tq1(const uint8_t* tile, int nb, int grp, const float* act, int kc, int lane,
-                                          float2 (&acc)[R]) {
-  const int b = grp;
-  float2 bs[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) bs[r] = f2(0.f, 0.f);
-  // bytes 0..47: three 16-byte pieces = 12 words = 12 x 4 bytes = 12 x 20 weights
-#pragma unroll 1
-  for (int q = 0; q < 3; ++q) {
-    const uint4 c4 = *reinterpret_cast<const uint4*>(tile + (b * 3 + q) * 512 + lane * 16);
-    const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      float t[20];
-#pragma unroll
-      for (int by = 0; by < 4; ++by) {
-        float tt[5];
-        tq1_byte((wd[w] >> (8 * by)) & 0xFF, tt);
-#pragma unroll
-        for (int r5 = 0; r5 < 5; ++r5) t[by * 5 + r5] = tt[r5];
-      }
-      const int k = grp * 256 + (q * 16 + w * 4) * 5;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-#pragma unroll
-        for (int i4 = 0; i4 < 5; ++i4) {
-          const float4 xa = *reinterpret_cast<const float4*>(act + r * kc + k + 4 * i4);
-          bs[r] = __ffma2_rn(f2(t[4 * i4], t[4 * i4 + 1]), f2(xa.x, xa.y), bs[r]);
-          bs[r] = __ffma2_rn(f2(t[4 * i4 + 2], t[4 * i4 + 3]), f2(xa.z, xa.w), bs[r]);
-        }
-      }
-    }
-  }
-  // bytes 48..55: three digit bytes (weights 240..254), byte 51 (weight 255), d
-  const uint2 tail = *reinterpret_cast<const uint2*>(tile + nb * 1536 + (b * 32 + lane) * 8);
-  float t[16];
-#pragma unroll
-  for (int by = 0; by < 3; ++by) {
-    float tt[5];
-    tq1_byte((tail.x >> (8 * by)) & 0xFF, tt);
-#pragma unroll
-    for (int r5 = 0; r5 < 5; ++r5) t[by * 5 + r5] = tt[r5];
-  }
-  t[15] = (float)((int)((tail.x >> 24) % 3u) - 1);
-  const float d = __half2float(__ushort_as_half((unsigned short)(tail.y & 0xFFFF)));
-  const int k = grp * 256 + 240;
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-#pragma unroll
-    for (int i4 = 0; i4 < 4; ++i4) {
-      const float4 xa = *reinterpret_cast<const float4*>(act + r * kc + k + 4 * i4);
-      bs[r] = __ffma2_rn(f2(t[4 * i4], t[4 * i4 + 1]), f2(xa.x, xa.y), bs[r]);
-      bs[r] = __ffma2_rn(f2(t[4 * i4 + 2], t[4 * i4 + 3]), f2(xa.z, xa.w), bs[r]);
-    }
-    acc[r] = __ffma2_rn(bs[r], f2(d, d), acc[r]);
-  }
-}
-
-template <int R>
-__device__ __forceinline__ void group_q3k(const uint8_t* tile, int nb, int grp, const float* act, int kc, int lane,
-                                          float2 (&acc)[R]) {
-  const int b = grp;
-  uint32_t lo[16], hi[8], sc[3];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 v = *reinterpret_cast<const uint4*>(tile + (b * 4 + q) * 512 + lane * 16);
-    lo[4 * q] = v.x; lo[4 * q + 1] = v.y; lo[4 * q + 2] = v.z; lo[4 * q + 3] = v.w;
-  }
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const uint4 v = *reinterpret_cast<const uint4*>(tile + nb * 2048 + (b * 2 + q) * 512 + lane * 16);
-    hi[4 * q] = v.x; hi[4 * q + 1] = v.y; hi[4 * q + 2] = v.z; hi[4 * q + 3] = v.w;
-  }
-  const uint8_t* scp = tile + nb * 3072 + (b * 32 + lane) * 12;
-#pragma unroll
-  for (int i = 0; i < 3; ++i) sc[i] = *reinterpret_cast<const uint32_t*>(scp + 4 * i);
-  const float d = __half2float(*reinterpret_cast<const __half*>(tile + nb * 3456 + (b * 32 + lane) * 2));
-  float2 bsum[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) bsum[r] = f2(0.f, 0.f);
-#pragma unroll 1
-  for (int sj = 0; sj < 16; ++sj) {
-    // 6-bit sub-scale sj at bits 6 sj .. 6 sj + 5 of the 96-bit little-endian string
-    const int bit = 6 * sj;
-    const uint64_t two = ((uint64_t)sc[bit >> 5]) | (((bit >> 5) < 2 ? (uint64_t)sc[(bit >> 5) + 1] : 0ull) << 32);
-    const float s = (float)((uint32_t)(two >> (bit & 31)) & 63u);
-    const uint32_t low = lo[sj];          // weights 16 sj .. 16 sj + 15: 2 bits each
-    const uint32_t high = hi[sj >> 1] >> ((sj & 1) * 16);  // 16 high bits
-    float2 ss[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) ss[r] = f2(0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-      float v[4];
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int qv = (int)(((low >> (2 * (j + jj))) & 3u) | (((high >> (j + jj)) & 1u) << 2));
-        v[jj] = (float)(qv - 4);
-      }
-      const int k = grp * 256 + sj * 16 + j;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float4 xa = *reinterpret_cast<const float4*>(act + r * kc + k);
-        ss[r] = __ffma2_rn(f2(v[0], v[1]), f2(xa.x, xa.y), ss[r]);
-        ss[r] = __ffma2_rn(f2(v[2], v[3]), f2(xa.z, xa.w), ss[r]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) bsum[r] = __ffma2_rn(ss[r], f2(s, s), bsum[r]);
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = __ffma2_rn(bsum[r], f2(d, d), acc[r]);
 }
 
 // ----------------------------------------------------------------------------
@@ -524,16 +337,15 @@ __device__ __forceinline__ void group_tq1_i(const uint8_t* tile, int nb, int grp
   }
 }
 
-// Activation modes of a stage: 0 fp32 rows, 1 f16 rows (x 2^s, MXFP4 only),
+// Activation modes of an item: 0 fp32 rows, 1 f16 rows (x 2^s, MXFP4 W1/W3),
 // 2 integer rows (X in the format's order, then the 16-column sums).
 enum { kActF32 = 0, kActF16 = 1, kActInt = 2 };
 
 // Mode of the activations of an item: integer for the fp16-scaled formats
-// (variants >= 1, both phases); for MXFP4 f16 in W1/W3 (variant 1), else fp32.
-__host__ __device__ inline int act_mode(int phase, int fmt, int variant) {
-  if (variant == 0) return 0;
-  if (fmt != BQE_FMT_MXFP4) return 2;
-  return phase == 0 && variant == 1 ? 1 : 0;
+// (both phases); for MXFP4 f16 in W1/W3 and fp32 in W2 (h stays fp32).
+__host__ __device__ inline int act_mode(int phase, int fmt) {
+  if (fmt != BQE_FMT_MXFP4) return kActInt;
+  return phase == 0 ? kActF16 : kActF32;
 }
 
 __host__ __device__ inline int act_row_bytes(int amode, int fmt, int kc) {
@@ -555,19 +367,10 @@ __device__ __forceinline__ void consume_group_R(int fmt, const uint8_t* tile, in
       case BQE_FMT_TQ1: group_tq1_i<R>(tile, nb, grp, act, rowb, kc, lane, acc); break;
       case BQE_FMT_Q3_K: group_q3k_i<R>(tile, nb, grp, act, rowb, kc, lane, acc); break;
     }
+  } else if (amode == kActF16) {
+    group_mxfp4_h<R>(tile, nb, grp, reinterpret_cast<const uint16_t*>(act), kc, lane, acc);
   } else {
-    const float* actf = reinterpret_cast<const float*>(act);
-    switch (fmt) {
-      case BQE_FMT_MXFP4:
-        if (amode == kActF16)
-          group_mxfp4_h<R>(tile, nb, grp, reinterpret_cast<const uint16_t*>(act), kc, lane, acc);
-        else
-          group_mxfp4<R>(tile, nb, grp, actf, kc, lane, acc);
-        break;
-      case BQE_FMT_Q2_0: group_q2_0<R>(tile, nb, grp, actf, kc, lane, acc); break;
-      case BQE_FMT_TQ1: group_tq1<R>(tile, nb, grp, actf, kc, lane, acc); break;
-      case BQE_FMT_Q3_K: group_q3k<R>(tile, nb, grp, actf, kc, lane, acc); break;
-    }
+    group_mxfp4<R>(tile, nb, grp, reinterpret_cast<const float*>(act), kc, lane, acc);
   }
 #pragma unroll
   for (int r = 0; r < R; ++r) outv[r * 32 + lane] = acc[r].x + acc[r].y;

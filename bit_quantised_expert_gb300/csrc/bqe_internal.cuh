@@ -76,41 +76,15 @@ __host__ __device__ inline uint32_t tile_byte_offset(int f, int nb, int b, int r
 // Decode-call geometry shared by host and kernels.
 // ----------------------------------------------------------------------------
 constexpr int kMaxM = 8;          // rows per decode call
-constexpr int kMaxWarps = 16;     // consumer warps per CTA
 constexpr int kMaxTopK = 16;
-constexpr int kRowChunk = 4;      // rows accumulated together (larger row sets are done in chunks)
-constexpr int kRed = 2;           // reduction buffers between consumers and the epilogue warp
-constexpr uint32_t kSmemBudget = 220 * 1024;
-constexpr uint32_t kEngineBase = 2048;  // headers and mbarriers in front of the reduction buffers
-constexpr int kFmtMaxBytesPerCol = 17;  // MXFP4 tile: 17 bytes per column per 32 rows (largest format)
+constexpr int kRowChunk = 4;      // rows accumulated together by the widest inner loops
 
 struct Geo {
   int H, I, E, K, M;
   int U;                          // max distinct experts incl. the shared one = M*K + 1 (<= E+1)
-  int kcA, nchA, GA, npanA, PA;   // W1/W3: K = H; PA panels of 32 rows per work item
-  int kcB, nchB, GB, npanB, PB;   // W2: K = I; PB panels per work item
+  int kcA, nchA, GA, npanA;       // W1/W3: K = H in chunks of kcA, GA 256-column groups per chunk, I/32 panels
+  int kcB, nchB, GB, npanB;       // W2: K = I in chunks of kcB, GB groups per chunk, H/32 panels
 };
-
-// Bytes of one ring stage: P panels of `mats` matrices (largest format) plus
-// the activation chunk of M rows (fp32, the larger of the two encodings).
-__host__ __device__ inline uint32_t stage_bytes_for(int mats, int P, int kc, int M) {
-  const uint32_t w = (uint32_t)mats * P * kFmtMaxBytesPerCol * kc;
-  return ((w + (uint32_t)M * kc * 4u) + 127u) & ~127u;
-}
-__host__ __device__ inline uint32_t red_bytes_for(int nw, int M) {
-  return ((uint32_t)kRed * nw * M * 32 * 4 + 127u) & ~127u;
-}
-// Largest P (panels per item) with mats*P*G consumer warps <= kMaxWarps,
-// P dividing the panel count and at least two stages fitting the budget.
-__host__ __device__ inline int pick_panels(int mats, int G, int npan, int kc, int M) {
-  int best = 1;
-  for (int P = 1; P * mats * G <= kMaxWarps; ++P) {
-    if (npan % P) continue;
-    const uint32_t need = kEngineBase + red_bytes_for(mats * P * G, M) + 2 * stage_bytes_for(mats, P, kc, M);
-    if (need <= kSmemBudget) best = P;
-  }
-  return best;
-}
 
 __host__ __device__ inline Geo make_geo(int H, int I, int E, int K, int M) {
   Geo g;
@@ -119,8 +93,6 @@ __host__ __device__ inline Geo make_geo(int H, int I, int E, int K, int M) {
   if (g.U > E + 1) g.U = E + 1;
   g.kcA = chunk_cols(H); g.nchA = H / g.kcA; g.GA = g.kcA / 256; g.npanA = I / 32;
   g.kcB = chunk_cols(I); g.nchB = I / g.kcB; g.GB = g.kcB / 256; g.npanB = H / 32;
-  g.PA = pick_panels(2, g.GA, g.npanA, g.kcA, M);
-  g.PB = pick_panels(1, g.GB, g.npanB, g.kcB, M);
   return g;
 }
 
@@ -139,17 +111,20 @@ __host__ __device__ constexpr uint32_t int_rec_bytes(int tq, int kc) {
 
 // Workspace layout (offsets in bytes, each 256-aligned).
 struct WsLayout {
-  uint64_t err, ctr_route, nu, u_slot, u_fmt, u_addr, u_nrows, u_rows;
-  uint64_t comb_u, comb_r, comb_w, z, xf, xh, xsc, xrq, xrt, pa, h, hr, pb, dbg;
-  uint64_t fctr, cnt_a, h_cnt, ctr_out;  // counters of the fused layer kernel
+  // the router kernel's arrival counter and the call's work list (distinct
+  // experts: slot, format, address, rows), combine indices and weights
+  uint64_t err, ctr_route, nu, u_slot, u_fmt, u_addr, u_nrows, u_rows, comb_u, comb_r, comb_w;
+  // logits; the layer input in fp32, in f16 x 2^s, 2^-s per row, and as the
+  // integer records of the two orders; the diagnostic counters
+  uint64_t z, xf, xh, xsc, xrq, xrt, dbg;
   // single-kernel decode layer (k_moe), per "row slot" (an expert's r-th row;
-  // M (K + 1) slots at most): call epoch, epoch-tagged logits, K-chunk
+  // M (K + 1) slots at most): call epoch, logits arrival counter, K-chunk
   // partials of g/u and of y, h in fp32, the integer records of h, the grid
   // barrier counter (64-bit, three arrivals per CTA per call)
-  uint64_t epoch, zt, m_pa, m_pb, m_h, m_hr, m_done;
+  uint64_t epoch, zt, m_done, m_pa, m_pb, m_h, m_hr;
   uint64_t total;
 };
-constexpr int kDbgSlots = 8;      // per-CTA cycle counters of the diagnostic mode
+constexpr int kDbgSlots = 8;      // per-CTA counters of the diagnostic mode
 constexpr int kDbgMaxCtas = 1024;
 
 __host__ __device__ inline uint64_t al256(uint64_t x) { return (x + 255) & ~(uint64_t)255; }
@@ -177,29 +152,19 @@ __host__ __device__ inline WsLayout make_ws(const Geo& g) {
   // of the integer GEMV paths (int_rec_bytes)
   w.xrq = o; o = al256(o + (uint64_t)int_rec_bytes(0, g.kcA) * g.M * g.nchA);
   w.xrt = o; o = al256(o + (uint64_t)int_rec_bytes(1, g.kcA) * g.M * g.nchA);
-  w.pa = o; o = al256(o + 4ull * g.U * g.npanA * g.nchA * 2 * g.M * 32);
-  w.h = o; o = al256(o + 4ull * g.U * g.M * g.I);
-  // h of every (expert, row) for the integer W2 paths: one record per K
-  // chunk in the order of that expert's format, each sized for T order
-  w.hr = o; o = al256(o + (uint64_t)int_rec_bytes(1, g.kcB) * g.U * g.M * g.nchB);
-  w.pb = o; o = al256(o + 4ull * g.U * g.nchB * g.M * g.H);
-  w.dbg = o; o = al256(o + 8ull * 3 * kDbgMaxCtas * kDbgSlots);  // [phase A, phase B, router][cta][slot] cycles
-  w.fctr = o; o = al256(o + 16);                                  // [0] logits done, [1] CTAs done
-  w.cnt_a = o; o = al256(o + 4ull * g.U * g.npanA);               // chunks done per (expert, panel group)
-  w.h_cnt = o; o = al256(o + 4ull * g.U);                         // panel groups of h done per expert
-  w.ctr_out = o; o = al256(o + 4ull * g.npanB);                   // (expert, chunk) items done per output panel group
+  w.dbg = o; o = al256(o + 8ull * 3 * kDbgMaxCtas * kDbgSlots);
+  // the call epoch and the two counters are contiguous: [epoch, m_pa) clears them
   w.epoch = o; o = al256(o + 16);
-  w.zt = o; o = al256(o + 8ull * g.M * g.E);                       // (logit bits | tag << 32) per (row, expert)
+  w.zt = o; o = al256(o + 16);                                     // logits arrival counter (64-bit)
+  w.m_done = o; o = al256(o + 16);                                 // grid barrier counter (64-bit)
   const uint64_t nrs = (uint64_t)g.M * (g.K + 1);
   w.m_pa = o; o = al256(o + 4ull * nrs * g.npanA * g.nchA * 2 * 32);
   w.m_pb = o; o = al256(o + 4ull * nrs * g.nchB * g.H);
   w.m_h = o; o = al256(o + 4ull * nrs * g.I);
   w.m_hr = o; o = al256(o + (uint64_t)int_rec_bytes(1, g.kcB) * nrs * g.nchB);
-  w.m_done = o; o = al256(o + 16);
   w.total = o;
   return w;
 }
-
 
 // Kernel parameter blocks (passed by value to the kernels).
 struct RouteParams {
@@ -218,48 +183,6 @@ struct RouteParams {
   float* topk_w;              // optional M x K
   int diag;                   // 1: add cycle counts into ws.dbg
 };
-
-struct ExpParams {
-  Geo g;
-  WsLayout L;
-  uint8_t* ws;
-  float* out;
-  int accumulate;
-  int nstages;        // ring depth (<= 16), chosen by the host from the smem budget
-  int drop_item;      // test hook: CTA 0's producer never issues its item number drop_item (-1: off)
-  int variant;        // inner-loop variant for MXFP4 in phase A (0: f32 FMA, 1: f16-input FMA)
-  const int32_t* slot_table;  // E + 1 slots, or null: with it, the shared expert's weights (slot_table[E])
-                              // are streamed in before the routing results are awaited
-  bqe_pool pool;
-  int max_pre;                // at most this many shared-expert stages streamed before the wait
-  int diag;           // 1: accumulate per-CTA cycle counters into ws.dbg
-  uint64_t limit_ns;  // bound on every mbarrier wait
-};
-
-// Fused decode layer: router + top-k + W1/W3 + SiLU-GLU + W2 + combine in one
-// cooperatively launched persistent kernel.
-struct LayerParams {
-  Geo g;
-  WsLayout L;
-  uint8_t* ws;
-  const uint16_t* x;          // bf16 M x H, or null when resid is given
-  const float* resid;         // fp32 M x H (chained step: normalise first)
-  uint16_t* t_out;            // optional bf16 M x H copy of the layer input
-  const float* router_w;
-  const float* bias;
-  const int32_t* forced;
-  const int32_t* slot_table;
-  bqe_pool pool;
-  float* out;
-  int accumulate;
-  int32_t* topk_idx;
-  float* topk_w;
-  int nstages, NW, NE;        // ring depth, consumer warps, epilogue warps
-  uint32_t slot_bytes;        // ring slot
-  int drop_item, variant, diag;
-  uint64_t limit_ns;
-};
-int launch_layer(const LayerParams& P, int grid, cudaStream_t st);
 
 // Single-kernel decode layer (bqe_moe.cu).
 struct MoeParams {
@@ -283,22 +206,28 @@ struct MoeParams {
   uint32_t rt_off;            // ring offset of this CTA's router rows (used until the routing is known)
   uint64_t magA, magA2, magB, magB2;  // ceil(2^32 / d) for the item-index divisors (exact here)
   int PB;                     // W2 output panels per item
-  int drop_item, variant, diag;
+  int drop_item, diag;
   uint64_t limit_ns;
 };
 int launch_moe(const MoeParams& P, int grid, cudaStream_t st);
+// Host-side argument checks of a decode-layer call (bqe_api.cu).
+int check_layer_args(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* resid, const float* router_w,
+                     const bqe_pool* pool, const int32_t* slot_table, const float* out);
+// The decode layer on workspace ws (bqe_api.cu); diag = 0 keeps the
+// diagnostic counters off whatever the process-wide setting.
+int moe_forward(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w, const float* sel_bias,
+                const bqe_pool* pool, const int32_t* slot_table, const int32_t* forced_idx, float* out,
+                int32_t accumulate, int32_t* topk_idx, float* topk_w, void* ws, uint64_t ws_bytes, cudaStream_t st,
+                bool allow_diag);
 
 uint32_t layer_smem_bytes(const Geo& g, int* nstages_out, int* nw_out, uint32_t* slot_out);
 
 // Launchers (one per translation unit that owns the kernel).
 int launch_route(const RouteParams& P, cudaStream_t st, bool pdl);
-int launch_experts(const ExpParams& P, int phase, int grid, cudaStream_t st, bool pdl);
-int launch_finalize(const ExpParams& P, int phase, int sms, cudaStream_t st, bool pdl);
-uint32_t experts_smem_bytes(const Geo& g, int phase, int* nstages_out);
 
 // Error detail codes written to ws.err[1].
 enum { kErrSlotRange = 1, kErrSlotFmt = 2, kErrSlotExtent = 3, kErrWaitFull = 4, kErrWaitEmpty = 5,
-       kErrForcedIdx = 6, kErrPreload = 12 };  // 7..11: the prefill kernels
+       kErrForcedIdx = 6 };  // 7..11: the prefill kernels
 
 #ifdef __CUDACC__
 // ----------------------------------------------------------------------------

@@ -167,7 +167,7 @@ __device__ __forceinline__ bool wait_ge(const unsigned int* p, uint32_t target, 
 __device__ inline void make_tpl(const MoeParams& P, ItemTpl& T, int ph, int u, int fmt, uint64_t addr, int R, int rb) {
   const Geo& g = P.g;
   const int kc = ph ? g.kcB : g.kcA;
-  const int amode = act_mode(ph, fmt, P.variant);
+  const int amode = act_mode(ph, fmt);
   ItemHdr& h = T.h;
   h.tb = tile_bytes(fmt, kc);
   h.arow = (uint32_t)act_row_bytes(amode, fmt, kc);
@@ -662,26 +662,25 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     if (P.diag && ct == 0) dacc(P, 1, globaltimer_ns() - t_cta0, 0);
     float* zg = (float*)(P.ws + P.L.z);
     // The routing: keys, top-k, mixing weights, work list, row slots and item
-    // templates (dry: a pass without effect outside this CTA's shared memory,
-    // kept for timing experiments; the call makes one real pass)
-    auto routing = [&](bool dry) {
+    // templates, once every CTA's logits are in
+    auto routing = [&]() {
     // logits and selection keys of every (row, expert), all threads; the keys
     // go where this CTA's router rows were (no longer needed)
-    uint32_t* s_key = dry ? reinterpret_cast<uint32_t*>(s_z) : reinterpret_cast<uint32_t*>(ring + P.rt_off);
-    const bool forced = P.forced && !dry;
+    uint32_t* s_key = reinterpret_cast<uint32_t*>(ring + P.rt_off);
+    const bool forced = P.forced != nullptr;
     for (int i = ct; i < M * E; i += NCT) {
-      const float zv = dry ? s_z[i] : __ldcg(zg + i);
-      if (!dry) s_z[i] = zv;
+      const float zv = __ldcg(zg + i);
+      s_z[i] = zv;
       if (!forced) s_key[i] = sel_key(zv, s_bias[i % E]);
     }
     for (int i = ct; i < E; i += NCT) s_mask[i] = 0u;
     named_bar_sync(1, NCT);
-    if (ct == 0 && !dry) {
+    if (ct == 0) {
       mstamp(P, kStRouted, false);
       rstamp(P, 0, t_cta0);
     }
     // ---- top-k of each row (warp m selects row m), mixing weights
-    if (cw < M && (dry || !s_abort)) {
+    if (cw < M && !s_abort) {
       const int m = cw;
       constexpr int QN = kMaxEM / 32;
       const int qn = (E + 31) / 32;
@@ -740,14 +739,14 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       if (lane < K) {
         const float w = ev / tot;
         s_cw[m][lane] = w;
-        if (cta == 0 && !dry) {
+        if (cta == 0) {
           if (P.topk_idx) P.topk_idx[m * K + lane] = s_idx[m][lane];
           if (P.topk_w) P.topk_w[m * K + lane] = w;
         }
       }
     }
     named_bar_sync(1, NCT);
-    if (ct == 0 && !dry) rstamp(P, 1, t_cta0);
+    if (ct == 0) rstamp(P, 1, t_cta0);
     // ---- work list: the chosen experts in ascending id order (u = 1..), shared u = 0
     {
       const int e = ct;  // E <= 512 = NCT
@@ -764,7 +763,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       if (on) {
         const int u = s_uof[e];
         const int my_bad = s_ebad[e], my_fmt = s_efmt[e], my_slot = s_eslot[e];
-        if (my_bad && !dry) {
+        if (my_bad) {
           set_error(err, BQE_EDEVICE, my_bad);
           s_bad = 1;
         }
@@ -775,7 +774,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         for (int m = 0; m < M; ++m)
           if (mask & (1u << m)) s_urows[u * kMaxM + n++] = (int8_t)m;
         s_unrows[u] = n;
-        if (cta == 0 && !dry) {  // the call's work list, for bqe_layer_stats
+        if (cta == 0) {  // the call's work list, for bqe_layer_stats
           ((int32_t*)(P.ws + P.L.u_slot))[u] = my_slot;
           ((int32_t*)(P.ws + P.L.u_fmt))[u] = my_fmt;
           ((int32_t*)(P.ws + P.L.u_nrows))[u] = n;
@@ -784,14 +783,14 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       if (ct == NCT - 1) {
         // the shared expert, u = 0 (validated like the others)
         const int sh_bad = s_ebad[E], sh_fmt = s_efmt[E], sh_slot = s_eslot[E];
-        if (sh_bad && !dry) {
+        if (sh_bad) {
           set_error(err, BQE_EDEVICE, sh_bad);
           s_bad = 2;
         }
         s_ufmt[0] = sh_fmt;
         s_uaddr[0] = s_eaddr[E];
         s_unrows[0] = M;
-        if (cta == 0 && !dry) {
+        if (cta == 0) {
           ((int32_t*)(P.ws + P.L.u_slot))[0] = sh_slot;
           ((int32_t*)(P.ws + P.L.u_fmt))[0] = sh_fmt;
           ((int32_t*)(P.ws + P.L.u_nrows))[0] = M;
@@ -799,7 +798,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         for (int m = 0; m < M; ++m) s_urows[m] = (int8_t)m;
       }
       named_bar_sync(1, NCT);
-      if (ct == 0 && !dry) rstamp(P, 2, t_cta0);
+      if (ct == 0) rstamp(P, 2, t_cta0);
       if (ct == 0) {
         int tot = 0;
         for (int w2 = 0; w2 < kCW; ++w2) tot += s_wcnt[w2];
@@ -815,11 +814,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         // reports the error; its output is undefined); an invalid shared slot
         // or an aborted routing streams nothing
         s_nu = (s_abort || s_bad == 2) ? 0 : s_bad ? 1 : 1 + tot;
-        if (cta == 0 && !dry) *(int32_t*)(P.ws + P.L.nu) = s_nu;
+        if (cta == 0) *(int32_t*)(P.ws + P.L.nu) = s_nu;
       }
       named_bar_sync(1, NCT);
-      if (ct == 0 && !dry) rstamp(P, 3, t_cta0);
-      if (ct < M * K && (dry || !s_abort)) {
+      if (ct == 0) rstamp(P, 3, t_cta0);
+      if (ct < M * K && !s_abort) {
         const int m = ct / K, j = ct % K;
         const int ee = s_idx[m][j];
         s_rs[m][j] = s_rbase[s_uof[ee]] + __popc(s_mask[ee] & ((1u << m) - 1u));
@@ -830,7 +829,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         if (fmt_ok(s_ufmt[u])) make_tpl(P, s_tpl[ph][u], ph, u, s_ufmt[u], s_uaddr[u], s_unrows[u], s_rbase[u]);
       }
       named_bar_sync(1, NCT);
-      if (ct == 0 && !dry) {
+      if (ct == 0) {
         mstamp(P, kStRoutedMax, true);
         if (P.diag) dacc(P, 3, globaltimer_ns() - t_cta0, 1);
         mbar_arrive(&route_bar);
@@ -907,7 +906,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       if (P.diag) dacc(P, 2, globaltimer_ns() - t_cta0, 0);
     }
     named_bar_sync(1, NCT);
-    routing(false);
+    routing();
     // ---- work items: this warp takes tasks cw, cw + 16, ... of the CTA's task sequence
     const int nU = s_nu;
     const int nTot = nU * (nAper + nBper), nA = nU * nAper;
@@ -1048,7 +1047,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           }
         const float hv = silu_m(a0) * a1;
         const int fmt = s_ufmt[u];
-        if (act_mode(1, fmt, P.variant) != kActInt) {
+        if (act_mode(1, fmt) != kActInt) {
           hbuf[(int64_t)rs * I + i] = hv;
           continue;
         }

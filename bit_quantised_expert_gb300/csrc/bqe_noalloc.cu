@@ -49,25 +49,47 @@ extern "C" int bqe_moe_layer_forward_noalloc(const bqe_layer_desc* d, int32_t M,
                                              const int32_t* slot_table, const int32_t* forced_idx, float* out,
                                              int32_t accumulate, int32_t* topk_idx, float* topk_w,
                                              int32_t* status_out, void* stream) {
+  // every argument check comes before the shared array is touched, so a
+  // rejected call leaves a call in flight on another stream undisturbed
+  if (!x) return BQE_EINVAL;
+  int rc = bqe::check_layer_args(d, M, x, nullptr, router_w, pool, slot_table, out);
+  if (rc) return rc;
   const uint64_t need = bqe_workspace_bytes(d, M);
   if (need == 0) return BQE_EINVAL;
   if (need > kNoAllocBytes) return BQE_ENOSPC;  // this layer's workspace is larger than the fixed array
   cudaStream_t st = (cudaStream_t)stream;
   void* ws = nullptr;
-  int rc = noalloc_scratch(st, &ws);
+  rc = noalloc_scratch(st, &ws);
   if (rc) return rc;
-  // the array keeps the previous call's contents: clear the error word, the
-  // counters and the work list before this call (all in front of the logits),
-  // and the counters of the single-kernel layer at the end of the layout
+  // the array keeps the previous call's contents: clear the error word and
+  // the work list (all in front of the logits), and the call epoch with the
+  // two arrival counters, so a call that failed leaves no trace in the next
   const bqe::WsLayout L = bqe::make_ws(bqe::make_geo(d->hidden, d->inter, d->n_experts, d->top_k, M));
   if (cudaMemsetAsync(ws, 0, L.z, st) != cudaSuccess) return BQE_ECUDA;
-  if (cudaMemsetAsync((uint8_t*)ws + L.fctr, 0, L.total - L.fctr, st) != cudaSuccess) return BQE_ECUDA;
-  rc = bqe_moe_layer_forward(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, out, accumulate, topk_idx,
-                             topk_w, ws, need, stream);
+  if (cudaMemsetAsync((uint8_t*)ws + L.epoch, 0, L.m_pa - L.epoch, st) != cudaSuccess) return BQE_ECUDA;
+  // diagnostic counters stay off: they would accumulate in the array, where
+  // no caller can read them
+  rc = bqe::moe_forward(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, out, accumulate, topk_idx, topk_w,
+                        ws, need, st, false);
   if (rc) return rc;
   if (status_out &&
       cudaMemcpyAsync(status_out, (uint8_t*)ws + L.err, 2 * sizeof(int32_t), cudaMemcpyDeviceToDevice, st) !=
           cudaSuccess)
     return BQE_ECUDA;
   return BQE_OK;
+}
+
+extern "C" int bqe_check_noalloc(void* stream, int32_t* detail) {
+  void* ws = nullptr;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BQE_ECUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    ws = g_noalloc_ptr[dev];
+  }
+  if (!ws) {  // no call on this device yet: nothing to report
+    if (detail) *detail = 0;
+    return BQE_OK;
+  }
+  return bqe_check(ws, stream, detail);
 }

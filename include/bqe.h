@@ -204,23 +204,14 @@ int bqe_moe_layer_forward(const bqe_layer_desc* d, int32_t M, const uint16_t* x,
                           int32_t accumulate, int32_t* topk_idx, float* topk_w, void* ws,
                           uint64_t ws_bytes, void* stream);
 
-/* The same call split in its two halves, for timing each: bqe_route runs the
- * router GEMV, the scores, the biased top-k and builds the per-expert work
- * list in ws; bqe_experts streams the selected experts (W1/W3 GEMV, SiLU-GLU,
- * W2 GEMV) and combines into out.  bqe_experts must follow bqe_route on the
- * same stream with the same ws. */
+/* The routing alone: the router GEMV, the scores, the biased top-k and the
+ * mixing weights of M rows (the first stage of bqe_moe_layer_forward, as its
+ * own kernel), with the per-call work list left in ws.  topk_idx / topk_w:
+ * device, M x top_k, or NULL.  Same argument rules as bqe_moe_layer_forward. */
 int bqe_route(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const float* router_w,
               const float* sel_bias, const bqe_pool* pool, const int32_t* slot_table,
               const int32_t* forced_idx, int32_t* topk_idx, float* topk_w, void* ws,
               uint64_t ws_bytes, void* stream);
-int bqe_experts(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out,
-                int32_t accumulate, void* ws, uint64_t ws_bytes, void* stream);
-
-/* One phase of bqe_experts alone (phase 0: W1/W3 GEMV + SiLU-GLU into the
- * workspace; phase 1: W2 GEMV + combine into out), so each kernel can be
- * timed on its own.  bqe_experts == phase 0 then phase 1. */
-int bqe_experts_phase(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, float* out,
-                      int32_t accumulate, int32_t phase, void* ws, uint64_t ws_bytes, void* stream);
 
 /* Chained decode step over n_layers layers: r_0 = resid (in place),
  * t_l = bf16(r_l / sqrt(mean(r_l^2) + 1e-6)), r_{l+1} = r_l + MoE_l(t_l).
@@ -231,7 +222,7 @@ int bqe_experts_phase(const bqe_layer_desc* d, int32_t M, const bqe_pool* pool, 
  *   forced_idx  device, n_layers x M x top_k int32, or NULL
  *   t_out       device, n_layers x M x hidden bf16, or NULL: each layer's
  *               normalised input (for per-layer checks)
- * Enqueues 3 kernels per layer; capture it in a CUDA graph to replay. */
+ * Enqueues one kernel per layer; capture it in a CUDA graph to replay. */
 int bqe_moe_step(const bqe_layer_desc* d, int32_t n_layers, int32_t M, float* resid,
                  const float* router_w, const float* sel_bias, const bqe_pool* pool,
                  const int32_t* slot_tables, const int32_t* forced_idx, uint16_t* t_out,
@@ -295,14 +286,23 @@ int bqe_moe_prefill(const bqe_layer_desc* d, int32_t T, const uint16_t* x, const
  *   - Every call reuses the same array and clears its counters and error
  *     word first, so calls whose GPU work overlaps (other streams, other
  *     threads) race on it: order them.
+ *   - Arguments are checked before the array is touched; a rejected call
+ *     enqueues nothing.
  *   - status_out: device, 2 int32 or NULL; receives the call's device error
- *     word and detail (0 = ok, else a BQE_* code as bqe_check reports). */
+ *     word and detail (0 = ok, else a BQE_* code as bqe_check reports).  With
+ *     NULL, bqe_check_noalloc reads the same word (until the next call).
+ *   - The diagnostic counters (bqe_set_diag) stay off for this call. */
 int bqe_moe_layer_forward_noalloc(const bqe_layer_desc* d, int32_t M, const uint16_t* x,
                                   const float* router_w, const float* sel_bias,
                                   const bqe_pool* pool, const int32_t* slot_table,
                                   const int32_t* forced_idx, float* out, int32_t accumulate,
                                   int32_t* topk_idx, float* topk_w, int32_t* status_out,
                                   void* stream);
+
+/* Synchronise `stream` and report the device error word of the last
+ * bqe_moe_layer_forward_noalloc call on the current device, then clear it
+ * (as bqe_check does for a caller's workspace).  BQE_OK if no call ran. */
+int bqe_check_noalloc(void* stream, int32_t* detail);
 
 /* After a decode call (bqe_moe_layer_forward, or the last layer of
  * bqe_moe_step) on `ws`: synchronise `stream` and describe what the call
@@ -318,49 +318,40 @@ int bqe_check(void* ws, void* stream, int32_t* detail);
 /* Human-readable name of a status code. */
 const char* bqe_status_str(int status);
 
-/* ---- diagnostics (process-wide settings, not part of the operation) ----- */
+/* ---- diagnostics and test hooks ------------------------------------------
+ * Process-wide settings, read by each call when it is enqueued; they are not
+ * part of the operation and not meant to be changed while other threads
+ * enqueue calls (no call reads them twice). */
 
 /* Bound on every in-kernel wait (default 2 s).  A wait that runs out records
  * BQE_ETIMEOUT in the workspace and the kernel returns; the workspace must be
  * re-initialised (bqe_workspace_init) after such an error. */
 void bqe_set_wait_limit_ns(uint64_t ns);
 
-/* Chain the kernels of a call with programmatic dependent launch (default
- * on).  Off: plain stream order. */
-void bqe_set_pdl(int on);
-
 /* Test hook for the timeout path, injected from the host: while item >= 0,
- * the first CTA of each expert kernel never issues the copies of its work
- * item number `item`, so the consumers' wait for that stage runs out of its
- * limit and the call reports BQE_ETIMEOUT.  -1 (default) turns it off. */
+ * the first CTA of the decode kernel never issues the copies of its work
+ * item number `item`, so the waits for that item run out of their limit and
+ * the call reports BQE_ETIMEOUT.  -1 (default) turns it off. */
 void bqe_set_test_drop_item(int32_t item);
 
-/* Inner-loop variant of the MXFP4 W1/W3 kernel (default 1): 0 converts
- * weights to fp32 and uses packed fp32 FMAs; 1 keeps weights and the
- * activations (scaled by a power of two per row, exact) in f16 and
- * accumulates with fp32-accumulating mixed-precision FMAs.  Both give the
- * same products; only the summation order differs. */
-void bqe_set_variant(int32_t v);
-
-/* Diagnostic mode (default off): the kernels add per-CTA clock64() cycle
- * counts into the workspace at byte offset bqe_diag_offset(d, M): uint64
- * [3][1024 CTAs][8 counters], zeroed by bqe_workspace_init.  Blocks 0 and 1
- * (W1/W3 and W2 kernels): producer waiting / issuing, consumer waiting for a
- * stage / for a reduction buffer / computing, epilogue waiting / working,
- * whole CTA.  Block 2 (router): counter 0 = CTA start to its logits written;
- * row 1022 counter 1 = start to end of the CTA that selects the experts, row
- * 1021 = its stage stamps.  Row 1023 of every block holds globaltimer
- * stamps (the caller presets minima to a large value and maxima to 0):
- * [0] first CTA start (minimum), [1] last CTA end (maximum); blocks 0 and 1:
- * [2] / [3] first / last CTA past its wait; block 2: [4] / [5] k_finalize_a
- * past its wait / last CTA end, [6] / [7] the same for k_finalize_b. */
+/* Diagnostic mode (default off): the decode kernel adds per-CTA timings into
+ * the workspace at byte offset bqe_diag_offset(d, M): uint64 [3][1024][8],
+ * zeroed by bqe_workspace_init.  Row 1023 of blocks 0 and 1 holds globaltimer
+ * stamps kept as minima or maxima over CTAs (the caller presets minima to a
+ * large value): block 0 [0] first CTA start, [1] last logits published,
+ * [2] first routing known, [3] first work item landed, [4] last W1/W3 item
+ * done, [6] last CTA end, [7] last producer done; block 1 [1] last compute
+ * warp done, [2] last routing known, [3] longest producer wait for h (ns).
+ * Rows 0..CTAs-1 (ns unless noted): block 0 [0] input staged, [1] staged
+ * slices fenced, [2] all logits seen, [3] / [5] / [7] waits at the three grid
+ * barriers, [4] the h phase, [6] the combine; block 1 [0] producer loop
+ * (cycles), [1] items issued, [2] logits published, [3] routing known, [4]
+ * router rows landed, [5] / [6] / [7] producer cycles issuing bulk copies /
+ * waiting for ring space / waiting for h; block 2 [1] producer wait for h,
+ * [2] / [3] compute warp 0 waiting / computing, [4] reducer waiting, [7] CTA
+ * start to end.  Block 0 rows 300 + CTA: routing step ends ([0] logits read,
+ * [1] top-k, [2] work list, [3] row slots). */
 void bqe_set_diag(int32_t on);
-
-/* bqe_moe_layer_forward and bqe_moe_step run the layer as the router kernel
- * followed by the bqe_experts kernels (default, on = 0), or as one
- * cooperatively launched persistent kernel (on = 1).  Same results up to the
- * order of the fp32 additions inside the router. */
-void bqe_set_fused(int32_t on);
 
 /* Operand type of the prefill tensor-core GEMMs: 1 (default) fp16 with the
  * per-token power-of-two scaling described at bqe_moe_prefill, MXFP4 experts
@@ -368,18 +359,6 @@ void bqe_set_fused(int32_t on);
  * bits: relative L2 error about 3e-3 against exact arithmetic, against about
  * 4e-4 for fp16).  Both run at the same tensor-core rate. */
 void bqe_set_prefill_f16(int32_t on);
-
-/* Diagnostic: at most n_a (W1/W3 kernel) and n_b (W2 kernel) ring stages of
- * shared-expert weights streamed by each expert-kernel CTA before it waits
- * for the previous kernel (default 16: as many as the ring holds; 0: none).
- * Results do not change. */
-void bqe_set_preload(int32_t n_a, int32_t n_b);
-
-/* Diagnostic: at most max_a (W1/W3) and max_b (W2) 32-row panels per work
- * item of the decode expert kernels (0: the default choice, the largest that
- * fits).  Fewer panels per item leave room for more ring stages.  Results do
- * not change. */
-void bqe_set_panels(int32_t max_a, int32_t max_b);
 
 /* Diagnostic (with bqe_set_diag(1)): bqe_moe_prefill records CUDA events on
  * its stream around each of its 8 kernels (router logits, selection, plan,

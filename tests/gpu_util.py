@@ -49,7 +49,22 @@ class DeviceLayer:
             self.ws_M = M
         return self.ws, self.ws_bytes
 
-    def forward(self, x_bits, forced=None, use_bias=True, accumulate_into=None, split=False):
+    def route(self, x_bits, use_bias=True):
+        """The routing-only entry point: (idx, w)."""
+        import torch
+        A = self.A
+        M = x_bits.shape[0]
+        ws, nb = self.workspace(M)
+        x = torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).to(self.dev)
+        idx = torch.zeros(M, self.K, dtype=torch.int32, device=self.dev)
+        w = torch.zeros(M, self.K, dtype=torch.float32, device=self.dev)
+        A.bqe_route(self.d, M, x, self.wr, self.bias if use_bias else None, self.pool.cstruct(), self.table, None,
+                    idx, w, ws, nb)
+        rc, det = A.bqe_check(ws)
+        assert rc == A.BQE_OK, (A.status_name(rc), det)
+        return idx.cpu().numpy(), w.cpu().numpy()
+
+    def forward(self, x_bits, forced=None, use_bias=True, accumulate_into=None):
         import torch
         A = self.A
         M = x_bits.shape[0]
@@ -60,12 +75,8 @@ class DeviceLayer:
         w = torch.zeros(M, self.K, dtype=torch.float32, device=self.dev)
         fi = None if forced is None else torch.from_numpy(np.ascontiguousarray(forced, dtype=np.int32)).to(self.dev)
         b = self.bias if use_bias else None
-        if split:
-            A.bqe_route(self.d, M, x, self.wr, b, self.pool.cstruct(), self.table, fi, idx, w, ws, nb)
-            A.bqe_experts(self.d, M, self.pool.cstruct(), out, accumulate_into is not None, ws, nb)
-        else:
-            A.bqe_moe_layer_forward(self.d, M, x, self.wr, b, self.pool.cstruct(), self.table, fi, out,
-                                    accumulate_into is not None, idx, w, ws, nb)
+        A.bqe_moe_layer_forward(self.d, M, x, self.wr, b, self.pool.cstruct(), self.table, fi, out,
+                                accumulate_into is not None, idx, w, ws, nb)
         rc, det = A.bqe_check(ws)
         assert rc == A.BQE_OK, (A.status_name(rc), det)
         return out.double().cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
@@ -95,8 +106,11 @@ def check_out(got, ref, rel=REL_L2, mabs=MAX_ABS, what=""):
 
 
 def oracle_layer_sampled(L_fmts, get_canon, x_bits, router, bias, idx, H, I, E, K, cols, shared=None):
-    """Oracle outputs out[m, n] for n in `cols` with the selection idx (M, K):
-    full fp64 W1/W3 of every used expert, only the sampled rows of W2."""
+    """Oracle outputs out[m, n] for n in `cols` (None: every column) with the
+    selection idx (M, K): full fp64 W1/W3 of every used expert and the
+    requested rows of W2."""
+    if cols is None:
+        cols = np.arange(H)
     shared = E if shared is None else shared
     x = O.bf16_bits_to_f64(x_bits).reshape(-1, H)
     r = O.route(x, router, bias, K, idx)
@@ -110,7 +124,10 @@ def oracle_layer_sampled(L_fmts, get_canon, x_bits, router, bias, idx, H, I, E, 
         w3 = F.dequant_matrix(fmt, p3, I, H)
         bw, bb = F.BLOCK[fmt]
         rowb = (I // bw) * bb
-        w2 = np.stack([F.dequant_matrix(fmt, p2[n * rowb:(n + 1) * rowb], 1, I)[0] for n in cols])
+        if len(cols) == H and np.array_equal(cols, np.arange(H)):
+            w2 = F.dequant_matrix(fmt, p2, H, I)
+        else:
+            w2 = np.stack([F.dequant_matrix(fmt, p2[n * rowb:(n + 1) * rowb], 1, I)[0] for n in cols])
         rows = [m for m in range(M) if e == shared or e in set(np.asarray(idx)[m].tolist())]
         h = O.silu(x[rows] @ w1.T) * (x[rows] @ w3.T)
         y = h @ w2.T

@@ -162,3 +162,94 @@ def test_argument_checks_before_any_device_work(A):
     assert lib.bqe_moe_prefill(ctypes.byref(d), 64, fake, fake, None, ctypes.byref(pool), fake, None, fake, 0, None,
                                None, fake, pneed - 256, None) == A.BQE_ENOSPC
     assert lib.bqe_workspace_init(None, 16, None) == A.BQE_EINVAL
+
+
+@pytest.mark.parametrize("fmt", [F.TQ1, F.Q2_0, F.Q3_K, F.MXFP4])
+def test_unpack_host_inverts_pack(A, fmt):
+    """bqe_unpack_host returns the codes and scale bytes bqe_pack was given,
+    for every code of the format's domain."""
+    rng = np.random.default_rng(40 + fmt)
+    rows, cols = 3, 1024
+    bw, _ = F.BLOCK[fmt]
+    nblk = rows * cols // bw
+    hi = {F.TQ1: 3, F.Q2_0: 4, F.Q3_K: 8, F.MXFP4: 16}[fmt]
+    codes = rng.integers(0, hi, size=rows * cols, dtype=np.uint8)
+    sb = A_SB[fmt]
+    if fmt == F.MXFP4:
+        scales = rng.integers(0, 255, size=nblk, dtype=np.uint8)  # 255 (NaN) is not an encodable scale
+    elif fmt == F.Q3_K:
+        d = rng.integers(0, 256, size=(nblk, 2), dtype=np.uint8)
+        scales = np.concatenate([rng.integers(0, 64, size=(nblk, 16), dtype=np.uint8), d], axis=1).reshape(-1)
+    else:
+        scales = rng.integers(0, 256, size=nblk * 2, dtype=np.uint8)
+    packed = np.zeros(A.bqe_packed_bytes(fmt, rows, cols), dtype=np.uint8)
+    A.bqe_pack(fmt, rows, cols, codes, np.ascontiguousarray(scales), packed)
+    c2 = np.zeros_like(codes)
+    s2 = np.zeros(nblk * sb, dtype=np.uint8)
+    A.bqe_unpack_host(fmt, rows, cols, packed, c2, s2)
+    assert np.array_equal(c2, codes)
+    assert np.array_equal(s2, scales)
+
+
+def test_unpack_host_rejects_bad_ternary_byte(A):
+    blk = np.zeros(56, dtype=np.uint8)
+    blk[7] = 243  # five trits span 0..242
+    with pytest.raises(A.BqeError) as e:
+        A.bqe_unpack_host(A.BQE_FMT_TQ1, 1, 256, blk, np.zeros(256, np.uint8), np.zeros(2, np.uint8))
+    assert e.value.status == A.BQE_EINVAL
+
+
+def test_pool_bytes_layout(A):
+    """Pool size = the two tables (uint64 offsets, int32 formats, each rounded
+    up to 256 bytes) + every slot's expert bytes rounded up to 256."""
+    d = A.desc(5120, 2304, 384, 6)
+    fm = np.array([F.TQ1, F.Q2_0, F.Q3_K, F.MXFP4, F.Q2_0], dtype=np.int32)
+    up = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    want = up(8 * 5) + up(4 * 5) + sum(up(synth.expert_bytes(int(f), 5120, 2304)) for f in fm)
+    assert A.bqe_pool_bytes(d, fm) == want
+    assert A.bqe_pool_bytes(d, np.array([1, 5], np.int32)) == 0  # unknown format
+    assert A.bqe_pool_bytes(A.desc(5000, 2304, 384, 6), fm) == 0
+
+
+def test_pool_init_argument_checks(A):
+    """bqe_pool_init rejects bad arguments before any copy: no GPU is needed
+    to see the status (the fake device address is never dereferenced)."""
+    import ctypes
+    d = A.desc(5120, 2304, 384, 6)
+    fm = np.array([F.MXFP4, F.Q2_0], dtype=np.int32)
+    need = A.bqe_pool_bytes(d, fm)
+    p = A.bqe_pool()
+    fp = fm.ctypes.data
+    lib = A.lib
+    assert lib.bqe_pool_init(None, ctypes.byref(d), 2, fp, 1 << 20, need, None) == A.BQE_EINVAL
+    assert lib.bqe_pool_init(ctypes.byref(p), ctypes.byref(d), 0, fp, 1 << 20, need, None) == A.BQE_EINVAL
+    assert lib.bqe_pool_init(ctypes.byref(p), ctypes.byref(d), 2, fp, None, need, None) == A.BQE_EINVAL
+    assert lib.bqe_pool_init(ctypes.byref(p), ctypes.byref(d), 2, fp, (1 << 20) + 64, need, None) == A.BQE_EINVAL
+    assert lib.bqe_pool_init(ctypes.byref(p), ctypes.byref(d), 2, fp, 1 << 20, need - 1, None) == A.BQE_ENOSPC
+    bad = np.array([F.MXFP4, 7], dtype=np.int32)
+    assert lib.bqe_pool_init(ctypes.byref(p), ctypes.byref(d), 2, bad.ctypes.data, 1 << 20, need, None) == A.BQE_EINVAL
+    # upload: slot out of range or an empty pool struct
+    assert lib.bqe_pool_upload(ctypes.byref(p), ctypes.byref(d), 0, 1 << 20, None) == A.BQE_EINVAL
+
+
+def test_noalloc_argument_checks_before_any_device_work(A):
+    """The allocation-free entry point checks its arguments before it touches
+    its fixed device array: without a GPU, a bad call still gets its own
+    status (a call that reached the device would report BQE_ECUDA)."""
+    import ctypes
+    lib = A.lib
+    d = A.desc(1024, 768, 24, 3)
+    fake = ctypes.c_void_p(1 << 20)
+    pool = A.bqe_pool(base=1 << 20, base_bytes=1 << 30, slot_off=1 << 21, slot_fmt=1 << 22, n_slots=25)
+    bad_pool = A.bqe_pool(base=None, base_bytes=0, slot_off=None, slot_fmt=None, n_slots=0)
+    call = lambda dd, M, x, p, out: lib.bqe_moe_layer_forward_noalloc(  # noqa: E731
+        ctypes.byref(dd), M, x, fake, None, ctypes.byref(p), fake, None, out, 0, None, None, None, None)
+    assert call(d, 0, fake, pool, fake) == A.BQE_EINVAL       # no rows
+    assert call(d, 9, fake, pool, fake) == A.BQE_EINVAL       # more than 8 rows
+    assert call(d, 1, None, pool, fake) == A.BQE_EINVAL       # no input
+    assert call(d, 1, fake, pool, None) == A.BQE_EINVAL       # no output
+    assert call(d, 1, fake, bad_pool, fake) == A.BQE_EINVAL   # empty pool
+    assert call(A.desc(1000, 768, 24, 3), 1, fake, pool, fake) == A.BQE_EINVAL  # hidden not a multiple of 512
+    big = A.desc(5120, 2304, 384, 6)
+    assert A.bqe_workspace_bytes(big, 7) > 8 << 20
+    assert call(big, 7, fake, pool, fake) == A.BQE_ENOSPC     # workspace beyond the fixed array

@@ -107,29 +107,23 @@ def test_mixed_small_layer(dev, M):
     check_routing(ref, idx, w)
     ref2 = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 1024, 768, 3, 24, forced_idx=idx)
     check_out(out, ref2["out"], what="mixed M=%d" % M)
-    # split entry points give the same bits
-    out2, idx2, _ = DL.forward(L["x"], split=True)
-    assert np.array_equal(out, out2) and np.array_equal(idx, idx2)
+    # the routing-only entry point selects the same experts with the same weights
+    idx2, w2 = DL.route(L["x"])
+    assert np.array_equal(idx, idx2) and np.allclose(w, w2, rtol=1e-6, atol=0)
 
 
-@pytest.mark.parametrize("variant", [0, 1])
 @pytest.mark.parametrize("fmt", ALL)
-def test_single_format_layer(dev, fmt, variant):
-    from bit_quantised_expert_gb300 import _abi as A
+def test_single_format_layer(dev, fmt):
     fm = [fmt] * 9
     L = synth.small_layer(40 + fmt, fm, 512, 512, 8, 2, 3, bias_std=0.0)
     # activations spanning many binades exercise the per-row f16 scaling
     L["x"][1] = synth.x_bf16(np.random.default_rng(3), 1, 512, std=1e-3)[0]
     L["x"][2] = synth.x_bf16(np.random.default_rng(4), 1, 512, std=20.0)[0]
     DL = DeviceLayer(L, dev)
-    A.bqe_set_variant(variant)
-    try:
-        out, idx, w = DL.forward(L["x"], forced=np.array([[0, 1], [2, 3], [4, 5]], np.int32))
-    finally:
-        A.bqe_set_variant(1)
+    out, idx, w = DL.forward(L["x"], forced=np.array([[0, 1], [2, 3], [4, 5]], np.int32))
     ref2 = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 512, 512, 2, 8, forced_idx=idx)
     for m in range(3):  # rows differ by orders of magnitude: check each on its own scale
-        check_out(out[m], ref2["out"][m], what="fmt %d variant %d row %d" % (fmt, variant, m))
+        check_out(out[m], ref2["out"][m], what="fmt %d row %d" % (fmt, m))
 
 
 def test_bias_changes_selection_not_weights(dev):
@@ -179,52 +173,47 @@ def test_forced_idx_with_repeats_and_accumulate(dev):
     assert np.array_equal(idx, forced)
     ref = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 512, 256, 3, 16, forced_idx=forced)
     assert np.allclose(w, ref["w"], rtol=2e-6)
-    check_out(out - keep, ref["out"], rel=2e-4, what="accumulate")
+    # out = prior + layer, against the same sum in fp64 at the decode bar
+    check_out(out, keep + ref["out"], what="accumulate")
 
 
 @pytest.mark.parametrize("M", [1, 2, 6, 8])
-def test_fused_layer_kernel(dev, M):
-    """The single-kernel layer (cooperative persistent kernel) against the oracle."""
-    from bit_quantised_expert_gb300 import _abi as A
+def test_repeated_calls_identical(dev, M):
+    """Consecutive calls on one workspace (the call epoch and the arrival
+    counters advance from call to call) give identical bits and routing."""
     fm = [ALL[(3 * e + 2) % 4] for e in range(24)] + [synth.MXFP4]
     L = synth.small_layer(60 + M, fm, 1024, 768, 24, 3, M, bias_std=0.25)
     DL = DeviceLayer(L, dev)
-    A.bqe_set_fused(True)
-    try:
-        out, idx, w = DL.forward(L["x"])
-        out2, idx2, _ = DL.forward(L["x"])
-    finally:
-        A.bqe_set_fused(False)
+    out, idx, w = DL.forward(L["x"])
     ref = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 1024, 768, 3, 24)
     check_routing(ref, idx, w)
     ref2 = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 1024, 768, 3, 24, forced_idx=idx)
-    check_out(out, ref2["out"], what="fused M=%d" % M)
-    assert np.array_equal(out, out2) and np.array_equal(idx, idx2)  # deterministic, counters reset
+    check_out(out, ref2["out"], what="M=%d" % M)
+    for _ in range(5):
+        out2, idx2, _ = DL.forward(L["x"])
+        assert np.array_equal(out, out2) and np.array_equal(idx, idx2)
 
 
-def test_deterministic(dev):
-    fm = [ALL[e % 4] for e in range(33)]
-    L = synth.small_layer(9, fm, 1024, 512, 32, 4, 6, bias_std=0.25)
-    DL = DeviceLayer(L, dev)
-    a = DL.forward(L["x"])
-    b = DL.forward(L["x"])
-    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
-
-
-def test_preload_does_not_change_results(dev):
-    """Streaming the shared expert's tiles before the routing wait is a
-    scheduling choice only: with and without it the outputs are identical."""
+def test_layer_stats(dev):
+    """bqe_layer_stats reports the distinct experts the call streamed and
+    their bytes, which the oracle's byte count states independently."""
     from bit_quantised_expert_gb300 import _abi as A
-    fm = [ALL[e % 4] for e in range(33)]
-    L = synth.small_layer(10, fm, 1024, 512, 32, 4, 3, bias_std=0.25)
+    fm = [ALL[e % 4] for e in range(24)] + [synth.Q2_0]
+    L = synth.small_layer(71, fm, 1024, 768, 24, 3, 4, bias_std=0.25)
     DL = DeviceLayer(L, dev)
-    a = DL.forward(L["x"])
-    A.bqe_set_preload(0, 0)
-    try:
-        b = DL.forward(L["x"])
-    finally:
-        A.bqe_set_preload(16, 16)
-    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    _, idx, _ = DL.forward(L["x"])
+    ws, _ = DL.workspace(4)
+    st = A.bqe_layer_stats(DL.d, 4, ws)
+    distinct = set(idx.reshape(-1).tolist())
+    assert st["rows"] == 4 and st["experts_streamed"] == len(distinct) + 1
+    assert st["expert_bytes"] == O.expert_bytes_streamed(idx, L["fmts"], 1024, 768, 24)
+    assert st["router_bytes"] == 24 * 1024 * 4
+    per = [0] * 5
+    for e in distinct | {24}:
+        per[int(L["fmts"][e])] += 1
+    assert st["per_format"] == per
+    # every row chose 3 distinct experts, and the shared expert serves all 4
+    assert st["row_uses"] == 4 * 3 + 4
 
 
 # ------------------------------------------------------- error reporting
@@ -266,8 +255,8 @@ def test_host_argument_errors(dev):
 
 
 def test_wait_timeout_is_reported_and_recoverable(dev):
-    """A stage that never lands (the host tells CTA 0's producer to skip one
-    item) makes the consumers' bounded wait run out: the call reports
+    """A work item that never lands (the host tells CTA 0's producers to skip
+    its copies) makes the bounded waits run out: the call reports
     BQE_ETIMEOUT, and after re-initialising the workspace the next call is
     correct.  No GPU fault is involved."""
     import torch

@@ -1,6 +1,7 @@
 """GPU parity at the full DeepSeek-V4.1-Flash layer sizes (hidden 5120,
 inter 2304, 384 routed + 1 shared, top-6), in the launch configuration the
-benchmark times, on sampled outputs the oracle computes one by one."""
+benchmark times: every output element of the decode layers against the fp64
+oracle, and of the prefill layer on sampled tokens and 1024 columns."""
 import numpy as np
 import pytest
 
@@ -40,13 +41,13 @@ def _run_layer(W, dev, xi, M):
     return out.double().cpu().numpy(), idx.cpu().numpy(), wts.cpu().numpy(), x_bits
 
 
-def _check_layer(W, dev, M, xi, ncols=48):
+def _check_layer(W, dev, M, xi):
     out, idx, wts, x_bits = _run_layer(W, dev, xi, M)
     router = W.wr.cpu().numpy()
     bias = None if W.bias is None else W.bias.cpu().numpy()
     ref = O.route(O.bf16_bits_to_f64(x_bits), router, bias, K)
-    check_routing(ref, idx, wts)
-    cols = np.random.default_rng(xi).choice(H, ncols, replace=False)
+    assert check_routing(ref, idx, wts) > 0  # at least one row's selection is compared (not all near-ties)
+    cols = None  # every column
     cache = {}
 
     def canon(e):
@@ -55,7 +56,7 @@ def _check_layer(W, dev, M, xi, ncols=48):
         return cache[e]
     oref, r2 = oracle_layer_sampled(W.fmts, canon, x_bits, router, bias, idx, H, I, E, K, cols)
     assert np.allclose(wts, r2["w"], rtol=2e-6, atol=0)
-    return check_out(out[:, cols], oref, what="full M=%d" % M)
+    return check_out(out, oref, what="full M=%d" % M)
 
 
 def test_fp4_layer_m1(dev):
@@ -69,11 +70,10 @@ def test_fp4_layer_m1(dev):
 def test_mixed_layer(dev, M):
     from synth import workloads as WL
     W = WL.mixed_layer(dev, m=M, n_x=2)
-    _check_layer(W, dev, M, 0, ncols=24 if M > 1 else 48)
+    _check_layer(W, dev, M, 0)
 
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_step40_teacher_forced(dev, fused):
+def test_step40_teacher_forced(dev):
     """40 chained layers over the 4288-slot pool (Zipf-forced routing): the
     whole step equals the layer-by-layer run bit for bit, each layer's input
     is the bf16 RMS-normalised residual, and sampled layers match the oracle
@@ -82,7 +82,6 @@ def test_step40_teacher_forced(dev, fused):
     from bit_quantised_expert_gb300 import _abi as A
     from synth import workloads as WL
     M = 1
-    A.bqe_set_fused(fused)
     S = WL.Step40(dev, m=M, n_steps_forced=1)
     L = S.n_layers
     nb = A.bqe_workspace_bytes(S.d, M)
@@ -110,15 +109,15 @@ def test_step40_teacher_forced(dev, fused):
         diff = np.abs(t_np[l].astype(np.int64) - want.astype(np.int64))
         assert diff.max() <= 1 and (diff > 0).mean() < 0.01, l
     router_all = S.wr.cpu().numpy()
-    for l in (0, 17, 39):
+    # eight of the 40 layers, every column: each layer's own output (the
+    # residual difference) against the oracle fed that layer's GPU input
+    for l in (0, 5, 11, 17, 23, 29, 34, 39):
         table = S.tables_np[l]
         fm = np.array([S.fmts[table[e]] for e in range(E + 1)], dtype=np.int32)
-        cols = np.random.default_rng(l).choice(H, 32, replace=False)
         oref, _ = oracle_layer_sampled(fm, lambda e: S.canon(int(table[e])).cpu().numpy(), t_np[l], router_all[l],
-                                       None, S.forced_np[0, l], H, I, E, K, cols)
-        got = (snaps[l + 1] - snaps[l])[:, cols]
+                                       None, S.forced_np[0, l], H, I, E, K, None)
+        got = snaps[l + 1] - snaps[l]
         check_out(got, oref, rel=1e-4, what="layer %d" % l)
-    A.bqe_set_fused(False)
 
 
 PF_TOL = 5e-3
@@ -189,7 +188,7 @@ def test_prefill_dsv4_zipf(dev):
     cnt = W.counts()
     assert cnt.sum() == T * K and cnt.max() > 512
     sample, most, least = _prefill_sample(W.forced_np, cnt, budget=48)
-    cols = np.random.default_rng(3).choice(H, 256, replace=False)
+    cols = np.random.default_rng(3).choice(H, 1024, replace=False)
     cache = {}
 
     def canon(e):
