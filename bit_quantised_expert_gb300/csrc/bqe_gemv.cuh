@@ -277,6 +277,36 @@ __device__ __forceinline__ void group_q3k_i(const uint8_t* tile, int nb, int grp
   for (int r = 0; r < R; ++r) acc[r].x = fmaf(d * row[r].sc, hi_lo(bh[r], bl[r]), acc[r].x);
 }
 
+// One 32-bit word of a TQ1 row (bytes 4m .. 4m + 3: run m of 20 columns):
+// its five base-3 digits per byte, met with the T-order X of run m.
+template <int R>
+__device__ __forceinline__ void tq1_run(uint32_t wv, int m, const IntRow (&row)[R], int (&ih)[R], int (&il)[R]) {
+  // bytes 4m, 4m+2 in the 16-bit lanes of ve; 4m+1, 4m+3 in vo
+  uint32_t ve = wv & 0x00FF00FFu, vo = (wv >> 8) & 0x00FF00FFu;
+  int B[5];
+#pragma unroll
+  for (int rd = 0; rd < 5; ++rd) {
+    // digit rd of the four bytes: v / 3 per 16-bit lane ((v * 171) >> 9 for v <= 255)
+    const uint32_t qe = ((ve * 171u) >> 9) & 0x007F007Fu, qo = ((vo * 171u) >> 9) & 0x007F007Fu;
+    const uint32_t de = ve - 3u * qe, dq = vo - 3u * qo;
+    ve = qe;
+    vo = qo;
+    B[rd] = (int)__byte_perm(de, dq, 0x6240);  // digits of bytes 4m, 4m+1, 4m+2, 4m+3
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int2* xp = reinterpret_cast<const int2*>(row[r].xh + m * 40);
+    const int* xl = reinterpret_cast<const int*>(row[r].xl + m * 20);
+#pragma unroll
+    for (int rd = 0; rd < 5; ++rd) {
+      const int2 v = xp[rd];
+      ih[r] = __dp2a_lo(v.x, B[rd], ih[r]);
+      ih[r] = __dp2a_hi(v.y, B[rd], ih[r]);
+      il[r] = __dp4a(xl[rd], B[rd], il[r]);
+    }
+  }
+}
+
 template <int R>
 __device__ __forceinline__ void group_tq1_i(const uint8_t* tile, int nb, int grp, const uint8_t* act, int rowb,
                                             int kc, int lane, float2 (&acc)[R]) {
@@ -284,45 +314,22 @@ __device__ __forceinline__ void group_tq1_i(const uint8_t* tile, int nb, int grp
 #pragma unroll
   for (int r = 0; r < R; ++r) row[r] = int_row(act, r, rowb, BQE_FMT_TQ1, kc, grp);
   const int b = grp;
-  uint32_t W[13];
-#pragma unroll
-  for (int q = 0; q < 3; ++q) {
-    const uint4 v = *reinterpret_cast<const uint4*>(tile + (b * 3 + q) * 512 + lane * 16);
-    W[4 * q] = v.x; W[4 * q + 1] = v.y; W[4 * q + 2] = v.z; W[4 * q + 3] = v.w;
-  }
   const uint2 tail = *reinterpret_cast<const uint2*>(tile + nb * 1536 + (b * 32 + lane) * 8);
-  W[12] = tail.x;  // bytes 48..51 (byte 51 <= 2: its higher digits are 0)
   const float d = __half2float(__ushort_as_half((unsigned short)(tail.y & 0xFFFFu)));
   int ih[R], il[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) ih[r] = il[r] = 0;
+  // words 0..11 (bytes 0..47) four at a time, then word 12 (bytes 48..51;
+  // byte 51 <= 2, so its higher digits are 0)
 #pragma unroll 1
-  for (int m = 0; m < 13; ++m) {
-    // bytes 4m, 4m+2 in the 16-bit lanes of ve; 4m+1, 4m+3 in vo
-    uint32_t ve = W[m] & 0x00FF00FFu, vo = (W[m] >> 8) & 0x00FF00FFu;
-    int B[5];
-#pragma unroll
-    for (int rd = 0; rd < 5; ++rd) {
-      // digit rd of the four bytes: v / 3 per 16-bit lane ((v * 171) >> 9 for v <= 255)
-      const uint32_t qe = ((ve * 171u) >> 9) & 0x007F007Fu, qo = ((vo * 171u) >> 9) & 0x007F007Fu;
-      const uint32_t de = ve - 3u * qe, dq = vo - 3u * qo;
-      ve = qe;
-      vo = qo;
-      B[rd] = (int)__byte_perm(de, dq, 0x6240);  // digits of bytes 4m, 4m+1, 4m+2, 4m+3
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int2* xp = reinterpret_cast<const int2*>(row[r].xh + m * 40);
-      const int* xl = reinterpret_cast<const int*>(row[r].xl + m * 20);
-#pragma unroll
-      for (int rd = 0; rd < 5; ++rd) {
-        const int2 v = xp[rd];
-        ih[r] = __dp2a_lo(v.x, B[rd], ih[r]);
-        ih[r] = __dp2a_hi(v.y, B[rd], ih[r]);
-        il[r] = __dp4a(xl[rd], B[rd], il[r]);
-      }
-    }
+  for (int q = 0; q < 3; ++q) {
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + (b * 3 + q) * 512 + lane * 16);
+    tq1_run<R>(v.x, 4 * q, row, ih, il);
+    tq1_run<R>(v.y, 4 * q + 1, row, ih, il);
+    tq1_run<R>(v.z, 4 * q + 2, row, ih, il);
+    tq1_run<R>(v.w, 4 * q + 3, row, ih, il);
   }
+  tq1_run<R>(tail.x, 12, row, ih, il);
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     int Sh = 0, Sl = 0;

@@ -78,6 +78,7 @@ __host__ __device__ inline uint32_t tile_byte_offset(int f, int nb, int b, int r
 constexpr int kMaxM = 8;          // rows per decode call
 constexpr int kMaxTopK = 16;
 constexpr int kRowChunk = 4;      // rows accumulated together by the widest inner loops
+constexpr int kMaxU = 64;         // distinct experts of one decode call (M top_k + 1 <= 64)
 
 struct Geo {
   int H, I, E, K, M;
@@ -117,11 +118,13 @@ struct WsLayout {
   // logits; the layer input in fp32, in f16 x 2^s, 2^-s per row, and as the
   // integer records of the two orders; the diagnostic counters
   uint64_t z, xf, xh, xsc, xrq, xrt, dbg;
-  // single-kernel decode layer (k_moe), per "row slot" (an expert's r-th row;
-  // M (K + 1) slots at most): call epoch, logits arrival counter, K-chunk
-  // partials of g/u and of y, h in fp32, the integer records of h, the grid
-  // barrier counter (64-bit, three arrivals per CTA per call)
-  uint64_t epoch, zt, m_done, m_pa, m_pb, m_h, m_hr;
+  // single-kernel decode layer: (selection key, logit) of every (row, expert)
+  uint64_t zk;
+  // single-kernel decode layer (k_moe): call epoch, logits arrival counter,
+  // per work-list expert the counts of its W1/W3 items done and of its h
+  // units written; per "row slot" (an expert's r-th row; M (K + 1) slots at
+  // most) the K-chunk partials of g/u, h in fp32 and the integer records of h
+  uint64_t epoch, zt, m_ca, m_ch, m_pa, m_h, m_hr;
   uint64_t total;
 };
 constexpr int kDbgSlots = 8;      // per-CTA counters of the diagnostic mode
@@ -153,13 +156,14 @@ __host__ __device__ inline WsLayout make_ws(const Geo& g) {
   w.xrq = o; o = al256(o + (uint64_t)int_rec_bytes(0, g.kcA) * g.M * g.nchA);
   w.xrt = o; o = al256(o + (uint64_t)int_rec_bytes(1, g.kcA) * g.M * g.nchA);
   w.dbg = o; o = al256(o + 8ull * 3 * kDbgMaxCtas * kDbgSlots);
-  // the call epoch and the two counters are contiguous: [epoch, m_pa) clears them
+  w.zk = o; o = al256(o + 8ull * g.M * g.E);
+  // the call epoch and the counters are contiguous: [epoch, m_pa) clears them
   w.epoch = o; o = al256(o + 16);
   w.zt = o; o = al256(o + 16);                                     // logits arrival counter (64-bit)
-  w.m_done = o; o = al256(o + 16);                                 // grid barrier counter (64-bit)
+  w.m_ca = o; o = al256(o + 4ull * kMaxU);                         // W1/W3 items done, per expert
+  w.m_ch = o; o = al256(o + 4ull * kMaxU);                         // h units written, per expert
   const uint64_t nrs = (uint64_t)g.M * (g.K + 1);
   w.m_pa = o; o = al256(o + 4ull * nrs * g.npanA * g.nchA * 2 * 32);
-  w.m_pb = o; o = al256(o + 4ull * nrs * g.nchB * g.H);
   w.m_h = o; o = al256(o + 4ull * nrs * g.I);
   w.m_hr = o; o = al256(o + (uint64_t)int_rec_bytes(1, g.kcB) * nrs * g.nchB);
   w.total = o;

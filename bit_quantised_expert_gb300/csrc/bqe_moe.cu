@@ -6,28 +6,26 @@
 //
 //   * one CTA per SM, launched cooperatively (every CTA resident, so CTAs may
 //     wait on one another; every such wait is bounded by %globaltimer);
-//   * warp 0 (one lane) streams work items into a byte ring in shared memory
-//     with cp.async.bulk and mbarrier completion; warps 1..16 compute; warp
-//     17 finishes each item (partial sums out, dependency counters);
-//   * before the routing is known, the producer streams this CTA's share of
+//   * warps 0-1 (one lane each) stream work items into a byte ring in shared
+//     memory with cp.async.bulk and mbarrier completion; warps 2-17 compute;
+//     warp 18 reduces each item (partial sums out, ring bytes freed); warp 19
+//     forms h = silu(g) * u;
+//   * before the routing is known, the producers stream this CTA's share of
 //     the shared expert's W1/W3 (always used), while the compute warps read
-//     this CTA's rows of the router (z = x Wr^T, fp32), write this CTA's slice
-//     of the staged activations, publish the logits tagged with the call's
-//     epoch, wait until every CTA's logits carry it, and then select the
-//     top-k and build the expert work list themselves (the same result in
-//     every CTA: no serial tail, no second kernel);
+//     this CTA's rows of the router (z = x Wr^T, fp32), publish (key, z) of
+//     those experts tagged with the call's epoch, and wait until every CTA's
+//     logits are in; then warp m selects row m's top-k from registers and
+//     warp 0 builds the work list, the row slots and the item templates (the
+//     same result in every CTA: no serial tail, no second kernel);
 //   * work items are (expert, 32-row panel, K chunk) of W1 and W3, then
 //     (expert, group of W2 output panels, K chunk) of W2, shared expert first,
 //     dealt round-robin over the CTAs, so every expert's W1/W3 is finished by
 //     all CTAs together, long before its W2 items come up;
-//   * the CTA that adds the last K chunk of a (expert, panel) forms
-//     h = silu(g) * u for it (a fixed order over the chunks); the last panel of
-//     a 256-column block of h writes its integer staging record; W2 items wait
-//     (bounded) only for the h chunk they read, and stream their weights
-//     before that wait;
-//   * the CTA that adds the last item of a W2 output panel group combines
-//     out = y_shared + sum_j w_j y_j for it, in a fixed order, so results are
-//     the same run to run.
+//   * no grid-wide barrier: the reducers count each expert's finished W1/W3
+//     items, the h warps form h for an expert once its count is complete, and
+//     the producers copy an expert's h rows once its h units are all written;
+//   * the W2 reducers add w_j y_j (the shared expert with weight 1) into the
+//     output rows with fp32 atomics.
 //
 // Router, selection and mixing follow the field report (384 routed experts,
 // 6 per token, one shared) and the Strata 4090 post, section 5.3 (the bias
@@ -44,10 +42,10 @@ namespace bqe {
 constexpr int kNQ = 16;                    // items in flight per CTA (barrier ring)
 constexpr int kCW = 16;                    // compute warps
 constexpr int kNP = 2;                     // producer warps
-// producers, compute warps, reducer: 19 warps, at most 5 per SM
+// producers, compute warps, reducer, h warp: 20 warps, 5 per SM
 // sub-partition, so each thread may hold 96 registers
-constexpr int kMoeThreads = 32 * (kNP + kCW + 1);
-constexpr int kMaxU = 64;                  // distinct experts of one call (M top_k + 1 <= 64)
+constexpr int kMoeThreads = 32 * (kNP + kCW + 2);
+constexpr int kRedWarp = kNP + kCW;  // then the h warp (the last)
 constexpr int kMaxEM = 512;                // routed experts supported
 constexpr int kRouteTasks = 16;            // (expert of this CTA, quarter of hidden) router tasks
 
@@ -209,7 +207,8 @@ __device__ inline void make_tpl(const MoeParams& P, ItemTpl& T, int ph, int u, i
 template <int RC>
 __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
   const Geo& g = P.g;
-  const int H = g.H, I = g.I, E = g.E, K = g.K, M = g.M;
+  // the one-row instance (RC == 1) runs only calls with M == 1: a constant there
+  const int H = g.H, I = g.I, E = g.E, K = g.K, M = RC == 1 ? 1 : g.M;
   const int G = gridDim.x, cta = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int32_t* err = (int32_t*)(P.ws + P.L.err);
@@ -222,7 +221,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
 
   __shared__ ItemHdr hdr[kNQ];
   __shared__ __align__(8) uint64_t full[kNQ], cons[kNQ], freed[kNQ], route_bar, rbar;
-  __shared__ __align__(8) uint64_t a_done, b_done, fb_bar;  // this CTA's W1/W3 / W2 partials written; h ready
+  __shared__ float s_rsw[kMaxM * (kMaxTopK + 1)];  // mixing weight of each row slot (shared expert: 1)
   __shared__ int s_rbase[kMaxU + 1];   // first row slot of each work-list expert
   __shared__ int s_rs[kMaxM][kMaxTopK];  // row slot of (row m, choice j)
   __shared__ int s_done[kNQ];
@@ -234,7 +233,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
   __shared__ float s_zsel[kMaxM][kMaxTopK];
   __shared__ uint32_t s_mask[kMaxEM];
   __shared__ int16_t s_uof[kMaxEM];
-  __shared__ int s_wcnt[kMaxEM / 32];
+  __shared__ int s_fidx[kMaxM][kMaxTopK];  // forced choices
+  __shared__ int s_first[kMaxEM];          // first (row, choice) index t = m K + j that chose each expert
   __shared__ float s_part[kRouteTasks][kMaxM];
   __shared__ float s_inv_rms[kMaxM], s_xsc[kMaxM];
   __shared__ int s_emax[kMaxM];
@@ -260,9 +260,6 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       mbar_init(&freed[s], 1);
       s_done[s] = 0;
     }
-    mbar_init(&a_done, 1);
-    mbar_init(&b_done, 1);
-    mbar_init(&fb_bar, 1);
     mbar_init(&route_bar, 1);
     mbar_init(&rbar, 1);
     s_abort = 0;
@@ -274,6 +271,10 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     s_bad = 0;
     s_nu = 0;
     fence_mbar_init();
+  }
+  for (int e = tid; e < E; e += kMoeThreads) {
+    s_mask[e] = 0u;
+    s_first[e] = 0x7FFF;
   }
   __syncthreads();
   if (tid == 0) mstamp(P, kStStart, false);
@@ -441,7 +442,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       const int nTot = nU * (nAper + nBper), nA = nU * nAper;
       long long hwait_max = 0;
       int dropped = -1;
-      bool h_ready = false;
+      int h_ready = -1;  // experts below this one have their h written
       long long cyc_loop = P.diag ? clock64() : 0, cyc_bulk = 0, cyc_alloc = 0, cyc_h = 0;
       int first = pp;
       while (first < npre) first += kNP;
@@ -490,12 +491,13 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         issue(i, T, p, c, true, false, false);
         if (P.diag) cyc_bulk += clock64() - tb0;
         issued = i;
-        if (ph == 1 && !h_ready) {
-          // h of every expert is written (all CTAs passed the h phase) before the
-          // first W2 activation rows are copied; the weights above are already on their way
+        if (ph == 1 && u > h_ready) {
+          // every h unit of expert u is written (by the h warps of all CTAs)
+          // before its rows are copied; the weights above are already on their way
           const long long w0 = P.diag ? (long long)globaltimer_ns() : 0;
           const long long tc0 = P.diag ? clock64() : 0;
-          if (!mwait(&fb_bar, 0, P.limit_ns, err)) {
+          const uint32_t need = (uint32_t)s_unrows[u] * (uint32_t)(I / 256);
+          if (!wait_ge((const unsigned int*)(P.ws + P.L.m_ch) + u, need, P.limit_ns, err)) {
             set_error(err, BQE_ETIMEOUT, kErrWaitFull);
             s_abort = 1;
             ok = false;  // the activation copies still go out (valid addresses) so the stage drains
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
             cyc_h += clock64() - tc0;
           }
           fence_proxy_async_global();
-          h_ready = true;
+          h_ready = u;
         }
         const long long tb1 = P.diag ? clock64() : 0;
         issue(i, T, p, c, false, true, false);
@@ -536,6 +538,12 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     const int Kq = H / 4, ni = Kq / 128;
     const int rj = cw >> 2, rq = cw & 3;
     const bool rtask = cw < nexp * 4;
+    // ---- first the loads that nothing computed here feeds (slot table, bias,
+    // forced choices): their latency overlaps the input staging below
+    const int sl0 = ct <= E ? P.slot_table[ct] : -1;
+    const int sl1 = ct + NCT <= E ? P.slot_table[ct + NCT] : -1;
+    const float bias0 = (ct < E && P.bias) ? P.bias[ct] : 0.f;
+    const int fidx0 = (P.forced && ct < M * K) ? P.forced[ct] : 0;
     // ---- the layer input as bf16 in shared memory: x, or bf16(rmsnorm(resid))
     uint16_t* xs = const_cast<uint16_t*>(s_x);
     if (ct < M) s_emax[ct] = -1000;
@@ -620,222 +628,60 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         }
       }
     }
-    // ---- selection inputs, read before the logits sync (no kernel writes them):
-    // the bias, and the slot descriptor of expert e = ct (e = E: the shared one)
-    for (int i = ct; i < E; i += NCT) s_bias[i] = P.bias ? P.bias[i] : 0.f;
-    auto slot_desc = [&](int e, int& slot, int& fmt, uint64_t& addr, int& bad) {
-      slot = P.slot_table[e];
-      fmt = 0;
-      addr = 0;
-      bad = 0;
+    // ---- this CTA's slice of the output (zero unless the call accumulates)
+    // and, in CTA 0, the per-expert counters of the call: both written before
+    // this CTA publishes its logits, so before any other CTA adds to them
+    if (!P.accumulate) {
+      const int n = M * H, per = (n + G - 1) / G, lo = min(n, per * cta), hi = min(n, lo + per);
+      for (int i = lo + ct; i < hi; i += NCT) P.out[i] = 0.f;
+    }
+    if (cta == 0 && ct < kMaxU) {
+      ((unsigned int*)(P.ws + P.L.m_ca))[ct] = 0u;
+      ((unsigned int*)(P.ws + P.L.m_ch))[ct] = 0u;
+    }
+    // ---- selection inputs: the bias, the forced choices (validated), and the
+    // slot descriptor of every expert (e = E: the shared one), into shared
+    // memory so that none of these loads waits until after the routing
+    if (ct < E) s_bias[ct] = bias0;
+    if (P.forced && ct < M * K) {
+      int f = fidx0;
+      if (f < 0 || f >= E) {
+        set_error(err, BQE_EDEVICE, kErrForcedIdx);
+        s_bad = 1;
+        f = 0;
+      }
+      s_fidx[ct / K][ct % K] = f;
+    }
+    auto slot_desc = [&](int e, int slot) {
+      int fmt = 0, bad = 0;
+      uint64_t addr = 0;
       if (slot < 0 || slot >= P.pool.n_slots) {
         bad = kErrSlotRange;
-        return;
+      } else {
+        const int f = P.pool.slot_fmt[slot];
+        const uint64_t off = P.pool.slot_off[slot];
+        if (!fmt_ok(f)) {
+          bad = kErrSlotFmt;
+        } else if ((off & 15) || off + 2 * matrix_bytes(f, I, H) + matrix_bytes(f, H, I) > P.pool.base_bytes) {
+          bad = kErrSlotExtent;
+        } else {
+          fmt = f;
+          addr = (uint64_t)P.pool.base + off;
+        }
       }
-      const int f = P.pool.slot_fmt[slot];
-      const uint64_t off = P.pool.slot_off[slot];
-      if (!fmt_ok(f)) {
-        bad = kErrSlotFmt;
-        return;
-      }
-      if ((off & 15) || off + 2 * matrix_bytes(f, I, H) + matrix_bytes(f, H, I) > P.pool.base_bytes) {
-        bad = kErrSlotExtent;
-        return;
-      }
-      fmt = f;
-      addr = (uint64_t)P.pool.base + off;
-    };
-    // into shared memory now, so none of these loads waits until after the routing
-    for (int e = ct; e <= E; e += NCT) {
-      int sl, f, bad;
-      uint64_t ad;
-      slot_desc(e, sl, f, ad, bad);
-      s_eslot[e] = (int16_t)sl;
-      s_efmt[e] = (uint8_t)f;
-      s_eaddr[e] = ad;
+      s_eslot[e] = (int16_t)slot;
+      s_efmt[e] = (uint8_t)fmt;
+      s_eaddr[e] = addr;
       s_ebad[e] = (uint8_t)bad;
-    }
+    };
+    if (ct <= E) slot_desc(ct, sl0);
+    if (ct + NCT <= E) slot_desc(ct + NCT, sl1);
     // the staged slices are read by other CTAs' bulk copies once the routing
     // is known: fence them now, while the router rows are still landing
     // (the gpu-scope release is the CTA's arrival on the logits counter below)
     fence_proxy_async_global();
     if (P.diag && ct == 0) dacc(P, 1, globaltimer_ns() - t_cta0, 0);
-    float* zg = (float*)(P.ws + P.L.z);
-    // The routing: keys, top-k, mixing weights, work list, row slots and item
-    // templates, once every CTA's logits are in
-    auto routing = [&]() {
-    // logits and selection keys of every (row, expert), all threads; the keys
-    // go where this CTA's router rows were (no longer needed)
-    uint32_t* s_key = reinterpret_cast<uint32_t*>(ring + P.rt_off);
-    const bool forced = P.forced != nullptr;
-    for (int i = ct; i < M * E; i += NCT) {
-      const float zv = __ldcg(zg + i);
-      s_z[i] = zv;
-      if (!forced) s_key[i] = sel_key(zv, s_bias[i % E]);
-    }
-    for (int i = ct; i < E; i += NCT) s_mask[i] = 0u;
-    named_bar_sync(1, NCT);
-    if (ct == 0) {
-      mstamp(P, kStRouted, false);
-      rstamp(P, 0, t_cta0);
-    }
-    // ---- top-k of each row (warp m selects row m), mixing weights
-    if (cw < M && !s_abort) {
-      const int m = cw;
-      constexpr int QN = kMaxEM / 32;
-      const int qn = (E + 31) / 32;
-      uint32_t kk[QN];
-#pragma unroll
-      for (int q = 0; q < QN; ++q) {
-        const int e = lane + 32 * q;
-        kk[q] = (!forced && q < qn && e < E) ? s_key[m * E + e] : 0u;
-      }
-      for (int j = 0; j < K; ++j) {
-        int best;
-        if (forced) {
-          best = P.forced[m * K + j];
-          if (best < 0 || best >= E) {
-            if (lane == 0) { set_error(err, BQE_EDEVICE, kErrForcedIdx); s_bad = 1; }
-            best = 0;
-          }
-        } else {
-          uint32_t bk = 0u;
-          int bq = 0;
-#pragma unroll
-          for (int q = 0; q < QN; ++q)
-            if (q < qn && kk[q] > bk) {
-              bk = kk[q];
-              bq = q;
-            }
-          const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
-          const uint32_t eb =
-              __reduce_min_sync(0xffffffffu, (bk == wk && wk != 0u) ? (uint32_t)(lane + 32 * bq) : 0xffffffffu);
-          if (eb != 0xffffffffu && (int)(eb & 31u) == lane) {
-#pragma unroll
-            for (int q = 0; q < QN; ++q)
-              if ((uint32_t)q == (eb >> 5)) kk[q] = 0u;
-          }
-          best = eb == 0xffffffffu ? 0 : (int)eb;
-        }
-        if (lane == 0) {
-          s_idx[m][j] = best;
-          s_zsel[m][j] = s_z[m * E + best];
-          atomicOr(&s_mask[best], 1u << m);
-        }
-      }
-      __syncwarp();
-      // w_j = s_j / sum s as exp(log s_j - max log s) / sum exp(...): finite
-      // even when every selected sigmoid underflows in fp32
-      float ls = -INFINITY;
-      if (lane < K) {
-        const float zz = s_zsel[m][lane];
-        ls = zz < 0.f ? zz - log1pf(expf(zz)) : -log1pf(expf(-zz));
-      }
-      float mx = ls;
-      for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float ev = lane < K ? expf(ls - mx) : 0.f;
-      float tot = ev;
-      for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-      if (lane < K) {
-        const float w = ev / tot;
-        s_cw[m][lane] = w;
-        if (cta == 0) {
-          if (P.topk_idx) P.topk_idx[m * K + lane] = s_idx[m][lane];
-          if (P.topk_w) P.topk_w[m * K + lane] = w;
-        }
-      }
-    }
-    named_bar_sync(1, NCT);
-    if (ct == 0) rstamp(P, 1, t_cta0);
-    // ---- work list: the chosen experts in ascending id order (u = 1..), shared u = 0
-    {
-      const int e = ct;  // E <= 512 = NCT
-      const bool on = e < E && s_mask[e] != 0u;
-      const uint32_t bal = __ballot_sync(0xffffffffu, on);
-      if (lane == 0) s_wcnt[cw] = __popc(bal);
-      named_bar_sync(1, NCT);
-      if (on) {
-        int base = 0;
-        for (int w2 = 0; w2 < cw; ++w2) base += s_wcnt[w2];
-        s_uof[e] = (int16_t)(1 + base + __popc(bal & ((1u << lane) - 1u)));
-      }
-      named_bar_sync(1, NCT);
-      if (on) {
-        const int u = s_uof[e];
-        const int my_bad = s_ebad[e], my_fmt = s_efmt[e], my_slot = s_eslot[e];
-        if (my_bad) {
-          set_error(err, BQE_EDEVICE, my_bad);
-          s_bad = 1;
-        }
-        s_ufmt[u] = my_fmt;
-        s_uaddr[u] = s_eaddr[e];
-        const uint32_t mask = s_mask[e];
-        int n = 0;
-        for (int m = 0; m < M; ++m)
-          if (mask & (1u << m)) s_urows[u * kMaxM + n++] = (int8_t)m;
-        s_unrows[u] = n;
-        if (cta == 0) {  // the call's work list, for bqe_layer_stats
-          ((int32_t*)(P.ws + P.L.u_slot))[u] = my_slot;
-          ((int32_t*)(P.ws + P.L.u_fmt))[u] = my_fmt;
-          ((int32_t*)(P.ws + P.L.u_nrows))[u] = n;
-        }
-      }
-      if (ct == NCT - 1) {
-        // the shared expert, u = 0 (validated like the others)
-        const int sh_bad = s_ebad[E], sh_fmt = s_efmt[E], sh_slot = s_eslot[E];
-        if (sh_bad) {
-          set_error(err, BQE_EDEVICE, sh_bad);
-          s_bad = 2;
-        }
-        s_ufmt[0] = sh_fmt;
-        s_uaddr[0] = s_eaddr[E];
-        s_unrows[0] = M;
-        if (cta == 0) {
-          ((int32_t*)(P.ws + P.L.u_slot))[0] = sh_slot;
-          ((int32_t*)(P.ws + P.L.u_fmt))[0] = sh_fmt;
-          ((int32_t*)(P.ws + P.L.u_nrows))[0] = M;
-        }
-        for (int m = 0; m < M; ++m) s_urows[m] = (int8_t)m;
-      }
-      named_bar_sync(1, NCT);
-      if (ct == 0) rstamp(P, 2, t_cta0);
-      if (ct == 0) {
-        int tot = 0;
-        for (int w2 = 0; w2 < kCW; ++w2) tot += s_wcnt[w2];
-        // row slots: the shared expert's M rows first, then each chosen
-        // expert's rows in work-list order
-        int acc = 0;
-        for (int u = 0; u <= tot; ++u) {
-          s_rbase[u] = acc;
-          acc += s_unrows[u];
-        }
-        s_rbase[tot + 1] = acc;
-        // on an invalid routed slot only the shared expert runs (the call
-        // reports the error; its output is undefined); an invalid shared slot
-        // or an aborted routing streams nothing
-        s_nu = (s_abort || s_bad == 2) ? 0 : s_bad ? 1 : 1 + tot;
-        if (cta == 0) *(int32_t*)(P.ws + P.L.nu) = s_nu;
-      }
-      named_bar_sync(1, NCT);
-      if (ct == 0) rstamp(P, 3, t_cta0);
-      if (ct < M * K && !s_abort) {
-        const int m = ct / K, j = ct % K;
-        const int ee = s_idx[m][j];
-        s_rs[m][j] = s_rbase[s_uof[ee]] + __popc(s_mask[ee] & ((1u << m) - 1u));
-      }
-      // item templates of every (phase, work-list expert)
-      if (ct >= 64 && ct < 64 + 2 * s_nu) {
-        const int ph = (ct - 64) & 1, u = (ct - 64) >> 1;
-        if (fmt_ok(s_ufmt[u])) make_tpl(P, s_tpl[ph][u], ph, u, s_ufmt[u], s_uaddr[u], s_unrows[u], s_rbase[u]);
-      }
-      named_bar_sync(1, NCT);
-      if (ct == 0) {
-        mstamp(P, kStRoutedMax, true);
-        if (P.diag) dacc(P, 3, globaltimer_ns() - t_cta0, 1);
-        mbar_arrive(&route_bar);
-      }
-    }
-    };
+    uint2* zk = (uint2*)(P.ws + P.L.zk);
     // ---- router dot products of this CTA's experts (rows landed in shared memory)
     {
       const bool okr = __all_sync(0xffffffffu, mwait(&rbar, 0, P.limit_ns, err));
@@ -876,8 +722,10 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     }
     named_bar_sync(1, NCT);  // logits partials of this CTA are in shared memory
     if (ct < nexp * M) {
+      // the logit and its selection key (the bias only steers the choice)
       const int j = ct / M, m = ct % M, e = cta + j * G;
-      zg[(size_t)m * E + e] = (s_part[4 * j][m] + s_part[4 * j + 1][m]) + (s_part[4 * j + 2][m] + s_part[4 * j + 3][m]);
+      const float zv = (s_part[4 * j][m] + s_part[4 * j + 1][m]) + (s_part[4 * j + 2][m] + s_part[4 * j + 3][m]);
+      zk[(size_t)m * E + e] = make_uint2(sel_key(zv, s_bias[e]), __float_as_uint(zv));
     }
     named_bar_sync(1, NCT);
     // publish: one arrival per CTA on the call's logits counter (monotonic:
@@ -904,14 +752,205 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         s_abort = 1;
       }
       if (P.diag) dacc(P, 2, globaltimer_ns() - t_cta0, 0);
+      rstamp(P, 0, t_cta0);
     }
     named_bar_sync(1, NCT);
-    routing();
+    // ---- the routing: per-row selection (warp m takes row m), then warp 0
+    // builds the work list, the row slots and the item templates
+    const bool forced = P.forced != nullptr;
+    if (cw < M) {
+      if (!s_abort) {
+        // Expert e's rank value is (key << 32) | ~e: keys descending, ties to
+        // the lower id, every value distinct.  Round j takes the largest value
+        // below round j - 1's winner (a tree over the lane's values, then the
+        // warp), so the values stay in registers.
+        const int m = cw;
+        constexpr int QN = kMaxEM / 32;
+        uint64_t vv[QN];
+        // every load issued before any is used (one round trip)
+#pragma unroll
+        for (int q = 0; q < QN; ++q) {
+          const int e = min(lane + 32 * q, E - 1);
+          const uint2 t = __ldcg(zk + (size_t)m * E + e);
+          vv[q] = ((uint64_t)t.x << 32) | t.y;
+        }
+#pragma unroll
+        for (int q = 0; q < QN; ++q) {
+          const int e = lane + 32 * q;
+          if (e < E) s_z[m * E + e] = __uint_as_float((uint32_t)vv[q]);
+          vv[q] = (e < E && !forced) ? ((vv[q] & 0xFFFFFFFF00000000ull) | (uint32_t)~e) : 0ull;
+        }
+        __syncwarp();
+        if (ct == 0) rstamp(P, 1, t_cta0);
+        uint64_t last = ~0ull;
+        for (int j = 0; j < K; ++j) {
+          int best;
+          if (forced) {
+            best = s_fidx[m][j];
+          } else {
+            uint64_t t[QN / 2];
+#pragma unroll
+            for (int q = 0; q < QN / 2; ++q) {
+              const uint64_t a = vv[2 * q] < last ? vv[2 * q] : 0ull;
+              const uint64_t b = vv[2 * q + 1] < last ? vv[2 * q + 1] : 0ull;
+              t[q] = a > b ? a : b;
+            }
+#pragma unroll
+            for (int w = QN / 4; w >= 1; w >>= 1)
+#pragma unroll
+              for (int q = 0; q < w; ++q) t[q] = t[q] > t[q + w] ? t[q] : t[q + w];
+            const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(t[0] >> 32));
+            const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(t[0] >> 32) == hi ? (uint32_t)t[0] : 0u);
+            last = ((uint64_t)hi << 32) | lo;
+            best = last ? (int)~lo : 0;
+          }
+          if (lane == 0) {
+            s_idx[m][j] = best;
+            s_zsel[m][j] = s_z[m * E + best];
+            atomicOr(&s_mask[best], 1u << m);
+            atomicMin(&s_first[best], m * K + j);
+          }
+        }
+        __syncwarp();
+        if (ct == 0) rstamp(P, 2, t_cta0);
+        // w_j = s_j / sum s as exp(log s_j - max log s) / sum exp(...): finite
+        // even when every selected sigmoid underflows in fp32
+        float ls = -INFINITY;
+        if (lane < K) {
+          const float zz = s_zsel[m][lane];
+          ls = zz < 0.f ? zz - log1pf(expf(zz)) : -log1pf(expf(-zz));
+        }
+        float mx = ls;
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float ev = lane < K ? expf(ls - mx) : 0.f;
+        float tot = ev;
+        for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (lane < K) {
+          const float w = ev / tot;
+          s_cw[m][lane] = w;
+          if (cta == 0) {
+            if (P.topk_idx) P.topk_idx[m * K + lane] = s_idx[m][lane];
+            if (P.topk_w) P.topk_w[m * K + lane] = w;
+          }
+        }
+      }
+      if (M > 1) named_bar_sync(2, 32 * M);  // every row's choices are in
+      if (cw == 0) {
+        if (lane == 0) {
+          mstamp(P, kStRouted, false);
+          rstamp(P, 3, t_cta0);
+        }
+        // work list: the chosen experts in the order of their first choice
+        // (row-major over (row, choice)), u = 1..; the shared expert u = 0
+        int base = 1;
+        for (int t0 = 0; t0 < M * K; t0 += 32) {
+          const int t = t0 + lane;
+          const int e = t < M * K ? s_idx[t / K][t - (t / K) * K] : 0;
+          const bool fst = t < M * K && s_first[e] == t;
+          const uint32_t bal = __ballot_sync(0xffffffffu, fst);
+          if (fst) {
+            const int u = base + __popc(bal & ((1u << lane) - 1u));
+            const uint32_t mk = s_mask[e];
+            s_uof[e] = (int16_t)u;
+            const int my_bad = s_ebad[e], my_fmt = s_efmt[e];
+            if (my_bad) {
+              set_error(err, BQE_EDEVICE, my_bad);
+              s_bad = 1;
+            }
+            s_ufmt[u] = my_fmt;
+            s_uaddr[u] = s_eaddr[e];
+            int n = 0;
+            for (int mm = 0; mm < M; ++mm)
+              if (mk & (1u << mm)) s_urows[u * kMaxM + n++] = (int8_t)mm;
+            s_unrows[u] = n;
+            if (cta == 0) {  // the call's work list, for bqe_layer_stats
+              ((int32_t*)(P.ws + P.L.u_slot))[u] = s_eslot[e];
+              ((int32_t*)(P.ws + P.L.u_fmt))[u] = my_fmt;
+              ((int32_t*)(P.ws + P.L.u_nrows))[u] = n;
+            }
+          }
+          base += __popc(bal);
+        }
+        const int tot = base - 1;
+        if (lane == 0) {
+          // the shared expert (validated like the others)
+          const int sh_bad = s_ebad[E], sh_fmt = s_efmt[E];
+          if (sh_bad) {
+            set_error(err, BQE_EDEVICE, sh_bad);
+            s_bad = 2;
+          }
+          s_ufmt[0] = sh_fmt;
+          s_uaddr[0] = s_eaddr[E];
+          s_unrows[0] = M;
+          if (cta == 0) {
+            ((int32_t*)(P.ws + P.L.u_slot))[0] = s_eslot[E];
+            ((int32_t*)(P.ws + P.L.u_fmt))[0] = sh_fmt;
+            ((int32_t*)(P.ws + P.L.u_nrows))[0] = M;
+          }
+        }
+        if (lane < M) s_urows[lane] = (int8_t)lane;
+        __syncwarp();
+        if (lane == 0) rstamp(P, 4, t_cta0);
+        // row slots: the shared expert's M rows first, then each chosen
+        // expert's rows in work-list order (exclusive prefix, two entries a lane)
+        const int u0 = 2 * lane, u1 = 2 * lane + 1;
+        const int n0 = u0 <= tot ? s_unrows[u0] : 0, n1 = u1 <= tot ? s_unrows[u1] : 0;
+        int incl = n0 + n1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int tv = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += tv;
+        }
+        const int ex = incl - n0 - n1;
+        if (u0 <= tot + 1) s_rbase[u0] = ex;
+        if (u1 <= tot + 1) s_rbase[u1] = ex + n0;
+        // on an invalid routed slot only the shared expert runs (the call
+        // reports the error; its output is undefined); an invalid shared slot
+        // or an aborted routing streams nothing
+        const int nu = (s_abort || s_bad == 2) ? 0 : s_bad ? 1 : 1 + tot;
+        if (lane == 0) {
+          s_nu = nu;
+          if (cta == 0) *(int32_t*)(P.ws + P.L.nu) = nu;
+        }
+        __syncwarp();
+        // row slot of each (row, choice), and each row slot's mixing weight
+        // (the sum over the row's choices of that expert; shared expert: 1)
+        if (lane < M) s_rsw[lane] = 1.0f;
+        if (nu > 1)
+          for (int t = lane; t < M * K; t += 32) {
+            const int m = t / K, j = t - (t / K) * K;
+            const int ee = s_idx[m][j];
+            const int rs = s_rbase[s_uof[ee]] + __popc(s_mask[ee] & ((1u << m) - 1u));
+            s_rs[m][j] = rs;
+            bool fj = true;
+            float w = 0.f;
+            for (int j2 = 0; j2 < K; ++j2)
+              if (s_idx[m][j2] == ee) {
+                fj = fj && j2 >= j;
+                w += s_cw[m][j2];
+              }
+            if (fj) s_rsw[rs] = w;
+          }
+        if (lane == 0) rstamp(P, 5, t_cta0);
+        // item templates of every (phase, work-list expert)
+        for (int t = lane; t < 2 * nu; t += 32) {
+          const int ph = t & 1, u = t >> 1;
+          if (fmt_ok(s_ufmt[u])) make_tpl(P, s_tpl[ph][u], ph, u, s_ufmt[u], s_uaddr[u], s_unrows[u], s_rbase[u]);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mstamp(P, kStRoutedMax, true);
+          rstamp(P, 6, t_cta0);
+          if (P.diag) dacc(P, 3, globaltimer_ns() - t_cta0, 1);
+          mbar_arrive(&route_bar);
+        }
+      }
+    }
+    named_bar_sync(1, NCT);
     // ---- work items: this warp takes tasks cw, cw + 16, ... of the CTA's task sequence
     const int nU = s_nu;
     const int nTot = nU * (nAper + nBper), nA = nU * nAper;
     const int nmine = cta < nTot ? (nTot - cta + G - 1) / G : 0;
-    const int nAmine = cta < nA ? (nA - cta + G - 1) / G : 0;
     int k = cw, Ki = 0;
     bool first = true, okc = !s_abort;
     auto run_items = [&](int i0, int i1) {
@@ -948,6 +987,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         }
         if (first && ct == 0) {
           mstamp(P, kStFirstItem, false);
+          rstamp(P, 7, t_cta0);
           first = false;
         }
         const uint64_t tc = (P.diag && cw == 0) ? globaltimer_ns() : 0;
@@ -980,185 +1020,32 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         Ki += T;
       }
     };
-    // grid barrier b of this call (thread ct == 0 arrives and waits; the other
-    // compute threads wait at the CTA barrier behind it)
-    auto grid_barrier = [&](int b, uint64_t* local_done) {
-      fence_proxy_async_global();  // this thread's writes are read by other CTAs' bulk copies
-      named_bar_sync(1, NCT);
-      if (ct == 0) {
-        const uint64_t tb0 = P.diag ? globaltimer_ns() : 0;
-        bool okb = true;
-        if (local_done) okb = mwait(local_done, 0, P.limit_ns, err);  // this CTA's partial sums are written
-        fence_proxy_async_global();
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        unsigned long long* ctr = (unsigned long long*)(P.ws + P.L.m_done);
-        atomicAdd(ctr, 1ull);
-        const unsigned long long target = (unsigned long long)G * (3ull * (tag - 1u) + (unsigned)b + 1ull);
-        const uint64_t t0 = globaltimer_ns();
-        while (okb && ld_acquire_u64(ctr) < target) {
-          __nanosleep(64);
-          if (*(volatile const int32_t*)err || globaltimer_ns() - t0 > P.limit_ns) okb = false;
-        }
-        if (!okb) {
-          set_error(err, BQE_ETIMEOUT, kErrWaitFull);
-          s_abort = 1;
-        }
-        if (P.diag) dacc(P, 3 + 2 * b, globaltimer_ns() - tb0, 0);  // slots 3, 5, 7: barriers 0, 1, 2
-      }
-      named_bar_sync(1, NCT);
-    };
-    // ---- phase A: W1/W3 items
-    run_items(0, nAmine);
-    if (lane == 0) mstamp(P, kStAEnd, true);
-    grid_barrier(0, &a_done);
-    const uint64_t tF = P.diag ? globaltimer_ns() : 0;
-    // ---- h = silu(g) * u of every (row slot, 256 columns of the intermediate
-    // dimension), the K-chunk partials added in chunk order, kept in fp32 for
-    // the MXFP4 W2 loops and as integer records (X_hi + X_lo / 128 of h 2^si,
-    // max |h| 2^si in [2^13, 2^14), in the order of the expert's format, with
-    // the 16-column sums and 2^-si) for the others; 256 threads per unit
-    {
-      const float* pa = (const float*)(P.ws + P.L.m_pa);
-      float* hbuf = (float*)(P.ws + P.L.m_h);
-      const int nrs = nU > 0 ? s_rbase[nU] : 0;
-      const int nblk = I / 256, nunits = nrs * nblk;
-      const int half = ct >> 8, j = ct & 255;
-      __shared__ uint32_t s_hmx[2][8];
-      // (no abort test inside: the 256 threads of a half meet at named barriers)
-      for (int unit = cta + half * G; unit < nunits; unit += 2 * G) {
-        const int rs = unit / nblk, blk = unit - (unit / nblk) * nblk;
-        int u = 0;
-        while (u + 1 < nU && s_rbase[u + 1] <= rs) ++u;
-        const int i = blk * 256 + j, p = i >> 5, l = i & 31;
-        const float* src = pa + (((int64_t)rs * g.npanA + p) * g.nchA) * 2 * 32 + l;
-        float pg[8], pu[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < g.nchA) {
-            pg[c] = __ldcg(src + c * 64);
-            pu[c] = __ldcg(src + c * 64 + 32);
-          }
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < g.nchA) {
-            a0 += pg[c];
-            a1 += pu[c];
-          }
-        const float hv = silu_m(a0) * a1;
-        const int fmt = s_ufmt[u];
-        if (act_mode(1, fmt) != kActInt) {
-          hbuf[(int64_t)rs * I + i] = hv;
-          continue;
-        }
-        const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(hv) & 0x7FFFFFFFu);
-        if (lane == 0) s_hmx[half][(ct >> 5) & 7] = mx;
-        named_bar_sync(3 + half, 256);
-        uint32_t bm = 0;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) bm = max(bm, s_hmx[half][w]);
-        named_bar_sync(3 + half, 256);  // s_hmx is reused by the next unit
-        const int ex = (int)(bm >> 23);  // biased exponent of max |h| (0: all zero or subnormal)
-        const int si = ex == 0 ? 0 : min(max(13 - (ex - 127), -100), 100);
-        const int tq = fmt == BQE_FMT_TQ1;
-        const int ck = blk / bpcB, kb = blk - ck * bpcB;
-        uint8_t* rec = P.ws + P.L.m_hr + ((size_t)rs * g.nchB + ck) * int_rec_bytes(1, g.kcB);
-        if (j == 0) rec_put_scale(rec, tq, g.kcB, kb, ldexpf(1.0f, -si));
-        const float v = ldexpf(hv, si);
-        const int Xh = __float2int_rn(v);
-        const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
-        rec_put(rec, tq, g.kcB, kb, j, Xh, Xl);
-        if (tq && j < 16) rec_put_pad(rec, g.kcB, kb, j);
-        int ph = Xh, pl = Xl;
-#pragma unroll
-        for (int o = 8; o; o >>= 1) {
-          ph += __shfl_xor_sync(0xffffffffu, ph, o);
-          pl += __shfl_xor_sync(0xffffffffu, pl, o);
-        }
-        if ((lane & 15) == 0) rec_put_sums(rec, tq, g.kcB, kb, j >> 4, ph, pl);
-      }
-    }
-    if (P.diag && ct == 0) dacc(P, 4, globaltimer_ns() - tF, 0);  // slot 4: the h phase
-    grid_barrier(1, nullptr);
-    if (ct == 0) mbar_arrive(&fb_bar);  // the producers may copy h now
-    // ---- phase B: W2 items
-    run_items(nAmine, nmine);
+    // ---- every item of this CTA: W1/W3 items, then W2 items (the W2 rows of h
+    // wait, in the producers, for the h units of their expert)
+    run_items(0, nmine);
     if (lane == 0) mstamp(P, kStConsEnd, true);
-    grid_barrier(2, &b_done);
-    const uint64_t tC = P.diag ? globaltimer_ns() : 0;
-    // ---- out = y_shared + sum_j w_j y_j (W2 chunk partials added in chunk
-    // order, experts in a fixed order), one output element per thread
-    {
-      const float* pb = (const float*)(P.ws + P.L.m_pb);
-      const int n_out = M * H, per = (n_out + G - 1) / G;
-      const int lo = min(n_out, per * cta), hi = min(n_out, lo + per);
-      const int nj = nU > 1 ? K : 0;
-      // every partial of one output element loaded together when the shared
-      // expert plus the row's experts number <= 8 and W2 has <= 3 K chunks
-      const bool batched = nj + 1 <= 8 && g.nchB <= 3;
-      for (int e = lo + ct; e < hi && !s_abort; e += NCT) {
-        const int m = e / H, n = e - m * H;
-        float val = 0.f;
-        if (batched) {
-          float ys[8][3];
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int rs = jj == 0 ? m : s_rs[m][jj > 0 ? jj - 1 : 0];
-#pragma unroll
-            for (int c = 0; c < 3; ++c)
-              if (jj <= nj && c < g.nchB) ys[jj][c] = __ldcg(pb + ((int64_t)rs * g.nchB + c) * H + n);
-          }
-#pragma unroll
-          for (int c = 0; c < 3; ++c)
-            if (c < g.nchB) val += ys[0][c];
-#pragma unroll
-          for (int jj = 1; jj < 8; ++jj) {
-            if (jj <= nj) {
-              float yj = 0.f;
-#pragma unroll
-              for (int c = 0; c < 3; ++c)
-                if (c < g.nchB) yj += ys[jj][c];
-              val = fmaf(s_cw[m][jj - 1], yj, val);
-            }
-          }
-        } else {
-          // expert by expert, in the same order
-          float ys[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            if (c < g.nchB) ys[c] = __ldcg(pb + ((int64_t)m * g.nchB + c) * H + n);
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            if (c < g.nchB) val += ys[c];
-          for (int jj = 0; jj < nj; ++jj) {
-            const int rs = s_rs[m][jj];
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              if (c < g.nchB) ys[c] = __ldcg(pb + ((int64_t)rs * g.nchB + c) * H + n);
-            float yj = 0.f;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              if (c < g.nchB) yj += ys[c];
-            val = fmaf(s_cw[m][jj], yj, val);
-          }
-        }
-        P.out[e] = P.accumulate ? P.out[e] + val : val;
-      }
-      if (P.diag && ct == 0) dacc(P, 6, globaltimer_ns() - tC, 0);  // slot 6: the combine
-    }
-  } else {
+  } else if (warp == kRedWarp) {
     // =============================== reducer ==================================
-    // Adds each item's task partials in a fixed order and writes them to the
-    // workspace, then frees the item's ring bytes; tells the compute warps
-    // when this CTA's W1/W3 and W2 partials are all written.
+    // Adds each item's task partials in a fixed order, then frees the item's
+    // ring bytes.  W1/W3 items: the g/u chunk partials go to the workspace and
+    // the expert's count of finished items is released (once per run of items
+    // of one expert).  W2 items: w * y is added to the output rows (fp32
+    // atomics: the order of these additions, and so the last bits of the
+    // output, can differ from call to call).
     const bool ok0 = __all_sync(0xffffffffu, mwait(&route_bar, 0, P.limit_ns, err));
     const int nU = ok0 ? s_nu : 0;
     const int nTot = nU * (nAper + nBper), nA = nU * nAper;
     const int nmine = cta < nTot ? (nTot - cta + G - 1) / G : 0;
-    const int nAmine = cta < nA ? (nA - cta + G - 1) / G : 0;
     float* pa = (float*)(P.ws + P.L.m_pa);
-    float* pb = (float*)(P.ws + P.L.m_pb);
-    if (nAmine == 0 && lane == 0) mbar_arrive(&a_done);
+    unsigned int* ca = (unsigned int*)(P.ws + P.L.m_ca);
+    int cur_u = -1, cur_n = 0;  // W1/W3 items of expert cur_u finished but not yet released
+    auto release_a = [&]() {
+      if (cur_n > 0 && lane == 0) {
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");  // the partials (whole warp: __syncwarp above) first
+        atomicAdd(ca + cur_u, (unsigned int)cur_n);
+      }
+      cur_n = 0;
+    };
     for (int i = 0; i < nmine; ++i) {
       const uint64_t tr = P.diag ? globaltimer_ns() : 0;
       const bool okc = __all_sync(0xffffffffu, mwait(&cons[i % kNQ], (i / kNQ) & 1, P.limit_ns, err));
@@ -1174,6 +1061,10 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       const float* red = reinterpret_cast<const float*>(ring + h.off + h.red);
       const int u = h.u, R = h.R, rb = s_rbase[u];
       if (h.phase == 0) {
+        if (u != cur_u) {
+          release_a();
+          cur_u = u;
+        }
         // chunk partials of g and u for this panel (the f16 input's scale removed: exact power of two)
         for (int r = 0; r < R; ++r) {
           const int row = u == 0 ? r : s_urows[u * kMaxM + r];
@@ -1187,27 +1078,143 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           pa[base + lane] = a0 * unscale;
           pa[base + 32 + lane] = a1 * unscale;
         }
+        ++cur_n;
+        __syncwarp();
+        if (cta + (i + 1) * G >= nA) release_a();  // this CTA's last W1/W3 item
       } else {
         for (int pi = 0; pi < P.PB; ++pi) {
           const int n = (h.p * P.PB + pi) * 32 + lane;
           for (int r = 0; r < R; ++r) {
             float y = 0.f;
             for (int gi = 0; gi < g.GB; ++gi) y += red[((pi * g.GB + gi) * R + r) * 32 + lane];
-            pb[((int64_t)(rb + r) * g.nchB + h.c) * H + n] = y;
+            const int row = u == 0 ? r : s_urows[u * kMaxM + r];
+            atomicAdd(P.out + (int64_t)row * H + n, s_rsw[rb + r] * y);
           }
         }
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&freed[i % kNQ]);  // the item's ring bytes may be reused
-        if (i + 1 == nAmine) mbar_arrive(&a_done);
-      }
+      if (lane == 0) mbar_arrive(&freed[i % kNQ]);  // the item's ring bytes may be reused
     }
-    if (lane == 0) mbar_arrive(&b_done);
+    __syncwarp();
+    release_a();
+  } else {
+    // ================================ h warp ==================================
+    // h = silu(g) * u of this CTA's units (row slot, 256 columns of the
+    // intermediate dimension), units dealt round-robin over the CTAs in
+    // work-list order: wait (bounded) until every W1/W3 item of the unit's
+    // expert is done, add the K-chunk partials in chunk order, and write h in
+    // fp32 (MXFP4 W2 loops) or as integer records (X_hi + X_lo / 128 of
+    // h 2^si, max |h| 2^si in [2^13, 2^14), in the expert's format order, with
+    // the 16-column sums and 2^-si); then release the expert's count of units.
+    const bool ok0 = __all_sync(0xffffffffu, mwait(&route_bar, 0, P.limit_ns, err));
+    const int nU = ok0 ? s_nu : 0;
+    const int nrs = nU > 0 ? s_rbase[nU] : 0;
+    const int nblk = I / 256, nunits = nrs * nblk;
+    const float* pa = (const float*)(P.ws + P.L.m_pa);
+    float* hbuf = (float*)(P.ws + P.L.m_h);
+    const unsigned int* ca = (const unsigned int*)(P.ws + P.L.m_ca);
+    unsigned int* chc = (unsigned int*)(P.ws + P.L.m_ch);
+    int u = 0, ready = -1, cur_n = 0;
+    bool okh = true;
+    auto release_h = [&]() {
+      if (cur_n > 0 && lane == 0) {
+        fence_proxy_async_global();  // h is read by other CTAs' bulk copies
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        atomicAdd(chc + u, (unsigned int)cur_n);
+      }
+      cur_n = 0;
+    };
+    for (int unit = cta; unit < nunits && okh; unit += G) {
+      const int rs = unit / nblk, blk = unit - (unit / nblk) * nblk;
+      int un = u;
+      while (un + 1 < nU && s_rbase[un + 1] <= rs) ++un;
+      if (un != u) {
+        release_h();
+        u = un;
+      }
+      if (u > ready) {
+        bool okw = true;
+        if (lane == 0) okw = wait_ge(ca + u, (uint32_t)nAper, P.limit_ns, err);
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) {
+          if (lane == 0) {
+            set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+            s_abort = 1;
+          }
+          okh = false;
+          break;
+        }
+        ready = u;
+      }
+      // lane: 8 consecutive columns i0 .. i0 + 7 of one 32-column panel, four at
+      // a time; the K-chunk partials of g and u added in chunk order, four
+      // chunks loaded together
+      const int i0 = blk * 256 + lane * 8, p = i0 >> 5, l0 = i0 & 31;
+      const float* src = pa + (((int64_t)rs * g.npanA + p) * g.nchA) * 2 * 32 + l0;
+      float hv[8];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+        for (int c0 = 0; c0 < g.nchA; c0 += 4) {
+          float4 gv[4], uv[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (c0 + c < g.nchA) {
+              gv[c] = __ldcg(reinterpret_cast<const float4*>(src + (c0 + c) * 64 + 4 * q));
+              uv[c] = __ldcg(reinterpret_cast<const float4*>(src + (c0 + c) * 64 + 32 + 4 * q));
+            }
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (c0 + c < g.nchA) {
+              a.x += gv[c].x; a.y += gv[c].y; a.z += gv[c].z; a.w += gv[c].w;
+              b.x += uv[c].x; b.y += uv[c].y; b.z += uv[c].z; b.w += uv[c].w;
+            }
+        }
+        hv[4 * q] = silu_m(a.x) * b.x;
+        hv[4 * q + 1] = silu_m(a.y) * b.y;
+        hv[4 * q + 2] = silu_m(a.z) * b.z;
+        hv[4 * q + 3] = silu_m(a.w) * b.w;
+      }
+      const int fmt = s_ufmt[u];
+      if (act_mode(1, fmt) != kActInt) {
+        float4* dst = reinterpret_cast<float4*>(hbuf + (int64_t)rs * I + i0);
+        dst[0] = make_float4(hv[0], hv[1], hv[2], hv[3]);
+        dst[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
+      } else {
+        uint32_t mx = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx = max(mx, __float_as_uint(hv[k]) & 0x7FFFFFFFu);
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        const int ex = (int)(mx >> 23);  // biased exponent of max |h| (0: all zero or subnormal)
+        const int si = ex == 0 ? 0 : min(max(13 - (ex - 127), -100), 100);
+        const int tq = fmt == BQE_FMT_TQ1;
+        const int ck = blk / bpcB, kb = blk - ck * bpcB;
+        uint8_t* rec = P.ws + P.L.m_hr + ((size_t)rs * g.nchB + ck) * int_rec_bytes(1, g.kcB);
+        if (lane == 0) rec_put_scale(rec, tq, g.kcB, kb, ldexpf(1.0f, -si));
+        if (tq && lane < 16) rec_put_pad(rec, g.kcB, kb, lane);
+        int ph = 0, pl = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float v = ldexpf(hv[k], si);
+          const int Xh = __float2int_rn(v);
+          const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
+          rec_put(rec, tq, g.kcB, kb, lane * 8 + k, Xh, Xl);
+          ph += Xh;
+          pl += Xl;
+        }
+        ph += __shfl_xor_sync(0xffffffffu, ph, 1);
+        pl += __shfl_xor_sync(0xffffffffu, pl, 1);
+        if ((lane & 1) == 0) rec_put_sums(rec, tq, g.kcB, kb, lane >> 1, ph, pl);
+      }
+      ++cur_n;
+      __syncwarp();
+    }
+    __syncwarp();
+    release_h();
   }
 
-  // ---- end: after the last grid barrier every CTA has read this call's tag,
-  // so CTA 0 advances the epoch for the next call
+  // ---- end: CTA 0 is past the logits sync, so every CTA has read this
+  // call's tag: CTA 0 advances the epoch for the next call
   __syncthreads();
   if (tid == 0) {
     mstamp(P, kStEnd, true);
@@ -1267,7 +1274,6 @@ int launch_moe(const MoeParams& P0, int grid, cudaStream_t st) {
   if (P.ring_bytes < moe_max_item(g, P.PB) || P.ring_bytes < xst + rtb + 1024) return BQE_EUNSUPPORTED;
   P.xstage_off = P.ring_bytes - xst;
   P.rt_off = P.xstage_off - rtb;
-  if ((uint64_t)g.M * g.E * 4 > rtb) return BQE_EUNSUPPORTED;  // the selection keys reuse the router rows' room
   // item index t -> (expert, panel, chunk) by multiply-high: exact while t * d < 2^32
   auto mag = [](uint64_t d) { return (0x100000000ull + d - 1) / d; };
   const uint32_t nAper = (uint32_t)g.npanA * g.nchA, nBper = (uint32_t)(g.npanB / P.PB) * g.nchB;

@@ -197,7 +197,10 @@ int bqe_workspace_init(void* ws, uint64_t ws_bytes, void* stream);
  *   topk_w     device, M x top_k fp32 or NULL: their mixing weights
  *   ws         device workspace of ws_bytes >= bqe_workspace_bytes(d, M)
  * Experts chosen by several rows are streamed once and applied to every row
- * that chose them. */
+ * that chose them.  Each output element is the sum of the experts' K-chunk
+ * contributions added with fp32 atomics: the order of those additions, and so
+ * the last bits of out, may differ from call to call (the selection and the
+ * mixing weights do not). */
 int bqe_moe_layer_forward(const bqe_layer_desc* d, int32_t M, const uint16_t* x,
                           const float* router_w, const float* sel_bias, const bqe_pool* pool,
                           const int32_t* slot_table, const int32_t* forced_idx, float* out,
@@ -339,18 +342,18 @@ void bqe_set_test_drop_item(int32_t item);
  * zeroed by bqe_workspace_init.  Row 1023 of blocks 0 and 1 holds globaltimer
  * stamps kept as minima or maxima over CTAs (the caller presets minima to a
  * large value): block 0 [0] first CTA start, [1] last logits published,
- * [2] first routing known, [3] first work item landed, [4] last W1/W3 item
- * done, [6] last CTA end, [7] last producer done; block 1 [1] last compute
- * warp done, [2] last routing known, [3] longest producer wait for h (ns).
- * Rows 0..CTAs-1 (ns unless noted): block 0 [0] input staged, [1] staged
- * slices fenced, [2] all logits seen, [3] / [5] / [7] waits at the three grid
- * barriers, [4] the h phase, [6] the combine; block 1 [0] producer loop
- * (cycles), [1] items issued, [2] logits published, [3] routing known, [4]
- * router rows landed, [5] / [6] / [7] producer cycles issuing bulk copies /
- * waiting for ring space / waiting for h; block 2 [1] producer wait for h,
- * [2] / [3] compute warp 0 waiting / computing, [4] reducer waiting, [7] CTA
- * start to end.  Block 0 rows 300 + CTA: routing step ends ([0] logits read,
- * [1] top-k, [2] work list, [3] row slots). */
+ * [2] first selection done, [3] first work item landed, [6] last CTA end,
+ * [7] last producer done; block 1 [1] last compute warp done, [2] last
+ * routing known, [3] longest producer wait for h (ns).  Rows 0..CTAs-1 (ns
+ * unless noted): block 0 [0] input staged, [1] selection inputs stored,
+ * [2] all logits seen; block 1 [0] producer loop (cycles), [1] items issued,
+ * [2] logits published, [3] routing known, [4] router rows landed, [5] / [6] /
+ * [7] producer cycles issuing bulk copies / waiting for ring space / waiting
+ * for h; block 2 [1] producer wait for h, [2] / [3] compute warp 0 waiting /
+ * computing, [4] reducer waiting, [7] CTA start to end.  Block 0 rows
+ * 300 + CTA, ns from the CTA's start: [0] logits seen, [1] keys loaded,
+ * [2] top-k, [3] mixing weights, [4] work list, [5] row slots, [6] item
+ * templates, [7] first item landed. */
 void bqe_set_diag(int32_t on);
 
 /* Operand type of the prefill tensor-core GEMMs: 1 (default) fp16 with the

@@ -250,6 +250,6 @@ def test_noalloc_argument_checks_before_any_device_work(A):
     assert call(d, 1, fake, pool, None) == A.BQE_EINVAL       # no output
     assert call(d, 1, fake, bad_pool, fake) == A.BQE_EINVAL   # empty pool
     assert call(A.desc(1000, 768, 24, 3), 1, fake, pool, fake) == A.BQE_EINVAL  # hidden not a multiple of 512
-    big = A.desc(5120, 2304, 384, 6)
-    assert A.bqe_workspace_bytes(big, 7) > 8 << 20
-    assert call(big, 7, fake, pool, fake) == A.BQE_ENOSPC     # workspace beyond the fixed array
+    big = A.desc(7168, 2304, 384, 6)
+    assert A.bqe_workspace_bytes(big, 8) > 8 << 20
+    assert call(big, 8, fake, pool, fake) == A.BQE_ENOSPC     # workspace beyond the fixed array

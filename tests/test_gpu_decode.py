@@ -178,9 +178,12 @@ def test_forced_idx_with_repeats_and_accumulate(dev):
 
 
 @pytest.mark.parametrize("M", [1, 2, 6, 8])
-def test_repeated_calls_identical(dev, M):
+def test_repeated_calls_consistent(dev, M):
     """Consecutive calls on one workspace (the call epoch and the arrival
-    counters advance from call to call) give identical bits and routing."""
+    counters advance from call to call) choose the same experts with the
+    same weights, and every call meets the decode bar against the oracle
+    (the output rows are sums of fp32 atomic additions, whose order may
+    differ from call to call)."""
     fm = [ALL[(3 * e + 2) % 4] for e in range(24)] + [synth.MXFP4]
     L = synth.small_layer(60 + M, fm, 1024, 768, 24, 3, M, bias_std=0.25)
     DL = DeviceLayer(L, dev)
@@ -190,8 +193,10 @@ def test_repeated_calls_identical(dev, M):
     ref2 = O.moe_layer(L["x"], L["router"], L["bias"], L["experts"], L["fmts"], 1024, 768, 3, 24, forced_idx=idx)
     check_out(out, ref2["out"], what="M=%d" % M)
     for _ in range(5):
-        out2, idx2, _ = DL.forward(L["x"])
-        assert np.array_equal(out, out2) and np.array_equal(idx, idx2)
+        out2, idx2, w2 = DL.forward(L["x"])
+        assert np.array_equal(idx, idx2) and np.array_equal(w, w2)
+        check_out(out2, ref2["out"], what="M=%d repeat" % M)
+        assert np.allclose(out2, out, rtol=1e-5, atol=1e-5 * float(np.abs(out).max()))
 
 
 def test_layer_stats(dev):
@@ -280,4 +285,4 @@ def test_wait_timeout_is_reported_and_recoverable(dev):
     assert rc == A.BQE_ETIMEOUT and det in (4, 5), (A.status_name(rc), det)
     A.bqe_workspace_init(ws, nb)
     again, _, _ = DL.forward(L["x"])
-    assert np.array_equal(good, again)
+    check_out(again, good, what="after the timeout")

@@ -47,10 +47,12 @@ def test_noalloc_matches_workspace_call(dev, M):
 
 def test_noalloc_rejects_layers_beyond_its_array(dev):
     from bit_quantised_expert_gb300 import _abi as A
-    d = A.desc(5120, 2304, 384, 6)
-    assert A.bqe_workspace_bytes(d, 6) <= 8 << 20 < A.bqe_workspace_bytes(d, 7)
+    # every row count of the DeepSeek-V4.1-Flash layer fits; a wider layer at 8 rows does not
+    assert A.bqe_workspace_bytes(A.desc(5120, 2304, 384, 6), 8) <= 8 << 20
+    d = A.desc(7168, 2304, 384, 6)
+    assert A.bqe_workspace_bytes(d, 8) > 8 << 20
     with pytest.raises(A.BqeError) as e:
-        A.bqe_moe_layer_forward_noalloc(d, 7, 16, 16, None, A.bqe_pool(16, 1, 16, 16, 1, 0), 16, None, 16, 0, None,
+        A.bqe_moe_layer_forward_noalloc(d, 8, 16, 16, None, A.bqe_pool(16, 1, 16, 16, 1, 0), 16, None, 16, 0, None,
                                         None, None)
     assert e.value.status == A.BQE_ENOSPC
 
