@@ -91,6 +91,10 @@ __device__ __forceinline__ void st_release_u64(void* p, unsigned long long v) {
 }
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ float silu_m(float t) { return t / (1.0f + expf(-t)); }
+// fp32 add into global memory with no value returned
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
 
 // Diagnostic timeline of one call: globaltimer stamps kept as minima or
 // maxima over CTAs in row 1023 of dbg blocks 0..2 (8 slots each).
@@ -1038,13 +1042,19 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     const int nmine = cta < nTot ? (nTot - cta + G - 1) / G : 0;
     float* pa = (float*)(P.ws + P.L.m_pa);
     unsigned int* ca = (unsigned int*)(P.ws + P.L.m_ca);
-    int cur_u = -1, cur_n = 0;  // W1/W3 items of expert cur_u finished but not yet released
+    // W1/W3 items reduced but not yet released: expert cur_u (cur_n items)
+    // and the one before it (prev_u, prev_n).  The release fence waits for the
+    // partials written so far, so it is taken every second change of expert
+    // (and after the last W1/W3 item): one fence publishes two experts.
+    int cur_u = -1, cur_n = 0, prev_u = -1, prev_n = 0;
     auto release_a = [&]() {
-      if (cur_n > 0 && lane == 0) {
+      if ((cur_n > 0 || prev_n > 0) && lane == 0) {
         asm volatile("fence.acq_rel.gpu;" ::: "memory");  // the partials (whole warp: __syncwarp above) first
-        atomicAdd(ca + cur_u, (unsigned int)cur_n);
+        if (prev_n > 0) atomicAdd(ca + prev_u, (unsigned int)prev_n);
+        if (cur_n > 0) atomicAdd(ca + cur_u, (unsigned int)cur_n);
       }
       cur_n = 0;
+      prev_n = 0;
     };
     for (int i = 0; i < nmine; ++i) {
       const uint64_t tr = P.diag ? globaltimer_ns() : 0;
@@ -1062,8 +1072,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       const int u = h.u, R = h.R, rb = s_rbase[u];
       if (h.phase == 0) {
         if (u != cur_u) {
-          release_a();
+          if (prev_n > 0) release_a();  // two experts pending: publish both
+          prev_u = cur_u;
+          prev_n = cur_n;
           cur_u = u;
+          cur_n = 0;
         }
         // chunk partials of g and u for this panel (the f16 input's scale removed: exact power of two)
         for (int r = 0; r < R; ++r) {
@@ -1088,7 +1101,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
             float y = 0.f;
             for (int gi = 0; gi < g.GB; ++gi) y += red[((pi * g.GB + gi) * R + r) * 32 + lane];
             const int row = u == 0 ? r : s_urows[u * kMaxM + r];
-            atomicAdd(P.out + (int64_t)row * H + n, s_rsw[rb + r] * y);
+            red_add_f32(P.out + (int64_t)row * H + n, s_rsw[rb + r] * y);
           }
         }
       }

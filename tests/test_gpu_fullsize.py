@@ -98,10 +98,21 @@ def test_step40_teacher_forced(dev):
         snaps.append(resid.double().cpu().numpy())
     rc, det = A.bqe_check(ws)
     assert rc == A.BQE_OK, (A.status_name(rc), det)
+    # the whole step as one call: its first layer sees the same input; after
+    # 40 chained layers the residual agrees only loosely (the layers add their
+    # outputs with fp32 atomics, and bf16 rounding of each layer's input
+    # amplifies the different last bits), while a skipped or repeated layer
+    # (each moves the residual by ~20 % of its norm) would be far off
     whole = S.x0[0].clone()
-    A.bqe_moe_step(S.d, L, M, whole, S.wr, None, pool, S.tables, forced, None, ws, nb)
+    t_whole = torch.zeros(L, M, H, dtype=torch.int16, device=dev)
+    A.bqe_moe_step(S.d, L, M, whole, S.wr, None, pool, S.tables, forced, t_whole, ws, nb)
     assert A.bqe_check(ws)[0] == A.BQE_OK
-    assert np.array_equal(whole.double().cpu().numpy(), snaps[-1])
+    assert torch.equal(t_whole[0], t_all[0])
+    wn = whole.double().cpu().numpy()
+    rel = np.linalg.norm(wn - snaps[-1]) / np.linalg.norm(snaps[-1])
+    assert rel < 0.1, rel
+    step = np.linalg.norm(snaps[-1] - snaps[-2]) / np.linalg.norm(snaps[-1])
+    assert step > 3 * rel, (step, rel)
     t_np = t_all.cpu().numpy().view(np.uint16)
     # layer inputs: bf16(rmsnorm(r_l)), within one bf16 step of the fp64 statement
     for l in range(L):
