@@ -1,6 +1,9 @@
-// bqe_gemv.cuh — the per-format dequant-GEMV group kernels of the decode
-// layer: one lane = one weight row, one 256-column group of a tile in shared
-// memory, R <= 4 activation rows at a time, fp32 accumulation.
+// bqe_gemv.cuh — the per-format dequant-GEMV inner loops of the decode
+// layer: one warp, one 32-row panel of a weight tile in shared memory, one
+// 256-column group, all activation rows of the item at once on the tensor
+// cores (mma.sync m16n8k16: the weights are decoded in registers straight
+// into the A fragments, so the skinny product needs no shared-memory operand
+// staging), fp32 accumulation.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -10,13 +13,6 @@
 #include "bqe_internal.cuh"
 
 namespace bqe {
-
-// ---------------------------------------------------------------------------
-// per-format group kernels: one lane = one weight row, 256 columns, R rows of
-// activations; acc[r] accumulates the row's dot products (two halves kept in
-// a float2 for the packed FMA, added at the end).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
 __device__ __forceinline__ float ue8m0_f32(uint32_t e) {
   return e == 0 ? __int_as_float(0x00400000) : __int_as_float((int)(e << 23));
@@ -38,385 +34,404 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& h0, uint32
       : "r"(w));
 }
 
-// a0 += lo(w) * lo(x), a1 += hi(w) * hi(x): f16 inputs, exact f32 products,
-// f32 accumulation (mixed-precision FMA of sm_100+).
-__device__ __forceinline__ void fma_f16x2_f32(uint32_t w, uint32_t x, float& a0, float& a1) {
-  asm("{ .reg .f16 wl, wh, xl, xh; mov.b32 {wl, wh}, %2; mov.b32 {xl, xh}, %3;\n"
-      "  fma.rn.f32.f16 %0, wl, xl, %0; fma.rn.f32.f16 %1, wh, xh, %1; }"
-      : "+f"(a0), "+f"(a1)
-      : "r"(w), "r"(x));
+__device__ __forceinline__ float silu_f(float t) { return t / (1.0f + expf(-t)); }
+
+// Activation rows of an item: f16 x 2^s in the format's column order (W1/W3)
+// or the f16 hi/lo records of h (W2).
+enum { kActF16 = 1, kActH16 = 3 };
+__host__ __device__ inline int act_mode(int phase) { return phase == 0 ? kActF16 : kActH16; }
+
+// Bytes of one staged activation row (one bulk copy) ...
+__host__ __device__ inline int act_row_bytes(int amode, int fmt, int kc) {
+  return amode == kActF16 ? f16_len(fmt, kc) * 2 : (int)h16_rec_bytes(fmt, kc);
+}
+// ... and the distance between two staged rows in shared memory: x rows sit
+// 64 bytes past a multiple of 128, so that the 16-byte B loads of two rows
+// (one quarter-warp) fall in different banks.
+__host__ __device__ inline int act_row_stride(int amode, int fmt, int kc) {
+  const int b = act_row_bytes(amode, fmt, kc);
+  return amode == kActF16 ? ((b + 127) & ~127) + 64 : (b + 15) & ~15;
 }
 
-template <int R>
-__device__ __forceinline__ void group_mxfp4(const uint8_t* tile, int nb, int grp, const float* act, int kc, int lane,
-                                            float2 (&acc)[R]) {
+// ----------------------------------------------------------------------------
+// Group loops: one warp, one 32-row panel (two m16 tiles), one 256-column
+// group, all rows of the item in one pass.  The weights are
+// decoded straight into the A fragments of mma.sync m16n8k16 (f16 inputs,
+// fp32 accumulation; every decoded value is an exact f16); the activation
+// rows are the B columns: row n of x in column n (W1/W3), or h of row r as two
+// columns, 2r (hi) and 2r + 1 (lo) (W2, h = hi + lo to about 2^-22 of the
+// group's largest value), four rows per MMA.  Thread (gq = lane / 4, tq =
+// lane % 4) holds rows gq, gq + 8 of each m16 tile.  The K order inside a k16
+// step is free as long as A and B follow the same one: each format takes the
+// order in which its codes decode cheapest (the staged rows follow it), and
+// its block scale multiplies the fp32 accumulators once per block.
+// ----------------------------------------------------------------------------
+// d += a b on the tensor cores (m16n8k16, row.col, f16 x f16 -> f32)
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// (a & b) | c
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t hadd2u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+constexpr uint32_t kF16x2One024 = 0x64006400u;  // (1024, 1024): a code c in its mantissa reads 1024 + c
+
+// MXFP4: thread tq takes byte-word tq of a row's 16-byte block (columns 8 tq
+// .. 8 tq + 7), natural column order: k16 step s of block b meets x columns
+// 32 b + 8 tq + 4 s .. + 3, one 16-byte load of B per block.
+template <int NJ>
+__device__ __forceinline__ void mma_mxfp4(const uint8_t* tile, int nb, int grp, const uint8_t* const (&bv)[NJ],
+                                          int lane, float (&acc)[NJ][2][4]) {
+  const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll 2
   for (int bi = 0; bi < 8; ++bi) {
     const int b = grp * 8 + bi;
-    const uint4 c4 = *reinterpret_cast<const uint4*>(tile + b * 512 + lane * 16);
-    const float sc = ue8m0_f32(tile[nb * 512 + b * 32 + lane]);
-    float2 bs[R][2];  // two independent chains per row
+    uint4 bx[NJ];
 #pragma unroll
-    for (int r = 0; r < R; ++r) bs[r][0] = bs[r][1] = f2(0.f, 0.f);
-    const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
+    for (int j = 0; j < NJ; ++j) bx[j] = *reinterpret_cast<const uint4*>(bv[j] + (b * 32 + 8 * tq) * 2);
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t h0, h1, h2, h3;
-      e2m1x8_to_f16x2(wd[w], h0, h1, h2, h3);
-      const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
-      const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
-      const float2 v2 = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-      const float2 v3 = __half22float2(*reinterpret_cast<const __half2*>(&h3));
-      const int k = grp * 256 + bi * 32 + w * 8;
+    for (int mt = 0; mt < 2; ++mt) {
+      const int r0 = 16 * mt + gq;
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(tile + b * 512 + r0 * 16 + 4 * tq);
+      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(tile + b * 512 + (r0 + 8) * 16 + 4 * tq);
+      const float s0 = ue8m0_f32(tile[nb * 512 + b * 32 + r0]), s1 = ue8m0_f32(tile[nb * 512 + b * 32 + r0 + 8]);
+      uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
+      e2m1x8_to_f16x2(w0, p0, p1, p2, p3);
+      e2m1x8_to_f16x2(w1, q0, q1, q2, q3);
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float4 xa = *reinterpret_cast<const float4*>(act + r * kc + k);
-        const float4 xb = *reinterpret_cast<const float4*>(act + r * kc + k + 4);
-        bs[r][0] = __ffma2_rn(v0, f2(xa.x, xa.y), bs[r][0]);
-        bs[r][1] = __ffma2_rn(v1, f2(xa.z, xa.w), bs[r][1]);
-        bs[r][0] = __ffma2_rn(v2, f2(xb.x, xb.y), bs[r][0]);
-        bs[r][1] = __ffma2_rn(v3, f2(xb.z, xb.w), bs[r][1]);
+      for (int j = 0; j < NJ; ++j) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16(d, p0, q0, p1, q1, bx[j].x, bx[j].y);
+        mma_f16(d, p2, q2, p3, q3, bx[j].z, bx[j].w);
+        acc[j][mt][0] = fmaf(d[0], s0, acc[j][mt][0]);
+        acc[j][mt][1] = fmaf(d[1], s0, acc[j][mt][1]);
+        acc[j][mt][2] = fmaf(d[2], s1, acc[j][mt][2]);
+        acc[j][mt][3] = fmaf(d[3], s1, acc[j][mt][3]);
       }
     }
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-      acc[r] = __ffma2_rn(f2(bs[r][0].x + bs[r][1].x, bs[r][0].y + bs[r][1].y), f2(sc, sc), acc[r]);
   }
 }
 
-// MXFP4 group with f16 activations (act_h: R rows x kc halves, scaled by a
-// power of two per row; the epilogue removes the scale).  Four accumulator
-// chains per row.
-template <int R>
-__device__ __forceinline__ void group_mxfp4_h(const uint8_t* tile, int nb, int grp, const uint16_t* act_h, int kc,
-                                              int lane, float2 (&acc)[R]) {
-#pragma unroll 1
-  for (int bi = 0; bi < 8; ++bi) {
-    const int b = grp * 8 + bi;
-    const uint4 c4 = *reinterpret_cast<const uint4*>(tile + b * 512 + lane * 16);
-    const float sc = ue8m0_f32(tile[nb * 512 + b * 32 + lane]);
-    float a[R][4];
-#pragma unroll
-    for (int r = 0; r < R; ++r) a[r][0] = a[r][1] = a[r][2] = a[r][3] = 0.f;
-    const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t h0, h1, h2, h3;
-      e2m1x8_to_f16x2(wd[w], h0, h1, h2, h3);
-      const int k = grp * 256 + bi * 32 + w * 8;
-      const int ch = (w & 1) * 2;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(act_h + r * kc + k);
-        fma_f16x2_f32(h0, xv.x, a[r][ch], a[r][ch + 1]);
-        fma_f16x2_f32(h1, xv.y, a[r][ch], a[r][ch + 1]);
-        fma_f16x2_f32(h2, xv.z, a[r][ch], a[r][ch + 1]);
-        fma_f16x2_f32(h3, xv.w, a[r][ch], a[r][ch + 1]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r].x = fmaf((a[r][0] + a[r][1]) + (a[r][2] + a[r][3]), sc, acc[r].x);
-  }
+// Q2_0: the codes of columns p and 8 + p of a 16-column word (bits 2p and
+// 16 + 2p) as f16 (2q - 3).  With the pair at bits 2P, 16 + 2P (P = 1..4;
+// pairs 0 and 5..7 are shifted there first) lop3 places it in the mantissa
+// of 1024 (1024 + 4^P q, exact), and one fma scales by 2 4^-P and subtracts
+// 2^(11 - 2P) + 3: exact, the constants being f16 numbers.
+template <int P>
+__device__ __forceinline__ uint32_t q2_pair(uint32_t w) {
+  constexpr uint32_t kMul[5] = {0u, 0x38003800u, 0x30003000u, 0x28002800u, 0x20002000u};  // 2 4^-P
+  constexpr uint32_t kAdd[5] = {0u, 0xE006E006u, 0xD818D818u, 0xD060D060u, 0xC980C980u};  // -(2^(11-2P) + 3)
+  return hfma2u(and_or(w, 0x00030003u << (2 * P), kF16x2One024), kMul[P], kAdd[P]);
+}
+// the eight pairs of one word, pair p in a[p]
+__device__ __forceinline__ void q2_pairs(uint32_t w, uint32_t (&a)[8]) {
+  const uint32_t wl = w << 2, wr = w >> 8;
+  a[0] = q2_pair<1>(wl);
+  a[1] = q2_pair<1>(w);
+  a[2] = q2_pair<2>(w);
+  a[3] = q2_pair<3>(w);
+  a[4] = q2_pair<4>(w);
+  a[5] = q2_pair<1>(wr);
+  a[6] = q2_pair<2>(wr);
+  a[7] = q2_pair<3>(wr);
 }
 
-// ----------------------------------------------------------------------------
-// Integer paths for the fp16-scaled formats (Q2_0, Q3_K, TQ1).  The layer
-// input x of a row is staged as X_hi + X_lo / 128 with X_hi = rint(x 2^si)
-// (int16, |X_hi| <= 2^14) and X_lo the int8 rounding of the remainder (so x
-// is held to about 2^-21 of the row's largest value), each in a per-format
-// order, plus the sums of X_hi and of X_lo over every 16 columns.  Each
-// weight's integer code sits in a byte lane: dp2a adds two int16 x int8
-// products and dp4a four int8 x int8 products per instruction, in exact int32
-// arithmetic.  The block's offset (2q - 3, q - 4, t - 1) is applied once per
-// block through the column sums, the block scale (and Q3_K sub-scale) once per
-// block in fp32.
-//
-// Order of X ("Q order", every 16 columns): X_hi word 2k = (x_k, x_{k+4}),
-// word 2k + 1 = (x_{k+8}, x_{k+12}); X_lo word k = (x_k, x_{k+4}, x_{k+8},
-// x_{k+12}), k = 0..3, so that the byte lanes of (codes >> 2k) & 0x03030303
-// meet their x.  Order for TQ1 ("T order", every 256 columns = 13 runs of 20
-// and padding): in run m, X_hi word 2r = (x_{20m+r}, x_{20m+5+r}), word 2r + 1
-// = (x_{20m+10+r}, x_{20m+15+r}); X_lo word r = (x_{20m+r}, x_{20m+5+r},
-// x_{20m+10+r}, x_{20m+15+r}), r = 0..4 (slots past column 255 are zero).
-// ----------------------------------------------------------------------------
-constexpr int kTOrderBlock = 528;   // bytes of one 256-column block of X_hi in T order
-constexpr int kTOrderBlockL = 272;  // ... of X_lo
-
-__host__ __device__ inline int act_x_bytes(int fmt, int kc) { return (int)int_rec_hi_bytes(fmt == BQE_FMT_TQ1, kc); }
-__host__ __device__ inline int act_xl_bytes(int fmt, int kc) { return (int)int_rec_lo_bytes(fmt == BQE_FMT_TQ1, kc); }
-
-// Pointers into one staged row of the integer mode: [X_hi | X_lo | sums of
-// X_hi | sums of X_lo | 2^-si of each 256 columns (4 slots)].
-struct IntRow {
-  const uint8_t* xh;  // X_hi of the 256-column group
-  const uint8_t* xl;  // X_lo of the group
-  const int* sh;      // 16 sums of X_hi
-  const int* sl;      // 16 sums of X_lo
-  float sc;           // 2^-si of the group: the sums below are in units of it
-};
-__device__ __forceinline__ IntRow int_row(const uint8_t* act, int r, int rowb, int fmt, int kc, int grp) {
-  const int xb = act_x_bytes(fmt, kc), xbl = act_xl_bytes(fmt, kc);
-  const uint8_t* base = act + r * rowb;
-  IntRow t;
-  t.xh = base + grp * (fmt == BQE_FMT_TQ1 ? kTOrderBlock : 512);
-  t.xl = base + xb + grp * (fmt == BQE_FMT_TQ1 ? kTOrderBlockL : 256);
-  t.sh = reinterpret_cast<const int*>(base + xb + xbl) + grp * 16;
-  t.sl = reinterpret_cast<const int*>(base + xb + xbl + kc / 4) + grp * 16;
-  t.sc = reinterpret_cast<const float*>(base + xb + xbl + kc / 2)[grp];
-  return t;
-}
-// a + b / 128 in fp32 (both exact integers below 2^24 in magnitude)
-__device__ __forceinline__ float hi_lo(int a, int b) { return fmaf((float)b, 0.0078125f, (float)a); }
-
-template <int R>
-__device__ __forceinline__ void group_q2_0_i(const uint8_t* tile, int nb, int grp, const uint8_t* act, int rowb,
-                                             int kc, int lane, float2 (&acc)[R]) {
-  IntRow row[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) row[r] = int_row(act, r, rowb, BQE_FMT_Q2_0, kc, grp);
+// Q2_0 (64-column blocks): thread tq takes word tq of a row's 16 code bytes
+// (columns 16 tq .. + 15 of the block); step s of the block = pairs 2s, 2s + 1,
+// the B rows in P order (positions 16 tq + 4 s .. + 3).
+template <int NJ>
+__device__ __forceinline__ void mma_q2_0(const uint8_t* tile, int nb, int grp, const uint8_t* const (&bv)[NJ],
+                                         int lane, float (&acc)[NJ][2][4]) {
+  const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll 1
   for (int bi = 0; bi < 4; ++bi) {
     const int b = grp * 4 + bi;
-    const uint4 c4 = *reinterpret_cast<const uint4*>(tile + b * 512 + lane * 16);
-    const float d = __half2float(*reinterpret_cast<const __half*>(tile + nb * 512 + (b * 32 + lane) * 2));
-    const uint32_t wd[4] = {c4.x, c4.y, c4.z, c4.w};
-    int ih[R], il[R];
+    uint4 bx[NJ][2];
 #pragma unroll
-    for (int r = 0; r < R; ++r) ih[r] = il[r] = 0;
+    for (int j = 0; j < NJ; ++j) {
+      bx[j][0] = *reinterpret_cast<const uint4*>(bv[j] + (b * 64 + 16 * tq) * 2);
+      bx[j][1] = *reinterpret_cast<const uint4*>(bv[j] + (b * 64 + 16 * tq + 8) * 2);
+    }
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {  // 16 weights: 16-column group 4 bi + w of this 256-column group
-      int B[4];
+    for (int mt = 0; mt < 2; ++mt) {
+      const int r0 = 16 * mt + gq;
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(tile + b * 512 + r0 * 16 + 4 * tq);
+      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(tile + b * 512 + (r0 + 8) * 16 + 4 * tq);
+      const float d0 = __half2float(*reinterpret_cast<const __half*>(tile + nb * 512 + (b * 32 + r0) * 2));
+      const float d1 = __half2float(*reinterpret_cast<const __half*>(tile + nb * 512 + (b * 32 + r0 + 8) * 2));
+      uint32_t a[8], c[8];
+      q2_pairs(w0, a);
+      q2_pairs(w1, c);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) B[k] = (int)((wd[w] >> (2 * k)) & 0x03030303u);
+      for (int j = 0; j < NJ; ++j) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16(d, a[0], c[0], a[1], c[1], bx[j][0].x, bx[j][0].y);
+        mma_f16(d, a[2], c[2], a[3], c[3], bx[j][0].z, bx[j][0].w);
+        mma_f16(d, a[4], c[4], a[5], c[5], bx[j][1].x, bx[j][1].y);
+        mma_f16(d, a[6], c[6], a[7], c[7], bx[j][1].z, bx[j][1].w);
+        acc[j][mt][0] = fmaf(d[0], d0, acc[j][mt][0]);
+        acc[j][mt][1] = fmaf(d[1], d0, acc[j][mt][1]);
+        acc[j][mt][2] = fmaf(d[2], d1, acc[j][mt][2]);
+        acc[j][mt][3] = fmaf(d[3], d1, acc[j][mt][3]);
+      }
+    }
+  }
+}
+
+// Q3_K, one 16-column sub-block of one row: low code bits w (16 x 2 bits,
+// columns 0..7 in the low half), high bits h16 (bit c = column c), sub-scale
+// s.  Pair p (columns p, 8 + p) as f16 s (q - 4): the two low bits moved to
+// bits 6..7 and the high bit to bit 8 of each half give 1024 + 64 q, and one
+// fma with (s / 64, -20 s) (f16 numbers) leaves s (q - 4) exactly (|.| <= 252).
+__device__ __forceinline__ void q3k_pairs(uint32_t w, uint32_t h16, int s, uint32_t (&a)[8]) {
+  const uint32_t hs = __byte_perm(h16, 0u, 0x4140);  // columns 0..7 -> bits 0..7, 8..15 -> bits 16..23
+  const __half sh = __int2half_rn(s);
+  const __half2 m2 = __half2half2(__hmul(sh, __ushort_as_half(0x2400)));  // s / 64
+  const __half2 c2 = __half2half2(__hmul(sh, __ushort_as_half(0xCD00)));  // -20 s
+  const uint32_t mu = *reinterpret_cast<const uint32_t*>(&m2), cu = *reinterpret_cast<const uint32_t*>(&c2);
+  const uint32_t lo[8] = {w << 6, w << 4, w << 2, w, w >> 2, w >> 4, w >> 6, w >> 8};
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int4* xp = reinterpret_cast<const int4*>(row[r].xh + (bi * 4 + w) * 32);
-        const int4 xa = xp[0], xb = xp[1];
-        const int4 xl = *reinterpret_cast<const int4*>(row[r].xl + (bi * 4 + w) * 16);
-        const int X[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-        const int XL[4] = {xl.x, xl.y, xl.z, xl.w};
+  for (int p = 0; p < 8; ++p) {
+    const uint32_t t = and_or(lo[p], 0x00C000C0u, kF16x2One024);
+    a[p] = hfma2u(and_or(hs << (8 - p), 0x01000100u, t), mu, cu);
+  }
+}
+
+// Q3_K (256-column blocks): thread tq takes sub-blocks tq, 4 + tq, 8 + tq,
+// 12 + tq (word tq of each 16-byte piece of low bits; the high bits of
+// sub-block j are half-word j of the 32 high-bit bytes); the sub-scales are
+// in A, the block's d on the accumulators.  B rows in P order.
+template <int NJ>
+__device__ __forceinline__ void mma_q3k(const uint8_t* tile, int nb, int grp, const uint8_t* const (&bv)[NJ],
+                                        int lane, float (&acc)[NJ][2][4]) {
+  const int gq = lane >> 2, tq = lane & 3;
+  const int b = grp;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          ih[r] = __dp2a_lo(X[2 * k], B[k], ih[r]);
-          ih[r] = __dp2a_hi(X[2 * k + 1], B[k], ih[r]);
-          il[r] = __dp4a(XL[k], B[k], il[r]);
+  for (int mt = 0; mt < 2; ++mt) {
+    float dd[NJ][4];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) dd[j][0] = dd[j][1] = dd[j][2] = dd[j][3] = 0.f;
+    const int r0 = 16 * mt + gq;
+    const uint8_t* sc0 = tile + nb * 3072 + (b * 32 + r0) * 12;
+    const uint8_t* sc1 = tile + nb * 3072 + (b * 32 + r0 + 8) * 12;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      const int sj = 4 * q + tq;  // this thread's sub-block
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(tile + (b * 4 + q) * 512 + r0 * 16 + 4 * tq);
+      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(tile + (b * 4 + q) * 512 + (r0 + 8) * 16 + 4 * tq);
+      const int ho = nb * 2048 + (b * 2 + (q >> 1)) * 512 + 4 * (2 * (q & 1) + (tq >> 1));
+      const uint32_t h0 = (*reinterpret_cast<const uint32_t*>(tile + ho + r0 * 16) >> (16 * (tq & 1))) & 0xFFFFu;
+      const uint32_t h1 = (*reinterpret_cast<const uint32_t*>(tile + ho + (r0 + 8) * 16) >> (16 * (tq & 1))) & 0xFFFFu;
+      // 6-bit sub-scale sj: bits 6 sj .. of the 12 scale bytes (two bytes hold it)
+      const int bit = 6 * sj, by = bit >> 3, sb = bit & 7;
+      const int s0 = (int)(((uint32_t)sc0[by] | ((uint32_t)(by < 11 ? sc0[by + 1] : 0) << 8)) >> sb) & 63;
+      const int s1 = (int)(((uint32_t)sc1[by] | ((uint32_t)(by < 11 ? sc1[by + 1] : 0) << 8)) >> sb) & 63;
+      uint32_t a[8], c[8];
+      q3k_pairs(w0, h0, s0, a);
+      q3k_pairs(w1, h1, s1, c);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const uint4 x0 = *reinterpret_cast<const uint4*>(bv[j] + (b * 256 + 64 * q + 16 * tq) * 2);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(bv[j] + (b * 256 + 64 * q + 16 * tq + 8) * 2);
+        mma_f16(dd[j], a[0], c[0], a[1], c[1], x0.x, x0.y);
+        mma_f16(dd[j], a[2], c[2], a[3], c[3], x0.z, x0.w);
+        mma_f16(dd[j], a[4], c[4], a[5], c[5], x1.x, x1.y);
+        mma_f16(dd[j], a[6], c[6], a[7], c[7], x1.z, x1.w);
+      }
+    }
+    const float d0 = __half2float(*reinterpret_cast<const __half*>(tile + nb * 3456 + (b * 32 + r0) * 2));
+    const float d1 = __half2float(*reinterpret_cast<const __half*>(tile + nb * 3456 + (b * 32 + r0 + 8) * 2));
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      acc[j][mt][0] = fmaf(dd[j][0], d0, acc[j][mt][0]);
+      acc[j][mt][1] = fmaf(dd[j][1], d0, acc[j][mt][1]);
+      acc[j][mt][2] = fmaf(dd[j][2], d1, acc[j][mt][2]);
+      acc[j][mt][3] = fmaf(dd[j][3], d1, acc[j][mt][3]);
+    }
+  }
+}
+
+// TQ1: five base-3 digits of the two code bytes in v = (1024 + B_lo, 1024 +
+// B_hi) as f16x2 (t = digit - 1), in f16 arithmetic: one fma with (1/3 in
+// f16, 682.5) rounds to 1024 + floor(B / 3) for every byte 0..242, a second
+// leaves digit - 2048 (exact), an add of 2047 gives t; four rounds, then the
+// last quotient is the fifth digit.
+__device__ __forceinline__ void tq1_digits(uint32_t v, uint32_t (&a)[5]) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const uint32_t q = hfma2u(v, 0x35553555u, 0x61556155u);    // 1024 + floor(B / 3)
+    a[r] = hadd2u(hfma2u(q, 0xC200C200u, v), 0x67FF67FFu);    // (v - 3 q) + 2047
+    v = q;
+  }
+  a[4] = hadd2u(v, 0xE401E401u);                              // - 1025
+}
+
+// TQ1 (256-column blocks): thread tq takes 13 code bytes of a row: word tq of
+// each of the three 16-byte pieces (bytes 16 q + 4 tq .. + 3) and byte 48 + tq;
+// bytes paired two by two in the halves of an f16x2 give five digit pairs
+// each (the last byte alone), 35 pairs = 18 k16 steps (T order of the B rows).
+template <int NJ>
+__device__ __forceinline__ void mma_tq1(const uint8_t* tile, int nb, int grp, const uint8_t* const (&bv)[NJ],
+                                        int lane, float (&acc)[NJ][2][4]) {
+  const int gq = lane >> 2, tq = lane & 3;
+  const int b = grp;
+  const uint32_t tsel = 0x5450u + (uint32_t)tq;  // byte tq, then 0x64, 0x00, 0x64
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    const int r0 = 16 * mt + gq;
+    float dd[NJ][4];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) dd[j][0] = dd[j][1] = dd[j][2] = dd[j][3] = 0.f;
+    uint32_t w0[3], w1[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      w0[q] = *reinterpret_cast<const uint32_t*>(tile + (b * 3 + q) * 512 + r0 * 16 + 4 * tq);
+      w1[q] = *reinterpret_cast<const uint32_t*>(tile + (b * 3 + q) * 512 + (r0 + 8) * 16 + 4 * tq);
+    }
+    const uint2 t0 = *reinterpret_cast<const uint2*>(tile + nb * 1536 + (b * 32 + r0) * 8);
+    const uint2 t1 = *reinterpret_cast<const uint2*>(tile + nb * 1536 + (b * 32 + r0 + 8) * 8);
+    uint32_t ca = 0, cc = 0;  // pair carried to the next step (rows r0, r0 + 8)
+    uint4 bx[NJ];
+#pragma unroll
+    for (int beta = 0; beta < 7; ++beta) {
+      uint32_t v0, v1;
+      if (beta < 6) {
+        const uint32_t sel = (beta & 1) ? 0x5352u : 0x5150u;
+        v0 = __byte_perm(w0[beta >> 1], 0x64006400u, sel);
+        v1 = __byte_perm(w1[beta >> 1], 0x64006400u, sel);
+      } else {
+        v0 = __byte_perm(t0.x, 0x64006400u, tsel);
+        v1 = __byte_perm(t1.x, 0x64006400u, tsel);
+      }
+      uint32_t a[5], c[5];
+      tq1_digits(v0, a);
+      tq1_digits(v1, c);
+      // pairs 5 beta .. 5 beta + 4; step s takes pairs 2s, 2s + 1
+#pragma unroll
+      for (int k = 0; k < 5; ++k) {
+        const int pi = 5 * beta + k;
+        if ((pi & 1) == 0) {
+          ca = a[k];
+          cc = c[k];
+          if (pi == 34) {  // the last pair meets the zero pair 35 (step 17: the B loaded for step 16)
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) mma_f16(dd[j], ca, cc, 0u, 0u, bx[j].z, bx[j].w);
+          }
+        } else {
+          const int s = pi >> 1;
+          if ((s & 1) == 0) {
+#pragma unroll
+            for (int j = 0; j < NJ; ++j)
+              bx[j] = *reinterpret_cast<const uint4*>(bv[j] + (b * 288 + (s >> 1) * 32 + tq * 8) * 2);
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) mma_f16(dd[j], ca, cc, a[k], c[k], bx[j].x, bx[j].y);
+          } else {
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) mma_f16(dd[j], ca, cc, a[k], c[k], bx[j].z, bx[j].w);
+          }
         }
       }
     }
+    const float d0 = __half2float(__ushort_as_half((unsigned short)(t0.y & 0xFFFFu)));
+    const float d1 = __half2float(__ushort_as_half((unsigned short)(t1.y & 0xFFFFu)));
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int4 sh = *reinterpret_cast<const int4*>(row[r].sh + bi * 4);
-      const int4 sl = *reinterpret_cast<const int4*>(row[r].sl + bi * 4);
-      const int Sh = (sh.x + sh.y) + (sh.z + sh.w), Sl = (sl.x + sl.y) + (sl.z + sl.w);
-      // sum of (2q - 3) X, exact in each part
-      acc[r].x = fmaf(d * row[r].sc, hi_lo(2 * ih[r] - 3 * Sh, 2 * il[r] - 3 * Sl), acc[r].x);
+    for (int j = 0; j < NJ; ++j) {
+      acc[j][mt][0] = fmaf(dd[j][0], d0, acc[j][mt][0]);
+      acc[j][mt][1] = fmaf(dd[j][1], d0, acc[j][mt][1]);
+      acc[j][mt][2] = fmaf(dd[j][2], d1, acc[j][mt][2]);
+      acc[j][mt][3] = fmaf(dd[j][3], d1, acc[j][mt][3]);
     }
   }
 }
 
-template <int R>
-__device__ __forceinline__ void group_q3k_i(const uint8_t* tile, int nb, int grp, const uint8_t* act, int rowb,
-                                            int kc, int lane, float2 (&acc)[R]) {
-  IntRow row[R];
+// B column pointers of the thread and the group loop of the format, then the
+// partial sums of each (row, weight row) into outv[r * 32 + weight row].
+template <int NJ>
+__device__ __forceinline__ void mma_group_nj(int R, int fmt, const uint8_t* tile, int kc, int nb, int grp,
+                                             const uint8_t* act, int rstr, int lane, float* outv, bool hl) {
+  const int gq = lane >> 2, tq = lane & 3;
+  const int flen = f16_len(fmt, kc);
+  const uint8_t* bv[NJ];
 #pragma unroll
-  for (int r = 0; r < R; ++r) row[r] = int_row(act, r, rowb, BQE_FMT_Q3_K, kc, grp);
-  const int b = grp;
-  uint32_t lo[16], hi[8], sc[3];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 v = *reinterpret_cast<const uint4*>(tile + (b * 4 + q) * 512 + lane * 16);
-    lo[4 * q] = v.x; lo[4 * q + 1] = v.y; lo[4 * q + 2] = v.z; lo[4 * q + 3] = v.w;
+  for (int j = 0; j < NJ; ++j) {
+    // B column gq: x row gq (W1/W3); hi (gq even) or lo of row 4 j + gq / 2 (W2).
+    // Columns past the item's rows repeat its last row: their results are dropped.
+    const int r = hl ? min(4 * j + (gq >> 1), R - 1) : min(gq, R - 1);
+    bv[j] = act + r * rstr + (hl && (gq & 1) ? 2 * flen + 64 : 0);
   }
+  float acc[NJ][2][4];
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const uint4 v = *reinterpret_cast<const uint4*>(tile + nb * 2048 + (b * 2 + q) * 512 + lane * 16);
-    hi[4 * q] = v.x; hi[4 * q + 1] = v.y; hi[4 * q + 2] = v.z; hi[4 * q + 3] = v.w;
+  for (int j = 0; j < NJ; ++j)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) acc[j][mt][0] = acc[j][mt][1] = acc[j][mt][2] = acc[j][mt][3] = 0.f;
+  switch (fmt) {
+    case BQE_FMT_MXFP4: mma_mxfp4<NJ>(tile, nb, grp, bv, lane, acc); break;
+    case BQE_FMT_Q2_0: mma_q2_0<NJ>(tile, nb, grp, bv, lane, acc); break;
+    case BQE_FMT_Q3_K: mma_q3k<NJ>(tile, nb, grp, bv, lane, acc); break;
+    case BQE_FMT_TQ1:
+      if (NJ == 1) mma_tq1<1>(tile, nb, grp, reinterpret_cast<const uint8_t* const(&)[1]>(bv), lane,
+                              reinterpret_cast<float(&)[1][2][4]>(acc));
+      break;
+    default: break;
   }
-  const uint8_t* scp = tile + nb * 3072 + (b * 32 + lane) * 12;
+  if (!hl) {
+    // thread tq holds x rows 2 tq, 2 tq + 1
 #pragma unroll
-  for (int i = 0; i < 3; ++i) sc[i] = *reinterpret_cast<const uint32_t*>(scp + 4 * i);
-  const float d = __half2float(*reinterpret_cast<const __half*>(tile + nb * 3456 + (b * 32 + lane) * 2));
-  int bh[R], bl[R];
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-  for (int r = 0; r < R; ++r) bh[r] = bl[r] = 0;
-#pragma unroll
-  for (int sj = 0; sj < 16; ++sj) {
-    const int bit = 6 * sj;
-    const uint64_t two = ((uint64_t)sc[bit >> 5]) | (((bit >> 5) < 2 ? (uint64_t)sc[(bit >> 5) + 1] : 0ull) << 32);
-    const int s = (int)((uint32_t)(two >> (bit & 31)) & 63u);
-    const uint32_t low = lo[sj];
-    const uint32_t h16 = (hi[sj >> 1] >> ((sj & 1) * 16)) & 0xFFFFu;  // high bits of weights 16 sj ..
-    int B[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      // byte i: q of weight k + 4i = low 2 bits | 4 * high bit (the high bit placed by a byte
-      // permute: selector nibble i is 4 when the bit is set, picking 0x04, else 0 picking 0x00)
-      const uint32_t sel = ((h16 >> k) << 2) & 0x4444u;
-      B[k] = (int)(((low >> (2 * k)) & 0x03030303u) | __byte_perm(0u, 0x04040404u, sel));
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int4* xp = reinterpret_cast<const int4*>(row[r].xh + sj * 32);
-      const int4 xa = xp[0], xb = xp[1];
-      const int4 xl = *reinterpret_cast<const int4*>(row[r].xl + sj * 16);
-      const int X[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-      const int XL[4] = {xl.x, xl.y, xl.z, xl.w};
-      int th = 0, tl = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        th = __dp2a_lo(X[2 * k], B[k], th);
-        th = __dp2a_hi(X[2 * k + 1], B[k], th);
-        tl = __dp4a(XL[k], B[k], tl);
+      for (int e = 0; e < 4; ++e) {
+        const int r = 2 * tq + (e & 1), wr = 16 * mt + gq + 8 * (e >> 1);
+        if (r < R) outv[r * 32 + wr] = acc[0][mt][e];
       }
-      // s_j * sum of (q - 4) X per part; |block sums| < 2^31
-      bh[r] += s * (th - 4 * row[r].sh[sj]);
-      bl[r] += s * (tl - 4 * row[r].sl[sj]);
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r) acc[r].x = fmaf(d * row[r].sc, hi_lo(bh[r], bl[r]), acc[r].x);
-}
-
-// One 32-bit word of a TQ1 row (bytes 4m .. 4m + 3: run m of 20 columns):
-// its five base-3 digits per byte, met with the T-order X of run m.
-template <int R>
-__device__ __forceinline__ void tq1_run(uint32_t wv, int m, const IntRow (&row)[R], int (&ih)[R], int (&il)[R]) {
-  // bytes 4m, 4m+2 in the 16-bit lanes of ve; 4m+1, 4m+3 in vo
-  uint32_t ve = wv & 0x00FF00FFu, vo = (wv >> 8) & 0x00FF00FFu;
-  int B[5];
-#pragma unroll
-  for (int rd = 0; rd < 5; ++rd) {
-    // digit rd of the four bytes: v / 3 per 16-bit lane ((v * 171) >> 9 for v <= 255)
-    const uint32_t qe = ((ve * 171u) >> 9) & 0x007F007Fu, qo = ((vo * 171u) >> 9) & 0x007F007Fu;
-    const uint32_t de = ve - 3u * qe, dq = vo - 3u * qo;
-    ve = qe;
-    vo = qo;
-    B[rd] = (int)__byte_perm(de, dq, 0x6240);  // digits of bytes 4m, 4m+1, 4m+2, 4m+3
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int2* xp = reinterpret_cast<const int2*>(row[r].xh + m * 40);
-    const int* xl = reinterpret_cast<const int*>(row[r].xl + m * 20);
-#pragma unroll
-    for (int rd = 0; rd < 5; ++rd) {
-      const int2 v = xp[rd];
-      ih[r] = __dp2a_lo(v.x, B[rd], ih[r]);
-      ih[r] = __dp2a_hi(v.y, B[rd], ih[r]);
-      il[r] = __dp4a(xl[rd], B[rd], il[r]);
-    }
-  }
-}
-
-template <int R>
-__device__ __forceinline__ void group_tq1_i(const uint8_t* tile, int nb, int grp, const uint8_t* act, int rowb,
-                                            int kc, int lane, float2 (&acc)[R]) {
-  IntRow row[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) row[r] = int_row(act, r, rowb, BQE_FMT_TQ1, kc, grp);
-  const int b = grp;
-  const uint2 tail = *reinterpret_cast<const uint2*>(tile + nb * 1536 + (b * 32 + lane) * 8);
-  const float d = __half2float(__ushort_as_half((unsigned short)(tail.y & 0xFFFFu)));
-  int ih[R], il[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) ih[r] = il[r] = 0;
-  // words 0..11 (bytes 0..47) four at a time, then word 12 (bytes 48..51;
-  // byte 51 <= 2, so its higher digits are 0)
-#pragma unroll 1
-  for (int q = 0; q < 3; ++q) {
-    const uint4 v = *reinterpret_cast<const uint4*>(tile + (b * 3 + q) * 512 + lane * 16);
-    tq1_run<R>(v.x, 4 * q, row, ih, il);
-    tq1_run<R>(v.y, 4 * q + 1, row, ih, il);
-    tq1_run<R>(v.z, 4 * q + 2, row, ih, il);
-    tq1_run<R>(v.w, 4 * q + 3, row, ih, il);
-  }
-  tq1_run<R>(tail.x, 12, row, ih, il);
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    int Sh = 0, Sl = 0;
-#pragma unroll
-    for (int i = 0; i < 16; i += 4) {
-      const int4 a = *reinterpret_cast<const int4*>(row[r].sh + i);
-      const int4 c = *reinterpret_cast<const int4*>(row[r].sl + i);
-      Sh += (a.x + a.y) + (a.z + a.w);
-      Sl += (c.x + c.y) + (c.z + c.w);
-    }
-    acc[r].x = fmaf(d * row[r].sc, hi_lo(ih[r] - Sh, il[r] - Sl), acc[r].x);  // sum of (t - 1) X, t the digit
-  }
-}
-
-// Activation modes of an item: 0 fp32 rows, 1 f16 rows (x 2^s, MXFP4 W1/W3),
-// 2 integer rows (X in the format's order, then the 16-column sums).
-enum { kActF32 = 0, kActF16 = 1, kActInt = 2 };
-
-// Mode of the activations of an item: integer for the fp16-scaled formats
-// (both phases); for MXFP4 f16 in W1/W3 and fp32 in W2 (h stays fp32).
-__host__ __device__ inline int act_mode(int phase, int fmt) {
-  if (fmt != BQE_FMT_MXFP4) return kActInt;
-  return phase == 0 ? kActF16 : kActF32;
-}
-
-__host__ __device__ inline int act_row_bytes(int amode, int fmt, int kc) {
-  return amode == kActF32 ? kc * 4 : amode == kActF16 ? kc * 2 : (int)int_rec_bytes(fmt == BQE_FMT_TQ1, kc);
-}
-
-// nb: format blocks per tile row (kc / block width), from the stage header
-template <int R>
-__device__ __forceinline__ void consume_group_R(int fmt, const uint8_t* tile, int kc, int nb, int grp,
-                                                const uint8_t* act, int lane, float* outv /* [r * 32 + lane] */,
-                                                int amode) {
-  float2 acc[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = f2(0.f, 0.f);
-  if (amode == kActInt) {
-    const int rowb = act_row_bytes(kActInt, fmt, kc);
-    switch (fmt) {
-      case BQE_FMT_Q2_0: group_q2_0_i<R>(tile, nb, grp, act, rowb, kc, lane, acc); break;
-      case BQE_FMT_TQ1: group_tq1_i<R>(tile, nb, grp, act, rowb, kc, lane, acc); break;
-      case BQE_FMT_Q3_K: group_q3k_i<R>(tile, nb, grp, act, rowb, kc, lane, acc); break;
-    }
-  } else if (amode == kActF16) {
-    group_mxfp4_h<R>(tile, nb, grp, reinterpret_cast<const uint16_t*>(act), kc, lane, acc);
   } else {
-    group_mxfp4<R>(tile, nb, grp, reinterpret_cast<const float*>(act), kc, lane, acc);
-  }
+    // thread tq holds hi and lo of row 4 j + tq; the group's 2^-s removed here
 #pragma unroll
-  for (int r = 0; r < R; ++r) outv[r * 32 + lane] = acc[r].x + acc[r].y;
+    for (int j = 0; j < NJ; ++j) {
+      const int r = 4 * j + tq;
+      if (r < R) {
+        const float us = reinterpret_cast<const float*>(act + r * rstr + 4 * flen + 64)[grp];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          outv[r * 32 + 16 * mt + gq] = (acc[j][mt][0] + acc[j][mt][1]) * us;
+          outv[r * 32 + 16 * mt + gq + 8] = (acc[j][mt][2] + acc[j][mt][3]) * us;
+        }
+      }
+    }
+  }
 }
 
+// The loop of one task: R <= 8 rows (RC == 1: one row).
 template <int RC>
-__device__ __forceinline__ void consume_group(int R, int fmt, const uint8_t* tile, int kc, int nb, int grp,
-                                              const uint8_t* act, int lane, float* outv, int amode) {
-  if (RC == 1 || R == 1) {
-    consume_group_R<1>(fmt, tile, kc, nb, grp, act, lane, outv, amode);
-    return;
-  }
-  if (RC == 2) {
-    consume_group_R<(RC >= 2 ? 2 : 1)>(fmt, tile, kc, nb, grp, act, lane, outv, amode);
-    return;
-  }
-  switch (R) {
-    case 2: consume_group_R<2>(fmt, tile, kc, nb, grp, act, lane, outv, amode); break;
-    case 3: consume_group_R<(RC >= 3 ? 3 : 1)>(fmt, tile, kc, nb, grp, act, lane, outv, amode); break;
-    case 4: consume_group_R<(RC >= 4 ? 4 : 1)>(fmt, tile, kc, nb, grp, act, lane, outv, amode); break;
-  }
-}
-
-// All R rows of one stage, RC (1 or kRowChunk) rows at a time (the weights of
-// the group are decoded again for each further chunk).  A kernel instance for
-// one-row calls (RC = 1) carries only the one-row inner loops, which keeps its
-// code small and its register count low.
-template <int RC>
-__device__ __forceinline__ void consume_rows(int R, int fmt, const uint8_t* tile, int kc, int nb, int grp,
-                                             const uint8_t* act, int lane, float* outv, int amode) {
-  static_assert(RC == 1 || RC == 2 || RC == kRowChunk, "row chunk");
-  const size_t row_bytes = (size_t)act_row_bytes(amode, fmt, kc);
-  for (int r0 = 0; r0 < R; r0 += RC) {
-    const int n = R - r0 < RC ? R - r0 : RC;
-    consume_group<RC>(n, fmt, tile, kc, nb, grp, act + r0 * row_bytes, lane, outv + r0 * 32, amode);
+__device__ __forceinline__ void consume_mma(int R, int fmt, const uint8_t* tile, int kc, int nb, int grp,
+                                            const uint8_t* act, int lane, float* outv, int amode) {
+  const int rstr = act_row_stride(amode, fmt, kc);
+  const bool hl = amode == kActH16;
+  if (RC == 1 || !hl || R <= 4) {
+    mma_group_nj<1>(RC == 1 ? 1 : R, fmt, tile, kc, nb, grp, act, rstr, lane, outv, hl);
+  } else if (fmt == BQE_FMT_TQ1) {
+    // W2 rows 0..3, then 4..: ternary codes decoded twice (two MMAs per step
+    // would not fit this kernel's register budget)
+    mma_group_nj<1>(4, fmt, tile, kc, nb, grp, act, rstr, lane, outv, true);
+    mma_group_nj<1>(R - 4, fmt, tile, kc, nb, grp, act + 4 * rstr, rstr, lane, outv + 4 * 32, true);
+  } else {
+    mma_group_nj<2>(R, fmt, tile, kc, nb, grp, act, rstr, lane, outv, hl);
   }
 }
-
-__device__ __forceinline__ float silu_f(float t) { return t / (1.0f + expf(-t)); }
-
 
 }  // namespace bqe

@@ -77,7 +77,6 @@ __host__ __device__ inline uint32_t tile_byte_offset(int f, int nb, int b, int r
 // ----------------------------------------------------------------------------
 constexpr int kMaxM = 8;          // rows per decode call
 constexpr int kMaxTopK = 16;
-constexpr int kRowChunk = 4;      // rows accumulated together by the widest inner loops
 constexpr int kMaxU = 64;         // distinct experts of one decode call (M top_k + 1 <= 64)
 
 struct Geo {
@@ -97,34 +96,63 @@ __host__ __device__ inline Geo make_geo(int H, int I, int E, int K, int M) {
   return g;
 }
 
-// Integer staging record of one activation row and one K chunk of kc
-// columns (kc a multiple of 256):
-//   [X_hi | X_lo | int32 sums of X_hi per 16 columns | the same of X_lo |
-//    2^-si of each 256 columns (4 float slots)]
-// with X_hi / X_lo in "Q order" (tq = 0: 2 kc + kc bytes) or "T order"
-// (tq = 1: 528 + 272 bytes per 256 columns).  One record is exactly one
-// staged activation row of a ring stage, so it moves with one bulk copy.
-__host__ __device__ constexpr uint32_t int_rec_hi_bytes(int tq, int kc) { return tq ? (kc / 256) * 528 : kc * 2; }
-__host__ __device__ constexpr uint32_t int_rec_lo_bytes(int tq, int kc) { return tq ? (kc / 256) * 272 : kc; }
-__host__ __device__ constexpr uint32_t int_rec_bytes(int tq, int kc) {
-  return int_rec_hi_bytes(tq, kc) + int_rec_lo_bytes(tq, kc) + kc / 2 + 16;
+// f16 activation rows of the tensor-core loops, in the column order of the
+// format (inside every 256 columns):
+//   natural (MXFP4): position = column;
+//   "P order" (Q2_0, Q3_K): in every 16 columns, position 2p holds column p
+//     and 2p + 1 column 8 + p (p = 0..7): the columns of the code pairs that
+//     one lop3 lifts out of a 32-bit word of codes;
+//   "T order" (TQ1): 288 positions per 256 columns (t16_col), 32 of them zero.
+// Halves per 256 columns:
+__host__ __device__ constexpr int f16_run(int fmt) { return fmt == BQE_FMT_TQ1 ? 288 : 256; }
+// halves of one staged row of kc columns
+__host__ __device__ constexpr int f16_len(int fmt, int kc) { return (kc / 256) * f16_run(fmt); }
+// Column (0..255) at position pos (0..287) of a T-order run, or -1 (zero).
+// The thread tq = (pos / 8) % 4 of a k16 step s = 2 (pos / 32) + (pos / 4) % 2
+// holds pair pi = 2 s + (pos / 2) % 2 of its TQ1 codes, half pos % 2; pair pi
+// is digit pi % 5 of two code bytes (pi / 5 = 0..5: bytes 2 (pi/5 % 2) + {0, 1}
+// of the tq-th 4-byte word of 16-byte piece pi / 10; pi / 5 = 6: code byte
+// 48 + tq, in the low half only; pi = 35: none).
+__host__ __device__ inline int t16_col(int pos) {
+  const int s = 2 * (pos >> 5) + ((pos >> 2) & 1), tq = (pos >> 3) & 3;
+  const int pi = 2 * s + ((pos >> 1) & 1), half = pos & 1;
+  if (pi >= 35) return -1;
+  const int beta = pi / 5, r = pi - 5 * beta;
+  int n;
+  if (beta == 6) {
+    if (half) return -1;
+    n = 48 + tq;
+    if (n == 51) return r == 0 ? 255 : -1;
+  } else {
+    n = 16 * (beta >> 1) + 4 * tq + 2 * (beta & 1) + half;
+  }
+  return 5 * n + r;
 }
+// P-order position of column c (both within their 16)
+__host__ __device__ inline int p16_pos(int c) { return 2 * (c & 7) + (c >> 3); }
+
+// f16 record of h for one row slot and one K chunk of W2 (the tensor-core
+// loops): [hi: f16_len halves | 64 bytes | lo: f16_len halves | 2^-s of each
+// 256 columns (4 float slots)], h 2^s = hi + lo, in the format's order.
+__host__ __device__ constexpr uint32_t h16_rec_bytes(int fmt, int kc) { return 4u * f16_len(fmt, kc) + 80u; }
+// workspace stride of the records of h (T order is the longest)
+__host__ __device__ constexpr uint32_t hrec_stride(int kc) { return (h16_rec_bytes(BQE_FMT_TQ1, kc) + 15u) & ~15u; }
 
 // Workspace layout (offsets in bytes, each 256-aligned).
 struct WsLayout {
   // the router kernel's arrival counter and the call's work list (distinct
   // experts: slot, format, address, rows), combine indices and weights
   uint64_t err, ctr_route, nu, u_slot, u_fmt, u_addr, u_nrows, u_rows, comb_u, comb_r, comb_w;
-  // logits; the layer input in fp32, in f16 x 2^s, 2^-s per row, and as the
-  // integer records of the two orders; the diagnostic counters
-  uint64_t z, xf, xh, xsc, xrq, xrt, dbg;
+  // logits; the layer input as f16 x 2^s (per-row s) in the natural, P and T
+  // orders; the diagnostic counters
+  uint64_t z, xh, xp, xt, dbg;
   // single-kernel decode layer: (selection key, logit) of every (row, expert)
   uint64_t zk;
   // single-kernel decode layer (k_moe): call epoch, logits arrival counter,
   // per work-list expert the counts of its W1/W3 items done and of its h
   // units written; per "row slot" (an expert's r-th row; M (K + 1) slots at
-  // most) the K-chunk partials of g/u, h in fp32 and the integer records of h
-  uint64_t epoch, zt, m_ca, m_ch, m_pa, m_h, m_hr;
+  // most) the K-chunk partials of g/u and the f16 records of h (h16_rec_bytes)
+  uint64_t epoch, zt, m_ca, m_ch, m_pa, m_hr;
   uint64_t total;
 };
 constexpr int kDbgSlots = 8;      // per-CTA counters of the diagnostic mode
@@ -147,14 +175,9 @@ __host__ __device__ inline WsLayout make_ws(const Geo& g) {
   w.comb_r = o; o = al256(o + 4ull * g.M * g.K);
   w.comb_w = o; o = al256(o + 4ull * g.M * g.K);
   w.z = o; o = al256(o + 4ull * g.M * g.E);
-  w.xf = o; o = al256(o + 4ull * g.M * g.H);
   w.xh = o; o = al256(o + 2ull * g.M * g.H);   // f16(x * 2^s_m): exact, per-row power-of-two scale
-  w.xsc = o; o = al256(o + 4ull * kMaxM);      // 2^-s_m
-  // x as X_hi + X_lo / 128 with X_hi = rint(x 2^si) (int16) and X_lo the
-  // int8 residual: one record per (row, K chunk) in each of the two orders
-  // of the integer GEMV paths (int_rec_bytes)
-  w.xrq = o; o = al256(o + (uint64_t)int_rec_bytes(0, g.kcA) * g.M * g.nchA);
-  w.xrt = o; o = al256(o + (uint64_t)int_rec_bytes(1, g.kcA) * g.M * g.nchA);
+  w.xp = o; o = al256(o + 2ull * g.M * g.H);   // the same in P order
+  w.xt = o; o = al256(o + 2ull * g.M * (g.H / 256) * 288);  // ... and in T order
   w.dbg = o; o = al256(o + 8ull * 3 * kDbgMaxCtas * kDbgSlots);
   w.zk = o; o = al256(o + 8ull * g.M * g.E);
   // the call epoch and the counters are contiguous: [epoch, m_pa) clears them
@@ -164,8 +187,7 @@ __host__ __device__ inline WsLayout make_ws(const Geo& g) {
   w.m_ch = o; o = al256(o + 4ull * kMaxU);                         // h units written, per expert
   const uint64_t nrs = (uint64_t)g.M * (g.K + 1);
   w.m_pa = o; o = al256(o + 4ull * nrs * g.npanA * g.nchA * 2 * 32);
-  w.m_h = o; o = al256(o + 4ull * nrs * g.I);
-  w.m_hr = o; o = al256(o + (uint64_t)int_rec_bytes(1, g.kcB) * nrs * g.nchB);
+  w.m_hr = o; o = al256(o + (uint64_t)hrec_stride(g.kcB) * nrs * g.nchB);
   w.total = o;
   return w;
 }
@@ -359,46 +381,6 @@ __device__ __forceinline__ float4 ldg_stream_f4(const float4* p, uint64_t pol) {
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "l"(p), "l"(pol));
   return v;
-}
-// Writers of the integer staging records (int_rec_bytes): X_hi / X_lo of
-// column j (0..255) of the k-th 256-column block of the chunk, in the
-// record's order.  Q order: within 16 columns, X_hi word 2q = (x_q, x_{q+4}),
-// word 2q + 1 = (x_{q+8}, x_{q+12}), X_lo word q = (x_q, x_{q+4}, x_{q+8},
-// x_{q+12}).  T order: in run m of 20 columns, X_hi word 2r = (x_{20m+r},
-// x_{20m+5+r}), word 2r + 1 = (x_{20m+10+r}, x_{20m+15+r}), X_lo word r =
-// (x_{20m+r}, x_{20m+5+r}, x_{20m+10+r}, x_{20m+15+r}); slots past column
-// 255 are zero (rec_put_pad).
-__device__ __forceinline__ void rec_put(uint8_t* rec, int tq, int kc, int k, int j, int Xh, int Xl) {
-  int16_t* hi = reinterpret_cast<int16_t*>(rec);
-  int8_t* lo = reinterpret_cast<int8_t*>(rec + int_rec_hi_bytes(tq, kc));
-  if (tq) {
-    const int run = j / 20, jr = j % 20, q4 = jr / 5, rd = jr % 5;
-    hi[k * 264 + run * 20 + 4 * rd + 2 * (q4 >> 1) + (q4 & 1)] = (int16_t)Xh;
-    lo[k * 272 + run * 20 + 4 * rd + q4] = (int8_t)Xl;
-  } else {
-    const int jj = j & 15, kq = jj & 3, iq = jj >> 2;
-    hi[k * 256 + (j & ~15) + 4 * kq + 2 * (iq >> 1) + (iq & 1)] = (int16_t)Xh;
-    lo[k * 256 + (j & ~15) + 4 * kq + iq] = (int8_t)Xl;
-  }
-}
-// T order: slot i (0..15) of the padding of block k (run 12's weights 256..259
-// and the tail slots), written as zero
-__device__ __forceinline__ void rec_put_pad(uint8_t* rec, int kc, int k, int i) {
-  int16_t* hi = reinterpret_cast<int16_t*>(rec);
-  int8_t* lo = reinterpret_cast<int8_t*>(rec + int_rec_hi_bytes(1, kc));
-  const int slot = i < 4 ? 240 + 4 * (i + 1) + 3 : 260 + (i - 4);
-  if (i < 8) hi[k * 264 + slot] = 0;
-  lo[k * 272 + slot] = 0;
-}
-// sums of X_hi and X_lo over the 16-column group g16 (0..15) of block k
-__device__ __forceinline__ void rec_put_sums(uint8_t* rec, int tq, int kc, int k, int g16, int sh, int sl) {
-  int32_t* sp = reinterpret_cast<int32_t*>(rec + int_rec_hi_bytes(tq, kc) + int_rec_lo_bytes(tq, kc));
-  sp[k * 16 + g16] = sh;
-  sp[kc / 16 + k * 16 + g16] = sl;
-}
-// 2^-si of block k
-__device__ __forceinline__ void rec_put_scale(uint8_t* rec, int tq, int kc, int k, float v) {
-  reinterpret_cast<float*>(rec + int_rec_hi_bytes(tq, kc) + int_rec_lo_bytes(tq, kc) + kc / 2)[k] = v;
 }
 
 // Selection key of an expert: sigmoid(z) + b as an order-preserving 32-bit

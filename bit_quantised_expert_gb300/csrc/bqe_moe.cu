@@ -57,7 +57,8 @@ struct ItemHdr {
   uint32_t tb;        // bytes of one weight tile
   uint32_t act;       // offset of the activation rows (from off)
   uint32_t red;       // offset of the partial sums (from off)
-  uint32_t arow;      // staged bytes of one activation row
+  uint32_t arow;      // staged bytes of one activation row (one bulk copy)
+  uint32_t astr;      // distance between two staged rows
   int16_t u, p, c, R; // expert (work-list index), panel (W1/W3) or panel group (W2), K chunk, rows
   uint8_t phase, fmt, amode, nb;
 };
@@ -169,13 +170,14 @@ __device__ __forceinline__ bool wait_ge(const unsigned int* p, uint32_t target, 
 __device__ inline void make_tpl(const MoeParams& P, ItemTpl& T, int ph, int u, int fmt, uint64_t addr, int R, int rb) {
   const Geo& g = P.g;
   const int kc = ph ? g.kcB : g.kcA;
-  const int amode = act_mode(ph, fmt);
+  const int amode = act_mode(ph);
   ItemHdr& h = T.h;
   h.tb = tile_bytes(fmt, kc);
   h.arow = (uint32_t)act_row_bytes(amode, fmt, kc);
+  h.astr = (uint32_t)act_row_stride(amode, fmt, kc);
   T.wbytes = (uint32_t)(ph ? P.PB : 2) * h.tb;
   h.act = al128(T.wbytes);
-  h.red = h.act + al128((uint32_t)R * h.arow);
+  h.red = h.act + al128((uint32_t)R * h.astr);
   h.off = 0;
   h.u = (int16_t)u; h.p = 0; h.c = 0; h.R = (int16_t)R;
   h.phase = (uint8_t)ph; h.fmt = (uint8_t)fmt; h.amode = (uint8_t)amode; h.nb = (uint8_t)(kc / fmt_bw(fmt));
@@ -183,28 +185,15 @@ __device__ inline void make_tpl(const MoeParams& P, ItemTpl& T, int ph, int u, i
   const uint64_t m13 = matrix_bytes(fmt, g.I, g.H);
   T.m13 = (uint32_t)m13;
   T.wsrc = addr + (ph ? 2 * m13 : 0);
-  if (ph == 0) {
-    if (amode == kActInt) {
-      T.act_base = (uint32_t)(fmt == BQE_FMT_TQ1 ? P.L.xrt : P.L.xrq);
-      T.act_cs = h.arow;
-      T.act_rs = h.arow * g.nchA;
-    } else {
-      const uint32_t es = amode == kActF16 ? 2 : 4;
-      T.act_base = (uint32_t)(amode == kActF16 ? P.L.xh : P.L.xf);
-      T.act_cs = (uint32_t)kc * es;
-      T.act_rs = (uint32_t)g.H * es;
-    }
-  } else {
-    if (amode == kActInt) {
-      const uint32_t rec = int_rec_bytes(1, g.kcB);
-      T.act_base = (uint32_t)(P.L.m_hr + (uint64_t)rb * g.nchB * rec);
-      T.act_cs = rec;
-      T.act_rs = rec * g.nchB;
-    } else {
-      T.act_base = (uint32_t)(P.L.m_h + (uint64_t)rb * g.I * 4);
-      T.act_cs = (uint32_t)g.kcB * 4;
-      T.act_rs = (uint32_t)g.I * 4;
-    }
+  if (ph == 0) {  // f16 x in the format's order
+    T.act_base = (uint32_t)(fmt == BQE_FMT_MXFP4 ? P.L.xh : fmt == BQE_FMT_TQ1 ? P.L.xt : P.L.xp);
+    T.act_cs = (uint32_t)f16_len(fmt, kc) * 2;
+    T.act_rs = (uint32_t)f16_len(fmt, g.H) * 2;
+  } else {  // the f16 records of h of the expert's row slots
+    const uint32_t rec = hrec_stride(g.kcB);
+    T.act_base = (uint32_t)(P.L.m_hr + (uint64_t)rb * g.nchB * rec);
+    T.act_cs = rec;
+    T.act_rs = rec * g.nchB;
   }
 }
 
@@ -242,6 +231,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
   __shared__ float s_part[kRouteTasks][kMaxM];
   __shared__ float s_inv_rms[kMaxM], s_xsc[kMaxM];
   __shared__ int s_emax[kMaxM];
+  __shared__ float s_hunit[256];  // h warp: one unit of h (T-order records)
   __shared__ float s_red[kCW][kMaxM];
   __shared__ float s_bias[kMaxEM];
   __shared__ uint64_t s_eaddr[kMaxEM + 1];  // slot address of each expert (E: the shared one)
@@ -373,7 +363,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           const uint8_t* src0 = P.ws + T.act_base + (uint64_t)c * T.act_cs;
           for (int r = 0; r < T.h.R; ++r) {
             const int row = (T.h.phase == 0 && T.h.u != 0) ? s_urows[T.h.u * kMaxM + r] : r;
-            bulk_g2s(dst + T.h.act + (size_t)r * T.h.arow, src0 + (uint64_t)row * T.act_rs, T.h.arow, bar);
+            bulk_g2s(dst + T.h.act + (size_t)r * T.h.astr, src0 + (uint64_t)row * T.act_rs, T.h.arow, bar);
           }
         }
       };
@@ -589,46 +579,30 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     if (ct < M) s_xsc[ct] = ldexpf(1.0f, -(s_emax[ct] == -1000 ? 0 : 14 - s_emax[ct]));
     // ---- this CTA's slice of the staged copies of the input (read by every CTA's bulk copies)
     {
-      float* xf = (float*)(P.ws + P.L.xf);
       uint16_t* xh = (uint16_t*)(P.ws + P.L.xh);
       const int n = M * H, per = (n + G - 1) / G, lo = min(n, per * cta), hi = min(n, lo + per);
+      uint16_t* xp = (uint16_t*)(P.ws + P.L.xp);
       for (int i = lo + ct; i < hi; i += NCT) {
         const int m = i / H;
         const float v = __uint_as_float((uint32_t)xs[i] << 16);
         const int sh = s_emax[m] == -1000 ? 0 : 14 - s_emax[m];
-        xf[i] = v;
-        xh[i] = __half_as_ushort(__float2half_rn(ldexpf(v, sh)));
+        const uint16_t hv = __half_as_ushort(__float2half_rn(ldexpf(v, sh)));
+        xh[i] = hv;
+        xp[(i & ~15) + p16_pos(i & 15)] = hv;  // P order
         if (P.t_out) P.t_out[i] = xs[i];
       }
-      // integer records X_hi + X_lo / 128 of x 2^si in the two orders, one
-      // 256-column block per 256 threads
-      const int nbr = H / 256, nblk = M * nbr, bpc = g.kcA / 256;
-      const int half = ct >> 8, j = ct & 255;
-      for (int blk = cta + half * G; blk < nblk; blk += 2 * G) {
-        const int m = blk / nbr, bj = blk % nbr;
-        const int c = bj / bpc, k = bj % bpc;
-        uint8_t* rq = P.ws + P.L.xrq + ((size_t)m * g.nchA + c) * int_rec_bytes(0, g.kcA);
-        uint8_t* rt = P.ws + P.L.xrt + ((size_t)m * g.nchA + c) * int_rec_bytes(1, g.kcA);
-        const int si = s_emax[m] == -1000 ? 0 : 13 - s_emax[m];
-        const float v = ldexpf(__uint_as_float((uint32_t)xs[m * H + bj * 256 + j] << 16), si);
-        const int Xh = __float2int_rn(v);
-        const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
-        rec_put(rq, 0, g.kcA, k, j, Xh, Xl);
-        rec_put(rt, 1, g.kcA, k, j, Xh, Xl);
-        if (j < 16) rec_put_pad(rt, g.kcA, k, j);
-        int ph = Xh, pl = Xl;
-#pragma unroll
-        for (int o = 8; o; o >>= 1) {
-          ph += __shfl_xor_sync(0xffffffffu, ph, o);
-          pl += __shfl_xor_sync(0xffffffffu, pl, o);
-        }
-        if ((lane & 15) == 0) {
-          rec_put_sums(rq, 0, g.kcA, k, j >> 4, ph, pl);
-          rec_put_sums(rt, 1, g.kcA, k, j >> 4, ph, pl);
-        }
-        if (j == 0) {
-          rec_put_scale(rq, 0, g.kcA, k, ldexpf(1.0f, -si));
-          rec_put_scale(rt, 1, g.kcA, k, ldexpf(1.0f, -si));
+      {  // T order: 288 positions per 256 columns, 32 of them zero
+        uint16_t* xt = (uint16_t*)(P.ws + P.L.xt);
+        const int nt = M * (H / 256) * 288, pt = (nt + G - 1) / G, tlo = min(nt, pt * cta), thi = min(nt, tlo + pt);
+        for (int i = tlo + ct; i < thi; i += NCT) {
+          const int run = i / 288, pos = i - run * 288, m = run / (H / 256);
+          const int col = t16_col(pos);
+          uint16_t hv = 0;
+          if (col >= 0) {
+            const float v = __uint_as_float((uint32_t)xs[run * 256 + col] << 16);
+            hv = __half_as_ushort(__float2half_rn(ldexpf(v, s_emax[m] == -1000 ? 0 : 14 - s_emax[m])));
+          }
+          xt[i] = hv;
         }
       }
     }
@@ -1008,8 +982,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           grp = tau - tile_i * g.GB;
         }
         float* red = reinterpret_cast<float*>(const_cast<uint8_t*>(base) + h.red) + tau * h.R * 32;
-        consume_rows<RC>(h.R, h.fmt, base + tile_i * h.tb, isA ? g.kcA : g.kcB, h.nb, grp, base + h.act, lane, red,
-                         h.amode);
+        consume_mma<RC>(h.R, h.fmt, base + tile_i * h.tb, isA ? g.kcA : g.kcB, h.nb, grp, base + h.act, lane, red,
+                        h.amode);
         __syncwarp();
         if (P.diag && cw == 0 && lane == 0) dacc(P, 3, globaltimer_ns() - tc);
         if (lane == 0) {
@@ -1124,7 +1098,6 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     const int nrs = nU > 0 ? s_rbase[nU] : 0;
     const int nblk = I / 256, nunits = nrs * nblk;
     const float* pa = (const float*)(P.ws + P.L.m_pa);
-    float* hbuf = (float*)(P.ws + P.L.m_h);
     const unsigned int* ca = (const unsigned int*)(P.ws + P.L.m_ca);
     unsigned int* chc = (unsigned int*)(P.ws + P.L.m_ch);
     int u = 0, ready = -1, cur_n = 0;
@@ -1189,35 +1162,67 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         hv[4 * q + 3] = silu_m(a.w) * b.w;
       }
       const int fmt = s_ufmt[u];
-      if (act_mode(1, fmt) != kActInt) {
-        float4* dst = reinterpret_cast<float4*>(hbuf + (int64_t)rs * I + i0);
-        dst[0] = make_float4(hv[0], hv[1], hv[2], hv[3]);
-        dst[1] = make_float4(hv[4], hv[5], hv[6], hv[7]);
-      } else {
+      {
+        // f16 hi + lo of h 2^si, max |h| 2^si in [2^14, 2^15)
         uint32_t mx = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx = max(mx, __float_as_uint(hv[k]) & 0x7FFFFFFFu);
         mx = __reduce_max_sync(0xffffffffu, mx);
-        const int ex = (int)(mx >> 23);  // biased exponent of max |h| (0: all zero or subnormal)
-        const int si = ex == 0 ? 0 : min(max(13 - (ex - 127), -100), 100);
-        const int tq = fmt == BQE_FMT_TQ1;
+        const int ex = (int)(mx >> 23);
+        const int si = ex == 0 ? 0 : min(max(14 - (ex - 127), -100), 100);
         const int ck = blk / bpcB, kb = blk - ck * bpcB;
-        uint8_t* rec = P.ws + P.L.m_hr + ((size_t)rs * g.nchB + ck) * int_rec_bytes(1, g.kcB);
-        if (lane == 0) rec_put_scale(rec, tq, g.kcB, kb, ldexpf(1.0f, -si));
-        if (tq && lane < 16) rec_put_pad(rec, g.kcB, kb, lane);
-        int ph = 0, pl = 0;
+        uint8_t* rec = P.ws + P.L.m_hr + ((size_t)rs * g.nchB + ck) * hrec_stride(g.kcB);
+        const int flen = f16_len(fmt, g.kcB);
+        uint16_t* hdst = reinterpret_cast<uint16_t*>(rec);
+        uint16_t* ldst = reinterpret_cast<uint16_t*>(rec + 2 * flen + 64);
+        if (lane == 0) reinterpret_cast<float*>(rec + 4 * flen + 64)[kb] = ldexpf(1.0f, -si);
+        if (fmt == BQE_FMT_TQ1) {
+          // T order: h of the unit through shared memory, 9 positions per lane
+          float* sh = s_hunit;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float v = ldexpf(hv[k], si);
-          const int Xh = __float2int_rn(v);
-          const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
-          rec_put(rec, tq, g.kcB, kb, lane * 8 + k, Xh, Xl);
-          ph += Xh;
-          pl += Xl;
+          for (int k = 0; k < 8; ++k) sh[lane * 8 + k] = hv[k];
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 9; ++k) {
+            const int pos = lane + 32 * k, col = t16_col(pos);
+            const float v = col >= 0 ? ldexpf(sh[col], si) : 0.f;
+            const __half h0 = __float2half_rn(v);
+            hdst[kb * 288 + pos] = __half_as_ushort(h0);
+            ldst[kb * 288 + pos] = __half_as_ushort(__float2half_rn(v - __half2float(h0)));
+          }
+          __syncwarp();
+        } else {
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float v0 = ldexpf(hv[2 * k], si), v1 = ldexpf(hv[2 * k + 1], si);
+            const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
+            const __half l0 = __float2half_rn(v0 - __half2float(h0)), l1 = __float2half_rn(v1 - __half2float(h1));
+            hw[k] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+            lw[k] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+          }
+          if (fmt != BQE_FMT_MXFP4) {
+            // P order: in every 16 columns (lanes 2m, 2m + 1) position 2p holds
+            // column p and 2p + 1 column 8 + p: the even lane writes (c0, c8, ..,
+            // c3, c11), the odd one (c4, c12, .., c7, c15)
+            const bool odd = lane & 1;
+            auto p_order = [&](uint32_t& w0, uint32_t& w1, uint32_t& w2, uint32_t& w3) {
+              const uint32_t s0 = __shfl_xor_sync(0xffffffffu, odd ? w0 : w2, 1);
+              const uint32_t s1 = __shfl_xor_sync(0xffffffffu, odd ? w1 : w3, 1);
+              const uint32_t m0 = odd ? s0 : w0, m1 = odd ? s1 : w1;  // columns 0..3 (4..7) of the 16
+              const uint32_t n0 = odd ? w2 : s0, n1 = odd ? w3 : s1;  // columns 8..11 (12..15)
+              w0 = __byte_perm(m0, n0, 0x5410);
+              w1 = __byte_perm(m0, n0, 0x7632);
+              w2 = __byte_perm(m1, n1, 0x5410);
+              w3 = __byte_perm(m1, n1, 0x7632);
+            };
+            p_order(hw[0], hw[1], hw[2], hw[3]);
+            p_order(lw[0], lw[1], lw[2], lw[3]);
+          }
+          const int col = kb * 256 + lane * 8;
+          *reinterpret_cast<uint4*>(hdst + col) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(ldst + col) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
-        ph += __shfl_xor_sync(0xffffffffu, ph, 1);
-        pl += __shfl_xor_sync(0xffffffffu, pl, 1);
-        if ((lane & 1) == 0) rec_put_sums(rec, tq, g.kcB, kb, lane >> 1, ph, pl);
       }
       ++cur_n;
       __syncwarp();
@@ -1248,13 +1253,13 @@ static int moe_pb(const Geo& g) {
   return best;
 }
 
-// Largest byte size of one item (MXFP4 tiles are the largest of the formats).
+// Largest byte size of one item (MXFP4 tiles and T-order x rows are the
+// largest of the formats).
 static uint32_t moe_max_item(const Geo& g, int PB) {
   auto a128 = [](uint32_t v) { return (v + 127u) & ~127u; };
-  const uint32_t actA = (uint32_t)int_rec_bytes(0, g.kcA) > (uint32_t)g.kcA * 4 ? int_rec_bytes(0, g.kcA) : g.kcA * 4;
-  const uint32_t actA2 = int_rec_bytes(1, g.kcA) > actA ? int_rec_bytes(1, g.kcA) : actA;
-  const uint32_t A = a128(2 * tile_bytes(BQE_FMT_MXFP4, g.kcA)) + a128(g.M * actA2) + 2 * g.GA * g.M * 128;
-  const uint32_t actB = int_rec_bytes(1, g.kcB) > (uint32_t)g.kcB * 4 ? int_rec_bytes(1, g.kcB) : g.kcB * 4;
+  const uint32_t actA = (uint32_t)act_row_stride(kActF16, BQE_FMT_TQ1, g.kcA);
+  const uint32_t A = a128(2 * tile_bytes(BQE_FMT_MXFP4, g.kcA)) + a128(g.M * actA) + 2 * g.GA * g.M * 128;
+  const uint32_t actB = hrec_stride(g.kcB);
   const uint32_t B = a128(PB * tile_bytes(BQE_FMT_MXFP4, g.kcB)) + a128(g.M * actB) + PB * g.GB * g.M * 128;
   return A > B ? A : B;
 }
@@ -1263,15 +1268,15 @@ int launch_moe(const MoeParams& P0, int grid, cudaStream_t st) {
   MoeParams P = P0;
   const Geo& g = P.g;
   if (g.E > kMaxEM || g.E > 4 * grid || g.H / 4 / 128 > 16 || g.H % 512 || g.I % 256 || g.K > kMaxTopK ||
-      g.U > kMaxU || 2 * g.nchA > 24 || (uint64_t)g.M * (g.K + 1) * g.nchB * int_rec_bytes(1, g.kcB) >= (1ull << 32))
+      g.U > kMaxU || 2 * g.nchA > 24 || (uint64_t)g.M * (g.K + 1) * g.nchB * hrec_stride(g.kcB) >= (1ull << 32))
     return BQE_EUNSUPPORTED;
   P.PB = moe_pb(g);
   static int limit_set[2][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BQE_ECUDA;
   const int rc = g.M == 1 ? 0 : 1;
-  // one-row calls carry only the one-row inner loops; others take rows two at
-  // a time (four at a time would spill under this kernel's register budget)
+  // one-row calls run an instance where M is the constant 1 (one B column
+  // group per MMA, no wide W2 items)
   void (*kfn)(MoeParams) = rc ? k_moe<2> : k_moe<1>;
   int optin = 0;
   cudaFuncAttributes fa;

@@ -44,7 +44,6 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
   if (P.diag && threadIdx.x == 0) dbg_span(P.ws, P.L.dbg, 2, false);
   int32_t* err = (int32_t*)(P.ws + P.L.err);
   float* z = (float*)(P.ws + P.L.z);
-  float* xf = (float*)(P.ws + P.L.xf);
   extern __shared__ __align__(16) uint16_t xs[];  // M x H bf16 layer input
 
   __shared__ float inv_rms[kMaxM];
@@ -158,8 +157,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
               (unsigned long long)(clock64() - t_start));
     dbg_span(P.ws, P.L.dbg, 2, true);
   }
-  // ---- arrival: the last CTA selects, every other one takes a share of the
-  // side job (the copies of x the expert kernels read), by arrival rank ------
+  // ---- arrival: the last CTA selects ----------------------------------------
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -169,78 +167,6 @@ __global__ void __launch_bounds__(kRouteThreads) k_route(RouteParams P) {
   __syncthreads();
   const int rank = s_last;
   const bool last = rank == (int)gridDim.x - 1;
-  __shared__ int s_emax[kMaxM];
-  if (!last || gridDim.x == 1) {
-    const int nside = gridDim.x == 1 ? 1 : (int)gridDim.x - 1;
-    const int srank = gridDim.x == 1 ? 0 : rank;
-  // ---- side job: fp32 and scaled-f16 copies of the layer input --------------
-  // f16(x * 2^s) is exact for a bf16 x as long as x * 2^s is a normal f16;
-  // s puts the row's largest |x| in [2^14, 2^15).  Every CTA derives the same s.
-  if (tid < M) s_emax[tid] = -1000;
-  __syncthreads();
-  for (int m = 0; m < M; ++m) {
-    uint32_t mx = 0;
-    for (int k = tid; k < H; k += kRouteThreads) mx = max(mx, (uint32_t)(xs[m * H + k] & 0x7FFFu));
-    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0 && mx) atomicMax(&s_emax[m], (int)(mx >> 7) - 127);  // floor(log2 max|x|)
-  }
-  __syncthreads();
-  {
-    uint16_t* xh = (uint16_t*)(P.ws + P.L.xh);
-    const int n = M * H;
-    const int per = (n + nside - 1) / nside;
-    const int lo = per * srank, hi = min(n, lo + per);
-    for (int i = lo + tid; i < hi; i += kRouteThreads) {
-      const float v = bf16_to_f32(xs[i]);
-      const int m = i / H;
-      const int sh = s_emax[m] == -1000 ? 0 : 14 - s_emax[m];
-      xf[i] = v;
-      xh[i] = __half_as_ushort(__float2half_rn(ldexpf(v, sh)));
-      if (P.t_out) P.t_out[i] = xs[i];
-    }
-    if (srank == 0 && tid < M) {
-      const int sh = s_emax[tid] == -1000 ? 0 : 14 - s_emax[tid];
-      ((float*)(P.ws + P.L.xsc))[tid] = ldexpf(1.0f, -sh);
-    }
-  }
-  {
-    // x as X_hi + X_lo / 128: X_hi = rint(x 2^si) (int16, max |x| 2^si in
-    // [2^13, 2^14)), X_lo = rint((x 2^si - X_hi) 128) (int8, |X_lo| <= 64), in
-    // the two orders the integer GEMV paths read, and the sums of X_hi and X_lo
-    // over every 16 columns.  One CTA per 256-column block, one column per
-    // thread, so the extra work is spread thinly over the side-job CTAs.
-    const int nbr = H / 256, nblk = M * nbr, bpc = g.kcA / 256;
-    for (int blk = srank; blk < nblk; blk += nside) {
-      const int m = blk / nbr, bj = blk % nbr;
-      const int c = bj / bpc, k = bj % bpc;  // K chunk of the block and its place in the chunk
-      uint8_t* rq = P.ws + P.L.xrq + ((size_t)m * g.nchA + c) * int_rec_bytes(0, g.kcA);
-      uint8_t* rt = P.ws + P.L.xrt + ((size_t)m * g.nchA + c) * int_rec_bytes(1, g.kcA);
-      const int si = s_emax[m] == -1000 ? 0 : 13 - s_emax[m];
-      const int j = tid;  // column within the block
-      const float v = ldexpf(bf16_to_f32(xs[m * H + bj * 256 + j]), si);
-      const int Xh = __float2int_rn(v);
-      const int Xl = __float2int_rn((v - (float)Xh) * 128.0f);
-      rec_put(rq, 0, g.kcA, k, j, Xh, Xl);
-      rec_put(rt, 1, g.kcA, k, j, Xh, Xl);
-      if (tid < 16) rec_put_pad(rt, g.kcA, k, tid);
-      int ph = Xh, pl = Xl;
-#pragma unroll
-      for (int o = 8; o; o >>= 1) {
-        ph += __shfl_xor_sync(0xffffffffu, ph, o);
-        pl += __shfl_xor_sync(0xffffffffu, pl, o);
-      }
-      if ((lane & 15) == 0) {
-        rec_put_sums(rq, 0, g.kcA, k, tid >> 4, ph, pl);
-        rec_put_sums(rt, 1, g.kcA, k, tid >> 4, ph, pl);
-      }
-      if (tid == 0) {  // 2^-si of this block
-        rec_put_scale(rq, 0, g.kcA, k, ldexpf(1.0f, -si));
-        rec_put_scale(rt, 1, g.kcA, k, ldexpf(1.0f, -si));
-      }
-    }
-  }
-
-  }
   if (!last) return;
   __threadfence();
   auto stamp = [&](int k) {

@@ -59,11 +59,12 @@ def _check_layer(W, dev, M, xi):
     return check_out(out, oref, what="full M=%d" % M)
 
 
-def test_fp4_layer_m1(dev):
+@pytest.mark.parametrize("M", [1, 6, 8])
+def test_fp4_layer(dev, M):
     from synth import workloads as WL
-    W = WL.fp4_layer(dev, m=1, n_x=3)
-    for xi in range(2):
-        _check_layer(W, dev, 1, xi)
+    W = WL.fp4_layer(dev, m=M, n_x=3)
+    for xi in range(2 if M == 1 else 1):
+        _check_layer(W, dev, M, xi)
 
 
 @pytest.mark.parametrize("M", [1, 6, 8])
