@@ -1030,8 +1030,44 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       cur_n = 0;
       prev_n = 0;
     };
+    // The reducer's shared-memory reads wait behind the compute warps' (a few
+    // hundred cycles each), so the loop keeps them off its critical path: the
+    // next item's header is read as soon as its copies have landed (a
+    // non-blocking test of its full barrier), the per-expert values (first
+    // row slot, rows, scales, mixing weights) only when the expert changes,
+    // and all partials of a row are loaded before any is added.
+    ItemHdr hn;
+    bool have = false;
+    int eu = -1, eph = -1, erb = 0;
+    int erow[kMaxM];
+    float esc[kMaxM];
     for (int i = 0; i < nmine; ++i) {
       const uint64_t tr = P.diag ? globaltimer_ns() : 0;
+      if (!have) {  // the header of item i is readable once its copies have landed
+        if (!__all_sync(0xffffffffu, mwait(&full[i % kNQ], (i / kNQ) & 1, P.limit_ns, err)) || s_abort) {
+          if (lane == 0) {
+            set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+            s_abort = 1;
+          }
+          break;
+        }
+        hn = hdr[i % kNQ];
+      }
+      const ItemHdr h = hn;
+      const int u = h.u, R = RC == 1 ? 1 : h.R;
+      if (u != eu || h.phase != eph) {  // this expert's row slots, rows and scales
+        eu = u;
+        eph = h.phase;
+        erb = s_rbase[u];
+#pragma unroll
+        for (int r = 0; r < kMaxM; ++r) {
+          if (r < R) {
+            const int row = u == 0 ? r : s_urows[u * kMaxM + r];
+            erow[r] = row;
+            esc[r] = h.phase == 0 ? s_xsc[row] : s_rsw[erb + r];
+          }
+        }
+      }
       const bool okc = __all_sync(0xffffffffu, mwait(&cons[i % kNQ], (i / kNQ) & 1, P.limit_ns, err));
       if (P.diag && lane == 0) dacc(P, 4, globaltimer_ns() - tr);
       if (!okc || s_abort) {
@@ -1041,9 +1077,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         }
         break;
       }
-      const ItemHdr h = hdr[i % kNQ];
+      // the next item's header, if it has landed already
+      have = i + 1 < nmine && mbar_test_wait(&full[(i + 1) % kNQ], ((i + 1) / kNQ) & 1);
+      have = __all_sync(0xffffffffu, have);
+      if (have) hn = hdr[(i + 1) % kNQ];
       const float* red = reinterpret_cast<const float*>(ring + h.off + h.red);
-      const int u = h.u, R = h.R, rb = s_rbase[u];
       if (h.phase == 0) {
         if (u != cur_u) {
           if (prev_n > 0) release_a();  // two experts pending: publish both
@@ -1053,17 +1091,19 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           cur_n = 0;
         }
         // chunk partials of g and u for this panel (the f16 input's scale removed: exact power of two)
-        for (int r = 0; r < R; ++r) {
-          const int row = u == 0 ? r : s_urows[u * kMaxM + r];
-          const float unscale = h.amode == kActF16 ? s_xsc[row] : 1.0f;
-          float a0 = 0.f, a1 = 0.f;
-          for (int gi = 0; gi < g.GA; ++gi) {
-            a0 += red[(gi * R + r) * 32 + lane];
-            a1 += red[((g.GA + gi) * R + r) * 32 + lane];
+#pragma unroll
+        for (int r = 0; r < (RC == 1 ? 1 : kMaxM); ++r) {
+          if (r >= R) break;
+          float v0[4], v1[4];
+#pragma unroll
+          for (int gi = 0; gi < 4; ++gi) {
+            v0[gi] = gi < g.GA ? red[(gi * R + r) * 32 + lane] : 0.f;
+            v1[gi] = gi < g.GA ? red[((g.GA + gi) * R + r) * 32 + lane] : 0.f;
           }
-          const int64_t base = ((((int64_t)(rb + r) * g.npanA + h.p) * g.nchA + h.c) * 2) * 32;
-          pa[base + lane] = a0 * unscale;
-          pa[base + 32 + lane] = a1 * unscale;
+          const float a0 = ((v0[0] + v0[1]) + v0[2]) + v0[3], a1 = ((v1[0] + v1[1]) + v1[2]) + v1[3];
+          const int64_t base = ((((int64_t)(erb + r) * g.npanA + h.p) * g.nchA + h.c) * 2) * 32;
+          pa[base + lane] = a0 * esc[r];
+          pa[base + 32 + lane] = a1 * esc[r];
         }
         ++cur_n;
         __syncwarp();
@@ -1071,11 +1111,14 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       } else {
         for (int pi = 0; pi < P.PB; ++pi) {
           const int n = (h.p * P.PB + pi) * 32 + lane;
-          for (int r = 0; r < R; ++r) {
-            float y = 0.f;
-            for (int gi = 0; gi < g.GB; ++gi) y += red[((pi * g.GB + gi) * R + r) * 32 + lane];
-            const int row = u == 0 ? r : s_urows[u * kMaxM + r];
-            red_add_f32(P.out + (int64_t)row * H + n, s_rsw[rb + r] * y);
+#pragma unroll
+          for (int r = 0; r < (RC == 1 ? 1 : kMaxM); ++r) {
+            if (r >= R) break;
+            float v[4];
+#pragma unroll
+            for (int gi = 0; gi < 4; ++gi) v[gi] = gi < g.GB ? red[((pi * g.GB + gi) * R + r) * 32 + lane] : 0.f;
+            const float y = ((v[0] + v[1]) + v[2]) + v[3];
+            red_add_f32(P.out + (int64_t)erow[r] * H + n, esc[r] * y);
           }
         }
       }
