@@ -1288,10 +1288,11 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
 }
 
 // W2 output panels per item: the largest count that divides the panels and
-// keeps the item at <= 8 compute tasks.
+// keeps the item at <= 16 compute tasks (one per compute warp).  Fewer, larger
+// W2 items cost less per byte in the producers and the reducer.
 static int moe_pb(const Geo& g) {
   int best = 1;
-  for (int pb = 1; pb * g.GB <= 8; ++pb)
+  for (int pb = 1; pb * g.GB <= kCW; ++pb)
     if (g.npanB % pb == 0) best = pb;
   return best;
 }
