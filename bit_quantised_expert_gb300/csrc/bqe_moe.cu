@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
   const float* s_rw = reinterpret_cast<const float*>(ring + P.rt_off);  // this CTA's router rows (startup only)
 
   __shared__ ItemHdr hdr[kNQ];
-  __shared__ __align__(8) uint64_t full[kNQ], cons[kNQ], freed[kNQ], route_bar, rbar;
+  __shared__ __align__(8) uint64_t full[kNQ], cons[kNQ], freed[kNQ], route_bar, rbar, lbar;
   __shared__ float s_rsw[kMaxM * (kMaxTopK + 1)];  // mixing weight of each row slot (shared expert: 1)
   __shared__ int s_rbase[kMaxU + 1];   // first row slot of each work-list expert
   __shared__ int s_rs[kMaxM][kMaxTopK];  // row slot of (row m, choice j)
@@ -256,6 +256,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     }
     mbar_init(&route_bar, 1);
     mbar_init(&rbar, 1);
+    mbar_init(&lbar, 1);
     s_abort = 0;
     for (int q = 0; q < kNP; ++q) s_issued[q] = 0;
     s_turn = 0;
@@ -421,6 +422,15 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         while (s_npre < 0 && globaltimer_ns() - t0 < P.limit_ns) __nanosleep(32);
       }
       const int npre = max(0, (int)s_npre);
+      // ---- the pre-issued items' x rows: every CTA's staged slices of x are
+      // published once all logits are in, well before the routing is known
+      // (copied on a failed wait too: the addresses are valid, the stage drains)
+      if (!mwait(&lbar, 0, P.limit_ns, err)) ok = false;
+      fence_proxy_async_global();  // the staged inputs of every CTA are read by bulk copies below
+      for (int i = pp; i < npre; i += kNP) {
+        issue(i, sh, hdr[i % kNQ].p, hdr[i % kNQ].c, false, true, true);
+        issued = i;
+      }
       // ---- the routing (work list and item templates built by the compute warps)
       if (!mwait(&route_bar, 0, P.limit_ns, err)) {
         set_error(err, BQE_ETIMEOUT, kErrWaitFull);
@@ -428,11 +438,6 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         ok = false;
       }
       const int nU = s_nu;
-      fence_proxy_async_global();  // the staged inputs of every CTA are read by bulk copies below
-      for (int i = pp; i < npre; i += kNP) {
-        issue(i, sh, hdr[i % kNQ].p, hdr[i % kNQ].c, false, true, true);
-        issued = i;
-      }
       const int nTot = nU * (nAper + nBper), nA = nU * nAper;
       long long hwait_max = 0;
       int dropped = -1;
@@ -731,6 +736,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       }
       if (P.diag) dacc(P, 2, globaltimer_ns() - t_cta0, 0);
       rstamp(P, 0, t_cta0);
+      mbar_arrive(&lbar);  // the producers may copy staged rows of other CTAs
     }
     named_bar_sync(1, NCT);
     // ---- the routing: per-row selection (warp m takes row m), then warp 0
@@ -760,12 +766,15 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         }
         __syncwarp();
         if (ct == 0) rstamp(P, 1, t_cta0);
-        uint64_t last = ~0ull;
-        for (int j = 0; j < K; ++j) {
-          int best;
-          if (forced) {
-            best = s_fidx[m][j];
-          } else {
+        // lane j keeps round j's winner; the bookkeeping (choice, logit, the
+        // expert's row mask and first choice) is done after the rounds, by
+        // lanes 0 .. K-1 at once, so no round waits on shared memory
+        int mine = 0;
+        if (forced) {
+          if (lane < K) mine = s_fidx[m][lane];
+        } else {
+          uint64_t last = ~0ull;
+          for (int j = 0; j < K; ++j) {
             uint64_t t[QN / 2];
 #pragma unroll
             for (int q = 0; q < QN / 2; ++q) {
@@ -780,24 +789,23 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
             const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(t[0] >> 32));
             const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(t[0] >> 32) == hi ? (uint32_t)t[0] : 0u);
             last = ((uint64_t)hi << 32) | lo;
-            best = last ? (int)~lo : 0;
+            if (lane == j) mine = last ? (int)~lo : 0;
           }
-          if (lane == 0) {
-            s_idx[m][j] = best;
-            s_zsel[m][j] = s_z[m * E + best];
-            atomicOr(&s_mask[best], 1u << m);
-            atomicMin(&s_first[best], m * K + j);
-          }
+        }
+        float zz = 0.f;
+        if (lane < K) {
+          s_idx[m][lane] = mine;
+          zz = s_z[m * E + mine];
+          s_zsel[m][lane] = zz;
+          atomicOr(&s_mask[mine], 1u << m);
+          atomicMin(&s_first[mine], m * K + lane);
         }
         __syncwarp();
         if (ct == 0) rstamp(P, 2, t_cta0);
         // w_j = s_j / sum s as exp(log s_j - max log s) / sum exp(...): finite
         // even when every selected sigmoid underflows in fp32
         float ls = -INFINITY;
-        if (lane < K) {
-          const float zz = s_zsel[m][lane];
-          ls = zz < 0.f ? zz - log1pf(expf(zz)) : -log1pf(expf(-zz));
-        }
+        if (lane < K) ls = zz < 0.f ? zz - log1pf(expf(zz)) : -log1pf(expf(-zz));
         float mx = ls;
         for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         const float ev = lane < K ? expf(ls - mx) : 0.f;
@@ -807,7 +815,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           const float w = ev / tot;
           s_cw[m][lane] = w;
           if (cta == 0) {
-            if (P.topk_idx) P.topk_idx[m * K + lane] = s_idx[m][lane];
+            if (P.topk_idx) P.topk_idx[m * K + lane] = mine;
             if (P.topk_w) P.topk_w[m * K + lane] = w;
           }
         }
