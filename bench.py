@@ -68,7 +68,7 @@ PREFILL_METRIC = "MoE layer prefill: tokens/s and expert-GEMM TFLOP/s at T=8192 
 # reports null until a new capture is taken.
 KERNEL_SOURCES = ("bit_quantised_expert_gb300/csrc/bqe_moe.cu", "bit_quantised_expert_gb300/csrc/bqe_gemv.cuh",
                   "bit_quantised_expert_gb300/csrc/bqe_internal.cuh")
-TRAFFIC_FP4_M1 = dict(sha256="efcd8201c7df6238905c51ae06641d091e2d0dbb8844330cf6a0e677bcd80d32", bytes=142543616)
+TRAFFIC_FP4_M1 = dict(sha256="912a641f2fc8acdc80010d22b25f3ee9514676432548d7e9defb44e90478bb83", bytes=142836224)
 
 
 def kernel_digest() -> str:
