@@ -87,6 +87,8 @@ SIGNATURES = {
     "bqe_prefill_diag_offset": (_U64, [_DESC, _I32]),
     "bqe_set_diag": (None, [_I32]),
     "bqe_diag_offset": (_U64, [_DESC, _I32]),
+    "bqe_assign_formats": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, _I32, ctypes.c_double, _P, _U64, _P, _P, _P,
+                                          _P]),
 }
 
 for _name, (_res, _args) in SIGNATURES.items():
@@ -248,6 +250,29 @@ def bqe_moe_step(d, n_layers, M, resid, router_w, sel_bias, pool, slot_tables, f
     _ok(lib.bqe_moe_step(ctypes.byref(d), n_layers, M, ptr(resid), ptr(router_w), ptr(sel_bias), ctypes.byref(pool),
                          ptr(slot_tables), ptr(forced_idx), ptr(t_out), ptr(ws), ws_bytes, stream_ptr(stream)),
         "bqe_moe_step")
+
+
+def bqe_assign_formats(err, energy, layer_weight, heldout_tokens, min_tokens: int, tq1_cap_frac: float,
+                       fmt_bytes, budget: int):
+    """Host call; err (L, E, 3) float64, energy / layer_weight (L,) float64,
+    heldout_tokens (L, E) int32 or None, fmt_bytes (3,) uint64.  Returns
+    (formats (L, E) int32, lambda, bytes, cost); raises BqeError on a bad
+    argument or a budget below what the guard rails allow."""
+    import numpy as np
+    err = np.ascontiguousarray(err, dtype=np.float64)
+    L, E = int(err.shape[0]), int(err.shape[1])
+    energy = np.ascontiguousarray(energy, dtype=np.float64)
+    layer_weight = np.ascontiguousarray(layer_weight, dtype=np.float64)
+    tok = None if heldout_tokens is None else np.ascontiguousarray(heldout_tokens, dtype=np.int32)
+    fb = np.ascontiguousarray(fmt_bytes, dtype=np.uint64)
+    out = np.zeros((L, E), dtype=np.int32)
+    lam = ctypes.c_double()
+    nbytes = ctypes.c_uint64()
+    cost = ctypes.c_double()
+    _ok(lib.bqe_assign_formats(L, E, ptr(err), ptr(energy), ptr(layer_weight), ptr(tok), int(min_tokens),
+                               float(tq1_cap_frac), ptr(fb), int(budget), ptr(out), ctypes.byref(lam),
+                               ctypes.byref(nbytes), ctypes.byref(cost)), "bqe_assign_formats")
+    return out, lam.value, nbytes.value, cost.value
 
 
 def bqe_check(ws, stream=None) -> tuple[int, int]:

@@ -302,6 +302,35 @@ int bqe_moe_layer_forward_noalloc(const bqe_layer_desc* d, int32_t M, const uint
                                   int32_t* topk_idx, float* topk_w, int32_t* status_out,
                                   void* stream);
 
+/* Byte-budgeted choice of each routed expert's format (host only; no GPU
+ * work).  Strata 4090 post, section 5, first paragraph: ternary (TQ1),
+ * Q2_0 or Q3_K per expert under a byte budget (all-Q2_0 bytes makes the
+ * mix budget-neutral), by a Lagrangian relaxation with a bisection on the
+ * multiplier and a greedy pass over the bytes left; an expert's cost for a
+ * format is layer_weight[l] * err / energy[l] (the post counts the first
+ * two and last three layers twice); at most floor(tq1_cap_frac * n_experts)
+ * ternary experts per layer (the post: half); an expert with fewer than
+ * min_tokens held-out tokens stays Q2_0 (the post: 8).
+ *   - err: host, n_layers x n_experts x 3 doubles (errors of TQ1, Q2_0,
+ *     Q3_K), >= 0; energy: host, n_layers doubles > 0; layer_weight: host,
+ *     n_layers doubles >= 0; heldout_tokens: host, n_layers x n_experts or
+ *     NULL (nothing locked); fmt_bytes: host, the bytes of one expert in
+ *     TQ1, Q2_0, Q3_K (bqe_expert_bytes), strictly increasing.
+ *   - fmt_out: host, n_layers x n_experts BQE_FMT_* codes; lambda_out,
+ *     bytes_out, cost_out (host, each may be NULL): the multiplier, the
+ *     bytes and the summed cost of the result.
+ *   - Ties: fewer bytes first; the layer's ternary experts beyond the cap
+ *     are those losing least by giving it up (then higher expert index);
+ *     100 halvings of the multiplier's range; greedy upgrades by largest
+ *     cost decrease per byte (then lower layer, expert, format).
+ *   - BQE_EINVAL on a bad argument or a budget below what the guard rails
+ *     allow (fmt_out untouched then).  Deterministic: IEEE double in a fixed
+ *     order, the same result on every host. */
+int bqe_assign_formats(int32_t n_layers, int32_t n_experts, const double* err, const double* energy,
+                       const double* layer_weight, const int32_t* heldout_tokens, int32_t min_tokens,
+                       double tq1_cap_frac, const uint64_t* fmt_bytes, uint64_t budget, int32_t* fmt_out,
+                       double* lambda_out, uint64_t* bytes_out, double* cost_out);
+
 /* Synchronise `stream` and report the device error word of the last
  * bqe_moe_layer_forward_noalloc call on the current device, then clear it
  * (as bqe_check does for a caller's workspace).  BQE_OK if no call ran. */

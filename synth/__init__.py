@@ -155,6 +155,30 @@ def assign_formats(rng, n: int, shares=MIX_SHARES) -> np.ndarray:
     return fm
 
 
+def format_error_proxy(rng, n_layers: int, n_experts: int):
+    """Synthetic inputs of the per-expert format assignment (the real ones
+    are held-out errors of quantised experts on calibration data, which is
+    not here).  Returns err (L, E, 3) for ternary / Q2_0 / Q3_K, the routed
+    output energy of each layer (L,) and held-out token counts (L, E):
+      energy_l     ~ lognormal(0, 0.5);
+      sensitivity  ~ lognormal(0, 0.7) per expert, x4 for every expert of one
+                     layer (three quarters of the way down: one layer much
+                     more sensitive than the rest, as the Strata 4090 post
+                     reports for one layer);
+      err[l,e,f]   = energy_l * sensitivity * 4^-bpw_f * lognormal(0, 0.15),
+                     bpw = 1.75 / 2.25 / 3.4375 (a round-to-nearest error
+                     that falls 4x per bit, with per-format scatter);
+      tokens       ~ Poisson(lognormal(3, 1)) (a few rarely routed experts)."""
+    energy = rng.lognormal(0.0, 0.5, size=n_layers)
+    sens = rng.lognormal(0.0, 0.7, size=(n_layers, n_experts))
+    sens[(3 * n_layers) // 4] *= 4.0
+    bpw = np.array([1.75, 2.25, 3.4375])
+    jitter = rng.lognormal(0.0, 0.15, size=(n_layers, n_experts, 3))
+    err = energy[:, None, None] * sens[:, :, None] * (4.0 ** -bpw)[None, None, :] * jitter
+    tokens = rng.poisson(rng.lognormal(3.0, 1.0, size=(n_layers, n_experts))).astype(np.int32)
+    return err, energy, tokens
+
+
 def zipf_probs(n: int, s: float) -> np.ndarray:
     p = 1.0 / np.arange(1, n + 1, dtype=np.float64) ** s
     return p / p.sum()
