@@ -38,6 +38,11 @@ class bqe_stats(ctypes.Structure):
                 ("row_uses", ctypes.c_int32), ("expert_bytes", ctypes.c_uint64), ("router_bytes", ctypes.c_uint64)]
 
 
+class bqe_cache_stats(ctypes.Structure):
+    _fields_ = [("requests", ctypes.c_uint64), ("hits", ctypes.c_uint64), ("misses", ctypes.c_uint64),
+                ("evictions", ctypes.c_uint64), ("bytes_uploaded", ctypes.c_uint64)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError("libbqe.so is not built (%s); run bit_quantised_expert_gb300.buildlib.build() "
@@ -89,6 +94,13 @@ SIGNATURES = {
     "bqe_diag_offset": (_U64, [_DESC, _I32]),
     "bqe_assign_formats": (ctypes.c_int, [_I32, _I32, _P, _P, _P, _P, _I32, ctypes.c_double, _P, _U64, _P, _P, _P,
                                           _P]),
+    "bqe_cache_create": (ctypes.c_int, [_DESC, _I32, _P, _POOL, _P, _I32, _I32, _P, ctypes.POINTER(_P)]),
+    "bqe_cache_destroy": (None, [_P]),
+    "bqe_cache_plan": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
+    "bqe_cache_fetch": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _U64, _P, _P, _P, _P]),
+    "bqe_cache_done": (ctypes.c_int, [_P, ctypes.c_int64, _P]),
+    "bqe_cache_ready": (ctypes.c_int, [_P, ctypes.c_int64, _P]),
+    "bqe_cache_stats_get": (ctypes.c_int, [_P, ctypes.POINTER(bqe_cache_stats)]),
 }
 
 for _name, (_res, _args) in SIGNATURES.items():
@@ -273,6 +285,59 @@ def bqe_assign_formats(err, energy, layer_weight, heldout_tokens, min_tokens: in
                                float(tq1_cap_frac), ptr(fb), int(budget), ptr(out), ctypes.byref(lam),
                                ctypes.byref(nbytes), ctypes.byref(cost)), "bqe_assign_formats")
     return out, lam.value, nbytes.value, cost.value
+
+
+def bqe_cache_create(d, n_layers: int, expert_fmt, pool: bqe_pool, pool_slot_fmt, first_slot: int, n_slots: int,
+                     slot_tables):
+    """expert_fmt (L, E) and pool_slot_fmt (pool slots,) host int32; slot_tables
+    a device tensor of L x (E + 1) int32.  Returns the cache handle (int)."""
+    import numpy as np
+    ef = np.ascontiguousarray(expert_fmt, dtype=np.int32)
+    pf = np.ascontiguousarray(pool_slot_fmt, dtype=np.int32)
+    h = _P()
+    _ok(lib.bqe_cache_create(ctypes.byref(d), int(n_layers), ptr(ef), ctypes.byref(pool), ptr(pf), int(first_slot),
+                             int(n_slots), ptr(slot_tables), ctypes.byref(h)), "bqe_cache_create")
+    return h.value
+
+
+def bqe_cache_destroy(h) -> None:
+    lib.bqe_cache_destroy(h)
+
+
+def bqe_cache_plan(h, layer: int, experts):
+    import numpy as np
+    ex = np.ascontiguousarray(experts, dtype=np.int32)
+    n = int(ex.size)
+    slots, miss, ev = (np.zeros(max(n, 1), np.int32) for _ in range(3))
+    _ok(lib.bqe_cache_plan(h, int(layer), n, ptr(ex), ptr(slots), ptr(miss), ptr(ev)), "bqe_cache_plan")
+    return slots[:n], miss[:n], ev[:n]
+
+
+def bqe_cache_fetch(h, layer: int, experts, host_src, staging, upload_stream, compute_stream):
+    """host_src: a ctypes array of L x E host pointers (pinned canonical expert
+    bytes); staging a device tensor.  Returns (plan number, misses)."""
+    import numpy as np
+    ex = np.ascontiguousarray(experts, dtype=np.int32)
+    nm = _I32()
+    pl = ctypes.c_int64()
+    _ok(lib.bqe_cache_fetch(h, int(layer), int(ex.size), ptr(ex), ctypes.cast(host_src, _P), ptr(staging),
+                            staging.numel() * staging.element_size(), stream_ptr(upload_stream),
+                            stream_ptr(compute_stream), ctypes.byref(pl), ctypes.byref(nm)), "bqe_cache_fetch")
+    return pl.value, nm.value
+
+
+def bqe_cache_ready(h, plan: int, compute_stream=None) -> None:
+    _ok(lib.bqe_cache_ready(h, int(plan), stream_ptr(compute_stream)), "bqe_cache_ready")
+
+
+def bqe_cache_done(h, plan: int, compute_stream=None) -> None:
+    _ok(lib.bqe_cache_done(h, int(plan), stream_ptr(compute_stream)), "bqe_cache_done")
+
+
+def bqe_cache_stats_get(h) -> dict:
+    st = bqe_cache_stats()
+    _ok(lib.bqe_cache_stats_get(h, ctypes.byref(st)), "bqe_cache_stats_get")
+    return {k: getattr(st, k) for k, _ in st._fields_}
 
 
 def bqe_check(ws, stream=None) -> tuple[int, int]:

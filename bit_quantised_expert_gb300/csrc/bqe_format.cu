@@ -179,6 +179,13 @@ static bool pool_offsets(const bqe_layer_desc* d, int32_t n, const int32_t* fmt,
   return true;
 }
 
+namespace bqe {
+bool pool_slot_offsets(const bqe_layer_desc* d, int32_t n, const int32_t* fmt, std::vector<uint64_t>& off) {
+  uint64_t sb = 0;
+  return pool_offsets(d, n, fmt, off, sb);
+}
+}  // namespace bqe
+
 extern "C" uint64_t bqe_pool_bytes(const bqe_layer_desc* d, int32_t n_slots, const int32_t* slot_fmt) {
   if (!shape_ok(d) || n_slots <= 0 || !slot_fmt) return 0;
   std::vector<uint64_t> off;

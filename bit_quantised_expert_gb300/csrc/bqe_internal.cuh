@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "../../include/bqe.h"
 
 namespace bqe {
@@ -247,6 +249,9 @@ int moe_forward(const bqe_layer_desc* d, int32_t M, const uint16_t* x, const flo
                 bool allow_diag);
 
 uint32_t layer_smem_bytes(const Geo& g, int* nstages_out, int* nw_out, uint32_t* slot_out);
+// Offsets (from the first slot) of the slots of a pool laid out by
+// bqe_pool_init for the formats fmt[0..n-1] (bqe_format.cu); false on a bad format.
+bool pool_slot_offsets(const bqe_layer_desc* d, int32_t n, const int32_t* fmt, std::vector<uint64_t>& off);
 
 // Launchers (one per translation unit that owns the kernel).
 int launch_route(const RouteParams& P, cudaStream_t st, bool pdl);

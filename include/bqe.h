@@ -331,6 +331,75 @@ int bqe_assign_formats(int32_t n_layers, int32_t n_experts, const double* err, c
                        double tq1_cap_frac, const uint64_t* fmt_bytes, uint64_t budget, int32_t* fmt_out,
                        double* lambda_out, uint64_t* bytes_out, double* cost_out);
 
+/* ---- expert cache ----------------------------------------------------------
+ * Least-recently-used replacement of expert slots when the pool holds fewer
+ * slots than there are experts (Strata 4090 post, section 5, second
+ * paragraph: an LRU set of VRAM expert slots in front of pinned host memory,
+ * fetched one layer ahead; field report, section 3B: 4288 expert slots and a
+ * per-step account of where each expert came from).  The cache manages pool
+ * slots first_slot .. first_slot + n_slots - 1 (the shared experts and any
+ * pinned ones live outside that range) and rewrites the routed entries of
+ * the per-layer slot tables (device, n_layers x (n_experts + 1), the layout
+ * bqe_moe_step reads; entry -1 = not resident; the caller fills the tables'
+ * initial contents and the shared-expert entries).
+ *   Plan c (c = 0, 1, ...): a requested expert already resident is a hit; a
+ * missing one takes, among the managed slots of its format that neither this
+ * plan nor the previous one uses, the one used longest ago (never-used
+ * first, then the lower slot), evicting what it held.  No such slot:
+ * BQE_ENOSPC and nothing changes. */
+typedef struct bqe_cache bqe_cache;  /* opaque, host */
+
+typedef struct {
+  uint64_t requests, hits, misses, evictions, bytes_uploaded;
+} bqe_cache_stats;
+
+/* Create a cache (host object; no GPU work).  expert_fmt: host, n_layers x
+ * d->n_experts formats; pool_slot_fmt: host, pool->n_slots formats (as given
+ * to bqe_pool_init); slot_tables: device (not read here).  The caller keeps
+ * the pool and the tables alive while the cache is used. */
+int bqe_cache_create(const bqe_layer_desc* d, int32_t n_layers, const int32_t* expert_fmt,
+                     const bqe_pool* pool, const int32_t* pool_slot_fmt, int32_t first_slot,
+                     int32_t n_slots, int32_t* slot_tables, bqe_cache** out);
+void bqe_cache_destroy(bqe_cache* c);
+
+/* Host only: the slot choice for `n` requested experts of `layer` (host ids;
+ * duplicates allowed).  slots_out: pool slot ids; miss_out: 1 for an expert
+ * that was not resident; evicted_out: the key layer * n_experts + expert it
+ * displaced, or -1.  Counts the request in the statistics. */
+int bqe_cache_plan(bqe_cache* c, int32_t layer, int32_t n, const int32_t* experts, int32_t* slots_out,
+                   int32_t* miss_out, int32_t* evicted_out);
+
+/* Plan as above, then make the experts resident: for each miss, copy its
+ * canonical bytes (host_src[layer * n_experts + expert], pinned host memory,
+ * bqe_expert_bytes of its format) to `staging` and rewrite them into the
+ * slot (bqe_pool_pack_slot), then update the tables (the new entries and -1
+ * for the evicted experts), all on upload_stream.  Before the first
+ * overwrite, upload_stream waits for the kernels of plan c - 2 (recorded by
+ * bqe_cache_done; if that was not recorded, for everything enqueued on
+ * compute_stream), the last that may have read a victim slot, so the uploads
+ * of one layer may run while the previous layer computes.  The layer's own
+ * kernels must be ordered after them with bqe_cache_ready.  staging: device, 256-byte aligned, at least
+ * (the largest expert of any format, rounded up to 256) + 16 n bytes.
+ * plan_out, n_miss_out (host, may be NULL): the plan's number c, the misses. */
+int bqe_cache_fetch(bqe_cache* c, int32_t layer, int32_t n, const int32_t* experts,
+                    const void* const* host_src, void* staging, uint64_t staging_bytes,
+                    void* upload_stream, void* compute_stream, int64_t* plan_out, int32_t* n_miss_out);
+
+/* Make compute_stream wait for the uploads of plan `plan` (fetch's
+ * plan_out; one of the last four plans), before the kernels that use its
+ * experts; nothing to wait for if the plan had no miss. */
+int bqe_cache_ready(bqe_cache* c, int64_t plan, void* compute_stream);
+
+/* After the kernels that use the experts of plan `plan` (fetch's plan_out)
+ * are enqueued on compute_stream: record their completion, the point later
+ * fetches wait for before overwriting those slots.  One of the last four
+ * plans (BQE_EINVAL otherwise).  A plan left unrecorded makes a later fetch
+ * wait for everything enqueued on its compute stream instead. */
+int bqe_cache_done(bqe_cache* c, int64_t plan, void* compute_stream);
+
+/* The counts since the cache was created (host). */
+int bqe_cache_stats_get(const bqe_cache* c, bqe_cache_stats* out);
+
 /* Synchronise `stream` and report the device error word of the last
  * bqe_moe_layer_forward_noalloc call on the current device, then clear it
  * (as bqe_check does for a caller's workspace).  BQE_OK if no call ran. */
