@@ -691,6 +691,15 @@ def run_decode(args, rank, world):
         res["sub_records_timing"] = ("%d interleaved rounds after the headline steps, CUDA-graph replay, "
                                      "events around each layer (step40: around the 40-layer graph, per layer)" % R)
         res["sub_records_gpu_launches"] = sum(c.launches for c in subcases)
+        sr = res["sub_records"]
+        if "mixed_m1" in sr and "mixed_m6" in sr:
+            # a verify pass of 5 drafts is one M = 6 call per layer: it pays when
+            # it emits more tokens than t(M = 6) / t(M = 1); the field report
+            # (section 3B) logs 3.39 tokens per pass
+            t1, t6 = sr["mixed_m1"]["us_per_layer_median"], sr["mixed_m6"]["us_per_layer_median"]
+            res["verify_m6"] = dict(break_even_tokens_per_pass=round(t6 / t1, 3),
+                                    speedup_at_3_39_tokens_per_pass=round(3.39 * t1 / t6, 3),
+                                    note="derived from the mixed_m1 / mixed_m6 sub-records")
     if clk:
         res["clocks"] = clk
     if args.diag and isinstance(head, LayerCase):

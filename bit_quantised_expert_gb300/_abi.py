@@ -43,6 +43,14 @@ class bqe_cache_stats(ctypes.Structure):
                 ("evictions", ctypes.c_uint64), ("bytes_uploaded", ctypes.c_uint64)]
 
 
+VERIFY_MAX_DRAFT = 15
+
+
+class bqe_verify_stats(ctypes.Structure):
+    _fields_ = [("passes", ctypes.c_uint64), ("tokens", ctypes.c_uint64),
+                ("hist", ctypes.c_uint64 * (VERIFY_MAX_DRAFT + 1))]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError("libbqe.so is not built (%s); run bit_quantised_expert_gb300.buildlib.build() "
@@ -100,6 +108,7 @@ SIGNATURES = {
     "bqe_cache_fetch": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _U64, _P, _P, _P, _P]),
     "bqe_cache_done": (ctypes.c_int, [_P, ctypes.c_int64, _P]),
     "bqe_cache_ready": (ctypes.c_int, [_P, ctypes.c_int64, _P]),
+    "bqe_verify_pass": (ctypes.c_int, [_I32, _P, _P, _P, ctypes.POINTER(_I32), _P, ctypes.POINTER(bqe_verify_stats)]),
     "bqe_cache_stats_get": (ctypes.c_int, [_P, ctypes.POINTER(bqe_cache_stats)]),
 }
 
@@ -338,6 +347,20 @@ def bqe_cache_stats_get(h) -> dict:
     st = bqe_cache_stats()
     _ok(lib.bqe_cache_stats_get(h, ctypes.byref(st)), "bqe_cache_stats_get")
     return {k: getattr(st, k) for k, _ in st._fields_}
+
+
+def bqe_verify_pass(draft, target, stats: "bqe_verify_stats | None" = None):
+    """Host call.  Returns (emitted tokens, commit mask) of one verify pass."""
+    import numpy as np
+    d = np.ascontiguousarray(draft, dtype=np.int32)
+    t = np.ascontiguousarray(target, dtype=np.int32)
+    n = int(d.size)
+    em = np.zeros(n + 1, np.int32)
+    mask = np.zeros(n + 1, np.int32)
+    ne = _I32()
+    _ok(lib.bqe_verify_pass(n, ptr(d) if n else None, ptr(t), ptr(em), ctypes.byref(ne), ptr(mask),
+                            ctypes.byref(stats) if stats is not None else None), "bqe_verify_pass")
+    return em[:ne.value], mask
 
 
 def bqe_check(ws, stream=None) -> tuple[int, int]:

@@ -400,6 +400,29 @@ int bqe_cache_done(bqe_cache* c, int64_t plan, void* compute_stream);
 /* The counts since the cache was created (host). */
 int bqe_cache_stats_get(const bqe_cache* c, bqe_cache_stats* out);
 
+/* ---- speculative verify pass ---------------------------------------------
+ * Bookkeeping around a decode call whose M rows are the last accepted token
+ * and M - 1 drafts (the DeepSeek-V4.1-Flash field report, section 3B:
+ * draft-and-verify passes, tokens per pass; the 2 x RTX PRO 6000 post:
+ * batched verification, the accepted prefix committed, the rejected tail
+ * rolled back).  Greedy acceptance: draft i is kept while every draft before
+ * it was and it equals target[i], the target's prediction after row i. */
+#define BQE_VERIFY_MAX_DRAFT 15
+
+typedef struct {
+  uint64_t passes, tokens;                 /* tokens emitted over all passes */
+  uint64_t hist[BQE_VERIFY_MAX_DRAFT + 1]; /* passes by accepted draft count */
+} bqe_verify_stats;
+
+/* Host.  draft: n_draft tokens (n_draft <= BQE_VERIFY_MAX_DRAFT); target:
+ * n_draft + 1 predictions (after rows 0..n_draft).  With a drafts accepted:
+ * emitted[0..a] = the a drafts then target[a] (*n_emitted = a + 1), and
+ * commit_mask[r] = 1 for the rows r <= a to keep, 0 for those to roll back
+ * (n_draft + 1 entries).  stats (host, may be NULL) accumulates the pass.
+ * BQE_EINVAL on a bad argument. */
+int bqe_verify_pass(int32_t n_draft, const int32_t* draft, const int32_t* target, int32_t* emitted,
+                    int32_t* n_emitted, int32_t* commit_mask, bqe_verify_stats* stats);
+
 /* Synchronise `stream` and report the device error word of the last
  * bqe_moe_layer_forward_noalloc call on the current device, then clear it
  * (as bqe_check does for a caller's workspace).  BQE_OK if no call ran. */
