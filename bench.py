@@ -50,13 +50,14 @@ METRIC = "MoE layer decode: expert-byte GB/s (% of HBM peak) and us/layer at M=1
 HBM_FALLBACK_GBS = 6800.0
 WORKLOADS = {
     "fp4-m1": "dsv4flash-moe-layer-mxfp4-decode-M1",
+    "nvfp4-m1": "dsv4flash-moe-layer-nvfp4-decode-M1",
     "mixed-m1": "dsv4flash-moe-layer-mixed-tq1-q2_0-q3_k-decode-M1",
     "mixed-m6": "dsv4flash-moe-layer-mixed-tq1-q2_0-q3_k-decode-M6",
     "step40-m1": "dsv4flash-40-layer-step-4288-slot-pool-M1",
     "step40-m6": "dsv4flash-40-layer-step-4288-slot-pool-M6",
     "prefill": "dsv4flash-moe-layer-mixed-prefill-T8192-zipf0.8",
 }
-SUB_RECORDS = ("mixed-m1", "mixed-m6", "step40-m1")
+SUB_RECORDS = ("mixed-m1", "mixed-m6", "step40-m1", "nvfp4-m1")
 PREFILL_METRIC = "MoE layer prefill: tokens/s and expert-GEMM TFLOP/s at T=8192 (Zipf 0.8 routing)"
 
 # DRAM traffic of one decode-layer launch (k_moe) on the MXFP4 M=1 layer:
@@ -252,8 +253,8 @@ def _oracle_worker_init(workload: str, seed: int):
         forced = np.array([[0, 1, 2, 3, 4, 5], [5, 4, 3, 2, 1, 0]], dtype=np.int32)
         _ORACLE_CASE = ("prefill", x, router, experts, np.array(fm, np.int32), forced, 6)
         return
-    if workload.startswith("fp4"):
-        fm = [synth.MXFP4] * 7
+    if workload.startswith("fp4") or workload.startswith("nvfp4"):
+        fm = [synth.NVFP4 if workload.startswith("nv") else synth.MXFP4] * 7
     else:
         fm = [synth.TQ1, synth.TQ1, synth.TQ1, synth.Q2_0, synth.Q2_0, synth.Q3_K, synth.Q2_0]
     M = 6 if workload.endswith("m6") else 1
@@ -282,8 +283,8 @@ def _oracle_worker_run(_):
 
 def _oracle_bytes(workload: str) -> int:
     import synth
-    if workload.startswith("fp4"):
-        fm = [synth.MXFP4] * 7
+    if workload.startswith("fp4") or workload.startswith("nvfp4"):
+        fm = [synth.NVFP4 if workload.startswith("nv") else synth.MXFP4] * 7
     else:
         fm = [synth.TQ1, synth.TQ1, synth.TQ1, synth.Q2_0, synth.Q2_0, synth.Q3_K, synth.Q2_0]
     if workload.endswith("m6"):
@@ -295,8 +296,9 @@ def _oracle_sample_desc(workload: str) -> str:
     if workload == "prefill":
         return ("two prefill tokens of the mixed layer (router over 384 experts, 6 routed + shared expert FFN "
                 "each), fp64")
-    if workload.startswith("fp4"):
-        return "one MXFP4 layer call at M=1 (router 384 x 5120 fp32, 6 routed + 1 shared expert FFN), fp64"
+    if workload.startswith("fp4") or workload.startswith("nvfp4"):
+        return ("one %s layer call at M=1 (router 384 x 5120 fp32, 6 routed + 1 shared expert FFN), fp64"
+                % ("NVFP4" if workload.startswith("nv") else "MXFP4"))
     if workload.endswith("m6"):
         return ("one mixed-format layer call at M=6 (router 384 x 5120 fp32, 6 routed experts per row among 12 "
                 "distinct ternary/Q2_0/Q3_K ones + Q2_0 shared), fp64")
@@ -525,11 +527,11 @@ def make_case(A, dev, workload, args, banks):
     M = 6 if workload.endswith("m6") else 1
     if workload.startswith("step40"):
         return Step40Case(A, dev, M, workload)
-    kind = "fp4" if workload.startswith("fp4") else "mixed"
+    kind = "fp4" if workload.startswith("fp4") else "nvfp4" if workload.startswith("nvfp4") else "mixed"
     if kind not in banks:
         m = 6 if kind == "mixed" else 1
-        banks[kind] = WL.LayerSet(dev, kind, args.instances, seed=1 if kind == "fp4" else 2, m=m, n_x=64,
-                                  n_experts=args.experts)
+        banks[kind] = WL.LayerSet(dev, kind, args.instances, seed={"fp4": 1, "mixed": 2, "nvfp4": 3}[kind], m=m,
+                                  n_x=64, n_experts=args.experts)
     W = banks[kind]
     xs = W.xs if W.m == M else W.xs[:, :M].contiguous()
     return LayerCase(A, dev, W, M, xs, workload)
@@ -646,7 +648,8 @@ def run_decode(args, rank, world):
                       "weights streamed between reuses vs %.0f MB L2)" % (
                           head.NL, (head.NL - 1) * mean(head.bytes) / 1e6, l2mb),
                    parallelism="replicas" if world > 1 else "single-gpu")
-        kind = "mxfp4" if head_name.startswith("fp4") else "ternary/q2_0/q3_k"
+        kind = ("mxfp4" if head_name.startswith("fp4") else "nvfp4" if head_name.startswith("nvfp4")
+                else "ternary/q2_0/q3_k")
     else:
         router_bytes = E * H * 4
         cfg = dict(workload=WORKLOADS[head_name], layers=head.S.n_layers, slots=4288, M=M,

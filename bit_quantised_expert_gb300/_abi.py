@@ -14,7 +14,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libbqe.so")
 
 BQE_OK, BQE_EINVAL, BQE_ENOSPC, BQE_ECUDA, BQE_EDEVICE, BQE_ETIMEOUT, BQE_EUNSUPPORTED = range(7)
-BQE_FMT_TQ1, BQE_FMT_Q2_0, BQE_FMT_Q3_K, BQE_FMT_MXFP4 = 1, 2, 3, 4
+BQE_FMT_TQ1, BQE_FMT_Q2_0, BQE_FMT_Q3_K, BQE_FMT_MXFP4, BQE_FMT_NVFP4 = 1, 2, 3, 4, 5
 
 
 class BqeError(RuntimeError):
@@ -34,7 +34,7 @@ class bqe_pool(ctypes.Structure):
 
 
 class bqe_stats(ctypes.Structure):
-    _fields_ = [("rows", ctypes.c_int32), ("experts_streamed", ctypes.c_int32), ("per_format", ctypes.c_int32 * 5),
+    _fields_ = [("rows", ctypes.c_int32), ("experts_streamed", ctypes.c_int32), ("per_format", ctypes.c_int32 * 6),
                 ("row_uses", ctypes.c_int32), ("expert_bytes", ctypes.c_uint64), ("router_bytes", ctypes.c_uint64)]
 
 

@@ -14,6 +14,9 @@
 //         little-endian, 108..109 fp16 d.  w = d s_{j/16} (q - 4)
 //   MXFP4 17 B / 32: byte i = code_{2i} | code_{2i+1} << 4 (E2M1), byte 16 =
 //         UE8M0 exponent E.  w = e2m1(code) 2^(E-127)
+//   NVFP4 9 B / 16: bytes 0..7 as MXFP4's, byte 8 = FP8 E4M3 scale S (OCP:
+//         sign, 4-bit exponent with bias 7, 3-bit mantissa, subnormal at
+//         exponent 0, NaN at S = 0x7F / 0xFF).  w = e2m1(code) e4m3(S)
 #include <cuda_fp16.h>
 
 #include <cstring>
@@ -48,6 +51,7 @@ extern "C" int32_t bqe_scale_bytes(int32_t fmt) {
     case BQE_FMT_Q2_0: return 2;
     case BQE_FMT_Q3_K: return 18;
     case BQE_FMT_MXFP4: return 1;
+    case BQE_FMT_NVFP4: return 1;
   }
   return 0;
 }
@@ -71,6 +75,14 @@ extern "C" int bqe_pack(int32_t fmt, int32_t rows, int32_t cols, const uint8_t* 
         }
         if (s[0] == 0xFF) return BQE_EINVAL;  // NaN scale is not a weight
         o[16] = s[0];
+        break;
+      case BQE_FMT_NVFP4:
+        for (int j = 0; j < 16; ++j) {
+          if (c[j] > 15) return BQE_EINVAL;
+          o[j >> 1] |= (uint8_t)(c[j] << ((j & 1) * 4));
+        }
+        if ((s[0] & 0x7F) == 0x7F) return BQE_EINVAL;  // NaN scale is not a weight
+        o[8] = s[0];
         break;
       case BQE_FMT_Q2_0:
         for (int j = 0; j < 64; ++j) {
@@ -252,6 +264,10 @@ extern "C" int bqe_unpack_host(int32_t fmt, int32_t rows, int32_t cols, const ui
         for (int j = 0; j < 32; ++j) c[j] = (uint8_t)((b[j >> 1] >> ((j & 1) * 4)) & 15);
         s[0] = b[16];
         break;
+      case BQE_FMT_NVFP4:
+        for (int j = 0; j < 16; ++j) c[j] = (uint8_t)((b[j >> 1] >> ((j & 1) * 4)) & 15);
+        s[0] = b[8];
+        break;
       case BQE_FMT_Q2_0:
         for (int j = 0; j < 64; ++j) c[j] = (uint8_t)((b[j >> 2] >> (2 * (j & 3))) & 3);
         s[0] = b[16];
@@ -304,6 +320,15 @@ __device__ __forceinline__ float e2m1_value(uint32_t c) {
   return (c & 8) ? -m : m;
 }
 
+// OCP FP8 E4M3 (sign, exponent bias 7, 3 mantissa bits; exponent 0 subnormal),
+// written out from the format's definition: exact in fp32.  NaN is refused
+// when packing and never decoded here.
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  const int e = (b >> 3) & 15, m = b & 7;
+  const float mag = e == 0 ? ldexpf((float)m, -9) : ldexpf((float)(8 + m), e - 10);
+  return (b & 0x80) ? -mag : mag;
+}
+
 __device__ __forceinline__ float ue8m0_value(uint32_t e) {
   return e == 0 ? __int_as_float(0x00400000) : __int_as_float((int)(e << 23));  // 2^(E-127)
 }
@@ -324,6 +349,9 @@ __global__ void k_dequant(int fmt, int rows, int K, const uint8_t* __restrict__ 
     if (fmt == BQE_FMT_MXFP4) {
       const float sc = ue8m0_value(by[16]);
       for (int j = 0; j < 32; ++j) o[j] = e2m1_value((by[j >> 1] >> ((j & 1) * 4)) & 15) * sc;
+    } else if (fmt == BQE_FMT_NVFP4) {
+      const float sc = e4m3_value(by[8]);
+      for (int j = 0; j < 16; ++j) o[j] = e2m1_value((by[j >> 1] >> ((j & 1) * 4)) & 15) * sc;
     } else if (fmt == BQE_FMT_Q2_0) {
       const float dd = fp16_bits_to_f32(by[16], by[17]);
       for (int j = 0; j < 64; ++j) o[j] = dd * (float)(2 * ((by[j >> 2] >> (2 * (j & 3))) & 3) - 3);

@@ -47,10 +47,11 @@ __host__ __device__ inline int act_row_bytes(int amode, int fmt, int kc) {
 }
 // ... and the distance between two staged rows in shared memory: x rows sit
 // 64 bytes past a multiple of 128, so that the 16-byte B loads of two rows
-// (one quarter-warp) fall in different banks.
+// (one quarter-warp) fall in different banks (NVFP4: 32 bytes, see below).
 __host__ __device__ inline int act_row_stride(int amode, int fmt, int kc) {
   const int b = act_row_bytes(amode, fmt, kc);
-  return amode == kActF16 ? ((b + 127) & ~127) + 64 : (b + 15) & ~15;
+  // NVFP4 reads 8-byte B pieces (half-warps over four rows): 32 bytes apart
+  return amode == kActF16 ? ((b + 127) & ~127) + (fmt == BQE_FMT_NVFP4 ? 32 : 64) : (b + 15) & ~15;
 }
 
 // ----------------------------------------------------------------------------
@@ -125,6 +126,71 @@ __device__ __forceinline__ void mma_mxfp4(const uint8_t* tile, int nb, int grp, 
         acc[j][mt][3] = fmaf(d[3], s1, acc[j][mt][3]);
       }
     }
+  }
+}
+
+// Two E2M1 code bytes (the low 16 bits of w) -> two f16x2, and two E4M3
+// scale bytes (the low 16 bits of s) -> one f16x2, by the hardware conversions.
+__device__ __forceinline__ void e2m1x4_to_f16x2(uint32_t w, uint32_t& h0, uint32_t& h1) {
+  asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %2;\n"
+      "  cvt.rn.f16x2.e2m1x2 %0, b0; cvt.rn.f16x2.e2m1x2 %1, b1; }"
+      : "=r"(h0), "=r"(h1)
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t s) {
+  uint32_t h;
+  asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %1; cvt.rn.f16x2.e4m3x2 %0, lo; }" : "=r"(h) : "r"(s));
+  return h;
+}
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// NVFP4 (16-column blocks = one k16 step): thread tq takes code bytes 2 tq,
+// 2 tq + 1 of a row's 8 (columns 4 tq .. 4 tq + 3), natural column order; the
+// block's E4M3 scale multiplies the decoded pair in f16, exactly (an E2M1
+// value times an E4M3 value has at most 6 significant bits and stays within
+// f16's normal range), so the scale rides in A and the accumulators need
+// none.  Even and odd blocks accumulate separately (two MMA chains).
+template <int NJ>
+__device__ __forceinline__ void mma_nvfp4(const uint8_t* tile, int nb, int grp, const uint8_t* const (&bv)[NJ],
+                                          int lane, float (&acc)[NJ][2][4]) {
+  const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    const int r0 = 16 * mt + gq;
+    float d[NJ][2][4];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) d[j][h][0] = d[j][h][1] = d[j][h][2] = d[j][h][3] = 0.f;
+#pragma unroll 4
+    for (int bi = 0; bi < 16; ++bi) {
+      const int b = grp * 16 + bi;
+      const uint32_t c0 = *reinterpret_cast<const uint16_t*>(tile + b * 256 + r0 * 8 + 2 * tq);
+      const uint32_t c1 = *reinterpret_cast<const uint16_t*>(tile + b * 256 + (r0 + 8) * 8 + 2 * tq);
+      const uint32_t sc = e4m3x2_to_f16x2((uint32_t)tile[nb * 256 + b * 32 + r0] |
+                                          ((uint32_t)tile[nb * 256 + b * 32 + r0 + 8] << 8));
+      const uint32_t s0 = __byte_perm(sc, sc, 0x1010), s1 = __byte_perm(sc, sc, 0x3232);
+      uint32_t p0, p1, q0, q1;
+      e2m1x4_to_f16x2(c0, p0, p1);
+      e2m1x4_to_f16x2(c1, q0, q1);
+      p0 = hmul2u(p0, s0);
+      p1 = hmul2u(p1, s0);
+      q0 = hmul2u(q0, s1);
+      q1 = hmul2u(q1, s1);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const uint2 x = *reinterpret_cast<const uint2*>(bv[j] + (b * 16 + 4 * tq) * 2);
+        mma_f16(d[j][bi & 1], p0, q0, p1, q1, x.x, x.y);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[j][mt][e] += d[j][0][e] + d[j][1][e];
   }
 }
 
@@ -388,6 +454,7 @@ __device__ __forceinline__ void mma_group_nj(int R, int fmt, const uint8_t* tile
       if (NJ == 1) mma_tq1<1>(tile, nb, grp, reinterpret_cast<const uint8_t* const(&)[1]>(bv), lane,
                               reinterpret_cast<float(&)[1][2][4]>(acc));
       break;
+    case BQE_FMT_NVFP4: mma_nvfp4<NJ>(tile, nb, grp, bv, lane, acc); break;
     default: break;
   }
   if (!hl) {

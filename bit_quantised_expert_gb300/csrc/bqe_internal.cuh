@@ -14,16 +14,19 @@ namespace bqe {
 
 // ----------------------------------------------------------------------------
 // Block formats.  Weights per block / bytes per block (bits per weight from
-// the Strata 4090 post, section 5.1, and the FP4 per-32 block of the field
-// report): TQ1 256/56, Q2_0 64/18, Q3_K 256/110, MXFP4 32/17.
+// the Strata 4090 post, section 5.1, the FP4 per-32 block of the field
+// report, and NVIDIA's NVFP4 for the news digest's NVFP4 checkpoint): TQ1
+// 256/56, Q2_0 64/18, Q3_K 256/110, MXFP4 32/17, NVFP4 16/9.
 // ----------------------------------------------------------------------------
 __host__ __device__ constexpr int fmt_bw(int f) {
-  return f == BQE_FMT_TQ1 ? 256 : f == BQE_FMT_Q2_0 ? 64 : f == BQE_FMT_Q3_K ? 256 : f == BQE_FMT_MXFP4 ? 32 : 0;
+  return f == BQE_FMT_TQ1 ? 256 : f == BQE_FMT_Q2_0 ? 64 : f == BQE_FMT_Q3_K ? 256 : f == BQE_FMT_MXFP4 ? 32
+         : f == BQE_FMT_NVFP4 ? 16 : 0;
 }
 __host__ __device__ constexpr int fmt_bb(int f) {
-  return f == BQE_FMT_TQ1 ? 56 : f == BQE_FMT_Q2_0 ? 18 : f == BQE_FMT_Q3_K ? 110 : f == BQE_FMT_MXFP4 ? 17 : 0;
+  return f == BQE_FMT_TQ1 ? 56 : f == BQE_FMT_Q2_0 ? 18 : f == BQE_FMT_Q3_K ? 110 : f == BQE_FMT_MXFP4 ? 17
+         : f == BQE_FMT_NVFP4 ? 9 : 0;
 }
-__host__ __device__ constexpr bool fmt_ok(int f) { return f >= BQE_FMT_TQ1 && f <= BQE_FMT_MXFP4; }
+__host__ __device__ constexpr bool fmt_ok(int f) { return f >= BQE_FMT_TQ1 && f <= BQE_FMT_NVFP4; }
 
 // ----------------------------------------------------------------------------
 // Device layout of one matrix (rows x K) of a slot.
@@ -38,6 +41,7 @@ __host__ __device__ constexpr bool fmt_ok(int f) { return f >= BQE_FMT_TQ1 && f 
 //    lanes reading the same piece of the same block for their own row read
 //    512 contiguous bytes:
 //      MXFP4: codes16 @ b*512 + r*16           | E   @ nb*512 + b*32 + r
+//      NVFP4: codes8 @ b*256 + r*8             | S   @ nb*256 + b*32 + r
 //      Q2_0 : codes16 @ b*512 + r*16           | d   @ nb*512 + (b*32+r)*2
 //      TQ1  : bytes0..47 @ (b*3+q)*512 + r*16  | bytes48..55 @ nb*1536 + (b*32+r)*8
 //      Q3_K : lo64 @ (b*4+q)*512 + r*16        | hi32 @ nb*2048 + (b*2+q)*512 + r*16
@@ -60,6 +64,8 @@ __host__ __device__ inline uint32_t tile_byte_offset(int f, int nb, int b, int r
   switch (f) {
     case BQE_FMT_MXFP4:
       return i < 16 ? (uint32_t)(b * 512 + r * 16 + i) : (uint32_t)(nb * 512 + b * 32 + r);
+    case BQE_FMT_NVFP4:
+      return i < 8 ? (uint32_t)(b * 256 + r * 8 + i) : (uint32_t)(nb * 256 + b * 32 + r);
     case BQE_FMT_Q2_0:
       return i < 16 ? (uint32_t)(b * 512 + r * 16 + i) : (uint32_t)(nb * 512 + (b * 32 + r) * 2 + (i - 16));
     case BQE_FMT_TQ1:

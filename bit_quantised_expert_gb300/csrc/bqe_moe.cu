@@ -186,7 +186,7 @@ __device__ inline void make_tpl(const MoeParams& P, ItemTpl& T, int ph, int u, i
   T.m13 = (uint32_t)m13;
   T.wsrc = addr + (ph ? 2 * m13 : 0);
   if (ph == 0) {  // f16 x in the format's order
-    T.act_base = (uint32_t)(fmt == BQE_FMT_MXFP4 ? P.L.xh : fmt == BQE_FMT_TQ1 ? P.L.xt : P.L.xp);
+    T.act_base = (uint32_t)(fmt == BQE_FMT_TQ1 ? P.L.xt : (fmt == BQE_FMT_Q2_0 || fmt == BQE_FMT_Q3_K) ? P.L.xp : P.L.xh);
     T.act_cs = (uint32_t)f16_len(fmt, kc) * 2;
     T.act_rs = (uint32_t)f16_len(fmt, g.H) * 2;
   } else {  // the f16 records of h of the expert's row slots
@@ -1252,7 +1252,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
             hw[k] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
             lw[k] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
           }
-          if (fmt != BQE_FMT_MXFP4) {
+          if (fmt == BQE_FMT_Q2_0 || fmt == BQE_FMT_Q3_K) {
             // P order: in every 16 columns (lanes 2m, 2m + 1) position 2p holds
             // column p and 2p + 1 column 8 + p: the even lane writes (c0, c8, ..,
             // c3, c11), the odd one (c4, c12, .., c7, c15)
@@ -1305,14 +1305,19 @@ static int moe_pb(const Geo& g) {
   return best;
 }
 
-// Largest byte size of one item (MXFP4 tiles and T-order x rows are the
-// largest of the formats).
+// Largest byte size of one item (the largest tile of any format, T-order x
+// rows the longest staged rows).
 static uint32_t moe_max_item(const Geo& g, int PB) {
   auto a128 = [](uint32_t v) { return (v + 127u) & ~127u; };
+  auto max_tile = [](int kc) {
+    uint32_t t = 0;
+    for (int f = BQE_FMT_TQ1; f <= BQE_FMT_NVFP4; ++f) t = tile_bytes(f, kc) > t ? tile_bytes(f, kc) : t;
+    return t;
+  };
   const uint32_t actA = (uint32_t)act_row_stride(kActF16, BQE_FMT_TQ1, g.kcA);
-  const uint32_t A = a128(2 * tile_bytes(BQE_FMT_MXFP4, g.kcA)) + a128(g.M * actA) + 2 * g.GA * g.M * 128;
+  const uint32_t A = a128(2 * max_tile(g.kcA)) + a128(g.M * actA) + 2 * g.GA * g.M * 128;
   const uint32_t actB = hrec_stride(g.kcB);
-  const uint32_t B = a128(PB * tile_bytes(BQE_FMT_MXFP4, g.kcB)) + a128(g.M * actB) + PB * g.GB * g.M * 128;
+  const uint32_t B = a128(PB * max_tile(g.kcB)) + a128(g.M * actB) + PB * g.GB * g.M * 128;
   return A > B ? A : B;
 }
 

@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(1024) k_pf_plan(PfParams P) {
     }
     gaddr[gi] = addr;
     gfmt[gi] = fmt;
-    gf16[gi] = P.f16 && fmt != BQE_FMT_MXFP4;
+    gf16[gi] = P.f16 && fmt != BQE_FMT_MXFP4 && fmt != BQE_FMT_NVFP4;  // FP4 values are exact in bf16
     cnt[gi] = n;
   }
   const int padded = (n + kPfRowAlign - 1) / kPfRowAlign * kPfRowAlign;
@@ -464,6 +464,10 @@ __device__ __forceinline__ void issue_raw_group(int fmt, const uint8_t* tile, in
       bulk_g2s(dst, tile + gi * 4096, 4096, bar);
       bulk_g2s(dst + 4096, tile + nb * 512 + gi * 256, 256, bar);
       break;
+    case BQE_FMT_NVFP4:
+      bulk_g2s(dst, tile + gi * 4096, 4096, bar);
+      bulk_g2s(dst + 4096, tile + nb * 256 + gi * 512, 512, bar);
+      break;
     case BQE_FMT_TQ1:
       bulk_g2s(dst, tile + gi * 1536, 1536, bar);
       bulk_g2s(dst + 1536, tile + nb * 1536 + gi * 256, 256, bar);
@@ -524,6 +528,33 @@ __device__ __forceinline__ void dq_mxfp4(const uint8_t* P, int kq, int lane, uin
         o[by] = pack2<false>(v.x * sc, v.y * sc);
       }
       store_chunk(A, row, bi * 4 + w, o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// NVFP4, K-step kq = blocks 4kq .. 4kq + 3 (16 columns each): w = e2m1(code) *
+// e4m3(scale), exact in bf16 (at most 6 significant bits).
+__device__ __forceinline__ float e4m3_f32(uint32_t b) {
+  const int e = (b >> 3) & 15, m = b & 7;
+  const float mag = e == 0 ? ldexpf((float)m, -9) : ldexpf((float)(8 + m), e - 10);
+  return (b & 0x80) ? -mag : mag;
+}
+__device__ __forceinline__ void dq_nvfp4(const uint8_t* P, int kq, int lane, uint8_t* A, int row) {  // bf16 only
+#pragma unroll
+  for (int bi = 0; bi < 4; ++bi) {
+    const int b = 4 * kq + bi;
+    const uint2 c2 = *reinterpret_cast<const uint2*>(P + b * 256 + lane * 8);
+    const float sc = e4m3_f32(P[4096 + b * 32 + lane]);
+    const uint32_t wd[2] = {c2.x, c2.y};
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {  // one word = 8 weights = one 16-byte chunk
+      uint32_t o[4];
+#pragma unroll
+      for (int by = 0; by < 4; ++by) {
+        const float2 v = e2m1x2_f32((wd[w] >> (8 * by)) & 0xFFu);
+        o[by] = pack2<false>(v.x * sc, v.y * sc);
+      }
+      store_chunk(A, row, bi * 2 + w, o[0], o[1], o[2], o[3]);
     }
   }
 }
@@ -715,6 +746,7 @@ __device__ __forceinline__ void dequant_kstep(int fmt, bool f16, const uint8_t* 
       if (f16) dq_q2_0_paired(P, kq, lane, A, row, bad); else dq_q2_0<false>(P, kq, lane, A, row, bad);
       break;
     case BQE_FMT_MXFP4: dq_mxfp4(P, kq, lane, A, row); break;
+    case BQE_FMT_NVFP4: dq_nvfp4(P, kq, lane, A, row); break;
     case BQE_FMT_TQ1:
       if (f16) dq_tq1<true>(P, kq, lane, A, row); else dq_tq1<false>(P, kq, lane, A, row);
       break;

@@ -15,7 +15,7 @@ constexpr int kPfAStages = 5;       // dequantised A ring (one 64-column K-step 
 constexpr int kPfBStages = 3;       // B (token rows) area: 3 stages of 256 rows, re-split per item
 constexpr int kPfBMaxStages = 16;   // stages of the B area for short tiles (area / (rows * 128 bytes), at most)
 constexpr int kPfRawStages = 2;     // quantised-weight ring (one 256-column group per stage)
-constexpr uint32_t kPfRawPanel = 4352;                 // 32 rows x 256 columns, largest format (MXFP4)
+constexpr uint32_t kPfRawPanel = 4608;                 // 32 rows x 256 columns, largest format (NVFP4)
 constexpr uint32_t kPfRawStage = 4 * kPfRawPanel;      // four 32-row panels = one 128-row A tile
 constexpr uint32_t kPfAStage = 128 * 128;              // 128 rows x 64 16-bit values
 constexpr uint32_t kPfBStage = kPfTileN * 128;         // 256 rows x 64 16-bit values

@@ -17,6 +17,9 @@
  *   BQE_FMT_Q2_0  64 weights / 18 B (2.25 bpw), w = d (2q - 3)
  *   BQE_FMT_Q3_K  256 weights / 110 B (3.4375 bpw), w = d s_j (q - 4)
  *   BQE_FMT_MXFP4 32 weights / 17 B (4.25 bpw), w = e2m1(c) 2^(E-127)
+ *   BQE_FMT_NVFP4 16 weights / 9 B (4.5 bpw), w = e2m1(c) e4m3(S): an NVFP4
+ *                 checkpoint (news digest) read as NVIDIA's published NVFP4,
+ *                 blocks of 16 with an FP8 E4M3 scale, no per-tensor scale
  *
  * Conventions for every entry point:
  *   - Return value: BQE_OK or an error code; nothing throws across the ABI.
@@ -49,7 +52,7 @@ enum {
   BQE_EUNSUPPORTED = 6  /* shape or device not supported */
 };
 
-enum { BQE_FMT_TQ1 = 1, BQE_FMT_Q2_0 = 2, BQE_FMT_Q3_K = 3, BQE_FMT_MXFP4 = 4 };
+enum { BQE_FMT_TQ1 = 1, BQE_FMT_Q2_0 = 2, BQE_FMT_Q3_K = 3, BQE_FMT_MXFP4 = 4, BQE_FMT_NVFP4 = 5 };
 
 /* Shape of one MoE layer.  hidden and inter must be multiples of 256 (every
  * format's block divides 256) and of 32 rows; n_shared must be 1; at most
@@ -85,7 +88,7 @@ typedef struct {
 typedef struct {
   int32_t rows;              /* token rows of the call (M) */
   int32_t experts_streamed;  /* distinct experts read, the shared one included */
-  int32_t per_format[5];     /* of those, how many in each format (index = BQE_FMT_*) */
+  int32_t per_format[6];     /* of those, how many in each format (index = BQE_FMT_*) */
   int32_t row_uses;          /* (expert, row) pairs computed: sum over experts of the rows that chose it */
   uint64_t expert_bytes;     /* packed bytes of those experts, each read once */
   uint64_t router_bytes;     /* fp32 router weights read (n_experts x hidden x 4) */
@@ -107,15 +110,17 @@ uint64_t bqe_expert_bytes(const bqe_layer_desc* d, int32_t fmt);
 
 /* Bytes of the scale field per block that bqe_pack() reads:
  * TQ1 2 (fp16 d), Q2_0 2 (fp16 d), Q3_K 18 (16 six-bit sub-scales as bytes
- * 0..63, then fp16 d), MXFP4 1 (the UE8M0 exponent byte). */
+ * 0..63, then fp16 d), MXFP4 1 (the UE8M0 exponent byte), NVFP4 1 (the E4M3
+ * scale byte). */
 int32_t bqe_scale_bytes(int32_t fmt);
 
 /* Host: pack a rows x cols matrix into canonical blocks (row-major; each row
  * is cols/block consecutive blocks).  codes: one byte per weight, row-major,
  * in the format's code domain (TQ1: t+1 in 0..2; Q2_0: q in 0..3; Q3_K: q in
- * 0..7; MXFP4: 4-bit code 0..15).  scales: bqe_scale_bytes(fmt) bytes per
+ * 0..7; MXFP4, NVFP4: 4-bit code 0..15).  scales: bqe_scale_bytes(fmt) bytes per
  * block, blocks in row-major order.  out: bqe_packed_bytes() bytes.
- * BQE_EINVAL on a code or scale out of its domain (nothing is written then
+ * BQE_EINVAL on a code or scale out of its domain (a NaN scale: MXFP4 0xFF,
+ * NVFP4 0x7F / 0xFF) (nothing is written then
  * for that block onward). */
 int bqe_pack(int32_t fmt, int32_t rows, int32_t cols, const uint8_t* codes,
              const uint8_t* scales, uint8_t* out);

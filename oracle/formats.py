@@ -6,10 +6,13 @@ The pages name the formats and their bits per weight but print no layout:
   * Q2_0: 2.25 bpw, the budget-neutral reference format (section 5.1);
   * Q3_K: 3.44 bpw (section 5.1);
   * FP4 experts with per-32 weight blocks (DeepSeek-V4.1-Flash 4xL20 field
-    report, header and section 2: "single expert = 3 x 5120 x 2304 x 0.5 B").
+    report, header and section 2: "single expert = 3 x 5120 x 2304 x 0.5 B");
+  * an NVFP4 checkpoint of the model (the news digest): FP4 codes in blocks
+    of 16 with an FP8 E4M3 scale each, the plainest reading of NVIDIA's
+    published NVFP4 (the pages give no layout; no per-tensor scale here).
 The block layouts decoded here are this library's specification of those
 formats (one block per bpw figure: 56 B / 256, 18 B / 64, 110 B / 256,
-17 B / 32).  Every value is exact in fp64, so decoding is exact.
+17 B / 32, 9 B / 16).  Every value is exact in fp64, so decoding is exact.
 
 Functions take an array of canonical blocks of shape (..., block_bytes) as
 uint8 and return float64 weights of shape (..., block_weights).
@@ -18,8 +21,8 @@ from __future__ import annotations
 
 import numpy as np
 
-TQ1, Q2_0, Q3_K, MXFP4 = 1, 2, 3, 4
-BLOCK = {TQ1: (256, 56), Q2_0: (64, 18), Q3_K: (256, 110), MXFP4: (32, 17)}
+TQ1, Q2_0, Q3_K, MXFP4, NVFP4 = 1, 2, 3, 4, 5
+BLOCK = {TQ1: (256, 56), Q2_0: (64, 18), Q3_K: (256, 110), MXFP4: (32, 17), NVFP4: (16, 9)}
 
 
 def fp16_to_f64(lo: np.ndarray, hi: np.ndarray) -> np.ndarray:
@@ -50,6 +53,29 @@ def ue8m0_to_f64(e: np.ndarray) -> np.ndarray:
     """UE8M0 scale byte: 2^(E - 127); 0xFF is NaN."""
     e = e.astype(np.int64)
     return np.where(e == 255, np.nan, np.exp2(e.astype(np.float64) - 127.0))
+
+
+def e4m3_to_f64(b: np.ndarray) -> np.ndarray:
+    """OCP FP8 E4M3: bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0
+    mantissa; exponent field 0 is subnormal (mantissa / 8 x 2^-6); exponent
+    15 with mantissa 7 is NaN (the format has no infinities)."""
+    b = b.astype(np.int64)
+    s = (b >> 7) & 1
+    e = (b >> 3) & 15
+    m = b & 7
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(s == 1, -mag, mag)
+
+
+def dequant_nvfp4(blocks: np.ndarray) -> np.ndarray:
+    """9-byte block of 16 weights: byte i (0..7) holds weight 2i in its low
+    nibble and 2i+1 in its high nibble (E2M1); byte 8 is the E4M3 scale.
+    w = e2m1(code) * e4m3(scale)."""
+    b = blocks.astype(np.int64)
+    codes = b[..., :8]
+    nib = np.stack([codes & 0xF, (codes >> 4) & 0xF], axis=-1).reshape(*b.shape[:-1], 16)
+    return e2m1_to_f64(nib) * e4m3_to_f64(b[..., 8])[..., None]
 
 
 def dequant_mxfp4(blocks: np.ndarray) -> np.ndarray:
@@ -121,7 +147,7 @@ def dequant_q3k(blocks: np.ndarray) -> np.ndarray:
     return d[..., None] * s * (q - 4)
 
 
-DECODERS = {TQ1: dequant_tq1, Q2_0: dequant_q2_0, Q3_K: dequant_q3k, MXFP4: dequant_mxfp4}
+DECODERS = {TQ1: dequant_tq1, Q2_0: dequant_q2_0, Q3_K: dequant_q3k, MXFP4: dequant_mxfp4, NVFP4: dequant_nvfp4}
 
 
 def dequant_matrix(fmt: int, packed: np.ndarray, rows: int, cols: int) -> np.ndarray:

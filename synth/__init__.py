@@ -21,15 +21,16 @@ dimension):
   Q3_K            256 weights, 110 B: 64 B low-2-bit plane, 32 B high-bit
                   plane, 12 B of sixteen 6-bit sub-scales, fp16 d
   MXFP4            32 weights, 17 B: 16 B of E2M1 nibbles, 1 B UE8M0 exponent
+  NVFP4            16 weights, 9 B: 8 B of E2M1 nibbles, 1 B FP8 E4M3 scale
 """
 from __future__ import annotations
 
 import numpy as np
 
-TQ1, Q2_0, Q3_K, MXFP4 = 1, 2, 3, 4
-FMT_NAMES = {TQ1: "tq1", Q2_0: "q2_0", Q3_K: "q3_k", MXFP4: "mxfp4"}
+TQ1, Q2_0, Q3_K, MXFP4, NVFP4 = 1, 2, 3, 4, 5
+FMT_NAMES = {TQ1: "tq1", Q2_0: "q2_0", Q3_K: "q3_k", MXFP4: "mxfp4", NVFP4: "nvfp4"}
 # format -> (weights per block, bytes per block)
-BLOCK = {TQ1: (256, 56), Q2_0: (64, 18), Q3_K: (256, 110), MXFP4: (32, 17)}
+BLOCK = {TQ1: (256, 56), Q2_0: (64, 18), Q3_K: (256, 110), MXFP4: (32, 17), NVFP4: (16, 9)}
 
 
 def block_weights(fmt: int) -> int:
@@ -68,6 +69,11 @@ def random_blocks(rng, fmt: int, nblocks: int) -> np.ndarray:
         out[:, :16] = rng.integers(0, 256, size=(nblocks, 16), dtype=np.uint8)
         # UE8M0 exponent byte uniform in 119..123, i.e. 2^-8 .. 2^-4
         out[:, 16] = rng.integers(119, 124, size=nblocks, dtype=np.uint8)
+    elif fmt == NVFP4:
+        out[:, :8] = rng.integers(0, 256, size=(nblocks, 8), dtype=np.uint8)
+        # positive E4M3 scale bytes 0..39: exponent field 0..4, i.e. up to
+        # 1.875 x 2^-3, subnormals and zero included (0x7F / 0xFF, NaN, never)
+        out[:, 8] = rng.integers(0, 40, size=nblocks, dtype=np.uint8)
     elif fmt == Q2_0:
         out[:, :16] = rng.integers(0, 256, size=(nblocks, 16), dtype=np.uint8)
         d = fp16_bits_abs_normal(rng, nblocks, 0.02)
@@ -249,6 +255,9 @@ def torch_random_blocks(gen, fmt: int, nblocks: int, device):
     if fmt == MXFP4:
         out[:, :16] = ri(0, 256, (nblocks, 16))
         out[:, 16] = ri(119, 124, (nblocks,))
+    elif fmt == NVFP4:
+        out[:, :8] = ri(0, 256, (nblocks, 8))
+        out[:, 8] = ri(0, 40, (nblocks,))
     elif fmt == Q2_0:
         out[:, :16] = ri(0, 256, (nblocks, 16))
         lo, hi = d_bits(0.02)

@@ -18,7 +18,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (MXFP4, Q2_0, assign_formats, expert_bytes, largest_remainder_counts, torch_random_expert,
+from . import (MXFP4, NVFP4, Q2_0, assign_formats, expert_bytes, largest_remainder_counts, torch_random_expert,
                zipf_forced_idx, MIX_SHARES)
 
 H, I, E, K = 5120, 2304, 384, 6
@@ -79,8 +79,9 @@ class Layer:
         return expert_bytes(int(self.fmts[e]), H, I)
 
 
-def fp4_layer(device, seed=1, m=1, n_x=64, n_experts=E):
-    return Layer(device, seed, [MXFP4] * (n_experts + 1), m, n_x, 0.0)
+def fp4_layer(device, seed=1, m=1, n_x=64, n_experts=E, fmt=MXFP4):
+    """Every expert in one FP4 format (MXFP4, or NVFP4 with fmt=5), zero bias."""
+    return Layer(device, seed, [fmt] * (n_experts + 1), m, n_x, 0.0)
 
 
 def mixed_fmts(seed: int, n: int) -> np.ndarray:
@@ -150,13 +151,13 @@ class LayerSet:
         per = n_experts + 1
         fm = []
         for i in range(n_inst):
-            if kind == "fp4":
-                fm.append(np.full(per, MXFP4, np.int32))
+            if kind in ("fp4", "nvfp4"):
+                fm.append(np.full(per, MXFP4 if kind == "fp4" else NVFP4, np.int32))
             else:
                 fm.append(np.concatenate([mixed_fmts(seed * 101 + i, n_experts), [Q2_0]]).astype(np.int32))
         self.fmts = np.concatenate(fm)
         self.d, self.pool = build_pool(device, seed, self.fmts, n_experts=n_experts)
-        wr, bias, xs = router_and_inputs(device, seed, n_inst, m, n_x, 0.0 if kind == "fp4" else 0.25,
+        wr, bias, xs = router_and_inputs(device, seed, n_inst, m, n_x, 0.0 if kind in ("fp4", "nvfp4") else 0.25,
                                          n_experts=n_experts)
         self.wr = [wr[i].contiguous() for i in range(n_inst)]
         self.bias = None if bias is None else [bias[i].contiguous() for i in range(n_inst)]

@@ -46,12 +46,13 @@ def test_block_sizes(A):
     for fmt, (bw, bb) in F.BLOCK.items():
         assert A.bqe_block_weights(fmt) == bw
         assert A.bqe_block_bytes(fmt) == bb
-    assert A.bqe_block_bytes(0) == 0 and A.bqe_block_bytes(5) == 0
+    assert A.bqe_block_bytes(0) == 0 and A.bqe_block_bytes(6) == 0
     assert A.bqe_packed_bytes(A.BQE_FMT_MXFP4, 2304, 5120) == 2304 * 160 * 17
     assert A.bqe_packed_bytes(A.BQE_FMT_TQ1, 32, 100) == 0  # not a whole block
     d = A.desc(5120, 2304, 384, 6)
     assert A.bqe_expert_bytes(d, A.BQE_FMT_MXFP4) == 18_800_640
-    for fmt in (1, 2, 3, 4):
+    assert A.bqe_expert_bytes(d, A.BQE_FMT_NVFP4) == 3 * 5120 * 2304 * 9 // 16 == 19_906_560  # 4.5 bpw
+    for fmt in (1, 2, 3, 4, 5):
         assert A.bqe_expert_bytes(d, fmt) == synth.expert_bytes(fmt, 5120, 2304)
 
 
@@ -70,11 +71,15 @@ def _intended(fmt, codes, scales):
     """Weights a packer input stands for, from the format definitions."""
     bw = F.BLOCK[fmt][0]
     c = codes.reshape(-1, bw).astype(np.float64)
-    if fmt == F.MXFP4:
+    if fmt in (F.MXFP4, F.NVFP4):
         mag = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6.0])
         ci = codes.reshape(-1, bw).astype(np.int64)
         v = np.where(ci & 8, -mag[ci & 7], mag[ci & 7])
-        return v * np.exp2(scales.reshape(-1, 1).astype(np.float64) - 127)
+        if fmt == F.MXFP4:
+            return v * np.exp2(scales.reshape(-1, 1).astype(np.float64) - 127)
+        import torch  # E4M3 scale through PyTorch's own float8 conversion
+        sc = torch.from_numpy(np.ascontiguousarray(scales)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        return v * sc.reshape(-1, 1)
     d = scales.reshape(-1, A_SB[fmt])[:, -2:].copy().view(np.float16).astype(np.float64)
     if fmt == F.Q2_0:
         return d * (2 * c - 3)
@@ -84,19 +89,22 @@ def _intended(fmt, codes, scales):
     return d * np.repeat(s, 16, axis=1) * (c - 4)
 
 
-A_SB = {F.TQ1: 2, F.Q2_0: 2, F.Q3_K: 18, F.MXFP4: 1}
+A_SB = {F.TQ1: 2, F.Q2_0: 2, F.Q3_K: 18, F.MXFP4: 1, F.NVFP4: 1}
 
 
-@pytest.mark.parametrize("fmt", [F.TQ1, F.Q2_0, F.Q3_K, F.MXFP4])
+@pytest.mark.parametrize("fmt", [F.TQ1, F.Q2_0, F.Q3_K, F.MXFP4, F.NVFP4])
 def test_pack_matches_oracle_decode(A, fmt):
     rng = np.random.default_rng(fmt)
     rows, cols = 4, 512
     bw, bb = F.BLOCK[fmt]
     nblk = rows * cols // bw
-    hi = {F.TQ1: 3, F.Q2_0: 4, F.Q3_K: 8, F.MXFP4: 16}[fmt]
+    hi = {F.TQ1: 3, F.Q2_0: 4, F.Q3_K: 8, F.MXFP4: 16, F.NVFP4: 16}[fmt]
     codes = rng.integers(0, hi, size=rows * cols, dtype=np.uint8)
     if fmt == F.MXFP4:
         scales = rng.integers(100, 140, size=nblk, dtype=np.uint8)
+    elif fmt == F.NVFP4:
+        scales = rng.integers(0, 256, size=nblk, dtype=np.uint8)
+        scales[(scales & 0x7F) == 0x7F] = 0x38  # no NaN scale
     else:
         d = np.abs(rng.normal(0, 0.05, size=nblk)).astype(np.float16).view(np.uint8).reshape(nblk, 2)
         if fmt == F.Q3_K:
@@ -121,6 +129,10 @@ def test_pack_rejects_out_of_domain(A):
     with pytest.raises(A.BqeError):
         A.bqe_pack(A.BQE_FMT_MXFP4, 1, 32, np.zeros(32, np.uint8), np.array([255], np.uint8),
                    np.zeros(17, np.uint8))
+    for nan in (0x7F, 0xFF):
+        with pytest.raises(A.BqeError):
+            A.bqe_pack(A.BQE_FMT_NVFP4, 1, 16, np.zeros(16, np.uint8), np.array([nan], np.uint8),
+                       np.zeros(9, np.uint8))
 
 
 def test_status_strings(A):
@@ -164,7 +176,7 @@ def test_argument_checks_before_any_device_work(A):
     assert lib.bqe_workspace_init(None, 16, None) == A.BQE_EINVAL
 
 
-@pytest.mark.parametrize("fmt", [F.TQ1, F.Q2_0, F.Q3_K, F.MXFP4])
+@pytest.mark.parametrize("fmt", [F.TQ1, F.Q2_0, F.Q3_K, F.MXFP4, F.NVFP4])
 def test_unpack_host_inverts_pack(A, fmt):
     """bqe_unpack_host returns the codes and scale bytes bqe_pack was given,
     for every code of the format's domain."""
@@ -172,11 +184,14 @@ def test_unpack_host_inverts_pack(A, fmt):
     rows, cols = 3, 1024
     bw, _ = F.BLOCK[fmt]
     nblk = rows * cols // bw
-    hi = {F.TQ1: 3, F.Q2_0: 4, F.Q3_K: 8, F.MXFP4: 16}[fmt]
+    hi = {F.TQ1: 3, F.Q2_0: 4, F.Q3_K: 8, F.MXFP4: 16, F.NVFP4: 16}[fmt]
     codes = rng.integers(0, hi, size=rows * cols, dtype=np.uint8)
     sb = A_SB[fmt]
     if fmt == F.MXFP4:
         scales = rng.integers(0, 255, size=nblk, dtype=np.uint8)  # 255 (NaN) is not an encodable scale
+    elif fmt == F.NVFP4:
+        scales = rng.integers(0, 256, size=nblk, dtype=np.uint8)
+        scales[(scales & 0x7F) == 0x7F] = 0  # 0x7F / 0xFF (NaN) are not encodable scales
     elif fmt == F.Q3_K:
         d = rng.integers(0, 256, size=(nblk, 2), dtype=np.uint8)
         scales = np.concatenate([rng.integers(0, 64, size=(nblk, 16), dtype=np.uint8), d], axis=1).reshape(-1)
@@ -203,11 +218,11 @@ def test_pool_bytes_layout(A):
     """Pool size = the two tables (uint64 offsets, int32 formats, each rounded
     up to 256 bytes) + every slot's expert bytes rounded up to 256."""
     d = A.desc(5120, 2304, 384, 6)
-    fm = np.array([F.TQ1, F.Q2_0, F.Q3_K, F.MXFP4, F.Q2_0], dtype=np.int32)
+    fm = np.array([F.TQ1, F.Q2_0, F.Q3_K, F.MXFP4, F.Q2_0, F.NVFP4], dtype=np.int32)
     up = lambda v: (v + 255) // 256 * 256  # noqa: E731
-    want = up(8 * 5) + up(4 * 5) + sum(up(synth.expert_bytes(int(f), 5120, 2304)) for f in fm)
+    want = up(8 * 6) + up(4 * 6) + sum(up(synth.expert_bytes(int(f), 5120, 2304)) for f in fm)
     assert A.bqe_pool_bytes(d, fm) == want
-    assert A.bqe_pool_bytes(d, np.array([1, 5], np.int32)) == 0  # unknown format
+    assert A.bqe_pool_bytes(d, np.array([1, 6], np.int32)) == 0  # unknown format
     assert A.bqe_pool_bytes(A.desc(5000, 2304, 384, 6), fm) == 0
 
 

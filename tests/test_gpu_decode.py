@@ -14,7 +14,7 @@ from gpu_util import DeviceLayer, check_out, check_routing, oracle_layer_sampled
 
 pytestmark = pytest.mark.gpu
 
-ALL = [synth.TQ1, synth.Q2_0, synth.Q3_K, synth.MXFP4]
+ALL = [synth.TQ1, synth.Q2_0, synth.Q3_K, synth.MXFP4, synth.NVFP4]
 
 
 @pytest.fixture(scope="module")
@@ -66,6 +66,12 @@ def test_dequant_special_values(dev):
             blk[0, 16] = 0        # 2^-127 (subnormal in fp32)
             blk[1, 16] = 254      # 2^127
             blk[2, :16] = 0x88    # -0.0 codes
+        elif fmt == synth.NVFP4:
+            blk[0, 8] = 0x01      # smallest E4M3 subnormal, 2^-9
+            blk[1, 8] = 0x7E      # largest E4M3, 448
+            blk[2, 8] = 0xFE      # -448
+            blk[3, :8] = 0x88     # -0.0 codes
+            blk[4, 8] = 0x00      # scale +0
         else:
             dpos = {synth.Q2_0: 16, synth.TQ1: 52, synth.Q3_K: 108}[fmt]
             blk[0, dpos:dpos + 2] = (0x01, 0x00)   # smallest fp16 subnormal
@@ -99,7 +105,7 @@ def test_tiny_q2_0_layer(dev, M):
 @pytest.mark.parametrize("M", [1, 2, 3, 5, 6, 8])
 def test_mixed_small_layer(dev, M):
     """All four formats in one layer, selection bias N(0, 0.25), independent rows."""
-    fm = [ALL[(3 * e + 1) % 4] for e in range(24)] + [synth.Q2_0]
+    fm = [ALL[(3 * e + 1) % len(ALL)] for e in range(24)] + [synth.Q2_0]
     L = synth.small_layer(20 + M, fm, 1024, 768, 24, 3, M, bias_std=0.25)
     DL = DeviceLayer(L, dev)
     out, idx, w = DL.forward(L["x"])
@@ -203,7 +209,7 @@ def test_layer_stats(dev):
     """bqe_layer_stats reports the distinct experts the call streamed and
     their bytes, which the oracle's byte count states independently."""
     from bit_quantised_expert_gb300 import _abi as A
-    fm = [ALL[e % 4] for e in range(24)] + [synth.Q2_0]
+    fm = [ALL[e % len(ALL)] for e in range(24)] + [synth.Q2_0]
     L = synth.small_layer(71, fm, 1024, 768, 24, 3, 4, bias_std=0.25)
     DL = DeviceLayer(L, dev)
     _, idx, _ = DL.forward(L["x"])
@@ -213,7 +219,7 @@ def test_layer_stats(dev):
     assert st["rows"] == 4 and st["experts_streamed"] == len(distinct) + 1
     assert st["expert_bytes"] == O.expert_bytes_streamed(idx, L["fmts"], 1024, 768, 24)
     assert st["router_bytes"] == 24 * 1024 * 4
-    per = [0] * 5
+    per = [0] * 6
     for e in distinct | {24}:
         per[int(L["fmts"][e])] += 1
     assert st["per_format"] == per

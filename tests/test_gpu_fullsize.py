@@ -67,6 +67,14 @@ def test_fp4_layer(dev, M):
         _check_layer(W, dev, M, xi)
 
 
+@pytest.mark.parametrize("M", [1, 6])
+def test_nvfp4_layer(dev, M):
+    """The NVFP4 variant (blocks of 16 with E4M3 scales) at full size."""
+    from synth import workloads as WL
+    W = WL.fp4_layer(dev, seed=5, m=M, n_x=2, fmt=synth.NVFP4)
+    _check_layer(W, dev, M, 0)
+
+
 @pytest.mark.parametrize("M", [1, 6, 8])
 def test_mixed_layer(dev, M):
     from synth import workloads as WL

@@ -19,7 +19,7 @@ from gpu_util import DeviceLayer, check_out, check_routing, torch_dev
 pytestmark = pytest.mark.gpu
 
 PF_TOL = 5e-3
-ALL = [synth.TQ1, synth.Q2_0, synth.Q3_K, synth.MXFP4]
+ALL = [synth.TQ1, synth.Q2_0, synth.Q3_K, synth.MXFP4, synth.NVFP4]
 
 
 @pytest.fixture(scope="module")
@@ -79,7 +79,7 @@ def test_prefill_tiny_q2_0(dev, T):
 @pytest.mark.parametrize("T", [129, 700])
 def test_prefill_mixed_formats_with_bias(dev, T):
     E = 16
-    fm = [ALL[e % 4] for e in range(E)] + [synth.Q3_K]
+    fm = [ALL[e % len(ALL)] for e in range(E)] + [synth.Q3_K]
     L = synth.small_layer(31, fm, 512, 512, E, 3, T, bias_std=0.25)
     check_all(L, DeviceLayer(L, dev), L["x"])
 

@@ -59,6 +59,7 @@ def same_bits(a, b):
     ("mxfp4.txt", F.dequant_mxfp4, 32),
     ("q2_0.txt", F.dequant_q2_0, 64),
     ("tq1.txt", F.dequant_tq1, 256),
+    ("nvfp4.txt", F.dequant_nvfp4, 16),
 ])
 def test_golden_blocks(name, fn, nw):
     cases = read_golden(name)
@@ -93,6 +94,32 @@ def test_e2m1_every_code_and_exponent():
             m = mags[c & 7] * math.ldexp(1.0, E - 127)
             want = -m if c & 8 else m
             assert same_bits(got[c], np.full(32, want)), (E, c)
+
+
+def test_e4m3_every_byte_against_torch():
+    """All 256 E4M3 scale bytes against PyTorch's float8_e4m3fn conversion."""
+    import torch
+    b = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = F.e4m3_to_f64(b)
+    fin = np.isfinite(ref)
+    assert same_bits(got[fin], ref[fin])
+    assert np.array_equal(np.isnan(got), np.isnan(ref)) and int(np.isnan(got).sum()) == 2
+
+
+def test_nvfp4_every_code_and_scale():
+    """Each code times each finite scale: the product of the two definitions."""
+    e2m1 = F.e2m1_to_f64(np.arange(16))
+    for sb in range(256):
+        if sb in (0x7F, 0xFF):
+            continue
+        blk = np.zeros((2, 9), dtype=np.uint8)
+        blk[0, :8] = [0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE]
+        blk[1, :8] = [0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE]
+        blk[:, 8] = sb
+        got = F.dequant_nvfp4(blk)
+        sc = F.e4m3_to_f64(np.array([sb], np.uint8))[0]
+        assert same_bits(got[0], e2m1 * sc), sb
 
 
 def test_ternary_all_243_bytes():
