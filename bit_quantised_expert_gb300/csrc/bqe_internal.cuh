@@ -154,13 +154,15 @@ struct WsLayout {
   // logits; the layer input as f16 x 2^s (per-row s) in the natural, P and T
   // orders; the diagnostic counters
   uint64_t z, xh, xp, xt, dbg;
-  // single-kernel decode layer: (selection key, logit) of every (row, expert)
-  uint64_t zk;
-  // single-kernel decode layer (k_moe): call epoch, logits arrival counter,
-  // per work-list expert the counts of its W1/W3 items done and of its h
-  // units written; per "row slot" (an expert's r-th row; M (K + 1) slots at
-  // most) the K-chunk partials of g/u and the f16 records of h (h16_rec_bytes)
-  uint64_t epoch, zt, m_ca, m_ch, m_pa, m_hr;
+  // single-kernel decode layer: of every (row, expert) the selection key and
+  // the logit, each tagged with the call's epoch (value << 32 | tag)
+  uint64_t zk, zl;
+  // single-kernel decode layer (k_moe): call epoch, staged-input arrival
+  // counter, per work-list expert the counts of its W1/W3 items done and of
+  // its h units written; per "row slot" (an expert's r-th row; M (K + 1)
+  // slots at most) the K-chunk partials of g/u and the f16 records of h
+  // (h16_rec_bytes)
+  uint64_t epoch, st, m_ca, m_ch, m_pa, m_hr;
   uint64_t total;
 };
 constexpr int kDbgSlots = 8;      // per-CTA counters of the diagnostic mode
@@ -187,10 +189,12 @@ __host__ __device__ inline WsLayout make_ws(const Geo& g) {
   w.xp = o; o = al256(o + 2ull * g.M * g.H);   // the same in P order
   w.xt = o; o = al256(o + 2ull * g.M * (g.H / 256) * 288);  // ... and in T order
   w.dbg = o; o = al256(o + 8ull * 3 * kDbgMaxCtas * kDbgSlots);
+  // the tagged keys, the logits, the call epoch and the counters are
+  // contiguous: [zk, m_pa) clears them
   w.zk = o; o = al256(o + 8ull * g.M * g.E);
-  // the call epoch and the counters are contiguous: [epoch, m_pa) clears them
+  w.zl = o; o = al256(o + 8ull * g.M * g.E);
   w.epoch = o; o = al256(o + 16);
-  w.zt = o; o = al256(o + 16);                                     // logits arrival counter (64-bit)
+  w.st = o; o = al256(o + 16);                                     // staged-input arrival counter (64-bit)
   w.m_ca = o; o = al256(o + 4ull * kMaxU);                         // W1/W3 items done, per expert
   w.m_ch = o; o = al256(o + 4ull * kMaxU);                         // h units written, per expert
   const uint64_t nrs = (uint64_t)g.M * (g.K + 1);

@@ -12,11 +12,15 @@
 //     forms h = silu(g) * u;
 //   * before the routing is known, the producers stream this CTA's share of
 //     the shared expert's W1/W3 (always used), while the compute warps read
-//     this CTA's rows of the router (z = x Wr^T, fp32), publish (key, z) of
-//     those experts tagged with the call's epoch, and wait until every CTA's
-//     logits are in; then warp m selects row m's top-k from registers and
+//     this CTA's rows of the router (z = x Wr^T, fp32) as soon as they land
+//     and publish the selection key and z of those experts, each as a 64-bit
+//     word tagged with the call's epoch; warp m reads row m's keys until
+//     every tag is this call's and selects its top-k from registers, while
+//     the other compute warps stage this CTA's slice of the f16 input copies
+//     (published on a counter, for the producers' activation copies); then
 //     warp 0 builds the work list, the row slots and the item templates (the
-//     same result in every CTA: no serial tail, no second kernel);
+//     same result in every CTA: no serial tail, no second kernel), and the h
+//     warp the mixing weights, off the critical path;
 //   * work items are (expert, 32-row panel, K chunk) of W1 and W3, then
 //     (expert, group of W2 output panels, K chunk) of W2, shared expert first,
 //     dealt round-robin over the CTAs, so every expert's W1/W3 is finished by
@@ -89,6 +93,14 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const void* p) {
 }
 __device__ __forceinline__ void st_release_u64(void* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const void* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(void* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ float silu_m(float t) { return t / (1.0f + expf(-t)); }
@@ -197,6 +209,20 @@ __device__ inline void make_tpl(const MoeParams& P, ItemTpl& T, int ph, int u, i
   }
 }
 
+// The template of an expert from its format's template (made for expert 0,
+// address 0, no rows, row slot 0): the fields that depend on those.
+__device__ inline void patch_tpl(const MoeParams& P, ItemTpl& T, const ItemTpl& B, int ph, int u, uint64_t addr,
+                                 int R, int rb) {
+  const Geo& g = P.g;
+  T = B;
+  T.h.u = (int16_t)u;
+  T.h.R = (int16_t)R;
+  T.h.red = B.h.act + al128((uint32_t)R * B.h.astr);
+  T.size = T.h.red + (uint32_t)(ph ? P.PB * g.GB : 2 * g.GA) * R * 32 * 4;
+  T.wsrc = addr + (ph ? 2 * (uint64_t)B.m13 : 0);
+  if (ph) T.act_base = B.act_base + (uint32_t)rb * B.act_rs;
+}
+
 template <int RC>
 __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
   const Geo& g = P.g;
@@ -207,16 +233,14 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
   int32_t* err = (int32_t*)(P.ws + P.L.err);
 
   extern __shared__ __align__(128) uint8_t dsm[];
-  float* s_z = reinterpret_cast<float*>(dsm);                       // M x E logits
-  uint8_t* ring = dsm + ((4u * M * E + 127u) & ~127u);
+  uint8_t* ring = dsm;
   const uint16_t* s_x = reinterpret_cast<const uint16_t*>(ring + P.xstage_off);  // M x H bf16 (startup only)
   const float* s_rw = reinterpret_cast<const float*>(ring + P.rt_off);  // this CTA's router rows (startup only)
 
   __shared__ ItemHdr hdr[kNQ];
-  __shared__ __align__(8) uint64_t full[kNQ], cons[kNQ], freed[kNQ], route_bar, rbar, lbar;
+  __shared__ __align__(8) uint64_t full[kNQ], cons[kNQ], freed[kNQ], route_bar, rbar, wbar;
   __shared__ float s_rsw[kMaxM * (kMaxTopK + 1)];  // mixing weight of each row slot (shared expert: 1)
   __shared__ int s_rbase[kMaxU + 1];   // first row slot of each work-list expert
-  __shared__ int s_rs[kMaxM][kMaxTopK];  // row slot of (row m, choice j)
   __shared__ int s_done[kNQ];
   __shared__ int32_t s_ufmt[kMaxU], s_unrows[kMaxU];
   __shared__ uint64_t s_uaddr[kMaxU];
@@ -245,6 +269,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
   __shared__ volatile int s_oldest;    // oldest item not yet known to be freed
   __shared__ volatile int s_npre;      // items pre-issued before the routing (-1: not yet known)
   __shared__ ItemTpl s_tpl[2][kMaxU];
+  __shared__ ItemTpl s_tbase[2][8];  // per (phase, format): the template of expert 0 at address 0, no rows
 
   const uint32_t tag = *(volatile const uint32_t*)(P.ws + P.L.epoch) + 1u;
   if (tid == 0) {
@@ -256,7 +281,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     }
     mbar_init(&route_bar, 1);
     mbar_init(&rbar, 1);
-    mbar_init(&lbar, 1);
+    mbar_init(&wbar, 1);
     s_abort = 0;
     for (int q = 0; q < kNP; ++q) s_issued[q] = 0;
     s_turn = 0;
@@ -422,10 +447,26 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         while (s_npre < 0 && globaltimer_ns() - t0 < P.limit_ns) __nanosleep(32);
       }
       const int npre = max(0, (int)s_npre);
-      // ---- the pre-issued items' x rows: every CTA's staged slices of x are
-      // published once all logits are in, well before the routing is known
-      // (copied on a failed wait too: the addresses are valid, the stage drains)
-      if (!mwait(&lbar, 0, P.limit_ns, err)) ok = false;
+      // ---- the pre-issued items' x rows, once every CTA has published its
+      // staged slices of x (well before the routing is known; copied on a
+      // failed wait too: the addresses are valid, the stage drains)
+      {
+        unsigned long long* scnt = (unsigned long long*)(P.ws + P.L.st);
+        const unsigned long long target = (unsigned long long)G * tag;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_u64(scnt) < target) {
+          __nanosleep(64);
+          if (*(volatile const int32_t*)err) {
+            ok = false;
+            break;
+          }
+          if (globaltimer_ns() - t0 > P.limit_ns) {
+            set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+            ok = false;
+            break;
+          }
+        }
+      }
       fence_proxy_async_global();  // the staged inputs of every CTA are read by bulk copies below
       for (int i = pp; i < npre; i += kNP) {
         issue(i, sh, hdr[i % kNQ].p, hdr[i % kNQ].c, false, true, true);
@@ -570,50 +611,23 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       uint4* dst = reinterpret_cast<uint4*>(xs);
       for (int i = ct; i < M * H / 8; i += NCT) dst[i] = src[i];
     }
-    named_bar_sync(1, NCT);
-    if (P.diag && ct == 0) dacc(P, 0, globaltimer_ns() - t_cta0, 0);
-    // per-row scale: s puts the row's largest |x| in [2^14, 2^15) for the f16
-    // copy and in [2^13, 2^14) for the integer records (every CTA derives the same)
-    for (int m = 0; m < M; ++m) {
-      uint32_t mx = 0;
-      for (int k = ct; k < H; k += NCT) mx = max(mx, (uint32_t)(xs[m * H + k] & 0x7FFFu));
-      for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      if (lane == 0 && mx) atomicMax(&s_emax[m], (int)(mx >> 7) - 127);
+    // the slot descriptors of the experts (the loads only; checked after the
+    // logits are out, so their latency overlaps the router dot products)
+    int sf0 = 0, sf1 = 0;
+    uint64_t so0 = 0, so1 = 0;
+    const bool sv0 = sl0 >= 0 && sl0 < P.pool.n_slots, sv1 = sl1 >= 0 && sl1 < P.pool.n_slots;
+    if (sv0) {
+      sf0 = P.pool.slot_fmt[sl0];
+      so0 = P.pool.slot_off[sl0];
     }
-    named_bar_sync(1, NCT);
-    if (ct < M) s_xsc[ct] = ldexpf(1.0f, -(s_emax[ct] == -1000 ? 0 : 14 - s_emax[ct]));
-    // ---- this CTA's slice of the staged copies of the input (read by every CTA's bulk copies)
-    {
-      uint16_t* xh = (uint16_t*)(P.ws + P.L.xh);
-      const int n = M * H, per = (n + G - 1) / G, lo = min(n, per * cta), hi = min(n, lo + per);
-      uint16_t* xp = (uint16_t*)(P.ws + P.L.xp);
-      for (int i = lo + ct; i < hi; i += NCT) {
-        const int m = i / H;
-        const float v = __uint_as_float((uint32_t)xs[i] << 16);
-        const int sh = s_emax[m] == -1000 ? 0 : 14 - s_emax[m];
-        const uint16_t hv = __half_as_ushort(__float2half_rn(ldexpf(v, sh)));
-        xh[i] = hv;
-        xp[(i & ~15) + p16_pos(i & 15)] = hv;  // P order
-        if (P.t_out) P.t_out[i] = xs[i];
-      }
-      {  // T order: 288 positions per 256 columns, 32 of them zero
-        uint16_t* xt = (uint16_t*)(P.ws + P.L.xt);
-        const int nt = M * (H / 256) * 288, pt = (nt + G - 1) / G, tlo = min(nt, pt * cta), thi = min(nt, tlo + pt);
-        for (int i = tlo + ct; i < thi; i += NCT) {
-          const int run = i / 288, pos = i - run * 288, m = run / (H / 256);
-          const int col = t16_col(pos);
-          uint16_t hv = 0;
-          if (col >= 0) {
-            const float v = __uint_as_float((uint32_t)xs[run * 256 + col] << 16);
-            hv = __half_as_ushort(__float2half_rn(ldexpf(v, s_emax[m] == -1000 ? 0 : 14 - s_emax[m])));
-          }
-          xt[i] = hv;
-        }
-      }
+    if (sv1) {
+      sf1 = P.pool.slot_fmt[sl1];
+      so1 = P.pool.slot_off[sl1];
     }
     // ---- this CTA's slice of the output (zero unless the call accumulates)
-    // and, in CTA 0, the per-expert counters of the call: both written before
-    // this CTA publishes its logits, so before any other CTA adds to them
+    // and, in CTA 0, the per-expert counters of the call: released with this
+    // CTA's staged slices of the input, which every CTA acquires before its
+    // first item, so before any other CTA adds to them
     if (!P.accumulate) {
       const int n = M * H, per = (n + G - 1) / G, lo = min(n, per * cta), hi = min(n, lo + per);
       for (int i = lo + ct; i < hi; i += NCT) P.out[i] = 0.f;
@@ -622,9 +636,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       ((unsigned int*)(P.ws + P.L.m_ca))[ct] = 0u;
       ((unsigned int*)(P.ws + P.L.m_ch))[ct] = 0u;
     }
-    // ---- selection inputs: the bias, the forced choices (validated), and the
-    // slot descriptor of every expert (e = E: the shared one), into shared
-    // memory so that none of these loads waits until after the routing
+    // ---- selection inputs: the bias and the forced choices (validated)
     if (ct < E) s_bias[ct] = bias0;
     if (P.forced && ct < M * K) {
       int f = fidx0;
@@ -635,36 +647,10 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       }
       s_fidx[ct / K][ct % K] = f;
     }
-    auto slot_desc = [&](int e, int slot) {
-      int fmt = 0, bad = 0;
-      uint64_t addr = 0;
-      if (slot < 0 || slot >= P.pool.n_slots) {
-        bad = kErrSlotRange;
-      } else {
-        const int f = P.pool.slot_fmt[slot];
-        const uint64_t off = P.pool.slot_off[slot];
-        if (!fmt_ok(f)) {
-          bad = kErrSlotFmt;
-        } else if ((off & 15) || off + 2 * matrix_bytes(f, I, H) + matrix_bytes(f, H, I) > P.pool.base_bytes) {
-          bad = kErrSlotExtent;
-        } else {
-          fmt = f;
-          addr = (uint64_t)P.pool.base + off;
-        }
-      }
-      s_eslot[e] = (int16_t)slot;
-      s_efmt[e] = (uint8_t)fmt;
-      s_eaddr[e] = addr;
-      s_ebad[e] = (uint8_t)bad;
-    };
-    if (ct <= E) slot_desc(ct, sl0);
-    if (ct + NCT <= E) slot_desc(ct + NCT, sl1);
-    // the staged slices are read by other CTAs' bulk copies once the routing
-    // is known: fence them now, while the router rows are still landing
-    // (the gpu-scope release is the CTA's arrival on the logits counter below)
-    fence_proxy_async_global();
-    if (P.diag && ct == 0) dacc(P, 1, globaltimer_ns() - t_cta0, 0);
-    uint2* zk = (uint2*)(P.ws + P.L.zk);
+    named_bar_sync(1, NCT);
+    if (P.diag && ct == 0) dacc(P, 0, globaltimer_ns() - t_cta0, 0);
+    unsigned long long* zk = (unsigned long long*)(P.ws + P.L.zk);
+    unsigned long long* zl = (unsigned long long*)(P.ws + P.L.zl);
     // ---- router dot products of this CTA's experts (rows landed in shared memory)
     {
       const bool okr = __all_sync(0xffffffffu, mwait(&rbar, 0, P.limit_ns, err));
@@ -698,75 +684,179 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       }
 #pragma unroll
       for (int m = 0; m < kMaxM; ++m) {
-        float v = acc[m];
-        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0 && rtask && m < M) s_part[cw][m] = v;
+        if (m < M) {
+          float v = acc[m];
+          for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0 && rtask) s_part[cw][m] = v;
+        }
       }
     }
     named_bar_sync(1, NCT);  // logits partials of this CTA are in shared memory
+    // publish the selection key (the bias only steers the choice) and the
+    // logit, each in one 64-bit word with the call's epoch as its tag: a
+    // reader that sees the tag has the value, so no fence is needed here
     if (ct < nexp * M) {
-      // the logit and its selection key (the bias only steers the choice)
       const int j = ct / M, m = ct % M, e = cta + j * G;
       const float zv = (s_part[4 * j][m] + s_part[4 * j + 1][m]) + (s_part[4 * j + 2][m] + s_part[4 * j + 3][m]);
-      zk[(size_t)m * E + e] = make_uint2(sel_key(zv, s_bias[e]), __float_as_uint(zv));
+      st_relaxed_u64(zk + (size_t)m * E + e, ((unsigned long long)sel_key(zv, s_bias[e]) << 32) | tag);
+      st_relaxed_u64(zl + (size_t)m * E + e, ((unsigned long long)__float_as_uint(zv) << 32) | tag);
     }
-    named_bar_sync(1, NCT);
-    // publish: one arrival per CTA on the call's logits counter (monotonic:
-    // G per call), released after this CTA's logits and staged slices; then
-    // wait (bounded) until every CTA has arrived, and read all logits
-    unsigned long long* zcnt = (unsigned long long*)(P.ws + P.L.zt);
     if (ct == 0) {
-      asm volatile("fence.acq_rel.gpu;" ::: "memory");
-      atomicAdd(zcnt, 1ull);
       mstamp(P, kStZPub, true);
       if (P.diag) dacc(P, 2, globaltimer_ns() - t_cta0, 1);
-      const unsigned long long target = (unsigned long long)G * tag;
-      const uint64_t t0 = globaltimer_ns();
-      bool okz = true;
-      while (ld_acquire_u64(zcnt) < target) {
-        __nanosleep(32);
-        if (globaltimer_ns() - t0 > P.limit_ns || *(volatile const int32_t*)err) {
-          okz = false;
-          break;
+    }
+    // ---- the slot descriptor of every expert (e = E: the shared one), into
+    // shared memory, so that no load waits after the routing
+    auto slot_desc = [&](int e, int slot, bool valid, int f, uint64_t off) {
+      int fmt = 0, bad = 0;
+      uint64_t addr = 0;
+      if (!valid) {
+        bad = kErrSlotRange;
+      } else if (!fmt_ok(f)) {
+        bad = kErrSlotFmt;
+      } else if ((off & 15) || off + 2 * matrix_bytes(f, I, H) + matrix_bytes(f, H, I) > P.pool.base_bytes) {
+        bad = kErrSlotExtent;
+      } else {
+        fmt = f;
+        addr = (uint64_t)P.pool.base + off;
+      }
+      s_eslot[e] = (int16_t)slot;
+      s_efmt[e] = (uint8_t)fmt;
+      s_eaddr[e] = addr;
+      s_ebad[e] = (uint8_t)bad;
+    };
+    if (ct <= E) slot_desc(ct, sl0, sv0, sf0, so0);
+    if (ct + NCT <= E) slot_desc(ct + NCT, sl1, sv1, sf1, so1);
+    // While warps 0 .. M-1 wait for the logits of every CTA and select, the
+    // other compute warps write this CTA's slice of the staged copies of the
+    // input (read by every CTA's bulk copies) and publish it on a second
+    // counter; both groups then meet before the work list is built (which
+    // takes the staging warps' per-format templates).
+    unsigned long long* scnt = (unsigned long long*)(P.ws + P.L.st);
+    if (cw >= M) {
+      const int sct = ct - 32 * M, NST = NCT - 32 * M;
+      // per-row scale: s puts the row's largest |x| in [2^14, 2^15) for the f16
+      // copy and in [2^13, 2^14) for the integer records (every CTA derives the same)
+      {
+        uint32_t mx[kMaxM];
+#pragma unroll
+        for (int m = 0; m < kMaxM; ++m) mx[m] = 0;
+        for (int k = sct; k < H; k += NST)
+#pragma unroll
+          for (int m = 0; m < kMaxM; ++m)
+            if (m < M) mx[m] = max(mx[m], (uint32_t)(xs[m * H + k] & 0x7FFFu));
+#pragma unroll
+        for (int m = 0; m < kMaxM; ++m) {
+          if (m < M) {
+            uint32_t v = mx[m];
+            for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0 && v) atomicMax(&s_emax[m], (int)(v >> 7) - 127);
+          }
         }
       }
-      if (!okz) {
-        set_error(err, BQE_ETIMEOUT, kErrWaitFull);
-        s_abort = 1;
+      named_bar_sync(3, NST);
+      if (sct < M) s_xsc[sct] = ldexpf(1.0f, -(s_emax[sct] == -1000 ? 0 : 14 - s_emax[sct]));
+      {
+        uint16_t* xh = (uint16_t*)(P.ws + P.L.xh);
+        const int n = M * H, per = (n + G - 1) / G, lo = min(n, per * cta), hi = min(n, lo + per);
+        uint16_t* xp = (uint16_t*)(P.ws + P.L.xp);
+        for (int i = lo + sct; i < hi; i += NST) {
+          const int m = i / H;
+          const float v = __uint_as_float((uint32_t)xs[i] << 16);
+          const int sh = s_emax[m] == -1000 ? 0 : 14 - s_emax[m];
+          const uint16_t hv = __half_as_ushort(__float2half_rn(ldexpf(v, sh)));
+          xh[i] = hv;
+          xp[(i & ~15) + p16_pos(i & 15)] = hv;  // P order
+          if (P.t_out) P.t_out[i] = xs[i];
+        }
+        {  // T order: 288 positions per 256 columns, 32 of them zero
+          uint16_t* xt = (uint16_t*)(P.ws + P.L.xt);
+          const int nt = M * (H / 256) * 288, pt = (nt + G - 1) / G, tlo = min(nt, pt * cta), thi = min(nt, tlo + pt);
+          for (int i = tlo + sct; i < thi; i += NST) {
+            const int run = i / 288, pos = i - run * 288, m = run / (H / 256);
+            const int col = t16_col(pos);
+            uint16_t hv = 0;
+            if (col >= 0) {
+              const float v = __uint_as_float((uint32_t)xs[run * 256 + col] << 16);
+              hv = __half_as_ushort(__float2half_rn(ldexpf(v, s_emax[m] == -1000 ? 0 : 14 - s_emax[m])));
+            }
+            xt[i] = hv;
+          }
+        }
       }
-      if (P.diag) dacc(P, 2, globaltimer_ns() - t_cta0, 0);
-      rstamp(P, 0, t_cta0);
-      mbar_arrive(&lbar);  // the producers may copy staged rows of other CTAs
+      // the item template of every (phase, format), for expert 0 at address 0
+      // with no rows (the work list's templates are these with a few fields changed)
+      if (sct < 16) {
+        const int ph = sct & 1, f = sct >> 1;
+        if (fmt_ok(f)) make_tpl(P, s_tbase[ph][f], ph, 0, f, 0ull, 0, 0);
+      }
+      // the slices are read by bulk copies (async proxy) of every CTA; their
+      // release also covers the output slice and counters zeroed above
+      fence_proxy_async_global();
+      named_bar_sync(3, NST);
+      if (sct == 0) {
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        atomicAdd(scnt, 1ull);
+        if (P.diag) dacc(P, 1, globaltimer_ns() - t_cta0, 0);
+      }
     }
-    named_bar_sync(1, NCT);
     // ---- the routing: per-row selection (warp m takes row m), then warp 0
     // builds the work list, the row slots and the item templates
     const bool forced = P.forced != nullptr;
     if (cw < M) {
-      if (!s_abort) {
-        // Expert e's rank value is (key << 32) | ~e: keys descending, ties to
-        // the lower id, every value distinct.  Round j takes the largest value
-        // below round j - 1's winner (a tree over the lane's values, then the
-        // warp), so the values stay in registers.
-        const int m = cw;
-        constexpr int QN = kMaxEM / 32;
-        uint64_t vv[QN];
-        // every load issued before any is used (one round trip)
+      // Expert e's rank value is (key << 32) | ~e: keys descending, ties to
+      // the lower id, every value distinct.  Round j takes the largest value
+      // below round j - 1's winner (a tree over the lane's values, then the
+      // warp), so the values stay in registers.
+      const int m = cw;
+      constexpr int QN = kMaxEM / 32;
+      uint64_t vv[QN];
+      {
+        // row m's tagged key of every expert, read until each carries this
+        // call's tag (bounded): every CTA publishes its own as soon as its
+        // logits are out, so the last one arrives one round trip before it
+        // is seen here; only the keys not yet seen are read again
+        uint32_t need = 0;
 #pragma unroll
         for (int q = 0; q < QN; ++q) {
-          const int e = min(lane + 32 * q, E - 1);
-          const uint2 t = __ldcg(zk + (size_t)m * E + e);
-          vv[q] = ((uint64_t)t.x << 32) | t.y;
+          vv[q] = 0ull;
+          if (lane + 32 * q < E) need |= 1u << q;
         }
+        const uint64_t t0 = globaltimer_ns();
+        bool okz = true;
+        for (int spin = 0;; ++spin) {
+#pragma unroll
+          for (int q = 0; q < QN; ++q)
+            if (need & (1u << q)) vv[q] = ld_relaxed_u64(zk + (size_t)m * E + lane + 32 * q);
+#pragma unroll
+          for (int q = 0; q < QN; ++q)
+            if ((need & (1u << q)) && (uint32_t)vv[q] == tag) need &= ~(1u << q);
+          if (!__any_sync(0xffffffffu, need != 0u)) break;
+          if (s_abort || globaltimer_ns() - t0 > P.limit_ns ||
+              ((spin & 15) == 15 && *(volatile const int32_t*)err)) {
+            okz = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+        okz = __all_sync(0xffffffffu, okz);
+        if (!okz && lane == 0) {
+          set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+          s_abort = 1;
+        }
+      }
+      if (ct == 0) {
+        if (P.diag) dacc(P, 2, globaltimer_ns() - t_cta0, 0);
+        rstamp(P, 0, t_cta0);
+        rstamp(P, 1, t_cta0);
+      }
+      if (!s_abort) {
 #pragma unroll
         for (int q = 0; q < QN; ++q) {
           const int e = lane + 32 * q;
-          if (e < E) s_z[m * E + e] = __uint_as_float((uint32_t)vv[q]);
           vv[q] = (e < E && !forced) ? ((vv[q] & 0xFFFFFFFF00000000ull) | (uint32_t)~e) : 0ull;
         }
-        __syncwarp();
-        if (ct == 0) rstamp(P, 1, t_cta0);
-        // lane j keeps round j's winner; the bookkeeping (choice, logit, the
+        // lane j keeps round j's winner; the bookkeeping (choice, the
         // expert's row mask and first choice) is done after the rounds, by
         // lanes 0 .. K-1 at once, so no round waits on shared memory
         int mine = 0;
@@ -792,35 +882,18 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
             if (lane == j) mine = last ? (int)~lo : 0;
           }
         }
-        float zz = 0.f;
         if (lane < K) {
           s_idx[m][lane] = mine;
-          zz = s_z[m * E + mine];
-          s_zsel[m][lane] = zz;
           atomicOr(&s_mask[mine], 1u << m);
           atomicMin(&s_first[mine], m * K + lane);
         }
         __syncwarp();
         if (ct == 0) rstamp(P, 2, t_cta0);
-        // w_j = s_j / sum s as exp(log s_j - max log s) / sum exp(...): finite
-        // even when every selected sigmoid underflows in fp32
-        float ls = -INFINITY;
-        if (lane < K) ls = zz < 0.f ? zz - log1pf(expf(zz)) : -log1pf(expf(-zz));
-        float mx = ls;
-        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        const float ev = lane < K ? expf(ls - mx) : 0.f;
-        float tot = ev;
-        for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-        if (lane < K) {
-          const float w = ev / tot;
-          s_cw[m][lane] = w;
-          if (cta == 0) {
-            if (P.topk_idx) P.topk_idx[m * K + lane] = mine;
-            if (P.topk_w) P.topk_w[m * K + lane] = w;
-          }
-        }
       }
-      if (M > 1) named_bar_sync(2, 32 * M);  // every row's choices are in
+    }
+    // every row's choices, the slot descriptors and the per-row scales are in
+    named_bar_sync(1, NCT);
+    {
       if (cw == 0) {
         if (lane == 0) {
           mstamp(P, kStRouted, false);
@@ -890,6 +963,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         const int ex = incl - n0 - n1;
         if (u0 <= tot + 1) s_rbase[u0] = ex;
         if (u1 <= tot + 1) s_rbase[u1] = ex + n0;
+        // the per-format templates (h warp), needed below
+        __syncwarp();
         // on an invalid routed slot only the shared expert runs (the call
         // reports the error; its output is undefined); an invalid shared slot
         // or an aborted routing streams nothing
@@ -899,29 +974,13 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           if (cta == 0) *(int32_t*)(P.ws + P.L.nu) = nu;
         }
         __syncwarp();
-        // row slot of each (row, choice), and each row slot's mixing weight
-        // (the sum over the row's choices of that expert; shared expert: 1)
-        if (lane < M) s_rsw[lane] = 1.0f;
-        if (nu > 1)
-          for (int t = lane; t < M * K; t += 32) {
-            const int m = t / K, j = t - (t / K) * K;
-            const int ee = s_idx[m][j];
-            const int rs = s_rbase[s_uof[ee]] + __popc(s_mask[ee] & ((1u << m) - 1u));
-            s_rs[m][j] = rs;
-            bool fj = true;
-            float w = 0.f;
-            for (int j2 = 0; j2 < K; ++j2)
-              if (s_idx[m][j2] == ee) {
-                fj = fj && j2 >= j;
-                w += s_cw[m][j2];
-              }
-            if (fj) s_rsw[rs] = w;
-          }
         if (lane == 0) rstamp(P, 5, t_cta0);
-        // item templates of every (phase, work-list expert)
+        // item templates of every (phase, work-list expert): the format's
+        // template (made by the staging warps) with the expert's address, rows and
+        // first row slot
         for (int t = lane; t < 2 * nu; t += 32) {
-          const int ph = t & 1, u = t >> 1;
-          if (fmt_ok(s_ufmt[u])) make_tpl(P, s_tpl[ph][u], ph, u, s_ufmt[u], s_uaddr[u], s_unrows[u], s_rbase[u]);
+          const int ph = t & 1, u = t >> 1, f = s_ufmt[u];
+          if (fmt_ok(f)) patch_tpl(P, s_tpl[ph][u], s_tbase[ph][f], ph, u, s_uaddr[u], s_unrows[u], s_rbase[u]);
         }
         __syncwarp();
         if (lane == 0) {
@@ -1045,7 +1104,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     // row slot, rows, scales, mixing weights) only when the expert changes,
     // and all partials of a row are loaded before any is added.
     ItemHdr hn;
-    bool have = false;
+    bool have = false, wready = false;
     int eu = -1, eph = -1, erb = 0;
     int erow[kMaxM];
     float esc[kMaxM];
@@ -1063,6 +1122,16 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       }
       const ItemHdr h = hn;
       const int u = h.u, R = RC == 1 ? 1 : h.R;
+      if (h.phase == 1 && !wready) {  // the mixing weights (h warp) before the first W2 item
+        if (!__all_sync(0xffffffffu, mwait(&wbar, 0, P.limit_ns, err)) || s_abort) {
+          if (lane == 0) {
+            set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+            s_abort = 1;
+          }
+          break;
+        }
+        wready = true;
+      }
       if (u != eu || h.phase != eph) {  // this expert's row slots, rows and scales
         eu = u;
         eph = h.phase;
@@ -1144,10 +1213,81 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     // fp32 (MXFP4 W2 loops) or as integer records (X_hi + X_lo / 128 of
     // h 2^si, max |h| 2^si in [2^13, 2^14), in the expert's format order, with
     // the 16-column sums and 2^-si); then release the expert's count of units.
+    // ---- first, while the routing runs: the item template of every (phase,
+    // format), for expert 0 at address 0 with no rows (the work list's
+    // templates are these with a few fields changed)
     const bool ok0 = __all_sync(0xffffffffu, mwait(&route_bar, 0, P.limit_ns, err));
     const int nU = ok0 ? s_nu : 0;
     const int nrs = nU > 0 ? s_rbase[nU] : 0;
     const int nblk = I / 256, nunits = nrs * nblk;
+    // ---- the mixing weights, off the routing's critical path (the reducer
+    // waits for them before its first W2 item): w_j = s_j / sum s over row m's
+    // choices as exp(log s_j - max log s) / sum exp(...), finite even when
+    // every selected sigmoid underflows in fp32; then each row slot's weight
+    // (the sum over the row's choices of that expert; shared expert rows: 1)
+    if (ok0 && !s_abort) {
+      // the selected logits, read until each carries this call's tag
+      // (bounded; their keys were seen, so they are normally there)
+      const unsigned long long* zl = (const unsigned long long*)(P.ws + P.L.zl);
+      bool okl = true;
+      for (int t = lane; t < M * K && okl; t += 32) {
+        const unsigned long long* a = zl + (size_t)(t / K) * E + s_idx[t / K][t % K];
+        const uint64_t t0 = globaltimer_ns();
+        unsigned long long v = ld_relaxed_u64(a);
+        while ((uint32_t)v != tag) {
+          if (globaltimer_ns() - t0 > P.limit_ns || *(volatile const int32_t*)err) {
+            okl = false;
+            break;
+          }
+          __nanosleep(64);
+          v = ld_relaxed_u64(a);
+        }
+        s_zsel[t / K][t % K] = __uint_as_float((uint32_t)(v >> 32));
+      }
+      if (!okl) {
+        set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+        s_abort = 1;
+      }
+      __syncwarp();
+      for (int m = 0; m < M; ++m) {
+        float ls = -INFINITY;
+        if (lane < K) {
+          const float zz = s_zsel[m][lane];
+          ls = zz < 0.f ? zz - log1pf(expf(zz)) : -log1pf(expf(-zz));
+        }
+        float mx = ls;
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float ev = lane < K ? expf(ls - mx) : 0.f;
+        float tot = ev;
+        for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (lane < K) {
+          const float w = ev / tot;
+          s_cw[m][lane] = w;
+          if (cta == 0) {
+            if (P.topk_idx) P.topk_idx[m * K + lane] = s_idx[m][lane];
+            if (P.topk_w) P.topk_w[m * K + lane] = w;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane < M) s_rsw[lane] = 1.0f;
+      if (nU > 1)
+        for (int t = lane; t < M * K; t += 32) {
+          const int m = t / K, j = t - (t / K) * K;
+          const int ee = s_idx[m][j];
+          const int rs = s_rbase[s_uof[ee]] + __popc(s_mask[ee] & ((1u << m) - 1u));
+          bool fj = true;
+          float w = 0.f;
+          for (int j2 = 0; j2 < K; ++j2)
+            if (s_idx[m][j2] == ee) {
+              fj = fj && j2 >= j;
+              w += s_cw[m][j2];
+            }
+          if (fj) s_rsw[rs] = w;
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&wbar);
     const float* pa = (const float*)(P.ws + P.L.m_pa);
     const unsigned int* ca = (const unsigned int*)(P.ws + P.L.m_ca);
     unsigned int* chc = (unsigned int*)(P.ws + P.L.m_ch);
@@ -1341,9 +1481,8 @@ int launch_moe(const MoeParams& P0, int grid, cudaStream_t st) {
       cudaFuncGetAttributes(&fa, (const void*)kfn) != cudaSuccess)
     return BQE_ECUDA;
   const int dyn_max = optin - (int)fa.sharedSizeBytes;
-  const uint32_t zb = (4u * g.M * g.E + 127u) & ~127u;
-  if (dyn_max <= (int)zb) return BQE_EUNSUPPORTED;
-  P.ring_bytes = ((uint32_t)dyn_max - zb) & ~127u;
+  if (dyn_max <= 0) return BQE_EUNSUPPORTED;
+  P.ring_bytes = (uint32_t)dyn_max & ~127u;
   const uint32_t xst = ((uint32_t)g.M * g.H * 2 + 127u) & ~127u;
   const uint32_t rtb = (uint32_t)((g.E + grid - 1) / grid) * g.H * 4;  // router rows of one CTA
   if (P.ring_bytes < moe_max_item(g, P.PB) || P.ring_bytes < xst + rtb + 1024) return BQE_EUNSUPPORTED;
@@ -1365,7 +1504,7 @@ int launch_moe(const MoeParams& P0, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kMoeThreads);
-  cfg.dynamicSmemBytes = zb + P.ring_bytes;
+  cfg.dynamicSmemBytes = P.ring_bytes;
   cfg.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: CTAs wait on one another

@@ -62,11 +62,12 @@ extern "C" int bqe_moe_layer_forward_noalloc(const bqe_layer_desc* d, int32_t M,
   rc = noalloc_scratch(st, &ws);
   if (rc) return rc;
   // the array keeps the previous call's contents: clear the error word and
-  // the work list (all in front of the logits), and the call epoch with the
-  // two arrival counters, so a call that failed leaves no trace in the next
+  // the work list (all in front of the logits), and the epoch-tagged keys
+  // with the call epoch and the counters, so a call that failed leaves no
+  // trace in the next
   const bqe::WsLayout L = bqe::make_ws(bqe::make_geo(d->hidden, d->inter, d->n_experts, d->top_k, M));
   if (cudaMemsetAsync(ws, 0, L.z, st) != cudaSuccess) return BQE_ECUDA;
-  if (cudaMemsetAsync((uint8_t*)ws + L.epoch, 0, L.m_pa - L.epoch, st) != cudaSuccess) return BQE_ECUDA;
+  if (cudaMemsetAsync((uint8_t*)ws + L.zk, 0, L.m_pa - L.zk, st) != cudaSuccess) return BQE_ECUDA;
   // diagnostic counters stay off: they would accumulate in the array, where
   // no caller can read them
   rc = bqe::moe_forward(d, M, x, router_w, sel_bias, pool, slot_table, forced_idx, out, accumulate, topk_idx, topk_w,
