@@ -69,7 +69,7 @@ PREFILL_METRIC = "MoE layer prefill: tokens/s and expert-GEMM TFLOP/s at T=8192 
 # reports null until a new capture is taken.
 KERNEL_SOURCES = ("bit_quantised_expert_gb300/csrc/bqe_moe.cu", "bit_quantised_expert_gb300/csrc/bqe_gemv.cuh",
                   "bit_quantised_expert_gb300/csrc/bqe_internal.cuh")
-TRAFFIC_FP4_M1 = dict(sha256="3e731c6d06c2ea428171128640118607807d091f963841dff8741b05eabb2f41", bytes=142919680)
+TRAFFIC_FP4_M1 = dict(sha256="87273b3b8c3946227ad8c3e1bd146c0ab053f080df5dc13fe33a20ff570b4d52", bytes=142556160)
 
 
 def kernel_digest() -> str:
