@@ -27,6 +27,11 @@ __host__ __device__ constexpr int fmt_bb(int f) {
          : f == BQE_FMT_NVFP4 ? 9 : 0;
 }
 __host__ __device__ constexpr bool fmt_ok(int f) { return f >= BQE_FMT_TQ1 && f <= BQE_FMT_NVFP4; }
+// log2 of the weights per block (every block width is a power of two)
+__host__ __device__ constexpr int fmt_lbw(int f) {
+  return f == BQE_FMT_TQ1 ? 8 : f == BQE_FMT_Q2_0 ? 6 : f == BQE_FMT_Q3_K ? 8 : f == BQE_FMT_MXFP4 ? 5
+         : f == BQE_FMT_NVFP4 ? 4 : 0;
+}
 
 // ----------------------------------------------------------------------------
 // Device layout of one matrix (rows x K) of a slot.

@@ -184,7 +184,8 @@ __device__ inline void make_tpl(const MoeParams& P, ItemTpl& T, int ph, int u, i
   const int kc = ph ? g.kcB : g.kcA;
   const int amode = act_mode(ph);
   ItemHdr& h = T.h;
-  h.tb = tile_bytes(fmt, kc);
+  const int lbw = fmt_lbw(fmt);  // blocks by shifts (no division by a format-dependent width)
+  h.tb = 32u * (uint32_t)(kc >> lbw) * (uint32_t)fmt_bb(fmt);
   h.arow = (uint32_t)act_row_bytes(amode, fmt, kc);
   h.astr = (uint32_t)act_row_stride(amode, fmt, kc);
   T.wbytes = (uint32_t)(ph ? P.PB : 2) * h.tb;
@@ -192,9 +193,9 @@ __device__ inline void make_tpl(const MoeParams& P, ItemTpl& T, int ph, int u, i
   h.red = h.act + al128((uint32_t)R * h.astr);
   h.off = 0;
   h.u = (int16_t)u; h.p = 0; h.c = 0; h.R = (int16_t)R;
-  h.phase = (uint8_t)ph; h.fmt = (uint8_t)fmt; h.amode = (uint8_t)amode; h.nb = (uint8_t)(kc / fmt_bw(fmt));
+  h.phase = (uint8_t)ph; h.fmt = (uint8_t)fmt; h.amode = (uint8_t)amode; h.nb = (uint8_t)(kc >> lbw);
   T.size = h.red + (uint32_t)(ph ? P.PB * g.GB : 2 * g.GA) * R * 32 * 4;
-  const uint64_t m13 = matrix_bytes(fmt, g.I, g.H);
+  const uint64_t m13 = (uint64_t)g.I * (uint64_t)(g.H >> lbw) * (uint64_t)fmt_bb(fmt);  // one of W1, W3
   T.m13 = (uint32_t)m13;
   T.wsrc = addr + (ph ? 2 * m13 : 0);
   if (ph == 0) {  // f16 x in the format's order
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
   const float* s_rw = reinterpret_cast<const float*>(ring + P.rt_off);  // this CTA's router rows (startup only)
 
   __shared__ ItemHdr hdr[kNQ];
-  __shared__ __align__(8) uint64_t full[kNQ], cons[kNQ], freed[kNQ], route_bar, rbar, wbar;
+  __shared__ __align__(8) uint64_t full[kNQ], cons[kNQ], freed[kNQ], route_bar, rbar, wbar, xbar;
   __shared__ float s_rsw[kMaxM * (kMaxTopK + 1)];  // mixing weight of each row slot (shared expert: 1)
   __shared__ int s_rbase[kMaxU + 1];   // first row slot of each work-list expert
   __shared__ int s_done[kNQ];
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     mbar_init(&route_bar, 1);
     mbar_init(&rbar, 1);
     mbar_init(&wbar, 1);
+    mbar_init(&xbar, 1);
     s_abort = 0;
     for (int q = 0; q < kNP; ++q) s_issued[q] = 0;
     s_turn = 0;
@@ -732,7 +734,6 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     // input (read by every CTA's bulk copies) and publish it on a second
     // counter; both groups then meet before the work list is built (which
     // takes the staging warps' per-format templates).
-    unsigned long long* scnt = (unsigned long long*)(P.ws + P.L.st);
     if (cw >= M) {
       const int sct = ct - 32 * M, NST = NCT - 32 * M;
       // per-row scale: s puts the row's largest |x| in [2^14, 2^15) for the f16
@@ -790,15 +791,12 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         const int ph = sct & 1, f = sct >> 1;
         if (fmt_ok(f)) make_tpl(P, s_tbase[ph][f], ph, 0, f, 0ull, 0, 0);
       }
-      // the slices are read by bulk copies (async proxy) of every CTA; their
-      // release also covers the output slice and counters zeroed above
+      // the slices are read by bulk copies (async proxy) of every CTA; the h
+      // warp releases them (and the output slice and counters zeroed above)
+      // on the counter, so that the fence waits in no compute warp
       fence_proxy_async_global();
       named_bar_sync(3, NST);
-      if (sct == 0) {
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        atomicAdd(scnt, 1ull);
-        if (P.diag) dacc(P, 1, globaltimer_ns() - t_cta0, 0);
-      }
+      if (sct == 0) mbar_arrive(&xbar);
     }
     // ---- the routing: per-row selection (warp m takes row m), then warp 0
     // builds the work list, the row slots and the item templates
@@ -1216,6 +1214,18 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     // ---- first, while the routing runs: the item template of every (phase,
     // format), for expert 0 at address 0 with no rows (the work list's
     // templates are these with a few fields changed)
+    // first: this CTA's staged slices of the input, once the staging warps
+    // have written them, released on the staged-input counter (one arrival
+    // per CTA per call; also releases the zeroed output slice and counters)
+    {
+      const bool okx = __all_sync(0xffffffffu, mwait(&xbar, 0, P.limit_ns, err));
+      if (lane == 0) {
+        if (!okx) set_error(err, BQE_ETIMEOUT, kErrWaitFull);
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        atomicAdd((unsigned long long*)(P.ws + P.L.st), 1ull);
+        if (P.diag) dacc(P, 1, globaltimer_ns() - t_cta0, 0);
+      }
+    }
     const bool ok0 = __all_sync(0xffffffffu, mwait(&route_bar, 0, P.limit_ns, err));
     const int nU = ok0 ? s_nu : 0;
     const int nrs = nU > 0 ? s_rbase[nU] : 0;
