@@ -30,7 +30,7 @@ class bqe_layer_desc(ctypes.Structure):
 
 class bqe_pool(ctypes.Structure):
     _fields_ = [("base", ctypes.c_void_p), ("base_bytes", ctypes.c_uint64), ("slot_off", ctypes.c_void_p),
-                ("slot_fmt", ctypes.c_void_p), ("n_slots", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("slot_fmt", ctypes.c_void_p), ("n_slots", ctypes.c_int32), ("fmt_mask", ctypes.c_int32)]
 
 
 class bqe_stats(ctypes.Structure):

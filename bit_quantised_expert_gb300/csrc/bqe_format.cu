@@ -226,7 +226,9 @@ extern "C" int bqe_pool_init(bqe_pool* p, const bqe_layer_desc* d, int32_t n_slo
   p->slot_off = (const uint64_t*)mem;
   p->slot_fmt = (const int32_t*)(mem + al256(8ull * n_slots));
   p->n_slots = n_slots;
-  p->reserved = 0;
+  int32_t mask = 0;
+  for (int32_t s = 0; s < n_slots; ++s) mask |= 1 << slot_fmt[s];
+  p->fmt_mask = mask;
   return BQE_OK;
 }
 

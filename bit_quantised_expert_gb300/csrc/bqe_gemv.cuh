@@ -129,6 +129,58 @@ __device__ __forceinline__ void mma_mxfp4(const uint8_t* tile, int nb, int grp, 
   }
 }
 
+// MXFP4 with one activation row (W1/W3 at M = 1): block bi of the group's 8
+// meets B column bi (x of the block's 32 columns in that column, zero in the
+// others), so each block's dot products collect in an accumulator column of
+// their own and the E8M0 scales multiply once per task instead of once per
+// block; the row sums are then the scaled columns added across the four
+// threads of a row.  Output as mma_group_nj's (row 0 of outv).
+__device__ __forceinline__ void mma_mxfp4_r1(const uint8_t* tile, int nb, int grp, const uint8_t* xrow, int lane,
+                                             float* outv) {
+  const int gq = lane >> 2, tq = lane & 3;
+  // x of block gq of the group, columns 8 tq .. 8 tq + 7 (natural order)
+  const uint4 xg = *reinterpret_cast<const uint4*>(xrow + ((grp * 8 + gq) * 32 + 8 * tq) * 2);
+  float d[2][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) d[mt][0] = d[mt][1] = d[mt][2] = d[mt][3] = 0.f;
+#pragma unroll 2
+  for (int bi = 0; bi < 8; ++bi) {
+    const int b = grp * 8 + bi;
+    const bool on = gq == bi;
+    const uint32_t x0 = on ? xg.x : 0u, x1 = on ? xg.y : 0u, x2 = on ? xg.z : 0u, x3 = on ? xg.w : 0u;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const int r0 = 16 * mt + gq;
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(tile + b * 512 + r0 * 16 + 4 * tq);
+      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(tile + b * 512 + (r0 + 8) * 16 + 4 * tq);
+      uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
+      e2m1x8_to_f16x2(w0, p0, p1, p2, p3);
+      e2m1x8_to_f16x2(w1, q0, q1, q2, q3);
+      mma_f16(d[mt], p0, q0, p1, q1, x0, x1);
+      mma_f16(d[mt], p2, q2, p3, q3, x2, x3);
+    }
+  }
+  // thread (gq, tq) holds columns (blocks) 2 tq, 2 tq + 1 of rows r0 and r0 + 8
+  const uint8_t* sc = tile + nb * 512;
+  const int c0 = (grp * 8 + 2 * tq) * 32;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    const int r0 = 16 * mt + gq;
+    float v0 = d[mt][0] * ue8m0_f32(sc[c0 + r0]);
+    v0 = fmaf(d[mt][1], ue8m0_f32(sc[c0 + 32 + r0]), v0);
+    float v1 = d[mt][2] * ue8m0_f32(sc[c0 + r0 + 8]);
+    v1 = fmaf(d[mt][3], ue8m0_f32(sc[c0 + 32 + r0 + 8]), v1);
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+    if (tq == 0) {
+      outv[r0] = v0;
+      outv[r0 + 8] = v1;
+    }
+  }
+}
+
 // Two E2M1 code bytes (the low 16 bits of w) -> two f16x2, and two E4M3
 // scale bytes (the low 16 bits of s) -> one f16x2, by the hardware conversions.
 __device__ __forceinline__ void e2m1x4_to_f16x2(uint32_t w, uint32_t& h0, uint32_t& h1) {
@@ -428,7 +480,7 @@ __device__ __forceinline__ void mma_tq1(const uint8_t* tile, int nb, int grp, co
 
 // B column pointers of the thread and the group loop of the format, then the
 // partial sums of each (row, weight row) into outv[r * 32 + weight row].
-template <int NJ>
+template <int NJ, int FS>
 __device__ __forceinline__ void mma_group_nj(int R, int fmt, const uint8_t* tile, int kc, int nb, int grp,
                                              const uint8_t* act, int rstr, int lane, float* outv, bool hl) {
   const int gq = lane >> 2, tq = lane & 3;
@@ -446,15 +498,25 @@ __device__ __forceinline__ void mma_group_nj(int R, int fmt, const uint8_t* tile
   for (int j = 0; j < NJ; ++j)
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) acc[j][mt][0] = acc[j][mt][1] = acc[j][mt][2] = acc[j][mt][3] = 0.f;
+  // (an instance carries only its formats' loops)
   switch (fmt) {
-    case BQE_FMT_MXFP4: mma_mxfp4<NJ>(tile, nb, grp, bv, lane, acc); break;
-    case BQE_FMT_Q2_0: mma_q2_0<NJ>(tile, nb, grp, bv, lane, acc); break;
-    case BQE_FMT_Q3_K: mma_q3k<NJ>(tile, nb, grp, bv, lane, acc); break;
-    case BQE_FMT_TQ1:
-      if (NJ == 1) mma_tq1<1>(tile, nb, grp, reinterpret_cast<const uint8_t* const(&)[1]>(bv), lane,
-                              reinterpret_cast<float(&)[1][2][4]>(acc));
+    case BQE_FMT_MXFP4:
+      if (fs_has<FS>(BQE_FMT_MXFP4)) mma_mxfp4<NJ>(tile, nb, grp, bv, lane, acc);
       break;
-    case BQE_FMT_NVFP4: mma_nvfp4<NJ>(tile, nb, grp, bv, lane, acc); break;
+    case BQE_FMT_Q2_0:
+      if (fs_has<FS>(BQE_FMT_Q2_0)) mma_q2_0<NJ>(tile, nb, grp, bv, lane, acc);
+      break;
+    case BQE_FMT_Q3_K:
+      if (fs_has<FS>(BQE_FMT_Q3_K)) mma_q3k<NJ>(tile, nb, grp, bv, lane, acc);
+      break;
+    case BQE_FMT_TQ1:
+      if (NJ == 1 && fs_has<FS>(BQE_FMT_TQ1))
+        mma_tq1<1>(tile, nb, grp, reinterpret_cast<const uint8_t* const(&)[1]>(bv), lane,
+                   reinterpret_cast<float(&)[1][2][4]>(acc));
+      break;
+    case BQE_FMT_NVFP4:
+      if (fs_has<FS>(BQE_FMT_NVFP4)) mma_nvfp4<NJ>(tile, nb, grp, bv, lane, acc);
+      break;
     default: break;
   }
   if (!hl) {
@@ -484,20 +546,22 @@ __device__ __forceinline__ void mma_group_nj(int R, int fmt, const uint8_t* tile
 }
 
 // The loop of one task: R <= 8 rows (RC == 1: one row).
-template <int RC>
+template <int RC, int FS>
 __device__ __forceinline__ void consume_mma(int R, int fmt, const uint8_t* tile, int kc, int nb, int grp,
                                             const uint8_t* act, int lane, float* outv, int amode) {
   const int rstr = act_row_stride(amode, fmt, kc);
   const bool hl = amode == kActH16;
-  if (RC == 1 || !hl || R <= 4) {
-    mma_group_nj<1>(RC == 1 ? 1 : R, fmt, tile, kc, nb, grp, act, rstr, lane, outv, hl);
-  } else if (fmt == BQE_FMT_TQ1) {
+  if (fs_has<FS>(BQE_FMT_MXFP4) && !hl && fmt == BQE_FMT_MXFP4 && (RC == 1 || R == 1)) {
+    mma_mxfp4_r1(tile, nb, grp, act, lane, outv);
+  } else if (RC == 1 || !hl || R <= 4) {
+    mma_group_nj<1, FS>(RC == 1 ? 1 : R, fmt, tile, kc, nb, grp, act, rstr, lane, outv, hl);
+  } else if (fs_has<FS>(BQE_FMT_TQ1) && fmt == BQE_FMT_TQ1) {
     // W2 rows 0..3, then 4..: ternary codes decoded twice (two MMAs per step
     // would not fit this kernel's register budget)
-    mma_group_nj<1>(4, fmt, tile, kc, nb, grp, act, rstr, lane, outv, true);
-    mma_group_nj<1>(R - 4, fmt, tile, kc, nb, grp, act + 4 * rstr, rstr, lane, outv + 4 * 32, true);
+    mma_group_nj<1, FS>(4, fmt, tile, kc, nb, grp, act, rstr, lane, outv, true);
+    mma_group_nj<1, FS>(R - 4, fmt, tile, kc, nb, grp, act + 4 * rstr, rstr, lane, outv + 4 * 32, true);
   } else {
-    mma_group_nj<2>(R, fmt, tile, kc, nb, grp, act, rstr, lane, outv, hl);
+    mma_group_nj<2, FS>(R, fmt, tile, kc, nb, grp, act, rstr, lane, outv, hl);
   }
 }
 

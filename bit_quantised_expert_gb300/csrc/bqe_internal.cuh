@@ -27,6 +27,17 @@ __host__ __device__ constexpr int fmt_bb(int f) {
          : f == BQE_FMT_NVFP4 ? 9 : 0;
 }
 __host__ __device__ constexpr bool fmt_ok(int f) { return f >= BQE_FMT_TQ1 && f <= BQE_FMT_NVFP4; }
+// Decode-kernel instances by the formats their loops carry: every format
+// (kFsAll), MXFP4 only (kFsFp4), or the low-bit formats TQ1 / Q2_0 / Q3_K
+// (kFsLowBit); a pool's format mask picks the instance, and an instance
+// rejects a slot of any other format like an invalid one.
+enum { kFsAll = 0, kFsFp4 = 1, kFsLowBit = 2 };
+template <int FS>
+__host__ __device__ constexpr bool fs_has(int f) {
+  return FS == kFsFp4 ? f == BQE_FMT_MXFP4
+         : FS == kFsLowBit ? (f == BQE_FMT_TQ1 || f == BQE_FMT_Q2_0 || f == BQE_FMT_Q3_K)
+         : fmt_ok(f);
+}
 // log2 of the weights per block (every block width is a power of two)
 __host__ __device__ constexpr int fmt_lbw(int f) {
   return f == BQE_FMT_TQ1 ? 8 : f == BQE_FMT_Q2_0 ? 6 : f == BQE_FMT_Q3_K ? 8 : f == BQE_FMT_MXFP4 ? 5

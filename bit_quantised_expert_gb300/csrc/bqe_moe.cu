@@ -224,7 +224,7 @@ __device__ inline void patch_tpl(const MoeParams& P, ItemTpl& T, const ItemTpl& 
   if (ph) T.act_base = B.act_base + (uint32_t)rb * B.act_rs;
 }
 
-template <int RC>
+template <int RC, int FS>
 __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
   const Geo& g = P.g;
   // the one-row instance (RC == 1) runs only calls with M == 1: a constant there
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         if (sl >= 0 && sl < P.pool.n_slots) {
           const int f = P.pool.slot_fmt[sl];
           const uint64_t off = P.pool.slot_off[sl];
-          if (fmt_ok(f) && !(off & 15) && off + 2 * matrix_bytes(f, I, H) + matrix_bytes(f, H, I) <= P.pool.base_bytes) {
+          if (fs_has<FS>(f) && !(off & 15) && off + 2 * matrix_bytes(f, I, H) + matrix_bytes(f, H, I) <= P.pool.base_bytes) {
             make_tpl(P, sh, 0, 0, f, (uint64_t)P.pool.base + off, M, 0);
             sh_ok = true;
           }
@@ -714,7 +714,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       uint64_t addr = 0;
       if (!valid) {
         bad = kErrSlotRange;
-      } else if (!fmt_ok(f)) {
+      } else if (!fs_has<FS>(f)) {  // (formats outside this instance's set included)
         bad = kErrSlotFmt;
       } else if ((off & 15) || off + 2 * matrix_bytes(f, I, H) + matrix_bytes(f, H, I) > P.pool.base_bytes) {
         bad = kErrSlotExtent;
@@ -789,7 +789,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       // with no rows (the work list's templates are these with a few fields changed)
       if (sct < 16) {
         const int ph = sct & 1, f = sct >> 1;
-        if (fmt_ok(f)) make_tpl(P, s_tbase[ph][f], ph, 0, f, 0ull, 0, 0);
+        if (fs_has<FS>(f)) make_tpl(P, s_tbase[ph][f], ph, 0, f, 0ull, 0, 0);
       }
       // the slices are read by bulk copies (async proxy) of every CTA; the h
       // warp releases them (and the output slice and counters zeroed above)
@@ -978,7 +978,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         // first row slot
         for (int t = lane; t < 2 * nu; t += 32) {
           const int ph = t & 1, u = t >> 1, f = s_ufmt[u];
-          if (fmt_ok(f)) patch_tpl(P, s_tpl[ph][u], s_tbase[ph][f], ph, u, s_uaddr[u], s_unrows[u], s_rbase[u]);
+          if (fs_has<FS>(f)) patch_tpl(P, s_tpl[ph][u], s_tbase[ph][f], ph, u, s_uaddr[u], s_unrows[u], s_rbase[u]);
         }
         __syncwarp();
         if (lane == 0) {
@@ -1047,7 +1047,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           grp = tau - tile_i * g.GB;
         }
         float* red = reinterpret_cast<float*>(const_cast<uint8_t*>(base) + h.red) + tau * h.R * 32;
-        consume_mma<RC>(h.R, h.fmt, base + tile_i * h.tb, isA ? g.kcA : g.kcB, h.nb, grp, base + h.act, lane, red,
+        consume_mma<RC, FS>(h.R, h.fmt, base + tile_i * h.tb, isA ? g.kcA : g.kcB, h.nb, grp, base + h.act, lane, red,
                         h.amode);
         __syncwarp();
         if (P.diag && cw == 0 && lane == 0) dacc(P, 3, globaltimer_ns() - tc);
@@ -1478,13 +1478,20 @@ int launch_moe(const MoeParams& P0, int grid, cudaStream_t st) {
       g.U > kMaxU || 2 * g.nchA > 24 || (uint64_t)g.M * (g.K + 1) * g.nchB * hrec_stride(g.kcB) >= (1ull << 32))
     return BQE_EUNSUPPORTED;
   P.PB = moe_pb(g);
-  static int limit_set[2][64] = {};
+  static int limit_set[2][3][64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return BQE_ECUDA;
   const int rc = g.M == 1 ? 0 : 1;
-  // one-row calls run an instance where M is the constant 1 (one B column
-  // group per MMA, no wide W2 items)
-  void (*kfn)(MoeParams) = rc ? k_moe<2> : k_moe<1>;
+  // the instance: one-row calls run one where M is the constant 1 (one B
+  // column group per MMA, no wide W2 items); a pool whose format mask names
+  // MXFP4 alone, or low-bit formats alone, runs one that carries only those
+  // formats' loops (a mask of 0: any format)
+  const uint32_t mask = (uint32_t)P.pool.fmt_mask;
+  const uint32_t low = (1u << BQE_FMT_TQ1) | (1u << BQE_FMT_Q2_0) | (1u << BQE_FMT_Q3_K);
+  const int fs = mask == (1u << BQE_FMT_MXFP4) ? kFsFp4 : (mask != 0 && (mask & ~low) == 0) ? kFsLowBit : kFsAll;
+  void (*const kfns[2][3])(MoeParams) = {{k_moe<1, kFsAll>, k_moe<1, kFsFp4>, k_moe<1, kFsLowBit>},
+                                         {k_moe<2, kFsAll>, k_moe<2, kFsFp4>, k_moe<2, kFsLowBit>}};
+  void (*kfn)(MoeParams) = kfns[rc][fs];
   int optin = 0;
   cudaFuncAttributes fa;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
@@ -1506,10 +1513,10 @@ int launch_moe(const MoeParams& P0, int grid, cudaStream_t st) {
   P.magA2 = mag(g.nchA);
   P.magB = mag(nBper);
   P.magB2 = mag(g.nchB);
-  if (limit_set[rc][dev] < dyn_max) {
+  if (limit_set[rc][fs][dev] < dyn_max) {
     if (cudaFuncSetAttribute((const void*)kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max) != cudaSuccess)
       return BQE_ECUDA;
-    limit_set[rc][dev] = dyn_max;
+    limit_set[rc][fs][dev] = dyn_max;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -72,14 +72,19 @@ typedef struct {
  * device layout (bqe_pool_pack_slot), plus two caller-owned device tables:
  * slot_off[s] = byte offset of slot s in base (multiple of 16), slot_fmt[s]
  * = its format.  The kernels check every slot id they use against n_slots
- * and every slot's extent against base_bytes. */
+ * and every slot's extent against base_bytes.  fmt_mask (host value): bit f
+ * set when slots of format f may be in the pool, 0 when unknown; the decode
+ * call runs a kernel carrying only the inner loops of those formats (MXFP4
+ * alone, or TQ1 / Q2_0 / Q3_K alone; any other mask: all formats), and a slot
+ * of a format outside them is reported like an invalid slot (BQE_EDEVICE).
+ * bqe_pool_init fills it from the slot formats. */
 typedef struct {
   const void* base;          /* device */
   uint64_t base_bytes;
   const uint64_t* slot_off;  /* device, n_slots entries */
   const int32_t* slot_fmt;   /* device, n_slots entries */
   int32_t n_slots;
-  int32_t reserved;
+  int32_t fmt_mask;
 } bqe_pool;
 
 /* Accounting of one decode call (bqe_layer_stats): what it streamed.  The
@@ -153,8 +158,9 @@ uint64_t bqe_pool_bytes(const bqe_layer_desc* d, int32_t n_slots, const int32_t*
  * aligned, dev_bytes >= bqe_pool_bytes): writes the two tables at its front
  * (copies enqueued on `stream`; slot_fmt is host memory and may be released
  * when the call returns) and fills *p (host struct) so that it describes the
- * pool: base = the first slot, slot_off / slot_fmt = the device tables.  The
- * library keeps no reference to dev_mem.  BQE_ENOSPC if dev_bytes is short,
+ * pool: base = the first slot, slot_off / slot_fmt = the device tables,
+ * fmt_mask = the formats of the slots.  The library keeps no reference to
+ * dev_mem.  BQE_ENOSPC if dev_bytes is short,
  * BQE_EINVAL on a bad argument. */
 int bqe_pool_init(bqe_pool* p, const bqe_layer_desc* d, int32_t n_slots, const int32_t* slot_fmt,
                   void* dev_mem, uint64_t dev_bytes, void* stream);

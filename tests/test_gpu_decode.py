@@ -246,6 +246,33 @@ def test_bad_slot_is_reported(dev):
     assert np.isfinite(o2).all()
 
 
+def test_pool_format_mask_selects_and_guards(dev):
+    """bqe_pool_init records the slots' formats; a mask that leaves out a
+    format in use is reported like an invalid slot (BQE_EDEVICE, slot-format
+    detail), not computed with the wrong loops; mask 0 runs every format."""
+    import torch
+    from bit_quantised_expert_gb300 import _abi as A
+    L = synth.tiny_layer(seed=2, m=1)
+    DL = DeviceLayer(L, dev)
+    assert DL.pool.cstruct().fmt_mask == 1 << synth.Q2_0
+    ref, _, _ = DL.forward(L["x"])
+    ws, nb = DL.workspace(1)
+    x = torch.from_numpy(L["x"].view(np.int16)).to(dev)
+    for mask, ok in ((1 << synth.MXFP4, False), (0, True), ((1 << synth.Q2_0) | (1 << synth.TQ1), True)):
+        p = A.bqe_pool.from_buffer_copy(DL.pool.cstruct())
+        p.fmt_mask = mask
+        A.bqe_workspace_init(ws, nb)
+        out = torch.zeros(1, 512, device=dev)
+        A.bqe_moe_layer_forward(DL.d, 1, x, DL.wr, DL.bias, p, DL.table, None, out, 0, None, None, ws, nb)
+        rc, det = A.bqe_check(ws)
+        if ok:
+            assert rc == A.BQE_OK, (mask, A.status_name(rc), det)
+            check_out(out.double().cpu().numpy(), ref, rel=1e-5, mabs=1e-5, what="mask %#x" % mask)
+        else:
+            assert rc == A.BQE_EDEVICE and det == 2, (mask, A.status_name(rc), det)
+    A.bqe_workspace_init(ws, nb)
+
+
 def test_host_argument_errors(dev):
     import torch
     from bit_quantised_expert_gb300 import _abi as A
