@@ -181,6 +181,65 @@ __device__ __forceinline__ void mma_mxfp4_r1(const uint8_t* tile, int nb, int gr
   }
 }
 
+// MXFP4 W2 with one activation row: the h record's hi and lo halves of
+// block bq (of four) meet B columns 2 bq and 2 bq + 1; two passes cover the
+// group's eight blocks, each in accumulators of its own, and the E8M0 scales
+// multiply once per task.  rec: the row's h record (hi | 64 B | lo | 2^-s of
+// each 256 columns), flen its halves per part.
+__device__ __forceinline__ void mma_mxfp4_r1_hl(const uint8_t* tile, int nb, int grp, const uint8_t* rec, int flen,
+                                                int lane, float* outv) {
+  const int gq = lane >> 2, tq = lane & 3;
+  const uint8_t* src = rec + ((gq & 1) ? 2 * flen + 64 : 0);  // B column gq: hi (even) or lo (odd)
+  const uint4 xa = *reinterpret_cast<const uint4*>(src + ((grp * 8 + (gq >> 1)) * 32 + 8 * tq) * 2);
+  const uint4 xb = *reinterpret_cast<const uint4*>(src + ((grp * 8 + 4 + (gq >> 1)) * 32 + 8 * tq) * 2);
+  float d[2][2][4];
+#pragma unroll
+  for (int ps = 0; ps < 2; ++ps)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) d[ps][mt][0] = d[ps][mt][1] = d[ps][mt][2] = d[ps][mt][3] = 0.f;
+#pragma unroll
+  for (int ps = 0; ps < 2; ++ps) {
+    const uint4 xg = ps ? xb : xa;
+#pragma unroll 2
+    for (int bq = 0; bq < 4; ++bq) {
+      const int b = grp * 8 + 4 * ps + bq;
+      const bool on = (gq >> 1) == bq;
+      const uint32_t x0 = on ? xg.x : 0u, x1 = on ? xg.y : 0u, x2 = on ? xg.z : 0u, x3 = on ? xg.w : 0u;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int r0 = 16 * mt + gq;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(tile + b * 512 + r0 * 16 + 4 * tq);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(tile + b * 512 + (r0 + 8) * 16 + 4 * tq);
+        uint32_t p0, p1, p2, p3, q0, q1, q2, q3;
+        e2m1x8_to_f16x2(w0, p0, p1, p2, p3);
+        e2m1x8_to_f16x2(w1, q0, q1, q2, q3);
+        mma_f16(d[ps][mt], p0, q0, p1, q1, x0, x1);
+        mma_f16(d[ps][mt], p2, q2, p3, q3, x2, x3);
+      }
+    }
+  }
+  // thread (gq, tq) holds hi and lo of block tq of each pass, rows r0, r0 + 8
+  const uint8_t* sc = tile + nb * 512;
+  const int ca = (grp * 8 + tq) * 32, cb = ca + 4 * 32;
+  const float us = reinterpret_cast<const float*>(rec + 4 * flen + 64)[grp];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    const int r0 = 16 * mt + gq;
+    float v0 = (d[0][mt][0] + d[0][mt][1]) * ue8m0_f32(sc[ca + r0]);
+    v0 = fmaf(d[1][mt][0] + d[1][mt][1], ue8m0_f32(sc[cb + r0]), v0);
+    float v1 = (d[0][mt][2] + d[0][mt][3]) * ue8m0_f32(sc[ca + r0 + 8]);
+    v1 = fmaf(d[1][mt][2] + d[1][mt][3], ue8m0_f32(sc[cb + r0 + 8]), v1);
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+    if (tq == 0) {
+      outv[r0] = v0 * us;
+      outv[r0 + 8] = v1 * us;
+    }
+  }
+}
+
 // Two E2M1 code bytes (the low 16 bits of w) -> two f16x2, and two E4M3
 // scale bytes (the low 16 bits of s) -> one f16x2, by the hardware conversions.
 __device__ __forceinline__ void e2m1x4_to_f16x2(uint32_t w, uint32_t& h0, uint32_t& h1) {
@@ -551,8 +610,11 @@ __device__ __forceinline__ void consume_mma(int R, int fmt, const uint8_t* tile,
                                             const uint8_t* act, int lane, float* outv, int amode) {
   const int rstr = act_row_stride(amode, fmt, kc);
   const bool hl = amode == kActH16;
-  if (fs_has<FS>(BQE_FMT_MXFP4) && !hl && fmt == BQE_FMT_MXFP4 && (RC == 1 || R == 1)) {
-    mma_mxfp4_r1(tile, nb, grp, act, lane, outv);
+  if (fs_has<FS>(BQE_FMT_MXFP4) && fmt == BQE_FMT_MXFP4 && (RC == 1 || R == 1)) {
+    if (!hl)
+      mma_mxfp4_r1(tile, nb, grp, act, lane, outv);
+    else
+      mma_mxfp4_r1_hl(tile, nb, grp, act, f16_len(fmt, kc), lane, outv);
   } else if (RC == 1 || !hl || R <= 4) {
     mma_group_nj<1, FS>(RC == 1 ? 1 : R, fmt, tile, kc, nb, grp, act, rstr, lane, outv, hl);
   } else if (fs_has<FS>(BQE_FMT_TQ1) && fmt == BQE_FMT_TQ1) {
