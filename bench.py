@@ -69,7 +69,7 @@ PREFILL_METRIC = "MoE layer prefill: tokens/s and expert-GEMM TFLOP/s at T=8192 
 # reports null until a new capture is taken.
 KERNEL_SOURCES = ("bit_quantised_expert_gb300/csrc/bqe_moe.cu", "bit_quantised_expert_gb300/csrc/bqe_gemv.cuh",
                   "bit_quantised_expert_gb300/csrc/bqe_internal.cuh")
-TRAFFIC_FP4_M1 = dict(sha256="87273b3b8c3946227ad8c3e1bd146c0ab053f080df5dc13fe33a20ff570b4d52", bytes=142556160)
+TRAFFIC_FP4_M1 = dict(sha256="e00088cb1c95abf41bb17b3870420ce0200c09da2511792bd877f310b5596af6", bytes=142621440)
 
 
 def kernel_digest() -> str:
