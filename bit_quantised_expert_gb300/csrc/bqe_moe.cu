@@ -38,6 +38,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "bqe_gemv.cuh"
 #include "bqe_internal.cuh"
 
@@ -1492,12 +1494,19 @@ int launch_moe(const MoeParams& P0, int grid, cudaStream_t st) {
   void (*const kfns[2][3])(MoeParams) = {{k_moe<1, kFsAll>, k_moe<1, kFsFp4>, k_moe<1, kFsLowBit>},
                                          {k_moe<2, kFsAll>, k_moe<2, kFsFp4>, k_moe<2, kFsLowBit>}};
   void (*kfn)(MoeParams) = kfns[rc][fs];
-  int optin = 0;
-  cudaFuncAttributes fa;
-  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-      cudaFuncGetAttributes(&fa, (const void*)kfn) != cudaSuccess)
-    return BQE_ECUDA;
-  const int dyn_max = optin - (int)fa.sharedSizeBytes;
+  // the dynamic shared memory an instance may take on this device (queried
+  // once per instance and device: the queries cost host time on every call)
+  static std::atomic<int> dyn_cache[2][3][64];
+  int dyn_max = dyn_cache[rc][fs][dev].load(std::memory_order_relaxed);
+  if (dyn_max == 0) {
+    int optin = 0;
+    cudaFuncAttributes fa;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, (const void*)kfn) != cudaSuccess)
+      return BQE_ECUDA;
+    dyn_max = optin - (int)fa.sharedSizeBytes;
+    if (dyn_max > 0) dyn_cache[rc][fs][dev].store(dyn_max, std::memory_order_relaxed);
+  }
   if (dyn_max <= 0) return BQE_EUNSUPPORTED;
   P.ring_bytes = (uint32_t)dyn_max & ~127u;
   const uint32_t xst = ((uint32_t)g.M * g.H * 2 + 127u) & ~127u;
