@@ -69,7 +69,7 @@ PREFILL_METRIC = "MoE layer prefill: tokens/s and expert-GEMM TFLOP/s at T=8192 
 # reports null until a new capture is taken.
 KERNEL_SOURCES = ("bit_quantised_expert_gb300/csrc/bqe_moe.cu", "bit_quantised_expert_gb300/csrc/bqe_gemv.cuh",
                   "bit_quantised_expert_gb300/csrc/bqe_internal.cuh")
-TRAFFIC_FP4_M1 = dict(sha256="e00088cb1c95abf41bb17b3870420ce0200c09da2511792bd877f310b5596af6", bytes=142621440)
+TRAFFIC_FP4_M1 = dict(sha256="4994e12ab3098f89d0dd547410c7796b459e8405e9966a7f24b69a7a2e7b2399", bytes=142588160)
 
 
 def kernel_digest() -> str:
