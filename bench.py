@@ -69,7 +69,7 @@ PREFILL_METRIC = "MoE layer prefill: tokens/s and expert-GEMM TFLOP/s at T=8192 
 # reports null until a new capture is taken.
 KERNEL_SOURCES = ("bit_quantised_expert_gb300/csrc/bqe_moe.cu", "bit_quantised_expert_gb300/csrc/bqe_gemv.cuh",
                   "bit_quantised_expert_gb300/csrc/bqe_internal.cuh")
-TRAFFIC_FP4_M1 = dict(sha256="4994e12ab3098f89d0dd547410c7796b459e8405e9966a7f24b69a7a2e7b2399", bytes=142588160)
+TRAFFIC_FP4_M1 = dict(sha256="dca4056367c3bb987359da34045496dd0f6aab3fc11939e696ed479ce0a1ea6a", bytes=142588160)
 
 
 def kernel_digest() -> str:

@@ -1434,8 +1434,9 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     release_h();
   }
 
-  // ---- end: CTA 0 is past the logits sync, so every CTA has read this
-  // call's tag: CTA 0 advances the epoch for the next call
+  // ---- end: CTA 0's producers saw every CTA's staged-input arrival (made
+  // after that CTA read the tag), so every CTA has read this call's tag: CTA 0
+  // advances the epoch for the next call
   __syncthreads();
   if (tid == 0) {
     mstamp(P, kStEnd, true);
