@@ -803,6 +803,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     // ---- the routing: per-row selection (warp m takes row m), then warp 0
     // builds the work list, the row slots and the item templates
     const bool forced = P.forced != nullptr;
+    int mine = 0;  // row cw's choice (lane) of the selecting warp, also read by warp 0's one-row work list
     if (cw < M) {
       // Expert e's rank value is (key << 32) | ~e: keys descending, ties to
       // the lower id, every value distinct.  Round j takes the largest value
@@ -859,7 +860,6 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         // lane j keeps round j's winner; the bookkeeping (choice, the
         // expert's row mask and first choice) is done after the rounds, by
         // lanes 0 .. K-1 at once, so no round waits on shared memory
-        int mine = 0;
         if (forced) {
           if (lane < K) mine = s_fidx[m][lane];
         } else {
@@ -900,9 +900,40 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           rstamp(P, 3, t_cta0);
         }
         // work list: the chosen experts in the order of their first choice
-        // (row-major over (row, choice)), u = 1..; the shared expert u = 0
+        // (row-major over (row, choice)), u = 1..; the shared expert u = 0.
+        // One row, selected (not forced): its K choices are distinct, so
+        // choice j is entry j + 1 with row slot j + 1; lane j holds it from
+        // the selection, lane K takes the shared expert, and the general
+        // pass below (and the row-slot scan) is skipped.
+        const bool one_row = RC == 1 && !forced;
+        if (one_row) {
+          const int u = lane < K ? lane + 1 : 0;
+          const int e = lane < K ? mine : E;
+          const bool act = lane <= K;
+          const int my_bad = act ? s_ebad[e] : 0, my_fmt = act ? s_efmt[e] : 0;
+          const uint64_t my_addr = act ? s_eaddr[e] : 0ull;
+          const uint32_t rbad = __ballot_sync(0xffffffffu, lane < K && my_bad != 0);
+          const bool sbad = __shfl_sync(0xffffffffu, my_bad, K) != 0;
+          if (act) {
+            if (my_bad) set_error(err, BQE_EDEVICE, my_bad);
+            if (lane < K) s_uof[e] = (int16_t)u;
+            s_ufmt[u] = my_fmt;
+            s_uaddr[u] = my_addr;
+            s_urows[u * kMaxM] = 0;
+            s_unrows[u] = 1;
+            s_rbase[u] = u;
+            if (lane == K) s_rbase[K + 1] = K + 1;
+            if (cta == 0) {  // the call's work list, for bqe_layer_stats
+              ((int32_t*)(P.ws + P.L.u_slot))[u] = s_eslot[e];
+              ((int32_t*)(P.ws + P.L.u_fmt))[u] = my_fmt;
+              ((int32_t*)(P.ws + P.L.u_nrows))[u] = 1;
+            }
+          }
+          if (lane == 0 && (sbad || rbad)) s_bad = sbad ? 2 : 1;
+          __syncwarp();
+        }
         int base = 1;
-        for (int t0 = 0; t0 < M * K; t0 += 32) {
+        for (int t0 = 0; t0 < (one_row ? 0 : M * K); t0 += 32) {
           const int t = t0 + lane;
           const int e = t < M * K ? s_idx[t / K][t - (t / K) * K] : 0;
           const bool fst = t < M * K && s_first[e] == t;
@@ -930,8 +961,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           }
           base += __popc(bal);
         }
-        const int tot = base - 1;
-        if (lane == 0) {
+        const int tot = one_row ? K : base - 1;
+        if (lane == 0 && !one_row) {
           // the shared expert (validated like the others)
           const int sh_bad = s_ebad[E], sh_fmt = s_efmt[E];
           if (sh_bad) {
@@ -947,23 +978,24 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
             ((int32_t*)(P.ws + P.L.u_nrows))[0] = M;
           }
         }
-        if (lane < M) s_urows[lane] = (int8_t)lane;
+        if (lane < M && !one_row) s_urows[lane] = (int8_t)lane;
         __syncwarp();
         if (lane == 0) rstamp(P, 4, t_cta0);
-        // row slots: the shared expert's M rows first, then each chosen
-        // expert's rows in work-list order (exclusive prefix, two entries a lane)
-        const int u0 = 2 * lane, u1 = 2 * lane + 1;
-        const int n0 = u0 <= tot ? s_unrows[u0] : 0, n1 = u1 <= tot ? s_unrows[u1] : 0;
-        int incl = n0 + n1;
+        if (!one_row) {
+          // row slots: the shared expert's M rows first, then each chosen
+          // expert's rows in work-list order (exclusive prefix, two entries a lane)
+          const int u0 = 2 * lane, u1 = 2 * lane + 1;
+          const int n0 = u0 <= tot ? s_unrows[u0] : 0, n1 = u1 <= tot ? s_unrows[u1] : 0;
+          int incl = n0 + n1;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int tv = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += tv;
+          for (int o = 1; o < 32; o <<= 1) {
+            const int tv = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += tv;
+          }
+          const int ex = incl - n0 - n1;
+          if (u0 <= tot + 1) s_rbase[u0] = ex;
+          if (u1 <= tot + 1) s_rbase[u1] = ex + n0;
         }
-        const int ex = incl - n0 - n1;
-        if (u0 <= tot + 1) s_rbase[u0] = ex;
-        if (u1 <= tot + 1) s_rbase[u1] = ex + n0;
-        // the per-format templates (h warp), needed below
         __syncwarp();
         // on an invalid routed slot only the shared expert runs (the call
         // reports the error; its output is undefined); an invalid shared slot
