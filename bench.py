@@ -69,7 +69,7 @@ PREFILL_METRIC = "MoE layer prefill: tokens/s and expert-GEMM TFLOP/s at T=8192 
 # reports null until a new capture is taken.
 KERNEL_SOURCES = ("bit_quantised_expert_gb300/csrc/bqe_moe.cu", "bit_quantised_expert_gb300/csrc/bqe_gemv.cuh",
                   "bit_quantised_expert_gb300/csrc/bqe_internal.cuh")
-TRAFFIC_FP4_M1 = dict(sha256="dca4056367c3bb987359da34045496dd0f6aab3fc11939e696ed479ce0a1ea6a", bytes=142588160)
+TRAFFIC_FP4_M1 = dict(sha256="b294bc49b9b1d01bc1af0d0ab76e1a7cc808fde53225a8e786ca30f2cd210e0d", bytes=142757632)
 
 
 def kernel_digest() -> str:
