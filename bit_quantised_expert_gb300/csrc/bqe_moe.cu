@@ -151,6 +151,11 @@ __device__ __forceinline__ void rstamp(const MoeParams& P, int k, uint64_t t0) {
               (unsigned long long)(globaltimer_ns() - t0));
 }
 
+// The CTA's abort flag as lane 0 of the calling warp reads it, the same for
+// every lane (a flag set by another warp meanwhile must not split a warp
+// before its next warp-wide operation); every lane of the warp calls it.
+__device__ __forceinline__ bool warp_abort(volatile int& flag) { return __shfl_sync(0xffffffffu, (int)flag, 0) != 0; }
+
 // Bounded wait on an mbarrier phase, sleeping between checks; also gives up
 // when another CTA has already recorded an error.
 __device__ __forceinline__ bool mwait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, const int32_t* err) {
@@ -833,8 +838,8 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           for (int q = 0; q < QN; ++q)
             if ((need & (1u << q)) && (uint32_t)vv[q] == tag) need &= ~(1u << q);
           if (!__any_sync(0xffffffffu, need != 0u)) break;
-          if (s_abort || globaltimer_ns() - t0 > P.limit_ns ||
-              ((spin & 15) == 15 && *(volatile const int32_t*)err)) {
+          if (__any_sync(0xffffffffu, s_abort || globaltimer_ns() - t0 > P.limit_ns ||
+                                          ((spin & 15) == 15 && *(volatile const int32_t*)err))) {
             okz = false;
             break;
           }
@@ -851,7 +856,10 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         rstamp(P, 0, t_cta0);
         rstamp(P, 1, t_cta0);
       }
-      if (!s_abort) {
+      __syncwarp();
+      // (one read of the abort flag for the whole warp: the rounds below use
+      // warp-wide reductions)
+      if (!warp_abort(s_abort)) {
 #pragma unroll
         for (int q = 0; q < QN; ++q) {
           const int e = lane + 32 * q;
@@ -1000,7 +1008,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
         // on an invalid routed slot only the shared expert runs (the call
         // reports the error; its output is undefined); an invalid shared slot
         // or an aborted routing streams nothing
-        const int nu = (s_abort || s_bad == 2) ? 0 : s_bad ? 1 : 1 + tot;
+        const int nu = (warp_abort(s_abort) || s_bad == 2) ? 0 : s_bad ? 1 : 1 + tot;
         if (lane == 0) {
           s_nu = nu;
           if (cta == 0) *(int32_t*)(P.ws + P.L.nu) = nu;
@@ -1029,7 +1037,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     const int nTot = nU * (nAper + nBper), nA = nU * nAper;
     const int nmine = cta < nTot ? (nTot - cta + G - 1) / G : 0;
     int k = cw, Ki = 0;
-    bool first = true, okc = !s_abort;
+    bool first = true, okc = !warp_abort(s_abort);
     auto run_items = [&](int i0, int i1) {
       for (int i = i0; i < i1 && okc; ++i) {
         const bool isA = cta + i * G < nA;
@@ -1054,7 +1062,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
           }
         }
         ok = __all_sync(0xffffffffu, ok && mwait(&full[i % kNQ], (i / kNQ) & 1, P.limit_ns, err));
-        if (!ok || s_abort) {
+        if (!ok || warp_abort(s_abort)) {
           if (lane == 0) {
             if (!ok) set_error(err, BQE_ETIMEOUT, kErrWaitFull);
             s_abort = 1;
@@ -1143,7 +1151,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     for (int i = 0; i < nmine; ++i) {
       const uint64_t tr = P.diag ? globaltimer_ns() : 0;
       if (!have) {  // the header of item i is readable once its copies have landed
-        if (!__all_sync(0xffffffffu, mwait(&full[i % kNQ], (i / kNQ) & 1, P.limit_ns, err)) || s_abort) {
+        if (!__all_sync(0xffffffffu, mwait(&full[i % kNQ], (i / kNQ) & 1, P.limit_ns, err)) || warp_abort(s_abort)) {
           if (lane == 0) {
             set_error(err, BQE_ETIMEOUT, kErrWaitFull);
             s_abort = 1;
@@ -1155,7 +1163,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       const ItemHdr h = hn;
       const int u = h.u, R = RC == 1 ? 1 : h.R;
       if (h.phase == 1 && !wready) {  // the mixing weights (h warp) before the first W2 item
-        if (!__all_sync(0xffffffffu, mwait(&wbar, 0, P.limit_ns, err)) || s_abort) {
+        if (!__all_sync(0xffffffffu, mwait(&wbar, 0, P.limit_ns, err)) || warp_abort(s_abort)) {
           if (lane == 0) {
             set_error(err, BQE_ETIMEOUT, kErrWaitFull);
             s_abort = 1;
@@ -1179,7 +1187,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
       }
       const bool okc = __all_sync(0xffffffffu, mwait(&cons[i % kNQ], (i / kNQ) & 1, P.limit_ns, err));
       if (P.diag && lane == 0) dacc(P, 4, globaltimer_ns() - tr);
-      if (!okc || s_abort) {
+      if (!okc || warp_abort(s_abort)) {
         if (lane == 0) {
           set_error(err, BQE_ETIMEOUT, kErrWaitFull);
           s_abort = 1;
@@ -1269,7 +1277,7 @@ __global__ void __launch_bounds__(kMoeThreads, 1) k_moe(MoeParams P) {
     // choices as exp(log s_j - max log s) / sum exp(...), finite even when
     // every selected sigmoid underflows in fp32; then each row slot's weight
     // (the sum over the row's choices of that expert; shared expert rows: 1)
-    if (ok0 && !s_abort) {
+    if (ok0 && !warp_abort(s_abort)) {  // (warp-uniform: shuffles below)
       // the selected logits, read until each carries this call's tag
       // (bounded; their keys were seen, so they are normally there)
       const unsigned long long* zl = (const unsigned long long*)(P.ws + P.L.zl);
