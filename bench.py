@@ -69,7 +69,7 @@ PREFILL_METRIC = "MoE layer prefill: tokens/s and expert-GEMM TFLOP/s at T=8192 
 # reports null until a new capture is taken.
 KERNEL_SOURCES = ("bit_quantised_expert_gb300/csrc/bqe_moe.cu", "bit_quantised_expert_gb300/csrc/bqe_gemv.cuh",
                   "bit_quantised_expert_gb300/csrc/bqe_internal.cuh")
-TRAFFIC_FP4_M1 = dict(sha256="b294bc49b9b1d01bc1af0d0ab76e1a7cc808fde53225a8e786ca30f2cd210e0d", bytes=142757632)
+TRAFFIC_FP4_M1 = dict(sha256="3d7a8eeea843a82e15916b7f3ec2dd861c4a2d10e8bda497b0e79dfb949ff2bc", bytes=142606592)
 
 
 def kernel_digest() -> str:
